@@ -1,0 +1,170 @@
+"""Pins of the oracle's layer steps (CPU only).
+
+Router logits against numpy's fp64 matmul; top-k against a stable numpy sort;
+gates against scipy's softmax over the selected logits; dispatch against
+bincount / stable argsort; the expert FFN against a numpy dense SwiGLU on the
+oracle's own dequantised weights; combine against zero-gate, linearity and
+token-permutation invariants; the whole layer against the textbook dense
+SwiGLU when E = 1, k = 1.
+"""
+import numpy as np
+import pytest
+from scipy.special import softmax
+
+import gen
+import oracle
+
+
+def _bf16_bits(a):
+    a = np.ascontiguousarray(a, np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def _bf16_vals(bits):
+    return gen.bf16_to_f32(bits).astype(np.float64)
+
+
+def _tiny_layer(fmt=oracle.FMT_NVFP4, H=64, I=32, E=6, k=2, shared=1, bias=True, seed=0):
+    if fmt == oracle.FMT_FP6:
+        H, I = max(H, 128), max(I, 128)
+    rng = np.random.default_rng(seed)
+    router = _bf16_bits(rng.standard_normal((E, H)) * 0.2)
+    b = (rng.standard_normal(E) * 0.1).astype(np.float32) if bias else None
+    L = oracle.Layer(fmt, H, I, E, k, shared, router, b)
+    for e in range(E + shared):
+        for m in range(3):
+            rows, K = L.shape(m)
+            L.quantize_matrix(e, m, (rng.standard_normal((rows, K)) * 0.05).astype(np.float32))
+    x = _bf16_bits(rng.standard_normal((5, H)))
+    return L, x
+
+
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+def _dense_swiglu(L, e, x_vals):
+    Wg, Wu, Wd = (L.dequant(e, m).astype(np.float64) for m in range(3))
+    a = _silu(x_vals @ Wg.T) * (x_vals @ Wu.T)
+    return a @ Wd.T
+
+
+def test_router_logits_match_numpy():
+    L, x = _tiny_layer()
+    got = L.logits(x)
+    ref = (_bf16_vals(x) @ _bf16_vals(L.router).T).astype(np.float32) + L.bias
+    assert np.array_equal(got, ref.astype(np.float32))
+
+
+def test_topk_matches_stable_sort_and_softmax():
+    rng = np.random.default_rng(7)
+    T, E, k = 40, 16, 4
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[3, 5] = lg[3, 9] = lg[3].max() + 1  # an exact tie: the lower index goes first
+    L = oracle.Layer(1, 16, 16, E, k, 0, np.zeros((E, 16), np.uint16))
+    idx, gates = L.topk(lg)
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -lg[t].astype(np.float64)))[:k]
+        assert list(idx[t]) == list(order)
+        ref = softmax(lg[t, order].astype(np.float64))
+        assert np.allclose(gates[t], ref, rtol=0, atol=2e-7)
+        assert abs(float(gates[t].astype(np.float64).sum()) - 1.0) <= k * 2.0 ** -23
+    assert list(idx[3][:2]) == [5, 9]
+
+
+def test_topk_single_expert_gate_is_one():
+    L = oracle.Layer(1, 16, 16, 1, 1, 0, np.zeros((1, 16), np.uint16))
+    idx, gates = L.topk(np.array([[0.3], [-7.0]], np.float32))
+    assert np.all(idx == 0) and np.all(gates == 1.0)
+
+
+def test_dispatch_matches_numpy():
+    rng = np.random.default_rng(8)
+    T, k, E = 33, 3, 10
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, perm = oracle.dispatch(idx, E)
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    assert offsets[0] == 0 and np.array_equal(offsets[1:], np.cumsum(counts))
+    assert offsets[-1] == T * k
+    assert np.array_equal(perm, np.argsort(idx.ravel(), kind="stable"))
+    assert np.array_equal(np.sort(perm), np.arange(T * k))
+
+
+@pytest.mark.parametrize("fmt", [oracle.FMT_NVFP4, oracle.FMT_FP6])
+def test_expert_ffn_matches_dense_swiglu(fmt):
+    L, x = _tiny_layer(fmt=fmt)
+    for e in (0, L.E):  # a routed expert and the shared one
+        got = L.expert_ffn(e, x)
+        ref = _dense_swiglu(L, e, _bf16_vals(x))
+        assert np.allclose(got, ref, rtol=1e-6, atol=1e-9), np.abs(got - ref).max()
+
+
+def test_combine_zero_gates_is_zero_without_shared():
+    L, x = _tiny_layer(shared=0)
+    idx = np.tile(np.array([[0, 3]], np.int32), (x.shape[0], 1))
+    out = L.combine(x, idx, np.zeros(idx.shape, np.float32))
+    assert np.all(out == 0.0)
+
+
+def test_combine_is_linear_in_gates_and_sums_the_shared_expert():
+    L, x = _tiny_layer(shared=1)
+    T = x.shape[0]
+    idx = np.tile(np.array([[1, 4]], np.int32), (T, 1))
+    xv = _bf16_vals(x)
+    y1, y4, ys = (_dense_swiglu(L, e, xv) for e in (1, 4, L.E))
+    g = np.array([[0.75, 0.25]] * T, np.float32)
+    out = L.combine(x, idx, g)
+    ref = 0.75 * y1 + 0.25 * y4 + ys
+    assert np.allclose(out, ref, rtol=1e-6, atol=1e-9)
+    g2 = np.array([[0.5, 2.0]] * T, np.float32)
+    out2 = L.combine(x, idx, g2)
+    both = L.combine(x, idx, g + g2)
+    assert np.allclose(both, out + out2 - ys, rtol=1e-6, atol=1e-7)
+
+
+def test_forward_token_permutation_equivariance():
+    L, x = _tiny_layer()
+    lg, idx, gates, out = L.forward(x)
+    p = np.array([3, 0, 4, 1, 2])
+    lg2, idx2, gates2, out2 = L.forward(x[p])
+    assert np.array_equal(lg2, lg[p]) and np.array_equal(idx2, idx[p])
+    assert np.array_equal(gates2, gates[p]) and np.array_equal(out2, out[p])
+
+
+def test_single_expert_top1_is_dense_swiglu():
+    L, x = _tiny_layer(E=1, k=1, shared=0, bias=False)
+    lg, idx, gates, out = L.forward(x)
+    assert np.all(idx == 0) and np.all(gates == 1.0)
+    ref = _dense_swiglu(L, 0, _bf16_vals(x))
+    assert np.allclose(out, ref, rtol=1e-6, atol=1e-9)
+
+
+def test_whole_layer_matches_numpy_composition():
+    L, x = _tiny_layer(E=8, k=3, shared=1)
+    lg, idx, gates, out = L.forward(x)
+    xv = _bf16_vals(x)
+    ref_lg = ((xv @ _bf16_vals(L.router).T).astype(np.float32) + L.bias).astype(np.float64)
+    p = softmax(ref_lg, axis=1)
+    ys = {e: _dense_swiglu(L, e, xv) for e in range(L.E + 1)}
+    for t in range(x.shape[0]):
+        sel = np.lexsort((np.arange(L.E), -p[t]))[:L.k]
+        assert list(idx[t]) == list(sel)
+        g = p[t, sel] / p[t, sel].sum()
+        ref = sum(g[j] * ys[sel[j]][t] for j in range(L.k)) + ys[L.E][t]
+        assert np.allclose(out[t], ref, rtol=1e-6, atol=1e-9)
+
+
+def test_workload_inputs_are_seeded_and_shaped():
+    w = gen.get_workload(0)
+    x1, x2 = gen.x_tokens(w), gen.x_tokens(w)
+    assert x1.shape == (w.T, w.H) and np.array_equal(x1, x2)
+    xs = _bf16_vals(x1)
+    assert abs(xs.mean()) < 0.1 and 0.9 < xs.std() < 1.1
+    W = gen.expert_weight(w, 0, 2)
+    assert W.shape == (w.H, w.I) and 0.018 < W.std() < 0.022
+    # a slice drawn on its own equals the same slice of the whole tensor
+    assert np.array_equal(gen.x_tokens(w, T=2, first=2), x1[2:4])
+    zb = gen.router_bias(gen.get_workload(1))
+    assert sorted(zb)[-1] == np.float32(0.5) and np.all(zb > 0)

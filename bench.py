@@ -1,0 +1,372 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized MoE expert layer on GB300.
+
+Metric: routed tokens/s per MoE layer (T / time per layer forward), on the
+decode workload H=2048, I=512, E=512, top-10 + 1 shared expert, NVFP4
+experts, T=1 token per step.  A step passes the token through a stack of L
+distinct layer instances (default 32; each its own weights, so the 32 x 21.6
+MB touched per step are far larger than the 129 MB L2), captured once as a
+CUDA graph and replayed.  Inputs are resident in HBM before the timed region.
+
+Also reported: the dominant kernel's (gate/up + SwiGLU) achieved HBM bandwidth
+against the measured copy bandwidth, the same metric end to end through the
+host-buffer C-ABI call (moe_forward_host: copies inside the timed region), SM
+clocks sampled during the timed region, and the CPU oracle timed on the host
+cores on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replicas (weak scaling: no
+collective on the data path); the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s per MoE layer on 1 GB300; HBM GB/s as % of ~8 TB/s roofline"
+UNIT = "tokens/s"
+WORKLOAD = 1  # decode-h2048-i512-e512-k10-s1-t1-nvfp4
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def config_block(w, L, extra=None):
+    c = {"workload": w.name, "H": w.H, "I": w.I, "E": w.E, "k": w.k, "shared_experts": w.shared,
+         "tokens_per_step": w.T, "format": "nvfp4 (e2m1, e4m3 per 16, fp32 tensor scale)",
+         "layer_instances_per_step": L, "l2": "inputs larger than L2 (distinct weights per layer)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.rows = []
+
+    def _one(self, loop):
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        if loop:
+            cmd += ["-lms", "100"]
+        return cmd
+
+    def start(self):
+        try:
+            self.rows += self._snap()
+            self.proc = subprocess.Popen(self._one(True), stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def _snap(self):
+        try:
+            out = subprocess.run(self._one(False), capture_output=True, text=True, timeout=10).stdout
+            return [l for l in out.splitlines() if l.strip()]
+        except Exception:
+            return []
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+                self.rows += [l for l in out.splitlines() if l.strip()]
+            except Exception:
+                self.proc.kill()
+        self.rows += self._snap()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def oracle_baseline(w, seconds, n_tok=8):
+    """The oracle as it stands on n_tok decode tokens of the workload (its weights
+    quantised by the oracle beforehand, not timed); repeated for ~`seconds`."""
+    import gen
+    import oracle
+    x = gen.x_tokens(w, n_tok)
+    base = oracle.Layer(w.fmt, w.H, w.I, w.E, w.k, w.shared, gen.router_weights(w),
+                        gen.router_bias(w))
+    idx, _ = base.topk(base.logits(x))
+    need = sorted(set(idx.ravel().tolist()) | {w.E})
+    L = oracle.layer_for_workload(w, need)
+    threads = min(n_tok, os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        L.forward(x, threads=threads)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": reps * n_tok / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n_tok} decode tokens of {w.name} x {reps} repetitions "
+                      f"({dt:.1f} s; oracle threaded over tokens, fp64)"}, dt / reps / n_tok
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import gen
+    oracle.build()
+    gen.build(device=False)
+    n_tok = 8
+    x = gen.x_tokens(w, n_tok)
+    base = oracle.Layer(w.fmt, w.H, w.I, w.E, w.k, w.shared, gen.router_weights(w),
+                        gen.router_bias(w))
+    idx, _ = base.topk(base.logits(x))
+    L = oracle.layer_for_workload(w, sorted(set(idx.ravel().tolist()) | {w.E}))
+    threads = min(n_tok, os.cpu_count() or 1)
+    for _ in range(args.warmup):
+        L.forward(x, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        L.forward(x, threads=threads)
+    dt = time.perf_counter() - t0
+    value = args.steps * n_tok / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator)",
+            "config": config_block(w, 1, {"reference": "CPU oracle (no reference implementation "
+                                                       "exists for this path)",
+                                          "tokens_per_step": n_tok}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{n_tok} decode tokens per step, {args.steps} steps"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def traffic_from_profile(kernel_src):
+    """dram bytes per launch of the gate/up kernel from the committed ncu summary,
+    or None if the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "gateup_kernel_decode-h2048-e512-k10-t1.md")
+    try:
+        txt = open(p).read()
+        sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt).group(1)
+        b = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt).group(1))
+    except Exception:
+        return None
+    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return b if cur == sha else None
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import gen
+    import quantized_moe_expert_layer_gb300 as moe
+    from quantized_moe_expert_layer_gb300.synthetic import build_layer
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    gen.build(device=True)
+    moe.build()
+    Ln = args.layers
+    T = w.T
+    layers = [build_layer(w, T_max=T, seed=1000 * rank + i) for i in range(Ln)]
+    x_np = gen.x_tokens(w, T, first=rank * T)
+    x = torch.from_numpy(x_np.view(np.int16)).cuda()
+    outs = [torch.empty((T, w.H), dtype=torch.float32, device="cuda") for _ in range(Ln)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for L, o in zip(layers, outs):
+            L.forward(x, o, stream=s)
+    s.synchronize()
+    for L in layers:
+        if L.status() != 0:
+            raise RuntimeError("device status word set after warm-up forward")
+
+    # one step = the token through the L layer instances, as one CUDA graph
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for L, o in zip(layers, outs):
+            L.forward(x, o, stream=s)
+    for _ in range(args.warmup):
+        g.replay()
+    s.synchronize()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(s)
+    for _ in range(args.steps):
+        g.replay()
+    ev1.record(s)
+    torch.cuda.synchronize()
+    clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T * Ln * args.steps / (ms / 1e3)
+
+    # dominant kernel: gate/up + SwiGLU, timed alone over the L layers (launch gaps included)
+    counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    per_launch_bytes = []
+    with torch.cuda.stream(s):
+        for L, o in zip(layers, outs):
+            L.forward(x, o, stream=s)
+            L.debug_routing(counts=counts, stream=s)
+            s.synchronize()
+            D = int((counts > 0).sum().item()) + w.shared
+            gu_bytes = (w.I // 16) * 2 * (w.H // 64 + (w.H // 64 + 7) // 8) * 512
+            per_launch_bytes.append(D * (gu_bytes + 8) + T * w.H * 2 + (T * w.k + T * w.shared) * w.I * 2)
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk, stream=s):
+        for L, o in zip(layers, outs):
+            L.run_phase(2, x, o, stream=s)
+    for _ in range(5):
+        gk.replay()
+    reps = max(20, min(500, args.steps))
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.synchronize()
+    k0.record(s)
+    for _ in range(reps):
+        gk.replay()
+    k1.record(s)
+    torch.cuda.synchronize()
+    k_us = k0.elapsed_time(k1) * 1e3 / (reps * Ln)
+    bytes_launch = sum(per_launch_bytes) / len(per_launch_bytes)
+    peak, peak_kind = peaks()
+    achieved = bytes_launch / (k_us * 1e-6) / 1e9
+    traffic = traffic_from_profile(os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc",
+                                                "expert.cu"))
+    roofline = {"bound": "hbm", "kernel": "gateup_kernel", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": k_us,
+                "peak_source": peak_kind,
+                "timing": "CUDA events over a graph of back-to-back launches, gaps included"}
+
+    # e2e: the host-buffer C-ABI call, copies inside the timed region
+    xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+    ohs = [torch.empty((T, w.H), dtype=torch.float32).pin_memory() for _ in range(Ln)]
+    for L, oh in zip(layers, ohs):
+        L.forward_host(xh, oh, stream=s)
+    k_e2e = max(5, min(args.steps, 100))
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        for L, oh in zip(layers, ohs):
+            L.forward_host(xh, oh, stream=s)
+    e2e_dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_dt], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_dt = float(t.item())
+    e2e = {"value": world * T * Ln * k_e2e / e2e_dt, "unit": UNIT,
+           "h2d_bytes_per_step": Ln * T * w.H * 2, "d2h_bytes_per_step": Ln * T * w.H * 4,
+           "call": "moe_forward_host per layer (pinned host buffers, synchronous)"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (nvfp4 weights)",
+            "data": "synthetic (seeded generator; random-init weights quantised on the device)",
+            "config": config_block(w, Ln, {"us_per_layer": ms * 1e3 / (args.steps * Ln),
+                                           "parallelism": f"replicas x{world}"}),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": 5 * Ln * args.steps,
+            "clocks": clocks.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"], _ = oracle_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for L in layers:
+        L.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    import gen
+    w = gen.get_workload(WORKLOAD)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

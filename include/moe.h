@@ -1,0 +1,178 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) quantized mixture-of-experts FFN layer.
+ *
+ * The layer step: router logits, softmax / top-k with renormalised gates,
+ * token-to-expert dispatch, per-expert SwiGLU  y = W_down (silu(W_gate x) * (W_up x))
+ * with the expert weights dequantised on the fly from NVFP4 (e2m1 codes, an
+ * e4m3 scale per 16 weights, an fp32 tensor scale) or FP6 e2m3 (a power-of-two
+ * scale per 128 weights), the gate-weighted combine, and an always-on shared
+ * expert.  The formats are those of the knivesysl README, "formats" (six-bit
+ * e2m3 values with a power-of-two scale per 128 weights; four-bit values with
+ * a scale per 16); the router with top-k and the shared expert are the
+ * "router_top10" / "shared_expert" kernels of "Strata on an Intel Arc",
+ * "The engine itself on Intel: the SYCL port".
+ *
+ * Conventions for every entry point:
+ *   - return 0 (MOE_OK) on success, a negative moe_status on failure; the
+ *     message of the last failure on the calling thread is moe_last_error();
+ *   - `stream` is a cudaStream_t passed as void* (0 = the legacy default stream);
+ *     device-side work is asynchronous on that stream unless stated;
+ *   - "device pointer" means memory of the layer's CUDA device that the caller
+ *     owns and keeps alive until the stream has finished with it;
+ *   - the library owns the packed weights, router copy and workspace of a layer;
+ *   - one layer is used from one stream at a time (its workspace is shared).
+ * Dimensions: H hidden size, I expert intermediate size, E routed experts,
+ * k experts per token, T tokens.  H and I are multiples of 64 (NVFP4) or of
+ * 128 (FP6); 1 <= E <= 1024; 1 <= k <= min(E, 32).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_layer moe_layer; /* opaque */
+
+enum moe_format { MOE_FMT_NVFP4 = 1, MOE_FMT_FP6_E2M3 = 2 };
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,   /* bad argument (null pointer, size, alignment) */
+  MOE_ENOMEM = -2,   /* device allocation failed */
+  MOE_ECUDA = -3,    /* a CUDA call failed; moe_last_error() names it */
+  MOE_ESTATE = -4,   /* call out of order (forward before pack / reserve) */
+  MOE_ETIMEOUT = -5  /* a bounded device wait gave up (see moe_layer_status) */
+};
+
+enum moe_matrix { MOE_GATE = 0, MOE_UP = 1, MOE_DOWN = 2 };
+
+/* where a pointer argument lives */
+enum moe_where { MOE_HOST = 0, MOE_DEVICE = 1 };
+
+/* ------------------------------------------------------------------ lifetime */
+
+/* Create a layer on the current CUDA device.  format: moe_format; shared: 0 or 1
+ * (one always-on shared expert of intermediate size I, weight 1).  Allocates
+ * the packed-weight arena (zero-filled) and the tensor-scale table.  *out gets
+ * the handle, or NULL on failure. */
+int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_layer** out);
+
+/* Size the forward workspace for up to T_max tokens per call.  May be called
+ * again to grow it, never while a forward is in flight.  moe_forward allocates
+ * nothing, so a forward can be captured into a CUDA graph after this call. */
+int moe_layer_reserve(moe_layer* L, int T_max);
+
+/* Free everything the layer owns (synchronises its device first).  NULL is a no-op. */
+void moe_layer_destroy(moe_layer* L);
+
+/* Message of the last failure on this thread ("" if none): the operation and,
+ * for MOE_ECUDA, the CUDA error name. */
+const char* moe_last_error(void);
+
+/* Read the layer's device status word into *status: 0, or the negative
+ * moe_status a kernel recorded (MOE_EINVAL from a device-side bounds check on
+ * an expert id or work entry).  Synchronises the device; clears the word when
+ * reset != 0.  Returns MOE_OK, or an error if the read itself failed. */
+int moe_layer_status(moe_layer* L, int reset, int* status);
+
+/* Bytes of the packed arena and of one packed expert (gate + up + down, without
+ * its three fp32 tensor scales). */
+int moe_layer_info(moe_layer* L, uint64_t* arena_bytes, uint64_t* expert_bytes);
+
+/* ------------------------------------------------------------------ weights */
+
+/* Router weights Wr [E x H] as bf16 bits (row-major) and an optional fp32 bias
+ * [E] (NULL = none), host or device memory per `where`.  Copied; synchronous. */
+int moe_set_router(moe_layer* L, const uint16_t* wr_bf16, const float* bias, int where);
+
+/* Pack one expert matrix from the canonical quantised format into the layer's
+ * device layout.  expert in [0, E) for routed experts, E for the shared one;
+ * matrix: moe_matrix (gate and up are [I x H], down is [H x I]; row-major,
+ * blocks run along the row).
+ *   NVFP4: codes [rows x K/2] bytes, two e2m1 codes per byte, the even column
+ *          in the low nibble; scales [rows x K/16] e4m3 bytes; *tscale the fp32
+ *          tensor scale (dequantised weight = (e2m1 * e4m3) * tscale).
+ *   FP6:   codes [rows x K] bytes, one e2m3 code in the low 6 bits of each;
+ *          scales [rows x K/128] ue8m0 exponent bytes (2^(b-127)); tscale
+ *          ignored (may be NULL).
+ * codes / scales / tscale are host or device pointers per `where`.  Device input is
+ * consumed asynchronously on `stream`; host input is copied synchronously. */
+int moe_pack_matrix(moe_layer* L, int expert, int matrix, const uint8_t* codes,
+                    const uint8_t* scales, const float* tscale, int where, void* stream);
+
+/* One matrix of the canonical format (see moe_pack_matrix). */
+typedef struct moe_canonical_matrix {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  float tscale;
+} moe_canonical_matrix;
+
+/* Pack a whole layer from host memory: router (+ optional bias) and
+ * mats[expert * 3 + matrix] for expert in [0, E + shared).  Synchronous. */
+int moe_pack_weights(moe_layer* L, const uint16_t* wr_bf16, const float* bias,
+                     const moe_canonical_matrix* mats);
+
+/* Quantise fp32 weights W [rows x K] (device) to canonical NVFP4 on the device:
+ * tscale = amax(W) / (6 * 448); per 16 weights along K the e4m3 scale
+ * s = rne((amax_16 / 6) / tscale); code = rne_e2m1(w / (s * tscale)); ties to
+ * the even code, saturating, +0 for zero, s = 0 gives code 0; IEEE fp32
+ * division.  Device outputs: codes [rows x K/2], scales [rows x K/16],
+ * tscale [1].  K % 16 == 0.  Uses no workspace beyond its outputs. */
+int moe_quantize_nvfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* scales,
+                       float* tscale, void* stream);
+
+/* Quantise fp32 weights W [rows x K] (device) to canonical FP6 e2m3 on the
+ * device: per 128 weights the exponent E = the smallest integer with
+ * amax_128 <= 7.5 * 2^E (byte E + 127; 127 for an all-zero block) and
+ * code = rne_e2m3(w / 2^E).  Device outputs codes [rows x K], exps [rows x K/128].
+ * K % 128 == 0. */
+int moe_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,
+                     void* stream);
+
+/* ------------------------------------------------------------------ forward */
+
+/* out[T x H] (fp32, device) = the layer applied to x[T x H] (bf16 bits, device).
+ * 1 <= T <= the reserved T_max.  Asynchronous on `stream`; allocates nothing.
+ * x and out must be 16-byte aligned. */
+int moe_forward(moe_layer* L, const uint16_t* x, int T, float* out, void* stream);
+
+/* moe_forward with host buffers: copies x (T x H bf16) to the workspace, runs
+ * the layer, copies out (T x H fp32) back and synchronises `stream`.  Pinned
+ * host memory gives the fastest copies. */
+int moe_forward_host(moe_layer* L, const uint16_t* x_host, int T, float* out_host, void* stream);
+
+/* The layer with the routing given instead of computed: idx [T x k] expert ids
+ * (distinct within a token, each in [0, E)) and gates [T x k] fp32, device
+ * pointers.  Dispatch, experts, shared expert and combine are the kernels
+ * moe_forward runs. */
+int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* idx,
+                       const float* gates, float* out, void* stream);
+
+/* ------------------------------------------------------------------ test hooks */
+
+/* Dequantise one packed matrix back to fp32 [rows x K] (device `out`) from the
+ * packed device bytes, with the decode the expert kernels use. */
+int moe_debug_dequant(moe_layer* L, int expert, int matrix, float* out, void* stream);
+
+/* Copy the routing of the last forward into caller device buffers (any may be
+ * NULL): logits [T x E] fp32 (moe_forward only), idx [T x k], gates [T x k],
+ * counts [E], offsets [E + 1], perm [T x k] (slot ids t*k + j, expert-sorted,
+ * stable). */
+int moe_debug_routing(moe_layer* L, float* logits, int32_t* idx, float* gates, int32_t* counts,
+                      int32_t* offsets, int32_t* perm, void* stream);
+
+/* Re-run one phase of the last moe_forward on the same arguments, for timing a
+ * kernel on its own: 0 router logits, 1 top-k + dispatch, 2 gate/up + SwiGLU,
+ * 3 down, 4 combine.  The workspace must hold that forward's state (same x, T). */
+int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float* out,
+                        void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

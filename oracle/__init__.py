@@ -285,7 +285,21 @@ def layer_for_workload(w, experts=None) -> Layer:
     L = Layer(w.fmt, w.H, w.I, w.E, w.k, w.shared, gen.router_weights(w), gen.router_bias(w))
     if experts is None:
         experts = range(w.n_experts_total)
-    for e in experts:
-        for m in range(3):
-            L.quantize_matrix(int(e), m, gen.expert_weight(w, int(e), m))
+    jobs = [(int(e), m) for e in experts for m in range(3)]
+
+    def one(job):  # the C calls release the GIL, so matrices quantise in parallel
+        e, m = job
+        return job, L_quantize(w, e, m)
+
+    def L_quantize(w_, e, m):
+        W = gen.expert_weight(w_, e, m)
+        if w_.fmt == FMT_NVFP4:
+            return quantize_nvfp4(W)
+        c, s = quantize_fp6(W)
+        return c, s, 1.0
+
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        for (e, m), (c, s, ts) in ex.map(one, jobs):
+            L.set_matrix(e, m, c, s, ts)
     return L

@@ -1,0 +1,233 @@
+"""Quantized MoE expert layer for GB300 (sm_103a): Python binding of the C ABI.
+
+Thin ctypes marshalling over ``libmoe_gb300.so`` (``include/moe.h``).  Every
+step of the layer runs in the library's CUDA kernels; torch is used here only
+to hold device memory and streams.  If the library is missing the import of
+``lib()`` raises: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+CSRC = os.path.join(_HERE, "csrc")
+BUILD = os.path.join(_HERE, "_build")
+LIB = os.path.join(_HERE, "libmoe_gb300.so")
+HEADER = os.path.join(_ROOT, "include", "moe.h")
+SOURCES = ["layer.cu", "quant_pack.cu", "route.cu", "expert.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-cudart", "shared"]
+
+FMT_NVFP4 = 1
+FMT_FP6 = 2
+GATE, UP, DOWN = 0, 1, 2
+HOST, DEVICE = 0, 1
+
+OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT = 0, -1, -2, -3, -4, -5
+
+# every symbol include/moe.h declares
+EXPORTS = [
+    "moe_layer_create", "moe_layer_reserve", "moe_layer_destroy", "moe_last_error",
+    "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
+    "moe_pack_weights", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_forward",
+    "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
+    "moe_debug_run_phase",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _deps():
+    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [HEADER]
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA sources for sm_103a (in parallel) and link the shared library."""
+    deps = _deps()
+    if not force and os.path.exists(LIB) and all(
+            os.path.getmtime(LIB) >= os.path.getmtime(d) for d in deps):
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        cmd = ["nvcc", *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj, r.stderr
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    if verbose:
+        for _, log in results:
+            print(log)
+    tmp = LIB + ".tmp"
+    subprocess.check_call(["nvcc", *ARCH, "-shared", "-cudart", "shared", "-o", tmp,
+                           *[o for o, _ in results]])
+    os.replace(tmp, LIB)
+    return LIB
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(f"{LIB} is missing: run __graft_entry__.build() "
+                                   "(the layer has no CPU fallback)")
+            L = ctypes.CDLL(LIB)
+            P, I, F, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64
+            sig = {
+                "moe_layer_create": (I, [I, I, I, I, I, I, ctypes.POINTER(P)]),
+                "moe_layer_reserve": (I, [P, I]),
+                "moe_layer_destroy": (None, [P]),
+                "moe_last_error": (ctypes.c_char_p, []),
+                "moe_layer_status": (I, [P, I, ctypes.POINTER(I)]),
+                "moe_layer_info": (I, [P, ctypes.POINTER(U64), ctypes.POINTER(U64)]),
+                "moe_set_router": (I, [P, P, P, I]),
+                "moe_pack_matrix": (I, [P, I, I, P, P, P, I, P]),
+                "moe_pack_weights": (I, [P, P, P, P]),
+                "moe_quantize_nvfp4": (I, [P, I, I, P, P, P, P]),
+                "moe_quantize_fp6": (I, [P, I, I, P, P, P]),
+                "moe_forward": (I, [P, P, I, P, P]),
+                "moe_forward_host": (I, [P, P, I, P, P]),
+                "moe_forward_routed": (I, [P, P, I, P, P, P, P]),
+                "moe_debug_dequant": (I, [P, I, I, P, P]),
+                "moe_debug_routing": (I, [P, P, P, P, P, P, P, P]),
+                "moe_debug_run_phase": (I, [P, I, P, I, P, P]),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(L, name)
+                f.restype, f.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+def check(rc: int) -> int:
+    if rc < 0:
+        raise MoeError(rc, lib().moe_last_error().decode())
+    return rc
+
+
+def _ptr(t):
+    """Device (or host) address of a torch tensor / numpy array / None."""
+    if t is None:
+        return None
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return t.ctypes.data
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class MoeLayer:
+    """One quantized MoE layer on the current CUDA device (see include/moe.h)."""
+
+    def __init__(self, fmt, H, I, E, k, shared):
+        self.fmt, self.H, self.I, self.E, self.k, self.shared = fmt, H, I, E, k, int(shared)
+        h = ctypes.c_void_p()
+        check(lib().moe_layer_create(fmt, H, I, E, k, int(shared), ctypes.byref(h)))
+        self.h = h
+
+    def close(self):
+        if self.h:
+            lib().moe_layer_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reserve(self, T_max):
+        check(lib().moe_layer_reserve(self.h, T_max))
+
+    def info(self):
+        a, e = ctypes.c_uint64(), ctypes.c_uint64()
+        check(lib().moe_layer_info(self.h, ctypes.byref(a), ctypes.byref(e)))
+        return a.value, e.value
+
+    def status(self, reset=False):
+        """The device status word (0 or a negative moe_status a kernel recorded)."""
+        v = ctypes.c_int()
+        check(lib().moe_layer_status(self.h, int(reset), ctypes.byref(v)))
+        return v.value
+
+    def set_router(self, wr, bias=None, where=None):
+        where = _where(wr) if where is None else where
+        check(lib().moe_set_router(self.h, _ptr(wr), _ptr(bias), where))
+
+    def pack_matrix(self, expert, matrix, codes, scales, tscale=None, stream=None):
+        """codes/scales (+ tscale) as torch device tensors or numpy host arrays."""
+        where = _where(codes)
+        if where == HOST:
+            import numpy as np
+            ts = None if tscale is None else np.array([tscale], np.float32)
+            check(lib().moe_pack_matrix(self.h, expert, matrix, _ptr(codes), _ptr(scales),
+                                        _ptr(ts), HOST, None))
+        else:
+            check(lib().moe_pack_matrix(self.h, expert, matrix, _ptr(codes), _ptr(scales),
+                                        _ptr(tscale), DEVICE, _stream(stream)))
+
+    def forward(self, x, out, T=None, stream=None):
+        T = x.shape[0] if T is None else T
+        check(lib().moe_forward(self.h, _ptr(x), T, _ptr(out), _stream(stream)))
+
+    def forward_host(self, x_host, out_host, T=None, stream=None):
+        T = x_host.shape[0] if T is None else T
+        check(lib().moe_forward_host(self.h, _ptr(x_host), T, _ptr(out_host), _stream(stream)))
+
+    def forward_routed(self, x, idx, gates, out, stream=None):
+        check(lib().moe_forward_routed(self.h, _ptr(x), x.shape[0], _ptr(idx), _ptr(gates),
+                                       _ptr(out), _stream(stream)))
+
+    def run_phase(self, phase, x, out, T=None, stream=None):
+        T = x.shape[0] if T is None else T
+        check(lib().moe_debug_run_phase(self.h, phase, _ptr(x), T, _ptr(out), _stream(stream)))
+
+    def debug_dequant(self, expert, matrix, out, stream=None):
+        check(lib().moe_debug_dequant(self.h, expert, matrix, _ptr(out), _stream(stream)))
+
+    def debug_routing(self, logits=None, idx=None, gates=None, counts=None, offsets=None,
+                      perm=None, stream=None):
+        check(lib().moe_debug_routing(self.h, _ptr(logits), _ptr(idx), _ptr(gates), _ptr(counts),
+                                      _ptr(offsets), _ptr(perm), _stream(stream)))
+
+
+def _where(t):
+    return DEVICE if (hasattr(t, "is_cuda") and t.is_cuda) else HOST
+
+
+def quantize_nvfp4(W, codes, scales, tscale, stream=None):
+    rows, K = W.shape
+    check(lib().moe_quantize_nvfp4(_ptr(W), rows, K, _ptr(codes), _ptr(scales), _ptr(tscale),
+                                   _stream(stream)))
+
+
+def quantize_fp6(W, codes, exps, stream=None):
+    rows, K = W.shape
+    check(lib().moe_quantize_fp6(_ptr(W), rows, K, _ptr(codes), _ptr(exps), _stream(stream)))

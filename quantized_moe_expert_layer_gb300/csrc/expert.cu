@@ -1,0 +1,386 @@
+// Expert kernels: fused dequant + gate/up GEMM + SwiGLU, dequant + down GEMM,
+// and the gate-weighted combine.
+//
+// Work unit: an entry = (expert, first row, up to 8 tokens) from dispatch, or
+// one of the leading shared-expert entries.  Each CTA takes one entry and one
+// group of 16-row weight tiles; its 4 warps split the tiles and/or the K
+// dimension.  Weights stream from HBM with 16-byte per-lane loads in the order
+// the packed layout stores them (layout.cuh) and are dequantised in registers
+// straight into m16n8k16 A fragments: NVFP4 code * e4m3 block scale is exact
+// in f16; FP6 e2m3 codes are exact in f16 and the power-of-two block scale is
+// applied to an fp32 per-block accumulator.  The activations (x, or the SwiGLU
+// output a) are the B operand, staged once per CTA in shared memory as f16.
+// The fp32 tensor scale is applied in the epilogue.  Partial sums over K are
+// added in a fixed warp order, so results are deterministic and each token's
+// value does not depend on which other tokens share its entry.
+//
+// SwiGLU: a = silu(g) * u with g = W_gate x, u = W_up x, silu(v) = v / (1 + e^-v);
+// y = W_down a.  The fused gate|up and separate down split follows the expert
+// kernels of "Strata on an Intel Arc" and of the nextsycl README ("the
+// experts' gate | up" / "down projection").
+#include "common.cuh"
+#include "kernels.cuh"
+#include "layout.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
+  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// Load the 16 f16 activations of token row `gi` at column `col` (two 16-byte reads).
+__device__ __forceinline__ void load_b(const uint16_t* xs, int stride, int gi, int col, bool have,
+                                       uint32_t (&xw)[8]) {
+  if (have) {
+    const uint4* px = reinterpret_cast<const uint4*>(xs + gi * stride + col);
+    const uint4 q0 = px[0], q1 = px[1];
+    xw[0] = q0.x; xw[1] = q0.y; xw[2] = q0.z; xw[3] = q0.w;
+    xw[4] = q1.x; xw[5] = q1.y; xw[6] = q1.z; xw[7] = q1.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xw[i] = 0u;
+  }
+}
+
+// NT NVFP4 tiles (same K) times the staged activations; super-chunks s0, s0+ds, ...
+template <int NT>
+__device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], const MatGeom& g,
+                                            int s0, int ds, const uint16_t* xs, int stride,
+                                            bool have_b, float (&acc)[NT][4]) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  for (int s = s0; s < g.nsc; s += ds) {
+    const int nc = sc_units(g, s);
+    uint4 sv[NT], cv[NT][8];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const uint8_t* b = tile[i] + (size_t)s * g.sc_bytes + 16 * lane;
+      sv[i] = ldg_stream(b);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < nc) cv[i][j] = ldg_stream(b + 512 * (1 + j));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < nc) {
+        uint32_t xw[8];
+        load_b(xs, stride, gi, 64 * (8 * s + j) + 16 * t, have_b, xw);
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
+          const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t h[4];
+            e2m1x8_to_f16x8(u4get(cv[i][j], w), h);
+            const uint32_t a[4] = {hmul2(h[0], s_lo), hmul2(h[1], s_hi), hmul2(h[2], s_lo),
+                                   hmul2(h[3], s_hi)};
+            mma_f16(acc[i], a, xw[2 * w], xw[2 * w + 1]);
+          }
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fp6_unpack(uint32_t Ha, uint32_t Hb, uint32_t L, uint32_t (&c)[4]) {
+  c[0] = ((Ha << 2) & 0x3C3C3C3Cu) | (L & 0x03030303u);
+  c[1] = ((Ha >> 2) & 0x3C3C3C3Cu) | ((L >> 2) & 0x03030303u);
+  c[2] = ((Hb << 2) & 0x3C3C3C3Cu) | ((L >> 4) & 0x03030303u);
+  c[3] = ((Hb >> 2) & 0x3C3C3C3Cu) | ((L >> 6) & 0x03030303u);
+}
+
+// NT FP6 tiles; pairs (128-column blocks) are loaded four at a time.
+template <int NT>
+__device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], const MatGeom& g,
+                                          int s0, int ds, const uint16_t* xs, int stride,
+                                          bool have_b, float (&acc)[NT][4]) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  for (int s = s0; s < g.nsc; s += ds) {
+    const int np = sc_units(g, s);
+    uint32_t ew[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) ew[i] = ldg_stream_u32(tile[i] + (size_t)s * g.sc_bytes + 4 * lane);
+    for (int j0 = 0; j0 < np; j0 += 4) {
+      uint4 cv[NT][4][3];
+#pragma unroll
+      for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          if (j0 + jj < np)
+#pragma unroll
+            for (int v = 0; v < 3; ++v)
+              cv[i][jj][v] = ldg_stream(tile[i] + (size_t)s * g.sc_bytes + 128 +
+                                        1536 * (j0 + jj) + 512 * v + 16 * lane);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (j0 + jj < np) {
+          const int j = j0 + jj;
+          float blk[NT][4];
+#pragma unroll
+          for (int i = 0; i < NT; ++i)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) blk[i][r] = 0.f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t xw[8];
+            load_b(xs, stride, gi, 128 * (8 * s + j) + 64 * h + 16 * t, have_b, xw);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+              const uint32_t words[12] = {cv[i][jj][0].x, cv[i][jj][0].y, cv[i][jj][0].z,
+                                          cv[i][jj][0].w, cv[i][jj][1].x, cv[i][jj][1].y,
+                                          cv[i][jj][1].z, cv[i][jj][1].w, cv[i][jj][2].x,
+                                          cv[i][jj][2].y, cv[i][jj][2].z, cv[i][jj][2].w};
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                uint32_t c[4];
+                fp6_unpack(words[h * 6 + q * 3], words[h * 6 + q * 3 + 1], words[h * 6 + q * 3 + 2], c);
+#pragma unroll
+                for (int ww = 0; ww < 2; ++ww) {
+                  const int w = 2 * q + ww;
+                  uint32_t u[2], v[2];
+                  e2m3x4_to_f16x4(c[2 * ww], u);      // rows g, g+8 at columns 4w, 4w+1
+                  e2m3x4_to_f16x4(c[2 * ww + 1], v);  // rows g, g+8 at columns 4w+2, 4w+3
+                  const uint32_t a[4] = {u[0], u[1], v[0], v[1]};
+                  mma_f16(blk[i], a, xw[2 * w], xw[2 * w + 1]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NT; ++i) {
+            const uint32_t e = __shfl_sync(0xffffffffu, ew[i], (gi << 2) | (j >> 1));
+            const float f0 = ue8m0_to_f32((e >> (16 * (j & 1))) & 0xFFu);
+            const float f1 = ue8m0_to_f32((e >> (16 * (j & 1) + 8)) & 0xFFu);
+            acc[i][0] = fmaf(blk[i][0], f0, acc[i][0]);
+            acc[i][1] = fmaf(blk[i][1], f0, acc[i][1]);
+            acc[i][2] = fmaf(blk[i][2], f1, acc[i][2]);
+            acc[i][3] = fmaf(blk[i][3], f1, acc[i][3]);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void tiles_mma(int fmt, const uint8_t* const (&tile)[NT],
+                                          const MatGeom& g, int s0, int ds, const uint16_t* xs,
+                                          int stride, bool have_b, float (&acc)[NT][4]) {
+  if (fmt == FMT_NVFP4)
+    tiles_nvfp4<NT>(tile, g, s0, ds, xs, stride, have_b, acc);
+  else
+    tiles_fp6<NT>(tile, g, s0, ds, xs, stride, have_b, acc);
+}
+
+// Entry y of the launch: the first p.nsh are the shared expert's token groups
+// (known without routing); the rest come from dispatch.
+__device__ __forceinline__ bool get_entry(const ExpertParams& p, int y, int& expert, int& row,
+                                          int& n) {
+  const int S = p.T * p.k;
+  if (y < p.nsh) {
+    expert = p.E;
+    row = S + kTokTile * y;
+    n = min(kTokTile, p.T - kTokTile * y);
+    return true;
+  }
+  const int r = y - p.nsh;
+  if (r >= *p.n_entries) return false;
+  const int4 e = p.entries[r];
+  expert = e.x;
+  row = e.y;
+  n = e.z;
+  if (expert < 0 || expert >= p.E || n < 1 || n > kTokTile || row < 0 || row + n > S) {
+    *p.status = -1;  // MOE_EINVAL: corrupt entry, skip it
+    return false;
+  }
+  return true;
+}
+
+// Sum the per-warp partials of warps sharing a tile (fixed order) into warp ks == 0.
+template <int NV>
+__device__ __forceinline__ void reduce_ksplit(float* red, float (&v)[NV], int tpc, int nks) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (nks == 1) return;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) red[(warp * 32 + lane) * NV + i] = v[i];
+  __syncthreads();
+  if (warp / tpc == 0) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    for (int ks = 0; ks < nks; ++ks) {
+      const int w2 = ks * tpc + warp;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] += red[(w2 * 32 + lane) * NV + i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- gate/up + SwiGLU
+__global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tpc) {
+  griddep_launch();
+  const int y = blockIdx.y;
+  if (y >= p.nsh) griddep_wait();
+  int expert, row, n;
+  if (!get_entry(p, y, expert, row, n)) return;
+  const int S = p.T * p.k;
+  const int H = p.H, stride = H + 8;
+  extern __shared__ uint4 smem_u4[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
+  float* red = reinterpret_cast<float*>(xs + min(kTokTile, p.T) * stride);
+  for (int i = threadIdx.x; i < n * (H / 8); i += kThreads) {
+    const int c = i / (H / 8), v = i % (H / 8);
+    const int tok = (expert == p.E) ? row - S + c : p.row_token[row + c];
+    const uint4 raw = *reinterpret_cast<const uint4*>(p.x + (size_t)tok * H + 8 * v);
+    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half lo = __float2half_rn(__uint_as_float(in[q] << 16));
+      const __half hi = __float2half_rn(__uint_as_float(in[q] & 0xFFFF0000u));
+      o[q] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    }
+    *reinterpret_cast<uint4*>(xs + c * stride + 8 * v) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int nks = kWarps / tpc;
+  const int pair = blockIdx.x * tpc + (warp % tpc), ks = warp / tpc;
+  const bool valid = pair < p.I / 16;
+  const MatGeom g = mat_geom(p.fmt, H);
+  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
+  const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
+                                   eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  if (valid) tiles_mma<2>(p.fmt, tiles, g, ks, nks, xs, stride, gi < n, acc);
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = acc[0][i];
+    v[4 + i] = acc[1][i];
+  }
+  reduce_ksplit<8>(red, v, tpc, nks);
+  if (ks != 0 || !valid) return;
+  const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 16 * pair + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+    if (col < n) {
+      const float G = ts_g * v[i], U = ts_u * v[4 + i];
+      const float a = G / (1.0f + expf(-G)) * U;
+      p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- down
+__global__ void __launch_bounds__(kThreads) down_kernel(ExpertParams p, int tpc) {
+  griddep_launch();
+  griddep_wait();
+  int expert, row, n;
+  if (!get_entry(p, blockIdx.y, expert, row, n)) return;
+  const int I = p.I, stride = I + 8;
+  extern __shared__ uint4 smem_u4[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
+  float* red = reinterpret_cast<float*>(xs + min(kTokTile, p.T) * stride);
+  for (int i = threadIdx.x; i < n * (I / 8); i += kThreads) {
+    const int c = i / (I / 8), v = i % (I / 8);
+    *reinterpret_cast<uint4*>(xs + c * stride + 8 * v) =
+        *reinterpret_cast<const uint4*>(p.abuf + (size_t)(row + c) * I + 8 * v);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int nks = kWarps / tpc;
+  const int tile = blockIdx.x * tpc + (warp % tpc), ks = warp / tpc;
+  const bool valid = tile < p.H / 16;
+  const MatGeom g = mat_geom(p.fmt, I);
+  const uint8_t* const tiles[1] = {p.arena + (size_t)expert * p.expert_bytes + p.gu_bytes +
+                                   (size_t)tile * p.dn_tile_bytes};
+  float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+  if (valid) tiles_mma<1>(p.fmt, tiles, g, ks, nks, xs, stride, gi < n, acc);
+  float v[4] = {acc[0][0], acc[0][1], acc[0][2], acc[0][3]};
+  reduce_ksplit<4>(red, v, tpc, nks);
+  if (ks != 0 || !valid) return;
+  const float ts = p.tscale[expert * 3 + 2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 16 * tile + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+    if (col < n) p.ybuf[(size_t)(row + col) * p.H + r] = ts * v[i];
+  }
+}
+
+// ---------------------------------------------------------------- combine
+// out[t] = sum_j gates[t,j] * y[row(t,j)] + y_shared[t], j in order.
+__global__ void __launch_bounds__(256) combine_kernel(ExpertParams p, const float* gates,
+                                                      const int* inv, float* out) {
+  griddep_launch();
+  griddep_wait();
+  const int H4 = p.H / 4, S = p.T * p.k;
+  const float4* y4 = reinterpret_cast<const float4*>(p.ybuf);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)p.T * H4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H4), h = (int)(i % H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < p.k; ++j) {
+      const float gj = gates[(size_t)t * p.k + j];
+      const float4 yv = y4[(size_t)inv[(size_t)t * p.k + j] * H4 + h];
+      acc.x = fmaf(gj, yv.x, acc.x);
+      acc.y = fmaf(gj, yv.y, acc.y);
+      acc.z = fmaf(gj, yv.z, acc.z);
+      acc.w = fmaf(gj, yv.w, acc.w);
+    }
+    if (p.shared) {
+      const float4 yv = y4[(size_t)(S + t) * H4 + h];
+      acc.x += yv.x; acc.y += yv.y; acc.z += yv.z; acc.w += yv.w;
+    }
+    reinterpret_cast<float4*>(out)[i] = acc;
+  }
+}
+
+int tiles_per_cta(int nsc) {
+  if (nsc >= kWarps) return 1;
+  if (nsc == 2) return 2;
+  if (nsc == 1) return kWarps;
+  return 1;
+}
+
+size_t stage_smem(int T, int K) {
+  return (size_t)(T < kTokTile ? T : kTokTile) * (K + 8) * 2 + (size_t)kThreads * 8 * sizeof(float);
+}
+
+}  // namespace
+
+cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
+  const int tpc = tiles_per_cta(mat_geom(p.fmt, p.H).nsc);
+  const int pairs = p.I / 16;
+  dim3 grid((pairs + tpc - 1) / tpc, grid_y);
+  return launch_k(gateup_kernel, grid, dim3(kThreads), stage_smem(p.T, p.H), st, pdl, p, tpc);
+}
+
+cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
+  const int tpc = tiles_per_cta(mat_geom(p.fmt, p.I).nsc);
+  const int tiles = p.H / 16;
+  dim3 grid((tiles + tpc - 1) / tpc, grid_y);
+  return launch_k(down_kernel, grid, dim3(kThreads), stage_smem(p.T, p.I), st, pdl, p, tpc);
+}
+
+cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int* inv, float* out,
+                           bool pdl, cudaStream_t st) {
+  const int64_t n = (int64_t)p.T * (p.H / 4);
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  return launch_k(combine_kernel, dim3(blocks), dim3(256), 0, st, pdl, p, gates, inv, out);
+}
+
+cudaError_t expert_kernels_init() {
+  cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       200 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+}
+
+}  // namespace moe

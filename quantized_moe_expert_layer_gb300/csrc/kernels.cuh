@@ -1,0 +1,94 @@
+// Launchers of the layer's kernels (implemented in quant_pack.cu, route.cu, expert.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace moe {
+
+constexpr int kTokTile = 8;     // tokens per expert entry (the n of m16n8k16)
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+
+// Everything the expert kernels read or write for one forward.
+struct ExpertParams {
+  const uint8_t* arena;
+  uint64_t expert_bytes;
+  uint64_t gu_bytes;
+  int gu_tile_bytes, dn_tile_bytes;
+  const float* tscale;   // [(E + shared) * 3]
+  int fmt, H, I, E, T, k, shared;
+  int nsh;               // leading shared-expert entries: ceil(T / 8) or 0
+  const int4* entries;   // routed entries {expert, first row, tokens, 0}
+  const int* n_entries;  // number of routed entries
+  const int* row_token;  // [T*k + T] token of each row of abuf / ybuf
+  const uint16_t* x;     // bf16 [T x H]
+  uint16_t* abuf;        // f16 bits [(T*k + T) x I]: silu(g) * u per row
+  float* ybuf;           // [(T*k + T) x H]: ts_down * (W_down a) per row
+  int* status;
+};
+
+struct RouteParams {
+  const uint16_t* x;      // bf16 [T x H]
+  const uint16_t* wr;     // bf16 [E x H]
+  const float* bias;      // [E] or null
+  int T, H, E, k, shared, ksplit;
+  float* partial;         // [ksplit x T x E] router partial dot products
+  float* logits;          // [T x E]
+  int* idx;               // [T x k]
+  float* gates;           // [T x k]
+  int* counts;            // [E]
+  int* offsets;           // [E + 1]
+  int* perm;              // [T*k] slot ids in expert-sorted order
+  int* inv;               // [T*k] row of each slot
+  int* row_token;         // [T*k + T]
+  int4* entries;
+  int* n_entries;
+  int* status;
+};
+
+cudaError_t launch_quantize_nvfp4(const float* W, int rows, int K, uint8_t* codes,
+                                  uint8_t* scales, float* tscale, cudaStream_t st);
+cudaError_t launch_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,
+                                cudaStream_t st);
+cudaError_t launch_pack(int fmt, const uint8_t* codes, const uint8_t* scales, int rows, int K,
+                        uint8_t* dst, uint64_t tile_stride, const float* ts_src, float ts_val,
+                        float* ts_dst, cudaStream_t st);
+cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stride, int rows,
+                                 int K, const float* ts_ptr, float* out, cudaStream_t st);
+
+// routing
+int router_ksplit(int T, int H, int E);
+cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
+cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st);
+cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st);
+size_t route_finish_smem(int E);
+cudaError_t route_kernels_init();
+
+// experts
+cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st);
+cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st);
+cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int* inv, float* out,
+                           bool pdl, cudaStream_t st);
+cudaError_t expert_kernels_init();
+
+// launch helper: optional programmatic dependent launch on the previous kernel in the stream
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace moe

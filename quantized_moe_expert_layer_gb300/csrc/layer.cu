@@ -1,0 +1,538 @@
+// The C ABI of include/moe.h: layer lifetime, weight packing, the forward
+// pass (router -> top-k / dispatch -> gate/up + SwiGLU -> down -> combine,
+// chained with programmatic dependent launch) and the test hooks.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "kernels.cuh"
+#include "layout.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(const char* op, cudaError_t e) {
+  return fail(MOE_ECUDA, "%s: %s (%s)", op, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define CK(op, call)                                 \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(op, e_); \
+  } while (0)
+
+// Makes the layer's device current for the scope of an entry point.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Upper bound on routed entries (ceil(count/8) summed over experts) for T tokens.
+int max_routed_entries(int T, int E, int k) {
+  const long S = (long)T * k;
+  const long m = S < E ? S : E;
+  long b = (S + 7 * m) / kTokTile;
+  if (b > S) b = S;
+  return (int)b;
+}
+
+}  // namespace
+
+struct moe_layer {
+  int device = 0;
+  int fmt = 0, H = 0, I = 0, E = 0, k = 0, shared = 0;
+  ExpertGeom geom{};
+  uint8_t* arena = nullptr;
+  uint64_t arena_bytes = 0;
+  float* tscale = nullptr;
+  uint16_t* router = nullptr;
+  float* bias = nullptr;
+  bool has_bias = false;
+  bool router_set = false;
+  int* status = nullptr;
+  // workspace
+  int T_max = 0;
+  void* ws = nullptr;
+  float* partial = nullptr;
+  float* logits = nullptr;
+  int* idx = nullptr;
+  float* gates = nullptr;
+  int* counts = nullptr;
+  int* offsets = nullptr;
+  int* perm = nullptr;
+  int* inv = nullptr;
+  int* row_token = nullptr;
+  int4* entries = nullptr;
+  int* n_entries = nullptr;
+  uint16_t* abuf = nullptr;
+  float* ybuf = nullptr;
+  uint16_t* x_stage = nullptr;
+  float* out_stage = nullptr;
+  int last_T = 0;
+  bool last_has_logits = false;
+};
+
+namespace {
+
+RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
+  RouteParams p{};
+  p.x = x;
+  p.wr = L->router;
+  p.bias = L->has_bias ? L->bias : nullptr;
+  p.T = T;
+  p.H = L->H;
+  p.E = L->E;
+  p.k = L->k;
+  p.shared = L->shared;
+  p.ksplit = router_ksplit(T, L->H, L->E);
+  p.partial = L->partial;
+  p.logits = L->logits;
+  p.idx = L->idx;
+  p.gates = L->gates;
+  p.counts = L->counts;
+  p.offsets = L->offsets;
+  p.perm = L->perm;
+  p.inv = L->inv;
+  p.row_token = L->row_token;
+  p.entries = L->entries;
+  p.n_entries = L->n_entries;
+  p.status = L->status;
+  return p;
+}
+
+ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
+  ExpertParams p{};
+  p.arena = L->arena;
+  p.expert_bytes = L->geom.expert_bytes;
+  p.gu_bytes = L->geom.gu_bytes;
+  p.gu_tile_bytes = L->geom.gu.tile_bytes;
+  p.dn_tile_bytes = L->geom.dn.tile_bytes;
+  p.tscale = L->tscale;
+  p.fmt = L->fmt;
+  p.H = L->H;
+  p.I = L->I;
+  p.E = L->E;
+  p.T = T;
+  p.k = L->k;
+  p.shared = L->shared;
+  p.nsh = L->shared ? (T + kTokTile - 1) / kTokTile : 0;
+  p.entries = L->entries;
+  p.n_entries = L->n_entries;
+  p.row_token = L->row_token;
+  p.x = x;
+  p.abuf = L->abuf;
+  p.ybuf = L->ybuf;
+  p.status = L->status;
+  return p;
+}
+
+int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
+  if (!L) return fail(MOE_EINVAL, "moe_forward: null layer");
+  if (!x || !out) return fail(MOE_EINVAL, "moe_forward: null x or out");
+  if (((uintptr_t)x | (uintptr_t)out) & 15u)
+    return fail(MOE_EINVAL, "moe_forward: x and out must be 16-byte aligned");
+  if (T < 1) return fail(MOE_EINVAL, "moe_forward: T = %d < 1", T);
+  if (!L->ws || T > L->T_max)
+    return fail(MOE_ESTATE, "moe_forward: T = %d exceeds the reserved T_max = %d", T, L->T_max);
+  if (!L->router_set) return fail(MOE_ESTATE, "moe_forward: router weights not set");
+  const long grid_y = (L->shared ? (T + kTokTile - 1) / kTokTile : 0) +
+                      max_routed_entries(T, L->E, L->k);
+  if (grid_y > 65535)
+    return fail(MOE_EINVAL, "moe_forward: T = %d needs %ld expert work entries (> 65535)", T, grid_y);
+  return MOE_OK;
+}
+
+// experts + combine, after routing has filled idx / gates / dispatch
+int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
+  ExpertParams ep = expert_params(L, x, T);
+  const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
+  CK("gate/up kernel launch", launch_gateup(ep, grid_y, true, st));
+  CK("down kernel launch", launch_down(ep, grid_y, true, st));
+  CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
+  return MOE_OK;
+}
+
+int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
+  RouteParams rp = route_params(L, x, T);
+  CK("router kernel launch", launch_router(rp, st));
+  if (T <= 64) {
+    CK("top-k/dispatch kernel launch", launch_route_finish(rp, true, true, st));
+  } else {
+    CK("top-k kernel launch", launch_topk(rp, true, st));
+    CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
+  }
+  L->last_T = T;
+  L->last_has_logits = true;
+  return run_experts(L, x, T, out, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_layer** out) {
+  if (!out) return fail(MOE_EINVAL, "moe_layer_create: null out");
+  *out = nullptr;
+  if (format != MOE_FMT_NVFP4 && format != MOE_FMT_FP6_E2M3)
+    return fail(MOE_EINVAL, "moe_layer_create: unknown format %d", format);
+  const int mult = format == MOE_FMT_NVFP4 ? 64 : 128;
+  if (H <= 0 || I <= 0 || H % mult || I % mult)
+    return fail(MOE_EINVAL, "moe_layer_create: H=%d and I=%d must be positive multiples of %d", H,
+                I, mult);
+  if (E < 1 || E > kMaxE) return fail(MOE_EINVAL, "moe_layer_create: E=%d not in [1, %d]", E, kMaxE);
+  if (k < 1 || k > E || k > kMaxK)
+    return fail(MOE_EINVAL, "moe_layer_create: k=%d not in [1, min(E, %d)]", k, kMaxK);
+  if (shared != 0 && shared != 1) return fail(MOE_EINVAL, "moe_layer_create: shared must be 0 or 1");
+  moe_layer* L = new moe_layer();
+  L->fmt = format;
+  L->H = H;
+  L->I = I;
+  L->E = E;
+  L->k = k;
+  L->shared = shared;
+  L->geom = expert_geom(format, H, I);
+  cudaError_t e = cudaGetDevice(&L->device);
+  if (e == cudaSuccess) e = route_kernels_init();
+  if (e == cudaSuccess) e = expert_kernels_init();
+  if (e != cudaSuccess) {
+    delete L;
+    return cuda_fail("moe_layer_create: device set-up", e);
+  }
+  const int n_total = E + shared;
+  L->arena_bytes = (uint64_t)n_total * L->geom.expert_bytes;
+  if (cudaMalloc(&L->arena, L->arena_bytes) != cudaSuccess ||
+      cudaMalloc(&L->tscale, sizeof(float) * 3 * n_total) != cudaSuccess ||
+      cudaMalloc(&L->router, sizeof(uint16_t) * (size_t)E * H) != cudaSuccess ||
+      cudaMalloc(&L->bias, sizeof(float) * E) != cudaSuccess ||
+      cudaMalloc(&L->status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    moe_layer_destroy(L);
+    return fail(MOE_ENOMEM, "moe_layer_create: cudaMalloc of %.1f MB failed",
+                L ? (double)L->arena_bytes / 1e6 : 0.0);
+  }
+  if (cudaMemset(L->arena, 0, L->arena_bytes) != cudaSuccess ||
+      cudaMemset(L->tscale, 0, sizeof(float) * 3 * n_total) != cudaSuccess ||
+      cudaMemset(L->status, 0, sizeof(int)) != cudaSuccess) {
+    moe_layer_destroy(L);
+    return fail(MOE_ECUDA, "moe_layer_create: cudaMemset failed");
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+int moe_layer_reserve(moe_layer* L, int T_max) {
+  if (!L) return fail(MOE_EINVAL, "moe_layer_reserve: null layer");
+  if (T_max < 1) return fail(MOE_EINVAL, "moe_layer_reserve: T_max = %d < 1", T_max);
+  if (T_max <= L->T_max) return MOE_OK;
+  DeviceGuard dg(L->device);
+  const size_t S = (size_t)T_max * L->k, E = L->E;
+  size_t partial = 0;
+  for (int T = 1; T <= T_max; ++T) {
+    size_t v = (size_t)router_ksplit(T, L->H, L->E) * T * E;
+    if (v > partial) partial = v;
+  }
+  const size_t n_entries = (size_t)max_routed_entries(T_max, L->E, L->k);
+  const size_t sizes[] = {
+      partial * 4,                       // partial
+      (size_t)T_max * E * 4,             // logits
+      S * 4, S * 4,                      // idx, gates
+      E * 4, (E + 1) * 4,                // counts, offsets
+      S * 4, S * 4,                      // perm, inv
+      (S + T_max) * 4,                   // row_token
+      n_entries * 16, 16,                // entries, n_entries
+      (S + T_max) * L->I * 2,            // abuf
+      (S + T_max) * L->H * 4,            // ybuf
+      (size_t)T_max * L->H * 2,          // x_stage
+      (size_t)T_max * L->H * 4,          // out_stage
+  };
+  const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += align_up(sizes[i], 256);
+  void* ws = nullptr;
+  if (cudaMalloc(&ws, total) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MOE_ENOMEM, "moe_layer_reserve: cudaMalloc of %.1f MB failed", total / 1e6);
+  }
+  if (L->ws) {
+    cudaDeviceSynchronize();
+    cudaFree(L->ws);
+  }
+  L->ws = ws;
+  char* p = static_cast<char*>(ws);
+  void* ptrs[16];
+  for (int i = 0; i < n; ++i) {
+    ptrs[i] = p;
+    p += align_up(sizes[i], 256);
+  }
+  L->partial = (float*)ptrs[0];
+  L->logits = (float*)ptrs[1];
+  L->idx = (int*)ptrs[2];
+  L->gates = (float*)ptrs[3];
+  L->counts = (int*)ptrs[4];
+  L->offsets = (int*)ptrs[5];
+  L->perm = (int*)ptrs[6];
+  L->inv = (int*)ptrs[7];
+  L->row_token = (int*)ptrs[8];
+  L->entries = (int4*)ptrs[9];
+  L->n_entries = (int*)ptrs[10];
+  L->abuf = (uint16_t*)ptrs[11];
+  L->ybuf = (float*)ptrs[12];
+  L->x_stage = (uint16_t*)ptrs[13];
+  L->out_stage = (float*)ptrs[14];
+  L->T_max = T_max;
+  CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
+  return MOE_OK;
+}
+
+void moe_layer_destroy(moe_layer* L) {
+  if (!L) return;
+  DeviceGuard dg(L->device);
+  cudaDeviceSynchronize();
+  cudaFree(L->arena);
+  cudaFree(L->tscale);
+  cudaFree(L->router);
+  cudaFree(L->bias);
+  cudaFree(L->status);
+  cudaFree(L->ws);
+  delete L;
+}
+
+int moe_layer_status(moe_layer* L, int reset, int* status) {
+  if (!L || !status) return fail(MOE_EINVAL, "moe_layer_status: null argument");
+  DeviceGuard dg(L->device);
+  CK("moe_layer_status: synchronize", cudaDeviceSynchronize());
+  CK("moe_layer_status: read", cudaMemcpy(status, L->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (reset) CK("moe_layer_status: reset", cudaMemset(L->status, 0, sizeof(int)));
+  return MOE_OK;
+}
+
+int moe_layer_info(moe_layer* L, uint64_t* arena_bytes, uint64_t* expert_bytes) {
+  if (!L) return fail(MOE_EINVAL, "moe_layer_info: null layer");
+  if (arena_bytes) *arena_bytes = L->arena_bytes;
+  if (expert_bytes) *expert_bytes = L->geom.expert_bytes;
+  return MOE_OK;
+}
+
+int moe_set_router(moe_layer* L, const uint16_t* wr_bf16, const float* bias, int where) {
+  if (!L || !wr_bf16) return fail(MOE_EINVAL, "moe_set_router: null argument");
+  DeviceGuard dg(L->device);
+  const cudaMemcpyKind kind = where == MOE_DEVICE ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+  CK("moe_set_router: copy weights",
+     cudaMemcpy(L->router, wr_bf16, sizeof(uint16_t) * (size_t)L->E * L->H, kind));
+  L->has_bias = bias != nullptr;
+  if (bias) CK("moe_set_router: copy bias", cudaMemcpy(L->bias, bias, sizeof(float) * L->E, kind));
+  L->router_set = true;
+  return MOE_OK;
+}
+
+int moe_pack_matrix(moe_layer* L, int expert, int matrix, const uint8_t* codes,
+                    const uint8_t* scales, const float* tscale, int where, void* stream) {
+  if (!L || !codes || !scales) return fail(MOE_EINVAL, "moe_pack_matrix: null argument");
+  if (L->fmt == MOE_FMT_NVFP4 && !tscale)
+    return fail(MOE_EINVAL, "moe_pack_matrix: NVFP4 needs a tensor scale");
+  if (expert < 0 || expert >= L->E + L->shared)
+    return fail(MOE_EINVAL, "moe_pack_matrix: expert %d out of range", expert);
+  if (matrix < 0 || matrix > 2) return fail(MOE_EINVAL, "moe_pack_matrix: matrix %d", matrix);
+  DeviceGuard dg(L->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int rows = matrix == MOE_DOWN ? L->H : L->I, K = matrix == MOE_DOWN ? L->I : L->H;
+  const size_t code_bytes = L->fmt == MOE_FMT_NVFP4 ? (size_t)rows * K / 2 : (size_t)rows * K;
+  const size_t scale_bytes = L->fmt == MOE_FMT_NVFP4 ? (size_t)rows * K / 16 : (size_t)rows * K / 128;
+  const uint8_t* c = codes;
+  const uint8_t* s = scales;
+  uint8_t* tmp = nullptr;
+  if (where != MOE_DEVICE) {
+    CK("moe_pack_matrix: staging cudaMalloc", cudaMalloc(&tmp, code_bytes + scale_bytes));
+    CK("moe_pack_matrix: copy codes", cudaMemcpy(tmp, codes, code_bytes, cudaMemcpyHostToDevice));
+    CK("moe_pack_matrix: copy scales",
+       cudaMemcpy(tmp + code_bytes, scales, scale_bytes, cudaMemcpyHostToDevice));
+    c = tmp;
+    s = tmp + code_bytes;
+    st = 0;
+  }
+  const ExpertGeom& g = L->geom;
+  uint8_t* dst = L->arena + (size_t)expert * g.expert_bytes + tile_offset(g, matrix, 0);
+  const uint64_t stride = matrix == MOE_DOWN ? (uint64_t)g.dn.tile_bytes : 2u * g.gu.tile_bytes;
+  const bool nv = L->fmt == MOE_FMT_NVFP4;
+  const float* ts_src = (nv && where == MOE_DEVICE) ? tscale : nullptr;
+  const float ts_val = (nv && where != MOE_DEVICE) ? *tscale : 1.0f;
+  cudaError_t e = launch_pack(L->fmt, c, s, rows, K, dst, stride, ts_src, ts_val,
+                              L->tscale + expert * 3 + matrix, st);
+  if (tmp) {
+    cudaError_t e2 = cudaDeviceSynchronize();
+    cudaFree(tmp);
+    if (e == cudaSuccess) e = e2;
+  }
+  CK("moe_pack_matrix: pack kernel", e);
+  return MOE_OK;
+}
+
+int moe_pack_weights(moe_layer* L, const uint16_t* wr_bf16, const float* bias,
+                     const moe_canonical_matrix* mats) {
+  if (!L || !wr_bf16 || !mats) return fail(MOE_EINVAL, "moe_pack_weights: null argument");
+  int rc = moe_set_router(L, wr_bf16, bias, MOE_HOST);
+  if (rc) return rc;
+  for (int e = 0; e < L->E + L->shared; ++e)
+    for (int m = 0; m < 3; ++m) {
+      const moe_canonical_matrix& M = mats[e * 3 + m];
+      rc = moe_pack_matrix(L, e, m, M.codes, M.scales, &M.tscale, MOE_HOST, nullptr);
+      if (rc) return rc;
+    }
+  return MOE_OK;
+}
+
+int moe_quantize_nvfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* scales,
+                       float* tscale, void* stream) {
+  if (!W || !codes || !scales || !tscale) return fail(MOE_EINVAL, "moe_quantize_nvfp4: null argument");
+  if (rows < 1 || K < 16 || K % 16) return fail(MOE_EINVAL, "moe_quantize_nvfp4: bad shape %dx%d", rows, K);
+  if (((uintptr_t)W | (uintptr_t)codes) & 15u)
+    return fail(MOE_EINVAL, "moe_quantize_nvfp4: W and codes must be 16-byte aligned");
+  CK("moe_quantize_nvfp4", launch_quantize_nvfp4(W, rows, K, codes, scales, tscale,
+                                                 (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps, void* stream) {
+  if (!W || !codes || !exps) return fail(MOE_EINVAL, "moe_quantize_fp6: null argument");
+  if (rows < 1 || K < 128 || K % 128) return fail(MOE_EINVAL, "moe_quantize_fp6: bad shape %dx%d", rows, K);
+  if (((uintptr_t)W | (uintptr_t)codes) & 15u)
+    return fail(MOE_EINVAL, "moe_quantize_fp6: W and codes must be 16-byte aligned");
+  CK("moe_quantize_fp6", launch_quantize_fp6(W, rows, K, codes, exps, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_forward(moe_layer* L, const uint16_t* x, int T, float* out, void* stream) {
+  int rc = check_forward_args(L, x, T, out);
+  if (rc) return rc;
+  DeviceGuard dg(L->device);
+  return forward_impl(L, x, T, out, (cudaStream_t)stream);
+}
+
+int moe_forward_host(moe_layer* L, const uint16_t* x_host, int T, float* out_host, void* stream) {
+  if (!L || !x_host || !out_host) return fail(MOE_EINVAL, "moe_forward_host: null argument");
+  int rc = check_forward_args(L, L->x_stage, T, L->out_stage);
+  if (rc) return rc;
+  DeviceGuard dg(L->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  CK("moe_forward_host: copy x", cudaMemcpyAsync(L->x_stage, x_host, (size_t)T * L->H * 2,
+                                                 cudaMemcpyHostToDevice, st));
+  rc = forward_impl(L, L->x_stage, T, L->out_stage, st);
+  if (rc) return rc;
+  CK("moe_forward_host: copy out", cudaMemcpyAsync(out_host, L->out_stage, (size_t)T * L->H * 4,
+                                                   cudaMemcpyDeviceToHost, st));
+  CK("moe_forward_host: synchronize", cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
+int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* idx,
+                       const float* gates, float* out, void* stream) {
+  int rc = check_forward_args(L, x, T, out);
+  if (rc) return rc;
+  if (!idx || !gates) return fail(MOE_EINVAL, "moe_forward_routed: null idx or gates");
+  DeviceGuard dg(L->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t S = (size_t)T * L->k;
+  CK("moe_forward_routed: copy idx", cudaMemcpyAsync(L->idx, idx, S * 4, cudaMemcpyDeviceToDevice, st));
+  CK("moe_forward_routed: copy gates",
+     cudaMemcpyAsync(L->gates, gates, S * 4, cudaMemcpyDeviceToDevice, st));
+  RouteParams rp = route_params(L, x, T);
+  CK("dispatch kernel launch", launch_route_finish(rp, false, false, st));
+  L->last_T = T;
+  L->last_has_logits = false;
+  return run_experts(L, x, T, out, st);
+}
+
+int moe_debug_dequant(moe_layer* L, int expert, int matrix, float* out, void* stream) {
+  if (!L || !out) return fail(MOE_EINVAL, "moe_debug_dequant: null argument");
+  if (expert < 0 || expert >= L->E + L->shared || matrix < 0 || matrix > 2)
+    return fail(MOE_EINVAL, "moe_debug_dequant: expert %d matrix %d out of range", expert, matrix);
+  DeviceGuard dg(L->device);
+  const ExpertGeom& g = L->geom;
+  const int rows = matrix == MOE_DOWN ? L->H : L->I, K = matrix == MOE_DOWN ? L->I : L->H;
+  const uint8_t* src = L->arena + (size_t)expert * g.expert_bytes + tile_offset(g, matrix, 0);
+  const uint64_t stride = matrix == MOE_DOWN ? (uint64_t)g.dn.tile_bytes : 2u * g.gu.tile_bytes;
+  CK("moe_debug_dequant", launch_debug_dequant(L->fmt, src, stride, rows, K,
+                                               L->tscale + expert * 3 + matrix, out,
+                                               (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_debug_routing(moe_layer* L, float* logits, int32_t* idx, float* gates, int32_t* counts,
+                      int32_t* offsets, int32_t* perm, void* stream) {
+  if (!L) return fail(MOE_EINVAL, "moe_debug_routing: null layer");
+  if (!L->last_T) return fail(MOE_ESTATE, "moe_debug_routing: no forward has run");
+  DeviceGuard dg(L->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t T = L->last_T, S = T * L->k, E = L->E;
+  const cudaMemcpyKind d2d = cudaMemcpyDeviceToDevice;
+  if (logits) {
+    if (!L->last_has_logits) return fail(MOE_ESTATE, "moe_debug_routing: last call was routed");
+    CK("moe_debug_routing: logits", cudaMemcpyAsync(logits, L->logits, T * E * 4, d2d, st));
+  }
+  if (idx) CK("moe_debug_routing: idx", cudaMemcpyAsync(idx, L->idx, S * 4, d2d, st));
+  if (gates) CK("moe_debug_routing: gates", cudaMemcpyAsync(gates, L->gates, S * 4, d2d, st));
+  if (counts) CK("moe_debug_routing: counts", cudaMemcpyAsync(counts, L->counts, E * 4, d2d, st));
+  if (offsets)
+    CK("moe_debug_routing: offsets", cudaMemcpyAsync(offsets, L->offsets, (E + 1) * 4, d2d, st));
+  if (perm) CK("moe_debug_routing: perm", cudaMemcpyAsync(perm, L->perm, S * 4, d2d, st));
+  return MOE_OK;
+}
+
+int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float* out,
+                        void* stream) {
+  int rc = check_forward_args(L, x, T, out);
+  if (rc) return rc;
+  if (L->last_T != T || !L->last_has_logits)
+    return fail(MOE_ESTATE, "moe_debug_run_phase: needs a moe_forward with T = %d first", T);
+  DeviceGuard dg(L->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  RouteParams rp = route_params(L, x, T);
+  ExpertParams ep = expert_params(L, x, T);
+  const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
+  switch (phase) {
+    case 0: CK("router", launch_router(rp, st)); break;
+    case 1:
+      if (T <= 64) {
+        CK("top-k/dispatch", launch_route_finish(rp, true, false, st));
+      } else {
+        CK("top-k", launch_topk(rp, false, st));
+        CK("dispatch", launch_route_finish(rp, false, false, st));
+      }
+      break;
+    case 2: CK("gate/up", launch_gateup(ep, grid_y, false, st)); break;
+    case 3: CK("down", launch_down(ep, grid_y, false, st)); break;
+    case 4: CK("combine", launch_combine(ep, L->gates, L->inv, out, false, st)); break;
+    default: return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,296 @@
+// Routing: router logits, softmax / top-k / renormalise, and the expert-sorted
+// dispatch (counts, offsets, stable permutation, per-expert work entries).
+//
+// The router and top-k are the "router_top10" kernel of "Strata on an Intel
+// Arc", "The engine itself on Intel: the SYCL port"; grouping tokens by expert
+// on the device instead of the host follows that page's device-built plan
+// ("resident_plan", "Decode round 2"), where host grouping cost 9% of prompt
+// time.  Readings where the pages are silent: logit = (x . Wr_e) + bias_e with
+// the dot product in fp32; top-k on the logits (softmax is monotone), ties to
+// the lower expert index; the k gates are the softmax over the k selected
+// logits (equal to softmax -> top-k -> renormalise); dispatch order is
+// expert-major, then slot id t*k + j (stable).
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouterThreads = 128;
+constexpr int kFinishThreads = 1024;
+
+// ---------------------------------------------------------------- router logits
+// grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); 4 warps split
+// the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
+// (ksplit slice, token, expert) partial sum goes to p.partial; the top-k step
+// adds the slices in a fixed order.
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
+  griddep_launch();
+  const int tile = blockIdx.x, t0 = blockIdx.y * kTokTile, ks = blockIdx.z;
+  const int n = min(kTokTile, p.T - t0);
+  const int C = p.H / 64;
+  const int c_begin = C * ks / p.ksplit, c_end = C * (ks + 1) / p.ksplit;
+  const int kbase = c_begin * 64, klen = (c_end - c_begin) * 64;
+  const int stride = klen + 8;  // +16 bytes per row: conflict-free 16-byte reads
+  extern __shared__ uint4 smem_u4[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
+  float* red = reinterpret_cast<float*>(xs + kTokTile * stride);
+
+  for (int i = threadIdx.x; i < n * (klen / 8); i += blockDim.x) {
+    const int r = i / (klen / 8), v = i % (klen / 8);
+    *reinterpret_cast<uint4*>(xs + r * stride + 8 * v) =
+        *reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + r) * p.H + kbase + 8 * v);
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int e0 = 16 * tile + gi, e1 = e0 + 8;
+  const uint16_t* r0 = p.wr + (size_t)min(e0, p.E - 1) * p.H;
+  const uint16_t* r1 = p.wr + (size_t)min(e1, p.E - 1) * p.H;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = c_begin + warp; c < c_end; c += 4) {
+    const int kc = 64 * c + 16 * t;
+    uint4 a00 = ldg_stream(r0 + kc), a01 = ldg_stream(r0 + kc + 8);
+    uint4 a10 = ldg_stream(r1 + kc), a11 = ldg_stream(r1 + kc + 8);
+    if (e0 >= p.E) a00 = a01 = make_uint4(0, 0, 0, 0);
+    if (e1 >= p.E) a10 = a11 = make_uint4(0, 0, 0, 0);
+    const uint32_t ra[8] = {a00.x, a00.y, a00.z, a00.w, a01.x, a01.y, a01.z, a01.w};
+    const uint32_t rb[8] = {a10.x, a10.y, a10.z, a10.w, a11.x, a11.y, a11.z, a11.w};
+    uint32_t xw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (gi < n) {
+      const uint4* px = reinterpret_cast<const uint4*>(xs + gi * stride + (kc - kbase));
+      const uint4 q0 = px[0], q1 = px[1];
+      xw[0] = q0.x; xw[1] = q0.y; xw[2] = q0.z; xw[3] = q0.w;
+      xw[4] = q1.x; xw[5] = q1.y; xw[6] = q1.z; xw[7] = q1.w;
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t a[4] = {ra[2 * w], rb[2 * w], ra[2 * w + 1], rb[2 * w + 1]};
+      mma_bf16(acc, a, xw[2 * w], xw[2 * w + 1]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) red[(warp * 32 + lane) * 4 + i] = acc[i];
+  __syncthreads();
+  if (warp != 0) return;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int w = 0; w < kRouterThreads / 32; ++w)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] += red[(w * 32 + lane) * 4 + i];
+  float* out = p.partial + (size_t)ks * p.T * p.E;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = (i < 2) ? e0 : e1, col = 2 * t + (i & 1);
+    if (e < p.E && col < n) out[(size_t)(t0 + col) * p.E + e] = s[i];
+  }
+}
+
+// ---------------------------------------------------------------- top-k (one warp per token)
+__device__ void topk_token(const RouteParams& p, int t, int lane) {
+  const int E = p.E, k = p.k;
+  float v[kMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = -INFINITY;
+    if (e < E) {
+      float l = 0.f;
+      for (int s = 0; s < p.ksplit; ++s) l += p.partial[((size_t)s * p.T + t) * E + e];
+      if (p.bias) l = l + p.bias[e];
+      p.logits[(size_t)t * E + e] = l;
+      v[i] = l;
+    }
+  }
+  uint32_t taken = 0;
+  float my_v = 0.f;
+  int my_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
+  }
+  const float top = __shfl_sync(0xffffffffu, my_v, 0);
+  float ex = (lane < k) ? expf(my_v - top) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    p.idx[(size_t)t * k + lane] = my_i;
+    p.gates[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
+  griddep_launch();
+  griddep_wait();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < p.T) topk_token(p, t, threadIdx.x & 31);
+}
+
+// ---------------------------------------------------------------- dispatch (one CTA of 1024 threads)
+// exclusive scan of v over the block; *total gets the sum
+__device__ int block_excl_scan(int v, int* sc, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sc[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = (lane < (int)(blockDim.x >> 5)) ? sc[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sc[32 + lane] = s;  // inclusive warp-total prefix
+  }
+  __syncthreads();
+  const int before = (w > 0) ? sc[32 + w - 1] : 0;
+  *total = sc[32 + (blockDim.x >> 5) - 1];
+  const int r = before + x - v;
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ int checked_expert(const RouteParams& p, int e) {
+  if (e < 0 || e >= p.E) {
+    *p.status = -1;  // MOE_EINVAL
+    return 0;
+  }
+  return e;
+}
+
+__device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
+  const int S = p.T * p.k, E = p.E;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, NW = blockDim.x >> 5;
+  for (int i = tid; i < NW * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int per = (S + NW - 1) / NW;
+  const int sb = min(S, w * per), se = min(S, sb + per);
+  for (int s = sb + lane; s < se; s += 32) atomicAdd(&hist[w * E + checked_expert(p, p.idx[s])], 1);
+  __syncthreads();
+  int c = 0;
+  if (tid < E)
+    for (int ww = 0; ww < NW; ++ww) c += hist[ww * E + tid];
+  int total;
+  const int excl = block_excl_scan(tid < E ? c : 0, sc, &total);
+  if (tid < E) {
+    p.counts[tid] = c;
+    p.offsets[tid] = excl;
+    int run = excl;
+    for (int ww = 0; ww < NW; ++ww) {
+      const int h = hist[ww * E + tid];
+      hist[ww * E + tid] = run;
+      run += h;
+    }
+  }
+  if (tid == 0) p.offsets[E] = total;
+  __syncthreads();
+  // stable placement: each warp walks its slot range in order, 32 at a time
+  for (int base = sb; base < se; base += 32) {
+    const int s = base + lane;
+    const bool valid = s < se;
+    const int e = valid ? checked_expert(p, p.idx[s]) : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (valid) {
+      const int pos = hist[w * E + e] + __popc(peers & lanemask_lt());
+      p.perm[pos] = s;
+      p.inv[s] = pos;
+      p.row_token[pos] = s / p.k;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) hist[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  for (int i = tid; i < p.T; i += blockDim.x) p.row_token[S + i] = i;
+  // routed work entries: ceil(count / 8) per expert, expert-major
+  const int nch = (tid < E) ? (c + kTokTile - 1) / kTokTile : 0;
+  int n_total;
+  const int ebase = block_excl_scan(nch, sc, &n_total);
+  if (tid < E) {
+    const int off = excl;
+    for (int i = 0; i < nch; ++i)
+      p.entries[ebase + i] = make_int4(tid, off + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
+  }
+  if (tid == 0) *p.n_entries = n_total;
+}
+
+__global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParams p, int do_topk) {
+  griddep_launch();
+  griddep_wait();
+  extern __shared__ int smem_i[];
+  if (do_topk) {
+    for (int t = threadIdx.x >> 5; t < p.T; t += kFinishThreads / 32)
+      topk_token(p, t, threadIdx.x & 31);
+    __syncthreads();
+  }
+  dispatch_block(p, smem_i + 64, smem_i);
+}
+
+}  // namespace
+
+int router_ksplit(int T, int H, int E) {
+  const int tiles = (E + 15) / 16, groups = (T + kTokTile - 1) / kTokTile;
+  const int C = H / 64;
+  int ks = (128 + tiles * groups - 1) / (tiles * groups);
+  if (ks > 8) ks = 8;
+  if (ks > C) ks = C;
+  if (ks < 1) ks = 1;
+  return ks;
+}
+
+size_t route_finish_smem(int E) { return (size_t)(64 + (kFinishThreads / 32) * E) * sizeof(int); }
+
+cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
+  const int C = p.H / 64;
+  const int max_klen = ((C + p.ksplit - 1) / p.ksplit) * 64;
+  const size_t smem = (size_t)kTokTile * (max_klen + 8) * 2 + kRouterThreads * 4 * sizeof(float);
+  dim3 grid((p.E + 15) / 16, (p.T + kTokTile - 1) / kTokTile, p.ksplit);
+  return launch_k(router_kernel, grid, dim3(kRouterThreads), smem, st, false, p);
+}
+
+cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st) {
+  return launch_k(topk_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, pdl, p);
+}
+
+cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st) {
+  return launch_k(route_finish_kernel, dim3(1), dim3(kFinishThreads), route_finish_smem(p.E), st,
+                  pdl, p, do_topk ? 1 : 0);
+}
+
+cudaError_t route_kernels_init() {
+  cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       200 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)route_finish_smem(kMaxE));
+}
+
+}  // namespace moe

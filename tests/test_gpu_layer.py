@@ -1,0 +1,163 @@
+"""GPU: the whole layer against the oracle on the seeded workloads, plus the
+properties that hold at any size (determinism, batch invariance, every output
+written, zero gates, linearity) and the error paths of the C ABI."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import quantized_moe_expert_layer_gb300 as moe
+from quantized_moe_expert_layer_gb300.synthetic import build_layer
+
+from parity import compare_layer, run_gpu, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+_layers = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_ok):
+    gen.build(device=True)
+    moe.build()
+    yield
+    for L in _layers.values():
+        L.close()
+    _layers.clear()
+
+
+def layer(w, T_max=None):
+    key = (w.H, w.I, w.E, w.k, w.shared, w.fmt, w.seed, w.bias, w.bias_scale)
+    if key not in _layers:
+        _layers[key] = build_layer(w, T_max=T_max or 4096)
+    return _layers[key]
+
+
+def small(fmt=1, H=256, I=128, E=8, k=2, shared=1, T=13, bias="normal", seed=3):
+    return gen.Workload(f"small-{fmt}-{H}-{I}-{E}-{k}-{shared}", H, I, E, k, shared, T, fmt, bias,
+                        0.0, 0.1, seed)
+
+
+# ---------------------------------------------------------------- parity per workload
+def test_tiny_workload():
+    w = gen.get_workload(0)
+    rel, ties = compare_layer(w, layer(w), gen.x_tokens(w))
+    assert ties == 0
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+@pytest.mark.parametrize("T", [1, 5, 13, 64, 70, 200])
+def test_small_layers_ragged_token_counts(fmt, T):
+    """Several tiles, ragged last entries, both routing paths (T <= 64 fused,
+    T > 64 separate top-k), both formats, with a shared expert."""
+    w = small(fmt=fmt, H=384 if fmt == 2 else 320, I=256 if fmt == 2 else 192, E=24, k=3, T=T)
+    compare_layer(w, layer(w), gen.x_tokens(w, T))
+
+
+def test_decode_nvfp4_full_size():
+    w = gen.get_workload(1)
+    rel, ties = compare_layer(w, layer(w), gen.x_tokens(w))
+    print(f"decode nvfp4: rel-L2 {rel:.2e}, near ties {ties}")
+
+
+def test_decode_fp6_full_size():
+    w = gen.get_workload(2)
+    L = build_layer(w, T_max=8)
+    try:
+        rel, ties = compare_layer(w, L, gen.x_tokens(w))
+        print(f"decode fp6: rel-L2 {rel:.2e}, near ties {ties}")
+    finally:
+        L.close()
+
+
+def test_batched_decode_full_size():
+    w = gen.get_workload(3)
+    rel, ties = compare_layer(w, layer(w), gen.x_tokens(w))
+    print(f"batched T=64: rel-L2 {rel:.2e}, near ties {ties}")
+
+
+def test_prefill_full_size_sampled():
+    w = gen.get_workload(4)
+    sample = [0, 1, 7, 8, 511, 1024, 2047, 2048, 3000, 4093, 4094, 4095]
+    rel, ties = compare_layer(w, layer(w), gen.x_tokens(w), sample=sample)
+    print(f"prefill T=4096 (sampled): rel-L2 {rel:.2e}, near ties {ties}")
+
+
+# ---------------------------------------------------------------- properties
+def test_deterministic_and_batch_invariant():
+    w = gen.get_workload(1)
+    L = layer(w)
+    x8 = gen.x_tokens(w, 8)
+    a = run_gpu(L, x8, w, want_routing=False)["out"]
+    b = run_gpu(L, x8, w, want_routing=False)["out"]
+    assert np.array_equal(a, b), "two runs differ"
+    for t in (0, 3, 7):
+        one = run_gpu(L, x8[t:t + 1], w, want_routing=False)["out"]
+        assert np.array_equal(one[0], a[t]), f"token {t} alone differs from its batch of 8"
+
+
+def test_zero_gates_and_linearity_with_given_routing():
+    w = small(shared=0, T=9)
+    L = layer(w)
+    x = to_dev_bf16(gen.x_tokens(w, 9))
+    rng = np.random.default_rng(5)
+    idx_np = np.stack([rng.choice(w.E, w.k, replace=False) for _ in range(9)]).astype(np.int32)
+    idx = torch.from_numpy(idx_np).cuda()
+    out = torch.full((9, w.H), float("nan"), device="cuda")
+    L.forward_routed(x, idx, torch.zeros((9, w.k), device="cuda"), out)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+    g1 = torch.rand((9, w.k), device="cuda")
+    g2 = torch.rand((9, w.k), device="cuda")
+    o1, o2, o12 = (torch.empty((9, w.H), device="cuda") for _ in range(3))
+    L.forward_routed(x, idx, g1, o1)
+    L.forward_routed(x, idx, g2, o2)
+    L.forward_routed(x, idx, g1 + g2, o12)
+    torch.cuda.synchronize()
+    assert torch.allclose(o12, o1 + o2, rtol=1e-5, atol=1e-7)
+    # and against the oracle with the same given routing
+    ol = oracle.layer_for_workload(w, sorted(set(idx_np.ravel().tolist())))
+    ref = ol.combine(gen.x_tokens(w, 9), idx_np, g1.cpu().numpy())
+    got = o1.cpu().numpy()
+    rel = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert np.all(rel <= 2e-3)
+
+
+def test_forward_host_matches_device_forward():
+    w = gen.get_workload(0)
+    L = layer(w)
+    x_np = gen.x_tokens(w)
+    dev = run_gpu(L, x_np, w, want_routing=False)["out"]
+    xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+    oh = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
+    L.forward_host(xh, oh)
+    assert np.array_equal(oh.numpy(), dev)
+
+
+def test_error_paths():
+    w = gen.get_workload(0)
+    L = moe.MoeLayer(w.fmt, w.H, w.I, w.E, w.k, w.shared)
+    x = to_dev_bf16(gen.x_tokens(w))
+    out = torch.empty((w.T, w.H), device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        L.forward(x, out)  # no workspace yet
+    assert e.value.code == moe.ESTATE
+    L.reserve(2)
+    with pytest.raises(moe.MoeError) as e:
+        L.forward(x, out)  # router not set
+    assert e.value.code == moe.ESTATE
+    L.set_router(gen.router_weights(w))
+    with pytest.raises(moe.MoeError) as e:
+        L.forward(x, out)  # T = 4 > T_max = 2
+    assert e.value.code == moe.ESTATE and "T_max" in str(e.value)
+    with pytest.raises(moe.MoeError) as e:
+        moe.check(moe.lib().moe_forward(L.h, x.data_ptr() + 2, 1, out.data_ptr(), None))
+    assert e.value.code == moe.EINVAL
+    bad = torch.full((1, w.k), 99, dtype=torch.int32, device="cuda")
+    L.forward_routed(x[:1], bad, torch.ones((1, w.k), device="cuda"), out[:1])
+    assert L.status(reset=True) == moe.EINVAL  # the device bounds check caught the expert id
+    assert L.status() == 0
+    L.close()

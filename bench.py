@@ -140,62 +140,73 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
-def oracle_baseline(w, seconds, n_tok=8):
-    """The oracle as it stands on n_tok decode tokens of the workload (its weights
-    quantised by the oracle beforehand, not timed); repeated for ~`seconds`."""
+def _oracle_setup(w, n_tok=4):
     import gen
     import oracle
+    oracle.build()
+    gen.build(device=False)
     x = gen.x_tokens(w, n_tok)
     base = oracle.Layer(w.fmt, w.H, w.I, w.E, w.k, w.shared, gen.router_weights(w),
                         gen.router_bias(w))
     idx, _ = base.topk(base.logits(x))
-    need = sorted(set(idx.ravel().tolist()) | {w.E})
-    L = oracle.layer_for_workload(w, need)
-    threads = min(n_tok, os.cpu_count() or 1)
+    need = sorted(set(idx.ravel().tolist()) | ({w.E} if w.shared else set()))
+    return x, idx, oracle.layer_for_workload(w, need)
+
+
+def oracle_baseline(w, seconds):
+    """The oracle as it stands: whole-layer forwards of single decode tokens (its
+    weights quantised by the oracle beforehand, not timed), for ~`seconds`.
+    A T=1 forward runs on one thread (the oracle threads over tokens)."""
+    x, _, L = _oracle_setup(w)
     t0 = time.perf_counter()
     reps = 0
     while True:
-        L.forward(x, threads=threads)
+        L.forward(x[reps % len(x): reps % len(x) + 1], threads=1)
         reps += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": reps * n_tok / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n_tok} decode tokens of {w.name} x {reps} repetitions "
-                      f"({dt:.1f} s; oracle threaded over tokens, fp64)"}, dt / reps / n_tok
+    return {"value": reps / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} single-token forwards of {w.name} ({dt:.1f} s, fp64, 1 thread)"}
 
 
 def run_reference(args, w):
+    """Reference arm: the CPU oracle (there is no other implementation of this
+    path).  A step is one bounded slice of the workload: one (token, expert)
+    SwiGLU FFN; a token-layer costs (k + shared) slices plus one router pass,
+    which is timed during warm-up and folded into the rate."""
     rank, _, world = dist_env()
     if rank != 0:
         return
-    import oracle
-    import gen
-    oracle.build()
-    gen.build(device=False)
-    n_tok = 8
-    x = gen.x_tokens(w, n_tok)
-    base = oracle.Layer(w.fmt, w.H, w.I, w.E, w.k, w.shared, gen.router_weights(w),
-                        gen.router_bias(w))
-    idx, _ = base.topk(base.logits(x))
-    L = oracle.layer_for_workload(w, sorted(set(idx.ravel().tolist()) | {w.E}))
-    threads = min(n_tok, os.cpu_count() or 1)
-    for _ in range(args.warmup):
-        L.forward(x, threads=threads)
+    x, idx, L = _oracle_setup(w)
+    n_slices = w.k + w.shared
+    experts = [(t, int(idx[t, j]) if j < w.k else w.E) for t in range(len(x)) for j in range(n_slices)]
+    tr = []
+    for i in range(max(3, args.warmup)):
+        t0 = time.perf_counter()
+        L.logits(x[i % len(x): i % len(x) + 1])
+        tr.append(time.perf_counter() - t0)
+    t_router = statistics.median(tr)
+    for i in range(args.warmup):
+        t, e = experts[i % len(experts)]
+        L.expert_ffn(e, x[t:t + 1])
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        L.forward(x, threads=threads)
+    for i in range(args.steps):
+        t, e = experts[i % len(experts)]
+        L.expert_ffn(e, x[t:t + 1])
     dt = time.perf_counter() - t0
-    value = args.steps * n_tok / dt
+    t_step = dt / args.steps
+    value = 1.0 / (n_slices * t_step + t_router)
+    sample = (f"{args.steps} (token, expert) SwiGLU slices of {w.name}; token-layer = "
+              f"{n_slices} slices + router ({t_router * 1e3:.2f} ms); fp64, 1 thread")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator)",
-            "config": config_block(w, 1, {"reference": "CPU oracle (no reference implementation "
-                                                       "exists for this path)",
-                                          "tokens_per_step": n_tok}),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"{n_tok} decode tokens per step, {args.steps} steps"},
+            "config": config_block(w, 1, {"reference": "CPU oracle (the pages hold no runnable "
+                                                       "implementation of this path)"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -250,8 +261,18 @@ def run_ours(args, w):
     with torch.cuda.graph(g, stream=s):
         for L, o in zip(layers, outs):
             L.forward(x, o, stream=s)
-    for _ in range(args.warmup):
+    ref_outs = [o.clone() for o in outs]
+    with torch.cuda.stream(s):
+        for o in outs:
+            o.zero_()
         g.replay()
+    s.synchronize()
+    for o, r in zip(outs, ref_outs):
+        if not torch.equal(o, r):
+            raise RuntimeError("graph replay differs from the eager forward")
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            g.replay()
     s.synchronize()
 
     uuid = None
@@ -267,10 +288,11 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(s)
-    for _ in range(args.steps):
-        g.replay()
-    ev1.record(s)
+    with torch.cuda.stream(s):  # replay() launches on the current stream
+        ev0.record(s)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(s)
     torch.cuda.synchronize()
     clocks.stop()
     if world > 1:
@@ -297,15 +319,15 @@ def run_ours(args, w):
     with torch.cuda.graph(gk, stream=s):
         for L, o in zip(layers, outs):
             L.run_phase(2, x, o, stream=s)
-    for _ in range(5):
-        gk.replay()
     reps = max(20, min(500, args.steps))
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.synchronize()
-    k0.record(s)
-    for _ in range(reps):
-        gk.replay()
-    k1.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(5):
+            gk.replay()
+        k0.record(s)
+        for _ in range(reps):
+            gk.replay()
+        k1.record(s)
     torch.cuda.synchronize()
     k_us = k0.elapsed_time(k1) * 1e3 / (reps * Ln)
     bytes_launch = sum(per_launch_bytes) / len(per_launch_bytes)
@@ -349,7 +371,7 @@ def run_ours(args, w):
             "roofline": roofline, "e2e": e2e, "gpu_launches": 5 * Ln * args.steps,
             "clocks": clocks.summary()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"], _ = oracle_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = oracle_baseline(w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     for L in layers:

@@ -171,6 +171,33 @@ int moe_debug_routing(moe_layer* L, float* logits, int32_t* idx, float* gates, i
 int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float* out,
                         void* stream);
 
+/* ------------------------------------------------------------------ no device allocation */
+
+/* Router logits, top-k and gates for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this entry point.  It is for code
+ * whose GPU memory belongs to someone else's allocator: a serving runtime that
+ * plans all of HBM at start-up and hands memory out only from its own pool, or
+ * a plug-in inside such a runtime.  For them a cudaMalloc could fail when HBM
+ * is full, or would go around the pool's accounting.
+ * It computes what moe_forward's routing step computes, with the same kernels:
+ *   logits [T x E] fp32 = x [T x H] (bf16 bits) . wr [E x H]^T (bf16 bits) + bias [E]
+ *   (bias may be NULL), idx [T x k] the top-k experts per token (ties to the
+ *   lower index) and gates [T x k] their renormalised softmax.
+ * All pointers are device pointers the caller owns; x and wr are 16-byte
+ * aligned; H % 64 == 0, 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ * It allocates nothing.  Its only scratch, the router's K-split partial sums,
+ * is a fixed 4 MiB device array inside the library, held by every GPU that
+ * loads the library until the process exits.  Inputs that would need more
+ * (ksplit(T, E) * T * E > 2^20 floats; always fine when T * E <= 131072) are
+ * rejected with MOE_EINVAL.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) and sets the router kernels'
+ * shared-memory limit; make that first call before any stream capture.  All
+ * calls share the one array and it keeps the last call's contents: calls that
+ * may overlap on the GPU (different streams, or several host threads) race on
+ * it and must be serialised by the caller.  Asynchronous on `stream`. */
+int moe_route_noalloc(const uint16_t* x, int T, int H, const uint16_t* wr, const float* bias,
+                      int E, int k, float* logits, int32_t* idx, float* gates, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,7 @@ CSRC = os.path.join(_HERE, "csrc")
 BUILD = os.path.join(_HERE, "_build")
 LIB = os.path.join(_HERE, "libmoe_gb300.so")
 HEADER = os.path.join(_ROOT, "include", "moe.h")
-SOURCES = ["layer.cu", "quant_pack.cu", "route.cu", "expert.cu"]
+SOURCES = ["layer.cu", "quant_pack.cu", "route.cu", "expert.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-cudart", "shared"]
 
@@ -36,7 +36,7 @@ EXPORTS = [
     "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
     "moe_pack_weights", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
-    "moe_debug_run_phase",
+    "moe_debug_run_phase", "moe_route_noalloc",
 ]
 
 _lock = threading.Lock()
@@ -111,6 +111,7 @@ def lib():
                 "moe_debug_dequant": (I, [P, I, I, P, P]),
                 "moe_debug_routing": (I, [P, P, P, P, P, P, P, P]),
                 "moe_debug_run_phase": (I, [P, I, P, I, P, P]),
+                "moe_route_noalloc": (I, [P, I, I, P, P, I, I, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -231,3 +232,11 @@ def quantize_nvfp4(W, codes, scales, tscale, stream=None):
 def quantize_fp6(W, codes, exps, stream=None):
     rows, K = W.shape
     check(lib().moe_quantize_fp6(_ptr(W), rows, K, _ptr(codes), _ptr(exps), _stream(stream)))
+
+
+def route_noalloc(x, wr, bias, E, k, logits, idx, gates, stream=None):
+    """Router logits + top-k with no device allocation (see moe_route_noalloc):
+    x [T x H] and wr [E x H] bf16 bits, bias [E] fp32 or None, outputs on the device."""
+    T, H = x.shape
+    check(lib().moe_route_noalloc(_ptr(x), T, H, _ptr(wr), _ptr(bias), E, k, _ptr(logits),
+                                  _ptr(idx), _ptr(gates), _stream(stream)))

@@ -64,6 +64,20 @@ int max_routed_entries(int T, int E, int k) {
 
 }  // namespace
 
+namespace moe {
+// Records the message of a failure for moe_last_error(); used by entry points
+// implemented in other translation units.
+int record_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+}  // namespace moe
+
 struct moe_layer {
   int device = 0;
   int fmt = 0, H = 0, I = 0, E = 0, k = 0, shared = 0;

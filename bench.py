@@ -368,7 +368,7 @@ def run_ours(args, w):
             "data": "synthetic (seeded generator; random-init weights quantised on the device)",
             "config": config_block(w, Ln, {"us_per_layer": ms * 1e3 / (args.steps * Ln),
                                            "parallelism": f"replicas x{world}"}),
-            "roofline": roofline, "e2e": e2e, "gpu_launches": 5 * Ln * args.steps,
+            "roofline": roofline, "e2e": e2e, "gpu_launches": layers[0].launches(T) * Ln * args.steps,
             "clocks": clocks.summary()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, args.cpu_seconds)

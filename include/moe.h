@@ -79,6 +79,9 @@ const char* moe_last_error(void);
  * reset != 0.  Returns MOE_OK, or an error if the read itself failed. */
 int moe_layer_status(moe_layer* L, int reset, int* status);
 
+/* Number of kernels one moe_forward of T tokens launches (>= 0), or an error. */
+int moe_forward_launches(moe_layer* L, int T);
+
 /* Bytes of the packed arena and of one packed expert (gate + up + down, without
  * its three fp32 tensor scales). */
 int moe_layer_info(moe_layer* L, uint64_t* arena_bytes, uint64_t* expert_bytes);
@@ -166,8 +169,10 @@ int moe_debug_routing(moe_layer* L, float* logits, int32_t* idx, float* gates, i
                       int32_t* offsets, int32_t* perm, void* stream);
 
 /* Re-run one phase of the last moe_forward on the same arguments, for timing a
- * kernel on its own: 0 router logits, 1 top-k + dispatch, 2 gate/up + SwiGLU,
- * 3 down, 4 combine.  The workspace must hold that forward's state (same x, T). */
+ * kernel on its own: 0 routing (router logits; for T <= 8 also top-k and
+ * dispatch, fused), 1 top-k + dispatch (nothing for T <= 8), 2 gate/up + SwiGLU,
+ * 3 down (down + combine, fused, when the few-token path runs), 4 combine
+ * (nothing when fused).  The workspace must hold that forward's state (same x, T). */
 int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float* out,
                         void* stream);
 

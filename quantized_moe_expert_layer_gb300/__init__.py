@@ -36,7 +36,7 @@ EXPORTS = [
     "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
     "moe_pack_weights", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
-    "moe_debug_run_phase", "moe_route_noalloc",
+    "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches",
 ]
 
 _lock = threading.Lock()
@@ -112,6 +112,7 @@ def lib():
                 "moe_debug_routing": (I, [P, P, P, P, P, P, P, P]),
                 "moe_debug_run_phase": (I, [P, I, P, I, P, P]),
                 "moe_route_noalloc": (I, [P, I, I, P, P, I, I, P, P, P, P]),
+                "moe_forward_launches": (I, [P, I]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -166,6 +167,10 @@ class MoeLayer:
 
     def reserve(self, T_max):
         check(lib().moe_layer_reserve(self.h, T_max))
+
+    def launches(self, T):
+        """Kernels one forward of T tokens launches."""
+        return check(lib().moe_forward_launches(self.h, T))
 
     def info(self):
         a, e = ctypes.c_uint64(), ctypes.c_uint64()

@@ -166,6 +166,27 @@ __device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], cons
   }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// Ask L2 for every 16-byte vector this lane will read from one tile's
+// super-chunks s0, s0+ds, ... (fire and forget: no registers, no waiting).
+__device__ __forceinline__ void prefetch_tile(int fmt, const uint8_t* tile, const MatGeom& g,
+                                              int s0, int ds) {
+  const int lane = threadIdx.x & 31;
+  for (int s = s0; s < g.nsc; s += ds) {
+    const uint8_t* b = tile + (size_t)s * g.sc_bytes;
+    const int u = sc_units(g, s);
+    if (fmt == FMT_NVFP4) {
+      for (int j = 0; j <= u; ++j) prefetch_l2(b + 512 * j + 16 * lane);
+    } else {
+      prefetch_l2(b + 4 * lane);
+      for (int j = 0; j < 3 * u; ++j) prefetch_l2(b + 128 + 512 * j + 16 * lane);
+    }
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void tiles_mma(int fmt, const uint8_t* const (&tile)[NT],
                                           const MatGeom& g, int s0, int ds, const uint16_t* xs,
@@ -221,9 +242,13 @@ __device__ __forceinline__ void reduce_ksplit(float* red, float (&v)[NV], int tp
 
 // ---------------------------------------------------------------- gate/up + SwiGLU
 __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tpc) {
-  griddep_launch();
   const int y = blockIdx.y;
+  // Shared-expert entries need no routing.  Routed ones wait for it, and only
+  // then let the next kernel start: once every CTA here has triggered, the
+  // routing outputs (work entries) are complete and the next kernel may read
+  // them before its own wait.
   if (y >= p.nsh) griddep_wait();
+  griddep_launch();
   int expert, row, n;
   if (!get_entry(p, y, expert, row, n)) return;
   const int S = p.T * p.k;
@@ -231,6 +256,16 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tp
   extern __shared__ uint4 smem_u4[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
   float* red = reinterpret_cast<float*>(xs + min(kTokTile, p.T) * stride);
+  {
+    const int warp = threadIdx.x >> 5, pair = blockIdx.x * tpc + (warp % tpc);
+    if (pair < p.I / 16) {
+      const MatGeom g = mat_geom(p.fmt, H);
+      const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
+      for (int m = 0; m < 2; ++m)
+        prefetch_tile(p.fmt, eb + (size_t)(2 * pair + m) * p.gu_tile_bytes, g, warp / tpc,
+                      kWarps / tpc);
+    }
+  }
   for (int i = threadIdx.x; i < n * (H / 8); i += kThreads) {
     const int c = i / (H / 8), v = i % (H / 8);
     const int tok = (expert == p.E) ? row - S + c : p.row_token[row + c];
@@ -325,20 +360,91 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertParams p, const floa
        i += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / H4), h = (int)(i % H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < p.k; ++j) {
-      const float gj = gates[(size_t)t * p.k + j];
-      const float4 yv = y4[(size_t)inv[(size_t)t * p.k + j] * H4 + h];
-      acc.x = fmaf(gj, yv.x, acc.x);
-      acc.y = fmaf(gj, yv.y, acc.y);
-      acc.z = fmaf(gj, yv.z, acc.z);
-      acc.w = fmaf(gj, yv.w, acc.w);
-    }
+    float gs[kMaxK];
+    int rows[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < p.k) {
+        gs[j] = gates[(size_t)t * p.k + j];
+        rows[j] = inv[(size_t)t * p.k + j];
+      }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < p.k) {
+        const float4 yv = y4[(size_t)rows[j] * H4 + h];
+        acc.x = fmaf(gs[j], yv.x, acc.x);
+        acc.y = fmaf(gs[j], yv.y, acc.y);
+        acc.z = fmaf(gs[j], yv.z, acc.z);
+        acc.w = fmaf(gs[j], yv.w, acc.w);
+      }
     if (p.shared) {
       const float4 yv = y4[(size_t)(S + t) * H4 + h];
       acc.x += yv.x; acc.y += yv.y; acc.z += yv.z; acc.w += yv.w;
     }
     reinterpret_cast<float4*>(out)[i] = acc;
   }
+}
+
+// ---------------------------------------------------------------- down + combine for a few tokens
+// CTA = one 16-row tile of H for every work entry of the forward; y of all rows
+// stays in shared memory and the CTA writes out[:, tile] = sum_j g_j y_j + y_s
+// with the same j-ordered fmaf chain as combine_kernel (so both paths agree bit
+// for bit).  The tile's weights are known once routing is done, so they are
+// requested from L2 before waiting for gate/up.
+constexpr int kDcThreads = 256;
+
+__global__ void __launch_bounds__(kDcThreads) down_combine_kernel(ExpertParams p, const float* gates,
+                                                                  const int* inv, float* out) {
+  const int tile = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = lane >> 2, t = lane & 3;
+  const int S = p.T * p.k, rows_total = S + (p.shared ? p.T : 0);
+  const int I = p.I, stride = I + 8;
+  const MatGeom g = mat_geom(p.fmt, I);
+  // routing is complete here (gate/up triggered this launch only after its wait)
+  const int n_entries = p.nsh + *p.n_entries;
+  const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
+  for (int y = warp; y < n_entries; y += kDcThreads / 32) {
+    const int expert = (y < p.nsh) ? p.E : p.entries[y - p.nsh].x;
+    if (expert >= 0 && expert <= p.E)
+      prefetch_tile(p.fmt, tile_base + (size_t)expert * p.expert_bytes, g, 0, 1);
+  }
+  griddep_wait();  // gate/up complete: abuf holds every row
+  extern __shared__ uint4 smem_u4[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
+  float* ys = reinterpret_cast<float*>(xs + (size_t)rows_total * stride);
+  for (int i = threadIdx.x; i < rows_total * (I / 8); i += kDcThreads) {
+    const int r = i / (I / 8), v = i % (I / 8);
+    *reinterpret_cast<uint4*>(xs + (size_t)r * stride + 8 * v) =
+        *reinterpret_cast<const uint4*>(p.abuf + (size_t)r * I + 8 * v);
+  }
+  __syncthreads();
+  for (int y = warp; y < n_entries; y += kDcThreads / 32) {
+    int expert, row, n;
+    if (!get_entry(p, y, expert, row, n)) continue;
+    const uint8_t* const tiles[1] = {tile_base + (size_t)expert * p.expert_bytes};
+    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    tiles_mma<1>(p.fmt, tiles, g, 0, 1, xs + (size_t)row * stride, stride, gi < n, acc);
+    const float ts = p.tscale[expert * 3 + 2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+      if (col < n) ys[(row + col) * 16 + r] = ts * acc[0][i];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.T * 16; i += kDcThreads) {
+    const int tk = i / 16, h = i % 16;
+    float a = 0.f;
+    for (int j = 0; j < p.k; ++j)
+      a = fmaf(gates[(size_t)tk * p.k + j], ys[inv[(size_t)tk * p.k + j] * 16 + h], a);
+    if (p.shared) a += ys[(S + tk) * 16 + h];
+    out[(size_t)tk * p.H + 16 * tile + h] = a;
+  }
+}
+
+size_t down_combine_smem(int T, int k, int shared, int I) {
+  const size_t rows = (size_t)T * k + (shared ? T : 0);
+  return rows * (I + 8) * 2 + rows * 16 * sizeof(float);
 }
 
 int tiles_per_cta(int nsc) {
@@ -376,7 +482,20 @@ cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int*
   return launch_k(combine_kernel, dim3(blocks), dim3(256), 0, st, pdl, p, gates, inv, out);
 }
 
+bool down_combine_ok(int T, int k, int shared, int I) {
+  return T <= kTokTile && down_combine_smem(T, k, shared, I) <= 100 * 1024;
+}
+
+cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const int* inv,
+                                float* out, bool pdl, cudaStream_t st) {
+  return launch_k(down_combine_kernel, dim3(p.H / 16), dim3(kDcThreads),
+                  down_combine_smem(p.T, p.k, p.shared, p.I), st, pdl, p, gates, inv, out);
+}
+
 cudaError_t expert_kernels_init() {
+  cudaError_t e0 = cudaFuncSetAttribute(down_combine_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e0 != cudaSuccess) return e0;
   cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        200 * 1024);
   if (e != cudaSuccess) return e;

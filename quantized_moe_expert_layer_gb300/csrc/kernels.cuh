@@ -62,6 +62,8 @@ cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stri
 // routing
 int router_ksplit(int T, int H, int E);
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
+bool router_small_ok(int T, int k);
+cudaError_t launch_router_small(const RouteParams& p, int* counter, cudaStream_t st);
 cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st);
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st);
 size_t route_finish_smem(int E);
@@ -72,6 +74,9 @@ cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStrea
 cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st);
 cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int* inv, float* out,
                            bool pdl, cudaStream_t st);
+bool down_combine_ok(int T, int k, int shared, int I);
+cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const int* inv,
+                                float* out, bool pdl, cudaStream_t st);
 cudaError_t expert_kernels_init();
 
 // launch helper: optional programmatic dependent launch on the previous kernel in the stream

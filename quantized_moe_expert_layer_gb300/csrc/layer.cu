@@ -104,6 +104,7 @@ struct moe_layer {
   int* row_token = nullptr;
   int4* entries = nullptr;
   int* n_entries = nullptr;
+  int* route_counter = nullptr;  // ticket counter of the fused small-T router
   uint16_t* abuf = nullptr;
   float* ybuf = nullptr;
   uint16_t* x_stage = nullptr;
@@ -183,21 +184,36 @@ int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
 }
 
 // experts + combine, after routing has filled idx / gates / dispatch
+bool fused_down(moe_layer* L, int T) { return down_combine_ok(T, L->k, L->shared, L->I); }
+
 int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
   CK("gate/up kernel launch", launch_gateup(ep, grid_y, true, st));
+  if (fused_down(L, T)) {
+    CK("down+combine kernel launch", launch_down_combine(ep, L->gates, L->inv, out, true, st));
+    return MOE_OK;
+  }
   CK("down kernel launch", launch_down(ep, grid_y, true, st));
   CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
   return MOE_OK;
 }
 
+// kernels one forward of T tokens launches
+int forward_launches(moe_layer* L, int T) {
+  const int routing = router_small_ok(T, L->k) ? 1 : (T <= 64 ? 2 : 3);
+  return routing + (fused_down(L, T) ? 2 : 3);
+}
+
 int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   RouteParams rp = route_params(L, x, T);
-  CK("router kernel launch", launch_router(rp, st));
-  if (T <= 64) {
+  if (router_small_ok(T, L->k)) {
+    CK("router kernel launch", launch_router_small(rp, L->route_counter, st));
+  } else if (T <= 64) {
+    CK("router kernel launch", launch_router(rp, st));
     CK("top-k/dispatch kernel launch", launch_route_finish(rp, true, true, st));
   } else {
+    CK("router kernel launch", launch_router(rp, st));
     CK("top-k kernel launch", launch_topk(rp, true, st));
     CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
   }
@@ -281,7 +297,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       E * 4, (E + 1) * 4,                // counts, offsets
       S * 4, S * 4,                      // perm, inv
       (S + T_max) * 4,                   // row_token
-      n_entries * 16, 16,                // entries, n_entries
+      n_entries * 16, 16, 16,            // entries, n_entries, route_counter
       (S + T_max) * L->I * 2,            // abuf
       (S + T_max) * L->H * 4,            // ybuf
       (size_t)T_max * L->H * 2,          // x_stage
@@ -301,7 +317,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   }
   L->ws = ws;
   char* p = static_cast<char*>(ws);
-  void* ptrs[16];
+  void* ptrs[20];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = p;
     p += align_up(sizes[i], 256);
@@ -317,10 +333,11 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->row_token = (int*)ptrs[8];
   L->entries = (int4*)ptrs[9];
   L->n_entries = (int*)ptrs[10];
-  L->abuf = (uint16_t*)ptrs[11];
-  L->ybuf = (float*)ptrs[12];
-  L->x_stage = (uint16_t*)ptrs[13];
-  L->out_stage = (float*)ptrs[14];
+  L->route_counter = (int*)ptrs[11];
+  L->abuf = (uint16_t*)ptrs[12];
+  L->ybuf = (float*)ptrs[13];
+  L->x_stage = (uint16_t*)ptrs[14];
+  L->out_stage = (float*)ptrs[15];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   return MOE_OK;
@@ -346,6 +363,11 @@ int moe_layer_status(moe_layer* L, int reset, int* status) {
   CK("moe_layer_status: read", cudaMemcpy(status, L->status, sizeof(int), cudaMemcpyDeviceToHost));
   if (reset) CK("moe_layer_status: reset", cudaMemset(L->status, 0, sizeof(int)));
   return MOE_OK;
+}
+
+int moe_forward_launches(moe_layer* L, int T) {
+  if (!L || T < 1) return fail(MOE_EINVAL, "moe_forward_launches: bad argument");
+  return forward_launches(L, T);
 }
 
 int moe_layer_info(moe_layer* L, uint64_t* arena_bytes, uint64_t* expert_bytes) {
@@ -531,9 +553,16 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
   RouteParams rp = route_params(L, x, T);
   ExpertParams ep = expert_params(L, x, T);
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
+  const bool small = router_small_ok(T, L->k), fused = fused_down(L, T);
   switch (phase) {
-    case 0: CK("router", launch_router(rp, st)); break;
+    case 0:
+      if (small)
+        CK("router", launch_router_small(rp, L->route_counter, st));
+      else
+        CK("router", launch_router(rp, st));
+      break;
     case 1:
+      if (small) break;
       if (T <= 64) {
         CK("top-k/dispatch", launch_route_finish(rp, true, false, st));
       } else {
@@ -542,8 +571,15 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       }
       break;
     case 2: CK("gate/up", launch_gateup(ep, grid_y, false, st)); break;
-    case 3: CK("down", launch_down(ep, grid_y, false, st)); break;
-    case 4: CK("combine", launch_combine(ep, L->gates, L->inv, out, false, st)); break;
+    case 3:
+      if (fused)
+        CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, st));
+      else
+        CK("down", launch_down(ep, grid_y, false, st));
+      break;
+    case 4:
+      if (!fused) CK("combine", launch_combine(ep, L->gates, L->inv, out, false, st));
+      break;
     default: return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
   }
   return MOE_OK;

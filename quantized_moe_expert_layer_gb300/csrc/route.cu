@@ -26,18 +26,28 @@ constexpr int kFinishThreads = 1024;
 // the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
 // (ksplit slice, token, expert) partial sum goes to p.partial; the top-k step
 // adds the slices in a fixed order.
-__global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
-  griddep_launch();
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+__device__ __forceinline__ void router_partials(const RouteParams& p, uint4* smem_u4) {
   const int tile = blockIdx.x, t0 = blockIdx.y * kTokTile, ks = blockIdx.z;
   const int n = min(kTokTile, p.T - t0);
   const int C = p.H / 64;
   const int c_begin = C * ks / p.ksplit, c_end = C * (ks + 1) / p.ksplit;
   const int kbase = c_begin * 64, klen = (c_end - c_begin) * 64;
   const int stride = klen + 8;  // +16 bytes per row: conflict-free 16-byte reads
-  extern __shared__ uint4 smem_u4[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
   float* red = reinterpret_cast<float*>(xs + kTokTile * stride);
-
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int e0 = 16 * tile + gi, e1 = e0 + 8;
+  const uint16_t* r0 = p.wr + (size_t)min(e0, p.E - 1) * p.H;
+  const uint16_t* r1 = p.wr + (size_t)min(e1, p.E - 1) * p.H;
+  // start the router-weight reads before the activations are staged
+  for (int c = c_begin + warp; c < c_end; c += 4) {
+    prefetch_l2(r0 + 64 * c + 16 * t);
+    prefetch_l2(r1 + 64 * c + 16 * t);
+  }
   for (int i = threadIdx.x; i < n * (klen / 8); i += blockDim.x) {
     const int r = i / (klen / 8), v = i % (klen / 8);
     *reinterpret_cast<uint4*>(xs + r * stride + 8 * v) =
@@ -45,10 +55,6 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
   }
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
-  const int e0 = 16 * tile + gi, e1 = e0 + 8;
-  const uint16_t* r0 = p.wr + (size_t)min(e0, p.E - 1) * p.H;
-  const uint16_t* r1 = p.wr + (size_t)min(e1, p.E - 1) * p.H;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int c = c_begin + warp; c < c_end; c += 4) {
     const int kc = 64 * c + 16 * t;
@@ -74,17 +80,28 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) red[(warp * 32 + lane) * 4 + i] = acc[i];
   __syncthreads();
-  if (warp != 0) return;
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int w = 0; w < kRouterThreads / 32; ++w)
+  if (warp == 0) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int w = 0; w < kRouterThreads / 32; ++w)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] += red[(w * 32 + lane) * 4 + i];
-  float* out = p.partial + (size_t)ks * p.T * p.E;
+      for (int i = 0; i < 4; ++i) s[i] += red[(w * 32 + lane) * 4 + i];
+    float* out = p.partial + (size_t)ks * p.T * p.E;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = (i < 2) ? e0 : e1, col = 2 * t + (i & 1);
-    if (e < p.E && col < n) out[(size_t)(t0 + col) * p.E + e] = s[i];
+    for (int i = 0; i < 4; ++i) {
+      const int e = (i < 2) ? e0 : e1, col = 2 * t + (i & 1);
+      if (e < p.E && col < n) out[(size_t)(t0 + col) * p.E + e] = s[i];
+    }
   }
+}
+
+// grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); 4 warps split
+// the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
+// (ksplit slice, token, expert) partial sum goes to p.partial; the top-k step
+// adds the slices in a fixed order.
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
+  griddep_launch();
+  extern __shared__ uint4 smem_u4[];
+  router_partials(p, smem_u4);
 }
 
 // ---------------------------------------------------------------- top-k (one warp per token)
@@ -92,15 +109,24 @@ __device__ void topk_token(const RouteParams& p, int t, int lane) {
   const int E = p.E, k = p.k;
   float v[kMaxE / 32];
 #pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) v[i] = 0.f;
+  // slices in a fixed order; within a slice every expert's load is independent
+  for (int s = 0; s < p.ksplit; ++s) {
+    const float* ps = p.partial + ((size_t)s * p.T + t) * E;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i)
+      if (lane + 32 * i < E) v[i] += ps[lane + 32 * i];
+  }
+#pragma unroll
   for (int i = 0; i < kMaxE / 32; ++i) {
     const int e = lane + 32 * i;
-    v[i] = -INFINITY;
     if (e < E) {
-      float l = 0.f;
-      for (int s = 0; s < p.ksplit; ++s) l += p.partial[((size_t)s * p.T + t) * E + e];
+      float l = v[i];
       if (p.bias) l = l + p.bias[e];
       p.logits[(size_t)t * E + e] = l;
       v[i] = l;
+    } else {
+      v[i] = -INFINITY;
     }
   }
   uint32_t taken = 0;
@@ -242,6 +268,79 @@ __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
   if (tid == 0) *p.n_entries = n_total;
 }
 
+// Dispatch for a few slots (T*k <= kSmallSlots) by any block size: the same
+// result as dispatch_block (expert-major, stable), with a per-expert count
+// table and a direct stable rank.  smem: 64 + E + S ints.
+constexpr int kSmallSlots = 256;
+
+__device__ void dispatch_small(const RouteParams& p, int* smem) {
+  const int S = p.T * p.k, E = p.E, nt = blockDim.x, tid = threadIdx.x;
+  int* sc = smem;
+  int* cnt = smem + 64;
+  int* sidx = cnt + E;
+  for (int e = tid; e < E; e += nt) cnt[e] = 0;
+  for (int s = tid; s < S; s += nt) sidx[s] = checked_expert(p, p.idx[s]);
+  __syncthreads();
+  for (int s = tid; s < S; s += nt) atomicAdd(&cnt[sidx[s]], 1);
+  __syncthreads();
+  const int ept = (E + nt - 1) / nt;
+  const int lo = min(E, tid * ept), hi = min(E, lo + ept);
+  int local = 0, lnch = 0;
+  for (int e = lo; e < hi; ++e) {
+    local += cnt[e];
+    lnch += (cnt[e] + kTokTile - 1) / kTokTile;
+  }
+  int total, n_total;
+  int run = block_excl_scan(local, sc, &total);
+  int runn = block_excl_scan(lnch, sc, &n_total);
+  for (int e = lo; e < hi; ++e) {
+    const int c = cnt[e];
+    p.counts[e] = c;
+    p.offsets[e] = run;
+    for (int i = 0; i * kTokTile < c; ++i)
+      p.entries[runn + i] = make_int4(e, run + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
+    cnt[e] = run;
+    run += c;
+    runn += (c + kTokTile - 1) / kTokTile;
+  }
+  if (tid == 0) {
+    p.offsets[E] = total;
+    *p.n_entries = n_total;
+  }
+  __syncthreads();
+  for (int s = tid; s < S; s += nt) {
+    const int e = sidx[s];
+    int r = 0;
+    for (int q = 0; q < s; ++q) r += (sidx[q] == e);
+    const int pos = cnt[e] + r;
+    p.perm[pos] = s;
+    p.inv[s] = pos;
+    p.row_token[pos] = s / p.k;
+  }
+  for (int t = tid; t < p.T; t += nt) p.row_token[S + t] = t;
+}
+
+// Router for T <= 8: the partial sums as in router_kernel, then the last CTA to
+// finish (a ticket from an atomic counter; nothing waits) does top-k, gates and
+// dispatch, and resets the counter for the next launch.
+__global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouteParams p, int* counter) {
+  griddep_launch();
+  extern __shared__ uint4 smem_u4[];
+  __shared__ int ticket;
+  router_partials(p, smem_u4);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) ticket = atomicAdd(counter, 1);
+  __syncthreads();
+  if (ticket != (int)(gridDim.x * gridDim.y * gridDim.z) - 1) return;
+  __threadfence();
+  for (int t = threadIdx.x >> 5; t < p.T; t += kRouterThreads / 32)
+    topk_token(p, t, threadIdx.x & 31);
+  __syncthreads();
+  dispatch_small(p, reinterpret_cast<int*>(smem_u4));
+  if (threadIdx.x == 0) *counter = 0;
+}
+
 __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParams p, int do_topk) {
   griddep_launch();
   griddep_wait();
@@ -276,6 +375,18 @@ cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
   return launch_k(router_kernel, grid, dim3(kRouterThreads), smem, st, false, p);
 }
 
+bool router_small_ok(int T, int k) { return T <= kTokTile && T * k <= kSmallSlots; }
+
+cudaError_t launch_router_small(const RouteParams& p, int* counter, cudaStream_t st) {
+  const int C = p.H / 64;
+  const int max_klen = ((C + p.ksplit - 1) / p.ksplit) * 64;
+  size_t smem = (size_t)kTokTile * (max_klen + 8) * 2 + kRouterThreads * 4 * sizeof(float);
+  const size_t disp = (size_t)(64 + p.E + p.T * p.k) * sizeof(int);
+  if (disp > smem) smem = disp;
+  dim3 grid((p.E + 15) / 16, 1, p.ksplit);
+  return launch_k(router_small_kernel, grid, dim3(kRouterThreads), smem, st, false, p, counter);
+}
+
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st) {
   return launch_k(topk_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, pdl, p);
 }
@@ -288,6 +399,9 @@ cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cu
 cudaError_t route_kernels_init() {
   cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        200 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           200 * 1024);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)route_finish_smem(kMaxE));

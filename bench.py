@@ -341,6 +341,24 @@ def run_ours(args, w):
                 "peak_source": peak_kind,
                 "timing": "CUDA events over a graph of back-to-back launches, gaps included"}
 
+    # steady-state time of each phase alone (graphs of L back-to-back launches)
+    phase_us = {}
+    for ph, name in [(0, "routing"), (1, "topk_dispatch"), (2, "gate_up"), (3, "down"), (4, "combine")]:
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp, stream=s):
+            for L, o in zip(layers, outs):
+                L.run_phase(ph, x, o, stream=s)
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                gp.replay()
+            p0.record(s)
+            for _ in range(50):
+                gp.replay()
+            p1.record(s)
+        torch.cuda.synchronize()
+        phase_us[name] = p0.elapsed_time(p1) * 1e3 / (50 * Ln)
+
     # e2e: the host-buffer C-ABI call, copies inside the timed region
     xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
     ohs = [torch.empty((T, w.H), dtype=torch.float32).pin_memory() for _ in range(Ln)]
@@ -367,6 +385,7 @@ def run_ours(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (nvfp4 weights)",
             "data": "synthetic (seeded generator; random-init weights quantised on the device)",
             "config": config_block(w, Ln, {"us_per_layer": ms * 1e3 / (args.steps * Ln),
+                                           "phase_us_alone": phase_us,
                                            "parallelism": f"replicas x{world}"}),
             "roofline": roofline, "e2e": e2e, "gpu_launches": layers[0].launches(T) * Ln * args.steps,
             "clocks": clocks.summary()}

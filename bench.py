@@ -46,7 +46,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer instances per step (default 32 for decode, 8 for larger T)")
+    ap.add_argument("--workload", type=int, default=WORKLOAD,
+                    help="workload index (default: the decode workload the metric is quoted on)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -168,6 +171,7 @@ def oracle_baseline(w, seconds):
     dt = time.perf_counter() - t0
     return {"value": reps / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{reps} single-token forwards of {w.name} ({dt:.1f} s, fp64, 1 thread)"}
+
 
 
 def run_reference(args, w):
@@ -402,7 +406,9 @@ def run_ours(args, w):
 def main():
     args = parse()
     import gen
-    w = gen.get_workload(WORKLOAD)
+    w = gen.get_workload(args.workload)
+    if args.layers is None:
+        args.layers = 32 if w.T <= 8 else 8
     if args.impl == "reference":
         run_reference(args, w)
     else:

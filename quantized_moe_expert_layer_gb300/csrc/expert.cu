@@ -32,11 +32,11 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
   return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
 }
 
-// Load the 16 f16 activations of token row `gi` at column `col` (two 16-byte reads).
-__device__ __forceinline__ void load_b(const uint16_t* xs, int stride, int gi, int col, bool have,
-                                       uint32_t (&xw)[8]) {
-  if (have) {
-    const uint4* px = reinterpret_cast<const uint4*>(xs + gi * stride + col);
+// The 16 f16 activations of this lane's token row at column `col` (two
+// 16-byte reads, kept in L1: the warps of a CTA share them), or zeros.
+__device__ __forceinline__ void load_b(const uint16_t* brow, int col, uint32_t (&xw)[8]) {
+  if (brow) {
+    const uint4* px = reinterpret_cast<const uint4*>(brow + col);
     const uint4 q0 = px[0], q1 = px[1];
     xw[0] = q0.x; xw[1] = q0.y; xw[2] = q0.z; xw[3] = q0.w;
     xw[4] = q1.x; xw[5] = q1.y; xw[6] = q1.z; xw[7] = q1.w;
@@ -46,11 +46,12 @@ __device__ __forceinline__ void load_b(const uint16_t* xs, int stride, int gi, i
   }
 }
 
-// NT NVFP4 tiles (same K) times the staged activations; super-chunks s0, s0+ds, ...
+// NT NVFP4 tiles (same K) times the activations; super-chunks s0, s0+ds, ...
+// brow: this lane's B row (f16, K long), null when the lane's column is empty.
 template <int NT>
 __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], const MatGeom& g,
-                                            int s0, int ds, const uint16_t* xs, int stride,
-                                            bool have_b, float (&acc)[NT][4]) {
+                                            int s0, int ds, const uint16_t* brow,
+                                            float (&acc)[NT][4]) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   for (int s = s0; s < g.nsc; s += ds) {
     const int nc = sc_units(g, s);
@@ -67,7 +68,7 @@ __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], co
     for (int j = 0; j < 8; ++j) {
       if (j < nc) {
         uint32_t xw[8];
-        load_b(xs, stride, gi, 64 * (8 * s + j) + 16 * t, have_b, xw);
+        load_b(brow, 64 * (8 * s + j) + 16 * t, xw);
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
           const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
@@ -96,8 +97,8 @@ __device__ __forceinline__ void fp6_unpack(uint32_t Ha, uint32_t Hb, uint32_t L,
 // NT FP6 tiles; pairs (128-column blocks) are loaded four at a time.
 template <int NT>
 __device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], const MatGeom& g,
-                                          int s0, int ds, const uint16_t* xs, int stride,
-                                          bool have_b, float (&acc)[NT][4]) {
+                                          int s0, int ds, const uint16_t* brow,
+                                          float (&acc)[NT][4]) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   for (int s = s0; s < g.nsc; s += ds) {
     const int np = sc_units(g, s);
@@ -127,7 +128,7 @@ __device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], cons
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t xw[8];
-            load_b(xs, stride, gi, 128 * (8 * s + j) + 64 * h + 16 * t, have_b, xw);
+            load_b(brow, 128 * (8 * s + j) + 64 * h + 16 * t, xw);
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
               const uint32_t words[12] = {cv[i][jj][0].x, cv[i][jj][0].y, cv[i][jj][0].z,
@@ -189,12 +190,12 @@ __device__ __forceinline__ void prefetch_tile(int fmt, const uint8_t* tile, cons
 
 template <int NT>
 __device__ __forceinline__ void tiles_mma(int fmt, const uint8_t* const (&tile)[NT],
-                                          const MatGeom& g, int s0, int ds, const uint16_t* xs,
-                                          int stride, bool have_b, float (&acc)[NT][4]) {
+                                          const MatGeom& g, int s0, int ds, const uint16_t* brow,
+                                          float (&acc)[NT][4]) {
   if (fmt == FMT_NVFP4)
-    tiles_nvfp4<NT>(tile, g, s0, ds, xs, stride, have_b, acc);
+    tiles_nvfp4<NT>(tile, g, s0, ds, brow, acc);
   else
-    tiles_fp6<NT>(tile, g, s0, ds, xs, stride, have_b, acc);
+    tiles_fp6<NT>(tile, g, s0, ds, brow, acc);
 }
 
 // Entry y of the launch: the first p.nsh are the shared expert's token groups
@@ -209,8 +210,8 @@ __device__ __forceinline__ bool get_entry(const ExpertParams& p, int y, int& exp
     return true;
   }
   const int r = y - p.nsh;
+  const int4 e = p.entries[r];  // read together with the count (the slot always exists)
   if (r >= *p.n_entries) return false;
-  const int4 e = p.entries[r];
   expert = e.x;
   row = e.y;
   n = e.z;
@@ -251,47 +252,23 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tp
   griddep_launch();
   int expert, row, n;
   if (!get_entry(p, y, expert, row, n)) return;
+  __shared__ float red[kThreads * 8];
   const int S = p.T * p.k;
-  const int H = p.H, stride = H + 8;
-  extern __shared__ uint4 smem_u4[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
-  float* red = reinterpret_cast<float*>(xs + min(kTokTile, p.T) * stride);
-  {
-    const int warp = threadIdx.x >> 5, pair = blockIdx.x * tpc + (warp % tpc);
-    if (pair < p.I / 16) {
-      const MatGeom g = mat_geom(p.fmt, H);
-      const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
-      for (int m = 0; m < 2; ++m)
-        prefetch_tile(p.fmt, eb + (size_t)(2 * pair + m) * p.gu_tile_bytes, g, warp / tpc,
-                      kWarps / tpc);
-    }
-  }
-  for (int i = threadIdx.x; i < n * (H / 8); i += kThreads) {
-    const int c = i / (H / 8), v = i % (H / 8);
-    const int tok = (expert == p.E) ? row - S + c : p.row_token[row + c];
-    const uint4 raw = *reinterpret_cast<const uint4*>(p.x + (size_t)tok * H + 8 * v);
-    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const __half lo = __float2half_rn(__uint_as_float(in[q] << 16));
-      const __half hi = __float2half_rn(__uint_as_float(in[q] & 0xFFFF0000u));
-      o[q] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-    }
-    *reinterpret_cast<uint4*>(xs + c * stride + 8 * v) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  __syncthreads();
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   const int nks = kWarps / tpc;
   const int pair = blockIdx.x * tpc + (warp % tpc), ks = warp / tpc;
   const bool valid = pair < p.I / 16;
-  const MatGeom g = mat_geom(p.fmt, H);
+  const MatGeom g = mat_geom(p.fmt, p.H);
   const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
   const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
                                    eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
+  const uint16_t* brow = nullptr;
+  if (gi < n) {
+    const int tok = (expert == p.E) ? row - S + gi : p.row_token[row + gi];
+    brow = p.xh + (size_t)tok * p.H;
+  }
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  if (valid) tiles_mma<2>(p.fmt, tiles, g, ks, nks, xs, stride, gi < n, acc);
+  if (valid) tiles_mma<2>(p.fmt, tiles, g, ks, nks, brow, acc);
   float v[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -314,29 +291,20 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tp
 
 // ---------------------------------------------------------------- down
 __global__ void __launch_bounds__(kThreads) down_kernel(ExpertParams p, int tpc) {
-  griddep_launch();
   griddep_wait();
   int expert, row, n;
   if (!get_entry(p, blockIdx.y, expert, row, n)) return;
-  const int I = p.I, stride = I + 8;
-  extern __shared__ uint4 smem_u4[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
-  float* red = reinterpret_cast<float*>(xs + min(kTokTile, p.T) * stride);
-  for (int i = threadIdx.x; i < n * (I / 8); i += kThreads) {
-    const int c = i / (I / 8), v = i % (I / 8);
-    *reinterpret_cast<uint4*>(xs + c * stride + 8 * v) =
-        *reinterpret_cast<const uint4*>(p.abuf + (size_t)(row + c) * I + 8 * v);
-  }
-  __syncthreads();
+  __shared__ float red[kThreads * 8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   const int nks = kWarps / tpc;
   const int tile = blockIdx.x * tpc + (warp % tpc), ks = warp / tpc;
   const bool valid = tile < p.H / 16;
-  const MatGeom g = mat_geom(p.fmt, I);
+  const MatGeom g = mat_geom(p.fmt, p.I);
   const uint8_t* const tiles[1] = {p.arena + (size_t)expert * p.expert_bytes + p.gu_bytes +
                                    (size_t)tile * p.dn_tile_bytes};
+  const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
   float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-  if (valid) tiles_mma<1>(p.fmt, tiles, g, ks, nks, xs, stride, gi < n, acc);
+  if (valid) tiles_mma<1>(p.fmt, tiles, g, ks, nks, brow, acc);
   float v[4] = {acc[0][0], acc[0][1], acc[0][2], acc[0][3]};
   reduce_ksplit<4>(red, v, tpc, nks);
   if (ks != 0 || !valid) return;
@@ -386,44 +354,39 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertParams p, const floa
 }
 
 // ---------------------------------------------------------------- down + combine for a few tokens
-// CTA = one 16-row tile of H for every work entry of the forward; y of all rows
-// stays in shared memory and the CTA writes out[:, tile] = sum_j g_j y_j + y_s
-// with the same j-ordered fmaf chain as combine_kernel (so both paths agree bit
-// for bit).  The tile's weights are known once routing is done, so they are
-// requested from L2 before waiting for gate/up.
-constexpr int kDcThreads = 256;
+// CTA = one 16-row tile of H for every work entry of the forward (one warp per
+// entry); y of all rows stays in shared memory and the CTA writes
+// out[:, tile] = sum_j g_j y_j + y_s with the same j-ordered fmaf chain as
+// combine_kernel, so both paths agree bit for bit.  The tile's weights are
+// known once routing is done, so they are requested from L2 before waiting
+// for gate/up.
+constexpr int kDcMaxWarps = 16;
 
-__global__ void __launch_bounds__(kDcThreads) down_combine_kernel(ExpertParams p, const float* gates,
-                                                                  const int* inv, float* out) {
+__global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertParams p,
+                                                                         const float* gates,
+                                                                         const int* inv, float* out) {
   const int tile = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
   const int gi = lane >> 2, t = lane & 3;
   const int S = p.T * p.k, rows_total = S + (p.shared ? p.T : 0);
-  const int I = p.I, stride = I + 8;
-  const MatGeom g = mat_geom(p.fmt, I);
+  const MatGeom g = mat_geom(p.fmt, p.I);
   // routing is complete here (gate/up triggered this launch only after its wait)
   const int n_entries = p.nsh + *p.n_entries;
   const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
-  for (int y = warp; y < n_entries; y += kDcThreads / 32) {
+  for (int y = warp; y < n_entries; y += nw) {
     const int expert = (y < p.nsh) ? p.E : p.entries[y - p.nsh].x;
     if (expert >= 0 && expert <= p.E)
       prefetch_tile(p.fmt, tile_base + (size_t)expert * p.expert_bytes, g, 0, 1);
   }
   griddep_wait();  // gate/up complete: abuf holds every row
-  extern __shared__ uint4 smem_u4[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
-  float* ys = reinterpret_cast<float*>(xs + (size_t)rows_total * stride);
-  for (int i = threadIdx.x; i < rows_total * (I / 8); i += kDcThreads) {
-    const int r = i / (I / 8), v = i % (I / 8);
-    *reinterpret_cast<uint4*>(xs + (size_t)r * stride + 8 * v) =
-        *reinterpret_cast<const uint4*>(p.abuf + (size_t)r * I + 8 * v);
-  }
-  __syncthreads();
-  for (int y = warp; y < n_entries; y += kDcThreads / 32) {
+  extern __shared__ float ys[];  // [rows_total x 16]
+  for (int y = warp; y < n_entries; y += nw) {
     int expert, row, n;
     if (!get_entry(p, y, expert, row, n)) continue;
     const uint8_t* const tiles[1] = {tile_base + (size_t)expert * p.expert_bytes};
+    const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    tiles_mma<1>(p.fmt, tiles, g, 0, 1, xs + (size_t)row * stride, stride, gi < n, acc);
+    tiles_mma<1>(p.fmt, tiles, g, 0, 1, brow, acc);
     const float ts = p.tscale[expert * 3 + 2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -432,7 +395,7 @@ __global__ void __launch_bounds__(kDcThreads) down_combine_kernel(ExpertParams p
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < p.T * 16; i += kDcThreads) {
+  for (int i = threadIdx.x; i < p.T * 16; i += blockDim.x) {
     const int tk = i / 16, h = i % 16;
     float a = 0.f;
     for (int j = 0; j < p.k; ++j)
@@ -440,11 +403,11 @@ __global__ void __launch_bounds__(kDcThreads) down_combine_kernel(ExpertParams p
     if (p.shared) a += ys[(S + tk) * 16 + h];
     out[(size_t)tk * p.H + 16 * tile + h] = a;
   }
+  (void)rows_total;
 }
 
-size_t down_combine_smem(int T, int k, int shared, int I) {
-  const size_t rows = (size_t)T * k + (shared ? T : 0);
-  return rows * (I + 8) * 2 + rows * 16 * sizeof(float);
+size_t down_combine_smem(int T, int k, int shared) {
+  return ((size_t)T * k + (shared ? T : 0)) * 16 * sizeof(float);
 }
 
 int tiles_per_cta(int nsc) {
@@ -454,9 +417,6 @@ int tiles_per_cta(int nsc) {
   return 1;
 }
 
-size_t stage_smem(int T, int K) {
-  return (size_t)(T < kTokTile ? T : kTokTile) * (K + 8) * 2 + (size_t)kThreads * 8 * sizeof(float);
-}
 
 }  // namespace
 
@@ -464,14 +424,14 @@ cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStrea
   const int tpc = tiles_per_cta(mat_geom(p.fmt, p.H).nsc);
   const int pairs = p.I / 16;
   dim3 grid((pairs + tpc - 1) / tpc, grid_y);
-  return launch_k(gateup_kernel, grid, dim3(kThreads), stage_smem(p.T, p.H), st, pdl, p, tpc);
+  return launch_k(gateup_kernel, grid, dim3(kThreads), 0, st, pdl, p, tpc);
 }
 
 cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
   const int tpc = tiles_per_cta(mat_geom(p.fmt, p.I).nsc);
   const int tiles = p.H / 16;
   dim3 grid((tiles + tpc - 1) / tpc, grid_y);
-  return launch_k(down_kernel, grid, dim3(kThreads), stage_smem(p.T, p.I), st, pdl, p, tpc);
+  return launch_k(down_kernel, grid, dim3(kThreads), 0, st, pdl, p, tpc);
 }
 
 cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int* inv, float* out,
@@ -483,23 +443,19 @@ cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int*
 }
 
 bool down_combine_ok(int T, int k, int shared, int I) {
-  return T <= kTokTile && down_combine_smem(T, k, shared, I) <= 100 * 1024;
+  (void)I;
+  return T <= kTokTile && down_combine_smem(T, k, shared) <= 48 * 1024;
 }
 
 cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const int* inv,
                                 float* out, bool pdl, cudaStream_t st) {
-  return launch_k(down_combine_kernel, dim3(p.H / 16), dim3(kDcThreads),
-                  down_combine_smem(p.T, p.k, p.shared, p.I), st, pdl, p, gates, inv, out);
+  // one warp per work entry (the routed entries are at most T*k for T <= 8)
+  int warps = p.nsh + (p.T * p.k < p.E ? p.T * p.k : p.E);
+  if (warps > kDcMaxWarps) warps = kDcMaxWarps;
+  return launch_k(down_combine_kernel, dim3(p.H / 16), dim3(32 * warps),
+                  down_combine_smem(p.T, p.k, p.shared), st, pdl, p, gates, inv, out);
 }
 
-cudaError_t expert_kernels_init() {
-  cudaError_t e0 = cudaFuncSetAttribute(down_combine_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-  if (e0 != cudaSuccess) return e0;
-  cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       200 * 1024);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-}
+cudaError_t expert_kernels_init() { return cudaSuccess; }
 
 }  // namespace moe

@@ -9,6 +9,7 @@
 namespace moe {
 
 constexpr int kTokTile = 8;     // tokens per expert entry (the n of m16n8k16)
+constexpr int kTcMaxN = 256;    // tokens per entry of the tensor-core path
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 
@@ -21,10 +22,14 @@ struct ExpertParams {
   const float* tscale;   // [(E + shared) * 3]
   int fmt, H, I, E, T, k, shared;
   int nsh;               // leading shared-expert entries: ceil(T / 8) or 0
+  int nsh_tc;            // leading shared-expert entries of the tensor-core path: ceil(T / 256)
+  const int4* tc_entries;  // routed entries of up to kTcMaxN tokens
+  const int* n_tc_entries;
   const int4* entries;   // routed entries {expert, first row, tokens, 0}
   const int* n_entries;  // number of routed entries
   const int* row_token;  // [T*k + T] token of each row of abuf / ybuf
   const uint16_t* x;     // bf16 [T x H]
+  const uint16_t* xh;    // f16 copy of x [T x H] (written by the router)
   uint16_t* abuf;        // f16 bits [(T*k + T) x I]: silu(g) * u per row
   float* ybuf;           // [(T*k + T) x H]: ts_down * (W_down a) per row
   int* status;
@@ -32,6 +37,7 @@ struct ExpertParams {
 
 struct RouteParams {
   const uint16_t* x;      // bf16 [T x H]
+  uint16_t* xh;           // f16 copy of x, written by the router (may be null)
   const uint16_t* wr;     // bf16 [E x H]
   const float* bias;      // [E] or null
   int T, H, E, k, shared, ksplit;
@@ -46,6 +52,8 @@ struct RouteParams {
   int* row_token;         // [T*k + T]
   int4* entries;
   int* n_entries;
+  int4* tc_entries;       // optional: entries of up to kTcMaxN tokens (tensor-core path)
+  int* n_tc_entries;
   int* status;
 };
 
@@ -78,6 +86,14 @@ bool down_combine_ok(int T, int k, int shared, int I);
 cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const int* inv,
                                 float* out, bool pdl, cudaStream_t st);
 cudaError_t expert_kernels_init();
+cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream_t st);
+
+// tensor-core (tcgen05) prefill path
+bool tc_path_ok(int fmt, int T, int k, int E, int H, int I);
+int max_tc_entries(int T, int E, int k);
+cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, cudaStream_t st);
+cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, cudaStream_t st);
+cudaError_t tc_kernels_init();
 
 // launch helper: optional programmatic dependent launch on the previous kernel in the stream
 template <typename... KArgs, typename... Args>

@@ -105,6 +105,9 @@ struct moe_layer {
   int4* entries = nullptr;
   int* n_entries = nullptr;
   int* route_counter = nullptr;  // ticket counter of the fused small-T router
+  int4* tc_entries = nullptr;    // entries of up to 256 tokens (tensor-core path)
+  int* n_tc_entries = nullptr;
+  uint16_t* xh = nullptr;        // f16 copy of x
   uint16_t* abuf = nullptr;
   float* ybuf = nullptr;
   uint16_t* x_stage = nullptr;
@@ -137,6 +140,10 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.row_token = L->row_token;
   p.entries = L->entries;
   p.n_entries = L->n_entries;
+  p.xh = L->xh;
+  const bool tc = tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I);
+  p.tc_entries = tc ? L->tc_entries : nullptr;
+  p.n_tc_entries = tc ? L->n_tc_entries : nullptr;
   p.status = L->status;
   return p;
 }
@@ -157,6 +164,10 @@ ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
   p.k = L->k;
   p.shared = L->shared;
   p.nsh = L->shared ? (T + kTokTile - 1) / kTokTile : 0;
+  p.nsh_tc = L->shared ? (T + kTcMaxN - 1) / kTcMaxN : 0;
+  p.tc_entries = L->tc_entries;
+  p.n_tc_entries = L->n_tc_entries;
+  p.xh = L->xh;
   p.entries = L->entries;
   p.n_entries = L->n_entries;
   p.row_token = L->row_token;
@@ -186,8 +197,17 @@ int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
 // experts + combine, after routing has filled idx / gates / dispatch
 bool fused_down(moe_layer* L, int T) { return down_combine_ok(T, L->k, L->shared, L->I); }
 
+bool tc_path(moe_layer* L, int T) { return tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I); }
+
 int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
+  if (tc_path(L, T)) {
+    const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
+    CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, st));
+    CK("tensor-core down kernel launch", launch_tc_down(ep, gy, st));
+    CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
+    return MOE_OK;
+  }
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
   CK("gate/up kernel launch", launch_gateup(ep, grid_y, true, st));
   if (fused_down(L, T)) {
@@ -202,6 +222,7 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
   const int routing = router_small_ok(T, L->k) ? 1 : (T <= 64 ? 2 : 3);
+  if (tc_path(L, T)) return routing + 3;
   return routing + (fused_down(L, T) ? 2 : 3);
 }
 
@@ -252,6 +273,7 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = route_kernels_init();
   if (e == cudaSuccess) e = expert_kernels_init();
+  if (e == cudaSuccess) e = tc_kernels_init();
   if (e != cudaSuccess) {
     delete L;
     return cuda_fail("moe_layer_create: device set-up", e);
@@ -298,6 +320,8 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       S * 4, S * 4,                      // perm, inv
       (S + T_max) * 4,                   // row_token
       n_entries * 16, 16, 16,            // entries, n_entries, route_counter
+      (size_t)max_tc_entries(T_max, L->E, L->k) * 16, 16,  // tc_entries, n_tc_entries
+      (size_t)T_max * L->H * 2,          // xh
       (S + T_max) * L->I * 2,            // abuf
       (S + T_max) * L->H * 4,            // ybuf
       (size_t)T_max * L->H * 2,          // x_stage
@@ -317,7 +341,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   }
   L->ws = ws;
   char* p = static_cast<char*>(ws);
-  void* ptrs[20];
+  void* ptrs[24];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = p;
     p += align_up(sizes[i], 256);
@@ -334,10 +358,13 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->entries = (int4*)ptrs[9];
   L->n_entries = (int*)ptrs[10];
   L->route_counter = (int*)ptrs[11];
-  L->abuf = (uint16_t*)ptrs[12];
-  L->ybuf = (float*)ptrs[13];
-  L->x_stage = (uint16_t*)ptrs[14];
-  L->out_stage = (float*)ptrs[15];
+  L->tc_entries = (int4*)ptrs[12];
+  L->n_tc_entries = (int*)ptrs[13];
+  L->xh = (uint16_t*)ptrs[14];
+  L->abuf = (uint16_t*)ptrs[15];
+  L->ybuf = (float*)ptrs[16];
+  L->x_stage = (uint16_t*)ptrs[17];
+  L->out_stage = (float*)ptrs[18];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   return MOE_OK;
@@ -499,6 +526,7 @@ int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* id
   CK("moe_forward_routed: copy idx", cudaMemcpyAsync(L->idx, idx, S * 4, cudaMemcpyDeviceToDevice, st));
   CK("moe_forward_routed: copy gates",
      cudaMemcpyAsync(L->gates, gates, S * 4, cudaMemcpyDeviceToDevice, st));
+  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, st));
   RouteParams rp = route_params(L, x, T);
   CK("dispatch kernel launch", launch_route_finish(rp, false, false, st));
   L->last_T = T;
@@ -570,9 +598,16 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
         CK("dispatch", launch_route_finish(rp, false, false, st));
       }
       break;
-    case 2: CK("gate/up", launch_gateup(ep, grid_y, false, st)); break;
+    case 2:
+      if (tc_path(L, T))
+        CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
+      else
+        CK("gate/up", launch_gateup(ep, grid_y, false, st));
+      break;
     case 3:
-      if (fused)
+      if (tc_path(L, T))
+        CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
+      else if (fused)
         CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, st));
       else
         CK("down", launch_down(ep, grid_y, false, st));

@@ -48,10 +48,23 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, uint4* sme
     prefetch_l2(r0 + 64 * c + 16 * t);
     prefetch_l2(r1 + 64 * c + 16 * t);
   }
+  const bool write_xh = p.xh != nullptr && tile == 0;
   for (int i = threadIdx.x; i < n * (klen / 8); i += blockDim.x) {
     const int r = i / (klen / 8), v = i % (klen / 8);
-    *reinterpret_cast<uint4*>(xs + r * stride + 8 * v) =
-        *reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + r) * p.H + kbase + 8 * v);
+    const size_t off = (size_t)(t0 + r) * p.H + kbase + 8 * v;
+    const uint4 raw = *reinterpret_cast<const uint4*>(p.x + off);
+    *reinterpret_cast<uint4*>(xs + r * stride + 8 * v) = raw;
+    if (write_xh) {  // the f16 copy the expert kernels read (exact for |x| in f16's normal range)
+      const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16),
+                                            __uint_as_float(in[q] & 0xFFFF0000u));
+        o[q] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(p.xh + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
   __syncthreads();
 
@@ -105,59 +118,78 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
 }
 
 // ---------------------------------------------------------------- top-k (one warp per token)
-__device__ void topk_token(const RouteParams& p, int t, int lane) {
+// Order-preserving map of an fp32 value to a uint32 key (larger value, larger key).
+__device__ __forceinline__ uint32_t f32_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_f32(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Logits of token t (sum of the router's K-split slices in order, + bias), then
+// k rounds of arg-max (largest logit, ties to the lower expert index), then the
+// softmax of the k selected logits.  Each round: a tree over the lane's values,
+// then one warp max of the value keys and one warp min of the expert ids that
+// hold it.  sidx (optional, shared memory) receives the indices too.
+__device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx) {
   const int E = p.E, k = p.k;
-  float v[kMaxE / 32];
+  constexpr int V = kMaxE / 32;
+  float v[V];
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) v[i] = 0.f;
+  for (int i = 0; i < V; ++i) v[i] = 0.f;
   // slices in a fixed order; within a slice every expert's load is independent
   for (int s = 0; s < p.ksplit; ++s) {
     const float* ps = p.partial + ((size_t)s * p.T + t) * E;
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i)
+    for (int i = 0; i < V; ++i)
       if (lane + 32 * i < E) v[i] += ps[lane + 32 * i];
   }
+  uint32_t key[V];
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
+  for (int i = 0; i < V; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
       float l = v[i];
       if (p.bias) l = l + p.bias[e];
       p.logits[(size_t)t * E + e] = l;
-      v[i] = l;
+      key[i] = f32_key(l);
     } else {
-      v[i] = -INFINITY;
+      key[i] = 0u;  // below every real key
     }
   }
-  uint32_t taken = 0;
-  float my_v = 0.f;
+  uint32_t my_key = 0;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
+    // tree over the lane's slots: keep the larger key, ties to the lower slot
+    uint32_t bk[V / 2];
+    int bs[V / 2];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
-      }
+    for (int i = 0; i < V / 2; ++i) {
+      const bool second = key[2 * i + 1] > key[2 * i];
+      bk[i] = second ? key[2 * i + 1] : key[2 * i];
+      bs[i] = second ? 2 * i + 1 : 2 * i;
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
+    for (int w = V / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const bool second = bk[i + w] > bk[i];
+        bk[i] = second ? bk[i + w] : bk[i];
+        bs[i] = second ? bs[i + w] : bs[i];
       }
-    }
-    if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const uint32_t best = __reduce_max_sync(0xffffffffu, bk[0]);
+    const uint32_t cand = (bk[0] == best) ? (uint32_t)(lane + 32 * bs[0]) : 0xFFFFFFFFu;
+    const int win = (int)__reduce_min_sync(0xffffffffu, cand);
+    const bool own = (win & 31) == lane;
+#pragma unroll
+    for (int i = 0; i < V; ++i) key[i] = (own && i == (win >> 5)) ? 0u : key[i];  // taken
     if (lane == j) {
-      my_v = bv;
-      my_i = bi;
+      my_key = best;
+      my_i = win;
     }
   }
+  const float my_v = key_f32(my_key);
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
   float ex = (lane < k) ? expf(my_v - top) : 0.f;
   float sum = ex;
@@ -166,6 +198,7 @@ __device__ void topk_token(const RouteParams& p, int t, int lane) {
   if (lane < k) {
     p.idx[(size_t)t * k + lane] = my_i;
     p.gates[(size_t)t * k + lane] = ex / sum;
+    if (sidx) sidx[t * k + lane] = my_i;
   }
 }
 
@@ -173,7 +206,7 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
   griddep_launch();
   griddep_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t < p.T) topk_token(p, t, threadIdx.x & 31);
+  if (t < p.T) topk_token(p, t, threadIdx.x & 31, nullptr);
 }
 
 // ---------------------------------------------------------------- dispatch (one CTA of 1024 threads)
@@ -266,6 +299,15 @@ __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
       p.entries[ebase + i] = make_int4(tid, off + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
   }
   if (tid == 0) *p.n_entries = n_total;
+  if (p.tc_entries) {
+    const int ntc = (tid < E) ? (c + kTcMaxN - 1) / kTcMaxN : 0;
+    int tc_total;
+    const int tbase = block_excl_scan(ntc, sc, &tc_total);
+    if (tid < E)
+      for (int i = 0; i < ntc; ++i)
+        p.tc_entries[tbase + i] = make_int4(tid, excl + kTcMaxN * i, min(kTcMaxN, c - kTcMaxN * i), 0);
+    if (tid == 0) *p.n_tc_entries = tc_total;
+  }
 }
 
 // Dispatch for a few slots (T*k <= kSmallSlots) by any block size: the same
@@ -273,13 +315,13 @@ __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
 // table and a direct stable rank.  smem: 64 + E + S ints.
 constexpr int kSmallSlots = 256;
 
-__device__ void dispatch_small(const RouteParams& p, int* smem) {
+// sidx: the S expert ids in shared memory (already written and synchronised)
+__device__ void dispatch_small(const RouteParams& p, int* smem, int* sidx) {
   const int S = p.T * p.k, E = p.E, nt = blockDim.x, tid = threadIdx.x;
   int* sc = smem;
   int* cnt = smem + 64;
-  int* sidx = cnt + E;
   for (int e = tid; e < E; e += nt) cnt[e] = 0;
-  for (int s = tid; s < S; s += nt) sidx[s] = checked_expert(p, p.idx[s]);
+  for (int s = tid; s < S; s += nt) sidx[s] = checked_expert(p, sidx[s]);
   __syncthreads();
   for (int s = tid; s < S; s += nt) atomicAdd(&cnt[sidx[s]], 1);
   __syncthreads();
@@ -327,17 +369,18 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouteParam
   griddep_launch();
   extern __shared__ uint4 smem_u4[];
   __shared__ int ticket;
+  __shared__ int sidx[kSmallSlots];
   router_partials(p, smem_u4);
-  __threadfence();
+  if (threadIdx.x < 32) __threadfence();  // warp 0 wrote this CTA's partial sums
   __syncthreads();
   if (threadIdx.x == 0) ticket = atomicAdd(counter, 1);
   __syncthreads();
   if (ticket != (int)(gridDim.x * gridDim.y * gridDim.z) - 1) return;
   __threadfence();
   for (int t = threadIdx.x >> 5; t < p.T; t += kRouterThreads / 32)
-    topk_token(p, t, threadIdx.x & 31);
+    topk_token(p, t, threadIdx.x & 31, sidx);
   __syncthreads();
-  dispatch_small(p, reinterpret_cast<int*>(smem_u4));
+  dispatch_small(p, reinterpret_cast<int*>(smem_u4), sidx);
   if (threadIdx.x == 0) *counter = 0;
 }
 
@@ -347,13 +390,37 @@ __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParam
   extern __shared__ int smem_i[];
   if (do_topk) {
     for (int t = threadIdx.x >> 5; t < p.T; t += kFinishThreads / 32)
-      topk_token(p, t, threadIdx.x & 31);
+      topk_token(p, t, threadIdx.x & 31, nullptr);
     __syncthreads();
   }
   dispatch_block(p, smem_i + 64, smem_i);
 }
 
+__global__ void convert_x_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xh, long n8) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long)gridDim.x * blockDim.x) {
+    const uint4 raw = reinterpret_cast<const uint4*>(x)[i];
+    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16),
+                                          __uint_as_float(in[q] & 0xFFFF0000u));
+      o[q] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    reinterpret_cast<uint4*>(xh)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream_t st) {
+  const long n8 = n / 8;
+  long blocks = (n8 + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  convert_x_kernel<<<(int)blocks, 256, 0, st>>>(x, xh, n8);
+  return cudaGetLastError();
+}
 
 int router_ksplit(int T, int H, int E) {
   const int tiles = (E + 15) / 16, groups = (T + kTokTile - 1) / kTokTile;
@@ -381,7 +448,7 @@ cudaError_t launch_router_small(const RouteParams& p, int* counter, cudaStream_t
   const int C = p.H / 64;
   const int max_klen = ((C + p.ksplit - 1) / p.ksplit) * 64;
   size_t smem = (size_t)kTokTile * (max_klen + 8) * 2 + kRouterThreads * 4 * sizeof(float);
-  const size_t disp = (size_t)(64 + p.E + p.T * p.k) * sizeof(int);
+  const size_t disp = (size_t)(64 + p.E) * sizeof(int);
   if (disp > smem) smem = disp;
   dim3 grid((p.E + 15) / 16, 1, p.ksplit);
   return launch_k(router_small_kernel, grid, dim3(kRouterThreads), smem, st, false, p, counter);

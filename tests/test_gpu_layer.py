@@ -57,6 +57,17 @@ def test_small_layers_ragged_token_counts(fmt, T):
     compare_layer(w, layer(w), gen.x_tokens(w, T))
 
 
+@pytest.mark.parametrize("T", [128, 300, 700])
+def test_tensor_core_path_small_layer(T):
+    """Enough tokens per expert for the tcgen05 grouped GEMMs (T*k >= 16 E): ragged
+    per-expert counts (N from 1 to ~250, padded to 16), several shared-expert
+    work items of up to 256 tokens."""
+    w = small(fmt=1, H=256, I=128, E=8, k=2, T=T, seed=5)
+    L = layer(w)
+    assert L.launches(T) == 6  # router, top-k, dispatch, tc gate/up, tc down, combine
+    compare_layer(w, L, gen.x_tokens(w, T))
+
+
 def test_decode_nvfp4_full_size():
     w = gen.get_workload(1)
     rel, ties = compare_layer(w, layer(w), gen.x_tokens(w))

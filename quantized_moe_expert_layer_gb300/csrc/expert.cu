@@ -34,12 +34,23 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
 
 // The 16 f16 activations of this lane's token row at column `col` (two
 // 16-byte reads, kept in L1: the warps of a CTA share them), or zeros.
-__device__ __forceinline__ void load_b(const uint16_t* brow, int col, uint32_t (&xw)[8]) {
+// A bf16 source row (b_bf16) is converted to f16 in registers: the shared
+// expert's CTAs start before the router has written the f16 copy of x.
+__device__ __forceinline__ void load_b(const uint16_t* brow, int col, bool b_bf16,
+                                       uint32_t (&xw)[8]) {
   if (brow) {
     const uint4* px = reinterpret_cast<const uint4*>(brow + col);
     const uint4 q0 = px[0], q1 = px[1];
     xw[0] = q0.x; xw[1] = q0.y; xw[2] = q0.z; xw[3] = q0.w;
     xw[4] = q1.x; xw[5] = q1.y; xw[6] = q1.z; xw[7] = q1.w;
+    if (b_bf16) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(xw[i] << 16),
+                                            __uint_as_float(xw[i] & 0xFFFF0000u));
+        xw[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) xw[i] = 0u;
@@ -50,7 +61,7 @@ __device__ __forceinline__ void load_b(const uint16_t* brow, int col, uint32_t (
 // brow: this lane's B row (f16, K long), null when the lane's column is empty.
 template <int NT>
 __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], const MatGeom& g,
-                                            int s0, int ds, const uint16_t* brow,
+                                            int s0, int ds, const uint16_t* brow, bool b_bf16,
                                             float (&acc)[NT][4]) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   for (int s = s0; s < g.nsc; s += ds) {
@@ -68,7 +79,7 @@ __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], co
     for (int j = 0; j < 8; ++j) {
       if (j < nc) {
         uint32_t xw[8];
-        load_b(brow, 64 * (8 * s + j) + 16 * t, xw);
+        load_b(brow, 64 * (8 * s + j) + 16 * t, b_bf16, xw);
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
           const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
@@ -97,7 +108,7 @@ __device__ __forceinline__ void fp6_unpack(uint32_t Ha, uint32_t Hb, uint32_t L,
 // NT FP6 tiles; pairs (128-column blocks) are loaded four at a time.
 template <int NT>
 __device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], const MatGeom& g,
-                                          int s0, int ds, const uint16_t* brow,
+                                          int s0, int ds, const uint16_t* brow, bool b_bf16,
                                           float (&acc)[NT][4]) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   for (int s = s0; s < g.nsc; s += ds) {
@@ -128,7 +139,7 @@ __device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], cons
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t xw[8];
-            load_b(brow, 128 * (8 * s + j) + 64 * h + 16 * t, xw);
+            load_b(brow, 128 * (8 * s + j) + 64 * h + 16 * t, b_bf16, xw);
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
               const uint32_t words[12] = {cv[i][jj][0].x, cv[i][jj][0].y, cv[i][jj][0].z,
@@ -191,11 +202,11 @@ __device__ __forceinline__ void prefetch_tile(int fmt, const uint8_t* tile, cons
 template <int NT>
 __device__ __forceinline__ void tiles_mma(int fmt, const uint8_t* const (&tile)[NT],
                                           const MatGeom& g, int s0, int ds, const uint16_t* brow,
-                                          float (&acc)[NT][4]) {
+                                          bool b_bf16, float (&acc)[NT][4]) {
   if (fmt == FMT_NVFP4)
-    tiles_nvfp4<NT>(tile, g, s0, ds, brow, acc);
+    tiles_nvfp4<NT>(tile, g, s0, ds, brow, b_bf16, acc);
   else
-    tiles_fp6<NT>(tile, g, s0, ds, brow, acc);
+    tiles_fp6<NT>(tile, g, s0, ds, brow, b_bf16, acc);
 }
 
 // Entry y of the launch: the first p.nsh are the shared expert's token groups
@@ -262,13 +273,16 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tp
   const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
   const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
                                    eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
+  // routed entries read the router's f16 copy of x; the shared expert's
+  // entries run ahead of the router and read (and convert) x itself
+  const bool shared_entry = expert == p.E;
   const uint16_t* brow = nullptr;
   if (gi < n) {
-    const int tok = (expert == p.E) ? row - S + gi : p.row_token[row + gi];
-    brow = p.xh + (size_t)tok * p.H;
+    const int tok = shared_entry ? row - S + gi : p.row_token[row + gi];
+    brow = (shared_entry ? p.x : p.xh) + (size_t)tok * p.H;
   }
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  if (valid) tiles_mma<2>(p.fmt, tiles, g, ks, nks, brow, acc);
+  if (valid) tiles_mma<2>(p.fmt, tiles, g, ks, nks, brow, shared_entry, acc);
   float v[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertParams p, int tpc)
                                    (size_t)tile * p.dn_tile_bytes};
   const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
   float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-  if (valid) tiles_mma<1>(p.fmt, tiles, g, ks, nks, brow, acc);
+  if (valid) tiles_mma<1>(p.fmt, tiles, g, ks, nks, brow, false, acc);
   float v[4] = {acc[0][0], acc[0][1], acc[0][2], acc[0][3]};
   reduce_ksplit<4>(red, v, tpc, nks);
   if (ks != 0 || !valid) return;
@@ -386,7 +400,7 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
     const uint8_t* const tiles[1] = {tile_base + (size_t)expert * p.expert_bytes};
     const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    tiles_mma<1>(p.fmt, tiles, g, 0, 1, brow, acc);
+    tiles_mma<1>(p.fmt, tiles, g, 0, 1, brow, false, acc);
     const float ts = p.tscale[expert * 3 + 2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

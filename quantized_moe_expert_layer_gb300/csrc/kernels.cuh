@@ -9,7 +9,7 @@
 namespace moe {
 
 constexpr int kTokTile = 8;     // tokens per expert entry (the n of m16n8k16)
-constexpr int kTcMaxN = 256;    // tokens per entry of the tensor-core path
+constexpr int kTcMaxN = 128;    // tokens per entry of the tensor-core path
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 

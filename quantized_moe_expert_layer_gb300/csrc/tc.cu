@@ -1,7 +1,7 @@
 // Prefill path: grouped expert GEMMs on the 5th-generation tensor cores
 // (tcgen05 kind::f16, fp32 accumulators in tensor memory).
 //
-// Per work item (expert e, 128-row block of W, up to 256 tokens routed to e):
+// Per work item (expert e, 128-row block of W, up to 128 tokens routed to e):
 //   D[128 x N] (TMEM, fp32) = sum over K of A[128 x 64] . B[N x 64]^T
 // A = the weights, dequantised exactly to f16 (e2m1 code * e4m3 block scale is
 // an f16) by four producer warps from the packed NVFP4 tiles and written to
@@ -26,14 +26,16 @@
 namespace moe {
 namespace {
 
-constexpr int kTcM = 128;          // rows of W per work item
-constexpr int kTcK = 64;           // K per pipeline stage (one packed chunk)
-constexpr int kTcStages = 4;
-constexpr int kTcProducers = 128;  // warps 0-3: producers, then epilogue
-constexpr int kTcThreads = 160;    // + warp 4: TMEM allocation and MMA issue
-constexpr int kTcAStageBytes = kTcM * kTcK * 2;      // 16 KB
-constexpr int kTcBStageBytes = kTcMaxN * kTcK * 2;   // 32 KB
-constexpr long long kWaitBudget = 2000000000LL;       // ~1 s of clock64 per wait
+constexpr int kTcM = 128;            // rows of W per work item
+constexpr int kTcK = 64;             // K per pipeline stage (one packed chunk)
+constexpr int kTcStages = 6;
+constexpr int kTcLookahead = kTcStages - 1;  // chunks whose copies are in flight
+constexpr int kTcProducers = 256;    // warps 0-7: producers, then epilogue
+constexpr int kTcThreads = 288;      // + warp 8: TMEM allocation and MMA issue
+constexpr int kTcAStageBytes = kTcM * kTcK * 2;     // 16 KB of dequantised f16 weights
+constexpr int kTcRawStageBytes = 8 * 512;           // 4 KB of packed codes (8 tiles)
+constexpr int kTcBStageBytes = kTcMaxN * kTcK * 2;  // 16 KB of f16 token rows
+constexpr long long kWaitBudget = 2000000000LL;      // ~1 s of clock64 per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -145,6 +147,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 struct TcShared {
   uint64_t full[kTcStages];
   uint64_t empty[kTcStages];
@@ -178,26 +192,35 @@ __device__ __forceinline__ bool tc_entry(const ExpertParams& p, int y, int& expe
 
 // The shared skeleton of both GEMMs.  MODE 0: gate/up + SwiGLU -> abuf;
 // MODE 1: down -> ybuf.
+//
+// Producer thread u (of 256) owns packed vector u of each chunk: tile u/32,
+// lane u%32 of the 16-row tile layout, i.e. rows 16*(u/32) + (u%32)/4 (+8) and
+// 16 columns.  Chunk c's raw codes and token rows are copied with cp.async
+// kTcLookahead chunks ahead; at chunk c the thread waits for its own copies,
+// dequantises its vector into the swizzled A stage, fences the async proxy and
+// arrives on full[c % stages].
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) {
   griddep_wait();
   int expert, row0, n;
   if (!tc_entry(p, blockIdx.y, expert, row0, n)) return;
   extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
-  // stage buffers at a 1024-byte aligned base
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
   const int n_pad = (n + 15) & ~15;
-  const int b_stage = n_pad * kTcK * 2;
+  const int b_stage = n_pad * kTcK * 2;  // multiple of 2 KB: stages stay 1024-byte aligned
   uint8_t* A = base;
-  uint8_t* B = base + kTcStages * kTcAStageBytes;
-  TcShared* sh = reinterpret_cast<TcShared*>(B + kTcStages * kTcBStageBytes);
+  uint8_t* B = A + kTcStages * kTcAStageBytes;
+  uint8_t* RAW = B + kTcStages * kTcBStageBytes;
+  TcShared* sh = reinterpret_cast<TcShared*>(RAW + kTcStages * kTcRawStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.T * p.k;
   const int K = MODE == 0 ? p.H : p.I;
   const int KC = K / kTcK;
   const int mb = blockIdx.x;
-  const uint32_t ncols = n_pad <= 32 ? 32 : (n_pad <= 64 ? 64 : (n_pad <= 128 ? 128 : 256));
+  const uint32_t ncols = n_pad <= 32 ? 32 : (n_pad <= 64 ? 64 : 128);
+  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
+  const MatGeom g = mat_geom(FMT_NVFP4, K);
 
   if (tid == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -213,77 +236,86 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
     if (i < n) tk = (MODE == 0) ? ((expert == p.E) ? row0 - S + i : p.row_token[row0 + i]) : row0 + i;
     sh->tok[i] = tk;  // MODE 0: token index into x; MODE 1: row of abuf
   }
-  if (warp == 4) tmem_alloc(&sh->tmem_base, ncols);
+  // token-row padding stays zero in every stage (cp.async never writes it)
+  for (int i = tid; i < kTcStages * (n_pad - n) * 8; i += kTcThreads) {
+    const int st = i / ((n_pad - n) * 8), rem = i % ((n_pad - n) * 8);
+    const int r = n + rem / 8, c16 = rem % 8;
+    *reinterpret_cast<uint4*>(B + st * b_stage + swz(r, c16)) = make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 8) tmem_alloc(&sh->tmem_base, ncols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_d = sh->tmem_base;
   volatile int* abort = &sh->abort;
 
-  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
-  const MatGeom g = mat_geom(FMT_NVFP4, K);
-  if (warp < 4) {
+  if (warp < 8) {
     // ---------------------------------------------------------------- producers
-    const uint32_t a_s = smem_u32(A), b_s = smem_u32(B);
-    uint4 sv[2];
-    for (int c = 0; c < KC; ++c) {
-      const int stage = c % kTcStages;
-      if (!mbar_wait(&sh->empty[stage], ((c / kTcStages) & 1) ^ 1, abort)) break;
-      const int s = c >> 3, j = c & 7;
-      // A: 8 tiles x 32 lanes of packed vectors; thread takes two of them
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int u = tid + h * kTcProducers, ti = u >> 5, ln = u & 31;
-        const int gi = ln >> 2, t = ln & 3;
-        const uint8_t* tile = (MODE == 0)
-                                  ? eb + (size_t)(8 * mb + ti) * p.gu_tile_bytes
-                                  : eb + p.gu_bytes + (size_t)(8 * mb + ti) * p.dn_tile_bytes;
-        const uint8_t* sc = tile + (size_t)s * g.sc_bytes;
-        if (j == 0) sv[h] = ldg_stream(sc + 16 * ln);
-        const uint4 cv = ldg_stream(sc + 512 * (1 + j) + 16 * ln);
-        const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[h], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
-        const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
-        uint32_t r0[8], r1[8];  // rows gi and gi+8: 16 f16 each
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t hh[4];
-          e2m1x8_to_f16x8(u4get(cv, w), hh);
-          r0[2 * w] = hmul2(hh[0], s_lo);
-          r0[2 * w + 1] = hmul2(hh[2], s_lo);
-          r1[2 * w] = hmul2(hh[1], s_hi);
-          r1[2 * w + 1] = hmul2(hh[3], s_hi);
-        }
-        const int ra = 16 * ti + gi, rb = ra + 8;
-        const uint32_t as = a_s + stage * kTcAStageBytes;
-        st_shared_v4(as + swz(ra, 2 * t), r0[0], r0[1], r0[2], r0[3]);
-        st_shared_v4(as + swz(ra, 2 * t + 1), r0[4], r0[5], r0[6], r0[7]);
-        st_shared_v4(as + swz(rb, 2 * t), r1[0], r1[1], r1[2], r1[3]);
-        st_shared_v4(as + swz(rb, 2 * t + 1), r1[4], r1[5], r1[6], r1[7]);
-      }
-      // B: n_pad rows x 8 chunks of 16 bytes
+    const int u = tid, ti = u >> 5, ln = u & 31, gi = ln >> 2, t = ln & 3;
+    const uint8_t* tile = (MODE == 0) ? eb + (size_t)(8 * mb + ti) * p.gu_tile_bytes
+                                      : eb + p.gu_bytes + (size_t)(8 * mb + ti) * p.dn_tile_bytes;
+    const uint16_t* bsrc = (MODE == 0) ? p.xh : p.abuf;
+    const int bld = (MODE == 0) ? p.H : p.I;
+    // ask L2 for everything this CTA will read
+    for (int s = 0; s < g.nsc; ++s)
+      for (int j = 0; j <= sc_units(g, s); ++j) prefetch_l2(tile + (size_t)s * g.sc_bytes + 512 * j + 16 * ln);
+    for (int i = tid; i < n * (K / 64); i += kTcProducers)
+      prefetch_l2(bsrc + (size_t)sh->tok[i / (K / 64)] * bld + 64 * (i % (K / 64)));
+    const uint32_t a_s = smem_u32(A), b_s = smem_u32(B), raw_s = smem_u32(RAW);
+    auto issue = [&](int c) {  // chunk c's copies into stage c % stages
+      const int stage = c % kTcStages, s = c >> 3, j = c & 7;
+      cp_async16(raw_s + stage * kTcRawStageBytes + 16 * u,
+                 tile + (size_t)s * g.sc_bytes + 512 * (1 + j) + 16 * ln);
       const uint32_t bs = b_s + stage * b_stage;
-      for (int v = tid; v < n_pad * 8; v += kTcProducers) {
+      for (int v = tid; v < n * 8; v += kTcProducers) {
         const int r = v >> 3, c16 = v & 7;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < n) {
-          if (MODE == 0) {
-            val = *reinterpret_cast<const uint4*>(p.xh + (size_t)sh->tok[r] * p.H + c * kTcK +
-                                                  8 * c16);
-          } else {
-            val = *reinterpret_cast<const uint4*>(p.abuf + (size_t)sh->tok[r] * p.I + c * kTcK +
-                                                  8 * c16);
-          }
-        }
-        st_shared_v4(bs + swz(r, c16), val.x, val.y, val.z, val.w);
+        cp_async16(bs + swz(r, c16), bsrc + (size_t)sh->tok[r] * bld + c * kTcK + 8 * c16);
       }
+    };
+    for (int c = 0; c < kTcLookahead; ++c) {
+      if (c < KC) issue(c);
+      cp_async_commit();
+    }
+    uint4 sv = ldg_stream(tile + 16 * ln), sv_next = sv;
+    for (int c = 0; c < KC; ++c) {
+      const int stage = c % kTcStages, s = c >> 3, j = c & 7;
+      if (j == 0 && c > 0) sv = sv_next;
+      if (j == 4 && s + 1 < g.nsc) sv_next = ldg_stream(tile + (size_t)(s + 1) * g.sc_bytes + 16 * ln);
+      cp_async_wait<kTcLookahead - 1>();  // this thread's copies of chunk c have landed
+      const uint4 cv = *reinterpret_cast<const uint4*>(RAW + stage * kTcRawStageBytes + 16 * u);
+      const uint32_t sp = e4m3x2_to_f16x2((u4get(sv, j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
+      const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
+      uint32_t r0[8], r1[8];  // rows gi and gi+8 of tile ti: 16 f16 each
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t hh[4];
+        e2m1x8_to_f16x8(u4get(cv, w), hh);
+        r0[2 * w] = hmul2(hh[0], s_lo);
+        r0[2 * w + 1] = hmul2(hh[2], s_lo);
+        r1[2 * w] = hmul2(hh[1], s_hi);
+        r1[2 * w + 1] = hmul2(hh[3], s_hi);
+      }
+      const int ra = 16 * ti + gi, rb = ra + 8;
+      const uint32_t as = a_s + stage * kTcAStageBytes;
+      st_shared_v4(as + swz(ra, 2 * t), r0[0], r0[1], r0[2], r0[3]);
+      st_shared_v4(as + swz(ra, 2 * t + 1), r0[4], r0[5], r0[6], r0[7]);
+      st_shared_v4(as + swz(rb, 2 * t), r1[0], r1[1], r1[2], r1[3]);
+      st_shared_v4(as + swz(rb, 2 * t + 1), r1[4], r1[5], r1[6], r1[7]);
       fence_async_smem();
       mbar_arrive(&sh->full[stage]);
+      // refill: chunk c + lookahead goes to the stage the MMAs of chunk c - 1 free
+      const int cn = c + kTcLookahead;
+      if (cn < KC) {
+        if (!mbar_wait(&sh->empty[cn % kTcStages], ((cn / kTcStages) & 1) ^ 1, abort)) break;
+        issue(cn);
+      }
+      cp_async_commit();
     }
+    cp_async_wait<0>();
   } else if (lane == 0) {
     // ---------------------------------------------------------------- MMA issue
     const uint32_t idesc = idesc_f16(kTcM, n_pad);
     const uint32_t a_s = smem_u32(A), b_s = smem_u32(B);
-    int issued = 0;
     for (int c = 0; c < KC; ++c) {
       const int stage = c % kTcStages;
       if (!mbar_wait(&sh->full[stage], (c / kTcStages) & 1, abort)) break;
@@ -294,9 +326,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
       for (int kk = 0; kk < kTcK / 16; ++kk)  // +32 bytes per 16-column step
         umma_f16(tmem_d, ad + 2 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
       umma_commit(&sh->empty[stage]);
-      ++issued;
     }
-    umma_commit(&sh->acc_full);  // also fires if nothing was issued
+    umma_commit(&sh->acc_full);  // fires once every issued MMA is done
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -308,19 +339,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
     }
   }
   tc_fence_after();
-  if (warp < 4 && ok && !*abort) {
-    const int r = 32 * warp + lane;  // row of the 128-row block, TMEM lane r
+  if (warp < 8 && ok && !*abort) {
+    const int q = warp & 3;              // TMEM lane quadrant of this warp
+    const int r = 32 * q + lane;         // row of the 128-row block
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
     if (MODE == 0) {
-      const int pair = 4 * mb + warp, i = 16 * pair + (lane & 15);
+      const int pair = 4 * mb + q, i = 16 * pair + (lane & 15);
       const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
-      for (int c0 = 0; c0 < n_pad; c0 += 32) {
+      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
         uint32_t v[32];
-        tmem_ld32(tmem_d + ((uint32_t)(32 * warp) << 16) + c0, v);
+        tmem_ld32(tmem_d + lane_addr + c0, v);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const float mine = __uint_as_float(v[q]);
+        for (int qq = 0; qq < 32; ++qq) {
+          const float mine = __uint_as_float(v[qq]);
           const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-          const int col = c0 + q;
+          const int col = c0 + qq;
           if (lane < 16 && col < n) {
             const float G = ts_g * mine, U = ts_u * other;
             const float a = G / (1.0f + expf(-G)) * U;
@@ -331,13 +364,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
     } else {
       const float ts = p.tscale[expert * 3 + 2];
       const int h = kTcM * mb + r;
-      for (int c0 = 0; c0 < n_pad; c0 += 32) {
+      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
         uint32_t v[32];
-        tmem_ld32(tmem_d + ((uint32_t)(32 * warp) << 16) + c0, v);
+        tmem_ld32(tmem_d + lane_addr + c0, v);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int col = c0 + q;
-          if (col < n) p.ybuf[(size_t)(row0 + col) * p.H + h] = ts * __uint_as_float(v[q]);
+        for (int qq = 0; qq < 32; ++qq) {
+          const int col = c0 + qq;
+          if (col < n) p.ybuf[(size_t)(row0 + col) * p.H + h] = ts * __uint_as_float(v[qq]);
         }
       }
     }
@@ -345,14 +378,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
   if (*abort && tid == 0) *p.status = -5;  // MOE_ETIMEOUT
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem_d, ncols);
   }
 }
 
 size_t tc_smem() {
-  return 1024 + (size_t)kTcStages * (kTcAStageBytes + kTcBStageBytes) + sizeof(TcShared);
+  return 1024 + (size_t)kTcStages * (kTcAStageBytes + kTcBStageBytes + kTcRawStageBytes) +
+         sizeof(TcShared);
 }
 
 }  // namespace

@@ -25,7 +25,7 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
@@ -57,32 +57,42 @@ __device__ __forceinline__ void load_b(const uint16_t* brow, int col, bool b_bf1
   }
 }
 
-// NT NVFP4 tiles (same K) times the activations; super-chunks s0, s0+ds, ...
+// Work is split along K in units of 256 columns: 4 NVFP4 chunks of 64 or 2
+// FP6 blocks of 128.  A warp handles units h0, h0 + dh, ...; per unit it keeps
+// all weight vectors and activation fragments in flight before doing the math.
+__host__ __device__ __forceinline__ int n_halves(const MatGeom& g) { return (g.K + 255) / 256; }
+
+// NT NVFP4 tiles (same K) times the activations.
 // brow: this lane's B row (f16, K long), null when the lane's column is empty.
 template <int NT>
 __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], const MatGeom& g,
-                                            int s0, int ds, const uint16_t* brow, bool b_bf16,
+                                            int h0, int dh, const uint16_t* brow, bool b_bf16,
                                             float (&acc)[NT][4]) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
-  for (int s = s0; s < g.nsc; s += ds) {
-    const int nc = sc_units(g, s);
-    uint4 sv[NT], cv[NT][8];
+  const int nh = n_halves(g);
+  for (int hh = h0; hh < nh; hh += dh) {
+    const int s = hh >> 1, jb = (hh & 1) * 4;
+    const int nc = min(4, sc_units(g, s) - jb);
+    uint4 sv[NT], cv[NT][4];
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       const uint8_t* b = tile[i] + (size_t)s * g.sc_bytes + 16 * lane;
       sv[i] = ldg_stream(b);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < nc) cv[i][j] = ldg_stream(b + 512 * (1 + j));
+      for (int j = 0; j < 4; ++j)
+        if (j < nc) cv[i][j] = ldg_stream(b + 512 * (1 + jb + j));
     }
+    uint32_t xb[4][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j)
+      if (j < nc) load_b(brow, 64 * (8 * s + jb + j) + 16 * t, b_bf16, xb[j]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
       if (j < nc) {
-        uint32_t xw[8];
-        load_b(brow, 64 * (8 * s + j) + 16 * t, b_bf16, xw);
+        const int jj = jb + j;  // chunk within the super-chunk
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
-          const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
+          const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], jj >> 1) >> (16 * (jj & 1))) & 0xFFFFu);
           const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
@@ -90,7 +100,7 @@ __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], co
             e2m1x8_to_f16x8(u4get(cv[i][j], w), h);
             const uint32_t a[4] = {hmul2(h[0], s_lo), hmul2(h[1], s_hi), hmul2(h[2], s_lo),
                                    hmul2(h[3], s_hi)};
-            mma_f16(acc[i], a, xw[2 * w], xw[2 * w + 1]);
+            mma_f16(acc[i], a, xb[j][2 * w], xb[j][2 * w + 1]);
           }
         }
       }
@@ -105,73 +115,78 @@ __device__ __forceinline__ void fp6_unpack(uint32_t Ha, uint32_t Hb, uint32_t L,
   c[3] = ((Hb >> 2) & 0x3C3C3C3Cu) | ((L >> 6) & 0x03030303u);
 }
 
-// NT FP6 tiles; pairs (128-column blocks) are loaded four at a time.
+// NT FP6 tiles; a unit is 2 blocks (pairs of 64-column chunks) of 128 columns.
 template <int NT>
 __device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], const MatGeom& g,
-                                          int s0, int ds, const uint16_t* brow, bool b_bf16,
+                                          int h0, int dh, const uint16_t* brow, bool b_bf16,
                                           float (&acc)[NT][4]) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
-  for (int s = s0; s < g.nsc; s += ds) {
+  const int nh = n_halves(g);
+  for (int hh = h0; hh < nh; hh += dh) {
+    const int s = hh >> 2, j0 = (hh & 3) * 2;
     const int np = sc_units(g, s);
     uint32_t ew[NT];
 #pragma unroll
     for (int i = 0; i < NT; ++i) ew[i] = ldg_stream_u32(tile[i] + (size_t)s * g.sc_bytes + 4 * lane);
-    for (int j0 = 0; j0 < np; j0 += 4) {
-      uint4 cv[NT][4][3];
+    uint4 cv[NT][2][3];
 #pragma unroll
-      for (int i = 0; i < NT; ++i)
+    for (int i = 0; i < NT; ++i)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          if (j0 + jj < np)
+      for (int jj = 0; jj < 2; ++jj)
+        if (j0 + jj < np)
 #pragma unroll
-            for (int v = 0; v < 3; ++v)
-              cv[i][jj][v] = ldg_stream(tile[i] + (size_t)s * g.sc_bytes + 128 +
-                                        1536 * (j0 + jj) + 512 * v + 16 * lane);
+          for (int v = 0; v < 3; ++v)
+            cv[i][jj][v] = ldg_stream(tile[i] + (size_t)s * g.sc_bytes + 128 + 1536 * (j0 + jj) +
+                                      512 * v + 16 * lane);
+    uint32_t xb[2][2][8];  // activation fragments of the 2 blocks, both chunks
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        if (j0 + jj < np) {
-          const int j = j0 + jj;
-          float blk[NT][4];
+    for (int jj = 0; jj < 2; ++jj)
+      if (j0 + jj < np)
 #pragma unroll
-          for (int i = 0; i < NT; ++i)
+        for (int h = 0; h < 2; ++h)
+          load_b(brow, 128 * (8 * s + j0 + jj) + 64 * h + 16 * t, b_bf16, xb[jj][h]);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) blk[i][r] = 0.f;
+    for (int jj = 0; jj < 2; ++jj) {
+      if (j0 + jj < np) {
+        const int j = j0 + jj;
+        float blk[NT][4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t xw[8];
-            load_b(brow, 128 * (8 * s + j) + 64 * h + 16 * t, b_bf16, xw);
+        for (int i = 0; i < NT; ++i)
 #pragma unroll
-            for (int i = 0; i < NT; ++i) {
-              const uint32_t words[12] = {cv[i][jj][0].x, cv[i][jj][0].y, cv[i][jj][0].z,
-                                          cv[i][jj][0].w, cv[i][jj][1].x, cv[i][jj][1].y,
-                                          cv[i][jj][1].z, cv[i][jj][1].w, cv[i][jj][2].x,
-                                          cv[i][jj][2].y, cv[i][jj][2].z, cv[i][jj][2].w};
+          for (int r = 0; r < 4; ++r) blk[i][r] = 0.f;
 #pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                uint32_t c[4];
-                fp6_unpack(words[h * 6 + q * 3], words[h * 6 + q * 3 + 1], words[h * 6 + q * 3 + 2], c);
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                for (int ww = 0; ww < 2; ++ww) {
-                  const int w = 2 * q + ww;
-                  uint32_t u[2], v[2];
-                  e2m3x4_to_f16x4(c[2 * ww], u);      // rows g, g+8 at columns 4w, 4w+1
-                  e2m3x4_to_f16x4(c[2 * ww + 1], v);  // rows g, g+8 at columns 4w+2, 4w+3
-                  const uint32_t a[4] = {u[0], u[1], v[0], v[1]};
-                  mma_f16(blk[i], a, xw[2 * w], xw[2 * w + 1]);
-                }
+          for (int i = 0; i < NT; ++i) {
+            const uint32_t words[12] = {cv[i][jj][0].x, cv[i][jj][0].y, cv[i][jj][0].z,
+                                        cv[i][jj][0].w, cv[i][jj][1].x, cv[i][jj][1].y,
+                                        cv[i][jj][1].z, cv[i][jj][1].w, cv[i][jj][2].x,
+                                        cv[i][jj][2].y, cv[i][jj][2].z, cv[i][jj][2].w};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t c[4];
+              fp6_unpack(words[h * 6 + q * 3], words[h * 6 + q * 3 + 1], words[h * 6 + q * 3 + 2], c);
+#pragma unroll
+              for (int ww = 0; ww < 2; ++ww) {
+                const int w = 2 * q + ww;
+                uint32_t u[2], v[2];
+                e2m3x4_to_f16x4(c[2 * ww], u);      // rows g, g+8 at columns 4w, 4w+1
+                e2m3x4_to_f16x4(c[2 * ww + 1], v);  // rows g, g+8 at columns 4w+2, 4w+3
+                const uint32_t a[4] = {u[0], u[1], v[0], v[1]};
+                mma_f16(blk[i], a, xb[jj][h][2 * w], xb[jj][h][2 * w + 1]);
               }
             }
           }
+        }
 #pragma unroll
-          for (int i = 0; i < NT; ++i) {
-            const uint32_t e = __shfl_sync(0xffffffffu, ew[i], (gi << 2) | (j >> 1));
-            const float f0 = ue8m0_to_f32((e >> (16 * (j & 1))) & 0xFFu);
-            const float f1 = ue8m0_to_f32((e >> (16 * (j & 1) + 8)) & 0xFFu);
-            acc[i][0] = fmaf(blk[i][0], f0, acc[i][0]);
-            acc[i][1] = fmaf(blk[i][1], f0, acc[i][1]);
-            acc[i][2] = fmaf(blk[i][2], f1, acc[i][2]);
-            acc[i][3] = fmaf(blk[i][3], f1, acc[i][3]);
-          }
+        for (int i = 0; i < NT; ++i) {
+          const uint32_t e = __shfl_sync(0xffffffffu, ew[i], (gi << 2) | (j >> 1));
+          const float f0 = ue8m0_to_f32((e >> (16 * (j & 1))) & 0xFFu);
+          const float f1 = ue8m0_to_f32((e >> (16 * (j & 1) + 8)) & 0xFFu);
+          acc[i][0] = fmaf(blk[i][0], f0, acc[i][0]);
+          acc[i][1] = fmaf(blk[i][1], f0, acc[i][1]);
+          acc[i][2] = fmaf(blk[i][2], f1, acc[i][2]);
+          acc[i][3] = fmaf(blk[i][3], f1, acc[i][3]);
         }
       }
     }
@@ -182,28 +197,33 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
-// Ask L2 for every 16-byte vector this lane will read from one tile's
-// super-chunks s0, s0+ds, ... (fire and forget: no registers, no waiting).
+// Ask L2 for every 16-byte vector this lane will read from one tile's halves
+// h0, h0+dh, ... (fire and forget: no registers, no waiting).
 __device__ __forceinline__ void prefetch_tile(int fmt, const uint8_t* tile, const MatGeom& g,
-                                              int s0, int ds) {
+                                              int h0, int dh) {
   const int lane = threadIdx.x & 31;
-  for (int s = s0; s < g.nsc; s += ds) {
-    const uint8_t* b = tile + (size_t)s * g.sc_bytes;
-    const int u = sc_units(g, s);
+  for (int hh = h0; hh < n_halves(g); hh += dh) {
     if (fmt == FMT_NVFP4) {
-      for (int j = 0; j <= u; ++j) prefetch_l2(b + 512 * j + 16 * lane);
+      const int s = hh >> 1, jb = (hh & 1) * 4;
+      const uint8_t* b = tile + (size_t)s * g.sc_bytes;
+      const int u = min(4, sc_units(g, s) - jb);
+      prefetch_l2(b + 16 * lane);
+      for (int j = 0; j < u; ++j) prefetch_l2(b + 512 * (1 + jb + j) + 16 * lane);
     } else {
+      const int s = hh >> 2, jb = (hh & 3) * 2;
+      const uint8_t* b = tile + (size_t)s * g.sc_bytes;
+      const int u = min(2, sc_units(g, s) - jb);
       prefetch_l2(b + 4 * lane);
-      for (int j = 0; j < 3 * u; ++j) prefetch_l2(b + 128 + 512 * j + 16 * lane);
+      for (int j = 0; j < 3 * u; ++j) prefetch_l2(b + 128 + 1536 * jb + 512 * j + 16 * lane);
     }
   }
 }
 
-template <int NT>
-__device__ __forceinline__ void tiles_mma(int fmt, const uint8_t* const (&tile)[NT],
-                                          const MatGeom& g, int s0, int ds, const uint16_t* brow,
-                                          bool b_bf16, float (&acc)[NT][4]) {
-  if (fmt == FMT_NVFP4)
+template <int FMT, int NT>
+__device__ __forceinline__ void tiles_mma(const uint8_t* const (&tile)[NT], const MatGeom& g,
+                                          int s0, int ds, const uint16_t* brow, bool b_bf16,
+                                          float (&acc)[NT][4]) {
+  if (FMT == FMT_NVFP4)
     tiles_nvfp4<NT>(tile, g, s0, ds, brow, b_bf16, acc);
   else
     tiles_fp6<NT>(tile, g, s0, ds, brow, b_bf16, acc);
@@ -253,7 +273,8 @@ __device__ __forceinline__ void reduce_ksplit(float* red, float (&v)[NV], int tp
 }
 
 // ---------------------------------------------------------------- gate/up + SwiGLU
-__global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tpc) {
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 2) gateup_kernel(ExpertParams p, int tpc) {
   const int y = blockIdx.y;
   // Shared-expert entries need no routing.  Routed ones wait for it, and only
   // then let the next kernel start: once every CTA here has triggered, the
@@ -269,7 +290,7 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tp
   const int nks = kWarps / tpc;
   const int pair = blockIdx.x * tpc + (warp % tpc), ks = warp / tpc;
   const bool valid = pair < p.I / 16;
-  const MatGeom g = mat_geom(p.fmt, p.H);
+  const MatGeom g = mat_geom(FMT, p.H);
   const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
   const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
                                    eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
@@ -282,7 +303,12 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tp
     brow = (shared_entry ? p.x : p.xh) + (size_t)tok * p.H;
   }
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  if (valid) tiles_mma<2>(p.fmt, tiles, g, ks, nks, brow, shared_entry, acc);
+  if (valid) {
+    // the warp's later K-units are requested from L2 now, so their loads do not wait on HBM
+    prefetch_tile(FMT, tiles[0], g, ks + nks, nks);
+    prefetch_tile(FMT, tiles[1], g, ks + nks, nks);
+    tiles_mma<FMT, 2>(tiles, g, ks, nks, brow, shared_entry, acc);
+  }
   float v[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -304,7 +330,8 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertParams p, int tp
 }
 
 // ---------------------------------------------------------------- down
-__global__ void __launch_bounds__(kThreads) down_kernel(ExpertParams p, int tpc) {
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 2) down_kernel(ExpertParams p, int tpc) {
   griddep_wait();
   int expert, row, n;
   if (!get_entry(p, blockIdx.y, expert, row, n)) return;
@@ -313,12 +340,15 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertParams p, int tpc)
   const int nks = kWarps / tpc;
   const int tile = blockIdx.x * tpc + (warp % tpc), ks = warp / tpc;
   const bool valid = tile < p.H / 16;
-  const MatGeom g = mat_geom(p.fmt, p.I);
+  const MatGeom g = mat_geom(FMT, p.I);
   const uint8_t* const tiles[1] = {p.arena + (size_t)expert * p.expert_bytes + p.gu_bytes +
                                    (size_t)tile * p.dn_tile_bytes};
   const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
   float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-  if (valid) tiles_mma<1>(p.fmt, tiles, g, ks, nks, brow, false, acc);
+  if (valid) {
+    prefetch_tile(FMT, tiles[0], g, ks + nks, nks);
+    tiles_mma<FMT, 1>(tiles, g, ks, nks, brow, false, acc);
+  }
   float v[4] = {acc[0][0], acc[0][1], acc[0][2], acc[0][3]};
   reduce_ksplit<4>(red, v, tpc, nks);
   if (ks != 0 || !valid) return;
@@ -374,8 +404,9 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertParams p, const floa
 // combine_kernel, so both paths agree bit for bit.  The tile's weights are
 // known once routing is done, so they are requested from L2 before waiting
 // for gate/up.
-constexpr int kDcMaxWarps = 16;
+constexpr int kDcMaxWarps = 12;
 
+template <int FMT>
 __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertParams p,
                                                                          const float* gates,
                                                                          const int* inv, float* out) {
@@ -383,14 +414,14 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
   const int nw = blockDim.x >> 5;
   const int gi = lane >> 2, t = lane & 3;
   const int S = p.T * p.k, rows_total = S + (p.shared ? p.T : 0);
-  const MatGeom g = mat_geom(p.fmt, p.I);
+  const MatGeom g = mat_geom(FMT, p.I);
   // routing is complete here (gate/up triggered this launch only after its wait)
   const int n_entries = p.nsh + *p.n_entries;
   const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
   for (int y = warp; y < n_entries; y += nw) {
     const int expert = (y < p.nsh) ? p.E : p.entries[y - p.nsh].x;
     if (expert >= 0 && expert <= p.E)
-      prefetch_tile(p.fmt, tile_base + (size_t)expert * p.expert_bytes, g, 0, 1);
+      prefetch_tile(FMT, tile_base + (size_t)expert * p.expert_bytes, g, 0, 1);
   }
   griddep_wait();  // gate/up complete: abuf holds every row
   extern __shared__ float ys[];  // [rows_total x 16]
@@ -400,7 +431,7 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
     const uint8_t* const tiles[1] = {tile_base + (size_t)expert * p.expert_bytes};
     const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    tiles_mma<1>(p.fmt, tiles, g, 0, 1, brow, false, acc);
+    tiles_mma<FMT, 1>(tiles, g, 0, 1, brow, false, acc);
     const float ts = p.tscale[expert * 3 + 2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -424,28 +455,34 @@ size_t down_combine_smem(int T, int k, int shared) {
   return ((size_t)T * k + (shared ? T : 0)) * 16 * sizeof(float);
 }
 
-int tiles_per_cta(int nsc) {
-  if (nsc >= kWarps) return 1;
-  if (nsc == 2) return 2;
-  if (nsc == 1) return kWarps;
-  return 1;
+// Warps of a CTA: kWarps / tpc of them split K, tpc tile groups side by side.
+// Each warp takes about two 256-column units (the second one requested from
+// L2 up front), which keeps the decode grid within one wave at two CTAs per SM.
+int tiles_per_cta(int units) {
+  int nks = 1;
+  while (nks * 2 <= kWarps && nks * 2 <= units / 2) nks *= 2;
+  return kWarps / nks;
 }
 
 
 }  // namespace
 
 cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
-  const int tpc = tiles_per_cta(mat_geom(p.fmt, p.H).nsc);
+  const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
   const int pairs = p.I / 16;
   dim3 grid((pairs + tpc - 1) / tpc, grid_y);
-  return launch_k(gateup_kernel, grid, dim3(kThreads), 0, st, pdl, p, tpc);
+  if (p.fmt == FMT_NVFP4)
+    return launch_k(gateup_kernel<FMT_NVFP4>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
+  return launch_k(gateup_kernel<FMT_FP6>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
 }
 
 cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
-  const int tpc = tiles_per_cta(mat_geom(p.fmt, p.I).nsc);
+  const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.I)));
   const int tiles = p.H / 16;
   dim3 grid((tiles + tpc - 1) / tpc, grid_y);
-  return launch_k(down_kernel, grid, dim3(kThreads), 0, st, pdl, p, tpc);
+  if (p.fmt == FMT_NVFP4)
+    return launch_k(down_kernel<FMT_NVFP4>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
+  return launch_k(down_kernel<FMT_FP6>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
 }
 
 cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int* inv, float* out,
@@ -466,8 +503,12 @@ cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const
   // one warp per work entry (the routed entries are at most T*k for T <= 8)
   int warps = p.nsh + (p.T * p.k < p.E ? p.T * p.k : p.E);
   if (warps > kDcMaxWarps) warps = kDcMaxWarps;
-  return launch_k(down_combine_kernel, dim3(p.H / 16), dim3(32 * warps),
-                  down_combine_smem(p.T, p.k, p.shared), st, pdl, p, gates, inv, out);
+  const size_t smem = down_combine_smem(p.T, p.k, p.shared);
+  if (p.fmt == FMT_NVFP4)
+    return launch_k(down_combine_kernel<FMT_NVFP4>, dim3(p.H / 16), dim3(32 * warps), smem, st,
+                    pdl, p, gates, inv, out);
+  return launch_k(down_combine_kernel<FMT_FP6>, dim3(p.H / 16), dim3(32 * warps), smem, st, pdl, p,
+                  gates, inv, out);
 }
 
 cudaError_t expert_kernels_init() { return cudaSuccess; }

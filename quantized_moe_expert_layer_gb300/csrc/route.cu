@@ -127,68 +127,59 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Logits of token t (sum of the router's K-split slices in order, + bias), then
-// k rounds of arg-max (largest logit, ties to the lower expert index), then the
-// softmax of the k selected logits.  Each round: a tree over the lane's values,
-// then one warp max of the value keys and one warp min of the expert ids that
-// hold it.  sidx (optional, shared memory) receives the indices too.
-__device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx) {
-  const int E = p.E, k = p.k;
-  constexpr int V = kMaxE / 32;
+// One top-k round over a lane's V slots: the largest key of the warp, ties to
+// the lower expert id (slot i of lane l holds expert id[i]); the winner's slot
+// is cleared.  Returns (key, expert id) of the winner in every lane.
+template <int V>
+__device__ __forceinline__ void warp_argmax_round(uint32_t (&key)[V], const int (&id)[V],
+                                                  uint32_t& best, int& win) {
+  uint32_t bk = key[0];
+  int bi = id[0];
+#pragma unroll
+  for (int i = 1; i < V; ++i) {  // ids ascend with i, so '>' keeps the lower id on ties
+    const bool take = key[i] > bk;
+    bk = take ? key[i] : bk;
+    bi = take ? id[i] : bi;
+  }
+  best = __reduce_max_sync(0xffffffffu, bk);
+  win = (int)__reduce_min_sync(0xffffffffu, bk == best ? (uint32_t)bi : 0xFFFFFFFFu);
+#pragma unroll
+  for (int i = 0; i < V; ++i) key[i] = (id[i] == win) ? 0u : key[i];
+}
+
+// Logits of token t for experts e = e0 + lane + 32 i (i < V, e < e_end): the
+// router's K-split slices added in order, then the bias; written to p.logits.
+template <int V>
+__device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0, int e_end,
+                                            int lane, uint32_t (&key)[V], int (&id)[V]) {
   float v[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) v[i] = 0.f;
-  // slices in a fixed order; within a slice every expert's load is independent
   for (int s = 0; s < p.ksplit; ++s) {
-    const float* ps = p.partial + ((size_t)s * p.T + t) * E;
+    const float* ps = p.partial + ((size_t)s * p.T + t) * p.E;
 #pragma unroll
     for (int i = 0; i < V; ++i)
-      if (lane + 32 * i < E) v[i] += ps[lane + 32 * i];
+      if (e0 + lane + 32 * i < e_end) v[i] += ps[e0 + lane + 32 * i];
   }
-  uint32_t key[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
+    const int e = e0 + lane + 32 * i;
+    id[i] = e;
+    if (e < e_end) {
       float l = v[i];
       if (p.bias) l = l + p.bias[e];
-      p.logits[(size_t)t * E + e] = l;
+      p.logits[(size_t)t * p.E + e] = l;
       key[i] = f32_key(l);
     } else {
       key[i] = 0u;  // below every real key
     }
   }
-  uint32_t my_key = 0;
-  int my_i = 0;
-  for (int j = 0; j < k; ++j) {
-    // tree over the lane's slots: keep the larger key, ties to the lower slot
-    uint32_t bk[V / 2];
-    int bs[V / 2];
-#pragma unroll
-    for (int i = 0; i < V / 2; ++i) {
-      const bool second = key[2 * i + 1] > key[2 * i];
-      bk[i] = second ? key[2 * i + 1] : key[2 * i];
-      bs[i] = second ? 2 * i + 1 : 2 * i;
-    }
-#pragma unroll
-    for (int w = V / 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int i = 0; i < w; ++i) {
-        const bool second = bk[i + w] > bk[i];
-        bk[i] = second ? bk[i + w] : bk[i];
-        bs[i] = second ? bs[i + w] : bs[i];
-      }
-    const uint32_t best = __reduce_max_sync(0xffffffffu, bk[0]);
-    const uint32_t cand = (bk[0] == best) ? (uint32_t)(lane + 32 * bs[0]) : 0xFFFFFFFFu;
-    const int win = (int)__reduce_min_sync(0xffffffffu, cand);
-    const bool own = (win & 31) == lane;
-#pragma unroll
-    for (int i = 0; i < V; ++i) key[i] = (own && i == (win >> 5)) ? 0u : key[i];  // taken
-    if (lane == j) {
-      my_key = best;
-      my_i = win;
-    }
-  }
+}
+
+// Gates = softmax of the k selected logits (lane j < k holds pick j).
+__device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lane, uint32_t my_key,
+                                            int my_i, int* sidx) {
+  const int k = p.k;
   const float my_v = key_f32(my_key);
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
   float ex = (lane < k) ? expf(my_v - top) : 0.f;
@@ -200,6 +191,95 @@ __device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx) {
     p.gates[(size_t)t * k + lane] = ex / sum;
     if (sidx) sidx[t * k + lane] = my_i;
   }
+}
+
+// Top-k of token t by one warp: k rounds of arg-max (largest logit, ties to
+// the lower expert index), then the softmax of the k selected logits.
+template <int V>
+__device__ void topk_token_v(const RouteParams& p, int t, int lane, int* sidx) {
+  uint32_t key[V];
+  int id[V];
+  load_logits<V>(p, t, 0, p.E, lane, key, id);
+  uint32_t my_key = 0;
+  int my_i = 0;
+  for (int j = 0; j < p.k; ++j) {
+    uint32_t best;
+    int win;
+    warp_argmax_round<V>(key, id, best, win);
+    if (lane == j) {
+      my_key = best;
+      my_i = win;
+    }
+  }
+  write_gates(p, t, lane, my_key, my_i, sidx);
+}
+
+__device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx) {
+  if (p.E <= 256)
+    topk_token_v<8>(p, t, lane, sidx);
+  else if (p.E <= 512)
+    topk_token_v<16>(p, t, lane, sidx);
+  else
+    topk_token_v<32>(p, t, lane, sidx);
+}
+
+// Top-k of token t by the 4 warps of a CTA: each warp takes a quarter of the
+// experts and finds its own k best; warp 0 then picks the k best of those 4k
+// candidates by the same rule, which gives the global top-k.
+template <int V>
+__device__ void topk_token_cta(const RouteParams& p, int t, int* sidx, uint32_t* ck, int* ci) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, k = p.k;
+  const int q = (p.E + 3) / 4;
+  uint32_t key[V];
+  int id[V];
+  load_logits<V>(p, t, warp * q, min(p.E, (warp + 1) * q), lane, key, id);
+  for (int j = 0; j < k; ++j) {
+    uint32_t best;
+    int win;
+    warp_argmax_round<V>(key, id, best, win);
+    if (lane == 0) {
+      ck[warp * kMaxK + j] = best;
+      ci[warp * kMaxK + j] = win;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t k2[4];
+    int i2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // candidate c = lane + 32 i: warp c / k, pick c % k
+      const int c = lane + 32 * i;
+      const bool ok = c < 4 * k;
+      k2[i] = ok ? ck[(c / k) * kMaxK + c % k] : 0u;
+      i2[i] = ok ? ci[(c / k) * kMaxK + c % k] : 0x7FFFFFFF;
+    }
+    // order slots by expert id within the lane so ties keep the lower id
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = a + 1; b < 4; ++b) {
+        const bool sw = i2[b] < i2[a];
+        const uint32_t tk = sw ? k2[b] : k2[a];
+        const int ti = sw ? i2[b] : i2[a];
+        k2[b] = sw ? k2[a] : k2[b];
+        i2[b] = sw ? i2[a] : i2[b];
+        k2[a] = tk;
+        i2[a] = ti;
+      }
+    uint32_t my_key = 0;
+    int my_i = 0;
+    for (int j = 0; j < k; ++j) {
+      uint32_t best;
+      int win;
+      warp_argmax_round<4>(k2, i2, best, win);
+      if (lane == j) {
+        my_key = best;
+        my_i = win;
+      }
+    }
+    write_gates(p, t, lane, my_key, my_i, sidx);
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
@@ -377,9 +457,14 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouteParam
   __syncthreads();
   if (ticket != (int)(gridDim.x * gridDim.y * gridDim.z) - 1) return;
   __threadfence();
-  for (int t = threadIdx.x >> 5; t < p.T; t += kRouterThreads / 32)
-    topk_token(p, t, threadIdx.x & 31, sidx);
-  __syncthreads();
+  __shared__ uint32_t cand_key[4 * kMaxK];
+  __shared__ int cand_id[4 * kMaxK];
+  for (int t = 0; t < p.T; ++t) {
+    if (p.E <= 512)
+      topk_token_cta<4>(p, t, sidx, cand_key, cand_id);
+    else
+      topk_token_cta<8>(p, t, sidx, cand_key, cand_id);
+  }
   dispatch_small(p, reinterpret_cast<int*>(smem_u4), sidx);
   if (threadIdx.x == 0) *counter = 0;
 }

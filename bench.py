@@ -215,18 +215,27 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def traffic_from_profile(kernel_src):
-    """dram bytes per launch of the gate/up kernel from the committed ncu summary,
-    or None if the kernel source changed since the capture."""
-    p = os.path.join(ROOT, "profiles", "gateup_kernel_decode-h2048-e512-k10-t1.md")
+def traffic_from_profile(kernel, csrc):
+    """dram bytes per launch of `kernel` from its committed ncu summary, or None
+    when any kernel source changed since the capture (the summary records a
+    hash of csrc/*)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_decode-h2048-e512-k10-t1.md")
     try:
         txt = open(p).read()
         sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt).group(1)
         b = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt).group(1))
     except Exception:
         return None
-    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return b if cur == sha else None
+    return b if sources_sha256(csrc) == sha else None
+
+
+def sources_sha256(csrc):
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
 
 
 # ---------------------------------------------------------------- our arm
@@ -308,8 +317,14 @@ def run_ours(args, w):
         ms = float(t.item())
     value = world * T * Ln * args.steps / (ms / 1e3)
 
-    # dominant kernel: gate/up + SwiGLU, timed alone over the L layers (launch gaps included)
+    # dominant kernel, timed alone over the L layers (graph of back-to-back launches,
+    # launch gaps included): the whole-layer decode kernel when a forward is one
+    # launch, else gate/up + SwiGLU
+    n_launch = layers[0].launches(T)
+    one_kernel = n_launch == 1
     counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    arena, expert_bytes = layers[0].info()
+    gu_bytes = (w.I // 16) * 2 * (w.H // 64 + (w.H // 64 + 7) // 8) * 512 if w.fmt == 1 else None
     per_launch_bytes = []
     with torch.cuda.stream(s):
         for L, o in zip(layers, outs):
@@ -317,12 +332,17 @@ def run_ours(args, w):
             L.debug_routing(counts=counts, stream=s)
             s.synchronize()
             D = int((counts > 0).sum().item()) + w.shared
-            gu_bytes = (w.I // 16) * 2 * (w.H // 64 + (w.H // 64 + 7) // 8) * 512
-            per_launch_bytes.append(D * (gu_bytes + 8) + T * w.H * 2 + (T * w.k + T * w.shared) * w.I * 2)
+            if one_kernel:  # every byte the layer must move once
+                b = D * (expert_bytes + 12) + w.E * w.H * 2 + (w.E * 4 if w.bias != "none" else 0)
+                per_launch_bytes.append(b + T * w.H * 2 + T * w.H * 4)
+            else:
+                per_launch_bytes.append(D * (gu_bytes + 8) + T * w.H * 2 +
+                                        (T * w.k + T * w.shared) * w.I * 2)
+    kphase = 0 if one_kernel else 2
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk, stream=s):
         for L, o in zip(layers, outs):
-            L.run_phase(2, x, o, stream=s)
+            L.run_phase(kphase, x, o, stream=s)
     reps = max(20, min(500, args.steps))
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
@@ -337,9 +357,10 @@ def run_ours(args, w):
     bytes_launch = sum(per_launch_bytes) / len(per_launch_bytes)
     peak, peak_kind = peaks()
     achieved = bytes_launch / (k_us * 1e-6) / 1e9
-    traffic = traffic_from_profile(os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc",
-                                                "expert.cu"))
-    roofline = {"bound": "hbm", "kernel": "gateup_kernel", "achieved": achieved, "peak": peak,
+    kname = "decode_kernel" if one_kernel else "gateup_kernel"
+    traffic = traffic_from_profile(kname, os.path.join(ROOT, "quantized_moe_expert_layer_gb300",
+                                                       "csrc"))
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": k_us,
                 "peak_source": peak_kind,

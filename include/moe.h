@@ -79,6 +79,18 @@ const char* moe_last_error(void);
  * reset != 0.  Returns MOE_OK, or an error if the read itself failed. */
 int moe_layer_status(moe_layer* L, int reset, int* status);
 
+/* Layer options (moe_layer_set_option). */
+enum moe_option {
+  /* 1 (default): for T <= 8 the whole layer runs as one cooperative kernel
+   * (routing, gate/up, down + combine separated by grid-wide barriers);
+   * 0: as three kernels chained with programmatic dependent launch.  Both give
+   * the same numbers (same device code, same order). */
+  MOE_OPT_DECODE_FUSED = 1
+};
+
+/* Set a layer option; not while a forward is in flight. */
+int moe_layer_set_option(moe_layer* L, int option, int value);
+
 /* Number of kernels one moe_forward of T tokens launches (>= 0), or an error. */
 int moe_forward_launches(moe_layer* L, int T);
 

@@ -95,6 +95,12 @@ cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, cudaStream_t st)
 cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, cudaStream_t st);
 cudaError_t tc_kernels_init();
 
+// decode megakernel (T <= 8): the whole layer in one cooperative launch
+bool decode_ok(int fmt, int T, int k, int shared, int H);
+cudaError_t launch_decode(const RouteParams& rp, const ExpertParams& ep, float* out, unsigned* bar,
+                          cudaStream_t st);
+cudaError_t decode_kernels_init();
+
 // launch helper: optional programmatic dependent launch on the previous kernel in the stream
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

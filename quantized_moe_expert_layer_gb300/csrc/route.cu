@@ -14,98 +14,10 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 namespace {
-
-constexpr int kRouterThreads = 128;
-constexpr int kFinishThreads = 1024;
-
-// ---------------------------------------------------------------- router logits
-// grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); 4 warps split
-// the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
-// (ksplit slice, token, expert) partial sum goes to p.partial; the top-k step
-// adds the slices in a fixed order.
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
-}
-
-__device__ __forceinline__ void router_partials(const RouteParams& p, uint4* smem_u4) {
-  const int tile = blockIdx.x, t0 = blockIdx.y * kTokTile, ks = blockIdx.z;
-  const int n = min(kTokTile, p.T - t0);
-  const int C = p.H / 64;
-  const int c_begin = C * ks / p.ksplit, c_end = C * (ks + 1) / p.ksplit;
-  const int kbase = c_begin * 64, klen = (c_end - c_begin) * 64;
-  const int stride = klen + 8;  // +16 bytes per row: conflict-free 16-byte reads
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
-  float* red = reinterpret_cast<float*>(xs + kTokTile * stride);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
-  const int e0 = 16 * tile + gi, e1 = e0 + 8;
-  const uint16_t* r0 = p.wr + (size_t)min(e0, p.E - 1) * p.H;
-  const uint16_t* r1 = p.wr + (size_t)min(e1, p.E - 1) * p.H;
-  // start the router-weight reads before the activations are staged
-  for (int c = c_begin + warp; c < c_end; c += 4) {
-    prefetch_l2(r0 + 64 * c + 16 * t);
-    prefetch_l2(r1 + 64 * c + 16 * t);
-  }
-  const bool write_xh = p.xh != nullptr && tile == 0;
-  for (int i = threadIdx.x; i < n * (klen / 8); i += blockDim.x) {
-    const int r = i / (klen / 8), v = i % (klen / 8);
-    const size_t off = (size_t)(t0 + r) * p.H + kbase + 8 * v;
-    const uint4 raw = *reinterpret_cast<const uint4*>(p.x + off);
-    *reinterpret_cast<uint4*>(xs + r * stride + 8 * v) = raw;
-    if (write_xh) {  // the f16 copy the expert kernels read (exact for |x| in f16's normal range)
-      const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16),
-                                            __uint_as_float(in[q] & 0xFFFF0000u));
-        o[q] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      *reinterpret_cast<uint4*>(p.xh + off) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-  __syncthreads();
-
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c = c_begin + warp; c < c_end; c += 4) {
-    const int kc = 64 * c + 16 * t;
-    uint4 a00 = ldg_stream(r0 + kc), a01 = ldg_stream(r0 + kc + 8);
-    uint4 a10 = ldg_stream(r1 + kc), a11 = ldg_stream(r1 + kc + 8);
-    if (e0 >= p.E) a00 = a01 = make_uint4(0, 0, 0, 0);
-    if (e1 >= p.E) a10 = a11 = make_uint4(0, 0, 0, 0);
-    const uint32_t ra[8] = {a00.x, a00.y, a00.z, a00.w, a01.x, a01.y, a01.z, a01.w};
-    const uint32_t rb[8] = {a10.x, a10.y, a10.z, a10.w, a11.x, a11.y, a11.z, a11.w};
-    uint32_t xw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (gi < n) {
-      const uint4* px = reinterpret_cast<const uint4*>(xs + gi * stride + (kc - kbase));
-      const uint4 q0 = px[0], q1 = px[1];
-      xw[0] = q0.x; xw[1] = q0.y; xw[2] = q0.z; xw[3] = q0.w;
-      xw[4] = q1.x; xw[5] = q1.y; xw[6] = q1.z; xw[7] = q1.w;
-    }
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const uint32_t a[4] = {ra[2 * w], rb[2 * w], ra[2 * w + 1], rb[2 * w + 1]};
-      mma_bf16(acc, a, xw[2 * w], xw[2 * w + 1]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) red[(warp * 32 + lane) * 4 + i] = acc[i];
-  __syncthreads();
-  if (warp == 0) {
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int w = 0; w < kRouterThreads / 32; ++w)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) s[i] += red[(w * 32 + lane) * 4 + i];
-    float* out = p.partial + (size_t)ks * p.T * p.E;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = (i < 2) ? e0 : e1, col = 2 * t + (i & 1);
-      if (e < p.E && col < n) out[(size_t)(t0 + col) * p.E + e] = s[i];
-    }
-  }
-}
 
 // grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); 4 warps split
 // the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
@@ -114,172 +26,7 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, uint4* sme
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
   griddep_launch();
   extern __shared__ uint4 smem_u4[];
-  router_partials(p, smem_u4);
-}
-
-// ---------------------------------------------------------------- top-k (one warp per token)
-// Order-preserving map of an fp32 value to a uint32 key (larger value, larger key).
-__device__ __forceinline__ uint32_t f32_key(float v) {
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_f32(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// One top-k round over a lane's V slots: the largest key of the warp, ties to
-// the lower expert id (slot i of lane l holds expert id[i]); the winner's slot
-// is cleared.  Returns (key, expert id) of the winner in every lane.
-template <int V>
-__device__ __forceinline__ void warp_argmax_round(uint32_t (&key)[V], const int (&id)[V],
-                                                  uint32_t& best, int& win) {
-  uint32_t bk = key[0];
-  int bi = id[0];
-#pragma unroll
-  for (int i = 1; i < V; ++i) {  // ids ascend with i, so '>' keeps the lower id on ties
-    const bool take = key[i] > bk;
-    bk = take ? key[i] : bk;
-    bi = take ? id[i] : bi;
-  }
-  best = __reduce_max_sync(0xffffffffu, bk);
-  win = (int)__reduce_min_sync(0xffffffffu, bk == best ? (uint32_t)bi : 0xFFFFFFFFu);
-#pragma unroll
-  for (int i = 0; i < V; ++i) key[i] = (id[i] == win) ? 0u : key[i];
-}
-
-// Logits of token t for experts e = e0 + lane + 32 i (i < V, e < e_end): the
-// router's K-split slices added in order, then the bias; written to p.logits.
-template <int V>
-__device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0, int e_end,
-                                            int lane, uint32_t (&key)[V], int (&id)[V]) {
-  float v[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) v[i] = 0.f;
-  for (int s = 0; s < p.ksplit; ++s) {
-    const float* ps = p.partial + ((size_t)s * p.T + t) * p.E;
-#pragma unroll
-    for (int i = 0; i < V; ++i)
-      if (e0 + lane + 32 * i < e_end) v[i] += ps[e0 + lane + 32 * i];
-  }
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = e0 + lane + 32 * i;
-    id[i] = e;
-    if (e < e_end) {
-      float l = v[i];
-      if (p.bias) l = l + p.bias[e];
-      p.logits[(size_t)t * p.E + e] = l;
-      key[i] = f32_key(l);
-    } else {
-      key[i] = 0u;  // below every real key
-    }
-  }
-}
-
-// Gates = softmax of the k selected logits (lane j < k holds pick j).
-__device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lane, uint32_t my_key,
-                                            int my_i, int* sidx) {
-  const int k = p.k;
-  const float my_v = key_f32(my_key);
-  const float top = __shfl_sync(0xffffffffu, my_v, 0);
-  float ex = (lane < k) ? expf(my_v - top) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) {
-    p.idx[(size_t)t * k + lane] = my_i;
-    p.gates[(size_t)t * k + lane] = ex / sum;
-    if (sidx) sidx[t * k + lane] = my_i;
-  }
-}
-
-// Top-k of token t by one warp: k rounds of arg-max (largest logit, ties to
-// the lower expert index), then the softmax of the k selected logits.
-template <int V>
-__device__ void topk_token_v(const RouteParams& p, int t, int lane, int* sidx) {
-  uint32_t key[V];
-  int id[V];
-  load_logits<V>(p, t, 0, p.E, lane, key, id);
-  uint32_t my_key = 0;
-  int my_i = 0;
-  for (int j = 0; j < p.k; ++j) {
-    uint32_t best;
-    int win;
-    warp_argmax_round<V>(key, id, best, win);
-    if (lane == j) {
-      my_key = best;
-      my_i = win;
-    }
-  }
-  write_gates(p, t, lane, my_key, my_i, sidx);
-}
-
-__device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx) {
-  if (p.E <= 256)
-    topk_token_v<8>(p, t, lane, sidx);
-  else if (p.E <= 512)
-    topk_token_v<16>(p, t, lane, sidx);
-  else
-    topk_token_v<32>(p, t, lane, sidx);
-}
-
-// Top-k of token t by the 4 warps of a CTA: each warp takes a quarter of the
-// experts and finds its own k best; warp 0 then picks the k best of those 4k
-// candidates by the same rule, which gives the global top-k.
-template <int V>
-__device__ void topk_token_cta(const RouteParams& p, int t, int* sidx, uint32_t* ck, int* ci) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, k = p.k;
-  const int q = (p.E + 3) / 4;
-  uint32_t key[V];
-  int id[V];
-  load_logits<V>(p, t, warp * q, min(p.E, (warp + 1) * q), lane, key, id);
-  for (int j = 0; j < k; ++j) {
-    uint32_t best;
-    int win;
-    warp_argmax_round<V>(key, id, best, win);
-    if (lane == 0) {
-      ck[warp * kMaxK + j] = best;
-      ci[warp * kMaxK + j] = win;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t k2[4];
-    int i2[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // candidate c = lane + 32 i: warp c / k, pick c % k
-      const int c = lane + 32 * i;
-      const bool ok = c < 4 * k;
-      k2[i] = ok ? ck[(c / k) * kMaxK + c % k] : 0u;
-      i2[i] = ok ? ci[(c / k) * kMaxK + c % k] : 0x7FFFFFFF;
-    }
-    // order slots by expert id within the lane so ties keep the lower id
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = a + 1; b < 4; ++b) {
-        const bool sw = i2[b] < i2[a];
-        const uint32_t tk = sw ? k2[b] : k2[a];
-        const int ti = sw ? i2[b] : i2[a];
-        k2[b] = sw ? k2[a] : k2[b];
-        i2[b] = sw ? i2[a] : i2[b];
-        k2[a] = tk;
-        i2[a] = ti;
-      }
-    uint32_t my_key = 0;
-    int my_i = 0;
-    for (int j = 0; j < k; ++j) {
-      uint32_t best;
-      int win;
-      warp_argmax_round<4>(k2, i2, best, win);
-      if (lane == j) {
-        my_key = best;
-        my_i = win;
-      }
-    }
-    write_gates(p, t, lane, my_key, my_i, sidx);
-  }
-  __syncthreads();
+  router_partials(p, blockIdx.x, blockIdx.y, blockIdx.z, smem_u4);
 }
 
 __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
@@ -287,159 +34,6 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
   griddep_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t < p.T) topk_token(p, t, threadIdx.x & 31, nullptr);
-}
-
-// ---------------------------------------------------------------- dispatch (one CTA of 1024 threads)
-// exclusive scan of v over the block; *total gets the sum
-__device__ int block_excl_scan(int v, int* sc, int* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sc[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int s = (lane < (int)(blockDim.x >> 5)) ? sc[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    sc[32 + lane] = s;  // inclusive warp-total prefix
-  }
-  __syncthreads();
-  const int before = (w > 0) ? sc[32 + w - 1] : 0;
-  *total = sc[32 + (blockDim.x >> 5) - 1];
-  const int r = before + x - v;
-  __syncthreads();
-  return r;
-}
-
-__device__ __forceinline__ int checked_expert(const RouteParams& p, int e) {
-  if (e < 0 || e >= p.E) {
-    *p.status = -1;  // MOE_EINVAL
-    return 0;
-  }
-  return e;
-}
-
-__device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
-  const int S = p.T * p.k, E = p.E;
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, NW = blockDim.x >> 5;
-  for (int i = tid; i < NW * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  const int per = (S + NW - 1) / NW;
-  const int sb = min(S, w * per), se = min(S, sb + per);
-  for (int s = sb + lane; s < se; s += 32) atomicAdd(&hist[w * E + checked_expert(p, p.idx[s])], 1);
-  __syncthreads();
-  int c = 0;
-  if (tid < E)
-    for (int ww = 0; ww < NW; ++ww) c += hist[ww * E + tid];
-  int total;
-  const int excl = block_excl_scan(tid < E ? c : 0, sc, &total);
-  if (tid < E) {
-    p.counts[tid] = c;
-    p.offsets[tid] = excl;
-    int run = excl;
-    for (int ww = 0; ww < NW; ++ww) {
-      const int h = hist[ww * E + tid];
-      hist[ww * E + tid] = run;
-      run += h;
-    }
-  }
-  if (tid == 0) p.offsets[E] = total;
-  __syncthreads();
-  // stable placement: each warp walks its slot range in order, 32 at a time
-  for (int base = sb; base < se; base += 32) {
-    const int s = base + lane;
-    const bool valid = s < se;
-    const int e = valid ? checked_expert(p, p.idx[s]) : -1 - lane;
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    if (valid) {
-      const int pos = hist[w * E + e] + __popc(peers & lanemask_lt());
-      p.perm[pos] = s;
-      p.inv[s] = pos;
-      p.row_token[pos] = s / p.k;
-    }
-    __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) hist[w * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  for (int i = tid; i < p.T; i += blockDim.x) p.row_token[S + i] = i;
-  // routed work entries: ceil(count / 8) per expert, expert-major
-  const int nch = (tid < E) ? (c + kTokTile - 1) / kTokTile : 0;
-  int n_total;
-  const int ebase = block_excl_scan(nch, sc, &n_total);
-  if (tid < E) {
-    const int off = excl;
-    for (int i = 0; i < nch; ++i)
-      p.entries[ebase + i] = make_int4(tid, off + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
-  }
-  if (tid == 0) *p.n_entries = n_total;
-  if (p.tc_entries) {
-    const int ntc = (tid < E) ? (c + kTcMaxN - 1) / kTcMaxN : 0;
-    int tc_total;
-    const int tbase = block_excl_scan(ntc, sc, &tc_total);
-    if (tid < E)
-      for (int i = 0; i < ntc; ++i)
-        p.tc_entries[tbase + i] = make_int4(tid, excl + kTcMaxN * i, min(kTcMaxN, c - kTcMaxN * i), 0);
-    if (tid == 0) *p.n_tc_entries = tc_total;
-  }
-}
-
-// Dispatch for a few slots (T*k <= kSmallSlots) by any block size: the same
-// result as dispatch_block (expert-major, stable), with a per-expert count
-// table and a direct stable rank.  smem: 64 + E + S ints.
-constexpr int kSmallSlots = 256;
-
-// sidx: the S expert ids in shared memory (already written and synchronised)
-__device__ void dispatch_small(const RouteParams& p, int* smem, int* sidx) {
-  const int S = p.T * p.k, E = p.E, nt = blockDim.x, tid = threadIdx.x;
-  int* sc = smem;
-  int* cnt = smem + 64;
-  for (int e = tid; e < E; e += nt) cnt[e] = 0;
-  for (int s = tid; s < S; s += nt) sidx[s] = checked_expert(p, sidx[s]);
-  __syncthreads();
-  for (int s = tid; s < S; s += nt) atomicAdd(&cnt[sidx[s]], 1);
-  __syncthreads();
-  const int ept = (E + nt - 1) / nt;
-  const int lo = min(E, tid * ept), hi = min(E, lo + ept);
-  int local = 0, lnch = 0;
-  for (int e = lo; e < hi; ++e) {
-    local += cnt[e];
-    lnch += (cnt[e] + kTokTile - 1) / kTokTile;
-  }
-  int total, n_total;
-  int run = block_excl_scan(local, sc, &total);
-  int runn = block_excl_scan(lnch, sc, &n_total);
-  for (int e = lo; e < hi; ++e) {
-    const int c = cnt[e];
-    p.counts[e] = c;
-    p.offsets[e] = run;
-    for (int i = 0; i * kTokTile < c; ++i)
-      p.entries[runn + i] = make_int4(e, run + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
-    cnt[e] = run;
-    run += c;
-    runn += (c + kTokTile - 1) / kTokTile;
-  }
-  if (tid == 0) {
-    p.offsets[E] = total;
-    *p.n_entries = n_total;
-  }
-  __syncthreads();
-  for (int s = tid; s < S; s += nt) {
-    const int e = sidx[s];
-    int r = 0;
-    for (int q = 0; q < s; ++q) r += (sidx[q] == e);
-    const int pos = cnt[e] + r;
-    p.perm[pos] = s;
-    p.inv[s] = pos;
-    p.row_token[pos] = s / p.k;
-  }
-  for (int t = tid; t < p.T; t += nt) p.row_token[S + t] = t;
 }
 
 // Router for T <= 8: the partial sums as in router_kernel, then the last CTA to
@@ -450,20 +44,22 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouteParam
   extern __shared__ uint4 smem_u4[];
   __shared__ int ticket;
   __shared__ int sidx[kSmallSlots];
-  router_partials(p, smem_u4);
+  router_partials(p, blockIdx.x, blockIdx.y, blockIdx.z, smem_u4);
   if (threadIdx.x < 32) __threadfence();  // warp 0 wrote this CTA's partial sums
   __syncthreads();
   if (threadIdx.x == 0) ticket = atomicAdd(counter, 1);
   __syncthreads();
   if (ticket != (int)(gridDim.x * gridDim.y * gridDim.z) - 1) return;
   __threadfence();
-  __shared__ uint32_t cand_key[4 * kMaxK];
-  __shared__ int cand_id[4 * kMaxK];
-  for (int t = 0; t < p.T; ++t) {
-    if (p.E <= 512)
-      topk_token_cta<4>(p, t, sidx, cand_key, cand_id);
+  __shared__ uint32_t cand_key[(kRouterThreads / 32) * kMaxK];
+  __shared__ int cand_id[(kRouterThreads / 32) * kMaxK];
+  for (int t = 0; t < p.T; ++t) {  // 8 warps share each token's top-k (E/8 experts each)
+    if (p.E <= 256)
+      topk_token_cta<1, 8>(p, t, sidx, cand_key, cand_id);
+    else if (p.E <= 512)
+      topk_token_cta<2, 8>(p, t, sidx, cand_key, cand_id);
     else
-      topk_token_cta<8>(p, t, sidx, cand_key, cand_id);
+      topk_token_cta<4, 8>(p, t, sidx, cand_key, cand_id);
   }
   dispatch_small(p, reinterpret_cast<int*>(smem_u4), sidx);
   if (threadIdx.x == 0) *counter = 0;

@@ -68,10 +68,34 @@ def test_tensor_core_path_small_layer(T):
     compare_layer(w, L, gen.x_tokens(w, T))
 
 
-def test_decode_nvfp4_full_size():
+@pytest.mark.parametrize("fused", [1, 0])
+def test_decode_nvfp4_full_size(fused):
     w = gen.get_workload(1)
-    rel, ties = compare_layer(w, layer(w), gen.x_tokens(w))
-    print(f"decode nvfp4: rel-L2 {rel:.2e}, near ties {ties}")
+    L = layer(w)
+    L.set_option(moe.OPT_DECODE_FUSED, fused)
+    try:
+        assert L.launches(1) == (1 if fused else 3)
+        rel, ties = compare_layer(w, L, gen.x_tokens(w))
+        print(f"decode nvfp4 (fused={fused}): rel-L2 {rel:.2e}, near ties {ties}")
+    finally:
+        L.set_option(moe.OPT_DECODE_FUSED, 1)
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_decode_fused_and_chained_paths_agree_bit_for_bit(T):
+    """The one-kernel decode path and the three-kernel chain run the same device
+    code in the same order."""
+    w = gen.get_workload(1)
+    L = layer(w)
+    x = gen.x_tokens(w, T)
+    a = run_gpu(L, x, w)
+    L.set_option(moe.OPT_DECODE_FUSED, 0)
+    try:
+        b = run_gpu(L, x, w)
+    finally:
+        L.set_option(moe.OPT_DECODE_FUSED, 1)
+    for key in ("out", "logits", "idx", "gates", "counts", "offsets", "perm"):
+        assert np.array_equal(a[key], b[key]), key
 
 
 def test_decode_fp6_full_size():
@@ -80,6 +104,11 @@ def test_decode_fp6_full_size():
     try:
         rel, ties = compare_layer(w, L, gen.x_tokens(w))
         print(f"decode fp6: rel-L2 {rel:.2e}, near ties {ties}")
+        x = gen.x_tokens(w)
+        a = run_gpu(L, x, w)
+        L.set_option(moe.OPT_DECODE_FUSED, 0)
+        b = run_gpu(L, x, w)
+        assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["idx"], b["idx"])
     finally:
         L.close()
 

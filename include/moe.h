@@ -81,10 +81,10 @@ int moe_layer_status(moe_layer* L, int reset, int* status);
 
 /* Layer options (moe_layer_set_option). */
 enum moe_option {
-  /* 1 (default): for T <= 8 the whole layer runs as one cooperative kernel
-   * (routing, gate/up, down + combine separated by grid-wide barriers);
-   * 0: as three kernels chained with programmatic dependent launch.  Both give
-   * the same numbers (same device code, same order). */
+  /* 1: for T <= 8 the whole layer runs as one cooperative kernel (routing,
+   * gate/up, down + combine separated by grid-wide barriers); 0 (default): as
+   * three kernels chained with programmatic dependent launch.  Both give the
+   * same numbers (same device code, same order). */
   MOE_OPT_DECODE_FUSED = 1
 };
 

@@ -32,6 +32,9 @@ struct ExpertParams {
   const uint16_t* xh;    // f16 copy of x [T x H] (written by the router)
   uint16_t* abuf;        // f16 bits [(T*k + T) x I]: silu(g) * u per row
   float* ybuf;           // [(T*k + T) x H]: ts_down * (W_down a) per row
+  const uint16_t* wr;    // router weights bf16 [E x H] (tensor-core router only)
+  const float* rbias;    // router bias [E] or null (tensor-core router only)
+  float* logits_out;     // router logits [T x E] (tensor-core router only)
   int* status;
 };
 
@@ -93,6 +96,8 @@ bool tc_path_ok(int fmt, int T, int k, int E, int H, int I);
 int max_tc_entries(int T, int E, int k);
 cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, cudaStream_t st);
 cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, cudaStream_t st);
+bool tc_router_ok(int E, int H);
+cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);
 cudaError_t tc_kernels_init();
 
 // decode megakernel (T <= 8): the whole layer in one cooperative launch

@@ -106,7 +106,7 @@ struct moe_layer {
   int* n_entries = nullptr;
   int* route_counter = nullptr;  // ticket counter of the fused small-T router
   unsigned* grid_bar = nullptr;  // grid-barrier state of the decode megakernel
-  bool decode_fused = true;      // T <= 8: one cooperative kernel (else three kernels)
+  bool decode_fused = false;     // T <= 8: one cooperative kernel (else three kernels)
   int4* tc_entries = nullptr;    // entries of up to 256 tokens (tensor-core path)
   int* n_tc_entries = nullptr;
   uint16_t* xh = nullptr;        // f16 copy of x
@@ -130,7 +130,9 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.E = L->E;
   p.k = L->k;
   p.shared = L->shared;
-  p.ksplit = router_ksplit(T, L->H, L->E);
+  const bool tc = tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I);
+  // the tensor-core router writes the whole dot product: one K slice
+  p.ksplit = tc && tc_router_ok(L->E, L->H) ? 1 : router_ksplit(T, L->H, L->E);
   p.partial = L->partial;
   p.logits = L->logits;
   p.idx = L->idx;
@@ -143,7 +145,6 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.entries = L->entries;
   p.n_entries = L->n_entries;
   p.xh = L->xh;
-  const bool tc = tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I);
   p.tc_entries = tc ? L->tc_entries : nullptr;
   p.n_tc_entries = tc ? L->n_tc_entries : nullptr;
   p.status = L->status;
@@ -176,6 +177,8 @@ ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
   p.x = x;
   p.abuf = L->abuf;
   p.ybuf = L->ybuf;
+  p.wr = L->router;
+  p.rbias = L->has_bias ? L->bias : nullptr;
   p.status = L->status;
   return p;
 }
@@ -200,6 +203,18 @@ int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
 bool fused_down(moe_layer* L, int T) { return down_combine_ok(T, L->k, L->shared, L->I); }
 
 bool tc_path(moe_layer* L, int T) { return tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I); }
+
+// prefill routing: logits as one bf16 GEMM on the tensor cores, then top-k and
+// dispatch as usual (the GEMM's output is the one K slice the top-k reads)
+bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E, L->H); }
+
+int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
+  ExpertParams ep = expert_params(L, x, T);
+  ep.logits_out = L->partial;
+  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, st));
+  CK("tensor-core router kernel launch", launch_tc_router(ep, st));
+  return MOE_OK;
+}
 
 int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
@@ -228,7 +243,8 @@ bool decode_path(moe_layer* L, int T) {
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
   if (decode_path(L, T)) return 1;
-  const int routing = router_small_ok(T, L->k) ? 1 : (T <= 64 ? 2 : 3);
+  const int routing =
+      tc_router(L, T) ? 4 : (router_small_ok(T, L->k) ? 1 : (T <= 64 ? 2 : 3));
   if (tc_path(L, T)) return routing + 3;
   return routing + (fused_down(L, T) ? 2 : 3);
 }
@@ -241,7 +257,12 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
     CK("decode kernel launch", launch_decode(rp, expert_params(L, x, T), out, L->grid_bar, st));
     return MOE_OK;
   }
-  if (router_small_ok(T, L->k)) {
+  if (tc_router(L, T)) {
+    const int rc = launch_tc_routing_gemm(L, x, T, st);
+    if (rc) return rc;
+    CK("top-k kernel launch", launch_topk(rp, true, st));
+    CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
+  } else if (router_small_ok(T, L->k)) {
     CK("router kernel launch", launch_router_small(rp, L->route_counter, st));
   } else if (T <= 64) {
     CK("router kernel launch", launch_router(rp, st));
@@ -614,10 +635,14 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
   const bool small = router_small_ok(T, L->k), fused = fused_down(L, T);
   switch (phase) {
     case 0:
-      if (small)
+      if (tc_router(L, T)) {
+        const int rc = launch_tc_routing_gemm(L, x, T, st);
+        if (rc) return rc;
+      } else if (small) {
         CK("router", launch_router_small(rp, L->route_counter, st));
-      else
+      } else {
         CK("router", launch_router(rp, st));
+      }
       break;
     case 1:
       if (small) break;

@@ -13,6 +13,10 @@
 // TMEM (warp w owns lanes 32w..32w+31) and apply the fp32 tensor scale and
 // SwiGLU (gate/up) or write y rows (down).
 //
+// MODE 2 is the router for large T: a plain bf16 GEMM, logits[t][e] =
+// x[t] . Wr[e], with 128 experts as M and 128 tokens as N; both operands are
+// copied straight into the swizzled stages (no dequantisation).
+//
 // The weights stay the M operand and the token count the N operand (N is 80 on
 // average for 4096 tokens over 512 experts), as the survey of the prompt paths
 // suggests: experts with few tokens keep the decoded weights as the wide side.
@@ -29,7 +33,7 @@ namespace {
 constexpr int kTcM = 128;            // rows of W per work item
 constexpr int kTcK = 64;             // K per pipeline stage (one packed chunk)
 constexpr int kTcStages = 6;
-constexpr int kTcLookahead = kTcStages - 1;  // chunks whose copies are in flight
+constexpr int kTcLookahead = kTcStages - 2;  // chunks in flight; one stage of slack for the MMAs
 constexpr int kTcProducers = 256;    // warps 0-7: producers, then epilogue
 constexpr int kTcThreads = 288;      // + warp 8: TMEM allocation and MMA issue
 constexpr int kTcAStageBytes = kTcM * kTcK * 2;     // 16 KB of dequantised f16 weights
@@ -186,8 +190,8 @@ __device__ __forceinline__ bool tc_entry(const ExpertParams& p, int y, int& expe
   return true;
 }
 
-// The shared skeleton of both GEMMs.  MODE 0: gate/up + SwiGLU -> abuf;
-// MODE 1: down -> ybuf.
+// The shared skeleton of the GEMMs.  MODE 0: gate/up + SwiGLU -> abuf;
+// MODE 1: down -> ybuf; MODE 2: router logits (bf16 x bf16) -> logits_out.
 //
 // Producer thread u (of 256) owns packed vector u of each chunk: tile u/32,
 // lane u%32 of the 16-row tile layout, i.e. rows 16*(u/32) + (u%32)/4 (+8) and
@@ -199,7 +203,14 @@ template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) {
   griddep_wait();
   int expert, row0, n;
-  if (!tc_entry(p, blockIdx.y, expert, row0, n)) return;
+  if (MODE == 2) {  // token tile blockIdx.y of the router GEMM
+    expert = 0;
+    row0 = kTcMaxN * blockIdx.y;
+    n = min(kTcMaxN, p.T - row0);
+    if (n <= 0) return;
+  } else if (!tc_entry(p, blockIdx.y, expert, row0, n)) {
+    return;
+  }
   extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
   TcShared* sh = reinterpret_cast<TcShared*>(RAW + kTcStages * kTcRawStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.T * p.k;
-  const int K = MODE == 0 ? p.H : p.I;
+  const int K = MODE == 1 ? p.I : p.H;
   const int KC = K / kTcK;
   const int mb = blockIdx.x;
   const uint32_t ncols = n_pad <= 32 ? 32 : (n_pad <= 64 ? 64 : 128);
@@ -230,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
   for (int i = tid; i < n_pad; i += kTcThreads) {
     int tk = 0;
     if (i < n) tk = (MODE == 0) ? ((expert == p.E) ? row0 - S + i : p.row_token[row0 + i]) : row0 + i;
-    sh->tok[i] = tk;  // MODE 0: token index into x; MODE 1: row of abuf
+    sh->tok[i] = tk;  // MODE 0 / 2: token index into x; MODE 1: row of abuf
   }
   // token-row padding stays zero in every stage (cp.async never writes it)
   for (int i = tid; i < kTcStages * (n_pad - n) * 8; i += kTcThreads) {
@@ -250,18 +261,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
     const int u = tid, ti = u >> 5, ln = u & 31, gi = ln >> 2, t = ln & 3;
     const uint8_t* tile = (MODE == 0) ? eb + (size_t)(8 * mb + ti) * p.gu_tile_bytes
                                       : eb + p.gu_bytes + (size_t)(8 * mb + ti) * p.dn_tile_bytes;
-    const uint16_t* bsrc = (MODE == 0) ? p.xh : p.abuf;
-    const int bld = (MODE == 0) ? p.H : p.I;
+    const uint16_t* bsrc = (MODE == 0) ? p.xh : (MODE == 1 ? p.abuf : p.x);
+    const int bld = (MODE == 1) ? p.I : p.H;
+    const uint16_t* arow = p.wr + (size_t)kTcM * mb * p.H;  // MODE 2: 128 router rows
     // ask L2 for everything this CTA will read
-    for (int s = 0; s < g.nsc; ++s)
-      for (int j = 0; j <= sc_units(g, s); ++j) prefetch_l2(tile + (size_t)s * g.sc_bytes + 512 * j + 16 * ln);
+    if (MODE == 2) {
+      for (int i = tid; i < kTcM * (K / 64); i += kTcProducers)
+        prefetch_l2(arow + (size_t)(i / (K / 64)) * p.H + 64 * (i % (K / 64)));
+    } else {
+      for (int s = 0; s < g.nsc; ++s)
+        for (int j = 0; j <= sc_units(g, s); ++j)
+          prefetch_l2(tile + (size_t)s * g.sc_bytes + 512 * j + 16 * ln);
+    }
     for (int i = tid; i < n * (K / 64); i += kTcProducers)
       prefetch_l2(bsrc + (size_t)sh->tok[i / (K / 64)] * bld + 64 * (i % (K / 64)));
     const uint32_t a_s = smem_u32(A), b_s = smem_u32(B), raw_s = smem_u32(RAW);
     auto issue = [&](int c) {  // chunk c's copies into stage c % stages
       const int stage = c % kTcStages, s = c >> 3, j = c & 7;
-      cp_async16(raw_s + stage * kTcRawStageBytes + 16 * u,
-                 tile + (size_t)s * g.sc_bytes + 512 * (1 + j) + 16 * ln);
+      if (MODE == 2) {  // router rows straight into the swizzled A stage
+        for (int v = tid; v < kTcM * 8; v += kTcProducers) {
+          const int r = v >> 3, c16 = v & 7;
+          cp_async16(a_s + stage * kTcAStageBytes + swz(r, c16),
+                     arow + (size_t)r * p.H + c * kTcK + 8 * c16);
+        }
+      } else {
+        cp_async16(raw_s + stage * kTcRawStageBytes + 16 * u,
+                   tile + (size_t)s * g.sc_bytes + 512 * (1 + j) + 16 * ln);
+      }
       const uint32_t bs = b_s + stage * b_stage;
       for (int v = tid; v < n * 8; v += kTcProducers) {
         const int r = v >> 3, c16 = v & 7;
@@ -272,12 +298,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
       if (c < KC) issue(c);
       cp_async_commit();
     }
-    uint4 sv = ldg_stream(tile + 16 * ln), sv_next = sv;
+    uint4 sv = make_uint4(0, 0, 0, 0), sv_next = sv;
+    if (MODE != 2) sv = sv_next = ldg_stream(tile + 16 * ln);
     for (int c = 0; c < KC; ++c) {
       const int stage = c % kTcStages, s = c >> 3, j = c & 7;
-      if (j == 0 && c > 0) sv = sv_next;
-      if (j == 4 && s + 1 < g.nsc) sv_next = ldg_stream(tile + (size_t)(s + 1) * g.sc_bytes + 16 * ln);
+      if (MODE != 2) {
+        if (j == 0 && c > 0) sv = sv_next;
+        if (j == 4 && s + 1 < g.nsc) sv_next = ldg_stream(tile + (size_t)(s + 1) * g.sc_bytes + 16 * ln);
+      }
       cp_async_wait<kTcLookahead - 1>();  // this thread's copies of chunk c have landed
+      if (MODE == 2) {  // nothing to dequantise
+        fence_async_smem();
+        mbar_arrive(&sh->full[stage]);
+        const int cn = c + kTcLookahead;
+        if (cn < KC) {
+          if (!mbar_wait(&sh->empty[cn % kTcStages], ((cn / kTcStages) & 1) ^ 1, abort)) break;
+          issue(cn);
+        }
+        cp_async_commit();
+        continue;
+      }
       const uint4 cv = *reinterpret_cast<const uint4*>(RAW + stage * kTcRawStageBytes + 16 * u);
       const uint32_t sp = e4m3x2_to_f16x2((u4get(sv, j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
       const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
@@ -308,9 +348,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
       cp_async_commit();
     }
     cp_async_wait<0>();
-  } else if (lane == 0) {
+  } else {
+    if (lane == 0) {
     // ---------------------------------------------------------------- MMA issue
-    const uint32_t idesc = idesc_f16(kTcM, n_pad);
+    const uint32_t idesc = idesc_f16(kTcM, n_pad) | (MODE == 2 ? (1u << 7) | (1u << 10) : 0u);  // bf16
     const uint32_t a_s = smem_u32(A), b_s = smem_u32(B);
     for (int c = 0; c < KC; ++c) {
       const int stage = c % kTcStages;
@@ -324,11 +365,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
       umma_commit(&sh->empty[stage]);
     }
     umma_commit(&sh->acc_full);  // fires once every issued MMA is done
+    }
+    __syncwarp();  // the other lanes of the MMA warp idle here instead of polling
   }
 
   // ---------------------------------------------------------------- epilogue
-  const bool ok = mbar_wait(&sh->acc_full, 0, abort);
-  if (!ok) {
+  // (the MMA warp goes straight to the final barrier: the epilogue warps only
+  // pass it once acc_full says every MMA has completed)
+  bool ok = true;
+  if (warp < 8) ok = mbar_wait(&sh->acc_full, 0, abort);
+  if (warp < 8 && !ok) {
     // wait (bounded) for the MMAs already in flight before freeing TMEM
     const long long t0 = clock64();
     while (!mbar_test(&sh->acc_full, 0) && clock64() - t0 < kWaitBudget) {
@@ -355,6 +401,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
             const float a = G / (1.0f + expf(-G)) * U;
             p.abuf[(size_t)(row0 + col) * p.I + i] = __half_as_ushort(__float2half_rn(a));
           }
+        }
+      }
+    } else if (MODE == 2) {
+      const int e = kTcM * mb + r;
+      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
+        uint32_t v[32];
+        tmem_ld32(tmem_d + lane_addr + c0, v);
+#pragma unroll
+        for (int qq = 0; qq < 32; ++qq) {
+          const int col = c0 + qq;
+          if (col < n) p.logits_out[(size_t)(row0 + col) * p.E + e] = __uint_as_float(v[qq]);
         }
       }
     } else {
@@ -409,11 +466,22 @@ cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, cudaStream_t st) {
   return launch_k(tc_gemm_kernel<1>, grid, dim3(kTcThreads), tc_smem(), st, true, p);
 }
 
+bool tc_router_ok(int E, int H) { return E % kTcM == 0 && H % kTcK == 0; }
+
+// logits_out gets the fp32 dot products (one K slice: the top-k step adds the bias)
+cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st) {
+  dim3 grid(p.E / kTcM, (p.T + kTcMaxN - 1) / kTcMaxN);
+  return launch_k(tc_gemm_kernel<2>, grid, dim3(kTcThreads), tc_smem(), st, true, p);
+}
+
 cudaError_t tc_kernels_init() {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)tc_smem());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tc_smem());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tc_smem());
 }
 

@@ -68,7 +68,17 @@ def test_tensor_core_path_small_layer(T):
     compare_layer(w, L, gen.x_tokens(w, T))
 
 
-@pytest.mark.parametrize("fused", [1, 0])
+@pytest.mark.parametrize("T", [1024, 1100])
+def test_tensor_core_router_small_layer(T):
+    """128 experts: the router runs as a bf16 tcgen05 GEMM (one 128-expert block,
+    token tiles of 128 with a ragged last one), ahead of the grouped expert GEMMs."""
+    w = small(fmt=1, H=256, I=128, E=128, k=2, T=T, seed=7)
+    L = layer(w)
+    assert L.launches(T) == 7  # convert x, tc router, top-k, dispatch, tc gate/up, tc down, combine
+    compare_layer(w, L, gen.x_tokens(w, T))
+
+
+@pytest.mark.parametrize("fused", [0, 1])
 def test_decode_nvfp4_full_size(fused):
     w = gen.get_workload(1)
     L = layer(w)
@@ -78,7 +88,7 @@ def test_decode_nvfp4_full_size(fused):
         rel, ties = compare_layer(w, L, gen.x_tokens(w))
         print(f"decode nvfp4 (fused={fused}): rel-L2 {rel:.2e}, near ties {ties}")
     finally:
-        L.set_option(moe.OPT_DECODE_FUSED, 1)
+        L.set_option(moe.OPT_DECODE_FUSED, 0)
 
 
 @pytest.mark.parametrize("T", [1, 3, 8])
@@ -89,11 +99,11 @@ def test_decode_fused_and_chained_paths_agree_bit_for_bit(T):
     L = layer(w)
     x = gen.x_tokens(w, T)
     a = run_gpu(L, x, w)
-    L.set_option(moe.OPT_DECODE_FUSED, 0)
+    L.set_option(moe.OPT_DECODE_FUSED, 1)
     try:
         b = run_gpu(L, x, w)
     finally:
-        L.set_option(moe.OPT_DECODE_FUSED, 1)
+        L.set_option(moe.OPT_DECODE_FUSED, 0)
     for key in ("out", "logits", "idx", "gates", "counts", "offsets", "perm"):
         assert np.array_equal(a[key], b[key]), key
 
@@ -106,7 +116,7 @@ def test_decode_fp6_full_size():
         print(f"decode fp6: rel-L2 {rel:.2e}, near ties {ties}")
         x = gen.x_tokens(w)
         a = run_gpu(L, x, w)
-        L.set_option(moe.OPT_DECODE_FUSED, 0)
+        L.set_option(moe.OPT_DECODE_FUSED, 1)
         b = run_gpu(L, x, w)
         assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["idx"], b["idx"])
     finally:

@@ -38,6 +38,7 @@ METRIC = "routed tokens/s per MoE layer on 1 GB300; HBM GB/s as % of ~8 TB/s roo
 UNIT = "tokens/s"
 WORKLOAD = 1  # decode-h2048-i512-e512-k10-s1-t1-nvfp4
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -60,19 +61,43 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
-def peaks():
+def peaks(kind="hbm"):
+    """Roofline denominator: HBM copy GB/s, or dense bf16 TFLOP/s (burst: the
+    kernel is timed alone; f16 runs at the bf16 rate on this tensor core)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(p) as f:
             d = json.load(f)
+        if kind == "tensor":
+            return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS; f16 = bf16 rate)"
         return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
     except Exception:
+        if kind == "tensor":
+            return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s (no MEASURED_PEAKS.json)"
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def packed_gateup_bytes(w):
+    """Bytes of one expert's packed gate + up tiles (layout.cuh)."""
+    if w.fmt == 1:
+        units = w.H // 64
+        tile = 512 * ((units + 7) // 8 + units)
+    else:
+        units = w.H // 128
+        tile = 128 * ((units + 7) // 8) + 1536 * units
+    return (w.I // 16) * 2 * tile
+
+
+def tc_path(w, T):
+    """The forward takes the tcgen05 grouped GEMMs (NVFP4, >= 16 routed slots per expert)."""
+    return w.fmt == 1 and T * w.k >= 16 * w.E and w.H % 128 == 0 and (2 * w.I) % 128 == 0
 
 
 def config_block(w, L, extra=None):
     c = {"workload": w.name, "H": w.H, "I": w.I, "E": w.E, "k": w.k, "shared_experts": w.shared,
-         "tokens_per_step": w.T, "format": "nvfp4 (e2m1, e4m3 per 16, fp32 tensor scale)",
+         "tokens_per_step": w.T,
+         "format": ("nvfp4 (e2m1, e4m3 per 16, fp32 tensor scale)" if w.fmt == 1
+                    else "fp6 e2m3 (power-of-two scale per 128)"),
          "layer_instances_per_step": L, "l2": "inputs larger than L2 (distinct weights per layer)"}
     if extra:
         c.update(extra)
@@ -215,11 +240,11 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def traffic_from_profile(kernel, csrc):
-    """dram bytes per launch of `kernel` from its committed ncu summary, or None
-    when any kernel source changed since the capture (the summary records a
-    hash of csrc/*)."""
-    p = os.path.join(ROOT, "profiles", f"{kernel}_decode-h2048-e512-k10-t1.md")
+def traffic_from_profile(kernel, workload, csrc):
+    """dram bytes per launch of `kernel` on `workload` from its committed ncu
+    summary, or None when any kernel source changed since the capture (the
+    summary records a hash of csrc/*)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         txt = open(p).read()
         sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt).group(1)
@@ -317,32 +342,31 @@ def run_ours(args, w):
         ms = float(t.item())
     value = world * T * Ln * args.steps / (ms / 1e3)
 
-    # dominant kernel, timed alone over the L layers (graph of back-to-back launches,
-    # launch gaps included): the whole-layer decode kernel when a forward is one
-    # launch, else gate/up + SwiGLU
-    n_launch = layers[0].launches(T)
-    one_kernel = n_launch == 1
+    # dominant kernel, timed alone over the L layers (graph of back-to-back
+    # launches, launch gaps included): gate/up + SwiGLU, the tcgen05 GEMM for
+    # prefill (tensor-bound) or the streaming kernel otherwise (HBM-bound)
     counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
-    arena, expert_bytes = layers[0].info()
-    gu_bytes = (w.I // 16) * 2 * (w.H // 64 + (w.H // 64 + 7) // 8) * 512 if w.fmt == 1 else None
-    per_launch_bytes = []
+    tc = tc_path(w, T)
+    gu = packed_gateup_bytes(w)
+    per_launch = []
     with torch.cuda.stream(s):
         for L, o in zip(layers, outs):
             L.forward(x, o, stream=s)
             L.debug_routing(counts=counts, stream=s)
             s.synchronize()
-            D = int((counts > 0).sum().item()) + w.shared
-            if one_kernel:  # every byte the layer must move once
-                b = D * (expert_bytes + 12) + w.E * w.H * 2 + (w.E * 4 if w.bias != "none" else 0)
-                per_launch_bytes.append(b + T * w.H * 2 + T * w.H * 4)
-            else:
-                per_launch_bytes.append(D * (gu_bytes + 8) + T * w.H * 2 +
-                                        (T * w.k + T * w.shared) * w.I * 2)
-    kphase = 0 if one_kernel else 2
+            c = counts.cpu().numpy()
+            D = int((c > 0).sum()) + w.shared
+            if tc:  # FLOPs of the contraction (N padded to 16 per work item as the MMA runs it)
+                n = [int(v) for v in c if v > 0] + [T] * w.shared
+                cols = sum(((min(128, v - 128 * j) + 15) // 16) * 16
+                           for v in n for j in range((v + 127) // 128))
+                per_launch.append(2.0 * cols * 2 * w.I * w.H)
+            else:  # unique weight bytes, x, and a
+                per_launch.append(D * (gu + 8) + T * w.H * 2 + (T * w.k + T * w.shared) * w.I * 2)
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk, stream=s):
         for L, o in zip(layers, outs):
-            L.run_phase(kphase, x, o, stream=s)
+            L.run_phase(2, x, o, stream=s)
     reps = max(20, min(500, args.steps))
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
@@ -354,17 +378,25 @@ def run_ours(args, w):
         k1.record(s)
     torch.cuda.synchronize()
     k_us = k0.elapsed_time(k1) * 1e3 / (reps * Ln)
-    bytes_launch = sum(per_launch_bytes) / len(per_launch_bytes)
-    peak, peak_kind = peaks()
-    achieved = bytes_launch / (k_us * 1e-6) / 1e9
-    kname = "decode_kernel" if one_kernel else "gateup_kernel"
-    traffic = traffic_from_profile(kname, os.path.join(ROOT, "quantized_moe_expert_layer_gb300",
-                                                       "csrc"))
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": k_us,
-                "peak_source": peak_kind,
-                "timing": "CUDA events over a graph of back-to-back launches, gaps included"}
+    work = sum(per_launch) / len(per_launch)
+    if tc:
+        kname = "tc_gemm_kernel"
+        peak, peak_kind = peaks("tensor")
+        achieved = work / (k_us * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "kernel": kname + "<0> (gate/up + SwiGLU)", "achieved": achieved,
+                    "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                    "algorithmic_flops_per_launch": work}
+    else:
+        kname = "stream_gateup_kernel"
+        peak, peak_kind = peaks("hbm")
+        achieved = work / (k_us * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "kernel": kname + " (gate/up + SwiGLU)", "achieved": achieved,
+                    "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "algorithmic_bytes_per_launch": work}
+    roofline.update({"traffic": traffic_from_profile(kname, w.name, os.path.join(
+                         ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
+                     "avg_launch_us": k_us, "peak_source": peak_kind,
+                     "timing": "CUDA events over a graph of back-to-back launches, gaps included"})
 
     # steady-state time of each phase alone (graphs of L back-to-back launches)
     phase_us = {}
@@ -407,7 +439,7 @@ def run_ours(args, w):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (nvfp4 weights)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (" + ("nvfp4" if w.fmt == 1 else "fp6 e2m3") + " weights)",
             "data": "synthetic (seeded generator; random-init weights quantised on the device)",
             "config": config_block(w, Ln, {"us_per_layer": ms * 1e3 / (args.steps * Ln),
                                            "phase_us_alone": phase_us,

@@ -1,5 +1,6 @@
 // Device code of the routing step (router partial sums, top-k, dispatch),
-// shared by the stand-alone routing kernels and the decode megakernel.
+// shared by the routing kernels and the small-batch expert kernels, which
+// route a few tokens themselves.
 #pragma once
 
 #include <climits>
@@ -10,8 +11,9 @@
 namespace moe {
 namespace {
 
-constexpr int kRouterThreads = 256;  // the decode megakernel's block size: same partial-sum order
+constexpr int kRouterThreads = 256;
 constexpr int kFinishThreads = 1024;
+constexpr int kMaxKsplit = 8;  // router K slices at most
 
 // ---------------------------------------------------------------- router logits
 // ---------------------------------------------------------------- router logits
@@ -34,11 +36,30 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
   const int e0 = 16 * tile + gi, e1 = e0 + 8;
   const uint16_t* r0 = p.wr + (size_t)min(e0, p.E - 1) * p.H;
   const uint16_t* r1 = p.wr + (size_t)min(e1, p.E - 1) * p.H;
-  // start the router-weight reads before the activations are staged
-  for (int c = c_begin + warp; c < c_end; c += nwarps) {
-    prefetch_l2(r0 + 64 * c + 16 * t);
-    prefetch_l2(r1 + 64 * c + 16 * t);
+  // The router weights do not depend on earlier kernels: the warp's first
+  // chunk is loaded, and the rest requested from L2, before waiting for them.
+  auto load_a = [&](int c, uint32_t (&ra)[8], uint32_t (&rb)[8]) {
+    const int kc = 64 * c + 16 * t;
+    uint4 a00 = ldg_stream(r0 + kc), a01 = ldg_stream(r0 + kc + 8);
+    uint4 a10 = ldg_stream(r1 + kc), a11 = ldg_stream(r1 + kc + 8);
+    if (e0 >= p.E) a00 = a01 = make_uint4(0, 0, 0, 0);
+    if (e1 >= p.E) a10 = a11 = make_uint4(0, 0, 0, 0);
+    ra[0] = a00.x; ra[1] = a00.y; ra[2] = a00.z; ra[3] = a00.w;
+    ra[4] = a01.x; ra[5] = a01.y; ra[6] = a01.z; ra[7] = a01.w;
+    rb[0] = a10.x; rb[1] = a10.y; rb[2] = a10.z; rb[3] = a10.w;
+    rb[4] = a11.x; rb[5] = a11.y; rb[6] = a11.z; rb[7] = a11.w;
+  };
+  uint32_t ra[8], rb[8];
+  int c = c_begin + warp;
+  if (c < c_end) load_a(c, ra, rb);
+  for (int cc = c + nwarps; cc < c_end; cc += nwarps) {
+    prefetch_l2(r0 + 64 * cc + 16 * t);
+    prefetch_l2(r1 + 64 * cc + 16 * t);
   }
+  // x (and everything written below) waits for the kernels before this one;
+  // the next kernel may start once every CTA is past this point
+  griddep_wait();
+  griddep_launch();
   const bool write_xh = p.xh != nullptr && tile == 0;
   for (int i = threadIdx.x; i < n * (klen / 8); i += blockDim.x) {
     const int r = i / (klen / 8), v = i % (klen / 8);
@@ -60,14 +81,8 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
   __syncthreads();
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c = c_begin + warp; c < c_end; c += nwarps) {
+  for (; c < c_end; c += nwarps) {
     const int kc = 64 * c + 16 * t;
-    uint4 a00 = ldg_stream(r0 + kc), a01 = ldg_stream(r0 + kc + 8);
-    uint4 a10 = ldg_stream(r1 + kc), a11 = ldg_stream(r1 + kc + 8);
-    if (e0 >= p.E) a00 = a01 = make_uint4(0, 0, 0, 0);
-    if (e1 >= p.E) a10 = a11 = make_uint4(0, 0, 0, 0);
-    const uint32_t ra[8] = {a00.x, a00.y, a00.z, a00.w, a01.x, a01.y, a01.z, a01.w};
-    const uint32_t rb[8] = {a10.x, a10.y, a10.z, a10.w, a11.x, a11.y, a11.z, a11.w};
     uint32_t xw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (gi < n) {
       const uint4* px = reinterpret_cast<const uint4*>(xs + gi * stride + (kc - kbase));
@@ -80,6 +95,7 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
       const uint32_t a[4] = {ra[2 * w], rb[2 * w], ra[2 * w + 1], rb[2 * w + 1]};
       mma_bf16(acc, a, xw[2 * w], xw[2 * w + 1]);
     }
+    if (c + nwarps < c_end) load_a(c + nwarps, ra, rb);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) red[(warp * 32 + lane) * 4 + i] = acc[i];
@@ -98,10 +114,6 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
   }
 }
 
-// grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); 4 warps split
-// the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
-// (ksplit slice, token, expert) partial sum goes to p.partial; the top-k step
-// adds the slices in a fixed order.
 // ---------------------------------------------------------------- top-k (one warp per token)
 // Order-preserving map of an fp32 value to a uint32 key (larger value, larger key).
 __device__ __forceinline__ uint32_t f32_key(float v) {
@@ -140,11 +152,27 @@ __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0,
   float v[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) v[i] = 0.f;
-  for (int s = 0; s < p.ksplit; ++s) {
-    const float* ps = p.partial + ((size_t)s * p.T + t) * p.E;
+  if constexpr (V <= 4) {  // few slots: every slice requested at once
+    float part[kMaxKsplit][V];
 #pragma unroll
-    for (int i = 0; i < V; ++i)  // written by other CTAs: read through L2
-      if (e0 + lane + 32 * i < e_end) v[i] += __ldcg(ps + e0 + lane + 32 * i);
+    for (int s = 0; s < kMaxKsplit; ++s)
+#pragma unroll
+      for (int i = 0; i < V; ++i) {  // written by other CTAs: read through L2
+        const float* ps = p.partial + ((size_t)s * p.T + t) * p.E;
+        part[s][i] = (s < p.ksplit && e0 + lane + 32 * i < e_end) ? __ldcg(ps + e0 + lane + 32 * i) : 0.f;
+      }
+#pragma unroll
+    for (int s = 0; s < kMaxKsplit; ++s)  // slices added in order
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (s < p.ksplit) v[i] += part[s][i];
+  } else {
+    for (int s = 0; s < p.ksplit; ++s) {
+      const float* ps = p.partial + ((size_t)s * p.T + t) * p.E;
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (e0 + lane + 32 * i < e_end) v[i] += __ldcg(ps + e0 + lane + 32 * i);
+    }
   }
 #pragma unroll
   for (int i = 0; i < V; ++i) {
@@ -426,6 +454,113 @@ __device__ void dispatch_small(const RouteParams& p, int* smem, int* sidx) {
   for (int t = tid; t < p.T; t += nt) p.row_token[S + t] = t;
 }
 
+
+// ---------------------------------------------------------------- routing of a few tokens by one CTA
+// For T <= kTokTile tokens no expert can receive more than kTokTile slots, so
+// every routed expert is exactly one work entry.  The small-batch expert
+// kernels route in every CTA from the router's partial sums (a few KB read
+// through L2) instead of waiting for a separate routing kernel.
+struct SmallRoute {
+  int4 entries[kSmallSlots];  // {expert, first row, tokens, 0}, expert order
+  int inv[kSmallSlots];       // row of each slot
+  int row_token[kSmallSlots + kTokTile];
+  float gates[kSmallSlots];
+  int sidx[kSmallSlots];      // expert of each slot
+  int lt[kSmallSlots];        // per slot: slots with a smaller expert id
+  int cnt[kSmallSlots];       // per slot: slots with the same expert
+  int lead[kSmallSlots];      // per slot: first slot of its expert
+  uint32_t ck[16 * kMaxK];    // per-warp top-k candidates (T == 1)
+  int ci[16 * kMaxK];
+  int n_entries;
+};
+
+// Top-k, gates and the stable expert-major dispatch of T <= kTokTile tokens,
+// T * k <= min(kSmallSlots, blockDim.x), by every thread of the block (at most
+// 16 warps); results in r, and in the global outputs of p that are non-null
+// (logits, idx, gates, perm, inv, row_token, entries, n_entries).  Row of slot
+// s: pos(s) = #{q : e_q < e_s} + #{q < s : e_q == e_s}, which is the dispatch
+// of dispatch_block.  Ends synchronised.
+template <int V2>
+__device__ void topk_one_token_cta(const RouteParams& p, SmallRoute& r) {
+  const int NW = blockDim.x >> 5, q = (p.E + NW - 1) / NW;
+  if (q <= 32)
+    topk_token_cta<1, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates);
+  else if (q <= 64)
+    topk_token_cta<2, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates);
+  else
+    topk_token_cta<4, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates);
+}
+
+__device__ void route_small_cta(const RouteParams& p, SmallRoute& r) {
+  const int T = p.T, k = p.k, S = T * k;
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31, NW = nt >> 5;
+  if (T == 1) {  // all warps share the token: E / NW experts each, then one merge
+    if (NW * k <= 32 * 3)
+      topk_one_token_cta<3>(p, r);
+    else if (NW * k <= 32 * 9)
+      topk_one_token_cta<9>(p, r);
+    else
+      topk_one_token_cta<16>(p, r);
+  } else {  // one warp per token
+    for (int t = warp; t < T; t += NW) topk_token(p, t, lane, r.sidx, r.gates);
+    __syncthreads();
+  }
+  int is_lead = 0;
+  for (int s = tid; s < S; s += nt) {
+    const int e = r.sidx[s];
+    int lt = 0, before = 0, cnt = 0;
+    for (int q = 0; q < S; ++q) {
+      const int f = r.sidx[q];
+      lt += f < e;
+      cnt += f == e;
+      before += (f == e) & (q < s);
+    }
+    const int pos = lt + before;
+    r.inv[s] = pos;
+    r.row_token[pos] = s / k;
+    r.lt[s] = lt;
+    r.cnt[s] = cnt;
+    r.lead[s] = before == 0;
+    is_lead = before == 0;
+    if (p.perm) p.perm[pos] = s;
+    if (p.inv) p.inv[s] = pos;
+    if (p.row_token) p.row_token[pos] = s / k;
+  }
+  for (int t = tid; t < T; t += nt) {
+    r.row_token[S + t] = t;
+    if (p.row_token) p.row_token[S + t] = t;
+  }
+  const int n_ent = __syncthreads_count(is_lead);  // one slot per thread at most
+  for (int s = tid; s < S; s += nt) {
+    if (!r.lead[s]) continue;
+    const int e = r.sidx[s];
+    int d = 0;
+    for (int q = 0; q < S; ++q) d += r.lead[q] & (r.sidx[q] < e);
+    const int4 en = make_int4(e, r.lt[s], r.cnt[s], 0);
+    r.entries[d] = en;
+    if (p.entries) p.entries[d] = en;
+  }
+  if (tid == 0) {
+    r.n_entries = n_ent;
+    if (p.n_entries) *p.n_entries = n_ent;
+  }
+  __syncthreads();
+}
+
+// counts[E] and offsets[E + 1] of a routing held in r (diagnostic outputs).
+__device__ void publish_counts(const RouteParams& p, const SmallRoute& r) {
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    int c = 0, off = 0;
+    for (int d = 0; d < r.n_entries; ++d) {
+      const int4 en = r.entries[d];
+      c += en.x == e ? en.z : 0;
+      off += en.x < e ? en.z : 0;
+    }
+    if (p.counts) p.counts[e] = c;
+    if (p.offsets) p.offsets[e] = off;
+  }
+  if (threadIdx.x == 0 && p.offsets) p.offsets[p.E] = p.T * p.k;
+}
 
 }  // namespace
 }  // namespace moe

@@ -23,6 +23,7 @@
 // Every wait is bounded: on a timeout the kernel records MOE_ETIMEOUT in the
 // status word, stops issuing work, waits (bounded) for its MMAs, frees its
 // TMEM and returns.
+#include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 #include "layout.cuh"
@@ -39,43 +40,6 @@ constexpr int kTcThreads = 288;      // + warp 8: TMEM allocation and MMA issue
 constexpr int kTcAStageBytes = kTcM * kTcK * 2;     // 16 KB of dequantised f16 weights
 constexpr int kTcRawStageBytes = 8 * 512;           // 4 KB of packed codes (8 tiles)
 constexpr int kTcBStageBytes = kTcMaxN * kTcK * 2;  // 16 KB of f16 token rows
-constexpr long long kWaitBudget = 2000000000LL;      // ~1 s of clock64 per wait
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// ---------------------------------------------------------------- mbarrier
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of the given parity to complete.  Returns false
-// (after setting *abort) on timeout, or at once if another thread aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const long long t0 = clock64();
-  while (!mbar_test(bar, parity)) {
-    if (*abort) return false;
-    if (clock64() - t0 > kWaitBudget) {
-      *abort = 1;
-      return false;
-    }
-  }
-  return true;
-}
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tc_fence_before() {
@@ -83,9 +47,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {  // one full warp
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
@@ -151,14 +112,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 struct TcShared {
   uint64_t full[kTcStages];
   uint64_t empty[kTcStages];
@@ -236,7 +189,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
     }
     mbar_init(&sh->acc_full, 1);
     sh->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   for (int i = tid; i < n_pad; i += kTcThreads) {
     int tk = 0;
@@ -376,9 +329,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
   if (warp < 8) ok = mbar_wait(&sh->acc_full, 0, abort);
   if (warp < 8 && !ok) {
     // wait (bounded) for the MMAs already in flight before freeing TMEM
-    const long long t0 = clock64();
-    while (!mbar_test(&sh->acc_full, 0) && clock64() - t0 < kWaitBudget) {
-    }
+    mbar_drain(&sh->acc_full, 0);
   }
   tc_fence_after();
   if (warp < 8 && ok && !*abort) {

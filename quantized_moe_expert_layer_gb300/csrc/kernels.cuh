@@ -101,15 +101,21 @@ struct StreamGeom {
   int sc_bytes;     // bytes of a full super-chunk
   int tile_bytes;
   int unit_cols, unit_bytes, hdr_bytes;  // per unit; the scale vector heading a super-chunk
-  int stage_units;  // units of one super-chunk per ring stage
-  int tile_w;       // bytes of one tile's part of a stage
-  int w_bytes;      // weight bytes of a stage (all tiles)
-  int seg_stride;   // bytes per activation row in a stage (16 bytes of padding)
+  int pair_stage;   // 1: a stage is a whole gate/up tile pair (one contiguous copy)
+  int sc_run;       // else: super-chunks of one tile per stage
+  int w_cap;        // weight bytes of a stage at most
+  int b_once;       // 1: the activation rows are staged once per CTA; 0: with every stage
+  int b_stride;     // bytes per activation row (staged once: K * 2; per stage: its columns + 16)
+  int b_bytes;      // staged-once activation area
   int n_max;        // activation rows per item at most
   int stage_bytes, n_stages;
+  int ts_bytes;     // the tensor-scale table staged in shared memory
 };
 constexpr int kStreamMaxDyn = 192 * 1024;  // dynamic shared memory per CTA at most (static: < 34 KB)
-StreamGeom stream_geom(int fmt, int K, int tiles, int n_max, int stage_units, int ring_bytes);
+constexpr int kStreamOnceMax = 64 * 1024;  // activations staged once per CTA at most
+// bytes of the tensor-scale table of n experts (3 fp32 each), padded to 16
+inline int tscale_bytes(int n_experts) { return (n_experts * 3 * 4 + 15) / 16 * 16; }
+StreamGeom stream_geom(int fmt, int K, int tiles, int n_max, int b_rows, int ring_bytes, int n_experts);
 size_t stream_smem(const StreamGeom& g, int ys_rows);
 bool stream_small_ok(int T, int k);
 cudaError_t launch_stream_gateup(const ExpertParams& p, const RouteParams& rp, const StreamGeom& g,

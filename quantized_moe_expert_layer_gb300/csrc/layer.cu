@@ -203,8 +203,11 @@ bool tc_path(moe_layer* L, int T) { return tc_path_ok(L->fmt, T, L->k, L->E, L->
 // dispatch as usual (the GEMM's output is the one K slice the top-k reads)
 bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E, L->H); }
 
-// T <= 8: the streaming expert kernels route themselves (router -> gate/up -> down + combine)
-bool small_path(moe_layer* L, int T) { return stream_small_ok(T, L->k); }
+// T <= 8 (and x small enough to stage once per CTA): the streaming expert
+// kernels route themselves (router -> gate/up -> down + combine)
+bool small_path(moe_layer* L, int T) {
+  return stream_small_ok(T, L->k) && (long)T * L->H * 2 <= kStreamOnceMax;
+}
 
 int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
@@ -216,17 +219,17 @@ int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t 
 
 // Ring geometry of the streaming kernels.  Two CTAs (gate/up and down, which
 // overlap) share an SM, so each takes well under half of its shared memory.
-// FP6 stages hold half a super-chunk (4 pairs of 128 columns) so that several
-// stages fit.
-StreamGeom gu_geom(moe_layer* L, int T) {
+// The routing variants stage their activation rows once per CTA (x for
+// gate/up, every row of a for down, when it fits).
+StreamGeom gu_geom(moe_layer* L, int T, bool route) {
   const int ring = L->ring_kb > 0 ? L->ring_kb * 1024 : 80 * 1024;
   const int n_max = T < kTokTile ? T : kTokTile;
-  return stream_geom(L->fmt, L->H, 2, n_max, L->fmt == MOE_FMT_NVFP4 ? 8 : 4, ring);
+  return stream_geom(L->fmt, L->H, 2, n_max, route ? T : 0, ring, L->E + L->shared);
 }
-StreamGeom dn_geom(moe_layer* L, int T) {
-  const int ring = L->ring_kb > 0 ? L->ring_kb * 1024 : 80 * 1024;
+StreamGeom dn_geom(moe_layer* L, int T, bool route) {
+  const int ring = L->ring_kb > 0 ? L->ring_kb * 1024 : 64 * 1024;
   const int n_max = T < kTokTile ? T : kTokTile;
-  return stream_geom(L->fmt, L->I, 1, n_max, L->fmt == MOE_FMT_NVFP4 ? 8 : 4, ring);
+  return stream_geom(L->fmt, L->I, 1, n_max, route ? T * L->k + T : 0, ring, L->E + L->shared);
 }
 
 // experts + combine, after routing has filled idx / gates / dispatch
@@ -240,8 +243,8 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
     return MOE_OK;
   }
   RouteParams rp = route_params(L, x, T);
-  CK("gate/up kernel launch", launch_stream_gateup(ep, rp, gu_geom(L, T), false, st));
-  CK("down kernel launch", launch_stream_down(ep, rp, dn_geom(L, T), false, nullptr, st));
+  CK("gate/up kernel launch", launch_stream_gateup(ep, rp, gu_geom(L, T, false), false, st));
+  CK("down kernel launch", launch_stream_down(ep, rp, dn_geom(L, T, false), false, nullptr, st));
   CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
   return MOE_OK;
 }
@@ -260,8 +263,8 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
   if (small_path(L, T)) {
     ExpertParams ep = expert_params(L, x, T);
     CK("router kernel launch", launch_router(rp, st));
-    CK("gate/up kernel launch", launch_stream_gateup(ep, rp, gu_geom(L, T), true, st));
-    CK("down kernel launch", launch_stream_down(ep, rp, dn_geom(L, T), true, out, st));
+    CK("gate/up kernel launch", launch_stream_gateup(ep, rp, gu_geom(L, T, true), true, st));
+    CK("down kernel launch", launch_stream_down(ep, rp, dn_geom(L, T, true), true, out, st));
     return MOE_OK;
   }
   if (tc_router(L, T)) {
@@ -318,7 +321,7 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   const int n_total = E + shared;
   L->arena_bytes = (uint64_t)n_total * L->geom.expert_bytes;
   if (cudaMalloc(&L->arena, L->arena_bytes) != cudaSuccess ||
-      cudaMalloc(&L->tscale, sizeof(float) * 3 * n_total) != cudaSuccess ||
+      cudaMalloc(&L->tscale, tscale_bytes(n_total)) != cudaSuccess ||  // padded: copied whole
       cudaMalloc(&L->router, sizeof(uint16_t) * (size_t)E * H) != cudaSuccess ||
       cudaMalloc(&L->bias, sizeof(float) * E) != cudaSuccess ||
       cudaMalloc(&L->status, sizeof(int)) != cudaSuccess) {
@@ -328,7 +331,7 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
                 L ? (double)L->arena_bytes / 1e6 : 0.0);
   }
   if (cudaMemset(L->arena, 0, L->arena_bytes) != cudaSuccess ||
-      cudaMemset(L->tscale, 0, sizeof(float) * 3 * n_total) != cudaSuccess ||
+      cudaMemset(L->tscale, 0, tscale_bytes(n_total)) != cudaSuccess ||
       cudaMemset(L->status, 0, sizeof(int)) != cudaSuccess) {
     moe_layer_destroy(L);
     return fail(MOE_ECUDA, "moe_layer_create: cudaMemset failed");
@@ -631,8 +634,8 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
   ExpertParams ep = expert_params(L, x, T);
   if (small_path(L, T)) {  // router; gate/up (routing inside); down + combine (routing inside)
     if (phase == 0) CK("router", launch_router(rp, st));
-    if (phase == 2) CK("gate/up", launch_stream_gateup(ep, rp, gu_geom(L, T), true, st));
-    if (phase == 3) CK("down", launch_stream_down(ep, rp, dn_geom(L, T), true, out, st));
+    if (phase == 2) CK("gate/up", launch_stream_gateup(ep, rp, gu_geom(L, T, true), true, st));
+    if (phase == 3) CK("down", launch_stream_down(ep, rp, dn_geom(L, T, true), true, out, st));
     if (phase < 0 || phase > 4) return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
     return MOE_OK;
   }
@@ -658,13 +661,13 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       if (tc)
         CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
       else
-        CK("gate/up", launch_stream_gateup(ep, rp, gu_geom(L, T), false, st));
+        CK("gate/up", launch_stream_gateup(ep, rp, gu_geom(L, T, false), false, st));
       break;
     case 3:
       if (tc)
         CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
       else
-        CK("down", launch_stream_down(ep, rp, dn_geom(L, T), false, nullptr, st));
+        CK("down", launch_stream_down(ep, rp, dn_geom(L, T, false), false, nullptr, st));
       break;
     case 4:
       CK("combine", launch_combine(ep, L->gates, L->inv, out, false, st));

@@ -148,7 +148,8 @@ __device__ __forceinline__ void warp_argmax_round(uint32_t (&key)[V], const int 
 // router's K-split slices added in order, then the bias; written to p.logits.
 template <int V>
 __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0, int e_end,
-                                            int lane, uint32_t (&key)[V], int (&id)[V]) {
+                                            int lane, uint32_t (&key)[V], int (&id)[V],
+                                            bool pub = true) {
   float v[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) v[i] = 0.f;
@@ -181,7 +182,7 @@ __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0,
     if (e < e_end) {
       float l = v[i];
       if (p.bias) l = l + p.bias[e];
-      if (p.logits) p.logits[(size_t)t * p.E + e] = l;
+      if (pub && p.logits) p.logits[(size_t)t * p.E + e] = l;
       key[i] = f32_key(l);
     } else {
       key[i] = 0u;  // below every real key
@@ -191,7 +192,8 @@ __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0,
 
 // Gates = softmax of the k selected logits (lane j < k holds pick j).
 __device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lane, uint32_t my_key,
-                                            int my_i, int* sidx, float* sgates = nullptr) {
+                                            int my_i, int* sidx, float* sgates = nullptr,
+                                            bool pub = true) {
   const int k = p.k;
   const float my_v = key_f32(my_key);
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
@@ -200,8 +202,8 @@ __device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lan
 #pragma unroll
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
-    if (p.idx) p.idx[(size_t)t * k + lane] = my_i;
-    if (p.gates) p.gates[(size_t)t * k + lane] = ex / sum;
+    if (pub && p.idx) p.idx[(size_t)t * k + lane] = my_i;
+    if (pub && p.gates) p.gates[(size_t)t * k + lane] = ex / sum;
     if (sidx) sidx[t * k + lane] = my_i;
     if (sgates) sgates[t * k + lane] = ex / sum;
   }
@@ -211,10 +213,10 @@ __device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lan
 // the lower expert index), then the softmax of the k selected logits.
 template <int V>
 __device__ void topk_token_v(const RouteParams& p, int t, int lane, int* sidx,
-                             float* sgates = nullptr) {
+                             float* sgates = nullptr, bool pub = true) {
   uint32_t key[V];
   int id[V];
-  load_logits<V>(p, t, 0, p.E, lane, key, id);
+  load_logits<V>(p, t, 0, p.E, lane, key, id, pub);
   uint32_t my_key = 0;
   int my_i = 0;
   for (int j = 0; j < p.k; ++j) {
@@ -226,17 +228,17 @@ __device__ void topk_token_v(const RouteParams& p, int t, int lane, int* sidx,
       my_i = win;
     }
   }
-  write_gates(p, t, lane, my_key, my_i, sidx, sgates);
+  write_gates(p, t, lane, my_key, my_i, sidx, sgates, pub);
 }
 
 __device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx,
-                           float* sgates = nullptr) {
+                           float* sgates = nullptr, bool pub = true) {
   if (p.E <= 256)
-    topk_token_v<8>(p, t, lane, sidx, sgates);
+    topk_token_v<8>(p, t, lane, sidx, sgates, pub);
   else if (p.E <= 512)
-    topk_token_v<16>(p, t, lane, sidx, sgates);
+    topk_token_v<16>(p, t, lane, sidx, sgates, pub);
   else
-    topk_token_v<32>(p, t, lane, sidx, sgates);
+    topk_token_v<32>(p, t, lane, sidx, sgates, pub);
 }
 
 // Top-k of token t by all warps of the CTA: each of the NW warps takes a
@@ -246,12 +248,12 @@ __device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx,
 // ck / ci: NW * kMaxK entries of shared memory.
 template <int V1, int V2>
 __device__ void topk_token_cta(const RouteParams& p, int t, int* sidx, uint32_t* ck, int* ci,
-                               float* sgates = nullptr) {
+                               float* sgates = nullptr, bool pub = true) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, k = p.k, NW = blockDim.x >> 5;
   const int q = (p.E + NW - 1) / NW;
   uint32_t key[V1];
   int id[V1];
-  load_logits<V1>(p, t, warp * q, min(p.E, (warp + 1) * q), lane, key, id);
+  load_logits<V1>(p, t, warp * q, min(p.E, (warp + 1) * q), lane, key, id, pub);
   for (int j = 0; j < k; ++j) {
     uint32_t best;
     int win;
@@ -296,7 +298,7 @@ __device__ void topk_token_cta(const RouteParams& p, int t, int* sidx, uint32_t*
         my_i = win;
       }
     }
-    write_gates(p, t, lane, my_key, my_i, sidx, sgates);
+    write_gates(p, t, lane, my_key, my_i, sidx, sgates, pub);
   }
   __syncthreads();
 }
@@ -402,58 +404,8 @@ __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
   }
 }
 
-// Dispatch for a few slots (T*k <= kSmallSlots) by any block size: the same
-// result as dispatch_block (expert-major, stable), with a per-expert count
-// table and a direct stable rank.  smem: 64 + E + S ints.
+// slots of the few-token path (T * k at most)
 constexpr int kSmallSlots = 256;
-
-// sidx: the S expert ids in shared memory (already written and synchronised)
-__device__ void dispatch_small(const RouteParams& p, int* smem, int* sidx) {
-  const int S = p.T * p.k, E = p.E, nt = blockDim.x, tid = threadIdx.x;
-  int* sc = smem;
-  int* cnt = smem + 64;
-  for (int e = tid; e < E; e += nt) cnt[e] = 0;
-  for (int s = tid; s < S; s += nt) sidx[s] = checked_expert(p, sidx[s]);
-  __syncthreads();
-  for (int s = tid; s < S; s += nt) atomicAdd(&cnt[sidx[s]], 1);
-  __syncthreads();
-  const int ept = (E + nt - 1) / nt;
-  const int lo = min(E, tid * ept), hi = min(E, lo + ept);
-  int local = 0, lnch = 0;
-  for (int e = lo; e < hi; ++e) {
-    local += cnt[e];
-    lnch += (cnt[e] + kTokTile - 1) / kTokTile;
-  }
-  int total, n_total;
-  int run = block_excl_scan(local, sc, &total);
-  int runn = block_excl_scan(lnch, sc, &n_total);
-  for (int e = lo; e < hi; ++e) {
-    const int c = cnt[e];
-    if (p.counts) p.counts[e] = c;
-    if (p.offsets) p.offsets[e] = run;
-    for (int i = 0; i * kTokTile < c; ++i)
-      p.entries[runn + i] = make_int4(e, run + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
-    cnt[e] = run;
-    run += c;
-    runn += (c + kTokTile - 1) / kTokTile;
-  }
-  if (tid == 0) {
-    if (p.offsets) p.offsets[E] = total;
-    *p.n_entries = n_total;
-  }
-  __syncthreads();
-  for (int s = tid; s < S; s += nt) {
-    const int e = sidx[s];
-    int r = 0;
-    for (int q = 0; q < s; ++q) r += (sidx[q] == e);
-    const int pos = cnt[e] + r;
-    if (p.perm) p.perm[pos] = s;
-    p.inv[s] = pos;
-    p.row_token[pos] = s / p.k;
-  }
-  for (int t = tid; t < p.T; t += nt) p.row_token[S + t] = t;
-}
-
 
 // ---------------------------------------------------------------- routing of a few tokens by one CTA
 // For T <= kTokTile tokens no expert can receive more than kTokTile slots, so
@@ -476,34 +428,62 @@ struct SmallRoute {
 
 // Top-k, gates and the stable expert-major dispatch of T <= kTokTile tokens,
 // T * k <= min(kSmallSlots, blockDim.x), by every thread of the block (at most
-// 16 warps); results in r, and in the global outputs of p that are non-null
+// 16 warps); results in r, and, when `pub`, in the global outputs of p
 // (logits, idx, gates, perm, inv, row_token, entries, n_entries).  Row of slot
 // s: pos(s) = #{q : e_q < e_s} + #{q < s : e_q == e_s}, which is the dispatch
 // of dispatch_block.  Ends synchronised.
 template <int V2>
-__device__ void topk_one_token_cta(const RouteParams& p, SmallRoute& r) {
+__device__ void topk_one_token_cta(const RouteParams& p, SmallRoute& r, bool pub) {
   const int NW = blockDim.x >> 5, q = (p.E + NW - 1) / NW;
   if (q <= 32)
-    topk_token_cta<1, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates);
+    topk_token_cta<1, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates, pub);
   else if (q <= 64)
-    topk_token_cta<2, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates);
+    topk_token_cta<2, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates, pub);
   else
-    topk_token_cta<4, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates);
+    topk_token_cta<4, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates, pub);
 }
 
-__device__ void route_small_cta(const RouteParams& p, SmallRoute& r) {
+__device__ __noinline__ void route_small_cta(const RouteParams& p, SmallRoute& r, bool pub) {
   const int T = p.T, k = p.k, S = T * k;
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31, NW = nt >> 5;
   if (T == 1) {  // all warps share the token: E / NW experts each, then one merge
     if (NW * k <= 32 * 3)
-      topk_one_token_cta<3>(p, r);
+      topk_one_token_cta<3>(p, r, pub);
     else if (NW * k <= 32 * 9)
-      topk_one_token_cta<9>(p, r);
+      topk_one_token_cta<9>(p, r, pub);
     else
-      topk_one_token_cta<16>(p, r);
+      topk_one_token_cta<16>(p, r, pub);
   } else {  // one warp per token
-    for (int t = warp; t < T; t += NW) topk_token(p, t, lane, r.sidx, r.gates);
+    for (int t = warp; t < T; t += NW) topk_token(p, t, lane, r.sidx, r.gates, pub);
     __syncthreads();
+  }
+  if (T == 1) {  // k distinct experts, one row each: the entries are the picks sorted by id
+    if (warp == 0) {
+      const int e = lane < k ? r.sidx[lane] : INT_MAX;
+      int rank = 0;
+      for (int l = 0; l < k; ++l) rank += __shfl_sync(0xffffffffu, e, l) < e;
+      if (lane < k) {
+        r.inv[lane] = rank;
+        r.row_token[rank] = 0;
+        r.entries[rank] = make_int4(e, rank, 1, 0);
+        if (pub) {
+          p.perm[rank] = lane;
+          p.inv[lane] = rank;
+          p.row_token[rank] = 0;
+          p.entries[rank] = make_int4(e, rank, 1, 0);
+        }
+      }
+      if (lane == 0) {
+        r.row_token[k] = 0;  // the shared expert's row
+        r.n_entries = k;
+        if (pub) {
+          p.row_token[k] = 0;
+          *p.n_entries = k;
+        }
+      }
+    }
+    __syncthreads();
+    return;
   }
   int is_lead = 0;
   for (int s = tid; s < S; s += nt) {
@@ -522,13 +502,15 @@ __device__ void route_small_cta(const RouteParams& p, SmallRoute& r) {
     r.cnt[s] = cnt;
     r.lead[s] = before == 0;
     is_lead = before == 0;
-    if (p.perm) p.perm[pos] = s;
-    if (p.inv) p.inv[s] = pos;
-    if (p.row_token) p.row_token[pos] = s / k;
+    if (pub) {
+      p.perm[pos] = s;
+      p.inv[s] = pos;
+      p.row_token[pos] = s / k;
+    }
   }
   for (int t = tid; t < T; t += nt) {
     r.row_token[S + t] = t;
-    if (p.row_token) p.row_token[S + t] = t;
+    if (pub) p.row_token[S + t] = t;
   }
   const int n_ent = __syncthreads_count(is_lead);  // one slot per thread at most
   for (int s = tid; s < S; s += nt) {
@@ -538,17 +520,17 @@ __device__ void route_small_cta(const RouteParams& p, SmallRoute& r) {
     for (int q = 0; q < S; ++q) d += r.lead[q] & (r.sidx[q] < e);
     const int4 en = make_int4(e, r.lt[s], r.cnt[s], 0);
     r.entries[d] = en;
-    if (p.entries) p.entries[d] = en;
+    if (pub) p.entries[d] = en;
   }
   if (tid == 0) {
     r.n_entries = n_ent;
-    if (p.n_entries) *p.n_entries = n_ent;
+    if (pub) *p.n_entries = n_ent;
   }
   __syncthreads();
 }
 
 // counts[E] and offsets[E + 1] of a routing held in r (diagnostic outputs).
-__device__ void publish_counts(const RouteParams& p, const SmallRoute& r) {
+__device__ __noinline__ void publish_counts(const RouteParams& p, const SmallRoute& r) {
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
     int c = 0, off = 0;
     for (int d = 0; d < r.n_entries; ++d) {

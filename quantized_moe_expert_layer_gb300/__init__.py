@@ -19,7 +19,7 @@ CSRC = os.path.join(_HERE, "csrc")
 BUILD = os.path.join(_HERE, "_build")
 LIB = os.path.join(_HERE, "libmoe_gb300.so")
 HEADER = os.path.join(_ROOT, "include", "moe.h")
-SOURCES = ["layer.cu", "quant_pack.cu", "route.cu", "combine.cu", "noalloc.cu", "tc.cu", "stream.cu"]
+SOURCES = ["layer.cu", "quant_pack.cu", "route.cu", "expert.cu", "noalloc.cu", "tc.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-cudart", "shared"]
 
@@ -39,7 +39,7 @@ EXPORTS = [
     "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches", "moe_layer_set_option",
 ]
 
-OPT_RING_KB = 1
+OPT_DECODE_FUSED = 1
 
 _lock = threading.Lock()
 _lib = None

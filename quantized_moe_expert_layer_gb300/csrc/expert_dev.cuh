@@ -1,0 +1,369 @@
+// Device code of the expert GEMMs (dequantise packed tiles into m16n8k16 A
+// fragments, activations as B), shared by the stand-alone expert kernels and
+// the decode megakernel.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "layout.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
+  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// The 16 f16 activations of this lane's token row at column `col` (two
+// 16-byte reads, kept in L1: the warps of a CTA share them), or zeros.
+// A bf16 source row (b_bf16) is converted to f16 in registers: the shared
+// expert's CTAs start before the router has written the f16 copy of x.
+__device__ __forceinline__ void load_b(const uint16_t* brow, int col, bool b_bf16,
+                                       uint32_t (&xw)[8]) {
+  if (brow) {
+    const uint4* px = reinterpret_cast<const uint4*>(brow + col);
+    const uint4 q0 = px[0], q1 = px[1];
+    xw[0] = q0.x; xw[1] = q0.y; xw[2] = q0.z; xw[3] = q0.w;
+    xw[4] = q1.x; xw[5] = q1.y; xw[6] = q1.z; xw[7] = q1.w;
+    if (b_bf16) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(xw[i] << 16),
+                                            __uint_as_float(xw[i] & 0xFFFF0000u));
+        xw[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xw[i] = 0u;
+  }
+}
+
+// Work is split along K in units of 256 columns: 4 NVFP4 chunks of 64 or 2
+// FP6 blocks of 128.  A warp handles units h0, h0 + dh, ...; per unit it keeps
+// all weight vectors and activation fragments in flight before doing the math.
+__host__ __device__ __forceinline__ int n_halves(const MatGeom& g) { return (g.K + 255) / 256; }
+
+// Warps of a CTA: kWarps / tpc of them split K, tpc tile groups side by side.
+// Each warp takes about two 256-column units (the second one requested from
+// L2 up front), which keeps the decode grid within one wave at two CTAs per SM.
+__host__ __device__ __forceinline__ int tiles_per_cta(int units) {
+  int nks = 1;
+  while (nks * 2 <= kWarps && nks * 2 <= units / 2) nks *= 2;
+  return kWarps / nks;
+}
+
+// NT NVFP4 tiles (same K) times the activations.
+// brow: this lane's B row (f16, K long), null when the lane's column is empty.
+template <int NT>
+__device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], const MatGeom& g,
+                                            int h0, int dh, const uint16_t* brow, bool b_bf16,
+                                            float (&acc)[NT][4]) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int nh = n_halves(g);
+  for (int hh = h0; hh < nh; hh += dh) {
+    const int s = hh >> 1, jb = (hh & 1) * 4;
+    const int nc = min(4, sc_units(g, s) - jb);
+    uint4 sv[NT], cv[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const uint8_t* b = tile[i] + (size_t)s * g.sc_bytes + 16 * lane;
+      sv[i] = ldg_stream(b);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < nc) cv[i][j] = ldg_stream(b + 512 * (1 + jb + j));
+    }
+    uint32_t xb[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < nc) load_b(brow, 64 * (8 * s + jb + j) + 16 * t, b_bf16, xb[j]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < nc) {
+        const int jj = jb + j;  // chunk within the super-chunk
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], jj >> 1) >> (16 * (jj & 1))) & 0xFFFFu);
+          const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t h[4];
+            e2m1x8_to_f16x8(u4get(cv[i][j], w), h);
+            const uint32_t a[4] = {hmul2(h[0], s_lo), hmul2(h[1], s_hi), hmul2(h[2], s_lo),
+                                   hmul2(h[3], s_hi)};
+            mma_f16(acc[i], a, xb[j][2 * w], xb[j][2 * w + 1]);
+          }
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fp6_unpack(uint32_t Ha, uint32_t Hb, uint32_t L, uint32_t (&c)[4]) {
+  c[0] = ((Ha << 2) & 0x3C3C3C3Cu) | (L & 0x03030303u);
+  c[1] = ((Ha >> 2) & 0x3C3C3C3Cu) | ((L >> 2) & 0x03030303u);
+  c[2] = ((Hb << 2) & 0x3C3C3C3Cu) | ((L >> 4) & 0x03030303u);
+  c[3] = ((Hb >> 2) & 0x3C3C3C3Cu) | ((L >> 6) & 0x03030303u);
+}
+
+// NT FP6 tiles; a unit is 2 blocks (pairs of 64-column chunks) of 128 columns.
+template <int NT>
+__device__ __forceinline__ void tiles_fp6(const uint8_t* const (&tile)[NT], const MatGeom& g,
+                                          int h0, int dh, const uint16_t* brow, bool b_bf16,
+                                          float (&acc)[NT][4]) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int nh = n_halves(g);
+  for (int hh = h0; hh < nh; hh += dh) {
+    const int s = hh >> 2, j0 = (hh & 3) * 2;
+    const int np = sc_units(g, s);
+    uint32_t ew[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) ew[i] = ldg_stream_u32(tile[i] + (size_t)s * g.sc_bytes + 4 * lane);
+    uint4 cv[NT][2][3];
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+        if (j0 + jj < np)
+#pragma unroll
+          for (int v = 0; v < 3; ++v)
+            cv[i][jj][v] = ldg_stream(tile[i] + (size_t)s * g.sc_bytes + 128 + 1536 * (j0 + jj) +
+                                      512 * v + 16 * lane);
+    uint32_t xb[2][2][8];  // activation fragments of the 2 blocks, both chunks
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+      if (j0 + jj < np)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          load_b(brow, 128 * (8 * s + j0 + jj) + 64 * h + 16 * t, b_bf16, xb[jj][h]);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      if (j0 + jj < np) {
+        const int j = j0 + jj;
+        float blk[NT][4];
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) blk[i][r] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < NT; ++i) {
+            const uint32_t words[12] = {cv[i][jj][0].x, cv[i][jj][0].y, cv[i][jj][0].z,
+                                        cv[i][jj][0].w, cv[i][jj][1].x, cv[i][jj][1].y,
+                                        cv[i][jj][1].z, cv[i][jj][1].w, cv[i][jj][2].x,
+                                        cv[i][jj][2].y, cv[i][jj][2].z, cv[i][jj][2].w};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t c[4];
+              fp6_unpack(words[h * 6 + q * 3], words[h * 6 + q * 3 + 1], words[h * 6 + q * 3 + 2], c);
+#pragma unroll
+              for (int ww = 0; ww < 2; ++ww) {
+                const int w = 2 * q + ww;
+                uint32_t u[2], v[2];
+                e2m3x4_to_f16x4(c[2 * ww], u);      // rows g, g+8 at columns 4w, 4w+1
+                e2m3x4_to_f16x4(c[2 * ww + 1], v);  // rows g, g+8 at columns 4w+2, 4w+3
+                const uint32_t a[4] = {u[0], u[1], v[0], v[1]};
+                mma_f16(blk[i], a, xb[jj][h][2 * w], xb[jj][h][2 * w + 1]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const uint32_t e = __shfl_sync(0xffffffffu, ew[i], (gi << 2) | (j >> 1));
+          const float f0 = ue8m0_to_f32((e >> (16 * (j & 1))) & 0xFFu);
+          const float f1 = ue8m0_to_f32((e >> (16 * (j & 1) + 8)) & 0xFFu);
+          acc[i][0] = fmaf(blk[i][0], f0, acc[i][0]);
+          acc[i][1] = fmaf(blk[i][1], f0, acc[i][1]);
+          acc[i][2] = fmaf(blk[i][2], f1, acc[i][2]);
+          acc[i][3] = fmaf(blk[i][3], f1, acc[i][3]);
+        }
+      }
+    }
+  }
+}
+
+// Ask L2 for every 16-byte vector this lane will read from one tile's halves
+// h0, h0+dh, ... (fire and forget: no registers, no waiting).
+__device__ __forceinline__ void prefetch_tile(int fmt, const uint8_t* tile, const MatGeom& g,
+                                              int h0, int dh) {
+  const int lane = threadIdx.x & 31;
+  for (int hh = h0; hh < n_halves(g); hh += dh) {
+    if (fmt == FMT_NVFP4) {
+      const int s = hh >> 1, jb = (hh & 1) * 4;
+      const uint8_t* b = tile + (size_t)s * g.sc_bytes;
+      const int u = min(4, sc_units(g, s) - jb);
+      prefetch_l2(b + 16 * lane);
+      for (int j = 0; j < u; ++j) prefetch_l2(b + 512 * (1 + jb + j) + 16 * lane);
+    } else {
+      const int s = hh >> 2, jb = (hh & 3) * 2;
+      const uint8_t* b = tile + (size_t)s * g.sc_bytes;
+      const int u = min(2, sc_units(g, s) - jb);
+      prefetch_l2(b + 4 * lane);
+      for (int j = 0; j < 3 * u; ++j) prefetch_l2(b + 128 + 1536 * jb + 512 * j + 16 * lane);
+    }
+  }
+}
+
+template <int FMT, int NT>
+__device__ __forceinline__ void tiles_mma(const uint8_t* const (&tile)[NT], const MatGeom& g,
+                                          int s0, int ds, const uint16_t* brow, bool b_bf16,
+                                          float (&acc)[NT][4]) {
+  if (FMT == FMT_NVFP4)
+    tiles_nvfp4<NT>(tile, g, s0, ds, brow, b_bf16, acc);
+  else
+    tiles_fp6<NT>(tile, g, s0, ds, brow, b_bf16, acc);
+}
+
+// Entry y of the launch: the first p.nsh are the shared expert's token groups
+// (known without routing); the rest come from dispatch.
+__device__ __forceinline__ bool get_entry(const ExpertParams& p, int y, int& expert, int& row,
+                                          int& n) {
+  const int S = p.T * p.k;
+  if (y < p.nsh) {
+    expert = p.E;
+    row = S + kTokTile * y;
+    n = min(kTokTile, p.T - kTokTile * y);
+    return true;
+  }
+  const int r = y - p.nsh;
+  const int4 e = p.entries[r];  // read together with the count (the slot always exists)
+  if (r >= *p.n_entries) return false;
+  expert = e.x;
+  row = e.y;
+  n = e.z;
+  if (expert < 0 || expert >= p.E || n < 1 || n > kTokTile || row < 0 || row + n > S) {
+    *p.status = -1;  // MOE_EINVAL: corrupt entry, skip it
+    return false;
+  }
+  return true;
+}
+
+// Sum the per-warp partials of warps sharing a tile (fixed order) into warp ks == 0.
+template <int NV>
+__device__ __forceinline__ void reduce_ksplit(float* red, float (&v)[NV], int tpc, int nks) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (nks == 1) return;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) red[(warp * 32 + lane) * NV + i] = v[i];
+  __syncthreads();
+  if (warp / tpc == 0) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    for (int ks = 0; ks < nks; ++ks) {
+      const int w2 = ks * tpc + warp;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] += red[(w2 * 32 + lane) * NV + i];
+    }
+  }
+}
+
+
+// ---------------------------------------------------------------- gate/up + SwiGLU
+// One CTA-level task: tile pairs group*tpc .. +tpc of `expert`, for the n
+// tokens of rows row..row+n-1; red: kThreads x 8 floats of shared memory.
+template <int FMT>
+__device__ __forceinline__ void gateup_task(const ExpertParams& p, int expert, int row, int n,
+                                            int group, int tpc, float* red) {
+  const int S = p.T * p.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int nks = kWarps / tpc;
+  const int pair = group * tpc + (warp % tpc), ks = warp / tpc;
+  const bool valid = pair < p.I / 16;
+  const MatGeom g = mat_geom(FMT, p.H);
+  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
+  const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
+                                   eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
+  // routed entries read the router's f16 copy of x; the shared expert's
+  // entries run ahead of the router and read (and convert) x itself
+  const bool shared_entry = expert == p.E;
+  const uint16_t* brow = nullptr;
+  if (gi < n) {
+    const int tok = shared_entry ? row - S + gi : p.row_token[row + gi];
+    brow = (shared_entry ? p.x : p.xh) + (size_t)tok * p.H;
+  }
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  if (valid) {
+    // the warp's later K-units are requested from L2 now, so their loads do not wait on HBM
+    prefetch_tile(FMT, tiles[0], g, ks + nks, nks);
+    prefetch_tile(FMT, tiles[1], g, ks + nks, nks);
+    tiles_mma<FMT, 2>(tiles, g, ks, nks, brow, shared_entry, acc);
+  }
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = acc[0][i];
+    v[4 + i] = acc[1][i];
+  }
+  reduce_ksplit<8>(red, v, tpc, nks);
+  if (ks != 0 || !valid) return;
+  const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 16 * pair + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+    if (col < n) {
+      const float G = ts_g * v[i], U = ts_u * v[4 + i];
+      const float a = G / (1.0f + expf(-G)) * U;
+      p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+    }
+  }
+}
+
+
+// Requests from L2 the down tile `tile` of every work entry (fire and forget).
+template <int FMT>
+__device__ __forceinline__ void down_prefetch(const ExpertParams& p, int tile) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const MatGeom g = mat_geom(FMT, p.I);
+  const int n_entries = p.nsh + *p.n_entries;
+  const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
+  for (int y = warp; y < n_entries; y += nw) {
+    const int expert = (y < p.nsh) ? p.E : p.entries[y - p.nsh].x;
+    if (expert >= 0 && expert <= p.E)
+      prefetch_tile(FMT, tile_base + (size_t)expert * p.expert_bytes, g, 0, 1);
+  }
+}
+
+// y of tile `tile` (16 rows of H) for every work entry, one warp per entry,
+// into ys [rows x 16] (shared memory), then out[:, tile] = sum_j g_j y_j + y_s
+// in j order (the same fmaf chain as combine_kernel).
+template <int FMT>
+__device__ __forceinline__ void down_combine_task(const ExpertParams& p, int tile, const float* gates,
+                                                  const int* inv, float* out, float* ys) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int gi = lane >> 2, t = lane & 3;
+  const int S = p.T * p.k;
+  const MatGeom g = mat_geom(FMT, p.I);
+  const int n_entries = p.nsh + *p.n_entries;
+  const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
+  for (int y = warp; y < n_entries; y += nw) {
+    int expert, row, n;
+    if (!get_entry(p, y, expert, row, n)) continue;
+    const uint8_t* const tiles[1] = {tile_base + (size_t)expert * p.expert_bytes};
+    const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
+    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    tiles_mma<FMT, 1>(tiles, g, 0, 1, brow, false, acc);
+    const float ts = p.tscale[expert * 3 + 2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+      if (col < n) ys[(row + col) * 16 + r] = ts * acc[0][i];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.T * 16; i += blockDim.x) {
+    const int tk = i / 16, h = i % 16;
+    float a = 0.f;
+    for (int j = 0; j < p.k; ++j)
+      a = fmaf(gates[(size_t)tk * p.k + j], ys[inv[(size_t)tk * p.k + j] * 16 + h], a);
+    if (p.shared) a += ys[(S + tk) * 16 + h];
+    out[(size_t)tk * p.H + 16 * tile + h] = a;
+  }
+}
+
+}  // namespace
+}  // namespace moe

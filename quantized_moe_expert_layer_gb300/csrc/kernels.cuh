@@ -73,14 +73,22 @@ cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stri
 // routing
 int router_ksplit(int T, int H, int E);
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
+bool router_small_ok(int T, int k);
+cudaError_t launch_router_small(const RouteParams& p, int* counter, cudaStream_t st);
 cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st);
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st);
 size_t route_finish_smem(int E);
 cudaError_t route_kernels_init();
 
 // experts
+cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st);
+cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st);
 cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int* inv, float* out,
                            bool pdl, cudaStream_t st);
+bool down_combine_ok(int T, int k, int shared, int I);
+cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const int* inv,
+                                float* out, bool pdl, cudaStream_t st);
+cudaError_t expert_kernels_init();
 cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream_t st);
 
 // tensor-core (tcgen05) prefill path
@@ -92,37 +100,11 @@ bool tc_router_ok(int E, int H);
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);
 cudaError_t tc_kernels_init();
 
-// small-batch expert path: weight streaming through a shared-memory ring (stream.cu)
-struct StreamGeom {
-  int fmt, K;
-  int tiles;        // weight tiles per item: 2 (gate, up) or 1 (down)
-  int units;        // units of a tile: NVFP4 64-column chunks, FP6 128-column pairs
-  int nsc;          // super-chunks of a tile (8 units each, the last may be short)
-  int sc_bytes;     // bytes of a full super-chunk
-  int tile_bytes;
-  int unit_cols, unit_bytes, hdr_bytes;  // per unit; the scale vector heading a super-chunk
-  int pair_stage;   // 1: a stage is a whole gate/up tile pair (one contiguous copy)
-  int sc_run;       // else: super-chunks of one tile per stage
-  int w_cap;        // weight bytes of a stage at most
-  int b_once;       // 1: the activation rows are staged once per CTA; 0: with every stage
-  int b_stride;     // bytes per activation row (staged once: K * 2; per stage: its columns + 16)
-  int b_bytes;      // staged-once activation area
-  int n_max;        // activation rows per item at most
-  int stage_bytes, n_stages;
-  int ts_bytes;     // the tensor-scale table staged in shared memory
-};
-constexpr int kStreamMaxDyn = 192 * 1024;  // dynamic shared memory per CTA at most (static: < 34 KB)
-constexpr int kStreamOnceMax = 64 * 1024;  // activations staged once per CTA at most
-// bytes of the tensor-scale table of n experts (3 fp32 each), padded to 16
-inline int tscale_bytes(int n_experts) { return (n_experts * 3 * 4 + 15) / 16 * 16; }
-StreamGeom stream_geom(int fmt, int K, int tiles, int n_max, int b_rows, int ring_bytes, int n_experts);
-size_t stream_smem(const StreamGeom& g, int ys_rows);
-bool stream_small_ok(int T, int k);
-cudaError_t launch_stream_gateup(const ExpertParams& p, const RouteParams& rp, const StreamGeom& g,
-                                 bool route, cudaStream_t st);
-cudaError_t launch_stream_down(const ExpertParams& p, const RouteParams& rp, const StreamGeom& g,
-                               bool route, float* out, cudaStream_t st);
-cudaError_t stream_kernels_init();
+// decode megakernel (T <= 8): the whole layer in one cooperative launch
+bool decode_ok(int fmt, int T, int k, int shared, int H);
+cudaError_t launch_decode(const RouteParams& rp, const ExpertParams& ep, float* out, unsigned* bar,
+                          cudaStream_t st);
+cudaError_t decode_kernels_init();
 
 // launch helper: optional programmatic dependent launch on the previous kernel in the stream
 template <typename... KArgs, typename... Args>

@@ -104,7 +104,9 @@ struct moe_layer {
   int* row_token = nullptr;
   int4* entries = nullptr;
   int* n_entries = nullptr;
-  int ring_kb = 0;               // ring of the streaming expert kernels per CTA (0: default)
+  int* route_counter = nullptr;  // ticket counter of the fused small-T router
+  unsigned* grid_bar = nullptr;  // grid-barrier state of the decode megakernel
+  bool decode_fused = false;     // T <= 8: one cooperative kernel (else three kernels)
   int4* tc_entries = nullptr;    // entries of up to 256 tokens (tensor-core path)
   int* n_tc_entries = nullptr;
   uint16_t* xh = nullptr;        // f16 copy of x
@@ -197,17 +199,14 @@ int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
   return MOE_OK;
 }
 
+// experts + combine, after routing has filled idx / gates / dispatch
+bool fused_down(moe_layer* L, int T) { return down_combine_ok(T, L->k, L->shared, L->I); }
+
 bool tc_path(moe_layer* L, int T) { return tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I); }
 
 // prefill routing: logits as one bf16 GEMM on the tensor cores, then top-k and
 // dispatch as usual (the GEMM's output is the one K slice the top-k reads)
 bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E, L->H); }
-
-// T <= 8 (and x small enough to stage once per CTA): the streaming expert
-// kernels route themselves (router -> gate/up -> down + combine)
-bool small_path(moe_layer* L, int T) {
-  return stream_small_ok(T, L->k) && (long)T * L->H * 2 <= kStreamOnceMax;
-}
 
 int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
@@ -217,22 +216,6 @@ int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t 
   return MOE_OK;
 }
 
-// Ring geometry of the streaming kernels.  Two CTAs (gate/up and down, which
-// overlap) share an SM, so each takes well under half of its shared memory.
-// The routing variants stage their activation rows once per CTA (x for
-// gate/up, every row of a for down, when it fits).
-StreamGeom gu_geom(moe_layer* L, int T, bool route) {
-  const int ring = L->ring_kb > 0 ? L->ring_kb * 1024 : 80 * 1024;
-  const int n_max = T < kTokTile ? T : kTokTile;
-  return stream_geom(L->fmt, L->H, 2, n_max, route ? T : 0, ring, L->E + L->shared);
-}
-StreamGeom dn_geom(moe_layer* L, int T, bool route) {
-  const int ring = L->ring_kb > 0 ? L->ring_kb * 1024 : 64 * 1024;
-  const int n_max = T < kTokTile ? T : kTokTile;
-  return stream_geom(L->fmt, L->I, 1, n_max, route ? T * L->k + T : 0, ring, L->E + L->shared);
-}
-
-// experts + combine, after routing has filled idx / gates / dispatch
 int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
   if (tc_path(L, T)) {
@@ -242,29 +225,36 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
     CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
     return MOE_OK;
   }
-  RouteParams rp = route_params(L, x, T);
-  CK("gate/up kernel launch", launch_stream_gateup(ep, rp, gu_geom(L, T, false), false, st));
-  CK("down kernel launch", launch_stream_down(ep, rp, dn_geom(L, T, false), false, nullptr, st));
+  const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
+  CK("gate/up kernel launch", launch_gateup(ep, grid_y, true, st));
+  if (fused_down(L, T)) {
+    CK("down+combine kernel launch", launch_down_combine(ep, L->gates, L->inv, out, true, st));
+    return MOE_OK;
+  }
+  CK("down kernel launch", launch_down(ep, grid_y, true, st));
   CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
   return MOE_OK;
 }
 
+bool decode_path(moe_layer* L, int T) {
+  return L->decode_fused && decode_ok(L->fmt, T, L->k, L->shared, L->H);
+}
+
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
-  if (small_path(L, T)) return 3;
-  const int routing = tc_router(L, T) ? 4 : (T <= 64 ? 2 : 3);
-  return routing + 3;
+  if (decode_path(L, T)) return 1;
+  const int routing =
+      tc_router(L, T) ? 4 : (router_small_ok(T, L->k) ? 1 : (T <= 64 ? 2 : 3));
+  if (tc_path(L, T)) return routing + 3;
+  return routing + (fused_down(L, T) ? 2 : 3);
 }
 
 int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   RouteParams rp = route_params(L, x, T);
   L->last_T = T;
   L->last_has_logits = true;
-  if (small_path(L, T)) {
-    ExpertParams ep = expert_params(L, x, T);
-    CK("router kernel launch", launch_router(rp, st));
-    CK("gate/up kernel launch", launch_stream_gateup(ep, rp, gu_geom(L, T, true), true, st));
-    CK("down kernel launch", launch_stream_down(ep, rp, dn_geom(L, T, true), true, out, st));
+  if (decode_path(L, T)) {
+    CK("decode kernel launch", launch_decode(rp, expert_params(L, x, T), out, L->grid_bar, st));
     return MOE_OK;
   }
   if (tc_router(L, T)) {
@@ -272,6 +262,8 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
     if (rc) return rc;
     CK("top-k kernel launch", launch_topk(rp, true, st));
     CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
+  } else if (router_small_ok(T, L->k)) {
+    CK("router kernel launch", launch_router_small(rp, L->route_counter, st));
   } else if (T <= 64) {
     CK("router kernel launch", launch_router(rp, st));
     CK("top-k/dispatch kernel launch", launch_route_finish(rp, true, true, st));
@@ -280,6 +272,8 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
     CK("top-k kernel launch", launch_topk(rp, true, st));
     CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
   }
+  L->last_T = T;
+  L->last_has_logits = true;
   return run_experts(L, x, T, out, st);
 }
 
@@ -312,8 +306,9 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   L->geom = expert_geom(format, H, I);
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = route_kernels_init();
+  if (e == cudaSuccess) e = expert_kernels_init();
   if (e == cudaSuccess) e = tc_kernels_init();
-  if (e == cudaSuccess) e = stream_kernels_init();
+  if (e == cudaSuccess) e = decode_kernels_init();
   if (e != cudaSuccess) {
     delete L;
     return cuda_fail("moe_layer_create: device set-up", e);
@@ -321,7 +316,7 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   const int n_total = E + shared;
   L->arena_bytes = (uint64_t)n_total * L->geom.expert_bytes;
   if (cudaMalloc(&L->arena, L->arena_bytes) != cudaSuccess ||
-      cudaMalloc(&L->tscale, tscale_bytes(n_total)) != cudaSuccess ||  // padded: copied whole
+      cudaMalloc(&L->tscale, sizeof(float) * 3 * n_total) != cudaSuccess ||
       cudaMalloc(&L->router, sizeof(uint16_t) * (size_t)E * H) != cudaSuccess ||
       cudaMalloc(&L->bias, sizeof(float) * E) != cudaSuccess ||
       cudaMalloc(&L->status, sizeof(int)) != cudaSuccess) {
@@ -331,7 +326,7 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
                 L ? (double)L->arena_bytes / 1e6 : 0.0);
   }
   if (cudaMemset(L->arena, 0, L->arena_bytes) != cudaSuccess ||
-      cudaMemset(L->tscale, 0, tscale_bytes(n_total)) != cudaSuccess ||
+      cudaMemset(L->tscale, 0, sizeof(float) * 3 * n_total) != cudaSuccess ||
       cudaMemset(L->status, 0, sizeof(int)) != cudaSuccess) {
     moe_layer_destroy(L);
     return fail(MOE_ECUDA, "moe_layer_create: cudaMemset failed");
@@ -359,7 +354,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       E * 4, (E + 1) * 4,                // counts, offsets
       S * 4, S * 4,                      // perm, inv
       (S + T_max) * 4,                   // row_token
-      n_entries * 16, 16,                // entries, n_entries
+      n_entries * 16, 16, 16, 16,        // entries, n_entries, route_counter, grid_bar
       (size_t)max_tc_entries(T_max, L->E, L->k) * 16, 16,  // tc_entries, n_tc_entries
       (size_t)T_max * L->H * 2,          // xh
       (S + T_max) * L->I * 2,            // abuf
@@ -397,13 +392,15 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->row_token = (int*)ptrs[8];
   L->entries = (int4*)ptrs[9];
   L->n_entries = (int*)ptrs[10];
-  L->tc_entries = (int4*)ptrs[11];
-  L->n_tc_entries = (int*)ptrs[12];
-  L->xh = (uint16_t*)ptrs[13];
-  L->abuf = (uint16_t*)ptrs[14];
-  L->ybuf = (float*)ptrs[15];
-  L->x_stage = (uint16_t*)ptrs[16];
-  L->out_stage = (float*)ptrs[17];
+  L->route_counter = (int*)ptrs[11];
+  L->grid_bar = (unsigned*)ptrs[12];
+  L->tc_entries = (int4*)ptrs[13];
+  L->n_tc_entries = (int*)ptrs[14];
+  L->xh = (uint16_t*)ptrs[15];
+  L->abuf = (uint16_t*)ptrs[16];
+  L->ybuf = (float*)ptrs[17];
+  L->x_stage = (uint16_t*)ptrs[18];
+  L->out_stage = (float*)ptrs[19];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   return MOE_OK;
@@ -434,10 +431,8 @@ int moe_layer_status(moe_layer* L, int reset, int* status) {
 int moe_layer_set_option(moe_layer* L, int option, int value) {
   if (!L) return fail(MOE_EINVAL, "moe_layer_set_option: null layer");
   switch (option) {
-    case MOE_OPT_RING_KB:
-      if (value < 0 || value * 1024 > kStreamMaxDyn - 32 * 1024)
-        return fail(MOE_EINVAL, "moe_layer_set_option: ring of %d KB out of range", value);
-      L->ring_kb = value;
+    case MOE_OPT_DECODE_FUSED:
+      L->decode_fused = value != 0;
       return MOE_OK;
     default:
       return fail(MOE_EINVAL, "moe_layer_set_option: unknown option %d", option);
@@ -632,25 +627,26 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
   cudaStream_t st = (cudaStream_t)stream;
   RouteParams rp = route_params(L, x, T);
   ExpertParams ep = expert_params(L, x, T);
-  if (small_path(L, T)) {  // router; gate/up (routing inside); down + combine (routing inside)
-    if (phase == 0) CK("router", launch_router(rp, st));
-    if (phase == 2) CK("gate/up", launch_stream_gateup(ep, rp, gu_geom(L, T, true), true, st));
-    if (phase == 3) CK("down", launch_stream_down(ep, rp, dn_geom(L, T, true), true, out, st));
-    if (phase < 0 || phase > 4) return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
+  const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
+  if (decode_path(L, T)) {  // one kernel: phase 0 is the whole layer
+    if (phase == 0) CK("decode", launch_decode(rp, ep, out, L->grid_bar, st));
     return MOE_OK;
   }
-  const bool tc = tc_path(L, T);
+  const bool small = router_small_ok(T, L->k), fused = fused_down(L, T);
   switch (phase) {
     case 0:
       if (tc_router(L, T)) {
         const int rc = launch_tc_routing_gemm(L, x, T, st);
         if (rc) return rc;
+      } else if (small) {
+        CK("router", launch_router_small(rp, L->route_counter, st));
       } else {
         CK("router", launch_router(rp, st));
       }
       break;
     case 1:
-      if (T <= 64 && !tc_router(L, T)) {
+      if (small) break;
+      if (T <= 64) {
         CK("top-k/dispatch", launch_route_finish(rp, true, false, st));
       } else {
         CK("top-k", launch_topk(rp, false, st));
@@ -658,19 +654,21 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       }
       break;
     case 2:
-      if (tc)
+      if (tc_path(L, T))
         CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
       else
-        CK("gate/up", launch_stream_gateup(ep, rp, gu_geom(L, T, false), false, st));
+        CK("gate/up", launch_gateup(ep, grid_y, false, st));
       break;
     case 3:
-      if (tc)
+      if (tc_path(L, T))
         CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
+      else if (fused)
+        CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, st));
       else
-        CK("down", launch_stream_down(ep, rp, dn_geom(L, T, false), false, nullptr, st));
+        CK("down", launch_down(ep, grid_y, false, st));
       break;
     case 4:
-      CK("combine", launch_combine(ep, L->gates, L->inv, out, false, st));
+      if (!fused) CK("combine", launch_combine(ep, L->gates, L->inv, out, false, st));
       break;
     default: return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
   }

@@ -78,30 +78,34 @@ def test_tensor_core_router_small_layer(T):
     compare_layer(w, L, gen.x_tokens(w, T))
 
 
-def test_decode_nvfp4_full_size():
+@pytest.mark.parametrize("fused", [0, 1])
+def test_decode_nvfp4_full_size(fused):
     w = gen.get_workload(1)
     L = layer(w)
-    assert L.launches(1) == 3  # router, gate/up (routing inside), down + combine (routing inside)
-    rel, ties = compare_layer(w, L, gen.x_tokens(w))
-    print(f"decode nvfp4: rel-L2 {rel:.2e}, near ties {ties}")
+    L.set_option(moe.OPT_DECODE_FUSED, fused)
+    try:
+        assert L.launches(1) == (1 if fused else 3)
+        rel, ties = compare_layer(w, L, gen.x_tokens(w))
+        print(f"decode nvfp4 (fused={fused}): rel-L2 {rel:.2e}, near ties {ties}")
+    finally:
+        L.set_option(moe.OPT_DECODE_FUSED, 0)
 
 
 @pytest.mark.parametrize("T", [1, 3, 8])
-def test_results_do_not_depend_on_the_ring_size(T):
-    """The streaming kernels' ring size changes how many stages are in flight and
-    which CTA takes which item, never the arithmetic of an item."""
+def test_decode_fused_and_chained_paths_agree_bit_for_bit(T):
+    """The one-kernel decode path and the three-kernel chain run the same device
+    code in the same order."""
     w = gen.get_workload(1)
     L = layer(w)
     x = gen.x_tokens(w, T)
     a = run_gpu(L, x, w)
+    L.set_option(moe.OPT_DECODE_FUSED, 1)
     try:
-        for kb in (24, 160):
-            L.set_option(moe.OPT_RING_KB, kb)
-            b = run_gpu(L, x, w)
-            for key in ("out", "logits", "idx", "gates", "counts", "offsets", "perm"):
-                assert np.array_equal(a[key], b[key]), (kb, key)
+        b = run_gpu(L, x, w)
     finally:
-        L.set_option(moe.OPT_RING_KB, 0)
+        L.set_option(moe.OPT_DECODE_FUSED, 0)
+    for key in ("out", "logits", "idx", "gates", "counts", "offsets", "perm"):
+        assert np.array_equal(a[key], b[key]), key
 
 
 def test_decode_fp6_full_size():
@@ -112,7 +116,7 @@ def test_decode_fp6_full_size():
         print(f"decode fp6: rel-L2 {rel:.2e}, near ties {ties}")
         x = gen.x_tokens(w)
         a = run_gpu(L, x, w)
-        L.set_option(moe.OPT_RING_KB, 48)
+        L.set_option(moe.OPT_DECODE_FUSED, 1)
         b = run_gpu(L, x, w)
         assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["idx"], b["idx"])
     finally:

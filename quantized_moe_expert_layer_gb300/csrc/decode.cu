@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(RouteParams rp, 
   // ---------------------------------------------------------------- phase 3
   float* ys = reinterpret_cast<float*>(dsm);
   for (int tile = cta; tile < ep.H / 16; tile += ncta) {
-    down_combine_task<FMT>(el, tile, sh.gates, sh.inv, out, ys);
+    DownPreload none;
+    down_combine_task<FMT>(el, tile, sh.gates, sh.inv, out, ys, none, false);
     __syncthreads();
   }
 }

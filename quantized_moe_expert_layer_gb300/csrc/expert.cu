@@ -123,11 +123,15 @@ template <int FMT>
 __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertParams p,
                                                                          const float* gates,
                                                                          const int* inv, float* out) {
-  // routing is complete here (gate/up triggered this launch only after its wait)
-  down_prefetch<FMT>(p, blockIdx.x);
+  // routing is complete here (gate/up triggered this launch only after its wait):
+  // the weights are read before waiting for gate/up
+  DownPreload pre;
+  bool have = false;
+  if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
+  down_prefetch<FMT>(p, blockIdx.x);  // (the rest: into L2)
   griddep_wait();  // gate/up complete: abuf holds every row
   extern __shared__ float ys[];  // [rows x 16]
-  down_combine_task<FMT>(p, blockIdx.x, gates, inv, out, ys);
+  down_combine_task<FMT>(p, blockIdx.x, gates, inv, out, ys, pre, have);
 }
 
 size_t down_combine_smem(int T, int k, int shared) {

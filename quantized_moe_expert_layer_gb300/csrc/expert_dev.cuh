@@ -328,12 +328,68 @@ __device__ __forceinline__ void down_prefetch(const ExpertParams& p, int tile) {
   }
 }
 
+// The down tile of one work entry, loaded into registers before the kernel
+// waits for gate/up: the weights do not depend on it (NVFP4, K <= 512: one
+// super-chunk of at most 8 chunks).
+struct DownPreload {
+  int expert, row, n;
+  float ts;
+  uint4 sv, cv[8];
+};
+
+__device__ __forceinline__ bool down_preload(const ExpertParams& p, int tile, int y, DownPreload& d) {
+  const int lane = threadIdx.x & 31;
+  if (y >= p.nsh + *p.n_entries || !get_entry(p, y, d.expert, d.row, d.n)) return false;
+  const uint8_t* b = p.arena + (size_t)d.expert * p.expert_bytes + p.gu_bytes +
+                     (size_t)tile * p.dn_tile_bytes + 16 * lane;
+  const int nc = p.I / 64;
+  d.sv = ldg_stream(b);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < nc) d.cv[j] = ldg_stream(b + 512 * (1 + j));
+  d.ts = p.tscale[d.expert * 3 + 2];
+  return true;
+}
+
+// The preloaded tile times the entry's rows of a (which gate/up wrote).
+__device__ __forceinline__ void down_preloaded_mma(const ExpertParams& p, const DownPreload& d,
+                                                   float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int nc = p.I / 64;
+  const uint16_t* brow = gi < d.n ? p.abuf + (size_t)(d.row + gi) * p.I : nullptr;
+#pragma unroll
+  for (int j0 = 0; j0 < 8; j0 += 4) {
+    uint32_t xb[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j0 + j < nc) load_b(brow, 64 * (j0 + j) + 16 * t, false, xb[j]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int jj = j0 + j;
+      if (jj < nc) {
+        const uint32_t sp = e4m3x2_to_f16x2((u4get(d.sv, jj >> 1) >> (16 * (jj & 1))) & 0xFFFFu);
+        const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t h[4];
+          e2m1x8_to_f16x8(u4get(d.cv[jj], w), h);
+          const uint32_t a[4] = {hmul2(h[0], s_lo), hmul2(h[1], s_hi), hmul2(h[2], s_lo),
+                                 hmul2(h[3], s_hi)};
+          mma_f16(acc, a, xb[j][2 * w], xb[j][2 * w + 1]);
+        }
+      }
+    }
+  }
+}
+
 // y of tile `tile` (16 rows of H) for every work entry, one warp per entry,
 // into ys [rows x 16] (shared memory), then out[:, tile] = sum_j g_j y_j + y_s
-// in j order (the same fmaf chain as combine_kernel).
+// in j order (the same fmaf chain as combine_kernel).  `pre`: the warp's first
+// entry, preloaded (when have_pre).
 template <int FMT>
 __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int tile, const float* gates,
-                                                  const int* inv, float* out, float* ys) {
+                                                  const int* inv, float* out, float* ys,
+                                                  const DownPreload& pre, bool have_pre) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int gi = lane >> 2, t = lane & 3;
   const int S = p.T * p.k;
@@ -341,6 +397,16 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
   const int n_entries = p.nsh + *p.n_entries;
   const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
   for (int y = warp; y < n_entries; y += nw) {
+    if (have_pre && y == warp) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      down_preloaded_mma(p, pre, acc);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+        if (col < pre.n) ys[(pre.row + col) * 16 + r] = pre.ts * acc[i];
+      }
+      continue;
+    }
     int expert, row, n;
     if (!get_entry(p, y, expert, row, n)) continue;
     const uint8_t* const tiles[1] = {tile_base + (size_t)expert * p.expert_bytes};

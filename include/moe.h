@@ -79,18 +79,6 @@ const char* moe_last_error(void);
  * reset != 0.  Returns MOE_OK, or an error if the read itself failed. */
 int moe_layer_status(moe_layer* L, int reset, int* status);
 
-/* Layer options (moe_layer_set_option). */
-enum moe_option {
-  /* 1: for T <= 8 the whole layer runs as one cooperative kernel (routing,
-   * gate/up, down + combine separated by grid-wide barriers); 0 (default): as
-   * three kernels chained with programmatic dependent launch.  Both give the
-   * same numbers (same device code, same order). */
-  MOE_OPT_DECODE_FUSED = 1
-};
-
-/* Set a layer option; not while a forward is in flight. */
-int moe_layer_set_option(moe_layer* L, int option, int value);
-
 /* Number of kernels one moe_forward of T tokens launches (>= 0), or an error. */
 int moe_forward_launches(moe_layer* L, int T);
 
@@ -181,10 +169,10 @@ int moe_debug_routing(moe_layer* L, float* logits, int32_t* idx, float* gates, i
                       int32_t* offsets, int32_t* perm, void* stream);
 
 /* Re-run one phase of the last moe_forward on the same arguments, for timing a
- * kernel on its own: 0 routing (router logits; for T <= 8 also top-k and
- * dispatch, fused), 1 top-k + dispatch (nothing for T <= 8), 2 gate/up + SwiGLU,
- * 3 down (down + combine, fused, when the few-token path runs), 4 combine
- * (nothing when fused).  The workspace must hold that forward's state (same x, T). */
+ * kernel on its own: 0 router logits, 1 top-k + dispatch, 2 gate/up + SwiGLU,
+ * 3 down, 4 combine.  For T <= 8 the expert kernels route themselves: 1 and 4
+ * launch nothing, 2 includes top-k and dispatch, 3 includes them and the
+ * combine.  The workspace must hold that forward's state (same x, T). */
 int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float* out,
                         void* stream);
 

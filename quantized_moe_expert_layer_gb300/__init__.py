@@ -19,7 +19,7 @@ CSRC = os.path.join(_HERE, "csrc")
 BUILD = os.path.join(_HERE, "_build")
 LIB = os.path.join(_HERE, "libmoe_gb300.so")
 HEADER = os.path.join(_ROOT, "include", "moe.h")
-SOURCES = ["layer.cu", "quant_pack.cu", "route.cu", "expert.cu", "noalloc.cu", "tc.cu", "decode.cu"]
+SOURCES = ["layer.cu", "quant_pack.cu", "route.cu", "expert.cu", "noalloc.cu", "tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-cudart", "shared"]
 
@@ -36,10 +36,8 @@ EXPORTS = [
     "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
     "moe_pack_weights", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
-    "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches", "moe_layer_set_option",
+    "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches"
 ]
-
-OPT_DECODE_FUSED = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -115,7 +113,6 @@ def lib():
                 "moe_debug_run_phase": (I, [P, I, P, I, P, P]),
                 "moe_route_noalloc": (I, [P, I, I, P, P, I, I, P, P, P, P]),
                 "moe_forward_launches": (I, [P, I]),
-                "moe_layer_set_option": (I, [P, I, I]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -171,8 +168,6 @@ class MoeLayer:
     def reserve(self, T_max):
         check(lib().moe_layer_reserve(self.h, T_max))
 
-    def set_option(self, option, value):
-        check(lib().moe_layer_set_option(self.h, option, int(value)))
 
     def launches(self, T):
         """Kernels one forward of T tokens launches."""

@@ -22,6 +22,7 @@
 #include "expert_dev.cuh"
 #include "kernels.cuh"
 #include "layout.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 namespace {
@@ -40,6 +41,35 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(ExpertParams p, int
   if (!get_entry(p, y, expert, row, n)) return;
   __shared__ float red[kThreads * 8];
   gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
+}
+
+// Gate/up for T <= 8 tokens that routes itself: every routed CTA takes the
+// top-k and the dispatch from the router's partial sums (a few KB through
+// L2) instead of waiting for a routing kernel and reading its work entries;
+// CTA (0, first routed) also publishes the routing.  The shared expert's CTAs
+// run at once.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 2) gateup_routed_kernel(ExpertParams p, RouteParams rp, int tpc) {
+  const int y = blockIdx.y;
+  __shared__ float red[kThreads * 8];
+  if (y < p.nsh) {
+    int expert, row, n;
+    if (get_entry(p, y, expert, row, n)) gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
+    return;
+  }
+  __shared__ SmallRoute rt;
+  griddep_wait();  // the router's partial sums
+  const bool pub = y == p.nsh && blockIdx.x == 0;
+  route_small_cta(rp, rt, pub);
+  griddep_launch();  // the next kernel routes itself from the same partial sums
+  const int d = y - p.nsh;
+  if (d < rt.n_entries) {
+    const int4 e = rt.entries[d];
+    ExpertParams el = p;  // the routed rows' tokens from shared memory
+    el.row_token = rt.row_token;
+    gateup_task<FMT>(el, e.x, e.y, e.z, blockIdx.x, tpc, red);
+  }
+  if (pub) publish_counts(rp, rt);
 }
 
 // ---------------------------------------------------------------- down
@@ -134,6 +164,28 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
   down_combine_task<FMT>(p, blockIdx.x, gates, inv, out, ys, pre, have);
 }
 
+// The same for T <= 8 with routing in the CTA: the router finished before
+// gate/up let this launch start, so its partial sums are final; the top-k,
+// the dispatch and the weights all come before waiting for gate/up.
+template <int FMT>
+__global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_routed_kernel(ExpertParams p,
+                                                                                RouteParams rp,
+                                                                                float* out) {
+  __shared__ SmallRoute rt;
+  route_small_cta(rp, rt, false);
+  ExpertParams el = p;
+  el.entries = rt.entries;
+  el.n_entries = &rt.n_entries;
+  el.row_token = rt.row_token;
+  DownPreload pre;
+  bool have = false;
+  if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(el, blockIdx.x, threadIdx.x >> 5, pre);
+  down_prefetch<FMT>(el, blockIdx.x);
+  griddep_wait();  // gate/up complete: abuf holds every row
+  extern __shared__ float ys[];
+  down_combine_task<FMT>(el, blockIdx.x, rt.gates, rt.inv, out, ys, pre, have);
+}
+
 size_t down_combine_smem(int T, int k, int shared) {
   return ((size_t)T * k + (shared ? T : 0)) * 16 * sizeof(float);
 }
@@ -184,6 +236,32 @@ cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const
                     pdl, p, gates, inv, out);
   return launch_k(down_combine_kernel<FMT_FP6>, dim3(p.H / 16), dim3(32 * warps), smem, st, pdl, p,
                   gates, inv, out);
+}
+
+bool small_route_ok(int T, int k) { return T <= kTokTile && T * k <= kSmallSlots; }
+
+cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, int grid_y,
+                                 cudaStream_t st) {
+  const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
+  const int pairs = p.I / 16;
+  dim3 grid((pairs + tpc - 1) / tpc, grid_y);
+  if (p.fmt == FMT_NVFP4)
+    return launch_k(gateup_routed_kernel<FMT_NVFP4>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
+  return launch_k(gateup_routed_kernel<FMT_FP6>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
+}
+
+cudaError_t launch_down_combine_routed(const ExpertParams& p, const RouteParams& rp, float* out,
+                                       cudaStream_t st) {
+  // one warp per work entry, at least 8 warps (the routing wants the slots covered)
+  int warps = p.nsh + (p.T * p.k < p.E ? p.T * p.k : p.E);
+  if (warps > kDcMaxWarps) warps = kDcMaxWarps;
+  if (warps < 8) warps = 8;
+  const size_t smem = down_combine_smem(p.T, p.k, p.shared);
+  if (p.fmt == FMT_NVFP4)
+    return launch_k(down_combine_routed_kernel<FMT_NVFP4>, dim3(p.H / 16), dim3(32 * warps), smem, st,
+                    true, p, rp, out);
+  return launch_k(down_combine_routed_kernel<FMT_FP6>, dim3(p.H / 16), dim3(32 * warps), smem, st, true,
+                  p, rp, out);
 }
 
 cudaError_t expert_kernels_init() { return cudaSuccess; }

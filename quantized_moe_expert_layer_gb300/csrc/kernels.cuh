@@ -73,8 +73,6 @@ cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stri
 // routing
 int router_ksplit(int T, int H, int E);
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
-bool router_small_ok(int T, int k);
-cudaError_t launch_router_small(const RouteParams& p, int* counter, cudaStream_t st);
 cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st);
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st);
 size_t route_finish_smem(int E);
@@ -100,11 +98,12 @@ bool tc_router_ok(int E, int H);
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);
 cudaError_t tc_kernels_init();
 
-// decode megakernel (T <= 8): the whole layer in one cooperative launch
-bool decode_ok(int fmt, int T, int k, int shared, int H);
-cudaError_t launch_decode(const RouteParams& rp, const ExpertParams& ep, float* out, unsigned* bar,
-                          cudaStream_t st);
-cudaError_t decode_kernels_init();
+// T <= 8: gate/up and down + combine that route themselves (expert.cu)
+bool small_route_ok(int T, int k);
+cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, int grid_y,
+                                 cudaStream_t st);
+cudaError_t launch_down_combine_routed(const ExpertParams& p, const RouteParams& rp, float* out,
+                                       cudaStream_t st);
 
 // launch helper: optional programmatic dependent launch on the previous kernel in the stream
 template <typename... KArgs, typename... Args>

@@ -104,9 +104,6 @@ struct moe_layer {
   int* row_token = nullptr;
   int4* entries = nullptr;
   int* n_entries = nullptr;
-  int* route_counter = nullptr;  // ticket counter of the fused small-T router
-  unsigned* grid_bar = nullptr;  // grid-barrier state of the decode megakernel
-  bool decode_fused = false;     // T <= 8: one cooperative kernel (else three kernels)
   int4* tc_entries = nullptr;    // entries of up to 256 tokens (tensor-core path)
   int* n_tc_entries = nullptr;
   uint16_t* xh = nullptr;        // f16 copy of x
@@ -236,15 +233,14 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   return MOE_OK;
 }
 
-bool decode_path(moe_layer* L, int T) {
-  return L->decode_fused && decode_ok(L->fmt, T, L->k, L->shared, L->H);
-}
+// T <= 8: router partial sums, then gate/up and down + combine that route
+// themselves from them (three launches, chained)
+bool small_path(moe_layer* L, int T) { return small_route_ok(T, L->k) && fused_down(L, T); }
 
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
-  if (decode_path(L, T)) return 1;
-  const int routing =
-      tc_router(L, T) ? 4 : (router_small_ok(T, L->k) ? 1 : (T <= 64 ? 2 : 3));
+  if (small_path(L, T)) return 3;
+  const int routing = tc_router(L, T) ? 4 : (T <= 64 ? 2 : 3);
   if (tc_path(L, T)) return routing + 3;
   return routing + (fused_down(L, T) ? 2 : 3);
 }
@@ -253,8 +249,12 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
   RouteParams rp = route_params(L, x, T);
   L->last_T = T;
   L->last_has_logits = true;
-  if (decode_path(L, T)) {
-    CK("decode kernel launch", launch_decode(rp, expert_params(L, x, T), out, L->grid_bar, st));
+  if (small_path(L, T)) {
+    ExpertParams ep = expert_params(L, x, T);
+    CK("router kernel launch", launch_router(rp, st));
+    CK("gate/up kernel launch",
+       launch_gateup_routed(ep, rp, ep.nsh + max_routed_entries(T, L->E, L->k), st));
+    CK("down+combine kernel launch", launch_down_combine_routed(ep, rp, out, st));
     return MOE_OK;
   }
   if (tc_router(L, T)) {
@@ -262,8 +262,6 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
     if (rc) return rc;
     CK("top-k kernel launch", launch_topk(rp, true, st));
     CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
-  } else if (router_small_ok(T, L->k)) {
-    CK("router kernel launch", launch_router_small(rp, L->route_counter, st));
   } else if (T <= 64) {
     CK("router kernel launch", launch_router(rp, st));
     CK("top-k/dispatch kernel launch", launch_route_finish(rp, true, true, st));
@@ -308,7 +306,6 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   if (e == cudaSuccess) e = route_kernels_init();
   if (e == cudaSuccess) e = expert_kernels_init();
   if (e == cudaSuccess) e = tc_kernels_init();
-  if (e == cudaSuccess) e = decode_kernels_init();
   if (e != cudaSuccess) {
     delete L;
     return cuda_fail("moe_layer_create: device set-up", e);
@@ -354,7 +351,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       E * 4, (E + 1) * 4,                // counts, offsets
       S * 4, S * 4,                      // perm, inv
       (S + T_max) * 4,                   // row_token
-      n_entries * 16, 16, 16, 16,        // entries, n_entries, route_counter, grid_bar
+      n_entries * 16, 16,                // entries, n_entries
       (size_t)max_tc_entries(T_max, L->E, L->k) * 16, 16,  // tc_entries, n_tc_entries
       (size_t)T_max * L->H * 2,          // xh
       (S + T_max) * L->I * 2,            // abuf
@@ -392,15 +389,13 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->row_token = (int*)ptrs[8];
   L->entries = (int4*)ptrs[9];
   L->n_entries = (int*)ptrs[10];
-  L->route_counter = (int*)ptrs[11];
-  L->grid_bar = (unsigned*)ptrs[12];
-  L->tc_entries = (int4*)ptrs[13];
-  L->n_tc_entries = (int*)ptrs[14];
-  L->xh = (uint16_t*)ptrs[15];
-  L->abuf = (uint16_t*)ptrs[16];
-  L->ybuf = (float*)ptrs[17];
-  L->x_stage = (uint16_t*)ptrs[18];
-  L->out_stage = (float*)ptrs[19];
+  L->tc_entries = (int4*)ptrs[11];
+  L->n_tc_entries = (int*)ptrs[12];
+  L->xh = (uint16_t*)ptrs[13];
+  L->abuf = (uint16_t*)ptrs[14];
+  L->ybuf = (float*)ptrs[15];
+  L->x_stage = (uint16_t*)ptrs[16];
+  L->out_stage = (float*)ptrs[17];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   return MOE_OK;
@@ -426,17 +421,6 @@ int moe_layer_status(moe_layer* L, int reset, int* status) {
   CK("moe_layer_status: read", cudaMemcpy(status, L->status, sizeof(int), cudaMemcpyDeviceToHost));
   if (reset) CK("moe_layer_status: reset", cudaMemset(L->status, 0, sizeof(int)));
   return MOE_OK;
-}
-
-int moe_layer_set_option(moe_layer* L, int option, int value) {
-  if (!L) return fail(MOE_EINVAL, "moe_layer_set_option: null layer");
-  switch (option) {
-    case MOE_OPT_DECODE_FUSED:
-      L->decode_fused = value != 0;
-      return MOE_OK;
-    default:
-      return fail(MOE_EINVAL, "moe_layer_set_option: unknown option %d", option);
-  }
 }
 
 int moe_forward_launches(moe_layer* L, int T) {
@@ -628,25 +612,26 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
   RouteParams rp = route_params(L, x, T);
   ExpertParams ep = expert_params(L, x, T);
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
-  if (decode_path(L, T)) {  // one kernel: phase 0 is the whole layer
-    if (phase == 0) CK("decode", launch_decode(rp, ep, out, L->grid_bar, st));
+  if (small_path(L, T)) {  // router; gate/up (routing inside); down + combine (routing inside)
+    if (phase < 0 || phase > 4) return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
+    if (phase == 0) CK("router", launch_router(rp, st));
+    if (phase == 2)
+      CK("gate/up", launch_gateup_routed(ep, rp, ep.nsh + max_routed_entries(T, L->E, L->k), st));
+    if (phase == 3) CK("down+combine", launch_down_combine_routed(ep, rp, out, st));
     return MOE_OK;
   }
-  const bool small = router_small_ok(T, L->k), fused = fused_down(L, T);
+  const bool fused = fused_down(L, T);
   switch (phase) {
     case 0:
       if (tc_router(L, T)) {
         const int rc = launch_tc_routing_gemm(L, x, T, st);
         if (rc) return rc;
-      } else if (small) {
-        CK("router", launch_router_small(rp, L->route_counter, st));
       } else {
         CK("router", launch_router(rp, st));
       }
       break;
     case 1:
-      if (small) break;
-      if (T <= 64) {
+      if (T <= 64 && !tc_router(L, T)) {
         CK("top-k/dispatch", launch_route_finish(rp, true, false, st));
       } else {
         CK("top-k", launch_topk(rp, false, st));

@@ -19,12 +19,11 @@
 namespace moe {
 namespace {
 
-// grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); 4 warps split
-// the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
-// (ksplit slice, token, expert) partial sum goes to p.partial; the top-k step
-// adds the slices in a fixed order.
+// grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); the 8 warps
+// split the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.
+// Each (ksplit slice, token, expert) partial sum goes to p.partial; the top-k
+// step adds the slices in a fixed order.
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
-  griddep_launch();
   extern __shared__ uint4 smem_u4[];
   router_partials(p, blockIdx.x, blockIdx.y, blockIdx.z, smem_u4);
 }
@@ -34,35 +33,6 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
   griddep_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t < p.T) topk_token(p, t, threadIdx.x & 31, nullptr);
-}
-
-// Router for T <= 8: the partial sums as in router_kernel, then the last CTA to
-// finish (a ticket from an atomic counter; nothing waits) does top-k, gates and
-// dispatch, and resets the counter for the next launch.
-__global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouteParams p, int* counter) {
-  griddep_launch();
-  extern __shared__ uint4 smem_u4[];
-  __shared__ int ticket;
-  __shared__ int sidx[kSmallSlots];
-  router_partials(p, blockIdx.x, blockIdx.y, blockIdx.z, smem_u4);
-  if (threadIdx.x < 32) __threadfence();  // warp 0 wrote this CTA's partial sums
-  __syncthreads();
-  if (threadIdx.x == 0) ticket = atomicAdd(counter, 1);
-  __syncthreads();
-  if (ticket != (int)(gridDim.x * gridDim.y * gridDim.z) - 1) return;
-  __threadfence();
-  __shared__ uint32_t cand_key[(kRouterThreads / 32) * kMaxK];
-  __shared__ int cand_id[(kRouterThreads / 32) * kMaxK];
-  for (int t = 0; t < p.T; ++t) {  // 8 warps share each token's top-k (E/8 experts each)
-    if (p.E <= 256)
-      topk_token_cta<1, 8>(p, t, sidx, cand_key, cand_id);
-    else if (p.E <= 512)
-      topk_token_cta<2, 8>(p, t, sidx, cand_key, cand_id);
-    else
-      topk_token_cta<4, 8>(p, t, sidx, cand_key, cand_id);
-  }
-  dispatch_small(p, reinterpret_cast<int*>(smem_u4), sidx);
-  if (threadIdx.x == 0) *counter = 0;
 }
 
 __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParams p, int do_topk) {
@@ -120,19 +90,8 @@ cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
   const int max_klen = ((C + p.ksplit - 1) / p.ksplit) * 64;
   const size_t smem = (size_t)kTokTile * (max_klen + 8) * 2 + kRouterThreads * 4 * sizeof(float);
   dim3 grid((p.E + 15) / 16, (p.T + kTokTile - 1) / kTokTile, p.ksplit);
-  return launch_k(router_kernel, grid, dim3(kRouterThreads), smem, st, false, p);
-}
-
-bool router_small_ok(int T, int k) { return T <= kTokTile && T * k <= kSmallSlots; }
-
-cudaError_t launch_router_small(const RouteParams& p, int* counter, cudaStream_t st) {
-  const int C = p.H / 64;
-  const int max_klen = ((C + p.ksplit - 1) / p.ksplit) * 64;
-  size_t smem = (size_t)kTokTile * (max_klen + 8) * 2 + kRouterThreads * 4 * sizeof(float);
-  const size_t disp = (size_t)(64 + p.E) * sizeof(int);
-  if (disp > smem) smem = disp;
-  dim3 grid((p.E + 15) / 16, 1, p.ksplit);
-  return launch_k(router_small_kernel, grid, dim3(kRouterThreads), smem, st, false, p, counter);
+  // launched early: only the weight reads run before the previous kernels finish
+  return launch_k(router_kernel, grid, dim3(kRouterThreads), smem, st, true, p);
 }
 
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st) {
@@ -147,9 +106,6 @@ cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cu
 cudaError_t route_kernels_init() {
   cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        200 * 1024);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           200 * 1024);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)route_finish_smem(kMaxE));

@@ -1,5 +1,6 @@
 // Device code of the routing step (router partial sums, top-k, dispatch),
-// shared by the stand-alone routing kernels and the decode megakernel.
+// shared by the routing kernels and the small-batch expert kernels, which
+// route a few tokens themselves.
 #pragma once
 
 #include <climits>
@@ -10,7 +11,7 @@
 namespace moe {
 namespace {
 
-constexpr int kRouterThreads = 256;  // the decode megakernel's block size: same partial-sum order
+constexpr int kRouterThreads = 256;
 constexpr int kFinishThreads = 1024;
 constexpr int kMaxKsplit = 8;  // router K slices at most
 
@@ -35,11 +36,30 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
   const int e0 = 16 * tile + gi, e1 = e0 + 8;
   const uint16_t* r0 = p.wr + (size_t)min(e0, p.E - 1) * p.H;
   const uint16_t* r1 = p.wr + (size_t)min(e1, p.E - 1) * p.H;
-  // start the router-weight reads before the activations are staged
-  for (int c = c_begin + warp; c < c_end; c += nwarps) {
-    prefetch_l2(r0 + 64 * c + 16 * t);
-    prefetch_l2(r1 + 64 * c + 16 * t);
+  // The router weights do not depend on earlier kernels: the warp's first
+  // chunk is loaded, and the rest requested from L2, before waiting for them.
+  auto load_a = [&](int c, uint32_t (&ra)[8], uint32_t (&rb)[8]) {
+    const int kc = 64 * c + 16 * t;
+    uint4 a00 = ldg_stream(r0 + kc), a01 = ldg_stream(r0 + kc + 8);
+    uint4 a10 = ldg_stream(r1 + kc), a11 = ldg_stream(r1 + kc + 8);
+    if (e0 >= p.E) a00 = a01 = make_uint4(0, 0, 0, 0);
+    if (e1 >= p.E) a10 = a11 = make_uint4(0, 0, 0, 0);
+    ra[0] = a00.x; ra[1] = a00.y; ra[2] = a00.z; ra[3] = a00.w;
+    ra[4] = a01.x; ra[5] = a01.y; ra[6] = a01.z; ra[7] = a01.w;
+    rb[0] = a10.x; rb[1] = a10.y; rb[2] = a10.z; rb[3] = a10.w;
+    rb[4] = a11.x; rb[5] = a11.y; rb[6] = a11.z; rb[7] = a11.w;
+  };
+  uint32_t ra[8], rb[8];
+  int c = c_begin + warp;
+  if (c < c_end) load_a(c, ra, rb);
+  for (int cc = c + nwarps; cc < c_end; cc += nwarps) {
+    prefetch_l2(r0 + 64 * cc + 16 * t);
+    prefetch_l2(r1 + 64 * cc + 16 * t);
   }
+  // x (and everything written below) waits for the kernels before this one;
+  // the next kernel may start once every CTA is past this point
+  griddep_wait();
+  griddep_launch();
   const bool write_xh = p.xh != nullptr && tile == 0;
   for (int i = threadIdx.x; i < n * (klen / 8); i += blockDim.x) {
     const int r = i / (klen / 8), v = i % (klen / 8);
@@ -61,14 +81,8 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
   __syncthreads();
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c = c_begin + warp; c < c_end; c += nwarps) {
+  for (; c < c_end; c += nwarps) {
     const int kc = 64 * c + 16 * t;
-    uint4 a00 = ldg_stream(r0 + kc), a01 = ldg_stream(r0 + kc + 8);
-    uint4 a10 = ldg_stream(r1 + kc), a11 = ldg_stream(r1 + kc + 8);
-    if (e0 >= p.E) a00 = a01 = make_uint4(0, 0, 0, 0);
-    if (e1 >= p.E) a10 = a11 = make_uint4(0, 0, 0, 0);
-    const uint32_t ra[8] = {a00.x, a00.y, a00.z, a00.w, a01.x, a01.y, a01.z, a01.w};
-    const uint32_t rb[8] = {a10.x, a10.y, a10.z, a10.w, a11.x, a11.y, a11.z, a11.w};
     uint32_t xw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (gi < n) {
       const uint4* px = reinterpret_cast<const uint4*>(xs + gi * stride + (kc - kbase));
@@ -81,6 +95,7 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
       const uint32_t a[4] = {ra[2 * w], rb[2 * w], ra[2 * w + 1], rb[2 * w + 1]};
       mma_bf16(acc, a, xw[2 * w], xw[2 * w + 1]);
     }
+    if (c + nwarps < c_end) load_a(c + nwarps, ra, rb);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) red[(warp * 32 + lane) * 4 + i] = acc[i];
@@ -99,10 +114,6 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
   }
 }
 
-// grid (ceil(E/16) expert tiles, ceil(T/8) token groups, ksplit); 4 warps split
-// the CTA's 64-column chunks; tensor cores take bf16 x bf16 -> fp32.  Each
-// (ksplit slice, token, expert) partial sum goes to p.partial; the top-k step
-// adds the slices in a fixed order.
 // ---------------------------------------------------------------- top-k (one warp per token)
 // Order-preserving map of an fp32 value to a uint32 key (larger value, larger key).
 __device__ __forceinline__ uint32_t f32_key(float v) {
@@ -137,11 +148,12 @@ __device__ __forceinline__ void warp_argmax_round(uint32_t (&key)[V], const int 
 // router's K-split slices added in order, then the bias; written to p.logits.
 template <int V>
 __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0, int e_end,
-                                            int lane, uint32_t (&key)[V], int (&id)[V]) {
+                                            int lane, uint32_t (&key)[V], int (&id)[V],
+                                            bool pub = true) {
   float v[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) v[i] = 0.f;
-  if constexpr (V <= 4) {  // few slots: every K slice requested at once
+  if constexpr (V <= 4) {  // few slots: every slice requested at once
     float part[kMaxKsplit][V];
 #pragma unroll
     for (int s = 0; s < kMaxKsplit; ++s)
@@ -159,7 +171,7 @@ __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0,
     for (int s = 0; s < p.ksplit; ++s) {
       const float* ps = p.partial + ((size_t)s * p.T + t) * p.E;
 #pragma unroll
-      for (int i = 0; i < V; ++i)  // written by other CTAs: read through L2
+      for (int i = 0; i < V; ++i)
         if (e0 + lane + 32 * i < e_end) v[i] += __ldcg(ps + e0 + lane + 32 * i);
     }
   }
@@ -170,7 +182,7 @@ __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0,
     if (e < e_end) {
       float l = v[i];
       if (p.bias) l = l + p.bias[e];
-      if (p.logits) p.logits[(size_t)t * p.E + e] = l;
+      if (pub && p.logits) p.logits[(size_t)t * p.E + e] = l;
       key[i] = f32_key(l);
     } else {
       key[i] = 0u;  // below every real key
@@ -180,7 +192,8 @@ __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0,
 
 // Gates = softmax of the k selected logits (lane j < k holds pick j).
 __device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lane, uint32_t my_key,
-                                            int my_i, int* sidx, float* sgates = nullptr) {
+                                            int my_i, int* sidx, float* sgates = nullptr,
+                                            bool pub = true) {
   const int k = p.k;
   const float my_v = key_f32(my_key);
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
@@ -189,8 +202,8 @@ __device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lan
 #pragma unroll
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
-    if (p.idx) p.idx[(size_t)t * k + lane] = my_i;
-    if (p.gates) p.gates[(size_t)t * k + lane] = ex / sum;
+    if (pub && p.idx) p.idx[(size_t)t * k + lane] = my_i;
+    if (pub && p.gates) p.gates[(size_t)t * k + lane] = ex / sum;
     if (sidx) sidx[t * k + lane] = my_i;
     if (sgates) sgates[t * k + lane] = ex / sum;
   }
@@ -200,10 +213,10 @@ __device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lan
 // the lower expert index), then the softmax of the k selected logits.
 template <int V>
 __device__ void topk_token_v(const RouteParams& p, int t, int lane, int* sidx,
-                             float* sgates = nullptr) {
+                             float* sgates = nullptr, bool pub = true) {
   uint32_t key[V];
   int id[V];
-  load_logits<V>(p, t, 0, p.E, lane, key, id);
+  load_logits<V>(p, t, 0, p.E, lane, key, id, pub);
   uint32_t my_key = 0;
   int my_i = 0;
   for (int j = 0; j < p.k; ++j) {
@@ -215,17 +228,17 @@ __device__ void topk_token_v(const RouteParams& p, int t, int lane, int* sidx,
       my_i = win;
     }
   }
-  write_gates(p, t, lane, my_key, my_i, sidx, sgates);
+  write_gates(p, t, lane, my_key, my_i, sidx, sgates, pub);
 }
 
 __device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx,
-                           float* sgates = nullptr) {
+                           float* sgates = nullptr, bool pub = true) {
   if (p.E <= 256)
-    topk_token_v<8>(p, t, lane, sidx, sgates);
+    topk_token_v<8>(p, t, lane, sidx, sgates, pub);
   else if (p.E <= 512)
-    topk_token_v<16>(p, t, lane, sidx, sgates);
+    topk_token_v<16>(p, t, lane, sidx, sgates, pub);
   else
-    topk_token_v<32>(p, t, lane, sidx, sgates);
+    topk_token_v<32>(p, t, lane, sidx, sgates, pub);
 }
 
 // Top-k of token t by all warps of the CTA: each of the NW warps takes a
@@ -235,12 +248,12 @@ __device__ void topk_token(const RouteParams& p, int t, int lane, int* sidx,
 // ck / ci: NW * kMaxK entries of shared memory.
 template <int V1, int V2>
 __device__ void topk_token_cta(const RouteParams& p, int t, int* sidx, uint32_t* ck, int* ci,
-                               float* sgates = nullptr) {
+                               float* sgates = nullptr, bool pub = true) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, k = p.k, NW = blockDim.x >> 5;
   const int q = (p.E + NW - 1) / NW;
   uint32_t key[V1];
   int id[V1];
-  load_logits<V1>(p, t, warp * q, min(p.E, (warp + 1) * q), lane, key, id);
+  load_logits<V1>(p, t, warp * q, min(p.E, (warp + 1) * q), lane, key, id, pub);
   for (int j = 0; j < k; ++j) {
     uint32_t best;
     int win;
@@ -285,7 +298,7 @@ __device__ void topk_token_cta(const RouteParams& p, int t, int* sidx, uint32_t*
         my_i = win;
       }
     }
-    write_gates(p, t, lane, my_key, my_i, sidx, sgates);
+    write_gates(p, t, lane, my_key, my_i, sidx, sgates, pub);
   }
   __syncthreads();
 }
@@ -391,89 +404,145 @@ __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
   }
 }
 
-// Dispatch for a few slots (T*k <= kSmallSlots) by any block size: the same
-// result as dispatch_block (expert-major, stable), with a per-expert count
-// table and a direct stable rank.  smem: 64 + E + S ints.
+// slots of the few-token path (T * k at most)
 constexpr int kSmallSlots = 256;
 
-// sidx: the S expert ids in shared memory (already written and synchronised)
-__device__ void dispatch_small(const RouteParams& p, int* smem, int* sidx) {
-  const int S = p.T * p.k, E = p.E, nt = blockDim.x, tid = threadIdx.x;
-  if (p.T == 1) {  // k distinct experts, one row each: rank the picks by expert id in one warp
-    const int k = p.k, lane = tid & 31;
-    if (tid < 32) {
-      const int e = lane < k ? checked_expert(p, sidx[lane]) : INT_MAX;
+// ---------------------------------------------------------------- routing of a few tokens by one CTA
+// For T <= kTokTile tokens no expert can receive more than kTokTile slots, so
+// every routed expert is exactly one work entry.  The small-batch expert
+// kernels route in every CTA from the router's partial sums (a few KB read
+// through L2) instead of waiting for a separate routing kernel.
+struct SmallRoute {
+  int4 entries[kSmallSlots];  // {expert, first row, tokens, 0}, expert order
+  int inv[kSmallSlots];       // row of each slot
+  int row_token[kSmallSlots + kTokTile];
+  float gates[kSmallSlots];
+  int sidx[kSmallSlots];      // expert of each slot
+  int lt[kSmallSlots];        // per slot: slots with a smaller expert id
+  int cnt[kSmallSlots];       // per slot: slots with the same expert
+  int lead[kSmallSlots];      // per slot: first slot of its expert
+  uint32_t ck[16 * kMaxK];    // per-warp top-k candidates (T == 1)
+  int ci[16 * kMaxK];
+  int n_entries;
+};
+
+// Top-k, gates and the stable expert-major dispatch of T <= kTokTile tokens,
+// T * k <= min(kSmallSlots, blockDim.x), by every thread of the block (at most
+// 16 warps); results in r, and, when `pub`, in the global outputs of p
+// (logits, idx, gates, perm, inv, row_token, entries, n_entries).  Row of slot
+// s: pos(s) = #{q : e_q < e_s} + #{q < s : e_q == e_s}, which is the dispatch
+// of dispatch_block.  Ends synchronised.
+template <int V2>
+__device__ void topk_one_token_cta(const RouteParams& p, SmallRoute& r, bool pub) {
+  const int NW = blockDim.x >> 5, q = (p.E + NW - 1) / NW;
+  if (q <= 32)
+    topk_token_cta<1, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates, pub);
+  else if (q <= 64)
+    topk_token_cta<2, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates, pub);
+  else
+    topk_token_cta<4, V2>(p, 0, r.sidx, r.ck, r.ci, r.gates, pub);
+}
+
+__device__ __noinline__ void route_small_cta(const RouteParams& p, SmallRoute& r, bool pub) {
+  const int T = p.T, k = p.k, S = T * k;
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31, NW = nt >> 5;
+  if (T == 1) {  // all warps share the token: E / NW experts each, then one merge
+    if (NW * k <= 32 * 3)
+      topk_one_token_cta<3>(p, r, pub);
+    else if (NW * k <= 32 * 9)
+      topk_one_token_cta<9>(p, r, pub);
+    else
+      topk_one_token_cta<16>(p, r, pub);
+  } else {  // one warp per token
+    for (int t = warp; t < T; t += NW) topk_token(p, t, lane, r.sidx, r.gates, pub);
+    __syncthreads();
+  }
+  if (T == 1) {  // k distinct experts, one row each: the entries are the picks sorted by id
+    if (warp == 0) {
+      const int e = lane < k ? r.sidx[lane] : INT_MAX;
       int rank = 0;
       for (int l = 0; l < k; ++l) rank += __shfl_sync(0xffffffffu, e, l) < e;
       if (lane < k) {
-        if (p.perm) p.perm[rank] = lane;
-        p.inv[lane] = rank;
-        p.row_token[rank] = 0;
-        p.entries[rank] = make_int4(e, rank, 1, 0);
+        r.inv[lane] = rank;
+        r.row_token[rank] = 0;
+        r.entries[rank] = make_int4(e, rank, 1, 0);
+        if (pub) {
+          p.perm[rank] = lane;
+          p.inv[lane] = rank;
+          p.row_token[rank] = 0;
+          p.entries[rank] = make_int4(e, rank, 1, 0);
+        }
       }
       if (lane == 0) {
-        p.row_token[k] = 0;  // the shared expert's row
-        *p.n_entries = k;
-      }
-    }
-    if (p.counts || p.offsets) {  // diagnostic outputs
-      for (int e = tid; e < E; e += nt) {
-        int c = 0, off = 0;
-        for (int l = 0; l < k; ++l) {
-          c += sidx[l] == e;
-          off += sidx[l] < e;
+        r.row_token[k] = 0;  // the shared expert's row
+        r.n_entries = k;
+        if (pub) {
+          p.row_token[k] = 0;
+          *p.n_entries = k;
         }
-        if (p.counts) p.counts[e] = c;
-        if (p.offsets) p.offsets[e] = off;
       }
-      if (tid == 0 && p.offsets) p.offsets[E] = k;
     }
+    __syncthreads();
     return;
   }
-  int* sc = smem;
-  int* cnt = smem + 64;
-  for (int e = tid; e < E; e += nt) cnt[e] = 0;
-  for (int s = tid; s < S; s += nt) sidx[s] = checked_expert(p, sidx[s]);
-  __syncthreads();
-  for (int s = tid; s < S; s += nt) atomicAdd(&cnt[sidx[s]], 1);
-  __syncthreads();
-  const int ept = (E + nt - 1) / nt;
-  const int lo = min(E, tid * ept), hi = min(E, lo + ept);
-  int local = 0, lnch = 0;
-  for (int e = lo; e < hi; ++e) {
-    local += cnt[e];
-    lnch += (cnt[e] + kTokTile - 1) / kTokTile;
+  int is_lead = 0;
+  for (int s = tid; s < S; s += nt) {
+    const int e = r.sidx[s];
+    int lt = 0, before = 0, cnt = 0;
+    for (int q = 0; q < S; ++q) {
+      const int f = r.sidx[q];
+      lt += f < e;
+      cnt += f == e;
+      before += (f == e) & (q < s);
+    }
+    const int pos = lt + before;
+    r.inv[s] = pos;
+    r.row_token[pos] = s / k;
+    r.lt[s] = lt;
+    r.cnt[s] = cnt;
+    r.lead[s] = before == 0;
+    is_lead = before == 0;
+    if (pub) {
+      p.perm[pos] = s;
+      p.inv[s] = pos;
+      p.row_token[pos] = s / k;
+    }
   }
-  int total, n_total;
-  int run = block_excl_scan(local, sc, &total);
-  int runn = block_excl_scan(lnch, sc, &n_total);
-  for (int e = lo; e < hi; ++e) {
-    const int c = cnt[e];
-    if (p.counts) p.counts[e] = c;
-    if (p.offsets) p.offsets[e] = run;
-    for (int i = 0; i * kTokTile < c; ++i)
-      p.entries[runn + i] = make_int4(e, run + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
-    cnt[e] = run;
-    run += c;
-    runn += (c + kTokTile - 1) / kTokTile;
+  for (int t = tid; t < T; t += nt) {
+    r.row_token[S + t] = t;
+    if (pub) p.row_token[S + t] = t;
+  }
+  const int n_ent = __syncthreads_count(is_lead);  // one slot per thread at most
+  for (int s = tid; s < S; s += nt) {
+    if (!r.lead[s]) continue;
+    const int e = r.sidx[s];
+    int d = 0;
+    for (int q = 0; q < S; ++q) d += r.lead[q] & (r.sidx[q] < e);
+    const int4 en = make_int4(e, r.lt[s], r.cnt[s], 0);
+    r.entries[d] = en;
+    if (pub) p.entries[d] = en;
   }
   if (tid == 0) {
-    if (p.offsets) p.offsets[E] = total;
-    *p.n_entries = n_total;
+    r.n_entries = n_ent;
+    if (pub) *p.n_entries = n_ent;
   }
   __syncthreads();
-  for (int s = tid; s < S; s += nt) {
-    const int e = sidx[s];
-    int r = 0;
-    for (int q = 0; q < s; ++q) r += (sidx[q] == e);
-    const int pos = cnt[e] + r;
-    if (p.perm) p.perm[pos] = s;
-    p.inv[s] = pos;
-    p.row_token[pos] = s / p.k;
-  }
-  for (int t = tid; t < p.T; t += nt) p.row_token[S + t] = t;
 }
 
+// counts[E] and offsets[E + 1] of a routing held in r (diagnostic outputs).
+__device__ __noinline__ void publish_counts(const RouteParams& p, const SmallRoute& r) {
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    int c = 0, off = 0;
+    for (int d = 0; d < r.n_entries; ++d) {
+      const int4 en = r.entries[d];
+      c += en.x == e ? en.z : 0;
+      off += en.x < e ? en.z : 0;
+    }
+    if (p.counts) p.counts[e] = c;
+    if (p.offsets) p.offsets[e] = off;
+  }
+  if (threadIdx.x == 0 && p.offsets) p.offsets[p.E] = p.T * p.k;
+}
 
 }  // namespace
 }  // namespace moe

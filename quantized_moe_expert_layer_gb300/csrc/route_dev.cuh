@@ -254,25 +254,31 @@ __device__ void topk_token_cta(const RouteParams& p, int t, int* sidx, uint32_t*
   uint32_t key[V1];
   int id[V1];
   load_logits<V1>(p, t, warp * q, min(p.E, (warp + 1) * q), lane, key, id, pub);
+  uint32_t c_key = 0;  // lane j keeps the warp's pick j
+  int c_id = 0x7FFFFFFF;
   for (int j = 0; j < k; ++j) {
     uint32_t best;
     int win;
     warp_argmax_round<V1>(key, id, best, win);
-    if (lane == 0) {
-      ck[warp * kMaxK + j] = best;
-      ci[warp * kMaxK + j] = win;
+    if (lane == j) {
+      c_key = best;
+      c_id = win;
     }
+  }
+  if (lane < k) {  // candidates packed: warp w's picks at w * k ...
+    ck[warp * k + lane] = c_key;
+    ci[warp * k + lane] = c_id;
   }
   __syncthreads();
   if (warp == 0) {
     uint32_t k2[V2];
     int i2[V2];
 #pragma unroll
-    for (int i = 0; i < V2; ++i) {  // candidate c = lane + 32 i: warp c / k, pick c % k
+    for (int i = 0; i < V2; ++i) {  // candidate c = lane + 32 i
       const int c = lane + 32 * i;
       const bool ok = c < NW * k;
-      k2[i] = ok ? ck[(c / k) * kMaxK + c % k] : 0u;
-      i2[i] = ok ? ci[(c / k) * kMaxK + c % k] : 0x7FFFFFFF;
+      k2[i] = ok ? ck[c] : 0u;
+      i2[i] = ok ? ci[c] : 0x7FFFFFFF;
     }
     // order each lane's slots by expert id so that ties keep the lower id
 #pragma unroll

@@ -387,7 +387,7 @@ def run_ours(args, w):
                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                     "algorithmic_flops_per_launch": work}
     else:
-        kname = "gateup_kernel"
+        kname = "gateup_routed_kernel" if T <= 8 else "gateup_kernel"
         peak, peak_kind = peaks("hbm")
         achieved = work / (k_us * 1e-6) / 1e9
         roofline = {"bound": "hbm", "kernel": kname + " (gate/up + SwiGLU)", "achieved": achieved,

@@ -28,8 +28,10 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- gate/up + SwiGLU
-template <int FMT>
-__global__ void __launch_bounds__(kThreads, 2) gateup_kernel(ExpertParams p, int tpc) {
+// SMEM: the NVFP4 tile pair through shared memory (gateup_task_nv, one tile
+// pair per CTA, several CTAs per SM); otherwise registers (gateup_task).
+template <int FMT, bool SMEM>
+__global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_kernel(ExpertParams p, int tpc) {
   const int y = blockIdx.y;
   // Shared-expert entries need no routing.  Routed ones wait for it, and only
   // then let the next kernel start: once every CTA here has triggered, the
@@ -40,34 +42,51 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(ExpertParams p, int
   int expert, row, n;
   if (!get_entry(p, y, expert, row, n)) return;
   __shared__ float red[kThreads * 8];
-  gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
+  if constexpr (SMEM) {
+    extern __shared__ __align__(16) uint8_t gu_smem[];
+    gateup_task_nv(p, expert, row, n, blockIdx.x, gu_smem, red, false);
+  } else {
+    gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
+  }
 }
 
 // Gate/up for T <= 8 tokens that routes itself: every routed CTA takes the
 // top-k and the dispatch from the router's partial sums (a few KB through
 // L2) instead of waiting for a routing kernel and reading its work entries;
-// CTA (0, first routed) also publishes the routing.  The shared expert's CTAs
-// run at once.
-template <int FMT>
-__global__ void __launch_bounds__(kThreads, 2) gateup_routed_kernel(ExpertParams p, RouteParams rp, int tpc) {
+// CTA (0, first routed) also publishes the routing for the down kernel (which
+// reads it after its wait).  Every CTA, once its gate/up weights have landed,
+// asks L2 for its share of its expert's down matrix, so the down kernel reads
+// its weights from L2.  The shared expert's CTAs run at once.
+template <int FMT, bool SMEM>
+__global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_routed_kernel(ExpertParams p, RouteParams rp, int tpc) {
   const int y = blockIdx.y;
   __shared__ float red[kThreads * 8];
+  extern __shared__ __align__(16) uint8_t gu_smem[];
   if (y < p.nsh) {
+    griddep_launch();
     int expert, row, n;
-    if (get_entry(p, y, expert, row, n)) gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
+    if (get_entry(p, y, expert, row, n)) {
+      if constexpr (SMEM)
+        gateup_task_nv(p, expert, row, n, blockIdx.x, gu_smem, red, true);
+      else
+        gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
+    }
     return;
   }
   __shared__ SmallRoute rt;
-  griddep_wait();  // the router's partial sums
+  griddep_wait();  // the router's partial sums and f16 copy of x
   const bool pub = y == p.nsh && blockIdx.x == 0;
   route_small_cta(rp, rt, pub);
-  griddep_launch();  // the next kernel routes itself from the same partial sums
+  griddep_launch();
   const int d = y - p.nsh;
   if (d < rt.n_entries) {
     const int4 e = rt.entries[d];
     ExpertParams el = p;  // the routed rows' tokens from shared memory
     el.row_token = rt.row_token;
-    gateup_task<FMT>(el, e.x, e.y, e.z, blockIdx.x, tpc, red);
+    if constexpr (SMEM)
+      gateup_task_nv(el, e.x, e.y, e.z, blockIdx.x, gu_smem, red, true);
+    else
+      gateup_task<FMT>(el, e.x, e.y, e.z, blockIdx.x, tpc, red);
   }
   if (pub) publish_counts(rp, rt);
 }
@@ -149,41 +168,39 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertParams p, const floa
 // for gate/up.
 constexpr int kDcMaxWarps = 12;
 
-template <int FMT>
+// WAIT_FIRST: the routing is published by the kernel before this one (the
+// self-routed gate/up), so nothing is read before the wait; the weights come
+// from L2, where gate/up asked for them.  Otherwise the routing is complete
+// before gate/up starts, and the first entry's tile is loaded into registers
+// and the others requested from L2 before the wait.  Either way the next
+// kernel may start at once (it waits for this whole grid before it reads
+// anything this one writes).
+template <int FMT, bool WAIT_FIRST>
 __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertParams p,
                                                                          const float* gates,
                                                                          const int* inv, float* out) {
-  // routing is complete here (gate/up triggered this launch only after its wait):
-  // the weights are read before waiting for gate/up
+  griddep_launch();
   DownPreload pre;
   bool have = false;
-  if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
-  down_prefetch<FMT>(p, blockIdx.x);  // (the rest: into L2)
+  if (!WAIT_FIRST) {
+    if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
+    down_prefetch<FMT>(p, blockIdx.x);  // (the rest: into L2)
+  }
   griddep_wait();  // gate/up complete: abuf holds every row
+  __shared__ float sg[kTokTile * kMaxK];
+  __shared__ int si[kTokTile * kMaxK];
+  if (WAIT_FIRST) {
+    // every entry's tile requested at once, then the combine's gates and rows
+    if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
+    for (int i = threadIdx.x; i < p.T * p.k; i += blockDim.x) {
+      sg[i] = gates[i];
+      si[i] = inv[i];
+    }
+    gates = sg;  // read after the task's barrier
+    inv = si;
+  }
   extern __shared__ float ys[];  // [rows x 16]
   down_combine_task<FMT>(p, blockIdx.x, gates, inv, out, ys, pre, have);
-}
-
-// The same for T <= 8 with routing in the CTA: the router finished before
-// gate/up let this launch start, so its partial sums are final; the top-k,
-// the dispatch and the weights all come before waiting for gate/up.
-template <int FMT>
-__global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_routed_kernel(ExpertParams p,
-                                                                                RouteParams rp,
-                                                                                float* out) {
-  __shared__ SmallRoute rt;
-  route_small_cta(rp, rt, false);
-  ExpertParams el = p;
-  el.entries = rt.entries;
-  el.n_entries = &rt.n_entries;
-  el.row_token = rt.row_token;
-  DownPreload pre;
-  bool have = false;
-  if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(el, blockIdx.x, threadIdx.x >> 5, pre);
-  down_prefetch<FMT>(el, blockIdx.x);
-  griddep_wait();  // gate/up complete: abuf holds every row
-  extern __shared__ float ys[];
-  down_combine_task<FMT>(el, blockIdx.x, rt.gates, rt.inv, out, ys, pre, have);
 }
 
 size_t down_combine_smem(int T, int k, int shared) {
@@ -194,13 +211,26 @@ size_t down_combine_smem(int T, int k, int shared) {
 
 }  // namespace
 
+// Dynamic shared memory the NVFP4 gate/up kernels may use (set in
+// expert_kernels_init); larger shapes take the register kernels.
+constexpr int kNvMaxDyn = 160 * 1024;
+
+// (T <= 8 only: for larger batches, entries of up to 8 tokens stream faster
+// through the register kernels, which keep two units per warp in flight)
+bool gateup_smem_ok(const ExpertParams& p) {
+  return p.fmt == FMT_NVFP4 && p.T <= kTokTile && gateup_nv_smem(p.H, p.T) <= kNvMaxDyn;
+}
+
 cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
-  const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
   const int pairs = p.I / 16;
+  if (gateup_smem_ok(p))
+    return launch_k(gateup_kernel<FMT_NVFP4, true>, dim3(pairs, grid_y), dim3(kThreads),
+                    gateup_nv_smem(p.H, p.T), st, pdl, p, 1);
+  const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
   dim3 grid((pairs + tpc - 1) / tpc, grid_y);
   if (p.fmt == FMT_NVFP4)
-    return launch_k(gateup_kernel<FMT_NVFP4>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
-  return launch_k(gateup_kernel<FMT_FP6>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
+    return launch_k(gateup_kernel<FMT_NVFP4, false>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
+  return launch_k(gateup_kernel<FMT_FP6, false>, grid, dim3(kThreads), 0, st, pdl, p, tpc);
 }
 
 cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
@@ -226,44 +256,43 @@ bool down_combine_ok(int T, int k, int shared, int I) {
 }
 
 cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const int* inv,
-                                float* out, bool pdl, cudaStream_t st) {
+                                float* out, bool pdl, bool wait_first, cudaStream_t st) {
   // one warp per work entry (the routed entries are at most T*k for T <= 8)
   int warps = p.nsh + (p.T * p.k < p.E ? p.T * p.k : p.E);
   if (warps > kDcMaxWarps) warps = kDcMaxWarps;
   const size_t smem = down_combine_smem(p.T, p.k, p.shared);
+  const dim3 grid(p.H / 16), block(32 * warps);
   if (p.fmt == FMT_NVFP4)
-    return launch_k(down_combine_kernel<FMT_NVFP4>, dim3(p.H / 16), dim3(32 * warps), smem, st,
-                    pdl, p, gates, inv, out);
-  return launch_k(down_combine_kernel<FMT_FP6>, dim3(p.H / 16), dim3(32 * warps), smem, st, pdl, p,
-                  gates, inv, out);
+    return wait_first
+               ? launch_k(down_combine_kernel<FMT_NVFP4, true>, grid, block, smem, st, pdl, p, gates, inv, out)
+               : launch_k(down_combine_kernel<FMT_NVFP4, false>, grid, block, smem, st, pdl, p, gates, inv, out);
+  return wait_first
+             ? launch_k(down_combine_kernel<FMT_FP6, true>, grid, block, smem, st, pdl, p, gates, inv, out)
+             : launch_k(down_combine_kernel<FMT_FP6, false>, grid, block, smem, st, pdl, p, gates, inv, out);
 }
 
 bool small_route_ok(int T, int k) { return T <= kTokTile && T * k <= kSmallSlots; }
 
 cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, int grid_y,
                                  cudaStream_t st) {
-  const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
   const int pairs = p.I / 16;
+  if (gateup_smem_ok(p))
+    return launch_k(gateup_routed_kernel<FMT_NVFP4, true>, dim3(pairs, grid_y), dim3(kThreads),
+                    gateup_nv_smem(p.H, p.T), st, true, p, rp, 1);
+  const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
   dim3 grid((pairs + tpc - 1) / tpc, grid_y);
   if (p.fmt == FMT_NVFP4)
-    return launch_k(gateup_routed_kernel<FMT_NVFP4>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
-  return launch_k(gateup_routed_kernel<FMT_FP6>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
+    return launch_k(gateup_routed_kernel<FMT_NVFP4, false>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
+  return launch_k(gateup_routed_kernel<FMT_FP6, false>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
 }
 
-cudaError_t launch_down_combine_routed(const ExpertParams& p, const RouteParams& rp, float* out,
-                                       cudaStream_t st) {
-  // one warp per work entry, at least 8 warps (the routing wants the slots covered)
-  int warps = p.nsh + (p.T * p.k < p.E ? p.T * p.k : p.E);
-  if (warps > kDcMaxWarps) warps = kDcMaxWarps;
-  if (warps < 8) warps = 8;
-  const size_t smem = down_combine_smem(p.T, p.k, p.shared);
-  if (p.fmt == FMT_NVFP4)
-    return launch_k(down_combine_routed_kernel<FMT_NVFP4>, dim3(p.H / 16), dim3(32 * warps), smem, st,
-                    true, p, rp, out);
-  return launch_k(down_combine_routed_kernel<FMT_FP6>, dim3(p.H / 16), dim3(32 * warps), smem, st, true,
-                  p, rp, out);
+cudaError_t expert_kernels_init() {
+  cudaError_t e = cudaFuncSetAttribute(gateup_kernel<FMT_NVFP4, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kNvMaxDyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_NVFP4, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kNvMaxDyn);
+  return e;
 }
-
-cudaError_t expert_kernels_init() { return cudaSuccess; }
 
 }  // namespace moe

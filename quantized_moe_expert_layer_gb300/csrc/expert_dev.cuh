@@ -3,6 +3,7 @@
 // the decode megakernel.
 #pragma once
 
+#include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 #include "layout.cuh"
@@ -62,8 +63,9 @@ template <int NT>
 __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], const MatGeom& g,
                                             int h0, int dh, const uint16_t* brow, bool b_bf16,
                                             float (&acc)[NT][4]) {
-  const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int lane = threadIdx.x & 31, t = lane & 3;
   const int nh = n_halves(g);
+  float acc2[NT][2][4] = {};  // even / odd chunks: two shorter mma chains per tile
   for (int hh = h0; hh < nh; hh += dh) {
     const int s = hh >> 1, jb = (hh & 1) * 4;
     const int nc = min(4, sc_units(g, s) - jb);
@@ -94,12 +96,16 @@ __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], co
             e2m1x8_to_f16x8(u4get(cv[i][j], w), h);
             const uint32_t a[4] = {hmul2(h[0], s_lo), hmul2(h[1], s_hi), hmul2(h[2], s_lo),
                                    hmul2(h[3], s_hi)};
-            mma_f16(acc[i], a, xb[j][2 * w], xb[j][2 * w + 1]);
+            mma_f16(acc2[i][jj & 1], a, xb[j][2 * w], xb[j][2 * w + 1]);
           }
         }
       }
     }
   }
+#pragma unroll
+  for (int i = 0; i < NT; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[i][r] += acc2[i][0][r] + acc2[i][1][r];
 }
 
 __device__ __forceinline__ void fp6_unpack(uint32_t Ha, uint32_t Hb, uint32_t L, uint32_t (&c)[4]) {
@@ -314,6 +320,184 @@ __device__ __forceinline__ void gateup_task(const ExpertParams& p, int expert, i
 }
 
 
+// ---------------------------------------------------------------- NVFP4 gate/up through shared memory
+// A CTA takes one tile pair over the whole K; warp w takes the 256-column
+// units w, w + 8, ... of both tiles (per unit and tile: the scale vector and
+// up to 4 code vectors, 2.5 KB) together with the entry's token rows over the
+// same 256 columns.  The warp copies them into its own stage of shared memory
+// with cp.async, so no registers wait on HBM: a CTA needs few of them,
+// several CTAs share an SM, and a decode step has every weight byte requested
+// at once.  Each warp starts its math as soon as its own copies have landed
+// (no CTA-wide barrier before the K-split reduction).  For T <= 8 tokens:
+// the staged token rows (f16, or bf16 converted on read for the shared
+// expert's entries) sit in slot = token, so an entry may hold any number of
+// rows (e.g. a token that picked one expert twice); rows are padded by 16
+// bytes so that the B-fragment reads of 8 slots hit distinct banks.
+constexpr int kNvUnitBytes = 2 * 5 * 512;
+constexpr int kNvXStride = 256 + 8;  // halfs per staged token-row slice
+
+__host__ __device__ __forceinline__ int gateup_nv_stages(int K) {
+  return (K + 255) / 256 > kWarps ? 2 : 1;
+}
+__host__ __device__ __forceinline__ int gateup_nv_stage_bytes(int T) {
+  return kNvUnitBytes + T * kNvXStride * 2;
+}
+__host__ __device__ __forceinline__ size_t gateup_nv_smem(int K, int T) {
+  return (size_t)kWarps * gateup_nv_stages(K) * gateup_nv_stage_bytes(T);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+// cp.async of unit hh (both tiles, and the token rows over its columns) into
+// the stage at `dst`.  tok_of(r): token of row r of the entry.
+template <typename TokOf>
+__device__ __forceinline__ void nv_unit_copy(const uint8_t* const (&tile)[2], const MatGeom& g,
+                                             int hh, uint32_t dst, const uint16_t* xsrc, int H,
+                                             int n, int T, TokOf tok_of) {
+  const int lane = threadIdx.x & 31;
+  const int s = hh >> 1, jb = (hh & 1) * 4;
+  const int nc = min(4, sc_units(g, s) - jb);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint8_t* b = tile[i] + (size_t)s * g.sc_bytes + 16 * lane;
+    const uint32_t d = dst + i * 2560 + 16 * lane;
+    cp_async16(d, b);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < nc) cp_async16(d + 512 * (1 + j), b + 512 * (1 + jb + j));
+  }
+  const int pieces = nc * 8, col0 = 256 * hh;  // 16-byte pieces of a row slice
+  for (int i = lane; i < n * pieces; i += 32) {
+    const int r = i / pieces, c = i - r * pieces;
+    const int tok = tok_of(r);
+    if ((unsigned)tok < (unsigned)T)
+      cp_async16(dst + kNvUnitBytes + 2 * (tok * kNvXStride + 8 * c),
+                 xsrc + (size_t)tok * H + col0 + 8 * c);
+  }
+}
+
+// Unit hh of both tiles (staged at `st`) times the staged token rows, into
+// two accumulators per tile (even / odd chunks: shorter mma chains).
+__device__ __forceinline__ void nv_unit_mma(const MatGeom& g, int hh, uint32_t st, int xslot,
+                                            bool b_bf16, float (&acc)[2][2][4]) {
+  const int lane = threadIdx.x & 31, t = lane & 3;
+  const int s = hh >> 1, jb = (hh & 1) * 4;
+  const int nc = min(4, sc_units(g, s) - jb);
+  const uint4 sv[2] = {lds128(st + 16 * lane), lds128(st + 2560 + 16 * lane)};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j < nc) {
+      const int jj = jb + j;
+      uint32_t xb[8];
+      if (xslot >= 0) {
+        const uint32_t xa = st + kNvUnitBytes + 2 * (xslot * kNvXStride + 64 * j + 16 * t);
+        const uint4 q0 = lds128(xa), q1 = lds128(xa + 16);
+        xb[0] = q0.x; xb[1] = q0.y; xb[2] = q0.z; xb[3] = q0.w;
+        xb[4] = q1.x; xb[5] = q1.y; xb[6] = q1.z; xb[7] = q1.w;
+        if (b_bf16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(xb[q] << 16),
+                                                __uint_as_float(xb[q] & 0xFFFF0000u));
+            xb[q] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xb[q] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 cv = lds128(st + i * 2560 + 512 * (1 + j) + 16 * lane);
+        const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], jj >> 1) >> (16 * (jj & 1))) & 0xFFFFu);
+        const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t h[4];
+          e2m1x8_to_f16x8(u4get(cv, w), h);
+          const uint32_t a[4] = {hmul2(h[0], s_lo), hmul2(h[1], s_hi), hmul2(h[2], s_lo),
+                                 hmul2(h[3], s_hi)};
+          mma_f16(acc[i][j & 1], a, xb[2 * w], xb[2 * w + 1]);
+        }
+      }
+    }
+  }
+}
+
+// Tile pair `pair` of `expert` for the n tokens of rows row..row+n-1, T <= 8.
+// smem: gateup_nv_smem(H, T) bytes (16-byte aligned); red: kThreads x 8 floats.  prefetch_down: also ask L2 for this CTA's share (1/gridDim.x) of
+// the expert's down matrix, for a down kernel that starts after this one.
+__device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert, int row, int n,
+                                               int pair, uint8_t* smem, float* red,
+                                               bool prefetch_down) {
+  const int S = p.T * p.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const MatGeom g = mat_geom(FMT_NVFP4, p.H);
+  const int nh = n_halves(g), nst = gateup_nv_stages(p.H);
+  const int sbytes = gateup_nv_stage_bytes(p.T);
+  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
+  const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
+                                   eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
+  const uint32_t wst = smem_u32(smem) + warp * nst * sbytes;
+  const bool shared_entry = expert == p.E;
+  const uint16_t* xsrc = shared_entry ? p.x : p.xh;
+  auto tok_of = [&](int r) { return shared_entry ? row - S + r : p.row_token[row + r]; };
+  if (warp < nh) nv_unit_copy(tiles, g, warp, wst, xsrc, p.H, n, p.T, tok_of);
+  cp_async_commit();
+  if (nst > 1 && warp + kWarps < nh)
+    nv_unit_copy(tiles, g, warp + kWarps, wst + sbytes, xsrc, p.H, n, p.T, tok_of);
+  cp_async_commit();
+  int xslot = -1;  // this lane's staged slot (B operand), or none
+  if (gi < n) {
+    const int tok = tok_of(gi);
+    if ((unsigned)tok < (unsigned)p.T) xslot = tok;
+  }
+  float acc[2][2][4] = {};
+  int u = 0;
+  for (int hh = warp; hh < nh; hh += kWarps, ++u) {
+    const uint32_t st = wst + (u & 1) * sbytes;
+    cp_async_wait<1>();
+    __syncwarp();  // the other lanes' token-row pieces of this stage
+    nv_unit_mma(g, hh, st, xslot, shared_entry, acc);
+    __syncwarp();  // every lane is done with the stage before it is refilled
+    if (hh + 2 * kWarps < nh)
+      nv_unit_copy(tiles, g, hh + 2 * kWarps, st, xsrc, p.H, n, p.T, tok_of);
+    cp_async_commit();
+  }
+  cp_async_wait<0>();
+  if (prefetch_down) {
+    const size_t len = (size_t)(p.H / 16) * p.dn_tile_bytes;
+    const size_t b0 = len * pair / gridDim.x, b1 = len * (pair + 1) / gridDim.x;
+    const uint8_t* dn = eb + p.gu_bytes;
+    for (size_t o = (b0 & ~(size_t)127) + 128 * threadIdx.x; o < b1; o += 128 * kThreads)
+      prefetch_l2(dn + o);
+  }
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = acc[0][0][i] + acc[0][1][i];
+    v[4 + i] = acc[1][0][i] + acc[1][1][i];
+  }
+  reduce_ksplit<8>(red, v, 1, kWarps);
+  if (warp != 0) return;
+  const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 16 * pair + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+    if (col < n) {
+      const float G = ts_g * v[i], U = ts_u * v[4 + i];
+      const float a = G / (1.0f + expf(-G)) * U;
+      p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+    }
+  }
+}
+
 // Requests from L2 the down tile `tile` of every work entry (fire and forget).
 template <int FMT>
 __device__ __forceinline__ void down_prefetch(const ExpertParams& p, int tile) {
@@ -339,7 +523,7 @@ struct DownPreload {
 
 __device__ __forceinline__ bool down_preload(const ExpertParams& p, int tile, int y, DownPreload& d) {
   const int lane = threadIdx.x & 31;
-  if (y >= p.nsh + *p.n_entries || !get_entry(p, y, d.expert, d.row, d.n)) return false;
+  if (!get_entry(p, y, d.expert, d.row, d.n)) return false;  // (reads the count and the entry together)
   const uint8_t* b = p.arena + (size_t)d.expert * p.expert_bytes + p.gu_bytes +
                      (size_t)tile * p.dn_tile_bytes + 16 * lane;
   const int nc = p.I / 64;
@@ -357,6 +541,7 @@ __device__ __forceinline__ void down_preloaded_mma(const ExpertParams& p, const 
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   const int nc = p.I / 64;
   const uint16_t* brow = gi < d.n ? p.abuf + (size_t)(d.row + gi) * p.I : nullptr;
+  float acc2[2][4] = {};  // even / odd chunks: two shorter mma chains
 #pragma unroll
   for (int j0 = 0; j0 < 8; j0 += 4) {
     uint32_t xb[4][8];
@@ -375,11 +560,13 @@ __device__ __forceinline__ void down_preloaded_mma(const ExpertParams& p, const 
           e2m1x8_to_f16x8(u4get(d.cv[jj], w), h);
           const uint32_t a[4] = {hmul2(h[0], s_lo), hmul2(h[1], s_hi), hmul2(h[2], s_lo),
                                  hmul2(h[3], s_hi)};
-          mma_f16(acc, a, xb[j][2 * w], xb[j][2 * w + 1]);
+          mma_f16(acc2[jj & 1], a, xb[j][2 * w], xb[j][2 * w + 1]);
         }
       }
     }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += acc2[0][i] + acc2[1][i];
 }
 
 // y of tile `tile` (16 rows of H) for every work entry, one warp per entry,

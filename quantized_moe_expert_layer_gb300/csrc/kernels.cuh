@@ -85,7 +85,12 @@ cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int*
                            bool pdl, cudaStream_t st);
 bool down_combine_ok(int T, int k, int shared, int I);
 cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const int* inv,
-                                float* out, bool pdl, cudaStream_t st);
+                                float* out, bool pdl, bool wait_first, cudaStream_t st);
+
+// T <= 8: gate/up that routes itself and publishes the routing (expert.cu)
+bool small_route_ok(int T, int k);
+cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, int grid_y,
+                                 cudaStream_t st);
 cudaError_t expert_kernels_init();
 cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream_t st);
 
@@ -97,13 +102,6 @@ cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, cudaStream_t st);
 bool tc_router_ok(int E, int H);
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);
 cudaError_t tc_kernels_init();
-
-// T <= 8: gate/up and down + combine that route themselves (expert.cu)
-bool small_route_ok(int T, int k);
-cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, int grid_y,
-                                 cudaStream_t st);
-cudaError_t launch_down_combine_routed(const ExpertParams& p, const RouteParams& rp, float* out,
-                                       cudaStream_t st);
 
 // launch helper: optional programmatic dependent launch on the previous kernel in the stream
 template <typename... KArgs, typename... Args>
@@ -121,5 +119,6 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
 
 }  // namespace moe

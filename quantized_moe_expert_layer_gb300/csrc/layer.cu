@@ -225,7 +225,7 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
   CK("gate/up kernel launch", launch_gateup(ep, grid_y, true, st));
   if (fused_down(L, T)) {
-    CK("down+combine kernel launch", launch_down_combine(ep, L->gates, L->inv, out, true, st));
+    CK("down+combine kernel launch", launch_down_combine(ep, L->gates, L->inv, out, true, false, st));
     return MOE_OK;
   }
   CK("down kernel launch", launch_down(ep, grid_y, true, st));
@@ -233,8 +233,8 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   return MOE_OK;
 }
 
-// T <= 8: router partial sums, then gate/up and down + combine that route
-// themselves from them (three launches, chained)
+// T <= 8: router partial sums; gate/up, which routes itself from them and
+// publishes the routing; down + combine (three launches, chained)
 bool small_path(moe_layer* L, int T) { return small_route_ok(T, L->k) && fused_down(L, T); }
 
 // kernels one forward of T tokens launches
@@ -254,7 +254,7 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
     CK("router kernel launch", launch_router(rp, st));
     CK("gate/up kernel launch",
        launch_gateup_routed(ep, rp, ep.nsh + max_routed_entries(T, L->E, L->k), st));
-    CK("down+combine kernel launch", launch_down_combine_routed(ep, rp, out, st));
+    CK("down+combine kernel launch", launch_down_combine(ep, L->gates, L->inv, out, true, true, st));
     return MOE_OK;
   }
   if (tc_router(L, T)) {
@@ -617,7 +617,7 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
     if (phase == 0) CK("router", launch_router(rp, st));
     if (phase == 2)
       CK("gate/up", launch_gateup_routed(ep, rp, ep.nsh + max_routed_entries(T, L->E, L->k), st));
-    if (phase == 3) CK("down+combine", launch_down_combine_routed(ep, rp, out, st));
+    if (phase == 3) CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, true, st));
     return MOE_OK;
   }
   const bool fused = fused_down(L, T);
@@ -648,7 +648,7 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       if (tc_path(L, T))
         CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
       else if (fused)
-        CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, st));
+        CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, false, st));
       else
         CK("down", launch_down(ep, grid_y, false, st));
       break;

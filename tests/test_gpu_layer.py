@@ -202,3 +202,44 @@ def test_error_paths():
     assert L.status(reset=True) == moe.EINVAL  # the device bounds check caught the expert id
     assert L.status() == 0
     L.close()
+
+
+# ---------------------------------------------------------------- top-k of one token: exact ties
+def _tie_biases(case, E, rng):
+    b = rng.uniform(-1.0, 0.9, E).astype(np.float32)
+    if case == "all_equal":          # every logit equal: the picks are experts 0..k-1
+        b[:] = 0.5
+    elif case == "tied_group":       # 20 experts tied at the top: their 10 lowest ids
+        b[rng.choice(E, 20, replace=False)] = 1.0
+    elif case == "straddle":         # 8 clear winners, then 5 tied for the last 2 places
+        ids = rng.choice(E, 13, replace=False)
+        b[ids[:8]] = np.linspace(2.0, 1.3, 8, dtype=np.float32)
+        b[ids[8:]] = 1.0
+    elif case == "one_share":        # the whole top 10 inside one 64-expert share
+        b[64:74] = np.linspace(3.0, 2.1, 10, dtype=np.float32)
+    elif case == "negative":         # all negative, ties among the best
+        b = -np.abs(b) - 0.25
+        b[rng.choice(E, 12, replace=False)] = -0.125
+    return b
+
+
+@pytest.mark.parametrize("case", ["all_equal", "tied_group", "straddle", "one_share", "negative"])
+def test_single_token_topk_exact_ties(case):
+    """The decode path's in-CTA top-k (candidates per warp, threshold, ranks)
+    against the oracle's top-k on logits that are exactly the bias (zero router
+    weights), with exact ties placed around the k-th pick."""
+    w = small(fmt=1, H=256, I=128, E=512, k=10, shared=1, T=1, seed=11)
+    L = layer(w, T_max=8)
+    rng = np.random.default_rng(["all_equal", "tied_group", "straddle", "one_share", "negative"].index(case))
+    bias = _tie_biases(case, w.E, rng)
+    L.set_router(np.zeros((w.E, w.H), np.uint16), bias)
+    try:
+        a = run_gpu(L, gen.x_tokens(w, 1), w)
+        assert L.launches(1) == 3
+        np.testing.assert_array_equal(a["logits"][0], bias)
+        ol = oracle.Layer(w.fmt, w.H, w.I, w.E, w.k, w.shared, np.zeros((w.E, w.H), np.uint16), bias)
+        idx, gates = ol.topk(bias[None, :])
+        np.testing.assert_array_equal(a["idx"], idx)
+        np.testing.assert_allclose(a["gates"], gates, rtol=1e-6, atol=0)
+    finally:
+        L.set_router(gen.router_weights(w), gen.router_bias(w))

@@ -88,6 +88,17 @@ def packed_gateup_bytes(w):
     return (w.I // 16) * 2 * tile
 
 
+def packed_down_bytes(w):
+    """Bytes of one expert's packed down tiles (layout.cuh)."""
+    if w.fmt == 1:
+        units = w.I // 64
+        tile = 512 * ((units + 7) // 8 + units)
+    else:
+        units = w.I // 128
+        tile = 128 * ((units + 7) // 8) + 1536 * units
+    return (w.H // 16) * tile
+
+
 def tc_path(w, T):
     """The forward takes the tcgen05 grouped GEMMs (NVFP4, >= 16 routed slots per expert)."""
     return w.fmt == 1 and T * w.k >= 16 * w.E and w.H % 128 == 0 and (2 * w.I) % 128 == 0
@@ -349,6 +360,10 @@ def run_ours(args, w):
     tc = tc_path(w, T)
     gu = packed_gateup_bytes(w)
     per_launch = []
+    # for T <= 8 (NVFP4) gate/up also asks L2 for the touched experts' down
+    # matrices, which the down kernel then reads from L2
+    prefetch_down = T <= 8 and w.fmt == 1
+    dn = packed_down_bytes(w)
     with torch.cuda.stream(s):
         for L, o in zip(layers, outs):
             L.forward(x, o, stream=s)
@@ -361,8 +376,9 @@ def run_ours(args, w):
                 cols = sum(((min(128, v - 128 * j) + 15) // 16) * 16
                            for v in n for j in range((v + 127) // 128))
                 per_launch.append(2.0 * cols * 2 * w.I * w.H)
-            else:  # unique weight bytes, x, and a
-                per_launch.append(D * (gu + 8) + T * w.H * 2 + (T * w.k + T * w.shared) * w.I * 2)
+            else:  # unique weight bytes, x, and a (+ the down matrices it pulls into L2)
+                per_launch.append(D * (gu + 8 + (dn if prefetch_down else 0)) + T * w.H * 2
+                                  + (T * w.k + T * w.shared) * w.I * 2)
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk, stream=s):
         for L, o in zip(layers, outs):

@@ -32,6 +32,7 @@ _lib = None
 
 FMT_NVFP4 = 1
 FMT_FP6 = 2
+FMT_MXFP4 = 3
 
 
 def build() -> None:
@@ -69,6 +70,8 @@ def lib():
                 "orc_e4m3_rne": (I, [F]),
                 "orc_quantize_nvfp4": (I, [P, I, I, P, P, P]),
                 "orc_quantize_fp6": (I, [P, I, I, P, P]),
+                "orc_quantize_mxfp4": (I, [P, I, I, P, P]),
+                "orc_dequant_mxfp4": (I, [P, P, I, I, P]),
                 "orc_dequant_nvfp4": (I, [P, P, F, I, I, P]),
                 "orc_dequant_fp6": (I, [P, P, I, I, P]),
                 "orc_router_logits": (I, [P, P, I, P]),
@@ -146,6 +149,22 @@ def quantize_fp6(W: np.ndarray):
     return codes, exps
 
 
+def quantize_mxfp4(W: np.ndarray):
+    """fp32 [rows x K] -> (codes u8 [rows x K/2], exps u8 [rows x K/32])."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    rows, K = W.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    exps = np.zeros((rows, K // 32), np.uint8)
+    _check(lib().orc_quantize_mxfp4(_p(W), rows, K, _p(codes), _p(exps)), "quantize")
+    return codes, exps
+
+
+def dequant_mxfp4(codes, exps, rows, K) -> np.ndarray:
+    out = np.empty((rows, K), np.float32)
+    _check(lib().orc_dequant_mxfp4(_p(codes), _p(exps), rows, K, _p(out)), "dequant")
+    return out
+
+
 def dequant_nvfp4(codes, scales, tscale, rows, K) -> np.ndarray:
     out = np.empty((rows, K), np.float32)
     _check(lib().orc_dequant_nvfp4(_p(codes), _p(scales), tscale, rows, K, _p(out)), "dequant")
@@ -185,6 +204,8 @@ class Layer:
     def quantize_matrix(self, expert, matrix, W):
         if self.fmt == FMT_NVFP4:
             c, s, ts = quantize_nvfp4(W)
+        elif self.fmt == FMT_MXFP4:
+            (c, s), ts = quantize_mxfp4(W), 1.0
         else:
             (c, s), ts = quantize_fp6(W), 1.0
         self.set_matrix(expert, matrix, c, s, ts)
@@ -195,6 +216,8 @@ class Layer:
         rows, K = self.shape(matrix)
         if self.fmt == FMT_NVFP4:
             return dequant_nvfp4(c, s, ts, rows, K)
+        if self.fmt == FMT_MXFP4:
+            return dequant_mxfp4(c, s, rows, K)
         return dequant_fp6(c, s, rows, K)
 
     def _struct(self):
@@ -295,6 +318,9 @@ def layer_for_workload(w, experts=None) -> Layer:
         W = gen.expert_weight(w_, e, m)
         if w_.fmt == FMT_NVFP4:
             return quantize_nvfp4(W)
+        if w_.fmt == FMT_MXFP4:
+            c, s = quantize_mxfp4(W)
+            return c, s, 1.0
         c, s = quantize_fp6(W)
         return c, s, 1.0
 

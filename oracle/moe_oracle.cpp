@@ -38,6 +38,10 @@
 //   R9 dispatch order: expert-major, then token, then rank j (stable).
 //   R10 shared expert: always on, weight 1, same format and I as the routed.
 //   R11 output = fp32(sum_j g_j * y_j + y_shared), summed in fp64.
+//   R17 MXFP4 (OCP MX v1.0 FP4): blocks of 32 along K share an e8m0 scale
+//      X = 2^(floor(log2 amax_b) - 2) (2 = the largest e2m1 exponent), clamped
+//      to [2^-127, 2^127]; q = e2m1_rne(w / X), saturating at 6; an all-zero
+//      block gets X = 2^0 (byte 127) and code 0; value = value(q) * X.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -186,6 +190,38 @@ int orc_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* e
   return 0;
 }
 
+// MXFP4, reading R17.  K % 32 == 0.  codes [rows x K/2] as for NVFP4;
+// exps [rows x K/32]: ue8m0 bytes.
+int orc_quantize_mxfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps) {
+  if (rows <= 0 || K <= 0 || K % 32 != 0) return -1;
+  for (int r = 0; r < rows; ++r) {
+    for (int b = 0; b < K / 32; ++b) {
+      const float* w = W + (long)r * K + b * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(w[i]));
+      int E = 0;
+      if (amax > 0.0f) {
+        int e2;
+        std::frexp((double)amax, &e2);  // amax = f * 2^e2, f in [0.5, 1): floor(log2 amax) = e2 - 1
+        E = std::min(127, std::max(-127, e2 - 1 - 2));
+      }
+      exps[(long)r * (K / 32) + b] = (uint8_t)(E + 127);
+      for (int i = 0; i < 32; ++i) {
+        // w / 2^E is exact; the grid decision is taken on that exact value
+        const double v = (amax > 0.0f) ? std::ldexp((double)w[i], -E) : 0.0;
+        const int q = e2m1_rne((float)v);
+        const long col = (long)b * 32 + i;
+        uint8_t& byte = codes[(long)r * (K / 2) + col / 2];
+        if (col % 2 == 0)
+          byte = (uint8_t)q;
+        else
+          byte = (uint8_t)(byte | (q << 4));
+      }
+    }
+  }
+  return 0;
+}
+
 // ---------------------------------------------------------------- dequantisers (R6)
 int orc_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float tscale, int rows, int K,
                       float* out) {
@@ -196,6 +232,18 @@ int orc_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float tscale,
       int q = (c % 2 == 0) ? (byte & 15) : (byte >> 4);
       float cs = (float)(e2m1_value(q) * e4m3_value(scales[(long)r * (K / 16) + c / 16]));
       out[(long)r * K + c] = cs * tscale;
+    }
+  return 0;
+}
+
+int orc_dequant_mxfp4(const uint8_t* codes, const uint8_t* exps, int rows, int K, float* out) {
+  if (K % 32 != 0) return -1;
+  for (int r = 0; r < rows; ++r)
+    for (int c = 0; c < K; ++c) {
+      uint8_t byte = codes[(long)r * (K / 2) + c / 2];
+      int q = (c % 2 == 0) ? (byte & 15) : (byte >> 4);
+      double v = e2m1_value(q) * ue8m0_value(exps[(long)r * (K / 32) + c / 32]);
+      out[(long)r * K + c] = (float)v;
     }
   return 0;
 }
@@ -216,11 +264,11 @@ int orc_dequant_fp6(const uint8_t* codes, const uint8_t* exps, int rows, int K, 
 // expert == E for the shared expert, matrix 0 gate [I x H], 1 up [I x H],
 // 2 down [H x I].  Pointers of experts a call does not touch may be null.
 struct orc_layer {
-  int format;  // 1 NVFP4, 2 FP6 e2m3
+  int format;  // 1 NVFP4, 2 FP6 e2m3, 3 MXFP4
   int H, I, E, k, shared;
   const uint8_t* const* codes;
-  const uint8_t* const* scales;  // e4m3 block scales (NVFP4) or ue8m0 exponents (FP6)
-  const float* tscales;          // NVFP4 tensor scales [(E + shared) * 3]; unused for FP6
+  const uint8_t* const* scales;  // e4m3 block scales (NVFP4) or ue8m0 exponents (FP6, MXFP4)
+  const float* tscales;          // NVFP4 tensor scales [(E + shared) * 3]; unused otherwise
   const uint16_t* router;        // bf16 bits [E x H]
   const float* bias;             // fp32 [E] or null
 };
@@ -243,6 +291,10 @@ void dequant_row(const orc_layer& L, int expert, int matrix, int row, int K, flo
     const uint8_t* c = L.codes[m] + (long)row * (K / 2);
     const uint8_t* s = L.scales[m] + (long)row * (K / 16);
     orc_dequant_nvfp4(c, s, L.tscales[m], 1, K, out);
+  } else if (L.format == 3) {
+    const uint8_t* c = L.codes[m] + (long)row * (K / 2);
+    const uint8_t* s = L.scales[m] + (long)row * (K / 32);
+    orc_dequant_mxfp4(c, s, 1, K, out);
   } else {
     const uint8_t* c = L.codes[m] + (long)row * K;
     const uint8_t* s = L.scales[m] + (long)row * (K / 128);

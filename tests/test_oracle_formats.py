@@ -234,3 +234,68 @@ def test_fp6_vs_nvfp4_byte_ratio():
     nvfp4 = 0.5 + 1 / 16          # e2m1 code + one e4m3 scale per 16
     fp6 = 0.75 + 1 / 128          # e2m3 code + one exponent byte per 128
     assert 1.3 < fp6 / nvfp4 < 1.45
+
+
+# ---------------------------------------------------------------- MXFP4 (OCP MX v1.0 FP4)
+def test_mxfp4_quantizer_scale_rule_and_codes_nearest():
+    """Shared scale X = 2^(floor(log2 amax) - 2) per 32 weights, written as the
+    binade bracket 2^(E+2) <= amax < 2^(E+3); codes = the binade-wise
+    round-half-even of w / X on the e2m1 grid, saturating at 6."""
+    rng = np.random.default_rng(7)
+    rows, K = 6, 256
+    W = _random_matrix(rng, rows, K)
+    W[2, 64:96] *= 1e4          # a loud block
+    W[4, 0:32] *= 1e-6          # a quiet one
+    W[5, 160:192] = 0.0         # an all-zero one
+    W[1, 32] = np.float32(2.0 ** -3 * 6.0)  # an exact power-of-two edge: amax = 0.75 -> E = -3
+    W[1, 33:64] = 0.0
+    codes, exps = oracle.quantize_mxfp4(W)
+    amax = np.abs(W).reshape(rows, K // 32, 32).max(axis=2).astype(np.float64)
+    E = exps.astype(np.int64) - 127
+    for r in range(rows):
+        for b in range(K // 32):
+            if amax[r, b] == 0:
+                assert exps[r, b] == 127
+                continue
+            assert 2.0 ** (E[r, b] + 2) <= amax[r, b] < 2.0 ** (E[r, b] + 3), (r, b)
+    assert E[1, 1] == -3
+    vals = np.array(E2M1_TABLE)
+    for r in range(rows):
+        for c in range(K):
+            byte = codes[r, c // 2]
+            code = (byte & 15) if c % 2 == 0 else (byte >> 4)
+            v = np.float32(np.ldexp(np.float64(W[r, c]), -int(E[r, c // 32])))
+            assert vals[code & 7] == _binade_rne(v, E2M1_STEPS), (r, c)
+            assert ((code & 8) != 0) == bool(v < 0 and vals[code & 7] > 0)
+
+
+def test_mxfp4_saturation_and_dequant_values():
+    W = np.zeros((1, 64), np.float32)
+    W[0, 0] = 7.5          # amax 7.5: E = floor(log2 7.5) - 2 = 0, 7.5 saturates to 6
+    W[0, 1] = -5.0         # midpoint of 4 and 6: ties to the even code (4)
+    W[0, 2] = 0.25         # midpoint of 0 and 0.5: ties to 0, never -0
+    W[0, 3] = -0.25
+    W[0, 32] = 1.0 / 1024  # second block: E = -10 - 2 = -12, 2^-10 / 2^-12 = 4
+    codes, exps = oracle.quantize_mxfp4(W)
+    assert exps[0, 0] == 127 and exps[0, 1] == 127 - 12
+    D = oracle.dequant_mxfp4(codes, exps, 1, 64)
+    assert D[0, 0] == 6.0 and D[0, 1] == -4.0 and D[0, 2] == 0.0 and D[0, 3] == 0.0
+    assert (codes[0, 1] >> 4) == 0  # -0.25 -> +0
+    assert D[0, 32] == np.float32(1.0 / 1024)
+    assert np.all(D[0, 4:32] == 0) and np.all(D[0, 33:] == 0)
+
+
+def test_mxfp4_error_bound():
+    """Away from saturation the error is at most half a grid step of the
+    element's binade times X (0.25 X below 2, 0.5 X below 4, X below 6)."""
+    rng = np.random.default_rng(9)
+    W = _random_matrix(rng, 16, 512)
+    codes, exps = oracle.quantize_mxfp4(W)
+    D = oracle.dequant_mxfp4(codes, exps, 16, 512).astype(np.float64)
+    X = np.repeat(2.0 ** (exps.astype(np.float64) - 127), 32, axis=1)
+    a = np.abs(W.astype(np.float64)) / X
+    step = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    err = np.abs(D - W) / X
+    inside = a <= 6.0
+    assert np.all(err[inside] <= step[inside] / 2 + 1e-12)
+    assert np.all(err[~inside] == a[~inside] - 6.0)  # saturated: clipped to 6 X

@@ -78,8 +78,8 @@ def peaks(kind="hbm"):
 
 
 def packed_gateup_bytes(w):
-    """Bytes of one expert's packed gate + up tiles (layout.cuh)."""
-    if w.fmt == 1:
+    """Bytes of one expert's packed gate + up tiles (layout.cuh; MXFP4 is packed as NVFP4)."""
+    if w.fmt in (1, 3):
         units = w.H // 64
         tile = 512 * ((units + 7) // 8 + units)
     else:
@@ -89,8 +89,8 @@ def packed_gateup_bytes(w):
 
 
 def packed_down_bytes(w):
-    """Bytes of one expert's packed down tiles (layout.cuh)."""
-    if w.fmt == 1:
+    """Bytes of one expert's packed down tiles (layout.cuh; MXFP4 is packed as NVFP4)."""
+    if w.fmt in (1, 3):
         units = w.I // 64
         tile = 512 * ((units + 7) // 8 + units)
     else:
@@ -101,14 +101,19 @@ def packed_down_bytes(w):
 
 def tc_path(w, T):
     """The forward takes the tcgen05 grouped GEMMs (NVFP4, >= 16 routed slots per expert)."""
-    return w.fmt == 1 and T * w.k >= 16 * w.E and w.H % 128 == 0 and (2 * w.I) % 128 == 0
+    return w.fmt in (1, 3) and T * w.k >= 16 * w.E and w.H % 128 == 0 and (2 * w.I) % 128 == 0
+
+
+FORMAT_NAMES = {1: "nvfp4 (e2m1, e4m3 per 16, fp32 tensor scale)",
+                2: "fp6 e2m3 (power-of-two scale per 128)",
+                3: "mxfp4 (e2m1, power-of-two scale per 32)"}
+SHORT_NAMES = {1: "nvfp4", 2: "fp6 e2m3", 3: "mxfp4"}
 
 
 def config_block(w, L, extra=None):
     c = {"workload": w.name, "H": w.H, "I": w.I, "E": w.E, "k": w.k, "shared_experts": w.shared,
          "tokens_per_step": w.T,
-         "format": ("nvfp4 (e2m1, e4m3 per 16, fp32 tensor scale)" if w.fmt == 1
-                    else "fp6 e2m3 (power-of-two scale per 128)"),
+         "format": FORMAT_NAMES[w.fmt],
          "layer_instances_per_step": L, "l2": "inputs larger than L2 (distinct weights per layer)"}
     if extra:
         c.update(extra)
@@ -362,7 +367,7 @@ def run_ours(args, w):
     per_launch = []
     # for T <= 8 (NVFP4) gate/up also asks L2 for the touched experts' down
     # matrices, which the down kernel then reads from L2
-    prefetch_down = T <= 8 and w.fmt == 1
+    prefetch_down = T <= 8 and w.fmt in (1, 3)
     dn = packed_down_bytes(w)
     with torch.cuda.stream(s):
         for L, o in zip(layers, outs):
@@ -455,7 +460,7 @@ def run_ours(args, w):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (" + ("nvfp4" if w.fmt == 1 else "fp6 e2m3") + " weights)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (" + SHORT_NAMES[w.fmt] + " weights)",
             "data": "synthetic (seeded generator; random-init weights quantised on the device)",
             "config": config_block(w, Ln, {"us_per_layer": ms * 1e3 / (args.steps * Ln),
                                            "phase_us_alone": phase_us,

@@ -1,4 +1,4 @@
-"""The five synthetic workloads of the quantized MoE expert layer.
+"""The synthetic workloads of the quantized MoE expert layer.
 
 Each is named by what it is and its sizes.  Shapes, formats, top-k, shared
 expert and router-bias recipes follow the layer shapes the engine pages speak
@@ -13,6 +13,7 @@ from dataclasses import dataclass
 
 FMT_NVFP4 = 1
 FMT_FP6 = 2
+FMT_MXFP4 = 3
 
 
 @dataclass(frozen=True)
@@ -47,6 +48,15 @@ WORKLOADS = {
                  "zipf", 1.1, 0.5, seed=0),
         Workload("prefill-h2048-i512-e512-k10-s1-t4096-nvfp4", 2048, 512, 512, 10, 1, 4096,
                  FMT_NVFP4, "normal", 0.0, 0.1, seed=0),
+        # MXFP4 and the DeepSeek-V4 expert shape (256 routed + 1 shared, top-6).
+        # The pages give no H or I; ~167 GB over 43 layers of 257 fp4 experts
+        # bounds a matrix at ~9.5M weights, and H = 4096, I = 2048 (8.4M) is
+        # the reading taken
+        Workload("tiny-h256-i128-e8-k2-t4-mxfp4", 256, 128, 8, 2, 0, 4, FMT_MXFP4, "none", seed=1),
+        Workload("decode-h4096-i2048-e256-k6-s1-t1-mxfp4", 4096, 2048, 256, 6, 1, 1, FMT_MXFP4,
+                 "normal", 0.0, 0.1, seed=0),
+        Workload("prefill-h4096-i2048-e256-k6-s1-t4096-mxfp4", 4096, 2048, 256, 6, 1, 4096,
+                 FMT_MXFP4, "normal", 0.0, 0.1, seed=0),
     ]
 }
 

@@ -37,7 +37,7 @@ extern "C" {
 
 typedef struct moe_layer moe_layer; /* opaque */
 
-enum moe_format { MOE_FMT_NVFP4 = 1, MOE_FMT_FP6_E2M3 = 2 };
+enum moe_format { MOE_FMT_NVFP4 = 1, MOE_FMT_FP6_E2M3 = 2, MOE_FMT_MXFP4 = 3 };
 
 enum moe_status {
   MOE_OK = 0,
@@ -102,6 +102,14 @@ int moe_set_router(moe_layer* L, const uint16_t* wr_bf16, const float* bias, int
  *   FP6:   codes [rows x K] bytes, one e2m3 code in the low 6 bits of each;
  *          scales [rows x K/128] ue8m0 exponent bytes (2^(b-127)); tscale
  *          ignored (may be NULL).
+ *   MXFP4 (OCP MX FP4): codes as for NVFP4; scales [rows x K/32] ue8m0
+ *          exponent bytes (weight = e2m1 * 2^(b-127)); tscale ignored.  The
+ *          device layout is NVFP4's: each block's scale becomes the e4m3
+ *          power of two 2^(b - b_max + 8) of both of its 16-column halves and
+ *          the matrix gets the fp32 tensor scale 2^(b_max - 135), b_max the
+ *          largest exponent of a block with a nonzero code.  That is exact
+ *          while every such block is within 17 binades of b_max; otherwise
+ *          MOE_EINVAL.  Synchronous (it checks that range on the device).
  * codes / scales / tscale are host or device pointers per `where`.  Device input is
  * consumed asynchronously on `stream`; host input is copied synchronously. */
 int moe_pack_matrix(moe_layer* L, int expert, int matrix, const uint8_t* codes,
@@ -135,6 +143,16 @@ int moe_quantize_nvfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t*
  * K % 128 == 0. */
 int moe_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,
                      void* stream);
+
+/* Quantise fp32 weights W [rows x K] (device) to canonical MXFP4 (OCP
+ * Microscaling v1.0, FP4 E2M1 elements) on the device: per 32 weights along K
+ * the shared exponent E = floor(log2 amax_32) - 2, clamped to [-127, 127]
+ * (byte E + 127; 127 for an all-zero block), code = rne_e2m1(w / 2^E), ties
+ * to the even code, saturating at 6, +0 for zero.  Device outputs codes
+ * [rows x K/2] (as NVFP4), exps [rows x K/32].  K % 32 == 0; W and codes
+ * 16-byte aligned. */
+int moe_quantize_mxfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,
+                       void* stream);
 
 /* ------------------------------------------------------------------ forward */
 

@@ -25,6 +25,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-cudart"
 
 FMT_NVFP4 = 1
 FMT_FP6 = 2
+FMT_MXFP4 = 3
 GATE, UP, DOWN = 0, 1, 2
 HOST, DEVICE = 0, 1
 
@@ -34,7 +35,7 @@ OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT = 0, -1, -2, -3, -4, -5
 EXPORTS = [
     "moe_layer_create", "moe_layer_reserve", "moe_layer_destroy", "moe_last_error",
     "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
-    "moe_pack_weights", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_forward",
+    "moe_pack_weights", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_quantize_mxfp4", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
     "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches"
 ]
@@ -105,6 +106,7 @@ def lib():
                 "moe_pack_weights": (I, [P, P, P, P]),
                 "moe_quantize_nvfp4": (I, [P, I, I, P, P, P, P]),
                 "moe_quantize_fp6": (I, [P, I, I, P, P, P]),
+                "moe_quantize_mxfp4": (I, [P, I, I, P, P, P]),
                 "moe_forward": (I, [P, P, I, P, P]),
                 "moe_forward_host": (I, [P, P, I, P, P]),
                 "moe_forward_routed": (I, [P, P, I, P, P, P, P]),
@@ -238,6 +240,11 @@ def quantize_nvfp4(W, codes, scales, tscale, stream=None):
 def quantize_fp6(W, codes, exps, stream=None):
     rows, K = W.shape
     check(lib().moe_quantize_fp6(_ptr(W), rows, K, _ptr(codes), _ptr(exps), _stream(stream)))
+
+
+def quantize_mxfp4(W, codes, exps, stream=None):
+    rows, K = W.shape
+    check(lib().moe_quantize_mxfp4(_ptr(W), rows, K, _ptr(codes), _ptr(exps), _stream(stream)))
 
 
 def route_noalloc(x, wr, bias, E, k, logits, idx, gates, stream=None):

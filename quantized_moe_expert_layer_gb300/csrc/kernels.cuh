@@ -64,6 +64,10 @@ cudaError_t launch_quantize_nvfp4(const float* W, int rows, int K, uint8_t* code
                                   uint8_t* scales, float* tscale, cudaStream_t st);
 cudaError_t launch_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,
                                 cudaStream_t st);
+cudaError_t launch_quantize_mxfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,
+                                  cudaStream_t st);
+cudaError_t launch_mx_to_tile_scales(const uint8_t* codes, const uint8_t* exps, int rows, int K,
+                                     uint8_t* nv_scales, float* ts_dst, int* bad, cudaStream_t st);
 cudaError_t launch_pack(int fmt, const uint8_t* codes, const uint8_t* scales, int rows, int K,
                         uint8_t* dst, uint64_t tile_stride, const float* ts_src, float ts_val,
                         float* ts_dst, cudaStream_t st);

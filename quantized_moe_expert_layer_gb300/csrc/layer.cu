@@ -81,6 +81,7 @@ int record_error(int code, const char* fmt, ...) {
 struct moe_layer {
   int device = 0;
   int fmt = 0, H = 0, I = 0, E = 0, k = 0, shared = 0;
+  int dev_fmt = 0;  // layout of the packed tiles (MXFP4 is packed as NVFP4)
   ExpertGeom geom{};
   uint8_t* arena = nullptr;
   uint64_t arena_bytes = 0;
@@ -127,7 +128,7 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.E = L->E;
   p.k = L->k;
   p.shared = L->shared;
-  const bool tc = tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I);
+  const bool tc = tc_path_ok(L->dev_fmt, T, L->k, L->E, L->H, L->I);
   // the tensor-core router writes the whole dot product: one K slice
   p.ksplit = tc && tc_router_ok(L->E, L->H) ? 1 : router_ksplit(T, L->H, L->E);
   p.partial = L->partial;
@@ -156,7 +157,7 @@ ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
   p.gu_tile_bytes = L->geom.gu.tile_bytes;
   p.dn_tile_bytes = L->geom.dn.tile_bytes;
   p.tscale = L->tscale;
-  p.fmt = L->fmt;
+  p.fmt = L->dev_fmt;
   p.H = L->H;
   p.I = L->I;
   p.E = L->E;
@@ -199,7 +200,7 @@ int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
 // experts + combine, after routing has filled idx / gates / dispatch
 bool fused_down(moe_layer* L, int T) { return down_combine_ok(T, L->k, L->shared, L->I); }
 
-bool tc_path(moe_layer* L, int T) { return tc_path_ok(L->fmt, T, L->k, L->E, L->H, L->I); }
+bool tc_path(moe_layer* L, int T) { return tc_path_ok(L->dev_fmt, T, L->k, L->E, L->H, L->I); }
 
 // prefill routing: logits as one bf16 GEMM on the tensor cores, then top-k and
 // dispatch as usual (the GEMM's output is the one K slice the top-k reads)
@@ -284,9 +285,10 @@ const char* moe_last_error(void) { return g_last_error.c_str(); }
 int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_layer** out) {
   if (!out) return fail(MOE_EINVAL, "moe_layer_create: null out");
   *out = nullptr;
-  if (format != MOE_FMT_NVFP4 && format != MOE_FMT_FP6_E2M3)
+  if (format != MOE_FMT_NVFP4 && format != MOE_FMT_FP6_E2M3 && format != MOE_FMT_MXFP4)
     return fail(MOE_EINVAL, "moe_layer_create: unknown format %d", format);
-  const int mult = format == MOE_FMT_NVFP4 ? 64 : 128;
+  const int mult = format == MOE_FMT_FP6_E2M3 ? 128 : 64;
+  const int dev_fmt = format == MOE_FMT_FP6_E2M3 ? FMT_FP6 : FMT_NVFP4;
   if (H <= 0 || I <= 0 || H % mult || I % mult)
     return fail(MOE_EINVAL, "moe_layer_create: H=%d and I=%d must be positive multiples of %d", H,
                 I, mult);
@@ -296,12 +298,13 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   if (shared != 0 && shared != 1) return fail(MOE_EINVAL, "moe_layer_create: shared must be 0 or 1");
   moe_layer* L = new moe_layer();
   L->fmt = format;
+  L->dev_fmt = dev_fmt;
   L->H = H;
   L->I = I;
   L->E = E;
   L->k = k;
   L->shared = shared;
-  L->geom = expert_geom(format, H, I);
+  L->geom = expert_geom(dev_fmt, H, I);
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = route_kernels_init();
   if (e == cudaSuccess) e = expert_kernels_init();
@@ -458,34 +461,61 @@ int moe_pack_matrix(moe_layer* L, int expert, int matrix, const uint8_t* codes,
   DeviceGuard dg(L->device);
   cudaStream_t st = (cudaStream_t)stream;
   const int rows = matrix == MOE_DOWN ? L->H : L->I, K = matrix == MOE_DOWN ? L->I : L->H;
-  const size_t code_bytes = L->fmt == MOE_FMT_NVFP4 ? (size_t)rows * K / 2 : (size_t)rows * K;
-  const size_t scale_bytes = L->fmt == MOE_FMT_NVFP4 ? (size_t)rows * K / 16 : (size_t)rows * K / 128;
+  const bool fp4 = L->dev_fmt == FMT_NVFP4, mx = L->fmt == MOE_FMT_MXFP4;
+  const size_t code_bytes = fp4 ? (size_t)rows * K / 2 : (size_t)rows * K;
+  const size_t scale_bytes =
+      mx ? (size_t)rows * K / 32 : (fp4 ? (size_t)rows * K / 16 : (size_t)rows * K / 128);
+  // MXFP4: the converted e4m3 scales and a range flag, on the device
+  const size_t tile_scale_bytes = mx ? (size_t)rows * K / 16 : 0;
+  const size_t tmp_bytes = (where != MOE_DEVICE ? code_bytes + scale_bytes : 0) +
+                           (mx ? tile_scale_bytes + 16 : 0);
   const uint8_t* c = codes;
   const uint8_t* s = scales;
   uint8_t* tmp = nullptr;
+  if (tmp_bytes) CK("moe_pack_matrix: staging cudaMalloc", cudaMalloc(&tmp, tmp_bytes));
+  size_t used = 0;
   if (where != MOE_DEVICE) {
-    CK("moe_pack_matrix: staging cudaMalloc", cudaMalloc(&tmp, code_bytes + scale_bytes));
-    CK("moe_pack_matrix: copy codes", cudaMemcpy(tmp, codes, code_bytes, cudaMemcpyHostToDevice));
-    CK("moe_pack_matrix: copy scales",
-       cudaMemcpy(tmp + code_bytes, scales, scale_bytes, cudaMemcpyHostToDevice));
+    cudaError_t e = cudaMemcpy(tmp, codes, code_bytes, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(tmp + code_bytes, scales, scale_bytes, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      cudaFree(tmp);
+      CK("moe_pack_matrix: copy codes and scales", e);
+    }
     c = tmp;
     s = tmp + code_bytes;
+    used = code_bytes + scale_bytes;
     st = 0;
   }
   const ExpertGeom& g = L->geom;
   uint8_t* dst = L->arena + (size_t)expert * g.expert_bytes + tile_offset(g, matrix, 0);
   const uint64_t stride = matrix == MOE_DOWN ? (uint64_t)g.dn.tile_bytes : 2u * g.gu.tile_bytes;
-  const bool nv = L->fmt == MOE_FMT_NVFP4;
-  const float* ts_src = (nv && where == MOE_DEVICE) ? tscale : nullptr;
-  const float ts_val = (nv && where != MOE_DEVICE) ? *tscale : 1.0f;
-  cudaError_t e = launch_pack(L->fmt, c, s, rows, K, dst, stride, ts_src, ts_val,
-                              L->tscale + expert * 3 + matrix, st);
+  float* ts_dst = L->tscale + expert * 3 + matrix;
+  cudaError_t e = cudaSuccess;
+  int* bad = nullptr;
+  if (mx) {  // MXFP4 -> NVFP4 tile scales and the tensor scale, then the NVFP4 packer
+    uint8_t* tile_scales = tmp + used;
+    bad = reinterpret_cast<int*>(tmp + used + tile_scale_bytes);
+    e = cudaMemsetAsync(bad, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = launch_mx_to_tile_scales(c, s, rows, K, tile_scales, ts_dst, bad, st);
+    if (e == cudaSuccess)
+      e = launch_pack(FMT_NVFP4, c, tile_scales, rows, K, dst, stride, nullptr, 1.0f, nullptr, st);
+  } else {
+    const float* ts_src = (fp4 && where == MOE_DEVICE) ? tscale : nullptr;
+    const float ts_val = (fp4 && where != MOE_DEVICE) ? *tscale : 1.0f;
+    e = launch_pack(L->dev_fmt, c, s, rows, K, dst, stride, ts_src, ts_val, ts_dst, st);
+  }
+  int bad_h = 0;
   if (tmp) {
-    cudaError_t e2 = cudaDeviceSynchronize();
-    cudaFree(tmp);
+    cudaError_t e2 = cudaStreamSynchronize(st);
     if (e == cudaSuccess) e = e2;
+    if (e == cudaSuccess && bad) e = cudaMemcpy(&bad_h, bad, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(tmp);
   }
   CK("moe_pack_matrix: pack kernel", e);
+  if (bad_h)
+    return fail(MOE_EINVAL,
+                "moe_pack_matrix: MXFP4 block exponents span more than 17 binades (or a NaN "
+                "scale); the tile layout holds them as e4m3 powers of two 2^-9..2^8");
   return MOE_OK;
 }
 
@@ -520,6 +550,15 @@ int moe_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* e
   if (((uintptr_t)W | (uintptr_t)codes) & 15u)
     return fail(MOE_EINVAL, "moe_quantize_fp6: W and codes must be 16-byte aligned");
   CK("moe_quantize_fp6", launch_quantize_fp6(W, rows, K, codes, exps, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_quantize_mxfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps, void* stream) {
+  if (!W || !codes || !exps) return fail(MOE_EINVAL, "moe_quantize_mxfp4: null argument");
+  if (rows < 1 || K < 32 || K % 32) return fail(MOE_EINVAL, "moe_quantize_mxfp4: bad shape %dx%d", rows, K);
+  if (((uintptr_t)W | (uintptr_t)codes) & 15u)
+    return fail(MOE_EINVAL, "moe_quantize_mxfp4: W and codes must be 16-byte aligned");
+  CK("moe_quantize_mxfp4", launch_quantize_mxfp4(W, rows, K, codes, exps, (cudaStream_t)stream));
   return MOE_OK;
 }
 
@@ -574,7 +613,7 @@ int moe_debug_dequant(moe_layer* L, int expert, int matrix, float* out, void* st
   const int rows = matrix == MOE_DOWN ? L->H : L->I, K = matrix == MOE_DOWN ? L->I : L->H;
   const uint8_t* src = L->arena + (size_t)expert * g.expert_bytes + tile_offset(g, matrix, 0);
   const uint64_t stride = matrix == MOE_DOWN ? (uint64_t)g.dn.tile_bytes : 2u * g.gu.tile_bytes;
-  CK("moe_debug_dequant", launch_debug_dequant(L->fmt, src, stride, rows, K,
+  CK("moe_debug_dequant", launch_debug_dequant(L->dev_fmt, src, stride, rows, K,
                                                L->tscale + expert * 3 + matrix, out,
                                                (cudaStream_t)stream));
   return MOE_OK;

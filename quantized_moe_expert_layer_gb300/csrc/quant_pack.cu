@@ -1,4 +1,4 @@
-// Device quantisers (fp32 -> canonical NVFP4 / FP6 e2m3), the packer
+// Device quantisers (fp32 -> canonical NVFP4 / FP6 e2m3 / MXFP4), the packer
 // (canonical -> the tile layout of layout.cuh) and the debug dequantiser that
 // reads the packed bytes back with the expert kernels' decode.
 //
@@ -124,6 +124,94 @@ __global__ void quant_fp6_kernel(const float* __restrict__ W, int rows, int K,
     reinterpret_cast<uint32_t*>(codes + b * 128)[lane] = out;
     if (lane == 0) exps[b] = (uint8_t)(E + 127);
   }
+}
+
+// MXFP4 (OCP MX FP4): one thread per 32-weight block.  X = 2^E with
+// E = floor(log2 amax) - 2 (frexpf gives amax = f 2^e2, f in [0.5, 1), so
+// floor(log2 amax) = e2 - 1), clamped to [-127, 127]; q = e2m1_rne(w / X)
+// with w / X taken exactly (ldexpf by a power of two); all-zero block: byte
+// 127, codes 0.
+__global__ void quant_mxfp4_kernel(const float* __restrict__ W, int rows, int K,
+                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ exps) {
+  const uint64_t total = (uint64_t)rows * (K / 32);
+  for (uint64_t b = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total;
+       b += (uint64_t)gridDim.x * blockDim.x) {
+    const float4* w4 = reinterpret_cast<const float4*>(W + b * 32);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = w4[i];
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    int E = 0;
+    if (amax > 0.0f) {
+      int e2;
+      frexpf(amax, &e2);
+      E = min(127, max(-127, e2 - 3));
+    }
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    if (amax > 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = w4[i];
+        const float w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float s = ldexpf(w[j], -E);
+          uint32_t q = e2m1_code_rne(fabsf(s));
+          if (s < 0.0f && q != 0u) q |= 8u;
+          const int c = 4 * i + j;
+          packed[c / 8] |= q << (4 * (c % 8));
+        }
+      }
+    }
+    reinterpret_cast<uint4*>(codes)[b] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    exps[b] = (uint8_t)(E + 127);
+  }
+}
+
+// e4m3 byte of 2^p, p in [-9, 8] (normal for p >= -6, subnormal m/8 * 2^-6 below)
+__device__ __forceinline__ uint32_t e4m3_pow2(int p) {
+  return p >= -6 ? (uint32_t)(p + 7) << 3 : (1u << (p + 9));
+}
+
+// MXFP4 -> the NVFP4 tile layout: the shared scale 2^(E_b - 127) of a block of
+// 32 becomes the e4m3 scale 2^(E_b - E_max + 8) of both its 16-column halves
+// and the fp32 tensor scale 2^(E_max - 135), E_max = the largest exponent of
+// a block with a nonzero code.  Exact while every such block lies within 17
+// binades of E_max (e4m3 holds 2^-9 .. 2^8); otherwise *bad is set.  One CTA.
+__global__ void __launch_bounds__(1024) mx_to_tile_scales_kernel(
+    const uint8_t* __restrict__ codes, const uint8_t* __restrict__ exps, int rows, int K,
+    uint8_t* __restrict__ nv_scales, float* ts_dst, int* bad) {
+  __shared__ int s_max;
+  const int64_t nb = (int64_t)rows * (K / 32);
+  if (threadIdx.x == 0) s_max = -1;
+  __syncthreads();
+  int m = -1;
+  for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) {
+    const uint4 c = reinterpret_cast<const uint4*>(codes)[b];
+    const bool nz = ((c.x | c.y | c.z | c.w) & 0x77777777u) != 0u;  // a nonzero magnitude
+    if (nz) m = max(m, (int)exps[b]);
+  }
+  atomicMax(&s_max, m);
+  __syncthreads();
+  const int emax = s_max < 0 ? 127 : s_max;
+  for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) {
+    const uint4 c = reinterpret_cast<const uint4*>(codes)[b];
+    const bool nz = ((c.x | c.y | c.z | c.w) & 0x77777777u) != 0u;
+    uint32_t s = 0u;
+    if (nz) {
+      const int p = (int)exps[b] - emax + 8;
+      if (p < -9 || exps[b] == 255) {
+        *bad = 1;
+      } else {
+        s = e4m3_pow2(p);
+      }
+    }
+    nv_scales[2 * b] = (uint8_t)s;
+    nv_scales[2 * b + 1] = (uint8_t)s;
+  }
+  if (threadIdx.x == 0) *ts_dst = ldexpf(1.0f, emax - 135);
 }
 
 // ---------------------------------------------------------------- packer
@@ -336,6 +424,19 @@ cudaError_t launch_quantize_fp6(const float* W, int rows, int K, uint8_t* codes,
                                 cudaStream_t st) {
   const int64_t blocks = (int64_t)rows * (K / 128);
   quant_fp6_kernel<<<blocks_for(blocks * 32, 256), 256, 0, st>>>(W, rows, K, codes, exps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,
+                                  cudaStream_t st) {
+  quant_mxfp4_kernel<<<blocks_for((int64_t)rows * (K / 32), 256), 256, 0, st>>>(W, rows, K, codes,
+                                                                                exps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_to_tile_scales(const uint8_t* codes, const uint8_t* exps, int rows, int K,
+                                     uint8_t* nv_scales, float* ts_dst, int* bad, cudaStream_t st) {
+  mx_to_tile_scales_kernel<<<1, 1024, 0, st>>>(codes, exps, rows, K, nv_scales, ts_dst, bad);
   return cudaGetLastError();
 }
 

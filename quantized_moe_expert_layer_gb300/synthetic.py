@@ -14,7 +14,7 @@ import torch
 
 import gen
 
-from . import FMT_NVFP4, MoeLayer, quantize_fp6, quantize_nvfp4
+from . import FMT_MXFP4, FMT_NVFP4, MoeLayer, quantize_fp6, quantize_mxfp4, quantize_nvfp4
 
 
 def build_layer(w, T_max=None, seed=None, experts=None, stream=None) -> MoeLayer:
@@ -48,6 +48,11 @@ def build_layer(w, T_max=None, seed=None, experts=None, stream=None) -> MoeLayer
                     sc = scales[: rows * K // 16]
                     quantize_nvfp4(Wm, c, sc, ts, stream=st)
                     L.pack_matrix(e, m, c, sc, ts, stream=st)
+                elif w.fmt == FMT_MXFP4:
+                    c = codes[: rows * K // 2]
+                    sc = scales[: rows * K // 32]
+                    quantize_mxfp4(Wm, c, sc, stream=st)
+                    L.pack_matrix(e, m, c, sc, None, stream=st)
                 else:
                     c = codes[: rows * K]
                     sc = scales[: rows * K // 128]

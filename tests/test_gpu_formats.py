@@ -109,6 +109,62 @@ def test_quantize_fp6_bit_exact(case):
     assert np.array_equal(c, rc)
 
 
+def _gpu_quant_mxfp4(W):
+    rows, K = W.shape
+    Wd = torch.from_numpy(W).cuda()
+    c = torch.empty(rows * K // 2, dtype=torch.uint8, device="cuda")
+    e = torch.empty(rows * K // 32, dtype=torch.uint8, device="cuda")
+    moe.quantize_mxfp4(Wd, c, e)
+    torch.cuda.synchronize()
+    return c.cpu().numpy().reshape(rows, K // 2), e.cpu().numpy().reshape(rows, K // 32)
+
+
+@pytest.mark.parametrize("case", ["ties", "random", "workload"])
+def test_quantize_mxfp4_bit_exact(case):
+    if case == "ties":
+        W = np.zeros((16, 128), np.float32)
+        grid = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 7.0, 7.99], np.float32)
+        W[0, :10] = grid                               # amax 7.99: E = 0, ties and saturation
+        W[0, 32:42] = -grid * 2.0 ** -20
+        W[1, :32] = np.float32(1e-40)                  # subnormal block
+        W[2, 64:96] = np.float32(2.0 ** 100)           # huge, exactly a power of two
+        W[3, 96] = np.float32(3e38)
+    elif case == "random":
+        rng = np.random.default_rng(3)
+        W = (rng.standard_normal((32, 256)) * np.exp(3 * rng.standard_normal((32, 1)))).astype(np.float32)
+        W[5] = 0.0
+    else:
+        W = gen.expert_weight(gen.get_workload(6), 3, 0)[:256]
+    c, e = _gpu_quant_mxfp4(W)
+    rc, re_ = oracle.quantize_mxfp4(W)
+    assert np.array_equal(e, re_)
+    assert np.array_equal(c, rc)
+
+
+def test_mxfp4_pack_rejects_exponents_beyond_the_tile_scale_range():
+    """The tile layout holds a block scale as an e4m3 power of two within 17
+    binades of the matrix's largest one; a wider spread is an error, and so is
+    a NaN scale byte."""
+    H, I = 128, 64
+    L = moe.MoeLayer(moe.FMT_MXFP4, H, I, 2, 1, 0)
+    c = np.full((I, H // 2), 0x22, np.uint8)            # every code 1.0
+    e = np.full((I, H // 32), 127, np.uint8)
+    e[3, 1] = 127 - 17                                  # 17 binades below: fine
+    L.pack_matrix(0, 0, c, e)
+    e[3, 1] = 127 - 18                                  # 18 binades: rejected
+    with pytest.raises(moe.MoeError) as err:
+        L.pack_matrix(0, 0, c, e)
+    assert err.value.code == moe.EINVAL
+    e[3, 1] = 127
+    c[3, 16:32] = 0                                     # an all-zero block may have any exponent
+    e[3, 1] = 0
+    L.pack_matrix(0, 0, c, e)
+    e[5, 0] = 255
+    with pytest.raises(moe.MoeError):
+        L.pack_matrix(0, 0, c, e)
+    L.close()
+
+
 def _dequant_gpu(L, expert, matrix, rows, K):
     out = torch.full((rows, K), float("nan"), device="cuda")
     L.debug_dequant(expert, matrix, out)
@@ -117,7 +173,8 @@ def _dequant_gpu(L, expert, matrix, rows, K):
 
 
 @pytest.mark.parametrize("name,fmt,H,I", [("nvfp4", 1, 256, 128), ("nvfp4-ragged", 1, 320, 192),
-                                           ("fp6", 2, 256, 128), ("fp6-ragged", 2, 1152, 384)])
+                                           ("fp6", 2, 256, 128), ("fp6-ragged", 2, 1152, 384),
+                                           ("mxfp4", 3, 256, 128), ("mxfp4-ragged", 3, 320, 192)])
 def test_pack_from_host_and_dequant_bit_exact(name, fmt, H, I):
     """Oracle-quantised canonical bytes, packed from the host, decode bit-exactly
     (super-chunks with a partial tail in the ragged shapes)."""
@@ -133,7 +190,8 @@ def test_pack_from_host_and_dequant_bit_exact(name, fmt, H, I):
     L.close()
 
 
-@pytest.mark.parametrize("widx,experts", [(0, None), (1, [0, 5, 511, 512]), (2, [0, 255, 256])])
+@pytest.mark.parametrize("widx,experts", [(0, None), (1, [0, 5, 511, 512]), (2, [0, 255, 256]),
+                                          (5, None), (6, [0, 255, 256])])
 def test_device_built_layer_dequant_bit_exact(widx, experts):
     """The full device pipeline (generator -> device quantiser -> packer) gives
     the weights the oracle's own quantiser gives, bit for bit."""

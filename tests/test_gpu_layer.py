@@ -48,7 +48,7 @@ def test_tiny_workload():
     assert ties == 0
 
 
-@pytest.mark.parametrize("fmt", [1, 2])
+@pytest.mark.parametrize("fmt", [1, 2, 3])
 @pytest.mark.parametrize("T", [1, 5, 13, 64, 70, 200])
 def test_small_layers_ragged_token_counts(fmt, T):
     """Several tiles, ragged last entries, both routing paths (T <= 64 fused,
@@ -125,6 +125,37 @@ def test_prefill_full_size_sampled():
     sample = [0, 1, 7, 8, 511, 1024, 2047, 2048, 3000, 4093, 4094, 4095]
     rel, ties = compare_layer(w, layer(w), gen.x_tokens(w), sample=sample)
     print(f"prefill T=4096 (sampled): rel-L2 {rel:.2e}, near ties {ties}")
+
+
+def test_tiny_mxfp4_workload():
+    w = gen.get_workload(5)
+    rel, ties = compare_layer(w, layer(w), gen.x_tokens(w))
+    assert ties == 0
+
+
+def test_deepseek_shape_mxfp4_decode_full_size():
+    w = gen.get_workload(6)
+    L = build_layer(w, T_max=8)
+    try:
+        assert L.launches(1) == 3
+        rel, ties = compare_layer(w, L, gen.x_tokens(w))
+        print(f"decode mxfp4 (H 4096, I 2048, E 256, k 6): rel-L2 {rel:.2e}, near ties {ties}")
+    finally:
+        L.close()
+
+
+def test_deepseek_shape_mxfp4_prefill_sampled():
+    """T = 4096 over 256 experts (96 tokens per expert): the tcgen05 grouped
+    GEMMs on MXFP4 weights packed as e4m3 powers of two."""
+    w = gen.get_workload(7)
+    L = build_layer(w, T_max=w.T)
+    try:
+        assert L.launches(w.T) == 7  # convert x, tc router, top-k, dispatch, tc gate/up, tc down, combine
+        sample = [0, 1, 100, 2047, 2048, 4095]
+        rel, ties = compare_layer(w, L, gen.x_tokens(w), sample=sample)
+        print(f"prefill mxfp4 T=4096 (sampled): rel-L2 {rel:.2e}, near ties {ties}")
+    finally:
+        L.close()
 
 
 # ---------------------------------------------------------------- properties

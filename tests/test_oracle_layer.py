@@ -92,7 +92,7 @@ def test_dispatch_matches_numpy():
     assert np.array_equal(np.sort(perm), np.arange(T * k))
 
 
-@pytest.mark.parametrize("fmt", [oracle.FMT_NVFP4, oracle.FMT_FP6])
+@pytest.mark.parametrize("fmt", [oracle.FMT_NVFP4, oracle.FMT_FP6, oracle.FMT_MXFP4])
 def test_expert_ffn_matches_dense_swiglu(fmt):
     L, x = _tiny_layer(fmt=fmt)
     for e in (0, L.E):  # a routed expert and the shared one

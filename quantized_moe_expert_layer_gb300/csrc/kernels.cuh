@@ -101,8 +101,15 @@ cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream
 // tensor-core (tcgen05) prefill path
 bool tc_path_ok(int fmt, int T, int k, int E, int H, int I);
 int max_tc_entries(int T, int E, int k);
-cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, cudaStream_t st);
-cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, cudaStream_t st);
+// tile_map: the CUtensorMap (128 bytes, 64-byte aligned) of the matrix region,
+// made by tc_make_tile_map with box_tiles = 8 * tc_group(M-blocks of the matrix)
+int tc_group(int mblocks);
+cudaError_t tc_make_tile_map(void* map, const uint8_t* region, int n_experts, int tiles,
+                             uint64_t tile_bytes, uint64_t expert_bytes, int box_tiles);
+cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, const void* tile_map,
+                             cudaStream_t st);
+cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, const void* tile_map,
+                           cudaStream_t st);
 bool tc_router_ok(int E, int H);
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);
 cudaError_t tc_kernels_init();

@@ -83,6 +83,11 @@ struct moe_layer {
   int fmt = 0, H = 0, I = 0, E = 0, k = 0, shared = 0;
   int dev_fmt = 0;  // layout of the packed tiles (MXFP4 is packed as NVFP4)
   ExpertGeom geom{};
+  // TMA tile maps (CUtensorMap) of the gate/up and down regions of the arena,
+  // for the tensor-core path; maps_ok false when they could not be made
+  alignas(64) unsigned char map_gu[128] = {};
+  alignas(64) unsigned char map_dn[128] = {};
+  bool maps_ok = false;
   uint8_t* arena = nullptr;
   uint64_t arena_bytes = 0;
   float* tscale = nullptr;
@@ -128,7 +133,7 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.E = L->E;
   p.k = L->k;
   p.shared = L->shared;
-  const bool tc = tc_path_ok(L->dev_fmt, T, L->k, L->E, L->H, L->I);
+  const bool tc = L->maps_ok && tc_path_ok(L->dev_fmt, T, L->k, L->E, L->H, L->I);
   // the tensor-core router writes the whole dot product: one K slice
   p.ksplit = tc && tc_router_ok(L->E, L->H) ? 1 : router_ksplit(T, L->H, L->E);
   p.partial = L->partial;
@@ -200,7 +205,9 @@ int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
 // experts + combine, after routing has filled idx / gates / dispatch
 bool fused_down(moe_layer* L, int T) { return down_combine_ok(T, L->k, L->shared, L->I); }
 
-bool tc_path(moe_layer* L, int T) { return tc_path_ok(L->dev_fmt, T, L->k, L->E, L->H, L->I); }
+bool tc_path(moe_layer* L, int T) {
+  return L->maps_ok && tc_path_ok(L->dev_fmt, T, L->k, L->E, L->H, L->I);
+}
 
 // prefill routing: logits as one bf16 GEMM on the tensor cores, then top-k and
 // dispatch as usual (the GEMM's output is the one K slice the top-k reads)
@@ -218,8 +225,8 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   ExpertParams ep = expert_params(L, x, T);
   if (tc_path(L, T)) {
     const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
-    CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, st));
-    CK("tensor-core down kernel launch", launch_tc_down(ep, gy, st));
+    CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, L->map_gu, st));
+    CK("tensor-core down kernel launch", launch_tc_down(ep, gy, L->map_dn, st));
     CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
     return MOE_OK;
   }
@@ -330,6 +337,15 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
       cudaMemset(L->status, 0, sizeof(int)) != cudaSuccess) {
     moe_layer_destroy(L);
     return fail(MOE_ECUDA, "moe_layer_create: cudaMemset failed");
+  }
+  if (L->dev_fmt == FMT_NVFP4 && H % 128 == 0 && (2 * I) % 128 == 0) {
+    const ExpertGeom& g = L->geom;
+    const int gu_tiles = 2 * I / 16, dn_tiles = H / 16;
+    L->maps_ok =
+        tc_make_tile_map(L->map_gu, L->arena, n_total, gu_tiles, g.gu.tile_bytes, g.expert_bytes,
+                         8 * tc_group(gu_tiles / 8)) == cudaSuccess &&
+        tc_make_tile_map(L->map_dn, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
+                         g.expert_bytes, 8 * tc_group(dn_tiles / 8)) == cudaSuccess;
   }
   *out = L;
   return MOE_OK;
@@ -679,13 +695,13 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       break;
     case 2:
       if (tc_path(L, T))
-        CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
+        CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu, st));
       else
         CK("gate/up", launch_gateup(ep, grid_y, false, st));
       break;
     case 3:
       if (tc_path(L, T))
-        CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), st));
+        CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn, st));
       else if (fused)
         CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, false, st));
       else

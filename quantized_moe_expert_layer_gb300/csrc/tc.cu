@@ -23,6 +23,9 @@
 // Every wait is bounded: on a timeout the kernel records MOE_ETIMEOUT in the
 // status word, stops issuing work, waits (bounded) for its MMAs, frees its
 // TMEM and returns.
+#include <cuda.h>  // CUtensorMap: the tile map of the packed arena
+#include <cudaTypedefs.h>
+
 #include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
@@ -393,7 +396,343 @@ size_t tc_smem() {
          sizeof(TcShared);
 }
 
+// ---------------------------------------------------------------- expert GEMMs with TMA-fed tiles
+// The expert GEMMs (MODE 0 gate/up + SwiGLU, MODE 1 down) with the packed
+// codes brought in by the Tensor Memory Accelerator and G M-blocks per CTA.
+//
+// Work item (expert, up to 128 tokens) x group of G 128-row M-blocks.  Per
+// 64-column K-chunk c:
+//   * one TMA load (warp 9) brings the code vectors of the group's 8G tiles
+//     (box {512 B, 1 piece, 8G tiles} of the arena's tile map, 4G KB) into a
+//     3-stage ring; once per super-chunk another brings their scale vectors
+//     into a 2-stage buffer.  The tile map views the packed layout as
+//     [expert][tile][512-byte piece][512 B], so a box is 8G pieces at the same
+//     offset of consecutive tiles: one bulk copy instead of 8G small ones,
+//     and several chunks in flight per SM.
+//   * the 8 producer warps copy the chunk's token rows (B, gathered through
+//     the dispatch, 64 columns each) with cp.async two chunks ahead into a
+//     4-stage ring, and dequantise each M-block's codes into a 128B-swizzled
+//     f16 A slot (a 4-slot ring, one slot per M-block);
+//   * one thread issues, per M-block, 4 MMAs into that M-block's TMEM
+//     accumulator (G accumulators of N columns side by side) and commits the
+//     A slot back; after the last M-block it commits the B stage back.
+// A token chunk is read once for G M-blocks (G = 4 where the matrix has 4k
+// M-blocks), which cuts the L2 traffic of the token rows by G.
+constexpr int kTxNA = 4;             // A slots (16 KB each)
+constexpr int kTxNB = 4;             // B stages (up to 16 KB each)
+constexpr int kTxLB = 2;             // B chunks in flight ahead of the dequantisation
+constexpr int kTxNR = 3;             // code stages (4 KB per M-block)
+constexpr int kTxThreads = 320;      // warps 0-7 producers / epilogue, 8 MMA, 9 TMA
+constexpr int kTxMaxG = 4;
+
+struct TxShared {
+  uint64_t a_full[kTxNA], a_empty[kTxNA];
+  uint64_t b_empty[kTxNB];
+  uint64_t r_full[kTxNR], r_empty[kTxNR];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t acc_full;
+  uint32_t tmem_base;
+  int abort;
+  int tok[kTcMaxN];
+};
+
+__host__ __device__ constexpr size_t tx_smem_bytes(int G) {
+  return 1024 + (size_t)kTxNA * kTcAStageBytes + (size_t)kTxNB * kTcBStageBytes +
+         (size_t)(kTxNR + 2) * 4096 * G + sizeof(TxShared);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+// 4-D tiled TMA load of the tile map box at (0, piece, tile, expert) into
+// shared memory, counted on `bar`.
+__device__ __forceinline__ void tma_load_tiles(uint32_t dst, const CUtensorMap* map, int piece,
+                                               int tile, int expert, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(piece), "r"(tile), "r"(expert),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTxThreads, 1)
+    tc_expert_kernel(ExpertParams p, const __grid_constant__ CUtensorMap tmap, int G) {
+  griddep_wait();
+  int expert, row0, n;
+  if (!tc_entry(p, blockIdx.y, expert, row0, n)) return;
+  extern __shared__ __align__(1024) uint8_t tx_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tx_smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int RB = 4096 * G;               // bytes of one code stage (8G tiles x 512 B)
+  const int n_pad = (n + 15) & ~15;
+  const int b_stage = n_pad * kTcK * 2;  // multiple of 2 KB: stages stay 1024-byte aligned
+  uint8_t* A = base;
+  uint8_t* B = A + kTxNA * kTcAStageBytes;
+  uint8_t* R = B + kTxNB * kTcBStageBytes;
+  uint8_t* SC = R + kTxNR * RB;
+  TxShared* sh = reinterpret_cast<TxShared*>(SC + 2 * RB);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.T * p.k;
+  const int K = MODE == 1 ? p.I : p.H;
+  const int KC = K / kTcK;
+  const int tile0 = 8 * G * blockIdx.x;  // first 16-row tile of this CTA's M-blocks
+  const int npc = n_pad <= 32 ? 32 : (n_pad <= 64 ? 64 : 128);  // TMEM columns per accumulator
+  const uint32_t ncols = (uint32_t)(G * npc);
+
+  if (tid == 0) {
+    for (int i = 0; i < kTxNA; ++i) {
+      mbar_init(&sh->a_full[i], kTcProducers);
+      mbar_init(&sh->a_empty[i], 1);
+    }
+    for (int i = 0; i < kTxNB; ++i) mbar_init(&sh->b_empty[i], 1);
+    for (int i = 0; i < kTxNR; ++i) {
+      mbar_init(&sh->r_full[i], 1);
+      mbar_init(&sh->r_empty[i], kTcProducers);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->s_full[i], 1);
+      mbar_init(&sh->s_empty[i], kTcProducers);
+    }
+    mbar_init(&sh->acc_full, 1);
+    sh->abort = 0;
+    mbar_init_fence();
+  }
+  for (int i = tid; i < n_pad; i += kTxThreads) {
+    int tk = 0;
+    if (i < n) tk = (MODE == 0) ? ((expert == p.E) ? row0 - S + i : p.row_token[row0 + i]) : row0 + i;
+    sh->tok[i] = tk;  // MODE 0: token index into x; MODE 1: row of abuf
+  }
+  // token-row padding stays zero in every stage (cp.async never writes it)
+  for (int i = tid; i < kTxNB * (n_pad - n) * 8; i += kTxThreads) {
+    const int st = i / ((n_pad - n) * 8), rem = i % ((n_pad - n) * 8);
+    const int r = n + rem / 8, c16 = rem % 8;
+    *reinterpret_cast<uint4*>(B + st * b_stage + swz(r, c16)) = make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 8) tmem_alloc(&sh->tmem_base, ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = sh->tmem_base;
+  volatile int* abort = &sh->abort;
+  const uint32_t a_s = smem_u32(A), b_s = smem_u32(B), r_s = smem_u32(R), sc_s = smem_u32(SC);
+
+  if (warp < 8) {
+    // ---------------------------------------------------------------- producers
+    // thread u: tile u/32 of every M-block of the group, lane u%32 of it
+    const int u = tid, ti = u >> 5, ln = u & 31, gi = ln >> 2, t = ln & 3;
+    const uint16_t* bsrc = (MODE == 0) ? p.xh : p.abuf;
+    const int bld = (MODE == 0) ? p.H : p.I;
+    auto issue_b = [&](int c) {  // chunk c's token rows into B stage c % kTxNB
+      const uint32_t bs = b_s + (c % kTxNB) * b_stage;
+      for (int v = tid; v < n * 8; v += kTcProducers) {
+        const int r = v >> 3, c16 = v & 7;
+        cp_async16(bs + swz(r, c16), bsrc + (size_t)sh->tok[r] * bld + c * kTcK + 8 * c16);
+      }
+    };
+    for (int c = 0; c < kTxLB; ++c) {
+      if (c < KC) issue_b(c);
+      cp_async_commit();
+    }
+    uint4 sv[kTxMaxG];
+    for (int c = 0; c < KC; ++c) {
+      const int s = c >> 3, j = c & 7;
+      if (j == 0) {  // the super-chunk's scale vectors of my tiles
+        if (!mbar_wait(&sh->s_full[s & 1], (s >> 1) & 1, abort)) break;
+#pragma unroll
+        for (int m = 0; m < kTxMaxG; ++m)
+          if (m < G) sv[m] = lds128(sc_s + (s & 1) * RB + (m * 8 + ti) * 512 + 16 * ln);
+        mbar_arrive(&sh->s_empty[s & 1]);
+      }
+      if (!mbar_wait(&sh->r_full[c % kTxNR], (c / kTxNR) & 1, abort)) break;
+      uint4 cv[kTxMaxG];
+#pragma unroll
+      for (int m = 0; m < kTxMaxG; ++m)
+        if (m < G) cv[m] = lds128(r_s + (c % kTxNR) * RB + (m * 8 + ti) * 512 + 16 * ln);
+      mbar_arrive(&sh->r_empty[c % kTxNR]);
+      cp_async_wait<kTxLB - 1>();  // this thread's token-row pieces of chunk c have landed
+      bool ok = true;
+#pragma unroll
+      for (int m = 0; m < kTxMaxG; ++m) {
+        if (m >= G) break;
+        const int q = c * G + m, slot = q % kTxNA;
+        if (!mbar_wait(&sh->a_empty[slot], ((q / kTxNA) & 1) ^ 1, abort)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[m], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
+        const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
+        uint32_t r0[8], r1[8];  // rows gi and gi+8 of tile ti: 16 f16 each
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t hh[4];
+          e2m1x8_to_f16x8(u4get(cv[m], w), hh);
+          r0[2 * w] = hmul2(hh[0], s_lo);
+          r0[2 * w + 1] = hmul2(hh[2], s_lo);
+          r1[2 * w] = hmul2(hh[1], s_hi);
+          r1[2 * w + 1] = hmul2(hh[3], s_hi);
+        }
+        const int ra = 16 * ti + gi, rb = ra + 8;
+        const uint32_t as = a_s + slot * kTcAStageBytes;
+        st_shared_v4(as + swz(ra, 2 * t), r0[0], r0[1], r0[2], r0[3]);
+        st_shared_v4(as + swz(ra, 2 * t + 1), r0[4], r0[5], r0[6], r0[7]);
+        st_shared_v4(as + swz(rb, 2 * t), r1[0], r1[1], r1[2], r1[3]);
+        st_shared_v4(as + swz(rb, 2 * t + 1), r1[4], r1[5], r1[6], r1[7]);
+        fence_async_smem();  // (also publishes the token rows of chunk c to the MMA)
+        mbar_arrive(&sh->a_full[slot]);
+      }
+      if (!ok) break;
+      // refill: chunk c + kTxLB goes to the B stage the MMAs of chunk c + kTxLB - kTxNB freed
+      const int cn = c + kTxLB;
+      if (cn < KC) {
+        if (!mbar_wait(&sh->b_empty[cn % kTxNB], ((cn / kTxNB) & 1) ^ 1, abort)) break;
+        issue_b(cn);
+      }
+      cp_async_commit();
+    }
+    cp_async_wait<0>();
+  } else if (warp == 8) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issue
+      const uint32_t idesc = idesc_f16(kTcM, n_pad);
+      bool ok = true;
+      for (int c = 0; c < KC && ok; ++c) {
+        const uint64_t bd = sw128_desc(b_s + (c % kTxNB) * b_stage);
+        for (int m = 0; m < G; ++m) {
+          const int q = c * G + m, slot = q % kTxNA;
+          if (!mbar_wait(&sh->a_full[slot], (q / kTxNA) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(a_s + slot * kTcAStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTcK / 16; ++kk)  // +32 bytes per 16-column step
+            umma_f16(tmem_d + m * npc, ad + 2 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
+          umma_commit(&sh->a_empty[slot]);
+        }
+        if (ok) umma_commit(&sh->b_empty[c % kTxNB]);
+      }
+      umma_commit(&sh->acc_full);  // fires once every issued MMA is done
+    }
+    __syncwarp();
+  } else {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA issue
+      const CUtensorMap* map = &tmap;
+      int issued = 0;  // code chunks issued
+      for (int c = 0; c < KC; ++c) {
+        const int s = c >> 3, j = c & 7;
+        if (j == 0) {
+          if (!mbar_wait(&sh->s_empty[s & 1], ((s >> 1) & 1) ^ 1, abort)) break;
+          mbar_arrive_expect(&sh->s_full[s & 1], (uint32_t)RB);
+          tma_load_tiles(sc_s + (s & 1) * RB, map, 9 * s, tile0, expert, &sh->s_full[s & 1]);
+        }
+        if (!mbar_wait(&sh->r_empty[c % kTxNR], ((c / kTxNR) & 1) ^ 1, abort)) break;
+        mbar_arrive_expect(&sh->r_full[c % kTxNR], (uint32_t)RB);
+        tma_load_tiles(r_s + (c % kTxNR) * RB, map, 9 * s + 1 + j, tile0, expert,
+                       &sh->r_full[c % kTxNR]);
+        ++issued;
+      }
+      if (*abort) {  // let the copies in flight land before the CTA exits (bounded waits)
+        for (int c = (issued > kTxNR ? issued - kTxNR : 0); c < issued; ++c)
+          mbar_drain(&sh->r_full[c % kTxNR], (c / kTxNR) & 1);
+        const int ns = issued > 0 ? ((issued - 1) >> 3) + 1 : 0;
+        for (int s = (ns > 2 ? ns - 2 : 0); s < ns; ++s) mbar_drain(&sh->s_full[s & 1], (s >> 1) & 1);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  bool ok = true;
+  if (warp < 8) ok = mbar_wait(&sh->acc_full, 0, abort);
+  if (warp < 8 && !ok) mbar_drain(&sh->acc_full, 0);  // MMAs in flight finish before TMEM is freed
+  tc_fence_after();
+  if (warp < 8 && ok && !*abort) {
+    const int qd = warp & 3;             // TMEM lane quadrant of this warp
+    const int r = 32 * qd + lane;        // row of the 128-row block
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    for (int m = 0; m < G; ++m) {
+      const int mb = G * blockIdx.x + m;  // M-block of the matrix
+      const uint32_t acc = tmem_d + lane_addr + (uint32_t)(m * npc);
+      if (MODE == 0) {
+        const int pair = 4 * mb + qd, i = 16 * pair + (lane & 15);
+        const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
+        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
+          uint32_t v[32];
+          tmem_ld32(acc + c0, v);
+#pragma unroll
+          for (int qq = 0; qq < 32; ++qq) {
+            const float mine = __uint_as_float(v[qq]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+            const int col = c0 + qq;
+            if (lane < 16 && col < n) {
+              const float Gv = ts_g * mine, U = ts_u * other;
+              const float a = Gv / (1.0f + expf(-Gv)) * U;
+              p.abuf[(size_t)(row0 + col) * p.I + i] = __half_as_ushort(__float2half_rn(a));
+            }
+          }
+        }
+      } else {
+        const float ts = p.tscale[expert * 3 + 2];
+        const int h = kTcM * mb + r;
+        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
+          uint32_t v[32];
+          tmem_ld32(acc + c0, v);
+#pragma unroll
+          for (int qq = 0; qq < 32; ++qq) {
+            const int col = c0 + qq;
+            if (col < n) p.ybuf[(size_t)(row0 + col) * p.H + h] = ts * __uint_as_float(v[qq]);
+          }
+        }
+      }
+    }
+  }
+  if (*abort && tid == 0) *p.status = -5;  // MOE_ETIMEOUT
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem_d, ncols);
+  }
+}
+
 }  // namespace
+
+// M-blocks per CTA of the TMA-fed expert GEMMs: 4 where they divide the matrix
+int tc_group(int mblocks) { return mblocks % 4 == 0 ? 4 : (mblocks % 2 == 0 ? 2 : 1); }
+
+cudaError_t tc_make_tile_map(void* map, const uint8_t* region, int n_experts, int tiles,
+                             uint64_t tile_bytes, uint64_t expert_bytes, int box_tiles) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // [expert][tile][512-byte piece][64 x 8 bytes]; a box: one piece of box_tiles consecutive tiles
+  const cuuint64_t dims[4] = {64, (cuuint64_t)(tile_bytes / 512), (cuuint64_t)tiles,
+                              (cuuint64_t)n_experts};
+  const cuuint64_t strides[3] = {512, tile_bytes, expert_bytes};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tiles, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT64, 4,
+                            const_cast<uint8_t*>(region), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 bool tc_path_ok(int fmt, int T, int k, int E, int H, int I) {
   // NVFP4 only; enough tokens per expert for a dense contraction; tile shapes
@@ -407,14 +746,20 @@ int max_tc_entries(int T, int E, int k) {
   return (int)(m + S / kTcMaxN + 1);
 }
 
-cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, cudaStream_t st) {
-  dim3 grid((2 * p.I) / kTcM, grid_y);
-  return launch_k(tc_gemm_kernel<0>, grid, dim3(kTcThreads), tc_smem(), st, true, p);
+cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, const void* tile_map,
+                             cudaStream_t st) {
+  const int mblocks = (2 * p.I) / kTcM, G = tc_group(mblocks);
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  return launch_k(tc_expert_kernel<0>, dim3(mblocks / G, grid_y), dim3(kTxThreads),
+                  tx_smem_bytes(G), st, true, p, map, G);
 }
 
-cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, cudaStream_t st) {
-  dim3 grid(p.H / kTcM, grid_y);
-  return launch_k(tc_gemm_kernel<1>, grid, dim3(kTcThreads), tc_smem(), st, true, p);
+cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, const void* tile_map,
+                           cudaStream_t st) {
+  const int mblocks = p.H / kTcM, G = tc_group(mblocks);
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  return launch_k(tc_expert_kernel<1>, dim3(mblocks / G, grid_y), dim3(kTxThreads),
+                  tx_smem_bytes(G), st, true, p, map, G);
 }
 
 bool tc_router_ok(int E, int H) { return E % kTcM == 0 && H % kTcK == 0; }
@@ -426,11 +771,11 @@ cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st) {
 }
 
 cudaError_t tc_kernels_init() {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tc_smem());
+  cudaError_t e = cudaFuncSetAttribute(tc_expert_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tx_smem_bytes(kTxMaxG));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc_smem());
+  e = cudaFuncSetAttribute(tc_expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tx_smem_bytes(kTxMaxG));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tc_smem());

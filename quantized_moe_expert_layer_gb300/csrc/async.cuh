@@ -54,6 +54,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
   return true;
 }
+// The same with a suspend-time hint: a waiting thread sleeps in the barrier
+// (woken when the phase completes) instead of spinning, so it leaves its
+// sub-partition's issue slots to the other warps.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const long long t0 = clock64();
+  while (!mbar_test_sleep(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitBudget) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
 // Bounded wait that ignores the abort flag (draining copies before exit).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();

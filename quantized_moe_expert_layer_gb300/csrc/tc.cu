@@ -1,28 +1,26 @@
 // Prefill path: grouped expert GEMMs on the 5th-generation tensor cores
-// (tcgen05 kind::f16, fp32 accumulators in tensor memory).
+// (tcgen05 kind::f16, fp32 accumulators in tensor memory), and the router as
+// a bf16 GEMM.
 //
-// Per work item (expert e, 128-row block of W, up to 128 tokens routed to e):
-//   D[128 x N] (TMEM, fp32) = sum over K of A[128 x 64] . B[N x 64]^T
+// Expert GEMMs (tc_expert_kernel): per work item (expert e, up to 128 tokens
+// routed to e) and group of G 128-row blocks of W,
+//   D_m[128 x N] (TMEM, fp32) = sum over K of A_m[128 x 64] . B[N x 64]^T
 // A = the weights, dequantised exactly to f16 (e2m1 code * e4m3 block scale is
-// an f16) by four producer warps from the packed NVFP4 tiles and written to
-// shared memory in the 128-byte-swizzled K-major layout the MMA reads; B = the
-// token rows (x, gathered through the dispatch permutation and converted from
-// bf16 to f16, or the SwiGLU output a), written the same way.  One thread
-// issues the MMAs; stages are handed over with mbarriers; tcgen05.commit frees
-// a stage when the MMAs reading it are done.  The epilogue warps read D from
-// TMEM (warp w owns lanes 32w..32w+31) and apply the fp32 tensor scale and
-// SwiGLU (gate/up) or write y rows (down).
-//
-// MODE 2 is the router for large T: a plain bf16 GEMM, logits[t][e] =
-// x[t] . Wr[e], with 128 experts as M and 128 tokens as N; both operands are
-// copied straight into the swizzled stages (no dequantisation).
+// an f16) by the producer warps from the packed NVFP4 tiles, which the Tensor
+// Memory Accelerator brings in, and written to shared memory in the
+// 128-byte-swizzled K-major layout the MMA reads; B = the token rows (x,
+// gathered through the dispatch permutation, or the SwiGLU output a), copied
+// the same way.  One thread issues the MMAs; stages are handed over with
+// mbarriers; tcgen05.commit frees a stage when the MMAs reading it are done.
+// The epilogue warps read D from TMEM (warp w owns lanes 32(w%4)..+31) and
+// apply the fp32 tensor scale and SwiGLU (gate/up) or write y rows (down).
 //
 // The weights stay the M operand and the token count the N operand (N is 80 on
 // average for 4096 tokens over 512 experts), as the survey of the prompt paths
 // suggests: experts with few tokens keep the decoded weights as the wide side.
 // Every wait is bounded: on a timeout the kernel records MOE_ETIMEOUT in the
-// status word, stops issuing work, waits (bounded) for its MMAs, frees its
-// TMEM and returns.
+// status word, stops issuing work, waits (bounded) for its MMAs and copies,
+// frees its TMEM and returns.
 #include <cuda.h>  // CUtensorMap: the tile map of the packed arena
 #include <cudaTypedefs.h>
 
@@ -41,7 +39,6 @@ constexpr int kTcLookahead = kTcStages - 2;  // chunks in flight; one stage of s
 constexpr int kTcProducers = 256;    // warps 0-7: producers, then epilogue
 constexpr int kTcThreads = 288;      // + warp 8: TMEM allocation and MMA issue
 constexpr int kTcAStageBytes = kTcM * kTcK * 2;     // 16 KB of dequantised f16 weights
-constexpr int kTcRawStageBytes = 8 * 512;           // 4 KB of packed codes (8 tiles)
 constexpr int kTcBStageBytes = kTcMaxN * kTcK * 2;  // 16 KB of f16 token rows
 
 // ---------------------------------------------------------------- tcgen05
@@ -121,7 +118,6 @@ struct TcShared {
   uint64_t acc_full;
   uint32_t tmem_base;
   int abort;
-  int tok[kTcMaxN];
 };
 
 // Work item y of a tc launch: leading shared-expert items, then routed ones.
@@ -146,27 +142,17 @@ __device__ __forceinline__ bool tc_entry(const ExpertParams& p, int y, int& expe
   return true;
 }
 
-// The shared skeleton of the GEMMs.  MODE 0: gate/up + SwiGLU -> abuf;
-// MODE 1: down -> ybuf; MODE 2: router logits (bf16 x bf16) -> logits_out.
-//
-// Producer thread u (of 256) owns packed vector u of each chunk: tile u/32,
-// lane u%32 of the 16-row tile layout, i.e. rows 16*(u/32) + (u%32)/4 (+8) and
-// 16 columns.  Chunk c's raw codes and token rows are copied with cp.async
-// kTcLookahead chunks ahead; at chunk c the thread waits for its own copies,
-// dequantises its vector into the swizzled A stage, fences the async proxy and
-// arrives on full[c % stages].
-template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) {
+// The router GEMM for large T: logits[t][e] = x[t] . Wr[e] (bf16 x bf16 ->
+// fp32), 128 experts as M and up to 128 tokens as N per CTA.  The 8 copy
+// warps bring the router rows and the token rows of each 64-column chunk
+// straight into 128B-swizzled stages with cp.async, kTcLookahead chunks ahead,
+// fence the async proxy and arrive on full[c % stages]; one thread issues the
+// MMAs and commits each stage back; the copy warps then read D from TMEM.
+__global__ void __launch_bounds__(kTcThreads, 1) tc_router_kernel(ExpertParams p) {
   griddep_wait();
-  int expert, row0, n;
-  if (MODE == 2) {  // token tile blockIdx.y of the router GEMM
-    expert = 0;
-    row0 = kTcMaxN * blockIdx.y;
-    n = min(kTcMaxN, p.T - row0);
-    if (n <= 0) return;
-  } else if (!tc_entry(p, blockIdx.y, expert, row0, n)) {
-    return;
-  }
+  const int row0 = kTcMaxN * blockIdx.y;  // token tile
+  const int n = min(kTcMaxN, p.T - row0);
+  if (n <= 0) return;
   extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -174,16 +160,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
   const int b_stage = n_pad * kTcK * 2;  // multiple of 2 KB: stages stay 1024-byte aligned
   uint8_t* A = base;
   uint8_t* B = A + kTcStages * kTcAStageBytes;
-  uint8_t* RAW = B + kTcStages * kTcBStageBytes;
-  TcShared* sh = reinterpret_cast<TcShared*>(RAW + kTcStages * kTcRawStageBytes);
+  TcShared* sh = reinterpret_cast<TcShared*>(B + kTcStages * kTcBStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = p.T * p.k;
-  const int K = MODE == 1 ? p.I : p.H;
-  const int KC = K / kTcK;
-  const int mb = blockIdx.x;
+  const int K = p.H, KC = K / kTcK, mb = blockIdx.x;
   const uint32_t ncols = n_pad <= 32 ? 32 : (n_pad <= 64 ? 64 : 128);
-  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
-  const MatGeom g = mat_geom(FMT_NVFP4, K);
 
   if (tid == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -193,11 +173,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
     mbar_init(&sh->acc_full, 1);
     sh->abort = 0;
     mbar_init_fence();
-  }
-  for (int i = tid; i < n_pad; i += kTcThreads) {
-    int tk = 0;
-    if (i < n) tk = (MODE == 0) ? ((expert == p.E) ? row0 - S + i : p.row_token[row0 + i]) : row0 + i;
-    sh->tok[i] = tk;  // MODE 0 / 2: token index into x; MODE 1: row of abuf
   }
   // token-row padding stays zero in every stage (cp.async never writes it)
   for (int i = tid; i < kTcStages * (n_pad - n) * 8; i += kTcThreads) {
@@ -213,89 +188,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
   volatile int* abort = &sh->abort;
 
   if (warp < 8) {
-    // ---------------------------------------------------------------- producers
-    const int u = tid, ti = u >> 5, ln = u & 31, gi = ln >> 2, t = ln & 3;
-    const uint8_t* tile = (MODE == 0) ? eb + (size_t)(8 * mb + ti) * p.gu_tile_bytes
-                                      : eb + p.gu_bytes + (size_t)(8 * mb + ti) * p.dn_tile_bytes;
-    const uint16_t* bsrc = (MODE == 0) ? p.xh : (MODE == 1 ? p.abuf : p.x);
-    const int bld = (MODE == 1) ? p.I : p.H;
-    const uint16_t* arow = p.wr + (size_t)kTcM * mb * p.H;  // MODE 2: 128 router rows
-    // ask L2 for everything this CTA will read
-    if (MODE == 2) {
-      for (int i = tid; i < kTcM * (K / 64); i += kTcProducers)
-        prefetch_l2(arow + (size_t)(i / (K / 64)) * p.H + 64 * (i % (K / 64)));
-    } else {
-      for (int s = 0; s < g.nsc; ++s)
-        for (int j = 0; j <= sc_units(g, s); ++j)
-          prefetch_l2(tile + (size_t)s * g.sc_bytes + 512 * j + 16 * ln);
-    }
-    for (int i = tid; i < n * (K / 64); i += kTcProducers)
-      prefetch_l2(bsrc + (size_t)sh->tok[i / (K / 64)] * bld + 64 * (i % (K / 64)));
-    const uint32_t a_s = smem_u32(A), b_s = smem_u32(B), raw_s = smem_u32(RAW);
+    // ---------------------------------------------------------------- copies
+    const uint16_t* arow = p.wr + (size_t)kTcM * mb * p.H;  // 128 router rows
+    for (int i = tid; i < kTcM * KC; i += kTcProducers)     // ask L2 for everything
+      prefetch_l2(arow + (size_t)(i / KC) * p.H + 64 * (i % KC));
+    const uint32_t a_s = smem_u32(A), b_s = smem_u32(B);
     auto issue = [&](int c) {  // chunk c's copies into stage c % stages
-      const int stage = c % kTcStages, s = c >> 3, j = c & 7;
-      if (MODE == 2) {  // router rows straight into the swizzled A stage
-        for (int v = tid; v < kTcM * 8; v += kTcProducers) {
-          const int r = v >> 3, c16 = v & 7;
-          cp_async16(a_s + stage * kTcAStageBytes + swz(r, c16),
-                     arow + (size_t)r * p.H + c * kTcK + 8 * c16);
-        }
-      } else {
-        cp_async16(raw_s + stage * kTcRawStageBytes + 16 * u,
-                   tile + (size_t)s * g.sc_bytes + 512 * (1 + j) + 16 * ln);
+      const int stage = c % kTcStages;
+      for (int v = tid; v < kTcM * 8; v += kTcProducers) {
+        const int r = v >> 3, c16 = v & 7;
+        cp_async16(a_s + stage * kTcAStageBytes + swz(r, c16), arow + (size_t)r * p.H + c * kTcK + 8 * c16);
       }
       const uint32_t bs = b_s + stage * b_stage;
       for (int v = tid; v < n * 8; v += kTcProducers) {
         const int r = v >> 3, c16 = v & 7;
-        cp_async16(bs + swz(r, c16), bsrc + (size_t)sh->tok[r] * bld + c * kTcK + 8 * c16);
+        cp_async16(bs + swz(r, c16), p.x + (size_t)(row0 + r) * p.H + c * kTcK + 8 * c16);
       }
     };
     for (int c = 0; c < kTcLookahead; ++c) {
       if (c < KC) issue(c);
       cp_async_commit();
     }
-    uint4 sv = make_uint4(0, 0, 0, 0), sv_next = sv;
-    if (MODE != 2) sv = sv_next = ldg_stream(tile + 16 * ln);
     for (int c = 0; c < KC; ++c) {
-      const int stage = c % kTcStages, s = c >> 3, j = c & 7;
-      if (MODE != 2) {
-        if (j == 0 && c > 0) sv = sv_next;
-        if (j == 4 && s + 1 < g.nsc) sv_next = ldg_stream(tile + (size_t)(s + 1) * g.sc_bytes + 16 * ln);
-      }
       cp_async_wait<kTcLookahead - 1>();  // this thread's copies of chunk c have landed
-      if (MODE == 2) {  // nothing to dequantise
-        fence_async_smem();
-        mbar_arrive(&sh->full[stage]);
-        const int cn = c + kTcLookahead;
-        if (cn < KC) {
-          if (!mbar_wait(&sh->empty[cn % kTcStages], ((cn / kTcStages) & 1) ^ 1, abort)) break;
-          issue(cn);
-        }
-        cp_async_commit();
-        continue;
-      }
-      const uint4 cv = *reinterpret_cast<const uint4*>(RAW + stage * kTcRawStageBytes + 16 * u);
-      const uint32_t sp = e4m3x2_to_f16x2((u4get(sv, j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
-      const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
-      uint32_t r0[8], r1[8];  // rows gi and gi+8 of tile ti: 16 f16 each
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        uint32_t hh[4];
-        e2m1x8_to_f16x8(u4get(cv, w), hh);
-        r0[2 * w] = hmul2(hh[0], s_lo);
-        r0[2 * w + 1] = hmul2(hh[2], s_lo);
-        r1[2 * w] = hmul2(hh[1], s_hi);
-        r1[2 * w + 1] = hmul2(hh[3], s_hi);
-      }
-      const int ra = 16 * ti + gi, rb = ra + 8;
-      const uint32_t as = a_s + stage * kTcAStageBytes;
-      st_shared_v4(as + swz(ra, 2 * t), r0[0], r0[1], r0[2], r0[3]);
-      st_shared_v4(as + swz(ra, 2 * t + 1), r0[4], r0[5], r0[6], r0[7]);
-      st_shared_v4(as + swz(rb, 2 * t), r1[0], r1[1], r1[2], r1[3]);
-      st_shared_v4(as + swz(rb, 2 * t + 1), r1[4], r1[5], r1[6], r1[7]);
       fence_async_smem();
-      mbar_arrive(&sh->full[stage]);
-      // refill: chunk c + lookahead goes to the stage the MMAs of chunk c - 1 free
+      mbar_arrive(&sh->full[c % kTcStages]);
       const int cn = c + kTcLookahead;
       if (cn < KC) {
         if (!mbar_wait(&sh->empty[cn % kTcStages], ((cn / kTcStages) & 1) ^ 1, abort)) break;
@@ -306,79 +223,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
     cp_async_wait<0>();
   } else {
     if (lane == 0) {
-    // ---------------------------------------------------------------- MMA issue
-    const uint32_t idesc = idesc_f16(kTcM, n_pad) | (MODE == 2 ? (1u << 7) | (1u << 10) : 0u);  // bf16
-    const uint32_t a_s = smem_u32(A), b_s = smem_u32(B);
-    for (int c = 0; c < KC; ++c) {
-      const int stage = c % kTcStages;
-      if (!mbar_wait(&sh->full[stage], (c / kTcStages) & 1, abort)) break;
-      tc_fence_after();
-      const uint64_t ad = sw128_desc(a_s + stage * kTcAStageBytes);
-      const uint64_t bd = sw128_desc(b_s + stage * b_stage);
+      // ---------------------------------------------------------------- MMA issue
+      const uint32_t idesc = idesc_f16(kTcM, n_pad) | (1u << 7) | (1u << 10);  // A and B bf16
+      const uint32_t a_s = smem_u32(A), b_s = smem_u32(B);
+      for (int c = 0; c < KC; ++c) {
+        const int stage = c % kTcStages;
+        if (!mbar_wait(&sh->full[stage], (c / kTcStages) & 1, abort)) break;
+        tc_fence_after();
+        const uint64_t ad = sw128_desc(a_s + stage * kTcAStageBytes);
+        const uint64_t bd = sw128_desc(b_s + stage * b_stage);
 #pragma unroll
-      for (int kk = 0; kk < kTcK / 16; ++kk)  // +32 bytes per 16-column step
-        umma_f16(tmem_d, ad + 2 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
-      umma_commit(&sh->empty[stage]);
+        for (int kk = 0; kk < kTcK / 16; ++kk)  // +32 bytes per 16-column step
+          umma_f16(tmem_d, ad + 2 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
+        umma_commit(&sh->empty[stage]);
+      }
+      umma_commit(&sh->acc_full);  // fires once every issued MMA is done
     }
-    umma_commit(&sh->acc_full);  // fires once every issued MMA is done
-    }
-    __syncwarp();  // the other lanes of the MMA warp idle here instead of polling
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- epilogue
-  // (the MMA warp goes straight to the final barrier: the epilogue warps only
-  // pass it once acc_full says every MMA has completed)
   bool ok = true;
   if (warp < 8) ok = mbar_wait(&sh->acc_full, 0, abort);
-  if (warp < 8 && !ok) {
-    // wait (bounded) for the MMAs already in flight before freeing TMEM
-    mbar_drain(&sh->acc_full, 0);
-  }
+  if (warp < 8 && !ok) mbar_drain(&sh->acc_full, 0);  // MMAs in flight finish before TMEM is freed
   tc_fence_after();
   if (warp < 8 && ok && !*abort) {
-    const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int r = 32 * q + lane;         // row of the 128-row block
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int e = kTcM * mb + 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    if (MODE == 0) {
-      const int pair = 4 * mb + q, i = 16 * pair + (lane & 15);
-      const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
-      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
-        uint32_t v[32];
-        tmem_ld32(tmem_d + lane_addr + c0, v);
+    for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
+      uint32_t v[32];
+      tmem_ld32(tmem_d + lane_addr + c0, v);
 #pragma unroll
-        for (int qq = 0; qq < 32; ++qq) {
-          const float mine = __uint_as_float(v[qq]);
-          const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-          const int col = c0 + qq;
-          if (lane < 16 && col < n) {
-            const float G = ts_g * mine, U = ts_u * other;
-            const float a = G / (1.0f + expf(-G)) * U;
-            p.abuf[(size_t)(row0 + col) * p.I + i] = __half_as_ushort(__float2half_rn(a));
-          }
-        }
-      }
-    } else if (MODE == 2) {
-      const int e = kTcM * mb + r;
-      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
-        uint32_t v[32];
-        tmem_ld32(tmem_d + lane_addr + c0, v);
-#pragma unroll
-        for (int qq = 0; qq < 32; ++qq) {
-          const int col = c0 + qq;
-          if (col < n) p.logits_out[(size_t)(row0 + col) * p.E + e] = __uint_as_float(v[qq]);
-        }
-      }
-    } else {
-      const float ts = p.tscale[expert * 3 + 2];
-      const int h = kTcM * mb + r;
-      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
-        uint32_t v[32];
-        tmem_ld32(tmem_d + lane_addr + c0, v);
-#pragma unroll
-        for (int qq = 0; qq < 32; ++qq) {
-          const int col = c0 + qq;
-          if (col < n) p.ybuf[(size_t)(row0 + col) * p.H + h] = ts * __uint_as_float(v[qq]);
-        }
+      for (int qq = 0; qq < 32; ++qq) {
+        const int col = c0 + qq;
+        if (col < n) p.logits_out[(size_t)(row0 + col) * p.E + e] = __uint_as_float(v[qq]);
       }
     }
   }
@@ -392,8 +271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(ExpertParams p) 
 }
 
 size_t tc_smem() {
-  return 1024 + (size_t)kTcStages * (kTcAStageBytes + kTcBStageBytes + kTcRawStageBytes) +
-         sizeof(TcShared);
+  return 1024 + (size_t)kTcStages * (kTcAStageBytes + kTcBStageBytes) + sizeof(TcShared);
 }
 
 // ---------------------------------------------------------------- expert GEMMs with TMA-fed tiles
@@ -404,32 +282,33 @@ size_t tc_smem() {
 // 64-column K-chunk c:
 //   * one TMA load (warp 9) brings the code vectors of the group's 8G tiles
 //     (box {512 B, 1 piece, 8G tiles} of the arena's tile map, 4G KB) into a
-//     3-stage ring; once per super-chunk another brings their scale vectors
-//     into a 2-stage buffer.  The tile map views the packed layout as
+//     4-stage ring (the scale vectors, 1/8 of the bytes, each producer thread
+//     reads for its tiles straight into registers, a super-chunk ahead).  The
+//     tile map views the packed layout as
 //     [expert][tile][512-byte piece][512 B], so a box is 8G pieces at the same
 //     offset of consecutive tiles: one bulk copy instead of 8G small ones,
 //     and several chunks in flight per SM.
 //   * the 8 producer warps copy the chunk's token rows (B, gathered through
-//     the dispatch, 64 columns each) with cp.async two chunks ahead into a
-//     4-stage ring, and dequantise each M-block's codes into a 128B-swizzled
+//     the dispatch, 64 columns each) with cp.async three chunks ahead into a
+//     5-stage ring, and dequantise each M-block's codes into a 128B-swizzled
 //     f16 A slot (a 4-slot ring, one slot per M-block);
 //   * one thread issues, per M-block, 4 MMAs into that M-block's TMEM
 //     accumulator (G accumulators of N columns side by side) and commits the
 //     A slot back; after the last M-block it commits the B stage back.
 // A token chunk is read once for G M-blocks (G = 4 where the matrix has 4k
 // M-blocks), which cuts the L2 traffic of the token rows by G.
-constexpr int kTxNA = 4;             // A slots (16 KB each)
-constexpr int kTxNB = 4;             // B stages (up to 16 KB each)
+constexpr int kTxNA = 8;             // A slots (16 KB each): two chunks of a 4-M-block group
+constexpr int kTxNB = 3;             // B stages (up to 16 KB each)
 constexpr int kTxLB = 2;             // B chunks in flight ahead of the dequantisation
 constexpr int kTxNR = 3;             // code stages (4 KB per M-block)
-constexpr int kTxThreads = 320;      // warps 0-7 producers / epilogue, 8 MMA, 9 TMA
+constexpr int kTxPW = 16;            // producer (and epilogue) warps
+constexpr int kTxThreads = 32 * (kTxPW + 2);  // + warp 16: MMA issue, warp 17: TMA issue
 constexpr int kTxMaxG = 4;
 
 struct TxShared {
   uint64_t a_full[kTxNA], a_empty[kTxNA];
   uint64_t b_empty[kTxNB];
   uint64_t r_full[kTxNR], r_empty[kTxNR];
-  uint64_t s_full[2], s_empty[2];
   uint64_t acc_full;
   uint32_t tmem_base;
   int abort;
@@ -438,7 +317,7 @@ struct TxShared {
 
 __host__ __device__ constexpr size_t tx_smem_bytes(int G) {
   return 1024 + (size_t)kTxNA * kTcAStageBytes + (size_t)kTxNB * kTcBStageBytes +
-         (size_t)(kTxNR + 2) * 4096 * G + sizeof(TxShared);
+         (size_t)kTxNR * 4096 * G + sizeof(TxShared);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -476,8 +355,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   uint8_t* A = base;
   uint8_t* B = A + kTxNA * kTcAStageBytes;
   uint8_t* R = B + kTxNB * kTcBStageBytes;
-  uint8_t* SC = R + kTxNR * RB;
-  TxShared* sh = reinterpret_cast<TxShared*>(SC + 2 * RB);
+  TxShared* sh = reinterpret_cast<TxShared*>(R + kTxNR * RB);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.T * p.k;
   const int K = MODE == 1 ? p.I : p.H;
@@ -487,18 +365,16 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   const uint32_t ncols = (uint32_t)(G * npc);
 
   if (tid == 0) {
+    // producer warps arrive once each (lane 0, after a __syncwarp): 256
+    // single-thread arrivals on one barrier serialise on its shared word
     for (int i = 0; i < kTxNA; ++i) {
-      mbar_init(&sh->a_full[i], kTcProducers);
+      mbar_init(&sh->a_full[i], 8);  // the 8 warps of an M-block's half
       mbar_init(&sh->a_empty[i], 1);
     }
     for (int i = 0; i < kTxNB; ++i) mbar_init(&sh->b_empty[i], 1);
     for (int i = 0; i < kTxNR; ++i) {
       mbar_init(&sh->r_full[i], 1);
-      mbar_init(&sh->r_empty[i], kTcProducers);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh->s_full[i], 1);
-      mbar_init(&sh->s_empty[i], kTcProducers);
+      mbar_init(&sh->r_empty[i], kTxPW);
     }
     mbar_init(&sh->acc_full, 1);
     sh->abort = 0;
@@ -515,23 +391,26 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     const int r = n + rem / 8, c16 = rem % 8;
     *reinterpret_cast<uint4*>(B + st * b_stage + swz(r, c16)) = make_uint4(0, 0, 0, 0);
   }
-  if (warp == 8) tmem_alloc(&sh->tmem_base, ncols);
+  if (warp == kTxPW) tmem_alloc(&sh->tmem_base, ncols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_d = sh->tmem_base;
   volatile int* abort = &sh->abort;
-  const uint32_t a_s = smem_u32(A), b_s = smem_u32(B), r_s = smem_u32(R), sc_s = smem_u32(SC);
+  const uint32_t a_s = smem_u32(A), b_s = smem_u32(B), r_s = smem_u32(R);
 
-  if (warp < 8) {
+  if (warp < kTxPW) {
     // ---------------------------------------------------------------- producers
-    // thread u: tile u/32 of every M-block of the group, lane u%32 of it
-    const int u = tid, ti = u >> 5, ln = u & 31, gi = ln >> 2, t = ln & 3;
+    // warp pw: tile pw%8 of the M-blocks m = pw/8, pw/8 + 2 (of the group's G),
+    // lane ln of that tile's 16-byte vectors; the warps of half 0 also copy the
+    // token rows (so that their a_full arrivals for M-block 0 publish them)
+    const int half = warp >> 3, ti = warp & 7, ln = lane, gi = ln >> 2, t = ln & 3;
     const uint16_t* bsrc = (MODE == 0) ? p.xh : p.abuf;
     const int bld = (MODE == 0) ? p.H : p.I;
     auto issue_b = [&](int c) {  // chunk c's token rows into B stage c % kTxNB
+      if (half != 0) return;
       const uint32_t bs = b_s + (c % kTxNB) * b_stage;
-      for (int v = tid; v < n * 8; v += kTcProducers) {
+      for (int v = tid; v < n * 8; v += 256) {
         const int r = v >> 3, c16 = v & 7;
         cp_async16(bs + swz(r, c16), bsrc + (size_t)sh->tok[r] * bld + c * kTcK + 8 * c16);
       }
@@ -540,39 +419,58 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       if (c < KC) issue_b(c);
       cp_async_commit();
     }
-    uint4 sv[kTxMaxG];
+    // my tiles' scale vectors, a super-chunk ahead
+    const MatGeom g = mat_geom(FMT_NVFP4, K);
+    const uint8_t* tiles = p.arena + (size_t)expert * p.expert_bytes + (MODE == 1 ? p.gu_bytes : 0);
+    const size_t tb = MODE == 1 ? (size_t)p.dn_tile_bytes : (size_t)p.gu_tile_bytes;
+    const uint8_t* mine = tiles + (size_t)(tile0 + ti) * tb + 16 * ln;
+    uint4 sv[2], sv_next[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int m = half + 2 * i;
+      if (m < G) sv[i] = sv_next[i] = ldg_stream(mine + (size_t)m * 8 * tb);
+    }
     for (int c = 0; c < KC; ++c) {
       const int s = c >> 3, j = c & 7;
-      if (j == 0) {  // the super-chunk's scale vectors of my tiles
-        if (!mbar_wait(&sh->s_full[s & 1], (s >> 1) & 1, abort)) break;
+      if (j == 0 && c > 0) {
 #pragma unroll
-        for (int m = 0; m < kTxMaxG; ++m)
-          if (m < G) sv[m] = lds128(sc_s + (s & 1) * RB + (m * 8 + ti) * 512 + 16 * ln);
-        mbar_arrive(&sh->s_empty[s & 1]);
+        for (int i = 0; i < 2; ++i) sv[i] = sv_next[i];
       }
-      if (!mbar_wait(&sh->r_full[c % kTxNR], (c / kTxNR) & 1, abort)) break;
-      uint4 cv[kTxMaxG];
+      if (j == 4 && s + 1 < g.nsc) {
 #pragma unroll
-      for (int m = 0; m < kTxMaxG; ++m)
-        if (m < G) cv[m] = lds128(r_s + (c % kTxNR) * RB + (m * 8 + ti) * 512 + 16 * ln);
-      mbar_arrive(&sh->r_empty[c % kTxNR]);
+        for (int i = 0; i < 2; ++i) {
+          const int m = half + 2 * i;
+          if (m < G) sv_next[i] = ldg_stream(mine + (size_t)m * 8 * tb + (size_t)(s + 1) * g.sc_bytes);
+        }
+      }
+      // (waits are made warp-uniform: the warps arrive with one lane after a __syncwarp)
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->r_full[c % kTxNR], (c / kTxNR) & 1, abort))) break;
+      uint4 cv[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int m = half + 2 * i;
+        if (m < G) cv[i] = lds128(r_s + (c % kTxNR) * RB + (m * 8 + ti) * 512 + 16 * ln);
+      }
+      __syncwarp();
+      if (ln == 0) mbar_arrive(&sh->r_empty[c % kTxNR]);
       cp_async_wait<kTxLB - 1>();  // this thread's token-row pieces of chunk c have landed
       bool ok = true;
 #pragma unroll
-      for (int m = 0; m < kTxMaxG; ++m) {
+      for (int i = 0; i < 2; ++i) {
+        const int m = half + 2 * i;
         if (m >= G) break;
         const int q = c * G + m, slot = q % kTxNA;
-        if (!mbar_wait(&sh->a_empty[slot], ((q / kTxNA) & 1) ^ 1, abort)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->a_empty[slot], ((q / kTxNA) & 1) ^ 1, abort))) {
           ok = false;
           break;
         }
-        const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[m], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
+        const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], j >> 1) >> (16 * (j & 1))) & 0xFFFFu);
         const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
         uint32_t r0[8], r1[8];  // rows gi and gi+8 of tile ti: 16 f16 each
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           uint32_t hh[4];
-          e2m1x8_to_f16x8(u4get(cv[m], w), hh);
+          e2m1x8_to_f16x8(u4get(cv[i], w), hh);
           r0[2 * w] = hmul2(hh[0], s_lo);
           r0[2 * w + 1] = hmul2(hh[2], s_lo);
           r1[2 * w] = hmul2(hh[1], s_hi);
@@ -584,20 +482,22 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         st_shared_v4(as + swz(ra, 2 * t + 1), r0[4], r0[5], r0[6], r0[7]);
         st_shared_v4(as + swz(rb, 2 * t), r1[0], r1[1], r1[2], r1[3]);
         st_shared_v4(as + swz(rb, 2 * t + 1), r1[4], r1[5], r1[6], r1[7]);
-        fence_async_smem();  // (also publishes the token rows of chunk c to the MMA)
-        mbar_arrive(&sh->a_full[slot]);
+        fence_async_smem();  // (for half 0 also publishes the token rows of chunk c)
+        __syncwarp();
+        if (ln == 0) mbar_arrive(&sh->a_full[slot]);
       }
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, ok)) break;
       // refill: chunk c + kTxLB goes to the B stage the MMAs of chunk c + kTxLB - kTxNB freed
       const int cn = c + kTxLB;
-      if (cn < KC) {
-        if (!mbar_wait(&sh->b_empty[cn % kTxNB], ((cn / kTxNB) & 1) ^ 1, abort)) break;
+      if (cn < KC && half == 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->b_empty[cn % kTxNB], ((cn / kTxNB) & 1) ^ 1, abort)))
+          break;
         issue_b(cn);
       }
       cp_async_commit();
     }
     cp_async_wait<0>();
-  } else if (warp == 8) {
+  } else if (warp == kTxPW) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issue
       const uint32_t idesc = idesc_f16(kTcM, n_pad);
@@ -606,7 +506,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         const uint64_t bd = sw128_desc(b_s + (c % kTxNB) * b_stage);
         for (int m = 0; m < G; ++m) {
           const int q = c * G + m, slot = q % kTxNA;
-          if (!mbar_wait(&sh->a_full[slot], (q / kTxNA) & 1, abort)) {
+          if (!mbar_wait_sleep(&sh->a_full[slot], (q / kTxNA) & 1, abort)) {
             ok = false;
             break;
           }
@@ -629,12 +529,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       int issued = 0;  // code chunks issued
       for (int c = 0; c < KC; ++c) {
         const int s = c >> 3, j = c & 7;
-        if (j == 0) {
-          if (!mbar_wait(&sh->s_empty[s & 1], ((s >> 1) & 1) ^ 1, abort)) break;
-          mbar_arrive_expect(&sh->s_full[s & 1], (uint32_t)RB);
-          tma_load_tiles(sc_s + (s & 1) * RB, map, 9 * s, tile0, expert, &sh->s_full[s & 1]);
-        }
-        if (!mbar_wait(&sh->r_empty[c % kTxNR], ((c / kTxNR) & 1) ^ 1, abort)) break;
+        if (!mbar_wait_sleep(&sh->r_empty[c % kTxNR], ((c / kTxNR) & 1) ^ 1, abort)) break;
         mbar_arrive_expect(&sh->r_full[c % kTxNR], (uint32_t)RB);
         tma_load_tiles(r_s + (c % kTxNR) * RB, map, 9 * s + 1 + j, tile0, expert,
                        &sh->r_full[c % kTxNR]);
@@ -643,8 +538,6 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       if (*abort) {  // let the copies in flight land before the CTA exits (bounded waits)
         for (int c = (issued > kTxNR ? issued - kTxNR : 0); c < issued; ++c)
           mbar_drain(&sh->r_full[c % kTxNR], (c / kTxNR) & 1);
-        const int ns = issued > 0 ? ((issued - 1) >> 3) + 1 : 0;
-        for (int s = (ns > 2 ? ns - 2 : 0); s < ns; ++s) mbar_drain(&sh->s_full[s & 1], (s >> 1) & 1);
       }
     }
     __syncwarp();
@@ -652,10 +545,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 
   // ---------------------------------------------------------------- epilogue
   bool ok = true;
-  if (warp < 8) ok = mbar_wait(&sh->acc_full, 0, abort);
-  if (warp < 8 && !ok) mbar_drain(&sh->acc_full, 0);  // MMAs in flight finish before TMEM is freed
+  if (warp < kTxPW) ok = mbar_wait_sleep(&sh->acc_full, 0, abort);
+  if (warp < kTxPW && !ok) mbar_drain(&sh->acc_full, 0);  // MMAs in flight finish before TMEM is freed
   tc_fence_after();
-  if (warp < 8 && ok && !*abort) {
+  if (warp < kTxPW && ok && !*abort) {
     const int qd = warp & 3;             // TMEM lane quadrant of this warp
     const int r = 32 * qd + lane;        // row of the 128-row block
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
@@ -665,7 +558,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       if (MODE == 0) {
         const int pair = 4 * mb + qd, i = 16 * pair + (lane & 15);
         const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
-        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
+        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 32 * (kTxPW / 4)) {
           uint32_t v[32];
           tmem_ld32(acc + c0, v);
 #pragma unroll
@@ -683,7 +576,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       } else {
         const float ts = p.tscale[expert * 3 + 2];
         const int h = kTcM * mb + r;
-        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 64) {
+        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 32 * (kTxPW / 4)) {
           uint32_t v[32];
           tmem_ld32(acc + c0, v);
 #pragma unroll
@@ -698,7 +591,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   if (*abort && tid == 0) *p.status = -5;  // MOE_ETIMEOUT
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kTxPW) {
     tc_fence_after();
     tmem_dealloc(tmem_d, ncols);
   }
@@ -767,7 +660,7 @@ bool tc_router_ok(int E, int H) { return E % kTcM == 0 && H % kTcK == 0; }
 // logits_out gets the fp32 dot products (one K slice: the top-k step adds the bias)
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st) {
   dim3 grid(p.E / kTcM, (p.T + kTcMaxN - 1) / kTcMaxN);
-  return launch_k(tc_gemm_kernel<2>, grid, dim3(kTcThreads), tc_smem(), st, true, p);
+  return launch_k(tc_router_kernel, grid, dim3(kTcThreads), tc_smem(), st, true, p);
 }
 
 cudaError_t tc_kernels_init() {
@@ -777,7 +670,7 @@ cudaError_t tc_kernels_init() {
   e = cudaFuncSetAttribute(tc_expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tx_smem_bytes(kTxMaxG));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tc_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tc_smem());
 }
 

@@ -203,6 +203,10 @@ int check_forward_args(moe_layer* L, const void* x, int T, const void* out) {
 }
 
 // experts + combine, after routing has filled idx / gates / dispatch
+// Top-k inside the one-CTA dispatch kernel up to this many tokens (one warp
+// each, no extra launch); more tokens take the top-k kernel (8 tokens per CTA)
+constexpr int kFusedTopkMaxT = 16;
+
 bool fused_down(moe_layer* L, int T) { return down_combine_ok(T, L->k, L->shared, L->I); }
 
 bool tc_path(moe_layer* L, int T) {
@@ -248,7 +252,7 @@ bool small_path(moe_layer* L, int T) { return small_route_ok(T, L->k) && fused_d
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
   if (small_path(L, T)) return 3;
-  const int routing = tc_router(L, T) ? 4 : (T <= 64 ? 2 : 3);
+  const int routing = tc_router(L, T) ? 4 : (T <= kFusedTopkMaxT ? 2 : 3);
   if (tc_path(L, T)) return routing + 3;
   return routing + (fused_down(L, T) ? 2 : 3);
 }
@@ -270,7 +274,7 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
     if (rc) return rc;
     CK("top-k kernel launch", launch_topk(rp, true, st));
     CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
-  } else if (T <= 64) {
+  } else if (T <= kFusedTopkMaxT) {
     CK("router kernel launch", launch_router(rp, st));
     CK("top-k/dispatch kernel launch", launch_route_finish(rp, true, true, st));
   } else {
@@ -686,7 +690,7 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       }
       break;
     case 1:
-      if (T <= 64 && !tc_router(L, T)) {
+      if (T <= kFusedTopkMaxT && !tc_router(L, T)) {
         CK("top-k/dispatch", launch_route_finish(rp, true, false, st));
       } else {
         CK("top-k", launch_topk(rp, false, st));

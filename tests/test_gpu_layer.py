@@ -51,8 +51,9 @@ def test_tiny_workload():
 @pytest.mark.parametrize("fmt", [1, 2, 3])
 @pytest.mark.parametrize("T", [1, 5, 13, 64, 70, 200])
 def test_small_layers_ragged_token_counts(fmt, T):
-    """Several tiles, ragged last entries, both routing paths (T <= 64 fused,
-    T > 64 separate top-k), both formats, with a shared expert."""
+    """Several tiles, ragged last entries, the routing paths (T = 1 in-CTA,
+    T <= 16 top-k inside the dispatch kernel, larger T a separate top-k
+    kernel), all formats, with a shared expert."""
     w = small(fmt=fmt, H=384 if fmt == 2 else 320, I=256 if fmt == 2 else 192, E=24, k=3, T=T)
     compare_layer(w, layer(w), gen.x_tokens(w, T))
 

@@ -76,6 +76,7 @@ def lib():
                 "orc_dequant_fp6": (I, [P, P, I, I, P]),
                 "orc_router_logits": (I, [P, P, I, P]),
                 "orc_topk_gates": (I, [P, I, I, I, P, P]),
+                "orc_topk_gates_sigmoid": (I, [P, P, I, I, I, P, P]),
                 "orc_dispatch": (I, [P, I, I, I, P, P, P]),
                 "orc_combine": (I, [P, P, I, P, P, P, I]),
                 "orc_moe_forward": (I, [P, P, I, P, P, P, P, I]),
@@ -289,6 +290,19 @@ class Layer:
         st, keep = self._struct()
         _check(lib().orc_expert_ffn(ctypes.byref(st), expert, _p(x), T, _p(out)), "expert_ffn")
         return out
+
+
+def topk_gates_sigmoid(logits: np.ndarray, bias, k: int):
+    """The sigmoid router (R19): logits [T x E] without the bias, bias [E] or
+    None; returns (idx [T x k], gates [T x k])."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    idx = np.empty((T, k), np.int32)
+    gates = np.empty((T, k), np.float32)
+    _check(lib().orc_topk_gates_sigmoid(_p(lg), None if b is None else _p(b), T, E, k, _p(idx),
+                                        _p(gates)), "topk sigmoid")
+    return idx, gates
 
 
 def dispatch(idx: np.ndarray, E: int):

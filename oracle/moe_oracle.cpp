@@ -38,6 +38,8 @@
 //   R9 dispatch order: expert-major, then token, then rank j (stable).
 //   R10 shared expert: always on, weight 1, same format and I as the routed.
 //   R11 output = fp32(sum_j g_j * y_j + y_shared), summed in fp64.
+//   R19 optional sigmoid router: s_e = sigmoid(x . Wr_e), top-k by s_e + b_e (the
+//      bias selects only), gates s_j / sum of the picked s.
 //   R17 MXFP4 (OCP MX v1.0 FP4): blocks of 32 along K share an e8m0 scale
 //      X = 2^(floor(log2 amax_b) - 2) (2 = the largest e2m1 exponent), clamped
 //      to [2^-127, 2^127]; q = e2m1_rne(w / X), saturating at 6; an all-zero
@@ -376,6 +378,33 @@ int orc_topk_gates(const float* logits, int T, int E, int k, int32_t* idx, float
     for (int j = 0; j < k; ++j) {
       idx[(long)t * k + j] = order[j];
       gates[(long)t * k + j] = (float)(p[order[j]] / s);
+    }
+  }
+  return 0;
+}
+
+// R19: the sigmoid router with a selection bias.  logits are x . Wr_e without
+// the bias; s_e = 1 / (1 + exp(-l_e)); the k experts with the largest
+// s_e + b_e (ties -> lower index) are picked, the bias deciding the
+// selection only; g_j = s_j / (sum of the picked s), in fp64, rounded to fp32.
+int orc_topk_gates_sigmoid(const float* logits, const float* bias, int T, int E, int k,
+                           int32_t* idx, float* gates) {
+  if (k < 1 || k > E) return -1;
+  std::vector<double> s((size_t)E), key((size_t)E);
+  std::vector<int> order((size_t)E);
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (long)t * E;
+    for (int e = 0; e < E; ++e) {
+      s[e] = 1.0 / (1.0 + std::exp(-(double)l[e]));
+      key[e] = s[e] + (bias ? (double)bias[e] : 0.0);
+      order[e] = e;
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return key[a] > key[b]; });
+    double z = 0.0;
+    for (int j = 0; j < k; ++j) z += s[order[j]];
+    for (int j = 0; j < k; ++j) {
+      idx[(long)t * k + j] = order[j];
+      gates[(long)t * k + j] = (float)(s[order[j]] / z);
     }
   }
   return 0;

@@ -168,3 +168,40 @@ def test_workload_inputs_are_seeded_and_shaped():
     assert np.array_equal(gen.x_tokens(w, T=2, first=2), x1[2:4])
     zb = gen.router_bias(gen.get_workload(1))
     assert sorted(zb)[-1] == np.float32(0.5) and np.all(zb > 0)
+
+
+# ---------------------------------------------------------------- sigmoid router (R19)
+def test_sigmoid_router_selection_and_gates_against_numpy():
+    rng = np.random.default_rng(21)
+    T, E, k = 7, 40, 6
+    lg = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+    b = (rng.standard_normal(E) * 0.3).astype(np.float32)
+    idx, gates = oracle.topk_gates_sigmoid(lg, b, k)
+    s = 1.0 / (1.0 + np.exp(-lg.astype(np.float64)))
+    key = s + b.astype(np.float64)
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -key[t]))[:k]  # key descending, ties to the lower index
+        assert np.array_equal(idx[t], order)
+        g = s[t, order] / s[t, order].sum()
+        assert np.allclose(gates[t], g, rtol=1e-6, atol=0)
+        assert abs(float(gates[t].sum()) - 1.0) < 1e-6
+
+
+def test_sigmoid_router_without_bias_picks_like_the_softmax_router():
+    # sigmoid is increasing, so with b = 0 the picks are the top-k logits
+    rng = np.random.default_rng(22)
+    lg = rng.standard_normal((5, 64)).astype(np.float32)
+    lg[2, 10] = lg[2, 20]  # an exact tie: the lower index first
+    idx_s, _ = oracle.topk_gates_sigmoid(lg, None, 8)
+    L = oracle.Layer(oracle.FMT_NVFP4, 64, 64, 64, 8, 0, np.zeros((64, 64), np.uint16))
+    idx_m, _ = L.topk(lg)
+    assert np.array_equal(idx_s, idx_m)
+
+
+def test_sigmoid_router_bias_selects_but_does_not_weight():
+    lg = np.array([[3.0, 2.0, -4.0, 1.0]], np.float32)
+    b = np.array([0.0, 0.0, 2.0, 0.0], np.float32)  # lifts expert 2 into the top 2
+    idx, gates = oracle.topk_gates_sigmoid(lg, b, 2)
+    assert list(idx[0]) == [2, 0]
+    s0, s2 = 1 / (1 + np.exp(-3.0)), 1 / (1 + np.exp(4.0))
+    assert np.allclose(gates[0], [s2 / (s0 + s2), s0 / (s0 + s2)], rtol=1e-6)

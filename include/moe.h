@@ -92,6 +92,17 @@ int moe_layer_info(moe_layer* L, uint64_t* arena_bytes, uint64_t* expert_bytes);
  * [E] (NULL = none), host or device memory per `where`.  Copied; synchronous. */
 int moe_set_router(moe_layer* L, const uint16_t* wr_bf16, const float* bias, int where);
 
+/* Router mode (default MOE_ROUTER_SOFTMAX):
+ *   MOE_ROUTER_SOFTMAX: logit = x . Wr_e + bias_e; the k largest logits (ties
+ *     to the lower expert index); gates = softmax over the k selected logits.
+ *   MOE_ROUTER_SIGMOID: score s_e = sigmoid(x . Wr_e); the k largest s_e +
+ *     bias_e are selected (the bias decides the selection only); gates =
+ *     s_j / (sum of the selected s).  The logits reported by
+ *     moe_debug_routing are then x . Wr_e without the bias.
+ * Applies to the following forwards.  MOE_EINVAL for an unknown mode. */
+enum moe_router_mode { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 };
+int moe_set_router_mode(moe_layer* L, int mode);
+
 /* Pack one expert matrix from the canonical quantised format into the layer's
  * device layout.  expert in [0, E) for routed experts, E for the shared one;
  * matrix: moe_matrix (gate and up are [I x H], down is [H x I]; row-major,

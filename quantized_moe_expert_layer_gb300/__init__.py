@@ -27,6 +27,7 @@ FMT_NVFP4 = 1
 FMT_FP6 = 2
 FMT_MXFP4 = 3
 GATE, UP, DOWN = 0, 1, 2
+ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 HOST, DEVICE = 0, 1
 
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT = 0, -1, -2, -3, -4, -5
@@ -35,7 +36,7 @@ OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT = 0, -1, -2, -3, -4, -5
 EXPORTS = [
     "moe_layer_create", "moe_layer_reserve", "moe_layer_destroy", "moe_last_error",
     "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
-    "moe_pack_weights", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_quantize_mxfp4", "moe_forward",
+    "moe_pack_weights", "moe_set_router_mode", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_quantize_mxfp4", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
     "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches"
 ]
@@ -107,6 +108,7 @@ def lib():
                 "moe_quantize_nvfp4": (I, [P, I, I, P, P, P, P]),
                 "moe_quantize_fp6": (I, [P, I, I, P, P, P]),
                 "moe_quantize_mxfp4": (I, [P, I, I, P, P, P]),
+                "moe_set_router_mode": (I, [P, I]),
                 "moe_forward": (I, [P, P, I, P, P]),
                 "moe_forward_host": (I, [P, P, I, P, P]),
                 "moe_forward_routed": (I, [P, P, I, P, P, P, P]),
@@ -189,6 +191,10 @@ class MoeLayer:
     def set_router(self, wr, bias=None, where=None):
         where = _where(wr) if where is None else where
         check(lib().moe_set_router(self.h, _ptr(wr), _ptr(bias), where))
+
+    def set_router_mode(self, mode):
+        """ROUTER_SOFTMAX (default) or ROUTER_SIGMOID (selection-only bias)."""
+        check(lib().moe_set_router_mode(self.h, mode))
 
     def pack_matrix(self, expert, matrix, codes, scales, tscale=None, stream=None):
         """codes/scales (+ tscale) as torch device tensors or numpy host arrays."""

@@ -38,12 +38,17 @@ struct ExpertParams {
   int* status;
 };
 
+// Router modes: softmax over the logits (the bias is part of the logit), or
+// sigmoid scores with the bias deciding the selection only.
+enum { ROUTER_SOFTMAX = 0, ROUTER_SIGMOID = 1 };
+
 struct RouteParams {
   const uint16_t* x;      // bf16 [T x H]
   uint16_t* xh;           // f16 copy of x, written by the router (may be null)
   const uint16_t* wr;     // bf16 [E x H]
   const float* bias;      // [E] or null
   int T, H, E, k, shared, ksplit;
+  int mode;               // ROUTER_SOFTMAX or ROUTER_SIGMOID
   float* partial;         // [ksplit x T x E] router partial dot products
   float* logits;          // [T x E]
   int* idx;               // [T x k]

@@ -95,6 +95,7 @@ struct moe_layer {
   float* bias = nullptr;
   bool has_bias = false;
   bool router_set = false;
+  int router_mode = ROUTER_SOFTMAX;
   int* status = nullptr;
   // workspace
   int T_max = 0;
@@ -125,6 +126,7 @@ namespace {
 
 RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   RouteParams p{};
+  p.mode = L->router_mode;
   p.x = x;
   p.wr = L->router;
   p.bias = L->has_bias ? L->bias : nullptr;
@@ -467,6 +469,14 @@ int moe_set_router(moe_layer* L, const uint16_t* wr_bf16, const float* bias, int
   L->has_bias = bias != nullptr;
   if (bias) CK("moe_set_router: copy bias", cudaMemcpy(L->bias, bias, sizeof(float) * L->E, kind));
   L->router_set = true;
+  return MOE_OK;
+}
+
+int moe_set_router_mode(moe_layer* L, int mode) {
+  if (!L) return fail(MOE_EINVAL, "moe_set_router_mode: null layer");
+  if (mode != MOE_ROUTER_SOFTMAX && mode != MOE_ROUTER_SIGMOID)
+    return fail(MOE_EINVAL, "moe_set_router_mode: unknown mode %d", mode);
+  L->router_mode = mode == MOE_ROUTER_SIGMOID ? ROUTER_SIGMOID : ROUTER_SOFTMAX;
   return MOE_OK;
 }
 

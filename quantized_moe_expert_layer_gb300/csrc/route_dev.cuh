@@ -115,6 +115,9 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
 }
 
 // ---------------------------------------------------------------- top-k (one warp per token)
+// The sigmoid router's score of a logit (fp32).
+__device__ __forceinline__ float sigmoid_score(float l) { return 1.0f / (1.0f + expf(-l)); }
+
 // Order-preserving map of an fp32 value to a uint32 key (larger value, larger key).
 __device__ __forceinline__ uint32_t f32_key(float v) {
   const uint32_t u = __float_as_uint(v);
@@ -181,23 +184,41 @@ __device__ __forceinline__ void load_logits(const RouteParams& p, int t, int e0,
     id[i] = e;
     if (e < e_end) {
       float l = v[i];
-      if (p.bias) l = l + p.bias[e];
-      if (pub && p.logits) p.logits[(size_t)t * p.E + e] = l;
-      key[i] = f32_key(l);
+      if (p.mode == ROUTER_SIGMOID) {  // score sigmoid(l); the bias moves the selection only
+        if (pub && p.logits) p.logits[(size_t)t * p.E + e] = l;
+        const float s = sigmoid_score(l);
+        key[i] = f32_key(p.bias ? s + p.bias[e] : s);
+      } else {
+        if (p.bias) l = l + p.bias[e];
+        if (pub && p.logits) p.logits[(size_t)t * p.E + e] = l;
+        key[i] = f32_key(l);
+      }
     } else {
       key[i] = 0u;  // below every real key
     }
   }
 }
 
-// Gates = softmax of the k selected logits (lane j < k holds pick j).
+// Gates (lane j < k holds pick j): the softmax of the k selected logits, or
+// for the sigmoid router the selected scores renormalised (each score
+// recomputed from the router's K slices, in the order the selection used).
 __device__ __forceinline__ void write_gates(const RouteParams& p, int t, int lane, uint32_t my_key,
                                             int my_i, int* sidx, float* sgates = nullptr,
                                             bool pub = true) {
   const int k = p.k;
-  const float my_v = key_f32(my_key);
-  const float top = __shfl_sync(0xffffffffu, my_v, 0);
-  float ex = (lane < k) ? expf(my_v - top) : 0.f;
+  float ex;
+  if (p.mode == ROUTER_SIGMOID) {
+    ex = 0.f;
+    if (lane < k) {
+      float l = 0.f;
+      for (int s = 0; s < p.ksplit; ++s) l += __ldcg(p.partial + ((size_t)s * p.T + t) * p.E + my_i);
+      ex = sigmoid_score(l);
+    }
+  } else {
+    const float my_v = key_f32(my_key);
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    ex = (lane < k) ? expf(my_v - top) : 0.f;
+  }
   float sum = ex;
 #pragma unroll
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);

@@ -275,3 +275,39 @@ def test_single_token_topk_exact_ties(case):
         np.testing.assert_allclose(a["gates"], gates, rtol=1e-6, atol=0)
     finally:
         L.set_router(gen.router_weights(w), gen.router_bias(w))
+
+
+# ---------------------------------------------------------------- sigmoid router with selection bias
+@pytest.mark.parametrize("T", [1, 5, 13, 64, 200, 1100])
+def test_sigmoid_router_layer(T):
+    """The sigmoid router (scores sigmoid(x . Wr_e), top-k by score + bias,
+    gates = the picked scores renormalised) on every routing path: T = 1 in
+    the gate/up CTAs, T <= 16 in the dispatch kernel, the top-k kernel, and
+    the tensor-core router (T = 1100, 128 experts)."""
+    E = 128 if T == 1100 else 64
+    w = small(fmt=1, H=256, I=128, E=E, k=6, shared=1, T=T, seed=13)
+    L = build_layer(w, T_max=T)
+    try:
+        L.set_router_mode(moe.ROUTER_SIGMOID)
+        x_np = gen.x_tokens(w, T)
+        g = run_gpu(L, x_np, w)
+        router, bias = gen.router_weights(w), gen.router_bias(w)
+        base = oracle.Layer(w.fmt, w.H, w.I, w.E, w.k, w.shared, router, None)
+        lg = base.logits(x_np)  # without the bias
+        assert np.allclose(g["logits"], lg, rtol=1e-5, atol=1e-5)
+        idx_o, gates_o = oracle.topk_gates_sigmoid(lg, bias, w.k)
+        # near ties of score + bias may pick either expert: compare the rest exactly
+        s = 1.0 / (1.0 + np.exp(-lg.astype(np.float64)))
+        key = s + bias.astype(np.float64)
+        for t in range(T):
+            if not np.array_equal(g["idx"][t], idx_o[t]):
+                kk = np.sort(key[t])[::-1]
+                assert kk[w.k - 1] - kk[w.k] < 1e-5, f"token {t}: {g['idx'][t]} vs {idx_o[t]}"
+            else:
+                assert np.allclose(g["gates"][t], gates_o[t], rtol=0, atol=2e-6)
+        ol = oracle.layer_for_workload(w, sorted(set(g["idx"].ravel().tolist()) | {w.E}))
+        ref = ol.combine(x_np, g["idx"], g["gates"])
+        rel = np.linalg.norm(g["out"] - ref, axis=1) / np.linalg.norm(ref, axis=1)
+        assert np.all(rel <= 2e-3), rel.max()
+    finally:
+        L.close()

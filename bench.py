@@ -53,6 +53,9 @@ def parse():
                     help="workload index (default: the decode workload the metric is quoted on)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--host-mirror", type=float, default=0.0,
+                    help="fraction of each layer's experts placed in the pinned host mirror "
+                         "(the coldest by router bias; the kernels read them over the CPU-GPU link)")
     return ap.parse_args()
 
 
@@ -108,6 +111,46 @@ FORMAT_NAMES = {1: "nvfp4 (e2m1, e4m3 per 16, fp32 tensor scale)",
                 2: "fp6 e2m3 (power-of-two scale per 128)",
                 3: "mxfp4 (e2m1, power-of-two scale per 32)"}
 SHORT_NAMES = {1: "nvfp4", 2: "fp6 e2m3", 3: "mxfp4"}
+
+
+def placement_mask(w, frac, seed):
+    """HBM flags per expert (routed, then shared) with round(frac * n) experts in
+    the host mirror: the coldest first by router bias (the routing-heat proxy a
+    fresh layer has), ties by index; the always-used shared expert last."""
+    import dataclasses
+
+    import numpy as np
+
+    import gen
+    n = w.n_experts_total
+    n_host = int(round(frac * n))
+    if n_host <= 0:
+        return None
+    b = gen.router_bias(dataclasses.replace(w, seed=seed))
+    heat = np.zeros(w.E) if b is None else b.astype(np.float64)
+    order = list(np.argsort(heat, kind="stable")) + ([w.E] if w.shared else [])
+    mask = np.ones(n, bool)
+    mask[order[:n_host]] = False
+    return mask
+
+
+def link_peak_gbs(stream):
+    """Host -> device bandwidth of the CPU-GPU link, measured here: a copy of a
+    256 MiB pinned host buffer, best of 10 (CUDA events)."""
+    import torch
+    src = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    best = None
+    with torch.cuda.stream(stream):
+        for _ in range(12):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+    return src.numel() / (best * 1e-3) / 1e9
 
 
 def config_block(w, L, extra=None):
@@ -258,24 +301,35 @@ def run_reference(args, w):
 
 def traffic_from_profile(kernel, workload, csrc):
     """dram bytes per launch of `kernel` on `workload` from its committed ncu
-    summary, or None when any kernel source changed since the capture (the
-    summary records a hash of csrc/*)."""
+    summary, or None when the kernel's sources changed since the capture (the
+    summary records the translation unit that defines the kernel and a hash of
+    it and every header it includes)."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         txt = open(p).read()
         sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt).group(1)
+        unit = re.search(r"source_unit:\s*(\S+)", txt).group(1)
         b = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt).group(1))
     except Exception:
         return None
-    return b if sources_sha256(csrc) == sha else None
+    return b if sources_sha256(csrc, unit) == sha else None
 
 
-def sources_sha256(csrc):
+def sources_sha256(csrc, unit):
+    """Hash of the translation unit `unit` and the local headers it includes,
+    followed recursively, in sorted file-name order."""
+    seen, todo = set(), [unit]
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.add(f)
+        txt = open(os.path.join(csrc, f)).read()
+        todo += re.findall(r'^#include "([^"/]+)"', txt, re.M)
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in sorted(seen):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
 
@@ -297,7 +351,8 @@ def run_ours(args, w):
     moe.build()
     Ln = args.layers
     T = w.T
-    layers = [build_layer(w, T_max=T, seed=1000 * rank + i) for i in range(Ln)]
+    masks = [placement_mask(w, args.host_mirror, 1000 * rank + i) for i in range(Ln)]
+    layers = [build_layer(w, T_max=T, seed=1000 * rank + i, in_hbm=masks[i]) for i in range(Ln)]
     x_np = gen.x_tokens(w, T, first=rank * T)
     x = torch.from_numpy(x_np.view(np.int16)).cuda()
     outs = [torch.empty((T, w.H), dtype=torch.float32, device="cuda") for _ in range(Ln)]
@@ -365,17 +420,21 @@ def run_ours(args, w):
     tc = tc_path(w, T)
     gu = packed_gateup_bytes(w)
     per_launch = []
+    host_per_launch = []
     # for T <= 8 (NVFP4) gate/up also asks L2 for the touched experts' down
     # matrices, which the down kernel then reads from L2
     prefetch_down = T <= 8 and w.fmt in (1, 3)
     dn = packed_down_bytes(w)
     with torch.cuda.stream(s):
-        for L, o in zip(layers, outs):
+        for L, o, m in zip(layers, outs, masks):
             L.forward(x, o, stream=s)
             L.debug_routing(counts=counts, stream=s)
             s.synchronize()
             c = counts.cpu().numpy()
             D = int((c > 0).sum()) + w.shared
+            if m is not None:  # weight bytes of the touched experts in the host mirror
+                used = np.concatenate([c > 0, [True] * w.shared])
+                host_per_launch.append(int((used & ~m).sum()) * (gu + (dn if prefetch_down else 0)))
             if tc:  # FLOPs of the contraction (N padded to 16 per work item as the MMA runs it)
                 n = [int(v) for v in c if v > 0] + [T] * w.shared
                 cols = sum(((min(128, v - 128 * j) + 15) // 16) * 16
@@ -414,8 +473,18 @@ def run_ours(args, w):
         roofline = {"bound": "hbm", "kernel": kname + " (gate/up + SwiGLU)", "achieved": achieved,
                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "algorithmic_bytes_per_launch": work}
-    roofline.update({"traffic": traffic_from_profile(kname, w.name, os.path.join(
-                         ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
+    if host_per_launch:  # the CPU-GPU link bounds the mirrored experts' share
+        hb = sum(host_per_launch) / len(host_per_launch)
+        lp = link_peak_gbs(s)
+        achieved = hb / (k_us * 1e-6) / 1e9
+        roofline = {"bound": "link", "kernel": kname + " (gate/up + SwiGLU)", "achieved": achieved,
+                    "peak": lp, "unit": "GB/s", "frac": achieved / lp,
+                    "algorithmic_bytes_per_launch": hb,
+                    "hbm_bytes_per_launch": work - hb,
+                    "note": "bytes read from the pinned host mirror over the CPU-GPU link"}
+        peak_kind = "measured here: 256 MiB pinned host -> device copy, best of 10"
+    roofline.update({"traffic": None if host_per_launch else traffic_from_profile(
+                         kname, w.name, os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
                      "avg_launch_us": k_us, "peak_source": peak_kind,
                      "timing": "CUDA events over a graph of back-to-back launches, gaps included"})
 
@@ -463,6 +532,7 @@ def run_ours(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (" + SHORT_NAMES[w.fmt] + " weights)",
             "data": "synthetic (seeded generator; random-init weights quantised on the device)",
             "config": config_block(w, Ln, {"us_per_layer": ms * 1e3 / (args.steps * Ln),
+                                           "host_mirror_fraction": args.host_mirror,
                                            "phase_us_alone": phase_us,
                                            "parallelism": f"replicas x{world}"}),
             "roofline": roofline, "e2e": e2e, "gpu_launches": layers[0].launches(T) * Ln * args.steps,
@@ -482,7 +552,8 @@ def main():
     import gen
     w = gen.get_workload(args.workload)
     if args.layers is None:
-        args.layers = 32 if w.T <= 8 else 8
+        # (16 decode instances with a host mirror: 14.5 GB pinned at most)
+        args.layers = (16 if args.host_mirror > 0 else 32) if w.T <= 8 else 8
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -86,6 +86,35 @@ int moe_forward_launches(moe_layer* L, int T);
  * its three fp32 tensor scales). */
 int moe_layer_info(moe_layer* L, uint64_t* arena_bytes, uint64_t* expert_bytes);
 
+/* ------------------------------------------------------------------ placement */
+
+/* Two memory tiers for the packed experts: HBM, and a pinned host mirror that
+ * the kernels read in place over the CPU-GPU link (NVLink-C2C on Grace
+ * systems).  This is the host mirror of "Strata on an Intel Arc" ("Planned",
+ * item 2: experts without a VRAM slot are read straight from pinned host
+ * memory by the expert kernels) and the placement tiers of the Colibri page
+ * ("Core techniques and measured findings": fast memory changes speed, not
+ * results).
+ *
+ * in_hbm: host array [E + shared] (the shared expert last); nonzero = the
+ * expert gets an HBM slot, zero = it lives in the host mirror.  Moves every
+ * expert's packed bytes (and nothing else: tensor scales, router and workspace
+ * stay in HBM) to its new place, frees the old storage, and rebuilds the
+ * per-expert address table the kernels read.  Results do not depend on the
+ * placement: every path runs the same arithmetic on the same bytes, so the
+ * output is bit-identical.  With any expert on the host, forwards take the
+ * non-tensor-core expert path (the TMA tile maps need one contiguous arena).
+ * Synchronises the device; invalidates CUDA graphs captured before it (they
+ * hold the old addresses).  May be called before or after packing, and again
+ * to move experts.  MOE_ENOMEM if the HBM slots or the pinned mirror cannot be
+ * allocated (the old placement then stays). */
+int moe_place_experts(moe_layer* L, const uint8_t* in_hbm);
+
+/* The current placement: in_hbm [E + shared] (may be NULL) gets 1 for an HBM
+ * slot and 0 for the host mirror; *hbm_bytes / *host_bytes (may be NULL) the
+ * packed-expert bytes held in each tier. */
+int moe_layer_placement(moe_layer* L, uint8_t* in_hbm, uint64_t* hbm_bytes, uint64_t* host_bytes);
+
 /* ------------------------------------------------------------------ weights */
 
 /* Router weights Wr [E x H] as bf16 bits (row-major) and an optional fp32 bias

@@ -38,7 +38,8 @@ EXPORTS = [
     "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
     "moe_pack_weights", "moe_set_router_mode", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_quantize_mxfp4", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
-    "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches"
+    "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches", "moe_place_experts",
+    "moe_layer_placement"
 ]
 
 _lock = threading.Lock()
@@ -117,6 +118,8 @@ def lib():
                 "moe_debug_run_phase": (I, [P, I, P, I, P, P]),
                 "moe_route_noalloc": (I, [P, I, I, P, P, I, I, P, P, P, P]),
                 "moe_forward_launches": (I, [P, I]),
+                "moe_place_experts": (I, [P, P]),
+                "moe_layer_placement": (I, [P, P, ctypes.POINTER(U64), ctypes.POINTER(U64)]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -181,6 +184,23 @@ class MoeLayer:
         a, e = ctypes.c_uint64(), ctypes.c_uint64()
         check(lib().moe_layer_info(self.h, ctypes.byref(a), ctypes.byref(e)))
         return a.value, e.value
+
+    def place_experts(self, in_hbm):
+        """Per expert (routed ones, then the shared one): True = an HBM slot,
+        False = the pinned host mirror the kernels read over the CPU-GPU link."""
+        import numpy as np
+        m = np.ascontiguousarray(np.asarray(in_hbm, dtype=np.uint8).reshape(-1))
+        if m.size != self.E + self.shared:
+            raise ValueError(f"place_experts: {m.size} flags for {self.E + self.shared} experts")
+        check(lib().moe_place_experts(self.h, _ptr(m)))
+
+    def placement(self):
+        """(in_hbm flags as a numpy bool array, HBM bytes, host-mirror bytes)."""
+        import numpy as np
+        m = np.zeros(self.E + self.shared, np.uint8)
+        a, b = ctypes.c_uint64(), ctypes.c_uint64()
+        check(lib().moe_layer_placement(self.h, _ptr(m), ctypes.byref(a), ctypes.byref(b)))
+        return m.astype(bool), a.value, b.value
 
     def status(self, reset=False):
         """The device status word (0 or a negative moe_status a kernel recorded)."""

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(ExpertParams p, int t
   const int tile = blockIdx.x * tpc + (warp % tpc), ks = warp / tpc;
   const bool valid = tile < p.H / 16;
   const MatGeom g = mat_geom(FMT, p.I);
-  const uint8_t* const tiles[1] = {p.arena + (size_t)expert * p.expert_bytes + p.gu_bytes +
+  const uint8_t* const tiles[1] = {expert_base(p, expert) + p.gu_bytes +
                                    (size_t)tile * p.dn_tile_bytes};
   const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
   float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};

@@ -281,7 +281,7 @@ __device__ __forceinline__ void gateup_task(const ExpertParams& p, int expert, i
   const int pair = group * tpc + (warp % tpc), ks = warp / tpc;
   const bool valid = pair < p.I / 16;
   const MatGeom g = mat_geom(FMT, p.H);
-  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
+  const uint8_t* eb = expert_base(p, expert);
   const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
                                    eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
   // routed entries read the router's f16 copy of x; the shared expert's
@@ -441,7 +441,7 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
   const MatGeom g = mat_geom(FMT_NVFP4, p.H);
   const int nh = n_halves(g), nst = gateup_nv_stages(p.H);
   const int sbytes = gateup_nv_stage_bytes(p.T);
-  const uint8_t* eb = p.arena + (size_t)expert * p.expert_bytes;
+  const uint8_t* eb = expert_base(p, expert);
   const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
                                    eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
   const uint32_t wst = smem_u32(smem) + warp * nst * sbytes;
@@ -504,11 +504,11 @@ __device__ __forceinline__ void down_prefetch(const ExpertParams& p, int tile) {
   const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const MatGeom g = mat_geom(FMT, p.I);
   const int n_entries = p.nsh + *p.n_entries;
-  const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
+  const size_t tile_off = p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
   for (int y = warp; y < n_entries; y += nw) {
     const int expert = (y < p.nsh) ? p.E : p.entries[y - p.nsh].x;
     if (expert >= 0 && expert <= p.E)
-      prefetch_tile(FMT, tile_base + (size_t)expert * p.expert_bytes, g, 0, 1);
+      prefetch_tile(FMT, expert_base(p, expert) + tile_off, g, 0, 1);
   }
 }
 
@@ -524,7 +524,7 @@ struct DownPreload {
 __device__ __forceinline__ bool down_preload(const ExpertParams& p, int tile, int y, DownPreload& d) {
   const int lane = threadIdx.x & 31;
   if (!get_entry(p, y, d.expert, d.row, d.n)) return false;  // (reads the count and the entry together)
-  const uint8_t* b = p.arena + (size_t)d.expert * p.expert_bytes + p.gu_bytes +
+  const uint8_t* b = expert_base(p, d.expert) + p.gu_bytes +
                      (size_t)tile * p.dn_tile_bytes + 16 * lane;
   const int nc = p.I / 64;
   d.sv = ldg_stream(b);
@@ -582,7 +582,7 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
   const int S = p.T * p.k;
   const MatGeom g = mat_geom(FMT, p.I);
   const int n_entries = p.nsh + *p.n_entries;
-  const uint8_t* tile_base = p.arena + p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
+  const size_t tile_off = p.gu_bytes + (size_t)tile * p.dn_tile_bytes;
   for (int y = warp; y < n_entries; y += nw) {
     if (have_pre && y == warp) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -596,7 +596,7 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
     }
     int expert, row, n;
     if (!get_entry(p, y, expert, row, n)) continue;
-    const uint8_t* const tiles[1] = {tile_base + (size_t)expert * p.expert_bytes};
+    const uint8_t* const tiles[1] = {expert_base(p, expert) + tile_off};
     const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
     tiles_mma<FMT, 1>(tiles, g, 0, 1, brow, false, acc);

@@ -16,6 +16,7 @@ constexpr int kMaxK = 32;
 // Everything the expert kernels read or write for one forward.
 struct ExpertParams {
   const uint8_t* arena;
+  const uint8_t* const* eptr;  // [E + shared] base of each expert, or null: arena + e * expert_bytes
   uint64_t expert_bytes;
   uint64_t gu_bytes;
   int gu_tile_bytes, dn_tile_bytes;
@@ -37,6 +38,14 @@ struct ExpertParams {
   float* logits_out;     // router logits [T x E] (tensor-core router only)
   int* status;
 };
+
+#ifdef __CUDACC__
+// First byte of expert e's packed matrices: in the arena, or wherever the
+// per-expert table puts it (an HBM slot or the pinned host mirror).
+__device__ __forceinline__ const uint8_t* expert_base(const ExpertParams& p, int e) {
+  return p.eptr ? p.eptr[e] : p.arena + (size_t)e * p.expert_bytes;
+}
+#endif
 
 // Router modes: softmax over the logits (the bias is part of the logit), or
 // sigmoid scores with the bias deciding the selection only.

@@ -88,8 +88,17 @@ struct moe_layer {
   alignas(64) unsigned char map_gu[128] = {};
   alignas(64) unsigned char map_dn[128] = {};
   bool maps_ok = false;
-  uint8_t* arena = nullptr;
+  uint8_t* arena = nullptr;      // HBM: every expert in order, or the HBM slots of a split placement
   uint64_t arena_bytes = 0;
+  // Split placement (moe_place_experts): experts without an HBM slot live in a
+  // pinned, device-mapped host mirror and the kernels read them there through
+  // the per-expert table.  eptr is null while every expert sits in the arena
+  // in expert order.
+  uint8_t* mirror = nullptr;
+  uint64_t mirror_bytes = 0;
+  const uint8_t** eptr = nullptr;           // device [E + shared]
+  std::vector<const uint8_t*> eptr_host;    // the same table, host copy
+  std::vector<uint8_t> in_hbm;              // [E + shared] 1: HBM slot, 0: host mirror
   float* tscale = nullptr;
   uint16_t* router = nullptr;
   float* bias = nullptr;
@@ -123,6 +132,25 @@ struct moe_layer {
 };
 
 namespace {
+
+// The TMA tile maps of the tensor-core path view the arena as
+// [expert][tile][piece]: only while every expert sits there in expert order.
+void make_tile_maps(moe_layer* L) {
+  L->maps_ok = false;
+  if (L->eptr || L->dev_fmt != FMT_NVFP4 || L->H % 128 || (2 * L->I) % 128) return;
+  const ExpertGeom& g = L->geom;
+  const int n_total = L->E + L->shared, gu_tiles = 2 * L->I / 16, dn_tiles = L->H / 16;
+  L->maps_ok =
+      tc_make_tile_map(L->map_gu, L->arena, n_total, gu_tiles, g.gu.tile_bytes, g.expert_bytes,
+                       8 * tc_group(gu_tiles / 8)) == cudaSuccess &&
+      tc_make_tile_map(L->map_dn, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
+                       g.expert_bytes, 8 * tc_group(dn_tiles / 8)) == cudaSuccess;
+}
+
+// Device address of expert e's packed matrices, wherever they are placed.
+const uint8_t* expert_ptr(const moe_layer* L, int e) {
+  return L->eptr ? L->eptr_host[e] : L->arena + (size_t)e * L->geom.expert_bytes;
+}
 
 RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   RouteParams p{};
@@ -159,6 +187,7 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
 ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
   ExpertParams p{};
   p.arena = L->arena;
+  p.eptr = L->eptr;
   p.expert_bytes = L->geom.expert_bytes;
   p.gu_bytes = L->geom.gu_bytes;
   p.gu_tile_bytes = L->geom.gu.tile_bytes;
@@ -318,6 +347,7 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   L->k = k;
   L->shared = shared;
   L->geom = expert_geom(dev_fmt, H, I);
+  L->in_hbm.assign(E + shared, 1);
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = route_kernels_init();
   if (e == cudaSuccess) e = expert_kernels_init();
@@ -344,15 +374,7 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
     moe_layer_destroy(L);
     return fail(MOE_ECUDA, "moe_layer_create: cudaMemset failed");
   }
-  if (L->dev_fmt == FMT_NVFP4 && H % 128 == 0 && (2 * I) % 128 == 0) {
-    const ExpertGeom& g = L->geom;
-    const int gu_tiles = 2 * I / 16, dn_tiles = H / 16;
-    L->maps_ok =
-        tc_make_tile_map(L->map_gu, L->arena, n_total, gu_tiles, g.gu.tile_bytes, g.expert_bytes,
-                         8 * tc_group(gu_tiles / 8)) == cudaSuccess &&
-        tc_make_tile_map(L->map_dn, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
-                         g.expert_bytes, 8 * tc_group(dn_tiles / 8)) == cudaSuccess;
-  }
+  make_tile_maps(L);
   *out = L;
   return MOE_OK;
 }
@@ -431,6 +453,8 @@ void moe_layer_destroy(moe_layer* L) {
   DeviceGuard dg(L->device);
   cudaDeviceSynchronize();
   cudaFree(L->arena);
+  cudaFreeHost(L->mirror);
+  cudaFree(L->eptr);
   cudaFree(L->tscale);
   cudaFree(L->router);
   cudaFree(L->bias);
@@ -451,6 +475,73 @@ int moe_layer_status(moe_layer* L, int reset, int* status) {
 int moe_forward_launches(moe_layer* L, int T) {
   if (!L || T < 1) return fail(MOE_EINVAL, "moe_forward_launches: bad argument");
   return forward_launches(L, T);
+}
+
+int moe_place_experts(moe_layer* L, const uint8_t* in_hbm) {
+  if (!L || !in_hbm) return fail(MOE_EINVAL, "moe_place_experts: null argument");
+  DeviceGuard dg(L->device);
+  const int n_total = L->E + L->shared;
+  const uint64_t eb = L->geom.expert_bytes;
+  int n_hbm = 0;
+  for (int e = 0; e < n_total; ++e) n_hbm += in_hbm[e] != 0;
+  const int n_host = n_total - n_hbm;
+  CK("moe_place_experts: synchronize", cudaDeviceSynchronize());
+  uint8_t* arena = nullptr;
+  uint8_t* mirror = nullptr;
+  uint8_t* mirror_dev = nullptr;
+  const uint8_t** eptr = nullptr;
+  cudaError_t err = cudaSuccess;
+  if (n_hbm) err = cudaMalloc(&arena, (size_t)n_hbm * eb);
+  if (err == cudaSuccess && n_host)
+    err = cudaHostAlloc(&mirror, (size_t)n_host * eb, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (err == cudaSuccess && n_host) err = cudaHostGetDevicePointer(&mirror_dev, mirror, 0);
+  if (err == cudaSuccess && n_host) err = cudaMalloc(&eptr, sizeof(uint8_t*) * n_total);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(arena);
+    cudaFreeHost(mirror);
+    cudaFree(eptr);
+    return fail(MOE_ENOMEM, "moe_place_experts: %d HBM slots + %d host experts of %.1f MB: %s",
+                n_hbm, n_host, eb / 1e6, cudaGetErrorName(err));
+  }
+  // HBM slots in expert order, then the mirror in expert order
+  std::vector<const uint8_t*> table(n_total);
+  for (int e = 0, ih = 0, im = 0; e < n_total; ++e)
+    table[e] = in_hbm[e] ? arena + (size_t)(ih++) * eb : mirror_dev + (size_t)(im++) * eb;
+  for (int e = 0; e < n_total && err == cudaSuccess; ++e)
+    err = cudaMemcpy(const_cast<uint8_t*>(table[e]), expert_ptr(L, e), eb, cudaMemcpyDefault);
+  if (err == cudaSuccess && n_host)
+    err = cudaMemcpy(eptr, table.data(), sizeof(uint8_t*) * n_total, cudaMemcpyHostToDevice);
+  if (err != cudaSuccess) {
+    cudaFree(arena);
+    cudaFreeHost(mirror);
+    cudaFree(eptr);
+    return cuda_fail("moe_place_experts: move the experts", err);
+  }
+  cudaFree(L->arena);
+  cudaFreeHost(L->mirror);
+  cudaFree(L->eptr);
+  L->arena = arena;
+  L->arena_bytes = (uint64_t)n_hbm * eb;
+  L->mirror = mirror;
+  L->mirror_bytes = (uint64_t)n_host * eb;
+  L->eptr = eptr;
+  if (n_host)
+    L->eptr_host = table;
+  else
+    L->eptr_host.clear();
+  for (int e = 0; e < n_total; ++e) L->in_hbm[e] = in_hbm[e] != 0;
+  make_tile_maps(L);
+  return MOE_OK;
+}
+
+int moe_layer_placement(moe_layer* L, uint8_t* in_hbm, uint64_t* hbm_bytes, uint64_t* host_bytes) {
+  if (!L) return fail(MOE_EINVAL, "moe_layer_placement: null layer");
+  if (in_hbm)
+    for (int e = 0; e < L->E + L->shared; ++e) in_hbm[e] = L->in_hbm[e];
+  if (hbm_bytes) *hbm_bytes = L->arena_bytes;
+  if (host_bytes) *host_bytes = L->mirror_bytes;
+  return MOE_OK;
 }
 
 int moe_layer_info(moe_layer* L, uint64_t* arena_bytes, uint64_t* expert_bytes) {
@@ -517,7 +608,7 @@ int moe_pack_matrix(moe_layer* L, int expert, int matrix, const uint8_t* codes,
     st = 0;
   }
   const ExpertGeom& g = L->geom;
-  uint8_t* dst = L->arena + (size_t)expert * g.expert_bytes + tile_offset(g, matrix, 0);
+  uint8_t* dst = const_cast<uint8_t*>(expert_ptr(L, expert)) + tile_offset(g, matrix, 0);
   const uint64_t stride = matrix == MOE_DOWN ? (uint64_t)g.dn.tile_bytes : 2u * g.gu.tile_bytes;
   float* ts_dst = L->tscale + expert * 3 + matrix;
   cudaError_t e = cudaSuccess;
@@ -641,7 +732,7 @@ int moe_debug_dequant(moe_layer* L, int expert, int matrix, float* out, void* st
   DeviceGuard dg(L->device);
   const ExpertGeom& g = L->geom;
   const int rows = matrix == MOE_DOWN ? L->H : L->I, K = matrix == MOE_DOWN ? L->I : L->H;
-  const uint8_t* src = L->arena + (size_t)expert * g.expert_bytes + tile_offset(g, matrix, 0);
+  const uint8_t* src = expert_ptr(L, expert) + tile_offset(g, matrix, 0);
   const uint64_t stride = matrix == MOE_DOWN ? (uint64_t)g.dn.tile_bytes : 2u * g.gu.tile_bytes;
   CK("moe_debug_dequant", launch_debug_dequant(L->dev_fmt, src, stride, rows, K,
                                                L->tscale + expert * 3 + matrix, out,

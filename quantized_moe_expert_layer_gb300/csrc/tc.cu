@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     }
     // my tiles' scale vectors, a super-chunk ahead
     const MatGeom g = mat_geom(FMT_NVFP4, K);
-    const uint8_t* tiles = p.arena + (size_t)expert * p.expert_bytes + (MODE == 1 ? p.gu_bytes : 0);
+    const uint8_t* tiles = expert_base(p, expert) + (MODE == 1 ? p.gu_bytes : 0);
     const size_t tb = MODE == 1 ? (size_t)p.dn_tile_bytes : (size_t)p.gu_tile_bytes;
     const uint8_t* mine = tiles + (size_t)(tile0 + ti) * tb + 16 * ln;
     uint4 sv[2], sv_next[2];

@@ -17,16 +17,20 @@ import gen
 from . import FMT_MXFP4, FMT_NVFP4, MoeLayer, quantize_fp6, quantize_mxfp4, quantize_nvfp4
 
 
-def build_layer(w, T_max=None, seed=None, experts=None, stream=None) -> MoeLayer:
+def build_layer(w, T_max=None, seed=None, experts=None, stream=None, in_hbm=None) -> MoeLayer:
     """Create, pack and reserve a layer for workload ``w``.
 
     seed: overrides the workload's seed (distinct layer instances);
     experts: iterable of expert ids to fill (default: all, E = shared expert);
-    the others keep zero weights.
+    the others keep zero weights;
+    in_hbm: per-expert placement (see MoeLayer.place_experts), applied before
+    packing, so the packer writes host-mirror experts in place.
     """
     s = w.seed if seed is None else seed
     L = MoeLayer(w.fmt, w.H, w.I, w.E, w.k, w.shared)
     L.reserve(T_max or w.T)
+    if in_hbm is not None:
+        L.place_experts(in_hbm)
     ws = dataclasses.replace(w, seed=s)
     L.set_router(gen.router_weights(ws), gen.router_bias(ws))
     dev = torch.device("cuda")

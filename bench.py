@@ -460,14 +460,15 @@ def run_ours(args, w):
     k_us = k0.elapsed_time(k1) * 1e3 / (reps * Ln)
     work = sum(per_launch) / len(per_launch)
     if tc:
-        kname = "tc_gemm_kernel"
+        kname = "tc_expert_kernel"
         peak, peak_kind = peaks("tensor")
         achieved = work / (k_us * 1e-6) / 1e12
         roofline = {"bound": "tensor", "kernel": kname + "<0> (gate/up + SwiGLU)", "achieved": achieved,
                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                     "algorithmic_flops_per_launch": work}
     else:
-        kname = "gateup_routed_kernel" if T <= 8 else "gateup_kernel"
+        kname = ("gateup_routed_kernel" if T <= 8 else
+                 "stream_kernel<0>" if w.fmt in (1, 3) else "gateup_kernel")
         peak, peak_kind = peaks("hbm")
         achieved = work / (k_us * 1e-6) / 1e9
         roofline = {"bound": "hbm", "kernel": kname + " (gate/up + SwiGLU)", "achieved": achieved,
@@ -484,7 +485,7 @@ def run_ours(args, w):
                     "note": "bytes read from the pinned host mirror over the CPU-GPU link"}
         peak_kind = "measured here: 256 MiB pinned host -> device copy, best of 10"
     roofline.update({"traffic": None if host_per_launch else traffic_from_profile(
-                         kname, w.name, os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
+                         kname.split("<")[0], w.name, os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
                      "avg_launch_us": k_us, "peak_source": peak_kind,
                      "timing": "CUDA events over a graph of back-to-back launches, gaps included"})
 

@@ -91,6 +91,20 @@ __global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_routed_kernel(E
   if (pub) publish_counts(rp, rt);
 }
 
+// ---------------------------------------------------------------- streamed NVFP4 GEMVs, 8 < T
+// MODE 0: gate/up + SwiGLU (shared-expert entries run ahead of the router);
+// MODE 1: down.  See stream_task.
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 2) stream_kernel(ExpertParams p) {
+  const int y = blockIdx.y;
+  if (MODE == 1 || y >= p.nsh) griddep_wait();
+  if (MODE == 0) griddep_launch();
+  int expert, row, n;
+  if (!get_entry(p, y, expert, row, n)) return;
+  extern __shared__ __align__(16) uint8_t stream_smem_buf[];
+  stream_task<MODE>(p, expert, row, n, blockIdx.x, stream_smem_buf);
+}
+
 // ---------------------------------------------------------------- down
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 2) down_kernel(ExpertParams p, int tpc) {
@@ -221,8 +235,18 @@ bool gateup_smem_ok(const ExpertParams& p) {
   return p.fmt == FMT_NVFP4 && p.T <= kTokTile && gateup_nv_smem(p.H, p.T) <= kNvMaxDyn;
 }
 
+// Streamed GEMVs: NVFP4 entries of more than one token group's worth of T
+constexpr int kStreamMaxDyn = 200 * 1024;
+bool stream_ok(const ExpertParams& p, int mode) {
+  return p.fmt == FMT_NVFP4 && p.T > kTokTile &&
+         stream_smem(mode == 0 ? 2 : 1, mode == 0 ? p.H : p.I) <= kStreamMaxDyn;
+}
+
 cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
   const int pairs = p.I / 16;
+  if (stream_ok(p, 0))
+    return launch_k(stream_kernel<0>, dim3((pairs + kWarps - 1) / kWarps, grid_y), dim3(kThreads),
+                    stream_smem(2, p.H), st, pdl, p);
   if (gateup_smem_ok(p))
     return launch_k(gateup_kernel<FMT_NVFP4, true>, dim3(pairs, grid_y), dim3(kThreads),
                     gateup_nv_smem(p.H, p.T), st, pdl, p, 1);
@@ -234,6 +258,9 @@ cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStrea
 }
 
 cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
+  if (stream_ok(p, 1))
+    return launch_k(stream_kernel<1>, dim3((p.H / 16 + kWarps - 1) / kWarps, grid_y),
+                    dim3(kThreads), stream_smem(1, p.I), st, pdl, p);
   const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.I)));
   const int tiles = p.H / 16;
   dim3 grid((tiles + tpc - 1) / tpc, grid_y);
@@ -292,6 +319,12 @@ cudaError_t expert_kernels_init() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_NVFP4, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kNvMaxDyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStreamMaxDyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStreamMaxDyn);
   return e;
 }
 

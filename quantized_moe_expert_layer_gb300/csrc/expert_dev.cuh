@@ -354,6 +354,25 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
   return v;
 }
 
+// cp.async of unit hh of NT tiles (per tile: its scale vector and up to 4
+// code vectors, 2560 bytes) into the stage at `dst`.
+template <int NT>
+__device__ __forceinline__ void nv_units_copy(const uint8_t* const* tile, const MatGeom& g, int hh,
+                                              uint32_t dst) {
+  const int lane = threadIdx.x & 31;
+  const int s = hh >> 1, jb = (hh & 1) * 4;
+  const int nc = min(4, sc_units(g, s) - jb);
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const uint8_t* b = tile[i] + (size_t)s * g.sc_bytes + 16 * lane;
+    const uint32_t d = dst + i * 2560 + 16 * lane;
+    cp_async16(d, b);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < nc) cp_async16(d + 512 * (1 + j), b + 512 * (1 + jb + j));
+  }
+}
+
 // cp.async of unit hh (both tiles, and the token rows over its columns) into
 // the stage at `dst`.  tok_of(r): token of row r of the entry.
 template <typename TokOf>
@@ -363,15 +382,7 @@ __device__ __forceinline__ void nv_unit_copy(const uint8_t* const (&tile)[2], co
   const int lane = threadIdx.x & 31;
   const int s = hh >> 1, jb = (hh & 1) * 4;
   const int nc = min(4, sc_units(g, s) - jb);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint8_t* b = tile[i] + (size_t)s * g.sc_bytes + 16 * lane;
-    const uint32_t d = dst + i * 2560 + 16 * lane;
-    cp_async16(d, b);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < nc) cp_async16(d + 512 * (1 + j), b + 512 * (1 + jb + j));
-  }
+  nv_units_copy<2>(tile, g, hh, dst);
   const int pieces = nc * 8, col0 = 256 * hh;  // 16-byte pieces of a row slice
   for (int i = lane; i < n * pieces; i += 32) {
     const int r = i / pieces, c = i - r * pieces;
@@ -382,21 +393,26 @@ __device__ __forceinline__ void nv_unit_copy(const uint8_t* const (&tile)[2], co
   }
 }
 
-// Unit hh of both tiles (staged at `st`) times the staged token rows, into
-// two accumulators per tile (even / odd chunks: shorter mma chains).
-__device__ __forceinline__ void nv_unit_mma(const MatGeom& g, int hh, uint32_t st, int xslot,
-                                            bool b_bf16, float (&acc)[2][2][4]) {
+// Unit hh of NT tiles (staged at `st`) times this lane's staged token row
+// (xrow: its shared-memory address at the unit's first column; has_x false:
+// an empty column), into two accumulators per tile (even / odd chunks:
+// shorter mma chains).
+template <int NT>
+__device__ __forceinline__ void nv_units_mma(const MatGeom& g, int hh, uint32_t st, uint32_t xrow,
+                                             bool has_x, bool b_bf16, float (&acc)[NT][2][4]) {
   const int lane = threadIdx.x & 31, t = lane & 3;
   const int s = hh >> 1, jb = (hh & 1) * 4;
   const int nc = min(4, sc_units(g, s) - jb);
-  const uint4 sv[2] = {lds128(st + 16 * lane), lds128(st + 2560 + 16 * lane)};
+  uint4 sv[NT];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) sv[i] = lds128(st + i * 2560 + 16 * lane);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     if (j < nc) {
       const int jj = jb + j;
       uint32_t xb[8];
-      if (xslot >= 0) {
-        const uint32_t xa = st + kNvUnitBytes + 2 * (xslot * kNvXStride + 64 * j + 16 * t);
+      if (has_x) {
+        const uint32_t xa = xrow + 2 * (64 * j + 16 * t);
         const uint4 q0 = lds128(xa), q1 = lds128(xa + 16);
         xb[0] = q0.x; xb[1] = q0.y; xb[2] = q0.z; xb[3] = q0.w;
         xb[4] = q1.x; xb[5] = q1.y; xb[6] = q1.z; xb[7] = q1.w;
@@ -413,7 +429,7 @@ __device__ __forceinline__ void nv_unit_mma(const MatGeom& g, int hh, uint32_t s
         for (int q = 0; q < 8; ++q) xb[q] = 0u;
       }
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < NT; ++i) {
         const uint4 cv = lds128(st + i * 2560 + 512 * (1 + j) + 16 * lane);
         const uint32_t sp = e4m3x2_to_f16x2((u4get(sv[i], jj >> 1) >> (16 * (jj & 1))) & 0xFFFFu);
         const uint32_t s_lo = dup_lo(sp), s_hi = dup_hi(sp);
@@ -464,7 +480,8 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
     const uint32_t st = wst + (u & 1) * sbytes;
     cp_async_wait<1>();
     __syncwarp();  // the other lanes' token-row pieces of this stage
-    nv_unit_mma(g, hh, st, xslot, shared_entry, acc);
+    nv_units_mma<2>(g, hh, st, st + kNvUnitBytes + 2 * (xslot > 0 ? xslot : 0) * kNvXStride,
+                    xslot >= 0, shared_entry, acc);
     __syncwarp();  // every lane is done with the stage before it is refilled
     if (hh + 2 * kWarps < nh)
       nv_unit_copy(tiles, g, hh + 2 * kWarps, st, xsrc, p.H, n, p.T, tok_of);
@@ -494,6 +511,114 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
       const float G = ts_g * v[i], U = ts_u * v[4 + i];
       const float a = G / (1.0f + expf(-G)) * U;
       p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- NVFP4 streamed expert GEMVs, 8 < T
+// CTA = (work entry of up to 8 tokens, group of kWarps tile pairs for gate/up
+// or kWarps tiles for down).  The entry's B rows (x for gate/up, a for down;
+// f16) are staged once in shared memory over the whole K and shared by the 8
+// warps.  Warp w streams its own tile pair (tile) over the whole K through a
+// two-stage cp.async ring of 256-column units, so it always has the next unit
+// in flight and owns its sums: no K-split reduction and no CTA barrier after
+// the staging.  Staged rows are padded by 16 bytes (bank-conflict-free
+// B-fragment reads of 8 rows).
+constexpr int kStreamStages = 2;
+__host__ __device__ __forceinline__ int stream_xstride(int K) { return K + 8; }
+__host__ __device__ __forceinline__ size_t stream_smem(int nt, int K) {
+  return (size_t)kTokTile * stream_xstride(K) * 2 + (size_t)kWarps * kStreamStages * nt * 2560;
+}
+
+// MODE 0: gate/up + SwiGLU of tile pairs group*kWarps + w into abuf;
+// MODE 1: down tiles group*kWarps + w into ybuf.  smem: stream_smem bytes.
+template <int MODE>
+__device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, int row, int n,
+                                            int group, uint8_t* smem) {
+  constexpr int NT = MODE == 0 ? 2 : 1;
+  const int S = p.T * p.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int K = MODE == 0 ? p.H : p.I;
+  const MatGeom g = mat_geom(FMT_NVFP4, K);
+  const int nh = n_halves(g), xs = stream_xstride(K);
+  const int idx = group * kWarps + warp;  // tile pair (gate/up) or tile (down)
+  const bool valid = idx < (MODE == 0 ? p.I / 16 : p.H / 16);
+  const uint8_t* eb = expert_base(p, expert);
+  const uint8_t* tiles[2];
+  if (MODE == 0) {
+    tiles[0] = eb + (size_t)(2 * idx) * p.gu_tile_bytes;
+    tiles[1] = eb + (size_t)(2 * idx + 1) * p.gu_tile_bytes;
+  } else {
+    tiles[0] = eb + p.gu_bytes + (size_t)idx * p.dn_tile_bytes;
+    tiles[1] = tiles[0];
+  }
+  const uint32_t xs_base = smem_u32(smem);
+  const uint32_t st_base = xs_base + kTokTile * xs * 2 + warp * kStreamStages * NT * 2560;
+  // the B rows first (one cp.async group), then the warp's first two units
+  const bool shared_entry = MODE == 0 && expert == p.E;
+  const int pieces = K / 8;  // 16-byte pieces of a row
+  for (int i = threadIdx.x; i < n * pieces; i += kThreads) {
+    const int r = i / pieces, c = i - r * pieces;
+    const uint32_t dst = xs_base + 2 * (r * xs + 8 * c);
+    if (MODE == 1) {
+      cp_async16(dst, p.abuf + (size_t)(row + r) * p.I + 8 * c);
+    } else if (!shared_entry) {
+      const int tok = p.row_token[row + r];
+      if ((unsigned)tok < (unsigned)p.T) cp_async16(dst, p.xh + (size_t)tok * p.H + 8 * c);
+    } else {  // the shared expert's entries run ahead of the router: convert x here
+      const uint4 q = *reinterpret_cast<const uint4*>(p.x + (size_t)(row - S + r) * p.H + 8 * c);
+      uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[k2] << 16),
+                                            __uint_as_float(w[k2] & 0xFFFF0000u));
+        w[k2] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w[0]), "r"(w[1]),
+                   "r"(w[2]), "r"(w[3])
+                   : "memory");
+    }
+  }
+  cp_async_commit();
+  if (valid) nv_units_copy<NT>(tiles, g, 0, st_base);
+  cp_async_commit();
+  if (valid && nh > 1) nv_units_copy<NT>(tiles, g, 1, st_base + NT * 2560);
+  cp_async_commit();
+  cp_async_wait<2>();  // this thread's B-row pieces
+  __syncthreads();     // everyone's
+  float acc[NT][2][4] = {};
+  if (valid) {
+    const uint32_t xrow = xs_base + 2 * gi * xs;
+    for (int hh = 0; hh < nh; ++hh) {
+      const uint32_t st = st_base + (hh & 1) * NT * 2560;
+      cp_async_wait<1>();
+      __syncwarp();  // the other lanes' pieces of this stage
+      nv_units_mma<NT>(g, hh, st, xrow + 2 * 256 * hh, gi < n, false, acc);
+      __syncwarp();  // every lane is done with the stage before it is refilled
+      if (hh + 2 < nh) nv_units_copy<NT>(tiles, g, hh + 2, st);
+      cp_async_commit();
+    }
+  }
+  cp_async_wait<0>();
+  if (!valid) return;
+  if (MODE == 0) {
+    const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 16 * idx + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+      if (col < n) {
+        const float G = ts_g * (acc[0][0][i] + acc[0][1][i]);
+        const float U = ts_u * (acc[NT - 1][0][i] + acc[NT - 1][1][i]);
+        const float a = G / (1.0f + expf(-G)) * U;
+        p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+      }
+    }
+  } else {
+    const float ts = p.tscale[expert * 3 + 2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 16 * idx + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+      if (col < n) p.ybuf[(size_t)(row + col) * p.H + r] = ts * (acc[0][0][i] + acc[0][1][i]);
     }
   }
 }

@@ -57,20 +57,28 @@ __global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_kernel(ExpertPa
 // reads it after its wait).  Every CTA, once its gate/up weights have landed,
 // asks L2 for its share of its expert's down matrix, so the down kernel reads
 // its weights from L2.  The shared expert's CTAs run at once.
-template <int FMT, bool SMEM>
-__global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_routed_kernel(ExpertParams p, RouteParams rp, int tpc) {
+// PATH 0: registers (gateup_task); 1: the NVFP4 tile pair through shared
+// memory (gateup_task_nv); 2: streamed tile pairs (stream_task, FP6).
+template <int FMT, int PATH>
+__device__ __forceinline__ void gateup_any_task(const ExpertParams& p, int expert, int row, int n,
+                                                int tpc, uint8_t* smem, float* red) {
+  if constexpr (PATH == 1)
+    gateup_task_nv(p, expert, row, n, blockIdx.x, smem, red, true);
+  else if constexpr (PATH == 2)
+    stream_task<FMT, 0>(p, expert, row, n, blockIdx.x, smem);
+  else
+    gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
+}
+
+template <int FMT, int PATH>
+__global__ void __launch_bounds__(kThreads, PATH == 1 ? 3 : 2) gateup_routed_kernel(ExpertParams p, RouteParams rp, int tpc) {
   const int y = blockIdx.y;
   __shared__ float red[kThreads * 8];
   extern __shared__ __align__(16) uint8_t gu_smem[];
   if (y < p.nsh) {
     griddep_launch();
     int expert, row, n;
-    if (get_entry(p, y, expert, row, n)) {
-      if constexpr (SMEM)
-        gateup_task_nv(p, expert, row, n, blockIdx.x, gu_smem, red, true);
-      else
-        gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
-    }
+    if (get_entry(p, y, expert, row, n)) gateup_any_task<FMT, PATH>(p, expert, row, n, tpc, gu_smem, red);
     return;
   }
   __shared__ SmallRoute rt;
@@ -83,10 +91,7 @@ __global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_routed_kernel(E
     const int4 e = rt.entries[d];
     ExpertParams el = p;  // the routed rows' tokens from shared memory
     el.row_token = rt.row_token;
-    if constexpr (SMEM)
-      gateup_task_nv(el, e.x, e.y, e.z, blockIdx.x, gu_smem, red, true);
-    else
-      gateup_task<FMT>(el, e.x, e.y, e.z, blockIdx.x, tpc, red);
+    gateup_any_task<FMT, PATH>(el, e.x, e.y, e.z, tpc, gu_smem, red);
   }
   if (pub) publish_counts(rp, rt);
 }
@@ -94,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_routed_kernel(E
 // ---------------------------------------------------------------- streamed NVFP4 GEMVs, 8 < T
 // MODE 0: gate/up + SwiGLU (shared-expert entries run ahead of the router);
 // MODE 1: down.  See stream_task.
-template <int MODE>
+template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stream_kernel(ExpertParams p) {
   const int y = blockIdx.y;
   if (MODE == 1 || y >= p.nsh) griddep_wait();
@@ -102,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_kernel(ExpertParams p) {
   int expert, row, n;
   if (!get_entry(p, y, expert, row, n)) return;
   extern __shared__ __align__(16) uint8_t stream_smem_buf[];
-  stream_task<MODE>(p, expert, row, n, blockIdx.x, stream_smem_buf);
+  stream_task<FMT, MODE>(p, expert, row, n, blockIdx.x, stream_smem_buf);
 }
 
 // ---------------------------------------------------------------- down
@@ -235,18 +240,27 @@ bool gateup_smem_ok(const ExpertParams& p) {
   return p.fmt == FMT_NVFP4 && p.T <= kTokTile && gateup_nv_smem(p.H, p.T) <= kNvMaxDyn;
 }
 
-// Streamed GEMVs: NVFP4 entries of more than one token group's worth of T
+// Streamed GEMVs: NVFP4 for T > 8 (T <= 8 keeps the tile-pair path), FP6 for
+// gate/up at any T and for down at T > 8 (T <= 8 takes the fused down +
+// combine); within the dynamic shared-memory budget.
 constexpr int kStreamMaxDyn = 200 * 1024;
 bool stream_ok(const ExpertParams& p, int mode) {
-  return p.fmt == FMT_NVFP4 && p.T > kTokTile &&
-         stream_smem(mode == 0 ? 2 : 1, mode == 0 ? p.H : p.I) <= kStreamMaxDyn;
+  if ((mode == 1 || p.fmt == FMT_NVFP4) && p.T <= kTokTile) return false;
+  return stream_smem(p.fmt, mode == 0 ? 2 : 1, mode == 0 ? p.H : p.I, p.T) <= kStreamMaxDyn;
+}
+
+template <int MODE>
+cudaError_t launch_stream(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
+  const dim3 grid(((MODE == 0 ? p.I : p.H) / 16 + kWarps - 1) / kWarps, grid_y);
+  const size_t smem = stream_smem(p.fmt, MODE == 0 ? 2 : 1, MODE == 0 ? p.H : p.I, p.T);
+  if (p.fmt == FMT_NVFP4)
+    return launch_k(stream_kernel<FMT_NVFP4, MODE>, grid, dim3(kThreads), smem, st, pdl, p);
+  return launch_k(stream_kernel<FMT_FP6, MODE>, grid, dim3(kThreads), smem, st, pdl, p);
 }
 
 cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
   const int pairs = p.I / 16;
-  if (stream_ok(p, 0))
-    return launch_k(stream_kernel<0>, dim3((pairs + kWarps - 1) / kWarps, grid_y), dim3(kThreads),
-                    stream_smem(2, p.H), st, pdl, p);
+  if (stream_ok(p, 0)) return launch_stream<0>(p, grid_y, pdl, st);
   if (gateup_smem_ok(p))
     return launch_k(gateup_kernel<FMT_NVFP4, true>, dim3(pairs, grid_y), dim3(kThreads),
                     gateup_nv_smem(p.H, p.T), st, pdl, p, 1);
@@ -258,9 +272,7 @@ cudaError_t launch_gateup(const ExpertParams& p, int grid_y, bool pdl, cudaStrea
 }
 
 cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
-  if (stream_ok(p, 1))
-    return launch_k(stream_kernel<1>, dim3((p.H / 16 + kWarps - 1) / kWarps, grid_y),
-                    dim3(kThreads), stream_smem(1, p.I), st, pdl, p);
+  if (stream_ok(p, 1)) return launch_stream<1>(p, grid_y, pdl, st);
   const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.I)));
   const int tiles = p.H / 16;
   dim3 grid((tiles + tpc - 1) / tpc, grid_y);
@@ -304,27 +316,40 @@ cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, i
                                  cudaStream_t st) {
   const int pairs = p.I / 16;
   if (gateup_smem_ok(p))
-    return launch_k(gateup_routed_kernel<FMT_NVFP4, true>, dim3(pairs, grid_y), dim3(kThreads),
+    return launch_k(gateup_routed_kernel<FMT_NVFP4, 1>, dim3(pairs, grid_y), dim3(kThreads),
                     gateup_nv_smem(p.H, p.T), st, true, p, rp, 1);
+  if (p.fmt == FMT_FP6 && stream_ok(p, 0))
+    return launch_k(gateup_routed_kernel<FMT_FP6, 2>, dim3((pairs + kWarps - 1) / kWarps, grid_y),
+                    dim3(kThreads), stream_smem(p.fmt, 2, p.H, p.T), st, true, p, rp, 1);
   const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
   dim3 grid((pairs + tpc - 1) / tpc, grid_y);
   if (p.fmt == FMT_NVFP4)
-    return launch_k(gateup_routed_kernel<FMT_NVFP4, false>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
-  return launch_k(gateup_routed_kernel<FMT_FP6, false>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
+    return launch_k(gateup_routed_kernel<FMT_NVFP4, 0>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
+  return launch_k(gateup_routed_kernel<FMT_FP6, 0>, grid, dim3(kThreads), 0, st, true, p, rp, tpc);
 }
 
 cudaError_t expert_kernels_init() {
   cudaError_t e = cudaFuncSetAttribute(gateup_kernel<FMT_NVFP4, true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kNvMaxDyn);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_NVFP4, true>,
+    e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_NVFP4, 1>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kNvMaxDyn);
+  // (the routed kernel also holds 23.6 KB of static shared memory)
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStreamMaxDyn);
+    e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_FP6, 2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStreamMaxDyn);
+    e = cudaFuncSetAttribute(stream_kernel<FMT_NVFP4, 0>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_kernel<FMT_NVFP4, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_kernel<FMT_FP6, 0>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_kernel<FMT_FP6, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
   return e;
 }
 

@@ -515,7 +515,7 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
   }
 }
 
-// ---------------------------------------------------------------- NVFP4 streamed expert GEMVs, 8 < T
+// ---------------------------------------------------------------- streamed expert GEMVs
 // CTA = (work entry of up to 8 tokens, group of kWarps tile pairs for gate/up
 // or kWarps tiles for down).  The entry's B rows (x for gate/up, a for down;
 // f16) are staged once in shared memory over the whole K and shared by the 8
@@ -523,23 +523,123 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
 // two-stage cp.async ring of 256-column units, so it always has the next unit
 // in flight and owns its sums: no K-split reduction and no CTA barrier after
 // the staging.  Staged rows are padded by 16 bytes (bank-conflict-free
-// B-fragment reads of 8 rows).
+// B-fragment reads of 8 rows).  NVFP4 (T > 8; decode keeps the tile-pair
+// path) and FP6 (every T).
 constexpr int kStreamStages = 2;
 __host__ __device__ __forceinline__ int stream_xstride(int K) { return K + 8; }
-__host__ __device__ __forceinline__ size_t stream_smem(int nt, int K) {
-  return (size_t)kTokTile * stream_xstride(K) * 2 + (size_t)kWarps * kStreamStages * nt * 2560;
+// bytes of one tile's 256-column unit in a stage
+__host__ __device__ __forceinline__ int stream_unit_bytes(int fmt) {
+  return fmt == FMT_NVFP4 ? 2560 : 3200;
+}
+__host__ __device__ __forceinline__ int stream_rows(int T) { return T < kTokTile ? T : kTokTile; }
+__host__ __device__ __forceinline__ size_t stream_smem(int fmt, int nt, int K, int T) {
+  return (size_t)stream_rows(T) * stream_xstride(K) * 2 +
+         (size_t)kWarps * kStreamStages * nt * stream_unit_bytes(fmt);
+}
+
+// cp.async of FP6 unit hh of NT tiles (per tile: the super-chunk's 128-byte
+// exponent vector and the code vectors of up to 2 blocks, 3200 bytes).
+template <int NT>
+__device__ __forceinline__ void fp6_units_copy(const uint8_t* const* tile, const MatGeom& g, int hh,
+                                               uint32_t dst) {
+  const int lane = threadIdx.x & 31;
+  const int s = hh >> 2, j0 = (hh & 3) * 2, np = sc_units(g, s);
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const uint8_t* b = tile[i] + (size_t)s * g.sc_bytes;
+    const uint32_t d = dst + i * 3200;
+    if (lane < 8) cp_async16(d + 16 * lane, b + 16 * lane);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+      if (j0 + jj < np)
+#pragma unroll
+        for (int v = 0; v < 3; ++v)
+          cp_async16(d + 128 + 1536 * jj + 512 * v + 16 * lane,
+                     b + 128 + 1536 * (j0 + jj) + 512 * v + 16 * lane);
+  }
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// FP6 unit hh of NT tiles (staged at `st`) times this lane's staged row: per
+// 128-column block an fp32 block sum, times the block's power-of-two scale,
+// into acc[i][block parity].
+template <int NT>
+__device__ __forceinline__ void fp6_units_mma(const MatGeom& g, int hh, uint32_t st, uint32_t xrow,
+                                              bool has_x, float (&acc)[NT][2][4]) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
+  const int s = hh >> 2, j0 = (hh & 3) * 2, np = sc_units(g, s);
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    if (j0 + jj < np) {
+      const int j = j0 + jj;
+      uint32_t xb[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (has_x) {
+          const uint32_t xa = xrow + 2 * (128 * jj + 64 * h + 16 * t);
+          const uint4 q0 = lds128(xa), q1 = lds128(xa + 16);
+          xb[h][0] = q0.x; xb[h][1] = q0.y; xb[h][2] = q0.z; xb[h][3] = q0.w;
+          xb[h][4] = q1.x; xb[h][5] = q1.y; xb[h][6] = q1.z; xb[h][7] = q1.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) xb[h][q] = 0u;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        const uint32_t tb = st + i * 3200;
+        const uint4 c0 = lds128(tb + 128 + 1536 * jj + 16 * lane);
+        const uint4 c1 = lds128(tb + 128 + 1536 * jj + 512 + 16 * lane);
+        const uint4 c2 = lds128(tb + 128 + 1536 * jj + 1024 + 16 * lane);
+        const uint32_t words[12] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y,
+                                    c1.z, c1.w, c2.x, c2.y, c2.z, c2.w};
+        float blk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t c[4];
+            fp6_unpack(words[h * 6 + q * 3], words[h * 6 + q * 3 + 1], words[h * 6 + q * 3 + 2], c);
+#pragma unroll
+            for (int ww = 0; ww < 2; ++ww) {
+              const int w = 2 * q + ww;
+              uint32_t u[2], v[2];
+              e2m3x4_to_f16x4(c[2 * ww], u);      // rows g, g+8 at columns 4w, 4w+1
+              e2m3x4_to_f16x4(c[2 * ww + 1], v);  // rows g, g+8 at columns 4w+2, 4w+3
+              const uint32_t a[4] = {u[0], u[1], v[0], v[1]};
+              mma_f16(blk, a, xb[h][2 * w], xb[h][2 * w + 1]);
+            }
+          }
+        }
+        // exponent bytes of rows g and g+8 for block j (the layout of tiles_fp6)
+        const uint32_t e = lds32(tb + 4 * ((gi << 2) | (j >> 1)));
+        const float f0 = ue8m0_to_f32((e >> (16 * (j & 1))) & 0xFFu);
+        const float f1 = ue8m0_to_f32((e >> (16 * (j & 1) + 8)) & 0xFFu);
+        acc[i][jj][0] = fmaf(blk[0], f0, acc[i][jj][0]);
+        acc[i][jj][1] = fmaf(blk[1], f0, acc[i][jj][1]);
+        acc[i][jj][2] = fmaf(blk[2], f1, acc[i][jj][2]);
+        acc[i][jj][3] = fmaf(blk[3], f1, acc[i][jj][3]);
+      }
+    }
+  }
 }
 
 // MODE 0: gate/up + SwiGLU of tile pairs group*kWarps + w into abuf;
 // MODE 1: down tiles group*kWarps + w into ybuf.  smem: stream_smem bytes.
-template <int MODE>
+template <int FMT, int MODE>
 __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, int row, int n,
                                             int group, uint8_t* smem) {
   constexpr int NT = MODE == 0 ? 2 : 1;
+  constexpr int SB = FMT == FMT_NVFP4 ? 2560 : 3200;  // stream_unit_bytes
   const int S = p.T * p.k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   const int K = MODE == 0 ? p.H : p.I;
-  const MatGeom g = mat_geom(FMT_NVFP4, K);
+  const MatGeom g = mat_geom(FMT, K);
   const int nh = n_halves(g), xs = stream_xstride(K);
   const int idx = group * kWarps + warp;  // tile pair (gate/up) or tile (down)
   const bool valid = idx < (MODE == 0 ? p.I / 16 : p.H / 16);
@@ -552,21 +652,33 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
     tiles[0] = eb + p.gu_bytes + (size_t)idx * p.dn_tile_bytes;
     tiles[1] = tiles[0];
   }
+  auto copy_unit = [&](int hh, uint32_t dst) {
+    if (FMT == FMT_NVFP4)
+      nv_units_copy<NT>(tiles, g, hh, dst);
+    else
+      fp6_units_copy<NT>(tiles, g, hh, dst);
+  };
   const uint32_t xs_base = smem_u32(smem);
-  const uint32_t st_base = xs_base + kTokTile * xs * 2 + warp * kStreamStages * NT * 2560;
-  // the B rows first (one cp.async group), then the warp's first two units
+  const uint32_t st_base = xs_base + stream_rows(p.T) * xs * 2 + warp * kStreamStages * NT * SB;
+  // The B rows first (one cp.async group), then the warp's first two units.
+  // Gate/up rows are tokens; with T <= 8 a row sits in slot = its token (an
+  // entry may hold one token twice, e.g. from a given routing), else in slot
+  // = its row of the entry (n <= 8).  Down runs only for T > 8 (slot = row).
   const bool shared_entry = MODE == 0 && expert == p.E;
+  const bool by_token = MODE == 0 && p.T <= kTokTile;
+  auto tok_of = [&](int r) { return shared_entry ? row - S + r : p.row_token[row + r]; };
   const int pieces = K / 8;  // 16-byte pieces of a row
   for (int i = threadIdx.x; i < n * pieces; i += kThreads) {
     const int r = i / pieces, c = i - r * pieces;
-    const uint32_t dst = xs_base + 2 * (r * xs + 8 * c);
+    const int tok = MODE == 0 ? tok_of(r) : 0;
+    if (MODE == 0 && (unsigned)tok >= (unsigned)p.T) continue;
+    const uint32_t dst = xs_base + 2 * ((by_token ? tok : r) * xs + 8 * c);
     if (MODE == 1) {
       cp_async16(dst, p.abuf + (size_t)(row + r) * p.I + 8 * c);
     } else if (!shared_entry) {
-      const int tok = p.row_token[row + r];
-      if ((unsigned)tok < (unsigned)p.T) cp_async16(dst, p.xh + (size_t)tok * p.H + 8 * c);
+      cp_async16(dst, p.xh + (size_t)tok * p.H + 8 * c);
     } else {  // the shared expert's entries run ahead of the router: convert x here
-      const uint4 q = *reinterpret_cast<const uint4*>(p.x + (size_t)(row - S + r) * p.H + 8 * c);
+      const uint4 q = *reinterpret_cast<const uint4*>(p.x + (size_t)tok * p.H + 8 * c);
       uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int k2 = 0; k2 < 4; ++k2) {
@@ -580,22 +692,30 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
     }
   }
   cp_async_commit();
-  if (valid) nv_units_copy<NT>(tiles, g, 0, st_base);
+  if (valid) copy_unit(0, st_base);
   cp_async_commit();
-  if (valid && nh > 1) nv_units_copy<NT>(tiles, g, 1, st_base + NT * 2560);
+  if (valid && nh > 1) copy_unit(1, st_base + NT * SB);
   cp_async_commit();
   cp_async_wait<2>();  // this thread's B-row pieces
   __syncthreads();     // everyone's
   float acc[NT][2][4] = {};
   if (valid) {
-    const uint32_t xrow = xs_base + 2 * gi * xs;
+    int slot = gi < n ? gi : -1;  // this lane's staged row (B column), or none
+    if (MODE == 0 && gi < n) {
+      const int tok = tok_of(gi);
+      slot = (unsigned)tok >= (unsigned)p.T ? -1 : (by_token ? tok : gi);
+    }
+    const uint32_t xrow = xs_base + 2 * (slot > 0 ? slot : 0) * xs;
     for (int hh = 0; hh < nh; ++hh) {
-      const uint32_t st = st_base + (hh & 1) * NT * 2560;
+      const uint32_t st = st_base + (hh & 1) * NT * SB;
       cp_async_wait<1>();
       __syncwarp();  // the other lanes' pieces of this stage
-      nv_units_mma<NT>(g, hh, st, xrow + 2 * 256 * hh, gi < n, false, acc);
+      if (FMT == FMT_NVFP4)
+        nv_units_mma<NT>(g, hh, st, xrow + 2 * 256 * hh, slot >= 0, false, acc);
+      else
+        fp6_units_mma<NT>(g, hh, st, xrow + 2 * 256 * hh, slot >= 0, acc);
       __syncwarp();  // every lane is done with the stage before it is refilled
-      if (hh + 2 < nh) nv_units_copy<NT>(tiles, g, hh + 2, st);
+      if (hh + 2 < nh) copy_unit(hh + 2, st);
       cp_async_commit();
     }
   }

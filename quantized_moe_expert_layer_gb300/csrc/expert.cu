@@ -65,7 +65,7 @@ __device__ __forceinline__ void gateup_any_task(const ExpertParams& p, int exper
   if constexpr (PATH == 1)
     gateup_task_nv(p, expert, row, n, blockIdx.x, smem, red, true);
   else if constexpr (PATH == 2)
-    stream_task<FMT, 0>(p, expert, row, n, blockIdx.x, smem);
+    stream_task<FMT, 0, 2>(p, expert, row, n, blockIdx.x, smem);
   else
     gateup_task<FMT>(p, expert, row, n, blockIdx.x, tpc, red);
 }
@@ -218,13 +218,16 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
     gates = sg;  // read after the task's barrier
     inv = si;
   }
-  extern __shared__ float ys[];  // [rows x 16]
-  down_combine_task<FMT>(p, blockIdx.x, gates, inv, out, ys, pre, have);
+  extern __shared__ float ys[];  // [rows x 16], then (FP6) the warps' unit rings
+  const int rows = p.T * p.k + (p.shared ? p.T : 0);
+  down_combine_task<FMT>(p, blockIdx.x, gates, inv, out, ys, smem_u32(ys + rows * 16), pre, have);
 }
 
+// ys (rows x 16 floats); the FP6 unit rings come on top (down_combine_ring)
 size_t down_combine_smem(int T, int k, int shared) {
   return ((size_t)T * k + (shared ? T : 0)) * 16 * sizeof(float);
 }
+size_t down_combine_ring(int fmt, int warps) { return fmt == FMT_FP6 ? (size_t)warps * 2 * 3200 : 0; }
 
 
 
@@ -246,13 +249,13 @@ bool gateup_smem_ok(const ExpertParams& p) {
 constexpr int kStreamMaxDyn = 200 * 1024;
 bool stream_ok(const ExpertParams& p, int mode) {
   if ((mode == 1 || p.fmt == FMT_NVFP4) && p.T <= kTokTile) return false;
-  return stream_smem(p.fmt, mode == 0 ? 2 : 1, mode == 0 ? p.H : p.I, p.T) <= kStreamMaxDyn;
+  return stream_smem(p.fmt, mode == 0 ? 2 : 1, mode == 0 ? p.H : p.I, p.T, 2) <= kStreamMaxDyn;
 }
 
 template <int MODE>
 cudaError_t launch_stream(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
   const dim3 grid(((MODE == 0 ? p.I : p.H) / 16 + kWarps - 1) / kWarps, grid_y);
-  const size_t smem = stream_smem(p.fmt, MODE == 0 ? 2 : 1, MODE == 0 ? p.H : p.I, p.T);
+  const size_t smem = stream_smem(p.fmt, MODE == 0 ? 2 : 1, MODE == 0 ? p.H : p.I, p.T, 2);
   if (p.fmt == FMT_NVFP4)
     return launch_k(stream_kernel<FMT_NVFP4, MODE>, grid, dim3(kThreads), smem, st, pdl, p);
   return launch_k(stream_kernel<FMT_FP6, MODE>, grid, dim3(kThreads), smem, st, pdl, p);
@@ -299,7 +302,7 @@ cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const
   // one warp per work entry (the routed entries are at most T*k for T <= 8)
   int warps = p.nsh + (p.T * p.k < p.E ? p.T * p.k : p.E);
   if (warps > kDcMaxWarps) warps = kDcMaxWarps;
-  const size_t smem = down_combine_smem(p.T, p.k, p.shared);
+  const size_t smem = down_combine_smem(p.T, p.k, p.shared) + down_combine_ring(p.fmt, warps);
   const dim3 grid(p.H / 16), block(32 * warps);
   if (p.fmt == FMT_NVFP4)
     return wait_first
@@ -320,7 +323,7 @@ cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, i
                     gateup_nv_smem(p.H, p.T), st, true, p, rp, 1);
   if (p.fmt == FMT_FP6 && stream_ok(p, 0))
     return launch_k(gateup_routed_kernel<FMT_FP6, 2>, dim3((pairs + kWarps - 1) / kWarps, grid_y),
-                    dim3(kThreads), stream_smem(p.fmt, 2, p.H, p.T), st, true, p, rp, 1);
+                    dim3(kThreads), stream_smem(p.fmt, 2, p.H, p.T, 2), st, true, p, rp, 1);
   const int tpc = tiles_per_cta(n_halves(mat_geom(p.fmt, p.H)));
   dim3 grid((pairs + tpc - 1) / tpc, grid_y);
   if (p.fmt == FMT_NVFP4)
@@ -338,6 +341,13 @@ cudaError_t expert_kernels_init() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_FP6, 2>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
+
+  if (e == cudaSuccess)  // ys (<= 48 KB) and 12 warps' FP6 rings
+    e = cudaFuncSetAttribute(down_combine_kernel<FMT_FP6, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(down_combine_kernel<FMT_FP6, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(stream_kernel<FMT_NVFP4, 0>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);

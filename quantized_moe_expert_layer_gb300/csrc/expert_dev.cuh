@@ -108,11 +108,20 @@ __device__ __forceinline__ void tiles_nvfp4(const uint8_t* const (&tile)[NT], co
     for (int r = 0; r < 4; ++r) acc[i][r] += acc2[i][0][r] + acc2[i][1][r];
 }
 
+// Byte containers for cvt.rn.f16x2.e2m3x2 from the 4-bit and 2-bit planes:
+// bits 2-5 of each byte from the 4-bit plane, bits 0-1 from the 2-bit plane.
+// cvt reads only bits 0-5 of a container (checked on sm_103a over every
+// 16-bit input), so bits 6-7 may keep whatever the 2-bit plane's shift left
+// there and each container is one bit-select.
+__device__ __forceinline__ uint32_t sel_bits(uint32_t hi4, uint32_t lo2) {
+  constexpr uint32_t M = 0x3C3C3C3Cu;
+  return (hi4 & M) | (lo2 & ~M);
+}
 __device__ __forceinline__ void fp6_unpack(uint32_t Ha, uint32_t Hb, uint32_t L, uint32_t (&c)[4]) {
-  c[0] = ((Ha << 2) & 0x3C3C3C3Cu) | (L & 0x03030303u);
-  c[1] = ((Ha >> 2) & 0x3C3C3C3Cu) | ((L >> 2) & 0x03030303u);
-  c[2] = ((Hb << 2) & 0x3C3C3C3Cu) | ((L >> 4) & 0x03030303u);
-  c[3] = ((Hb >> 2) & 0x3C3C3C3Cu) | ((L >> 6) & 0x03030303u);
+  c[0] = sel_bits(Ha << 2, L);
+  c[1] = sel_bits(Ha >> 2, L >> 2);
+  c[2] = sel_bits(Hb << 2, L >> 4);
+  c[3] = sel_bits(Hb >> 2, L >> 6);
 }
 
 // NT FP6 tiles; a unit is 2 blocks (pairs of 64-column chunks) of 128 columns.
@@ -525,16 +534,16 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
 // the staging.  Staged rows are padded by 16 bytes (bank-conflict-free
 // B-fragment reads of 8 rows).  NVFP4 (T > 8; decode keeps the tile-pair
 // path) and FP6 (every T).
-constexpr int kStreamStages = 2;
 __host__ __device__ __forceinline__ int stream_xstride(int K) { return K + 8; }
 // bytes of one tile's 256-column unit in a stage
 __host__ __device__ __forceinline__ int stream_unit_bytes(int fmt) {
   return fmt == FMT_NVFP4 ? 2560 : 3200;
 }
 __host__ __device__ __forceinline__ int stream_rows(int T) { return T < kTokTile ? T : kTokTile; }
-__host__ __device__ __forceinline__ size_t stream_smem(int fmt, int nt, int K, int T) {
+// ns: ring stages per warp (2 or 3)
+__host__ __device__ __forceinline__ size_t stream_smem(int fmt, int nt, int K, int T, int ns) {
   return (size_t)stream_rows(T) * stream_xstride(K) * 2 +
-         (size_t)kWarps * kStreamStages * nt * stream_unit_bytes(fmt);
+         (size_t)kWarps * ns * nt * stream_unit_bytes(fmt);
 }
 
 // cp.async of FP6 unit hh of NT tiles (per tile: the super-chunk's 128-byte
@@ -565,12 +574,13 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   return v;
 }
 
-// FP6 unit hh of NT tiles (staged at `st`) times this lane's staged row: per
+// FP6 unit hh of NT tiles (staged at `st`) times this lane's B row: per
 // 128-column block an fp32 block sum, times the block's power-of-two scale,
-// into acc[i][block parity].
-template <int NT>
-__device__ __forceinline__ void fp6_units_mma(const MatGeom& g, int hh, uint32_t st, uint32_t xrow,
-                                              bool has_x, float (&acc)[NT][2][4]) {
+// into acc[i][block parity].  ldx(col, xb): this lane's 16 f16 B values at
+// column `col` of the unit (its 16-column block of the m16n8k16 k-permutation).
+template <int NT, typename LdX>
+__device__ __forceinline__ void fp6_units_mma(const MatGeom& g, int hh, uint32_t st, LdX ldx,
+                                              float (&acc)[NT][2][4]) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   const int s = hh >> 2, j0 = (hh & 3) * 2, np = sc_units(g, s);
 #pragma unroll
@@ -579,17 +589,7 @@ __device__ __forceinline__ void fp6_units_mma(const MatGeom& g, int hh, uint32_t
       const int j = j0 + jj;
       uint32_t xb[2][8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (has_x) {
-          const uint32_t xa = xrow + 2 * (128 * jj + 64 * h + 16 * t);
-          const uint4 q0 = lds128(xa), q1 = lds128(xa + 16);
-          xb[h][0] = q0.x; xb[h][1] = q0.y; xb[h][2] = q0.z; xb[h][3] = q0.w;
-          xb[h][4] = q1.x; xb[h][5] = q1.y; xb[h][6] = q1.z; xb[h][7] = q1.w;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) xb[h][q] = 0u;
-        }
-      }
+      for (int h = 0; h < 2; ++h) ldx(128 * jj + 64 * h + 16 * t, xb[h]);
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
         const uint32_t tb = st + i * 3200;
@@ -630,8 +630,9 @@ __device__ __forceinline__ void fp6_units_mma(const MatGeom& g, int hh, uint32_t
 }
 
 // MODE 0: gate/up + SwiGLU of tile pairs group*kWarps + w into abuf;
-// MODE 1: down tiles group*kWarps + w into ybuf.  smem: stream_smem bytes.
-template <int FMT, int MODE>
+// MODE 1: down tiles group*kWarps + w into ybuf.  NS ring stages per warp.
+// smem: stream_smem bytes.
+template <int FMT, int MODE, int NS = 2>
 __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, int row, int n,
                                             int group, uint8_t* smem) {
   constexpr int NT = MODE == 0 ? 2 : 1;
@@ -659,8 +660,8 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
       fp6_units_copy<NT>(tiles, g, hh, dst);
   };
   const uint32_t xs_base = smem_u32(smem);
-  const uint32_t st_base = xs_base + stream_rows(p.T) * xs * 2 + warp * kStreamStages * NT * SB;
-  // The B rows first (one cp.async group), then the warp's first two units.
+  const uint32_t st_base = xs_base + stream_rows(p.T) * xs * 2 + warp * NS * NT * SB;
+  // The B rows first (one cp.async group), then the warp's first NS units.
   // Gate/up rows are tokens; with T <= 8 a row sits in slot = its token (an
   // entry may hold one token twice, e.g. from a given routing), else in slot
   // = its row of the entry (n <= 8).  Down runs only for T > 8 (slot = row).
@@ -692,12 +693,13 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
     }
   }
   cp_async_commit();
-  if (valid) copy_unit(0, st_base);
-  cp_async_commit();
-  if (valid && nh > 1) copy_unit(1, st_base + NT * SB);
-  cp_async_commit();
-  cp_async_wait<2>();  // this thread's B-row pieces
-  __syncthreads();     // everyone's
+#pragma unroll
+  for (int u = 0; u < NS; ++u) {
+    if (valid && u < nh) copy_unit(u, st_base + u * NT * SB);
+    cp_async_commit();
+  }
+  cp_async_wait<NS>();  // this thread's B-row pieces
+  __syncthreads();      // everyone's
   float acc[NT][2][4] = {};
   if (valid) {
     int slot = gi < n ? gi : -1;  // this lane's staged row (B column), or none
@@ -707,15 +709,25 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
     }
     const uint32_t xrow = xs_base + 2 * (slot > 0 ? slot : 0) * xs;
     for (int hh = 0; hh < nh; ++hh) {
-      const uint32_t st = st_base + (hh & 1) * NT * SB;
-      cp_async_wait<1>();
+      const uint32_t st = st_base + (hh % NS) * NT * SB;
+      cp_async_wait<NS - 1>();
       __syncwarp();  // the other lanes' pieces of this stage
       if (FMT == FMT_NVFP4)
         nv_units_mma<NT>(g, hh, st, xrow + 2 * 256 * hh, slot >= 0, false, acc);
       else
-        fp6_units_mma<NT>(g, hh, st, xrow + 2 * 256 * hh, slot >= 0, acc);
+        fp6_units_mma<NT>(g, hh, st, [&](int col, uint32_t(&xb)[8]) {
+          if (slot >= 0) {
+            const uint32_t xa = xrow + 2 * (256 * hh + col);
+            const uint4 q0 = lds128(xa), q1 = lds128(xa + 16);
+            xb[0] = q0.x; xb[1] = q0.y; xb[2] = q0.z; xb[3] = q0.w;
+            xb[4] = q1.x; xb[5] = q1.y; xb[6] = q1.z; xb[7] = q1.w;
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xb[q] = 0u;
+          }
+        }, acc);
       __syncwarp();  // every lane is done with the stage before it is refilled
-      if (hh + 2 < nh) copy_unit(hh + 2, st);
+      if (hh + NS < nh) copy_unit(hh + NS, st);
       cp_async_commit();
     }
   }
@@ -818,10 +830,12 @@ __device__ __forceinline__ void down_preloaded_mma(const ExpertParams& p, const 
 // into ys [rows x 16] (shared memory), then out[:, tile] = sum_j g_j y_j + y_s
 // in j order (the same fmaf chain as combine_kernel).  `pre`: the warp's first
 // entry, preloaded (when have_pre).
+// FP6: `ring` is a shared-memory ring of 2 x 3200 bytes per warp.
 template <int FMT>
 __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int tile, const float* gates,
                                                   const int* inv, float* out, float* ys,
-                                                  const DownPreload& pre, bool have_pre) {
+                                                  uint32_t ring, const DownPreload& pre,
+                                                  bool have_pre) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int gi = lane >> 2, t = lane & 3;
   const int S = p.T * p.k;
@@ -844,7 +858,36 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
     const uint8_t* const tiles[1] = {expert_base(p, expert) + tile_off};
     const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    tiles_mma<FMT, 1>(tiles, g, 0, 1, brow, false, acc);
+    if (FMT == FMT_FP6) {
+      // the tile's units through this warp's two-stage cp.async ring (`ring`),
+      // the entry's rows of a pulled into L1 first
+      for (int r = 0; r < n; ++r)
+        for (int o = 128 * lane; o < 2 * p.I; o += 128 * 32)
+          prefetch_l1(reinterpret_cast<const uint8_t*>(p.abuf + (size_t)(row + r) * p.I) + o);
+      const int nh = n_halves(g);
+      const uint32_t wr = ring + warp * 2 * 3200;
+      fp6_units_copy<1>(tiles, g, 0, wr);
+      cp_async_commit();
+      if (nh > 1) fp6_units_copy<1>(tiles, g, 1, wr + 3200);
+      cp_async_commit();
+      float a2[1][2][4] = {};
+      for (int hh = 0; hh < nh; ++hh) {
+        const uint32_t st = wr + (hh & 1) * 3200;
+        cp_async_wait<1>();
+        __syncwarp();
+        fp6_units_mma<1>(g, hh, st, [&](int col, uint32_t(&xb)[8]) {
+          load_b(brow, 256 * hh + col, false, xb);
+        }, a2);
+        __syncwarp();
+        if (hh + 2 < nh) fp6_units_copy<1>(tiles, g, hh + 2, st);
+        cp_async_commit();
+      }
+      cp_async_wait<0>();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[0][i] = a2[0][0][i] + a2[0][1][i];
+    } else {
+      tiles_mma<FMT, 1>(tiles, g, 0, 1, brow, false, acc);
+    }
     const float ts = p.tscale[expert * 3 + 2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

@@ -28,11 +28,29 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouteParams p) {
   router_partials(p, blockIdx.x, blockIdx.y, blockIdx.z, smem_u4);
 }
 
+// One token per CTA: the 8 warps take E/8 experts each and find their k best,
+// warp 0 merges the 8k candidates (topk_token_cta); a warp per token would
+// run k arg-max rounds over E/32 slots per lane, a longer serial chain.
+template <int V1, int V2>
+__device__ __forceinline__ void topk_cta_task(const RouteParams& p, uint32_t* ck, int* ci) {
+  topk_token_cta<V1, V2>(p, blockIdx.x, nullptr, ck, ci);
+}
+
 __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
   griddep_launch();
   griddep_wait();
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t < p.T) topk_token(p, t, threadIdx.x & 31, nullptr);
+  __shared__ uint32_t ck[8 * kMaxK];
+  __shared__ int ci[8 * kMaxK];
+  const int q = (p.E + 7) / 8;  // experts per warp (E <= 1024: q <= 128)
+  if (8 * p.k <= 96) {
+    if (q <= 32) topk_cta_task<1, 3>(p, ck, ci);
+    else if (q <= 64) topk_cta_task<2, 3>(p, ck, ci);
+    else topk_cta_task<4, 3>(p, ck, ci);
+  } else {
+    if (q <= 32) topk_cta_task<1, 8>(p, ck, ci);
+    else if (q <= 64) topk_cta_task<2, 8>(p, ck, ci);
+    else topk_cta_task<4, 8>(p, ck, ci);
+  }
 }
 
 __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParams p, int do_topk) {
@@ -95,7 +113,7 @@ cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st) {
-  return launch_k(topk_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, pdl, p);
+  return launch_k(topk_kernel, dim3(p.T), dim3(256), 0, st, pdl, p);
 }
 
 cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st) {

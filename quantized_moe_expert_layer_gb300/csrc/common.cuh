@@ -109,9 +109,6 @@ __device__ __forceinline__ void griddep_launch() {
 }
 
 // fire-and-forget request to bring a line into L2
-__device__ __forceinline__ void prefetch_l1(const void* ptr) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
-}
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }

@@ -142,39 +142,55 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(ExpertParams p, int t
 }
 
 // ---------------------------------------------------------------- combine
-// out[t] = sum_j gates[t,j] * y[row(t,j)] + y_shared[t], j in order.
+// out[t] = sum_j gates[t,j] * y[row(t,j)] + y_shared[t], j in order.  One
+// warp per (token, slice of 32U float4s of the row): lane j < k reads gate j
+// and row j once and hands them out by shuffle; each lane accumulates U
+// float4s (h, h + 32, ...), so every step of the j loop has U independent
+// row loads in flight (U = 1 when there are too few tokens to fill the GPU).
+template <int U>
 __global__ void __launch_bounds__(256) combine_kernel(ExpertParams p, const float* gates,
                                                       const int* inv, float* out) {
   griddep_launch();
   griddep_wait();
-  const int H4 = p.H / 4, S = p.T * p.k;
+  const int H4 = p.H / 4, S = p.T * p.k, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const float4* y4 = reinterpret_cast<const float4*>(p.ybuf);
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)p.T * H4;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / H4), h = (int)(i % H4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float gs[kMaxK];
-    int rows[kMaxK];
+  float4* o4 = reinterpret_cast<float4*>(out);
+  const int ns = (H4 + 32 * U - 1) / (32 * U);  // slices per row
+  for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < p.T * ns; item += nwarps) {
+    const int t = item / ns;
+    const float g_l = lane < p.k ? gates[(size_t)t * p.k + lane] : 0.f;
+    const int r_l = lane < p.k ? inv[(size_t)t * p.k + lane] : 0;
+    {
+      const int h0 = (item - t * ns) * 32 * U + lane;
+      float4 acc[U];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j < p.k) {
-        gs[j] = gates[(size_t)t * p.k + j];
-        rows[j] = inv[(size_t)t * p.k + j];
+      for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+      for (int j = 0; j < p.k; ++j) {
+        const float g = __shfl_sync(0xffffffffu, g_l, j);
+        const float4* yr = y4 + (size_t)__shfl_sync(0xffffffffu, r_l, j) * H4;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (h0 + 32 * u < H4) {
+            const float4 yv = yr[h0 + 32 * u];
+            acc[u].x = fmaf(g, yv.x, acc[u].x);
+            acc[u].y = fmaf(g, yv.y, acc[u].y);
+            acc[u].z = fmaf(g, yv.z, acc[u].z);
+            acc[u].w = fmaf(g, yv.w, acc[u].w);
+          }
       }
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j < p.k) {
-        const float4 yv = y4[(size_t)rows[j] * H4 + h];
-        acc.x = fmaf(gs[j], yv.x, acc.x);
-        acc.y = fmaf(gs[j], yv.y, acc.y);
-        acc.z = fmaf(gs[j], yv.z, acc.z);
-        acc.w = fmaf(gs[j], yv.w, acc.w);
+      for (int u = 0; u < U; ++u) {
+        const int h = h0 + 32 * u;
+        if (h >= H4) continue;
+        if (p.shared) {
+          const float4 yv = y4[(size_t)(S + t) * H4 + h];
+          acc[u].x += yv.x; acc[u].y += yv.y; acc[u].z += yv.z; acc[u].w += yv.w;
+        }
+        o4[(size_t)t * H4 + h] = acc[u];
       }
-    if (p.shared) {
-      const float4 yv = y4[(size_t)(S + t) * H4 + h];
-      acc.x += yv.x; acc.y += yv.y; acc.z += yv.z; acc.w += yv.w;
     }
-    reinterpret_cast<float4*>(out)[i] = acc;
   }
 }
 
@@ -227,7 +243,9 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
 size_t down_combine_smem(int T, int k, int shared) {
   return ((size_t)T * k + (shared ? T : 0)) * 16 * sizeof(float);
 }
-size_t down_combine_ring(int fmt, int warps) { return fmt == FMT_FP6 ? (size_t)warps * 2 * 3200 : 0; }
+size_t down_combine_ring(int fmt, int warps) {
+  return fmt == FMT_FP6 ? (size_t)warps * 2 * kDcFp6Stage : 0;
+}
 
 
 
@@ -286,10 +304,14 @@ cudaError_t launch_down(const ExpertParams& p, int grid_y, bool pdl, cudaStream_
 
 cudaError_t launch_combine(const ExpertParams& p, const float* gates, const int* inv, float* out,
                            bool pdl, cudaStream_t st) {
-  const int64_t n = (int64_t)p.T * (p.H / 4);
-  int blocks = (int)((n + 255) / 256);
-  if (blocks > 152 * 8) blocks = 152 * 8;
-  return launch_k(combine_kernel, dim3(blocks), dim3(256), 0, st, pdl, p, gates, inv, out);
+  // a warp per item; 4 float4s per lane once that still gives every SM 16 warps
+  const int64_t items4 = (int64_t)p.T * ((p.H / 4 + 127) / 128);
+  const bool wide = items4 >= 152 * 16;
+  const int64_t items = wide ? items4 : (int64_t)p.T * ((p.H / 4 + 31) / 32);
+  int blocks = (int)((items + 7) / 8);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (wide) return launch_k(combine_kernel<4>, dim3(blocks), dim3(256), 0, st, pdl, p, gates, inv, out);
+  return launch_k(combine_kernel<1>, dim3(blocks), dim3(256), 0, st, pdl, p, gates, inv, out);
 }
 
 bool down_combine_ok(int T, int k, int shared, int I) {

@@ -830,7 +830,8 @@ __device__ __forceinline__ void down_preloaded_mma(const ExpertParams& p, const 
 // into ys [rows x 16] (shared memory), then out[:, tile] = sum_j g_j y_j + y_s
 // in j order (the same fmaf chain as combine_kernel).  `pre`: the warp's first
 // entry, preloaded (when have_pre).
-// FP6: `ring` is a shared-memory ring of 2 x 3200 bytes per warp.
+// FP6: `ring` is a shared-memory ring of 2 stages of kDcFp6Stage bytes per warp.
+constexpr int kDcFp6Stage = 3200 + 512;  // a unit's weights and one row of a over its columns
 template <int FMT>
 __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int tile, const float* gates,
                                                   const int* inv, float* out, float* ys,
@@ -859,27 +860,42 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
     const uint16_t* brow = gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr;
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
     if (FMT == FMT_FP6) {
-      // the tile's units through this warp's two-stage cp.async ring (`ring`),
-      // the entry's rows of a pulled into L1 first
-      for (int r = 0; r < n; ++r)
-        for (int o = 128 * lane; o < 2 * p.I; o += 128 * 32)
-          prefetch_l1(reinterpret_cast<const uint8_t*>(p.abuf + (size_t)(row + r) * p.I) + o);
+      // The tile's units through this warp's two-stage cp.async ring (`ring`,
+      // kDcFp6Stage bytes a stage).  A one-row entry (every entry of a
+      // self-routed token) copies its row of a over the unit's columns into
+      // the same stage; other entries read a from global memory.
+      const bool b_smem = n == 1;
+      const uint16_t* arow = p.abuf + (size_t)row * p.I;
       const int nh = n_halves(g);
-      const uint32_t wr = ring + warp * 2 * 3200;
-      fp6_units_copy<1>(tiles, g, 0, wr);
+      const uint32_t wr = ring + warp * 2 * kDcFp6Stage;
+      auto copy_unit = [&](int hh, uint32_t dst) {
+        fp6_units_copy<1>(tiles, g, hh, dst);
+        if (b_smem && 256 * hh + 8 * lane < p.I)
+          cp_async16(dst + 3200 + 16 * lane, arow + 256 * hh + 8 * lane);
+      };
+      copy_unit(0, wr);
       cp_async_commit();
-      if (nh > 1) fp6_units_copy<1>(tiles, g, 1, wr + 3200);
+      if (nh > 1) copy_unit(1, wr + kDcFp6Stage);
       cp_async_commit();
       float a2[1][2][4] = {};
       for (int hh = 0; hh < nh; ++hh) {
-        const uint32_t st = wr + (hh & 1) * 3200;
+        const uint32_t st = wr + (hh & 1) * kDcFp6Stage;
         cp_async_wait<1>();
         __syncwarp();
         fp6_units_mma<1>(g, hh, st, [&](int col, uint32_t(&xb)[8]) {
-          load_b(brow, 256 * hh + col, false, xb);
+          if (!b_smem) {
+            load_b(brow, 256 * hh + col, false, xb);
+          } else if (gi == 0) {
+            const uint4 q0 = lds128(st + 3200 + 2 * col), q1 = lds128(st + 3200 + 2 * col + 16);
+            xb[0] = q0.x; xb[1] = q0.y; xb[2] = q0.z; xb[3] = q0.w;
+            xb[4] = q1.x; xb[5] = q1.y; xb[6] = q1.z; xb[7] = q1.w;
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xb[q] = 0u;
+          }
         }, a2);
         __syncwarp();
-        if (hh + 2 < nh) fp6_units_copy<1>(tiles, g, hh + 2, st);
+        if (hh + 2 < nh) copy_unit(hh + 2, st);
         cp_async_commit();
       }
       cp_async_wait<0>();

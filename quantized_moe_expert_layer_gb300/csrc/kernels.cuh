@@ -71,8 +71,14 @@ struct RouteParams {
   int* n_entries;
   int4* tc_entries;       // optional: entries of up to kTcMaxN tokens (tensor-core path)
   int* n_tc_entries;
+  int* blk;               // [ceil(T*k / kDispChunk) x E] per-chunk expert counts, then bases
   int* status;
 };
+
+// Slots per CTA of the several-CTA dispatch (count, scan, place), used when
+// T*k is above kDispOneCtaMax; below it one CTA does the whole dispatch.
+constexpr int kDispChunk = 1024;
+constexpr int kDispOneCtaMax = 8192;
 
 cudaError_t launch_quantize_nvfp4(const float* W, int rows, int K, uint8_t* codes,
                                   uint8_t* scales, float* tscale, cudaStream_t st);
@@ -92,6 +98,10 @@ cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stri
 int router_ksplit(int T, int H, int E);
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
 cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st);
+// Dispatch of p.idx (top-k done): one CTA, or count / scan / place kernels
+// for T*k > kDispOneCtaMax.  dispatch_launches: how many kernels that is.
+cudaError_t launch_dispatch(const RouteParams& p, bool pdl, cudaStream_t st);
+int dispatch_launches(int S);
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st);
 size_t route_finish_smem(int E);
 cudaError_t route_kernels_init();

@@ -122,6 +122,7 @@ struct moe_layer {
   int* n_entries = nullptr;
   int4* tc_entries = nullptr;    // entries of up to 256 tokens (tensor-core path)
   int* n_tc_entries = nullptr;
+  int* blk = nullptr;            // per-chunk expert counts of the several-CTA dispatch
   uint16_t* xh = nullptr;        // f16 copy of x
   uint16_t* abuf = nullptr;
   float* ybuf = nullptr;
@@ -180,6 +181,7 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.xh = L->xh;
   p.tc_entries = tc ? L->tc_entries : nullptr;
   p.n_tc_entries = tc ? L->n_tc_entries : nullptr;
+  p.blk = L->blk;
   p.status = L->status;
   return p;
 }
@@ -283,7 +285,9 @@ bool small_path(moe_layer* L, int T) { return small_route_ok(T, L->k) && fused_d
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
   if (small_path(L, T)) return 3;
-  const int routing = tc_router(L, T) ? 4 : (T <= kFusedTopkMaxT ? 2 : 3);
+  // (convert x, tc router | router), top-k, dispatch (1 or 3 kernels); T <= 16: router, top-k + dispatch
+  const int dispatch = dispatch_launches(T * L->k);
+  const int routing = tc_router(L, T) ? 3 + dispatch : (T <= kFusedTopkMaxT ? 2 : 2 + dispatch);
   if (tc_path(L, T)) return routing + 3;
   return routing + (fused_down(L, T) ? 2 : 3);
 }
@@ -304,14 +308,14 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
     const int rc = launch_tc_routing_gemm(L, x, T, st);
     if (rc) return rc;
     CK("top-k kernel launch", launch_topk(rp, true, st));
-    CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
+    CK("dispatch kernel launch", launch_dispatch(rp, true, st));
   } else if (T <= kFusedTopkMaxT) {
     CK("router kernel launch", launch_router(rp, st));
     CK("top-k/dispatch kernel launch", launch_route_finish(rp, true, true, st));
   } else {
     CK("router kernel launch", launch_router(rp, st));
     CK("top-k kernel launch", launch_topk(rp, true, st));
-    CK("dispatch kernel launch", launch_route_finish(rp, false, true, st));
+    CK("dispatch kernel launch", launch_dispatch(rp, true, st));
   }
   L->last_T = T;
   L->last_has_logits = true;
@@ -405,6 +409,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       (S + T_max) * L->H * 4,            // ybuf
       (size_t)T_max * L->H * 2,          // x_stage
       (size_t)T_max * L->H * 4,          // out_stage
+      ((S + kDispChunk - 1) / kDispChunk) * E * 4,  // blk
   };
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t total = 0;
@@ -443,6 +448,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->ybuf = (float*)ptrs[15];
   L->x_stage = (uint16_t*)ptrs[16];
   L->out_stage = (float*)ptrs[17];
+  L->blk = (int*)ptrs[18];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   return MOE_OK;
@@ -719,7 +725,7 @@ int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* id
      cudaMemcpyAsync(L->gates, gates, S * 4, cudaMemcpyDeviceToDevice, st));
   CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, st));
   RouteParams rp = route_params(L, x, T);
-  CK("dispatch kernel launch", launch_route_finish(rp, false, false, st));
+  CK("dispatch kernel launch", launch_dispatch(rp, false, st));
   L->last_T = T;
   L->last_has_logits = false;
   return run_experts(L, x, T, out, st);
@@ -795,7 +801,7 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
         CK("top-k/dispatch", launch_route_finish(rp, true, false, st));
       } else {
         CK("top-k", launch_topk(rp, false, st));
-        CK("dispatch", launch_route_finish(rp, false, false, st));
+        CK("dispatch", launch_dispatch(rp, false, st));
       }
       break;
     case 2:

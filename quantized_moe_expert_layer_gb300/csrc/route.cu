@@ -65,6 +65,92 @@ __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParam
   dispatch_block(p, smem_i + 64, smem_i);
 }
 
+// ---------------------------------------------------------------- dispatch over several CTAs
+// For many slots the one-CTA dispatch walks them serially; here CTA b of the
+// count and place kernels takes slots [b * kDispChunk, (b + 1) * kDispChunk)
+// (one per thread), and one CTA scans the per-chunk counts in between.  The
+// rows come out the same as dispatch_block's: expert-major, ascending slot
+// within an expert.
+
+// Per-chunk expert counts into p.blk[b * E + e].
+__global__ void __launch_bounds__(kDispChunk) dispatch_count_kernel(RouteParams p) {
+  griddep_launch();
+  griddep_wait();
+  extern __shared__ int hist_c[];  // [E]
+  const int b = blockIdx.x, tid = threadIdx.x, E = p.E, S = p.T * p.k;
+  for (int i = tid; i < E; i += blockDim.x) hist_c[i] = 0;
+  __syncthreads();
+  const int s = b * kDispChunk + tid;
+  if (s < S) atomicAdd(&hist_c[checked_expert(p, p.idx[s])], 1);
+  __syncthreads();
+  for (int i = tid; i < E; i += blockDim.x) p.blk[(size_t)b * E + i] = hist_c[i];
+}
+
+// Per expert (thread e < E, blockDim.x >= E): the chunks' counts become the
+// expert's rows before each chunk (in place); counts, offsets, entries.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(RouteParams p, int nb) {
+  griddep_launch();
+  griddep_wait();
+  __shared__ int sc[64];
+  const int tid = threadIdx.x, E = p.E;
+  int c = 0;
+  if (tid < E) {
+    for (int b0 = 0; b0 < nb; b0 += 16) {  // 16 loads in flight, then the running sum
+      int v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) v[u] = (b0 + u < nb) ? p.blk[(size_t)(b0 + u) * E + tid] : 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (b0 + u < nb) {
+          p.blk[(size_t)(b0 + u) * E + tid] = c;
+          c += v[u];
+        }
+    }
+  }
+  int total;
+  const int excl = block_excl_scan(tid < E ? c : 0, sc, &total);
+  if (tid < E) {
+    p.counts[tid] = c;
+    p.offsets[tid] = excl;
+  }
+  if (tid == 0) p.offsets[E] = total;
+  write_entries(p, c, excl, sc);
+}
+
+// Stable placement of chunk b: row = offsets[e] + rows of e in earlier chunks
+// + rows of e in earlier warps of this chunk + rank among the warp's lanes.
+__global__ void __launch_bounds__(kDispChunk) dispatch_place_kernel(RouteParams p) {
+  griddep_launch();
+  griddep_wait();
+  extern __shared__ int hist_p[];  // [warps][E]
+  const int b = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int E = p.E, S = p.T * p.k, NW = blockDim.x >> 5;
+  for (int i = tid; i < NW * E; i += blockDim.x) hist_p[i] = 0;
+  __syncthreads();
+  const int s = b * kDispChunk + tid;
+  const bool valid = s < S;
+  const int e = valid ? checked_expert(p, p.idx[s]) : -1 - lane;
+  const uint32_t peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & lanemask_lt());
+  if (valid && lane == __ffs(peers) - 1) hist_p[w * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = tid; x < E; x += blockDim.x) {
+    int run = p.offsets[x] + p.blk[(size_t)b * E + x];
+    for (int ww = 0; ww < NW; ++ww) {
+      const int v = hist_p[ww * E + x];
+      hist_p[ww * E + x] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  if (valid) {
+    const int pos = hist_p[w * E + e] + rank;
+    p.perm[pos] = s;
+    p.inv[s] = pos;
+    p.row_token[pos] = s / p.k;
+  }
+}
+
 __global__ void convert_x_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xh, long n8) {
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long)gridDim.x * blockDim.x) {
     const uint4 raw = reinterpret_cast<const uint4*>(x)[i];
@@ -121,9 +207,27 @@ cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cu
                   pdl, p, do_topk ? 1 : 0);
 }
 
+int dispatch_launches(int S) { return S > kDispOneCtaMax ? 3 : 1; }
+
+cudaError_t launch_dispatch(const RouteParams& p, bool pdl, cudaStream_t st) {
+  const int S = p.T * p.k;
+  if (S <= kDispOneCtaMax) return launch_route_finish(p, false, pdl, st);
+  const int nb = (S + kDispChunk - 1) / kDispChunk;
+  cudaError_t e = launch_k(dispatch_count_kernel, dim3(nb), dim3(kDispChunk), p.E * sizeof(int),
+                           st, pdl, p);
+  if (e == cudaSuccess) e = launch_k(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, pdl, p, nb);
+  if (e == cudaSuccess)
+    e = launch_k(dispatch_place_kernel, dim3(nb), dim3(kDispChunk),
+                 (size_t)(kDispChunk / 32) * p.E * sizeof(int), st, pdl, p);
+  return e;
+}
+
 cudaError_t route_kernels_init() {
   cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        200 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dispatch_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (kDispChunk / 32) * kMaxE * (int)sizeof(int));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)route_finish_smem(kMaxE));

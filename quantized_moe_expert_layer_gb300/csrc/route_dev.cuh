@@ -367,6 +367,31 @@ __device__ __forceinline__ int checked_expert(const RouteParams& p, int e) {
   return e;
 }
 
+// The shared rows' tokens and the work entries, by every thread of the block
+// (blockDim.x >= E): thread e < E holds expert e's slot count c and first row
+// excl.  Routed entries: ceil(c / 8) per expert, expert-major; tensor-core
+// entries (when p.tc_entries): ceil(c / 128).
+__device__ void write_entries(const RouteParams& p, int c, int excl, int* sc) {
+  const int tid = threadIdx.x, E = p.E, S = p.T * p.k;
+  for (int i = tid; i < p.T; i += blockDim.x) p.row_token[S + i] = i;
+  const int nch = (tid < E) ? (c + kTokTile - 1) / kTokTile : 0;
+  int n_total;
+  const int ebase = block_excl_scan(nch, sc, &n_total);
+  if (tid < E)
+    for (int i = 0; i < nch; ++i)
+      p.entries[ebase + i] = make_int4(tid, excl + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
+  if (tid == 0) *p.n_entries = n_total;
+  if (p.tc_entries) {
+    const int ntc = (tid < E) ? (c + kTcMaxN - 1) / kTcMaxN : 0;
+    int tc_total;
+    const int tbase = block_excl_scan(ntc, sc, &tc_total);
+    if (tid < E)
+      for (int i = 0; i < ntc; ++i)
+        p.tc_entries[tbase + i] = make_int4(tid, excl + kTcMaxN * i, min(kTcMaxN, c - kTcMaxN * i), 0);
+    if (tid == 0) *p.n_tc_entries = tc_total;
+  }
+}
+
 __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
   const int S = p.T * p.k, E = p.E;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, NW = blockDim.x >> 5;
@@ -409,26 +434,7 @@ __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
     if (valid && lane == __ffs(peers) - 1) hist[w * E + e] += __popc(peers);
     __syncwarp();
   }
-  for (int i = tid; i < p.T; i += blockDim.x) p.row_token[S + i] = i;
-  // routed work entries: ceil(count / 8) per expert, expert-major
-  const int nch = (tid < E) ? (c + kTokTile - 1) / kTokTile : 0;
-  int n_total;
-  const int ebase = block_excl_scan(nch, sc, &n_total);
-  if (tid < E) {
-    const int off = excl;
-    for (int i = 0; i < nch; ++i)
-      p.entries[ebase + i] = make_int4(tid, off + kTokTile * i, min(kTokTile, c - kTokTile * i), 0);
-  }
-  if (tid == 0) *p.n_entries = n_total;
-  if (p.tc_entries) {
-    const int ntc = (tid < E) ? (c + kTcMaxN - 1) / kTcMaxN : 0;
-    int tc_total;
-    const int tbase = block_excl_scan(ntc, sc, &tc_total);
-    if (tid < E)
-      for (int i = 0; i < ntc; ++i)
-        p.tc_entries[tbase + i] = make_int4(tid, excl + kTcMaxN * i, min(kTcMaxN, c - kTcMaxN * i), 0);
-    if (tid == 0) *p.n_tc_entries = tc_total;
-  }
+  write_entries(p, c, excl, sc);
 }
 
 // slots of the few-token path (T * k at most)

@@ -103,7 +103,7 @@ template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stream_kernel(ExpertParams p) {
   const int y = blockIdx.y;
   if (MODE == 1 || y >= p.nsh) griddep_wait();
-  if (MODE == 0) griddep_launch();
+  griddep_launch();
   int expert, row, n;
   if (!get_entry(p, y, expert, row, n)) return;
   extern __shared__ __align__(16) uint8_t stream_smem_buf[];
@@ -261,12 +261,12 @@ bool gateup_smem_ok(const ExpertParams& p) {
   return p.fmt == FMT_NVFP4 && p.T <= kTokTile && gateup_nv_smem(p.H, p.T) <= kNvMaxDyn;
 }
 
-// Streamed GEMVs: NVFP4 for T > 8 (T <= 8 keeps the tile-pair path), FP6 for
-// gate/up at any T and for down at T > 8 (T <= 8 takes the fused down +
-// combine); within the dynamic shared-memory budget.
+// Streamed GEMVs: NVFP4 for T > 8 (T <= 8 keeps the tile-pair gate/up and
+// the fused down + combine), FP6 at every T; within the dynamic shared-memory
+// budget.
 constexpr int kStreamMaxDyn = 200 * 1024;
 bool stream_ok(const ExpertParams& p, int mode) {
-  if ((mode == 1 || p.fmt == FMT_NVFP4) && p.T <= kTokTile) return false;
+  if (p.fmt == FMT_NVFP4 && p.T <= kTokTile) return false;
   return stream_smem(p.fmt, mode == 0 ? 2 : 1, mode == 0 ? p.H : p.I, p.T, 2) <= kStreamMaxDyn;
 }
 

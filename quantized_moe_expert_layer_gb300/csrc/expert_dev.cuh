@@ -664,12 +664,15 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
   // The B rows first (one cp.async group), then the warp's first NS units.
   // Gate/up rows are tokens; with T <= 8 a row sits in slot = its token (an
   // entry may hold one token twice, e.g. from a given routing), else in slot
-  // = its row of the entry (n <= 8).  Down runs only for T > 8 (slot = row).
+  // = its row of the entry (n <= 8).  Down rows are rows of a, in slot = row;
+  // with T <= 8 (FP6 only) an entry of more rows than slots (a token that
+  // picked one expert twice) reads a from global memory instead.
   const bool shared_entry = MODE == 0 && expert == p.E;
   const bool by_token = MODE == 0 && p.T <= kTokTile;
+  const bool b_global = MODE == 1 && n > stream_rows(p.T);
   auto tok_of = [&](int r) { return shared_entry ? row - S + r : p.row_token[row + r]; };
   const int pieces = K / 8;  // 16-byte pieces of a row
-  for (int i = threadIdx.x; i < n * pieces; i += kThreads) {
+  for (int i = threadIdx.x; i < (b_global ? 0 : n) * pieces; i += kThreads) {
     const int r = i / pieces, c = i - r * pieces;
     const int tok = MODE == 0 ? tok_of(r) : 0;
     if (MODE == 0 && (unsigned)tok >= (unsigned)p.T) continue;
@@ -716,7 +719,9 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
         nv_units_mma<NT>(g, hh, st, xrow + 2 * 256 * hh, slot >= 0, false, acc);
       else
         fp6_units_mma<NT>(g, hh, st, [&](int col, uint32_t(&xb)[8]) {
-          if (slot >= 0) {
+          if (b_global) {
+            load_b(gi < n ? p.abuf + (size_t)(row + gi) * p.I : nullptr, 256 * hh + col, false, xb);
+          } else if (slot >= 0) {
             const uint32_t xa = xrow + 2 * (256 * hh + col);
             const uint4 q0 = lds128(xa), q1 = lds128(xa + 16);
             xb[0] = q0.x; xb[1] = q0.y; xb[2] = q0.z; xb[3] = q0.w;

@@ -267,13 +267,15 @@ bool gateup_smem_ok(const ExpertParams& p) {
 constexpr int kStreamMaxDyn = 200 * 1024;
 bool stream_ok(const ExpertParams& p, int mode) {
   if (p.fmt == FMT_NVFP4 && p.T <= kTokTile) return false;
-  return stream_smem(p.fmt, mode == 0 ? 2 : 1, mode == 0 ? p.H : p.I, p.T, 2) <= kStreamMaxDyn;
+  return stream_smem(p.fmt, 2, mode == 0 ? p.H : p.I, p.T, 2) <= kStreamMaxDyn;
 }
 
 template <int MODE>
 cudaError_t launch_stream(const ExpertParams& p, int grid_y, bool pdl, cudaStream_t st) {
-  const dim3 grid(((MODE == 0 ? p.I : p.H) / 16 + kWarps - 1) / kWarps, grid_y);
-  const size_t smem = stream_smem(p.fmt, MODE == 0 ? 2 : 1, MODE == 0 ? p.H : p.I, p.T, 2);
+  // a warp per gate/up tile pair (I/16 of them) or per two down tiles (H/32)
+  const int items = MODE == 0 ? p.I / 16 : p.H / 32;
+  const dim3 grid((items + kWarps - 1) / kWarps, grid_y);
+  const size_t smem = stream_smem(p.fmt, 2, MODE == 0 ? p.H : p.I, p.T, 2);
   if (p.fmt == FMT_NVFP4)
     return launch_k(stream_kernel<FMT_NVFP4, MODE>, grid, dim3(kThreads), smem, st, pdl, p);
   return launch_k(stream_kernel<FMT_FP6, MODE>, grid, dim3(kThreads), smem, st, pdl, p);

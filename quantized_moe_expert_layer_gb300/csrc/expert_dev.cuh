@@ -629,29 +629,30 @@ __device__ __forceinline__ void fp6_units_mma(const MatGeom& g, int hh, uint32_t
   }
 }
 
-// MODE 0: gate/up + SwiGLU of tile pairs group*kWarps + w into abuf;
-// MODE 1: down tiles group*kWarps + w into ybuf.  NS ring stages per warp.
-// smem: stream_smem bytes.
+// MODE 0: gate/up + SwiGLU of tile pair group*kWarps + w into abuf; MODE 1:
+// down tiles 2i and 2i + 1 (i = group*kWarps + w) into ybuf, the two tiles
+// sharing the warp's B fragments like a gate/up pair.  NS ring stages per
+// warp.  smem: stream_smem bytes (nt = 2).
 template <int FMT, int MODE, int NS = 2>
 __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, int row, int n,
                                             int group, uint8_t* smem) {
-  constexpr int NT = MODE == 0 ? 2 : 1;
+  constexpr int NT = 2;
   constexpr int SB = FMT == FMT_NVFP4 ? 2560 : 3200;  // stream_unit_bytes
   const int S = p.T * p.k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, t = lane & 3;
   const int K = MODE == 0 ? p.H : p.I;
   const MatGeom g = mat_geom(FMT, K);
   const int nh = n_halves(g), xs = stream_xstride(K);
-  const int idx = group * kWarps + warp;  // tile pair (gate/up) or tile (down)
-  const bool valid = idx < (MODE == 0 ? p.I / 16 : p.H / 16);
+  const int idx = group * kWarps + warp;  // tile pair (gate/up) or pair of down tiles
+  const bool valid = idx < (MODE == 0 ? p.I / 16 : p.H / 32);
   const uint8_t* eb = expert_base(p, expert);
   const uint8_t* tiles[2];
   if (MODE == 0) {
     tiles[0] = eb + (size_t)(2 * idx) * p.gu_tile_bytes;
     tiles[1] = eb + (size_t)(2 * idx + 1) * p.gu_tile_bytes;
   } else {
-    tiles[0] = eb + p.gu_bytes + (size_t)idx * p.dn_tile_bytes;
-    tiles[1] = tiles[0];
+    tiles[0] = eb + p.gu_bytes + (size_t)(2 * idx) * p.dn_tile_bytes;
+    tiles[1] = eb + p.gu_bytes + (size_t)(2 * idx + 1) * p.dn_tile_bytes;
   }
   auto copy_unit = [&](int hh, uint32_t dst) {
     if (FMT == FMT_NVFP4)
@@ -753,10 +754,12 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
   } else {
     const float ts = p.tscale[expert * 3 + 2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = 16 * idx + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
-      if (col < n) p.ybuf[(size_t)(row + col) * p.H + r] = ts * (acc[0][0][i] + acc[0][1][i]);
-    }
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = 16 * (2 * idx + q) + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
+        if (col < n) p.ybuf[(size_t)(row + col) * p.H + r] = ts * (acc[q][0][i] + acc[q][1][i]);
+      }
   }
 }
 

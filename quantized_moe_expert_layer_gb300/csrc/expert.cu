@@ -217,16 +217,36 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
   griddep_launch();
   DownPreload pre;
   bool have = false;
+  const bool preload = FMT == FMT_NVFP4 && p.I <= 512;
   if (!WAIT_FIRST) {
-    if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
+    if (preload) have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
     down_prefetch<FMT>(p, blockIdx.x);  // (the rest: into L2)
+  } else if (preload) {
+    // Speculative: the routing this grid reads is published by the gate/up
+    // grid long before that grid ends, so the entry read now is almost always
+    // the final one.  It is checked again after the wait; a stale or torn
+    // read only costs a reload (every address it forms is bounds-checked).
+    have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre, true);
   }
   griddep_wait();  // gate/up complete: abuf holds every row
   __shared__ float sg[kTokTile * kMaxK];
   __shared__ int si[kTokTile * kMaxK];
   if (WAIT_FIRST) {
-    // every entry's tile requested at once, then the combine's gates and rows
-    if (FMT == FMT_NVFP4 && p.I <= 512) have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
+    // the warp's entry read again now that it is final: the speculative
+    // tile stays if it is this entry's expert, else every entry's tile is
+    // requested at once; then the combine's gates and rows
+    if (preload) {
+      int e, r, n;
+      const bool ok = get_entry(p, threadIdx.x >> 5, e, r, n);
+      if (!ok) {
+        have = false;
+      } else if (have && e == pre.expert) {
+        pre.row = r;
+        pre.n = n;
+      } else {
+        have = down_preload(p, blockIdx.x, threadIdx.x >> 5, pre);
+      }
+    }
     for (int i = threadIdx.x; i < p.T * p.k; i += blockDim.x) {
       sg[i] = gates[i];
       si[i] = inv[i];

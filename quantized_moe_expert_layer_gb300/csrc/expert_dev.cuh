@@ -236,8 +236,10 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* const (&tile)[NT], cons
 
 // Entry y of the launch: the first p.nsh are the shared expert's token groups
 // (known without routing); the rest come from dispatch.
+// quiet: a read that may race with the writer (speculation): an entry that
+// fails the checks is skipped without setting the status word.
 __device__ __forceinline__ bool get_entry(const ExpertParams& p, int y, int& expert, int& row,
-                                          int& n) {
+                                          int& n, bool quiet = false) {
   const int S = p.T * p.k;
   if (y < p.nsh) {
     expert = p.E;
@@ -252,7 +254,7 @@ __device__ __forceinline__ bool get_entry(const ExpertParams& p, int y, int& exp
   row = e.y;
   n = e.z;
   if (expert < 0 || expert >= p.E || n < 1 || n > kTokTile || row < 0 || row + n > S) {
-    *p.status = -1;  // MOE_EINVAL: corrupt entry, skip it
+    if (!quiet) *p.status = -1;  // MOE_EINVAL: corrupt entry, skip it
     return false;
   }
   return true;
@@ -786,9 +788,10 @@ struct DownPreload {
   uint4 sv, cv[8];
 };
 
-__device__ __forceinline__ bool down_preload(const ExpertParams& p, int tile, int y, DownPreload& d) {
+__device__ __forceinline__ bool down_preload(const ExpertParams& p, int tile, int y, DownPreload& d,
+                                             bool quiet = false) {
   const int lane = threadIdx.x & 31;
-  if (!get_entry(p, y, d.expert, d.row, d.n)) return false;  // (reads the count and the entry together)
+  if (!get_entry(p, y, d.expert, d.row, d.n, quiet)) return false;  // (reads the count and the entry together)
   const uint8_t* b = expert_base(p, d.expert) + p.gu_bytes +
                      (size_t)tile * p.dn_tile_bytes + 16 * lane;
   const int nc = p.I / 64;

@@ -58,12 +58,22 @@ __global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_kernel(ExpertPa
 // asks L2 for its share of its expert's down matrix, so the down kernel reads
 // its weights from L2.  The shared expert's CTAs run at once.
 // PATH 0: registers (gateup_task); 1: the NVFP4 tile pair through shared
-// memory (gateup_task_nv); 2: streamed tile pairs (stream_task, FP6).
+// memory (gateup_task_nv); 3: the same for tile pairs blockIdx.x * tpc ...
+// + tpc - 1 one after another (when one pair per CTA would not fit the GPU at
+// once: a CTA then routes once for several tile pairs); 2: streamed tile
+// pairs (stream_task, FP6).
 template <int FMT, int PATH>
 __device__ __forceinline__ void gateup_any_task(const ExpertParams& p, int expert, int row, int n,
                                                 int tpc, uint8_t* smem, float* red) {
-  if constexpr (PATH == 1)
+  if constexpr (PATH == 1) {
     gateup_task_nv(p, expert, row, n, blockIdx.x, smem, red, true);
+  } else if constexpr (PATH == 3) {
+    const int pairs = p.I / 16, end = min(pairs, (int)(blockIdx.x + 1) * tpc);
+    for (int pair = blockIdx.x * tpc; pair < end; ++pair) {
+      gateup_task_nv(p, expert, row, n, pair, smem, red, true);
+      __syncthreads();  // warp 0 has read `red`, every warp is done with its stages
+    }
+  }
   else if constexpr (PATH == 2)
     stream_task<FMT, 0, 2>(p, expert, row, n, blockIdx.x, smem);
   else
@@ -71,7 +81,7 @@ __device__ __forceinline__ void gateup_any_task(const ExpertParams& p, int exper
 }
 
 template <int FMT, int PATH>
-__global__ void __launch_bounds__(kThreads, PATH == 1 ? 3 : 2) gateup_routed_kernel(ExpertParams p, RouteParams rp, int tpc) {
+__global__ void __launch_bounds__(kThreads, PATH == 1 || PATH == 3 ? 3 : 2) gateup_routed_kernel(ExpertParams p, RouteParams rp, int tpc) {
   const int y = blockIdx.y;
   __shared__ float red[kThreads * 8];
   extern __shared__ __align__(16) uint8_t gu_smem[];
@@ -210,7 +220,8 @@ constexpr int kDcMaxWarps = 12;
 // and the others requested from L2 before the wait.  Either way the next
 // kernel may start at once (it waits for this whole grid before it reads
 // anything this one writes).
-template <int FMT, bool WAIT_FIRST>
+// LONGK (NVFP4, I > 512): one-row entries stream their tile through a ring
+template <int FMT, bool WAIT_FIRST, bool LONGK = false>
 __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertParams p,
                                                                          const float* gates,
                                                                          const int* inv, float* out) {
@@ -256,15 +267,17 @@ __global__ void __launch_bounds__(kDcMaxWarps * 32) down_combine_kernel(ExpertPa
   }
   extern __shared__ float ys[];  // [rows x 16], then (FP6) the warps' unit rings
   const int rows = p.T * p.k + (p.shared ? p.T : 0);
-  down_combine_task<FMT>(p, blockIdx.x, gates, inv, out, ys, smem_u32(ys + rows * 16), pre, have);
+  down_combine_task<FMT, LONGK>(p, blockIdx.x, gates, inv, out, ys, smem_u32(ys + rows * 16), pre,
+                                have);
 }
 
 // ys (rows x 16 floats); the FP6 unit rings come on top (down_combine_ring)
 size_t down_combine_smem(int T, int k, int shared) {
   return ((size_t)T * k + (shared ? T : 0)) * 16 * sizeof(float);
 }
-size_t down_combine_ring(int fmt, int warps) {
-  return fmt == FMT_FP6 ? (size_t)warps * 2 * kDcFp6Stage : 0;
+size_t down_combine_ring(int fmt, int I, int warps) {
+  if (fmt == FMT_FP6) return (size_t)warps * 2 * kDcFp6Stage;
+  return I > 512 ? (size_t)warps * kDcNvStages * kDcNvStage : 0;
 }
 
 
@@ -346,8 +359,12 @@ cudaError_t launch_down_combine(const ExpertParams& p, const float* gates, const
   // one warp per work entry (the routed entries are at most T*k for T <= 8)
   int warps = p.nsh + (p.T * p.k < p.E ? p.T * p.k : p.E);
   if (warps > kDcMaxWarps) warps = kDcMaxWarps;
-  const size_t smem = down_combine_smem(p.T, p.k, p.shared) + down_combine_ring(p.fmt, warps);
+  const size_t smem = down_combine_smem(p.T, p.k, p.shared) + down_combine_ring(p.fmt, p.I, warps);
   const dim3 grid(p.H / 16), block(32 * warps);
+  if (p.fmt == FMT_NVFP4 && p.I > 512)
+    return wait_first
+               ? launch_k(down_combine_kernel<FMT_NVFP4, true, true>, grid, block, smem, st, pdl, p, gates, inv, out)
+               : launch_k(down_combine_kernel<FMT_NVFP4, false, true>, grid, block, smem, st, pdl, p, gates, inv, out);
   if (p.fmt == FMT_NVFP4)
     return wait_first
                ? launch_k(down_combine_kernel<FMT_NVFP4, true>, grid, block, smem, st, pdl, p, gates, inv, out)
@@ -362,9 +379,23 @@ bool small_route_ok(int T, int k) { return T <= kTokTile && T * k <= kSmallSlots
 cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, int grid_y,
                                  cudaStream_t st) {
   const int pairs = p.I / 16;
-  if (gateup_smem_ok(p))
-    return launch_k(gateup_routed_kernel<FMT_NVFP4, 1>, dim3(pairs, grid_y), dim3(kThreads),
-                    gateup_nv_smem(p.H, p.T), st, true, p, rp, 1);
+  if (gateup_smem_ok(p)) {
+    // tile pairs per CTA: enough that the grid fits the GPU at once (CTAs
+    // per SM from the shared memory a CTA holds: dynamic + 23.6 KB static)
+    const size_t dyn = gateup_nv_smem(p.H, p.T);
+    int per_sm = (int)((228u * 1024u) / (dyn + 25u * 1024u));
+    per_sm = per_sm < 1 ? 1 : (per_sm > 3 ? 3 : per_sm);
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long slots = (long)sms * per_sm, ctas = (long)pairs * grid_y;
+    if (ctas <= slots)
+      return launch_k(gateup_routed_kernel<FMT_NVFP4, 1>, dim3(pairs, grid_y), dim3(kThreads), dyn,
+                      st, true, p, rp, 1);
+    const int ppc = (int)((ctas + slots - 1) / slots);
+    return launch_k(gateup_routed_kernel<FMT_NVFP4, 3>, dim3((pairs + ppc - 1) / ppc, grid_y),
+                    dim3(kThreads), dyn, st, true, p, rp, ppc);
+  }
   if (p.fmt == FMT_FP6 && stream_ok(p, 0))
     return launch_k(gateup_routed_kernel<FMT_FP6, 2>, dim3((pairs + kWarps - 1) / kWarps, grid_y),
                     dim3(kThreads), stream_smem(p.fmt, 2, p.H, p.T, 2), st, true, p, rp, 1);
@@ -381,12 +412,21 @@ cudaError_t expert_kernels_init() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_NVFP4, 1>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kNvMaxDyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_NVFP4, 3>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kNvMaxDyn);
   // (the routed kernel also holds 23.6 KB of static shared memory)
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_FP6, 2>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
 
-  if (e == cudaSuccess)  // ys (<= 48 KB) and 12 warps' FP6 rings
+  if (e == cudaSuccess)  // ys (<= 48 KB) and 12 warps' rings
+    e = cudaFuncSetAttribute(down_combine_kernel<FMT_NVFP4, true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(down_combine_kernel<FMT_NVFP4, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+  if (e == cudaSuccess)
     e = cudaFuncSetAttribute(down_combine_kernel<FMT_FP6, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
   if (e == cudaSuccess)

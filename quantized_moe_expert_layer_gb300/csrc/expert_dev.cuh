@@ -458,7 +458,7 @@ __device__ __forceinline__ void nv_units_mma(const MatGeom& g, int hh, uint32_t 
 }
 
 // Tile pair `pair` of `expert` for the n tokens of rows row..row+n-1, T <= 8.
-// smem: gateup_nv_smem(H, T) bytes (16-byte aligned); red: kThreads x 8 floats.  prefetch_down: also ask L2 for this CTA's share (1/gridDim.x) of
+// smem: gateup_nv_smem(H, T) bytes (16-byte aligned); red: kThreads x 8 floats.  prefetch_down: also ask L2 for this tile pair's share (1/(I/16)) of
 // the expert's down matrix, for a down kernel that starts after this one.
 __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert, int row, int n,
                                                int pair, uint8_t* smem, float* red,
@@ -501,7 +501,8 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
   cp_async_wait<0>();
   if (prefetch_down) {
     const size_t len = (size_t)(p.H / 16) * p.dn_tile_bytes;
-    const size_t b0 = len * pair / gridDim.x, b1 = len * (pair + 1) / gridDim.x;
+    const size_t npairs = (size_t)(p.I / 16);
+    const size_t b0 = len * pair / npairs, b1 = len * (pair + 1) / npairs;
     const uint8_t* dn = eb + p.gu_bytes;
     for (size_t o = (b0 & ~(size_t)127) + 128 * threadIdx.x; o < b1; o += 128 * kThreads)
       prefetch_l2(dn + o);
@@ -841,9 +842,12 @@ __device__ __forceinline__ void down_preloaded_mma(const ExpertParams& p, const 
 // into ys [rows x 16] (shared memory), then out[:, tile] = sum_j g_j y_j + y_s
 // in j order (the same fmaf chain as combine_kernel).  `pre`: the warp's first
 // entry, preloaded (when have_pre).
-// FP6: `ring` is a shared-memory ring of 2 stages of kDcFp6Stage bytes per warp.
+// FP6: `ring` is a shared-memory ring of 2 stages of kDcFp6Stage bytes per
+// warp; NVFP4 with I > 512: kDcNvStages stages of kDcNvStage bytes.
 constexpr int kDcFp6Stage = 3200 + 512;  // a unit's weights and one row of a over its columns
-template <int FMT>
+constexpr int kDcNvStages = 4;
+constexpr int kDcNvStage = 2560 + 512;
+template <int FMT, bool LONGK = false>
 __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int tile, const float* gates,
                                                   const int* inv, float* out, float* ys,
                                                   uint32_t ring, const DownPreload& pre,
@@ -907,6 +911,35 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
         }, a2);
         __syncwarp();
         if (hh + 2 < nh) copy_unit(hh + 2, st);
+        cp_async_commit();
+      }
+      cp_async_wait<0>();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[0][i] = a2[0][0][i] + a2[0][1][i];
+    } else if (LONGK && n == 1) {
+      // NVFP4 with a long K (the fused decode down of wide experts), one row:
+      // the tile's units and the row of a through this warp's kDcNvStages-
+      // stage cp.async ring, several units in flight instead of one at a time
+      const uint16_t* arow = p.abuf + (size_t)row * p.I;
+      const int nh = n_halves(g);
+      const uint32_t wr = ring + warp * kDcNvStages * kDcNvStage;
+      auto copy_unit = [&](int hh, uint32_t dst) {
+        nv_units_copy<1>(tiles, g, hh, dst);
+        if (256 * hh + 8 * lane < p.I) cp_async16(dst + 2560 + 16 * lane, arow + 256 * hh + 8 * lane);
+      };
+#pragma unroll
+      for (int u = 0; u < kDcNvStages; ++u) {
+        if (u < nh) copy_unit(u, wr + u * kDcNvStage);
+        cp_async_commit();
+      }
+      float a2[1][2][4] = {};
+      for (int hh = 0; hh < nh; ++hh) {
+        const uint32_t st = wr + (hh % kDcNvStages) * kDcNvStage;
+        cp_async_wait<kDcNvStages - 1>();
+        __syncwarp();
+        nv_units_mma<1>(g, hh, st, st + 2560, gi == 0, false, a2);
+        __syncwarp();
+        if (hh + kDcNvStages < nh) copy_unit(hh + kDcNvStages, st);
         cp_async_commit();
       }
       cp_async_wait<0>();

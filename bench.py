@@ -59,6 +59,25 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x, world):
+    """The largest of the ranks' values of x (x itself on one rank): the job's
+    time is its slowest rank's."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, tokens, layers, steps, seconds):
+    """Whole-job throughput: every rank processes `steps` steps of `tokens`
+    tokens through `layers` layer instances in (at most) `seconds`."""
+    return world * tokens * layers * steps / seconds
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
             int(os.environ.get("WORLD_SIZE", 1)))
@@ -406,12 +425,8 @@ def run_ours(args, w):
     clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T * Ln * args.steps / (ms / 1e3)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    value = job_rate(world, T, Ln, args.steps, ms / 1e3)
 
     # dominant kernel, timed alone over the L layers (graph of back-to-back
     # launches, launch gaps included): gate/up + SwiGLU, the tcgen05 GEMM for
@@ -519,12 +534,8 @@ def run_ours(args, w):
     for _ in range(k_e2e):
         for L, oh in zip(layers, ohs):
             L.forward_host(xh, oh, stream=s)
-    e2e_dt = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_dt], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_dt = float(t.item())
-    e2e = {"value": world * T * Ln * k_e2e / e2e_dt, "unit": UNIT,
+    e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": job_rate(world, T, Ln, k_e2e, e2e_dt), "unit": UNIT,
            "h2d_bytes_per_step": Ln * T * w.H * 2, "d2h_bytes_per_step": Ln * T * w.H * 4,
            "call": "moe_forward_host per layer (pinned host buffers, synchronous)"}
 

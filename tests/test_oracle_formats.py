@@ -5,18 +5,30 @@ code tables typed in as published literals, torch's float8 conversions
 (library routines), an independent binade-wise round-half-even built on
 numpy, and the invariants the format definitions fix.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _table(name):
+    """Element magnitudes of the positive codes, as published (tests/golden, cited there)."""
+    vals = []
+    for line in open(os.path.join(GOLDEN, name)):
+        if not line.startswith("#"):
+            vals += [float(v) for v in line.split()]
+    return vals
+
+
 # OCP Microscaling Formats (MX) v1.0: element magnitudes of the positive codes.
-E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
-E2M3_TABLE = [0.0, 0.125, 0.25, 0.375, 0.5, 0.625, 0.75, 0.875,
-              1.0, 1.125, 1.25, 1.375, 1.5, 1.625, 1.75, 1.875,
-              2.0, 2.25, 2.5, 2.75, 3.0, 3.25, 3.5, 3.75,
-              4.0, 4.5, 5.0, 5.5, 6.0, 6.5, 7.0, 7.5]
+E2M1_TABLE = _table("e2m1_magnitudes.txt")
+E2M3_TABLE = _table("e2m3_magnitudes.txt")
+assert len(E2M1_TABLE) == 8 and len(E2M3_TABLE) == 32
 
 
 def test_e2m1_table_exhaustive():

@@ -103,13 +103,16 @@ def test_mirror_dequant_bit_exact(fmt):
         L.close()
 
 
-@pytest.mark.parametrize("T", [13, 300])
-def test_small_layer_mirror_against_oracle(T):
-    """A small layer with most experts in the host mirror, at a token count of
-    the grouped-GEMV path (13) and one that takes the tensor-core path while
-    every expert is in HBM (300) but the mma.sync path with any in the mirror;
-    both against the oracle."""
-    w = gen.Workload("place-small", 256, 128, 8, 2, 1, T, 1, "normal", 0.0, 0.1, 5)
+@pytest.mark.parametrize("fmt", [1, 2, 3])
+@pytest.mark.parametrize("T", [1, 13, 300])
+def test_small_layer_mirror_against_oracle(fmt, T):
+    """A small layer with most experts in the host mirror, in every format, at
+    the self-routed decode (1), the streamed small-N path (13) and a token
+    count that takes the tensor-core path while every expert is in HBM (300,
+    NVFP4 / MXFP4) but the streamed path with any in the mirror; against the
+    oracle, then again with every expert back in HBM."""
+    H, I = (384, 256) if fmt == 2 else (256, 128)
+    w = gen.Workload("place-small", H, I, 8, 2, 1, T, fmt, "normal", 0.0, 0.1, 5)
     mask = np.array([0, 0, 1, 0, 0, 0, 1, 0, 0], bool)
     L = build_layer(w, T_max=T, in_hbm=mask)
     try:

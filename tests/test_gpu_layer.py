@@ -214,14 +214,27 @@ def test_zero_gates_and_linearity_with_given_routing():
 
 
 def test_forward_host_matches_device_forward():
-    w = gen.get_workload(0)
-    L = layer(w)
-    x_np = gen.x_tokens(w)
-    dev = run_gpu(L, x_np, w, want_routing=False)["out"]
-    xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
-    oh = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
-    L.forward_host(xh, oh)
-    assert np.array_equal(oh.numpy(), dev)
+    """The host-buffer call gives the device forward's bits: new contents of
+    the same buffers, another token count, other buffers, both router modes."""
+    w = dataclasses.replace(gen.get_workload(0), bias="normal", bias_scale=0.1, seed=11)
+    L = build_layer(w, T_max=16)
+    try:
+        xh = torch.empty((16, w.H), dtype=torch.int16).pin_memory()
+        oh = torch.empty((16, w.H), dtype=torch.float32).pin_memory()
+        for T, first, mode in [(4, 0, 0), (4, 4, 0), (13, 0, 0), (13, 3, 1), (4, 8, 1)]:
+            L.set_router_mode(mode)
+            x_np = gen.x_tokens(w, T, first=first)
+            dev = run_gpu(L, x_np, w, want_routing=False)["out"]
+            xh[:T].copy_(torch.from_numpy(x_np.view(np.int16)))
+            L.forward_host(xh, oh[:T], T=T)
+            assert np.array_equal(oh[:T].numpy(), dev), (T, first, mode)
+        other = torch.from_numpy(gen.x_tokens(w, 4, first=2).view(np.int16)).pin_memory()
+        o2 = torch.empty((4, w.H), dtype=torch.float32).pin_memory()
+        L.forward_host(other, o2)
+        dev = run_gpu(L, gen.x_tokens(w, 4, first=2), w, want_routing=False)["out"]
+        assert np.array_equal(o2.numpy(), dev)
+    finally:
+        L.close()
 
 
 def test_error_paths():

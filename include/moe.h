@@ -201,9 +201,11 @@ int moe_quantize_mxfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t*
  * x and out must be 16-byte aligned. */
 int moe_forward(moe_layer* L, const uint16_t* x, int T, float* out, void* stream);
 
-/* moe_forward with host buffers: copies x (T x H bf16) to the workspace, runs
- * the layer, copies out (T x H fp32) back and synchronises `stream`.  Pinned
- * host memory gives the fastest copies. */
+/* moe_forward with host buffers x (T x H bf16) and out (T x H fp32); returns
+ * once `stream` has finished.  Page-locked, device-mapped buffers
+ * (cudaHostAlloc / cudaHostRegister, 16-byte aligned) are read and written by
+ * the kernels in place over the CPU-GPU link; any other host memory is copied
+ * through the layer's staging buffers. */
 int moe_forward_host(moe_layer* L, const uint16_t* x_host, int T, float* out_host, void* stream);
 
 /* The layer with the routing given instead of computed: idx [T x k] expert ids

@@ -702,6 +702,21 @@ int moe_forward_host(moe_layer* L, const uint16_t* x_host, int T, float* out_hos
   if (rc) return rc;
   DeviceGuard dg(L->device);
   cudaStream_t st = (cudaStream_t)stream;
+  // Page-locked, device-mapped buffers (cudaHostAlloc, cudaHostRegister): the
+  // kernels read x and write out through the CPU-GPU link themselves, with no
+  // separate copies.  Other host memory goes through the staging buffers.
+  cudaPointerAttributes ax{}, ao{};
+  if (cudaPointerGetAttributes(&ax, x_host) == cudaSuccess && ax.type == cudaMemoryTypeHost &&
+      ax.devicePointer && cudaPointerGetAttributes(&ao, out_host) == cudaSuccess &&
+      ao.type == cudaMemoryTypeHost && ao.devicePointer &&
+      !(((uintptr_t)ax.devicePointer | (uintptr_t)ao.devicePointer) & 15u)) {
+    rc = forward_impl(L, static_cast<const uint16_t*>(ax.devicePointer), T,
+                      static_cast<float*>(ao.devicePointer), st);
+    if (rc) return rc;
+    CK("moe_forward_host: synchronize", cudaStreamSynchronize(st));
+    return MOE_OK;
+  }
+  cudaGetLastError();  // (pageable memory: the attribute query's status is not an error here)
   CK("moe_forward_host: copy x", cudaMemcpyAsync(L->x_stage, x_host, (size_t)T * L->H * 2,
                                                  cudaMemcpyHostToDevice, st));
   rc = forward_impl(L, L->x_stage, T, L->out_stage, st);

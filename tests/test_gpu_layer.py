@@ -214,8 +214,10 @@ def test_zero_gates_and_linearity_with_given_routing():
 
 
 def test_forward_host_matches_device_forward():
-    """The host-buffer call gives the device forward's bits: new contents of
-    the same buffers, another token count, other buffers, both router modes."""
+    """The host-buffer call gives the device forward's bits: pinned buffers
+    (read and written by the kernels in place) with new contents, another
+    token count, other buffers, both router modes; and pageable buffers (the
+    staged copies)."""
     w = dataclasses.replace(gen.get_workload(0), bias="normal", bias_scale=0.1, seed=11)
     L = build_layer(w, T_max=16)
     try:
@@ -233,6 +235,11 @@ def test_forward_host_matches_device_forward():
         L.forward_host(other, o2)
         dev = run_gpu(L, gen.x_tokens(w, 4, first=2), w, want_routing=False)["out"]
         assert np.array_equal(o2.numpy(), dev)
+        xp = np.ascontiguousarray(gen.x_tokens(w, 5, first=1)).view(np.int16)  # pageable
+        op = np.zeros((5, w.H), np.float32)
+        L.forward_host(xp, op)
+        dev = run_gpu(L, gen.x_tokens(w, 5, first=1), w, want_routing=False)["out"]
+        assert np.array_equal(op, dev)
     finally:
         L.close()
 

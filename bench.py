@@ -537,7 +537,8 @@ def run_ours(args, w):
     e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
     e2e = {"value": job_rate(world, T, Ln, k_e2e, e2e_dt), "unit": UNIT,
            "h2d_bytes_per_step": Ln * T * w.H * 2, "d2h_bytes_per_step": Ln * T * w.H * 4,
-           "call": "moe_forward_host per layer (pinned host buffers, synchronous)"}
+           "call": "moe_forward_host per layer (pinned host buffers, read and written in place "
+                   "by the kernels over the CPU-GPU link; synchronous)"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,

@@ -1,6 +1,6 @@
 // Asynchronous-copy and mbarrier helpers (sm_103a): shared-memory mbarriers
-// with bounded waits, cp.async (16-byte, per thread) and cp.async.bulk (one
-// thread moves a contiguous range, its bytes counted on an mbarrier).
+// with bounded waits (the tensor-core kernels' TMA and MMA hand-offs) and
+// cp.async (16 bytes, per thread).
 #pragma once
 
 #include <stdint.h>
@@ -98,31 +98,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// ---------------------------------------------------------------- bulk copies
-// L2 policy for data read once (streamed weights): evict first.
-__device__ __forceinline__ uint64_t l2_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-// Global -> this CTA's shared memory, `bytes` (a multiple of 16, both
-// addresses 16-byte aligned) counted on `bar`'s transaction count.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
-      "%2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
 }
 
 }  // namespace

@@ -106,9 +106,9 @@ __global__ void __launch_bounds__(kThreads, PATH == 1 || PATH == 3 ? 3 : 2) gate
   if (pub) publish_counts(rp, rt);
 }
 
-// ---------------------------------------------------------------- streamed NVFP4 GEMVs, 8 < T
-// MODE 0: gate/up + SwiGLU (shared-expert entries run ahead of the router);
-// MODE 1: down.  See stream_task.
+// ---------------------------------------------------------------- streamed GEMVs
+// NVFP4 for 8 < T, FP6 at every T.  MODE 0: gate/up + SwiGLU (shared-expert
+// entries run ahead of the router); MODE 1: down.  See stream_task.
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stream_kernel(ExpertParams p) {
   const int y = blockIdx.y;
@@ -284,12 +284,14 @@ size_t down_combine_ring(int fmt, int I, int warps) {
 
 }  // namespace
 
-// Dynamic shared memory the NVFP4 gate/up kernels may use (set in
+// Dynamic shared memory the NVFP4 tile-pair gate/up kernels may use (set in
 // expert_kernels_init); larger shapes take the register kernels.
 constexpr int kNvMaxDyn = 160 * 1024;
 
-// (T <= 8 only: for larger batches, entries of up to 8 tokens stream faster
-// through the register kernels, which keep two units per warp in flight)
+// The tile-pair task (one pair per CTA, warps splitting K) for T <= 8 only:
+// for larger batches it would stage every entry's token rows once per tile
+// pair, and the streamed kernels (a warp per pair over the whole K, rows
+// staged once per CTA) take over.
 bool gateup_smem_ok(const ExpertParams& p) {
   return p.fmt == FMT_NVFP4 && p.T <= kTokTile && gateup_nv_smem(p.H, p.T) <= kNvMaxDyn;
 }

@@ -177,12 +177,13 @@ cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream
   return cudaGetLastError();
 }
 
-// K slices of the router: about 128 CTAs for a decode step (few slices keep the
-// top-k's partial-sum reads short), about 1024 for larger T (each warp then
-// has one or two 64-column chunks instead of a serial chain of them)
+// K slices of the router: about 128 CTAs up to 16 tokens (their top-k reads
+// the slices with a warp per token, a serial loop over them), about 1024 above
+// (the CTA-per-token top-k requests every slice at once; each router warp
+// then has one or two 64-column chunks instead of a serial chain of them)
 int router_ksplit(int T, int H, int E) {
   const int tiles = (E + 15) / 16, groups = (T + kTokTile - 1) / kTokTile;
-  const int C = H / 64, target = T <= kTokTile ? 128 : 1024;
+  const int C = H / 64, target = T <= 2 * kTokTile ? 128 : 1024;
   int ks = (target + tiles * groups - 1) / (tiles * groups);
   if (ks > 8) ks = 8;
   if (ks > C) ks = C;

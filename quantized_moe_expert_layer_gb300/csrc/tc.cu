@@ -16,8 +16,8 @@
 // apply the fp32 tensor scale and SwiGLU (gate/up) or write y rows (down).
 //
 // The weights stay the M operand and the token count the N operand (N is 80 on
-// average for 4096 tokens over 512 experts), as the survey of the prompt paths
-// suggests: experts with few tokens keep the decoded weights as the wide side.
+// average for 4096 tokens over 512 experts): an expert with few tokens keeps
+// its decoded weights on the 128-row side of the MMA.
 // Every wait is bounded: on a timeout the kernel records MOE_ETIMEOUT in the
 // status word, stops issuing work, waits (bounded) for its MMAs and copies,
 // frees its TMEM and returns.

@@ -50,7 +50,7 @@ class _Layer(ctypes.Structure):
                 ("codes", ctypes.POINTER(ctypes.c_void_p)),
                 ("scales", ctypes.POINTER(ctypes.c_void_p)),
                 ("tscales", ctypes.c_void_p), ("router", ctypes.c_void_p),
-                ("bias", ctypes.c_void_p)]
+                ("bias", ctypes.c_void_p), ("act_fp4", ctypes.c_int)]
 
 
 def lib():
@@ -186,8 +186,11 @@ class Layer:
     shared expert; matrices a call does not touch may be absent.
     """
 
-    def __init__(self, fmt, H, I, E, k, shared, router_bf16, bias=None):
+    def __init__(self, fmt, H, I, E, k, shared, router_bf16, bias=None, act_fp4=False):
+        """act_fp4: W4A4 (R20), every product's activations quantised to NVFP4
+        per row (x per token, a per token and expert) before it."""
         self.fmt, self.H, self.I, self.E, self.k, self.shared = fmt, H, I, E, k, int(bool(shared))
+        self.act_fp4 = bool(act_fp4)
         self.router = np.ascontiguousarray(router_bf16, dtype=np.uint16)
         self.bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
         self.mats = {}
@@ -234,7 +237,7 @@ class Layer:
                     ctypes.cast(codes, ctypes.POINTER(ctypes.c_void_p)),
                     ctypes.cast(scales, ctypes.POINTER(ctypes.c_void_p)),
                     ts.ctypes.data, self.router.ctypes.data,
-                    None if self.bias is None else self.bias.ctypes.data)
+                    None if self.bias is None else self.bias.ctypes.data, int(self.act_fp4))
         return st, (codes, scales, ts)  # keep the arrays alive with the struct
 
     def _need(self, experts):

@@ -40,6 +40,11 @@
 //   R11 output = fp32(sum_j g_j * y_j + y_shared), summed in fp64.
 //   R19 optional sigmoid router: s_e = sigmoid(x . Wr_e), top-k by s_e + b_e (the
 //      bias selects only), gates s_j / sum of the picked s.
+//   R20 W4A4 (optional, act_fp4): the activations of each product are quantised
+//      to NVFP4 too, per row with the weight recipe (R1, R3, R4, R6): x of a
+//      token before gate/up, and a = silu(g) * u, rounded to fp32, per
+//      (token, expert) row before down; the products then take the dequantised
+//      values.
 //   R17 MXFP4 (OCP MX v1.0 FP4): blocks of 32 along K share an e8m0 scale
 //      X = 2^(floor(log2 amax_b) - 2) (2 = the largest e2m1 exponent), clamped
 //      to [2^-127, 2^127]; q = e2m1_rne(w / X), saturating at 6; an all-zero
@@ -273,6 +278,7 @@ struct orc_layer {
   const float* tscales;          // NVFP4 tensor scales [(E + shared) * 3]; unused otherwise
   const uint16_t* router;        // bf16 bits [E x H]
   const float* bias;             // fp32 [E] or null
+  int act_fp4;                   // 1: W4A4, activations quantised to NVFP4 per row (R20)
 };
 
 }  // extern "C"
@@ -304,11 +310,25 @@ void dequant_row(const orc_layer& L, int expert, int matrix, int row, int K, flo
   }
 }
 
+// R20: one activation row (fp32 values) through the NVFP4 recipe and back.
+void act_fp4_row(std::vector<double>& v) {
+  const int K = (int)v.size();
+  std::vector<float> f((size_t)K), back((size_t)K);
+  std::vector<uint8_t> codes((size_t)K / 2), scales((size_t)K / 16);
+  for (int i = 0; i < K; ++i) f[i] = (float)v[i];
+  float ts = 0.f;
+  orc_quantize_nvfp4(f.data(), 1, K, codes.data(), scales.data(), &ts);
+  orc_dequant_nvfp4(codes.data(), scales.data(), ts, 1, K, back.data());
+  for (int i = 0; i < K; ++i) v[i] = (double)back[i];
+}
+
 // y[h] = sum_i Wd'[h,i] * a_i with a_i = silu(g_i) * u_i, g = Wg' x, u = Wu' x (fp64).
-void expert_ffn(const orc_layer& L, int expert, const double* x, double* y) {
+void expert_ffn(const orc_layer& L, int expert, const double* x_in, double* y) {
   const int H = L.H, I = L.I;
   std::vector<float> row((size_t)std::max(H, I));
-  std::vector<double> a((size_t)I);
+  std::vector<double> a((size_t)I), xq(x_in, x_in + H);
+  if (L.act_fp4) act_fp4_row(xq);
+  const double* x = xq.data();
   for (int i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
     dequant_row(L, expert, 0, i, H, row.data());
@@ -318,6 +338,7 @@ void expert_ffn(const orc_layer& L, int expert, const double* x, double* y) {
     double silu = g / (1.0 + std::exp(-g));
     a[i] = silu * u;
   }
+  if (L.act_fp4) act_fp4_row(a);
   for (int h = 0; h < H; ++h) {
     dequant_row(L, expert, 2, h, I, row.data());
     double acc = 0.0;

@@ -205,3 +205,51 @@ def test_sigmoid_router_bias_selects_but_does_not_weight():
     assert list(idx[0]) == [2, 0]
     s0, s2 = 1 / (1 + np.exp(-3.0)), 1 / (1 + np.exp(4.0))
     assert np.allclose(gates[0], [s2 / (s0 + s2), s0 / (s0 + s2)], rtol=1e-6)
+
+
+# ---------------------------------------------------------------- W4A4 (R20)
+def _fp4_rows(v):
+    """Rows of v through the NVFP4 recipe and back, with the oracle's (pinned)
+    quantiser and dequantiser, one row at a time."""
+    v32 = np.ascontiguousarray(v, np.float32)
+    out = np.empty_like(v32)
+    for r in range(v32.shape[0]):
+        c, s, ts = oracle.quantize_nvfp4(v32[r:r + 1])
+        out[r] = oracle.dequant_nvfp4(c, s, ts, 1, v32.shape[1])[0]
+    return out.astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt", [oracle.FMT_NVFP4, oracle.FMT_MXFP4, oracle.FMT_FP6])
+def test_w4a4_expert_ffn_matches_numpy_composition(fmt):
+    """The W4A4 expert (R20) against numpy over the oracle's pinned quantiser:
+    x per token through NVFP4, the dense gate / up, a rounded to fp32 and per
+    row through NVFP4, then the down projection."""
+    L, x = _tiny_layer(fmt=fmt)
+    L.act_fp4 = True
+    xq = _fp4_rows(_bf16_vals(x))
+    for e in (0, L.E):
+        Wg, Wu, Wd = (L.dequant(e, m).astype(np.float64) for m in range(3))
+        a = (_silu(xq @ Wg.T) * (xq @ Wu.T)).astype(np.float32)
+        ref = _fp4_rows(a) @ Wd.T
+        got = L.expert_ffn(e, x)
+        assert np.allclose(got, ref, rtol=1e-6, atol=1e-9), np.abs(got - ref).max()
+
+
+def test_w4a4_layer_differs_from_w4a16_by_activation_rounding_only():
+    """The whole W4A4 layer: routing unchanged (the router keeps bf16 x), the
+    output off the W4A16 one by the activation rounding (a few per cent for
+    Gaussian activations, never zero), and exactly zero with zero down
+    weights and no shared expert."""
+    L, x = _tiny_layer(E=8, k=3, shared=1, seed=2)
+    lg16, idx16, g16, out16 = L.forward(x)
+    L.act_fp4 = True
+    lg4, idx4, g4, out4 = L.forward(x)
+    assert np.array_equal(lg16, lg4) and np.array_equal(idx16, idx4) and np.array_equal(g16, g4)
+    rel = np.linalg.norm(out4 - out16, axis=1) / np.linalg.norm(out16, axis=1)
+    assert np.all(rel > 1e-4) and np.all(rel < 0.3), rel
+    # zero down weights: both give exactly zero (no shared expert)
+    Z, xz = _tiny_layer(E=4, k=1, shared=0, seed=3)
+    for e in range(4):
+        Z.set_matrix(e, 2, np.zeros_like(Z.mats[(e, 2)][0]), np.zeros_like(Z.mats[(e, 2)][1]), 1.0)
+    Z.act_fp4 = True
+    assert np.all(Z.forward(xz)[3] == 0.0)

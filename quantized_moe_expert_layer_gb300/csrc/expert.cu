@@ -422,18 +422,21 @@ cudaError_t expert_kernels_init() {
     e = cudaFuncSetAttribute(gateup_routed_kernel<FMT_FP6, 2>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);
 
-  if (e == cudaSuccess)  // ys (<= 48 KB) and 12 warps' rings
+  // ys (at most 48 KB: down_combine_ok) and up to kDcMaxWarps warps' rings
+  // (12 x 4 x 3072 bytes NVFP4 with I > 512, 12 x 2 x 3712 FP6): 195 KB at most
+  constexpr int kDcMaxDyn = 200 * 1024;
+  if (e == cudaSuccess)
     e = cudaFuncSetAttribute(down_combine_kernel<FMT_NVFP4, true, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDcMaxDyn);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(down_combine_kernel<FMT_NVFP4, false, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDcMaxDyn);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(down_combine_kernel<FMT_FP6, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDcMaxDyn);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(down_combine_kernel<FMT_FP6, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDcMaxDyn);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(stream_kernel<FMT_NVFP4, 0>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamMaxDyn);

@@ -147,12 +147,25 @@ def test_tiny_mxfp4_workload():
 
 
 def test_deepseek_shape_mxfp4_decode_full_size():
+    """The wide-expert decode (128 tile pairs an expert): more CTAs than fit the
+    GPU at once, so a routed CTA takes several tile pairs in turn; T = 1 and a
+    batch of 8 against the oracle, and for T = 3 the self-routed kernel gives
+    the bits of the explicitly dispatched one (one tile pair per CTA)."""
     w = gen.get_workload(6)
     L = build_layer(w, T_max=8)
     try:
         assert L.launches(1) == 3
         rel, ties = compare_layer(w, L, gen.x_tokens(w))
         print(f"decode mxfp4 (H 4096, I 2048, E 256, k 6): rel-L2 {rel:.2e}, near ties {ties}")
+        rel8, _ = compare_layer(w, L, gen.x_tokens(w, 8))
+        print(f"the same, 8 tokens: rel-L2 {rel8:.2e}")
+        x_np = gen.x_tokens(w, 3, first=5)
+        a = run_gpu(L, x_np, w)
+        out = torch.empty((3, w.H), device="cuda")
+        L.forward_routed(to_dev_bf16(x_np), torch.from_numpy(a["idx"]).cuda(),
+                         torch.from_numpy(a["gates"]).cuda(), out)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), a["out"])
     finally:
         L.close()
 

@@ -22,8 +22,8 @@
  *   - the library owns the packed weights, router copy and workspace of a layer;
  *   - one layer is used from one stream at a time (its workspace is shared).
  * Dimensions: H hidden size, I expert intermediate size, E routed experts,
- * k experts per token, T tokens.  H and I are multiples of 64 (NVFP4) or of
- * 128 (FP6); 1 <= E <= 1024; 1 <= k <= min(E, 32).
+ * k experts per token, T tokens.  H and I are multiples of 64 (NVFP4, MXFP4)
+ * or of 128 (FP6), at most 65536; 1 <= E <= 1024; 1 <= k <= min(E, 32).
  */
 #ifndef MOE_H
 #define MOE_H

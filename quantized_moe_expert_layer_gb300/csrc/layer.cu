@@ -338,6 +338,8 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   if (H <= 0 || I <= 0 || H % mult || I % mult)
     return fail(MOE_EINVAL, "moe_layer_create: H=%d and I=%d must be positive multiples of %d", H,
                 I, mult);
+  if (H > 65536 || I > 65536)
+    return fail(MOE_EINVAL, "moe_layer_create: H=%d and I=%d must be at most 65536", H, I);
   if (E < 1 || E > kMaxE) return fail(MOE_EINVAL, "moe_layer_create: E=%d not in [1, %d]", E, kMaxE);
   if (k < 1 || k > E || k > kMaxK)
     return fail(MOE_EINVAL, "moe_layer_create: k=%d not in [1, min(E, %d)]", k, kMaxK);

@@ -187,6 +187,10 @@ int router_ksplit(int T, int H, int E) {
   int ks = (target + tiles * groups - 1) / (tiles * groups);
   if (ks > 8) ks = 8;
   if (ks > C) ks = C;
+  // a slice's 8 staged token rows must fit the kernel's shared memory
+  // (launch_router: 8 x (slice + 8) bf16 + 4 KB <= 200 KB): at most 12288 columns
+  const int min_ks = (H + 12287) / 12288;
+  if (ks < min_ks) ks = min_ks;
   if (ks < 1) ks = 1;
   return ks;
 }

@@ -37,5 +37,9 @@ def test_errors_without_a_layer_are_reported():
     assert rc == moe.EINVAL and b"multiples" in lib.moe_last_error()
     rc = lib.moe_layer_create(1, 256, 128, 8, 9, 0, ctypes.byref(out))
     assert rc == moe.EINVAL
+    rc = lib.moe_layer_create(1, 65536 + 64, 128, 8, 2, 0, ctypes.byref(out))
+    assert rc == moe.EINVAL and b"at most" in lib.moe_last_error()
     assert lib.moe_forward(None, None, 1, None, None) == moe.EINVAL
+    assert lib.moe_place_experts(None, None) == moe.EINVAL
+    assert lib.moe_layer_placement(None, None, None, None) == moe.EINVAL
     assert lib.moe_layer_reserve(None, 4) == moe.EINVAL

@@ -1,18 +1,23 @@
 #!/usr/bin/env python3
 """Benchmark of the quantized MoE expert layer on GB300.
 
-Metric: routed tokens/s per MoE layer (T / time per layer forward), on the
-decode workload H=2048, I=512, E=512, top-10 + 1 shared expert, NVFP4
-experts, T=1 token per step.  A step passes the token through a stack of L
-distinct layer instances (default 32; each its own weights, so the 32 x 21.6
-MB touched per step are far larger than the 129 MB L2), captured once as a
+Metric: routed tokens/s per MoE layer (T / time per layer forward).  The
+headline line is the largest configuration, the prefill chunk: H=2048, I=512,
+E=512, top-10 + 1 shared expert, NVFP4 experts, T=4096 tokens per step.  A
+step passes the tokens through a stack of L distinct layer instances (each its
+own weights, so a step touches more than 4x the 129 MB L2), captured once as a
 CUDA graph and replayed.  Inputs are resident in HBM before the timed region.
 
-Also reported: the dominant kernel's (gate/up + SwiGLU) achieved HBM bandwidth
-against the measured copy bandwidth, the same metric end to end through the
-host-buffer C-ABI call (moe_forward_host: copies inside the timed region), SM
-clocks sampled during the timed region, and the CPU oracle timed on the host
-cores on a bounded sample.
+`per_config` times the other layer configurations in the same run, each the
+same way: decode (T=1, NVFP4), decode of the larger expert shape (T=1, FP6
+e2m3) and the batched decode step (T=64, NVFP4).
+
+Also reported: the dominant kernel's (gate/up + SwiGLU) achieved FLOP rate
+(prefill) or HBM bandwidth (the others) against the measured peak, the same
+metric end to end through the host-buffer C-ABI call (moe_forward_host: copies
+inside the timed region), SM clocks sampled during the timed region, and the
+CPU oracle timed on the host cores on a bounded sample (one thread, and every
+core).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs its own replicas (weak scaling: no
@@ -36,7 +41,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "routed tokens/s per MoE layer on 1 GB300; HBM GB/s as % of ~8 TB/s roofline"
 UNIT = "tokens/s"
-WORKLOAD = 1  # decode-h2048-i512-e512-k10-s1-t1-nvfp4
+WORKLOAD = 4  # prefill-h2048-i512-e512-k10-s1-t4096-nvfp4: the largest config
+PER_CONFIG = [1, 2, 3]  # decode NVFP4, decode FP6, batched T=64: timed in the same run
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -44,13 +50,17 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=None,
-                    help="layer instances per step (default 32 for decode, 8 for larger T)")
+                    help="layer instances per step (default: enough that a step's weights are "
+                         "more than 4x L2)")
     ap.add_argument("--workload", type=int, default=WORKLOAD,
-                    help="workload index (default: the decode workload the metric is quoted on)")
+                    help="workload index of the headline line (default: the prefill config)")
+    ap.add_argument("--per-config", dest="per_config", action="store_true", default=True,
+                    help="also time the decode, FP6 decode and batched configs (default)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--host-mirror", type=float, default=0.0,
@@ -260,21 +270,35 @@ def _oracle_setup(w, n_tok=4):
 
 
 def oracle_baseline(w, seconds):
-    """The oracle as it stands: whole-layer forwards of single decode tokens (its
-    weights quantised by the oracle beforehand, not timed), for ~`seconds`.
-    A T=1 forward runs on one thread (the oracle threads over tokens)."""
-    x, _, L = _oracle_setup(w)
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        L.forward(x[reps % len(x): reps % len(x) + 1], threads=1)
-        reps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": reps / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} single-token forwards of {w.name} ({dt:.1f} s, fp64, 1 thread)"}
+    """The oracle as it stands, on a bounded sample of the workload: whole-layer
+    forwards (router, top-k, the k + shared expert FFNs, combine) of the
+    workload's first tokens, its weights quantised by the oracle beforehand
+    (not timed).  Timed twice for about seconds/2 each: one token per call on
+    one thread, and one token per host core per call, the oracle threading
+    over tokens on every core."""
+    cores = os.cpu_count() or 1
+    x, _, L = _oracle_setup(w, n_tok=max(4, cores))
 
+    def rate(n, threads, budget):
+        t0 = time.perf_counter()
+        calls = 0
+        while True:
+            i = (calls * n) % len(x)
+            xs = x[i:i + n] if i + n <= len(x) else x[:n]
+            L.forward(xs, threads=threads)
+            calls += 1
+            if time.perf_counter() - t0 >= budget:
+                break
+        dt = time.perf_counter() - t0
+        return calls * n / dt, calls, dt
+
+    v1, c1, d1 = rate(1, 1, seconds / 2)
+    va, ca, da = rate(cores, cores, seconds / 2)
+    return {"value": va, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{ca} whole-layer forwards of {cores} tokens of {w.name} ({da:.1f} s, fp64, "
+                      f"threaded over tokens on {cores} host cores)",
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1,
+                              "sample": f"{c1} single-token forwards ({d1:.1f} s, fp64, 1 thread)"}}
 
 
 def run_reference(args, w):
@@ -353,24 +377,50 @@ def sources_sha256(csrc, unit):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, w):
+def no_launch_phases(L, T):
+    """Phases of moe_debug_run_phase that launch nothing at T tokens: for the
+    self-routed path (3 kernels) top-k/dispatch and combine live inside the
+    expert kernels; for the other T <= 8 paths the combine is fused."""
+    n = L.launches(T)
+    if n == 3:
+        return {1, 4}
+    if T <= 8:
+        return {4}
+    return set()
+
+
+def graph_time_us(s, fn, reps, warm=3):
+    """Average time of one fn() call: fn captured once into a CUDA graph,
+    replayed warm + reps times, CUDA events on the capture stream."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for _ in range(warm):
+            g.replay()
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False):
+    """Builds Ln layer instances of workload w, captures one step (the T
+    tokens through the Ln layers) as a CUDA graph and times `steps` replays
+    after `warmup` (CUDA events, max over ranks).  Also times the dominant
+    kernel alone, each phase alone, and (headline) the host-buffer call."""
     import numpy as np
     import torch
 
     import gen
-    import quantized_moe_expert_layer_gb300 as moe
     from quantized_moe_expert_layer_gb300.synthetic import build_layer
 
-    rank, local_rank, world = dist_env()
-    torch.cuda.set_device(local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    gen.build(device=True)
-    moe.build()
-    Ln = args.layers
     T = w.T
-    masks = [placement_mask(w, args.host_mirror, 1000 * rank + i) for i in range(Ln)]
+    masks = [placement_mask(w, host_mirror, 1000 * rank + i) for i in range(Ln)]
     layers = [build_layer(w, T_max=T, seed=1000 * rank + i, in_hbm=masks[i]) for i in range(Ln)]
     x_np = gen.x_tokens(w, T, first=rank * T)
     x = torch.from_numpy(x_np.view(np.int16)).cuda()
@@ -384,7 +434,6 @@ def run_ours(args, w):
         if L.status() != 0:
             raise RuntimeError("device status word set after warm-up forward")
 
-    # one step = the token through the L layer instances, as one CUDA graph
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for L, o in zip(layers, outs):
@@ -399,47 +448,54 @@ def run_ours(args, w):
         if not torch.equal(o, r):
             raise RuntimeError("graph replay differs from the eager forward")
     with torch.cuda.stream(s):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             g.replay()
     s.synchronize()
 
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
-        if not uuid.startswith("GPU-"):
-            uuid = "GPU-" + uuid
-    except Exception:
+    clocks = None
+    if headline:
         uuid = None
-    clocks = ClockSampler(uuid)
+        try:
+            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+        except Exception:
+            uuid = None
+        clocks = ClockSampler(uuid)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
+    if clocks:
+        clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):  # replay() launches on the current stream
         ev0.record(s)
-        for _ in range(args.steps):
+        for _ in range(steps):
             g.replay()
         ev1.record(s)
     torch.cuda.synchronize()
-    clocks.stop()
+    if clocks:
+        clocks.stop()
     if world > 1:
         dist.barrier()
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
-    value = job_rate(world, T, Ln, args.steps, ms / 1e3)
+    res = {"value": job_rate(world, T, Ln, steps, ms / 1e3), "ms": ms,
+           "us_per_layer": ms * 1e3 / (steps * Ln), "launches_per_layer": layers[0].launches(T)}
+    if clocks:
+        res["clocks"] = clocks.summary()
 
-    # dominant kernel, timed alone over the L layers (graph of back-to-back
-    # launches, launch gaps included): gate/up + SwiGLU, the tcgen05 GEMM for
+    # dominant kernel (gate/up + SwiGLU) alone over the L layers (graph of
+    # back-to-back launches, launch gaps included): the tcgen05 GEMM for
     # prefill (tensor-bound) or the streaming kernel otherwise (HBM-bound)
     counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
     tc = tc_path(w, T)
     gu = packed_gateup_bytes(w)
-    per_launch = []
-    host_per_launch = []
+    dn = packed_down_bytes(w)
+    per_launch, padded, host_per_launch = [], [], []
     # for T <= 8 (NVFP4) gate/up also asks L2 for the touched experts' down
     # matrices, which the down kernel then reads from L2
     prefetch_down = T <= 8 and w.fmt in (1, 3)
-    dn = packed_down_bytes(w)
     with torch.cuda.stream(s):
         for L, o, m in zip(layers, outs, masks):
             L.forward(x, o, stream=s)
@@ -450,37 +506,34 @@ def run_ours(args, w):
             if m is not None:  # weight bytes of the touched experts in the host mirror
                 used = np.concatenate([c > 0, [True] * w.shared])
                 host_per_launch.append(int((used & ~m).sum()) * (gu + (dn if prefetch_down else 0)))
-            if tc:  # FLOPs of the contraction (N padded to 16 per work item as the MMA runs it)
+            if tc:  # FLOPs of the contraction: the routed (token, expert) pairs as computed,
+                # and as the MMA runs them (N padded to 16 per work item of <= 128 tokens)
                 n = [int(v) for v in c if v > 0] + [T] * w.shared
+                per_launch.append(2.0 * sum(n) * 2 * w.I * w.H)
                 cols = sum(((min(128, v - 128 * j) + 15) // 16) * 16
                            for v in n for j in range((v + 127) // 128))
-                per_launch.append(2.0 * cols * 2 * w.I * w.H)
+                padded.append(2.0 * cols * 2 * w.I * w.H)
             else:  # unique weight bytes, x, and a (+ the down matrices it pulls into L2)
                 per_launch.append(D * (gu + 8 + (dn if prefetch_down else 0)) + T * w.H * 2
                                   + (T * w.k + T * w.shared) * w.I * 2)
-    gk = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gk, stream=s):
+
+    def run_gateup():
         for L, o in zip(layers, outs):
             L.run_phase(2, x, o, stream=s)
-    reps = max(20, min(500, args.steps))
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        for _ in range(5):
-            gk.replay()
-        k0.record(s)
-        for _ in range(reps):
-            gk.replay()
-        k1.record(s)
-    torch.cuda.synchronize()
-    k_us = k0.elapsed_time(k1) * 1e3 / (reps * Ln)
+    k_us = graph_time_us(s, run_gateup, max(20, min(200, steps))) / Ln
     work = sum(per_launch) / len(per_launch)
     if tc:
         kname = "tc_expert_kernel"
         peak, peak_kind = peaks("tensor")
         achieved = work / (k_us * 1e-6) / 1e12
-        roofline = {"bound": "tensor", "kernel": kname + "<0> (gate/up + SwiGLU)", "achieved": achieved,
-                    "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                    "algorithmic_flops_per_launch": work}
+        pw = sum(padded) / len(padded)
+        roofline = {"bound": "tensor", "kernel": kname + "<0> (gate/up + SwiGLU)",
+                    "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                    "algorithmic_flops_per_launch": work,
+                    "flops_as_run_per_launch": pw,
+                    "note": "algorithmic FLOPs count the routed (token, expert) pairs; the MMA "
+                            "also runs the padding of each work item to a multiple of 16 tokens "
+                            "(flops_as_run_per_launch)"}
     else:
         kname = ("gateup_routed_kernel" if T <= 8 else
                  "stream_kernel<0>" if w.fmt in (1, 3) else "gateup_kernel")
@@ -503,59 +556,112 @@ def run_ours(args, w):
                          kname.split("<")[0], w.name, os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
                      "avg_launch_us": k_us, "peak_source": peak_kind,
                      "timing": "CUDA events over a graph of back-to-back launches, gaps included"})
+    res["roofline"] = roofline
+    res["hbm_gbs_layer"] = None if tc else (
+        (work + (D * dn if not prefetch_down else 0)) / (res["us_per_layer"] * 1e-6) / 1e9)
 
-    # steady-state time of each phase alone (graphs of L back-to-back launches)
+    # steady-state time of each phase alone (graphs of L back-to-back launches);
+    # phases that launch nothing at this T are null
+    skip = no_launch_phases(layers[0], T)
     phase_us = {}
     for ph, name in [(0, "routing"), (1, "topk_dispatch"), (2, "gate_up"), (3, "down"), (4, "combine")]:
-        gp = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gp, stream=s):
+        if ph in skip:
+            phase_us[name] = None
+            continue
+
+        def run_ph(ph=ph):
             for L, o in zip(layers, outs):
                 L.run_phase(ph, x, o, stream=s)
-        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s):
-            for _ in range(3):
-                gp.replay()
-            p0.record(s)
-            for _ in range(50):
-                gp.replay()
-            p1.record(s)
-        torch.cuda.synchronize()
-        phase_us[name] = p0.elapsed_time(p1) * 1e3 / (50 * Ln)
+        phase_us[name] = graph_time_us(s, run_ph, 30) / Ln
+    res["phase_us_alone"] = phase_us
 
-    # e2e: the host-buffer C-ABI call, copies inside the timed region
-    xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
-    ohs = [torch.empty((T, w.H), dtype=torch.float32).pin_memory() for _ in range(Ln)]
-    for L, oh in zip(layers, ohs):
-        L.forward_host(xh, oh, stream=s)
-    k_e2e = max(5, min(args.steps, 100))
-    if world > 1:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(k_e2e):
+    if headline:
+        # e2e: the host-buffer C-ABI call, copies inside the timed region
+        xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+        ohs = [torch.empty((T, w.H), dtype=torch.float32).pin_memory() for _ in range(Ln)]
         for L, oh in zip(layers, ohs):
             L.forward_host(xh, oh, stream=s)
-    e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
-    e2e = {"value": job_rate(world, T, Ln, k_e2e, e2e_dt), "unit": UNIT,
-           "h2d_bytes_per_step": Ln * T * w.H * 2, "d2h_bytes_per_step": Ln * T * w.H * 4,
-           "call": "moe_forward_host per layer (pinned host buffers, read and written in place "
-                   "by the kernels over the CPU-GPU link; synchronous)"}
+        k_e2e = max(3, min(steps, 20 if T > 8 else 100))
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(k_e2e):
+            for L, oh in zip(layers, ohs):
+                L.forward_host(xh, oh, stream=s)
+        e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
+        res["e2e"] = {"value": job_rate(world, T, Ln, k_e2e, e2e_dt), "unit": UNIT,
+                      "h2d_bytes_per_step": Ln * T * w.H * 2, "d2h_bytes_per_step": Ln * T * w.H * 4,
+                      "call": "moe_forward_host per layer (pinned host buffers, read and written in "
+                              "place by the kernels over the CPU-GPU link; synchronous)"}
+    for L in layers:
+        L.close()
+    del layers, outs
+    torch.cuda.empty_cache()
+    return res
 
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32 (" + SHORT_NAMES[w.fmt] + " weights)",
+
+def default_layers(w, host_mirror=0.0):
+    """Layer instances per step: enough distinct weights that a step touches
+    more than 4x the 129 MB L2 (each instance its own arena)."""
+    if w.T <= 8:
+        if w.fmt == 2:
+            return 4           # 4 x 260 MB touched
+        return 16 if host_mirror > 0 else 32   # 32 x 21.6 MB (decode), 32 x 44 MB (DeepSeek shape)
+    return 4 if w.T <= 64 else 8   # batched: 4 x 650 MB; prefill: 8 x 960 MB
+
+
+def run_ours(args, w):
+    import torch
+
+    import gen
+    import quantized_moe_expert_layer_gb300 as moe
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    gen.build(device=True)
+    moe.build()
+    Ln = args.layers or default_layers(w, args.host_mirror)
+    r = measure(w, Ln, args.steps, args.warmup, rank, world, args.host_mirror, headline=True)
+    per_config = {}
+    if args.per_config:
+        for idx in PER_CONFIG:
+            wc = gen.get_workload(idx)
+            if wc.name == w.name:
+                continue
+            Lc = default_layers(wc)
+            # each config's timed region: about a second of replays
+            one = measure(wc, Lc, max(20, args.warmup), 3, rank, world)
+            steps_c = max(20, min(5000, int(1.0 / max(one["ms"] * 1e-3 / max(20, args.warmup), 1e-6))))
+            rc = measure(wc, Lc, steps_c, 3, rank, world)
+            per_config[wc.name] = {
+                "tokens_per_step": wc.T, "layer_instances_per_step": Lc, "steps": steps_c,
+                "value": rc["value"], "unit": UNIT, "us_per_layer": rc["us_per_layer"],
+                "format": SHORT_NAMES[wc.fmt], "gpu_launches_per_layer": rc["launches_per_layer"],
+                "roofline": rc["roofline"], "hbm_gbs_whole_layer": rc["hbm_gbs_layer"],
+                "phase_us_alone": rc["phase_us_alone"]}
+
+    line = {"metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 x f16 -> f32 (" + SHORT_NAMES[w.fmt] + " weights dequantised exactly to "
+                     "f16; bf16 x copied exactly to f16)",
             "data": "synthetic (seeded generator; random-init weights quantised on the device)",
-            "config": config_block(w, Ln, {"us_per_layer": ms * 1e3 / (args.steps * Ln),
+            "config": config_block(w, Ln, {"us_per_layer": r["us_per_layer"],
                                            "host_mirror_fraction": args.host_mirror,
-                                           "phase_us_alone": phase_us,
+                                           "phase_us_alone": r["phase_us_alone"],
                                            "parallelism": f"replicas x{world}"}),
-            "roofline": roofline, "e2e": e2e, "gpu_launches": layers[0].launches(T) * Ln * args.steps,
-            "clocks": clocks.summary()}
+            "roofline": r["roofline"], "e2e": r["e2e"],
+            "gpu_launches": r["launches_per_layer"] * Ln * args.steps,
+            "clocks": r["clocks"]}
+    if per_config:
+        line["per_config"] = per_config
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    for L in layers:
-        L.close()
     if world > 1:
         dist.destroy_process_group()
 
@@ -564,9 +670,6 @@ def main():
     args = parse()
     import gen
     w = gen.get_workload(args.workload)
-    if args.layers is None:
-        # (16 decode instances with a host mirror: 14.5 GB pinned at most)
-        args.layers = (16 if args.host_mirror > 0 else 32) if w.T <= 8 else 8
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -24,6 +24,14 @@
  * Dimensions: H hidden size, I expert intermediate size, E routed experts,
  * k experts per token, T tokens.  H and I are multiples of 64 (NVFP4, MXFP4)
  * or of 128 (FP6), at most 65536; 1 <= E <= 1024; 1 <= k <= min(E, 32).
+ *
+ * Value range.  The expert kernels multiply f16 copies of x and of the SwiGLU
+ * output a = silu(g) * u (every product is exact, the sums are fp32): the
+ * copies are exact to bf16's 8 bits for |x| in [2^-14, 65504] and keep 11 bits
+ * of a in the same range.  Below 2^-14 an element keeps an absolute precision
+ * of 2^-25 (f16 subnormals).  An element of x or a above 65504 in magnitude
+ * (or not finite) records MOE_ERANGE in the layer's status word
+ * (moe_layer_status); that forward's output is then not valid.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -45,7 +53,8 @@ enum moe_status {
   MOE_ENOMEM = -2,   /* device allocation failed */
   MOE_ECUDA = -3,    /* a CUDA call failed; moe_last_error() names it */
   MOE_ESTATE = -4,   /* call out of order (forward before pack / reserve) */
-  MOE_ETIMEOUT = -5  /* a bounded device wait gave up (see moe_layer_status) */
+  MOE_ETIMEOUT = -5, /* a bounded device wait gave up (see moe_layer_status) */
+  MOE_ERANGE = -6    /* x or a beyond the f16 range the experts compute in (status word only) */
 };
 
 enum moe_matrix { MOE_GATE = 0, MOE_UP = 1, MOE_DOWN = 2 };
@@ -56,14 +65,20 @@ enum moe_where { MOE_HOST = 0, MOE_DEVICE = 1 };
 /* ------------------------------------------------------------------ lifetime */
 
 /* Create a layer on the current CUDA device.  format: moe_format; shared: 0 or 1
- * (one always-on shared expert of intermediate size I, weight 1).  Allocates
- * the packed-weight arena (zero-filled) and the tensor-scale table.  *out gets
- * the handle, or NULL on failure. */
+ * (one always-on shared expert of intermediate size I, weight 1: the
+ * "shared_expert" kernel of "Strata on an Intel Arc", parity table of "Where
+ * it stands").  Allocates the packed-weight arena (zero-filled) and the
+ * tensor-scale table.  *out gets the handle, or NULL on failure (MOE_ENOMEM
+ * when an allocation fails; nothing stays allocated). */
 int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_layer** out);
 
-/* Size the forward workspace for up to T_max tokens per call.  May be called
- * again to grow it, never while a forward is in flight.  moe_forward allocates
- * nothing, so a forward can be captured into a CUDA graph after this call. */
+/* Size the forward workspace for up to T_max tokens per call (reserved at
+ * start-up so the forward never allocates, as the knivesysl README reserves
+ * its buffers at initialisation, "runtime diagnostics").  May be called again
+ * to grow it, never while a forward is in flight.  moe_forward allocates
+ * nothing, so a forward can be captured into a CUDA graph after this call.
+ * MOE_ENOMEM leaves the previous workspace in place.  The workspace buffers
+ * are separated by guard regions (see moe_debug_check_workspace). */
 int moe_layer_reserve(moe_layer* L, int T_max);
 
 /* Free everything the layer owns (synchronises its device first).  NULL is a no-op. */
@@ -74,13 +89,24 @@ void moe_layer_destroy(moe_layer* L);
 const char* moe_last_error(void);
 
 /* Read the layer's device status word into *status: 0, or the negative
- * moe_status a kernel recorded (MOE_EINVAL from a device-side bounds check on
- * an expert id or work entry).  Synchronises the device; clears the word when
- * reset != 0.  Returns MOE_OK, or an error if the read itself failed. */
+ * moe_status a kernel recorded: MOE_EINVAL from a device-side bounds check on
+ * an expert id or work entry, MOE_ETIMEOUT from a bounded wait that gave up
+ * (every device wait is capped, as the bounded spins of "Strata on an Intel
+ * Arc" are), MOE_ERANGE from a value beyond f16's range (see "Value range").
+ * Synchronises the device; clears the word when reset != 0.  Returns MOE_OK,
+ * or an error if the read itself failed. */
 int moe_layer_status(moe_layer* L, int reset, int* status);
 
 /* Number of kernels one moe_forward of T tokens launches (>= 0), or an error. */
 int moe_forward_launches(moe_layer* L, int T);
+
+/* Budget of each bounded wait in the tensor-core kernels, in SM clock cycles
+ * (clock64); cycles <= 0 restores the default of 2e9 (about one second).  A
+ * wait that runs out stops its CTA's work: the CTA lets its copies and MMAs in
+ * flight finish (those drains keep the default budget), frees its tensor
+ * memory, records MOE_ETIMEOUT in the status word and returns, leaving the
+ * context usable.  Applies to the following forwards. */
+int moe_set_wait_budget(moe_layer* L, int64_t cycles);
 
 /* Bytes of the packed arena and of one packed expert (gate + up + down, without
  * its three fp32 tensor scales). */
@@ -118,7 +144,9 @@ int moe_layer_placement(moe_layer* L, uint8_t* in_hbm, uint64_t* hbm_bytes, uint
 /* ------------------------------------------------------------------ weights */
 
 /* Router weights Wr [E x H] as bf16 bits (row-major) and an optional fp32 bias
- * [E] (NULL = none), host or device memory per `where`.  Copied; synchronous. */
+ * [E] (NULL = none), host or device memory per `where`.  Copied; synchronous.
+ * The router with top-k is the "router_top10" kernel of "Strata on an Intel
+ * Arc" (parity table of "Where it stands"). */
 int moe_set_router(moe_layer* L, const uint16_t* wr_bf16, const float* bias, int where);
 
 /* Router mode (default MOE_ROUTER_SOFTMAX):
@@ -133,7 +161,9 @@ enum moe_router_mode { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 };
 int moe_set_router_mode(moe_layer* L, int mode);
 
 /* Pack one expert matrix from the canonical quantised format into the layer's
- * device layout.  expert in [0, E) for routed experts, E for the shared one;
+ * device layout.  The formats are those of the knivesysl README, the
+ * paragraph under the table of supported service formats (e2m3 with a
+ * power-of-two scale per 128 weights; four-bit values with a scale per 16).  expert in [0, E) for routed experts, E for the shared one;
  * matrix: moe_matrix (gate and up are [I x H], down is [H x I]; row-major,
  * blocks run along the row).
  *   NVFP4: codes [rows x K/2] bytes, two e2m1 codes per byte, the even column
@@ -163,11 +193,15 @@ typedef struct moe_canonical_matrix {
 } moe_canonical_matrix;
 
 /* Pack a whole layer from host memory: router (+ optional bias) and
- * mats[expert * 3 + matrix] for expert in [0, E + shared).  Synchronous. */
+ * mats[expert * 3 + matrix] for expert in [0, E + shared), each in the
+ * canonical format of moe_pack_matrix.  Synchronous; the host arrays may be
+ * freed when it returns. */
 int moe_pack_weights(moe_layer* L, const uint16_t* wr_bf16, const float* bias,
                      const moe_canonical_matrix* mats);
 
-/* Quantise fp32 weights W [rows x K] (device) to canonical NVFP4 on the device:
+/* Quantise fp32 weights W [rows x K] (device) to canonical NVFP4 on the device
+ * (the knivesysl README's nvfp4, a scale per 16 weights, in the two-level
+ * reading: an e4m3 block scale under an fp32 tensor scale):
  * tscale = amax(W) / (6 * 448); per 16 weights along K the e4m3 scale
  * s = rne((amax_16 / 6) / tscale); code = rne_e2m1(w / (s * tscale)); ties to
  * the even code, saturating, +0 for zero, s = 0 gives code 0; IEEE fp32
@@ -177,7 +211,7 @@ int moe_quantize_nvfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t*
                        float* tscale, void* stream);
 
 /* Quantise fp32 weights W [rows x K] (device) to canonical FP6 e2m3 on the
- * device: per 128 weights the exponent E = the smallest integer with
+ * device (the knivesysl README's fp6, a power-of-two scale per 128 weights): per 128 weights the exponent E = the smallest integer with
  * amax_128 <= 7.5 * 2^E (byte E + 127; 127 for an all-zero block) and
  * code = rne_e2m3(w / 2^E).  Device outputs codes [rows x K], exps [rows x K/128].
  * K % 128 == 0. */
@@ -196,13 +230,19 @@ int moe_quantize_mxfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t*
 
 /* ------------------------------------------------------------------ forward */
 
-/* out[T x H] (fp32, device) = the layer applied to x[T x H] (bf16 bits, device).
+/* out[T x H] (fp32, device) = the layer applied to x[T x H] (bf16 bits, device):
+ * router logits, top-k with renormalised gates ("router_top10"), the
+ * expert-sorted dispatch, each selected expert's SwiGLU on weights dequantised
+ * on the fly, the shared expert ("shared_expert"), and the gate-weighted
+ * combine (the kernels of "Strata on an Intel Arc", parity table of "Where it
+ * stands", over the formats of the knivesysl README).
  * 1 <= T <= the reserved T_max.  Asynchronous on `stream`; allocates nothing.
- * x and out must be 16-byte aligned. */
+ * x and out must be 16-byte aligned.  Errors in the arguments return at once;
+ * device-side errors land in the status word. */
 int moe_forward(moe_layer* L, const uint16_t* x, int T, float* out, void* stream);
 
 /* moe_forward with host buffers x (T x H bf16) and out (T x H fp32); returns
- * once `stream` has finished.  Page-locked, device-mapped buffers
+ * once `stream` has finished.  MOE_ESTATE before moe_layer_reserve.  Page-locked, device-mapped buffers
  * (cudaHostAlloc / cudaHostRegister, 16-byte aligned) are read and written by
  * the kernels in place over the CPU-GPU link; any other host memory is copied
  * through the layer's staging buffers. */
@@ -211,11 +251,25 @@ int moe_forward_host(moe_layer* L, const uint16_t* x_host, int T, float* out_hos
 /* The layer with the routing given instead of computed: idx [T x k] expert ids
  * (distinct within a token, each in [0, E)) and gates [T x k] fp32, device
  * pointers.  Dispatch, experts, shared expert and combine are the kernels
- * moe_forward runs. */
+ * moe_forward runs.  An expert id out of range records MOE_EINVAL in the
+ * status word and its slot is skipped. */
 int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* idx,
                        const float* gates, float* out, void* stream);
 
 /* ------------------------------------------------------------------ test hooks */
+
+/* Make the n-th following device or pinned-host allocation of the library
+ * fail as if memory were exhausted (n = 0: none).  Process-wide.  It lets
+ * tests drive every MOE_ENOMEM path (layer creation, workspace, staging of a
+ * host pack, placement) on a GPU with memory to spare, as the knivesysl
+ * README's regressions check allocation and error recovery. */
+int moe_debug_fail_alloc(int n);
+
+/* Check the guard regions between the workspace buffers: *bad_bytes gets the
+ * number of guard bytes a kernel overwrote (0 when every kernel stayed inside
+ * its buffers).  Synchronises the device.  MOE_ESTATE before
+ * moe_layer_reserve. */
+int moe_debug_check_workspace(moe_layer* L, int* bad_bytes);
 
 /* Dequantise one packed matrix back to fp32 [rows x K] (device `out`) from the
  * packed device bytes, with the decode the expert kernels use. */
@@ -249,7 +303,9 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
  *   (bias may be NULL), idx [T x k] the top-k experts per token (ties to the
  *   lower index) and gates [T x k] their renormalised softmax.
  * All pointers are device pointers the caller owns; x and wr are 16-byte
- * aligned; H % 64 == 0, 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ * aligned; H % 64 == 0, 64 <= H <= 65536, 1 <= E <= 1024, 1 <= k <= min(E, 32),
+ * T <= 524280.  The router starts only when the previous work on `stream` has
+ * finished, so x, wr and bias may be written by the kernel just before.
  * It allocates nothing.  Its only scratch, the router's K-split partial sums,
  * is a fixed 4 MiB device array inside the library, held by every GPU that
  * loads the library until the process exits.  Inputs that would need more

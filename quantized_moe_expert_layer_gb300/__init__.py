@@ -30,7 +30,7 @@ GATE, UP, DOWN = 0, 1, 2
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 HOST, DEVICE = 0, 1
 
-OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT = 0, -1, -2, -3, -4, -5
+OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT, ERANGE = 0, -1, -2, -3, -4, -5, -6
 
 # every symbol include/moe.h declares
 EXPORTS = [
@@ -39,7 +39,8 @@ EXPORTS = [
     "moe_pack_weights", "moe_set_router_mode", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_quantize_mxfp4", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
     "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches", "moe_place_experts",
-    "moe_layer_placement"
+    "moe_layer_placement", "moe_set_wait_budget", "moe_debug_fail_alloc",
+    "moe_debug_check_workspace"
 ]
 
 _lock = threading.Lock()
@@ -120,6 +121,9 @@ def lib():
                 "moe_forward_launches": (I, [P, I]),
                 "moe_place_experts": (I, [P, P]),
                 "moe_layer_placement": (I, [P, P, ctypes.POINTER(U64), ctypes.POINTER(U64)]),
+                "moe_set_wait_budget": (I, [P, ctypes.c_int64]),
+                "moe_debug_fail_alloc": (I, [I]),
+                "moe_debug_check_workspace": (I, [P, ctypes.POINTER(I)]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -208,6 +212,39 @@ class MoeLayer:
         check(lib().moe_layer_status(self.h, int(reset), ctypes.byref(v)))
         return v.value
 
+    def set_wait_budget(self, cycles):
+        """Budget (clock64 cycles) of each bounded wait in the tensor-core
+        kernels; 0 restores the default (about one second)."""
+        check(lib().moe_set_wait_budget(self.h, int(cycles)))
+
+    def check_workspace(self):
+        """Guard bytes of the workspace that a kernel overwrote (0 = none)."""
+        v = ctypes.c_int()
+        check(lib().moe_debug_check_workspace(self.h, ctypes.byref(v)))
+        return v.value
+
+    def pack_weights(self, router, bias, mats):
+        """Whole layer from host memory (moe_pack_weights): router bf16 bits
+        [E x H], bias fp32 [E] or None, mats[(expert, matrix)] = (codes,
+        scales, tscale) numpy arrays in the canonical format for every expert
+        in [0, E + shared) and matrix 0..2."""
+        import numpy as np
+        n = self.E + self.shared
+        arr = (_CanonicalMatrix * (3 * n))()
+        keep = []
+        for e in range(n):
+            for m in range(3):
+                c, sc, ts = mats[(e, m)]
+                c = np.ascontiguousarray(c, dtype=np.uint8)
+                sc = np.ascontiguousarray(sc, dtype=np.uint8)
+                keep += [c, sc]
+                arr[3 * e + m].codes = c.ctypes.data
+                arr[3 * e + m].scales = sc.ctypes.data
+                arr[3 * e + m].tscale = float(ts)
+        wr = np.ascontiguousarray(router, dtype=np.uint16)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        check(lib().moe_pack_weights(self.h, _ptr(wr), _ptr(b), ctypes.cast(arr, ctypes.c_void_p)))
+
     def set_router(self, wr, bias=None, where=None):
         where = _where(wr) if where is None else where
         check(lib().moe_set_router(self.h, _ptr(wr), _ptr(bias), where))
@@ -251,6 +288,16 @@ class MoeLayer:
                       perm=None, stream=None):
         check(lib().moe_debug_routing(self.h, _ptr(logits), _ptr(idx), _ptr(gates), _ptr(counts),
                                       _ptr(offsets), _ptr(perm), _stream(stream)))
+
+
+class _CanonicalMatrix(ctypes.Structure):
+    """moe_canonical_matrix of include/moe.h."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("tscale", ctypes.c_float)]
+
+
+def fail_alloc(n):
+    """Test hook: the n-th following allocation of the library fails (0 = none)."""
+    check(lib().moe_debug_fail_alloc(int(n)))
 
 
 def _where(t):

@@ -8,7 +8,11 @@
 namespace moe {
 namespace {
 
-constexpr long long kWaitBudget = 2000000000LL;  // ~1 s of clock64 per wait
+// Default budget of one bounded wait (clock64 cycles, about 1 s).  The
+// waits of a forward take the layer's budget (moe_set_wait_budget); the drains
+// before a CTA exits always take this one, so that no CTA leaves with a copy or
+// an MMA in flight.
+constexpr long long kWaitBudget = 2000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -42,12 +46,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of the given parity to complete.  Returns false
-// (after setting *abort) on timeout, or at once if another thread aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// (after setting *abort) when `budget` cycles pass, or at once if another
+// thread aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long budget) {
   const long long t0 = clock64();
   while (!mbar_test(bar, parity)) {
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudget) {
+    if (clock64() - t0 > budget) {
       *abort = 1;
       return false;
     }
@@ -68,11 +74,12 @@ __device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity) 
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                long long budget) {
   const long long t0 = clock64();
   while (!mbar_test_sleep(bar, parity)) {
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudget) {
+    if (clock64() - t0 > budget) {
       *abort = 1;
       return false;
     }

@@ -56,6 +56,26 @@ __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float v) {
   return r & 0xFFu;
 }
 
+// Status word values the kernels record (the negative moe_status codes).
+constexpr int kStatusInvalid = -1;  // MOE_EINVAL: a bad expert id or work entry
+constexpr int kStatusTimeout = -5;  // MOE_ETIMEOUT: a bounded wait gave up
+constexpr int kStatusRange = -6;    // MOE_ERANGE: a value outside f16's finite range
+
+// True when an f16 (either half of an f16x2 word) is infinite or NaN.
+__device__ __forceinline__ bool f16_nonfinite(uint32_t h) { return (h & 0x7C00u) == 0x7C00u; }
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t h) {
+  return f16_nonfinite(h) || f16_nonfinite(h >> 16);
+}
+
+// The SwiGLU output a as f16 bits (round to nearest even).  The f16 copy is
+// exact to 11 bits for |a| in [2^-14, 65504]; larger values (and non-finite
+// ones) record MOE_ERANGE in the status word.
+__device__ __forceinline__ uint16_t a_to_f16(float a, int* status) {
+  const uint16_t h = __half_as_ushort(__float2half_rn(a));
+  if (f16_nonfinite(h)) *status = kStatusRange;
+  return h;
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

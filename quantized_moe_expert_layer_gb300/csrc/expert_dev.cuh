@@ -254,7 +254,7 @@ __device__ __forceinline__ bool get_entry(const ExpertParams& p, int y, int& exp
   row = e.y;
   n = e.z;
   if (expert < 0 || expert >= p.E || n < 1 || n > kTokTile || row < 0 || row + n > S) {
-    if (!quiet) *p.status = -1;  // MOE_EINVAL: corrupt entry, skip it
+    if (!quiet) *p.status = kStatusInvalid;  // corrupt entry: skip it
     return false;
   }
   return true;
@@ -325,7 +325,7 @@ __device__ __forceinline__ void gateup_task(const ExpertParams& p, int expert, i
     if (col < n) {
       const float G = ts_g * v[i], U = ts_u * v[4 + i];
       const float a = G / (1.0f + expf(-G)) * U;
-      p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+      p.abuf[(size_t)(row + col) * p.I + r] = a_to_f16(a, p.status);
     }
   }
 }
@@ -522,7 +522,7 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
     if (col < n) {
       const float G = ts_g * v[i], U = ts_u * v[4 + i];
       const float a = G / (1.0f + expf(-G)) * U;
-      p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+      p.abuf[(size_t)(row + col) * p.I + r] = a_to_f16(a, p.status);
     }
   }
 }
@@ -751,7 +751,7 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
         const float G = ts_g * (acc[0][0][i] + acc[0][1][i]);
         const float U = ts_u * (acc[NT - 1][0][i] + acc[NT - 1][1][i]);
         const float a = G / (1.0f + expf(-G)) * U;
-        p.abuf[(size_t)(row + col) * p.I + r] = __half_as_ushort(__float2half_rn(a));
+        p.abuf[(size_t)(row + col) * p.I + r] = a_to_f16(a, p.status);
       }
     }
   } else {

@@ -12,6 +12,7 @@ constexpr int kTokTile = 8;     // tokens per expert entry (the n of m16n8k16)
 constexpr int kTcMaxN = 128;    // tokens per entry of the tensor-core path
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
+constexpr int kMaxKsplitHost = 8;  // router K slices at most (router_ksplit)
 
 // Everything the expert kernels read or write for one forward.
 struct ExpertParams {
@@ -37,6 +38,7 @@ struct ExpertParams {
   const float* rbias;    // router bias [E] or null (tensor-core router only)
   float* logits_out;     // router logits [T x E] (tensor-core router only)
   int* status;
+  long long wait_budget; // clock64 cycles one bounded wait of the tensor-core kernels may take
 };
 
 #ifdef __CUDACC__
@@ -96,7 +98,9 @@ cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stri
 
 // routing
 int router_ksplit(int T, int H, int E);
-cudaError_t launch_router(const RouteParams& p, cudaStream_t st);
+// pdl: may start while the previous kernel on the stream drains (it then reads
+// the router weights before its wait: they must not be written by that kernel)
+cudaError_t launch_router(const RouteParams& p, cudaStream_t st, bool pdl = true);
 cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st);
 // Dispatch of p.idx (top-k done): one CTA, or count / scan / place kernels
 // for T*k > kDispOneCtaMax.  dispatch_launches: how many kernels that is.
@@ -120,7 +124,8 @@ bool small_route_ok(int T, int k);
 cudaError_t launch_gateup_routed(const ExpertParams& p, const RouteParams& rp, int grid_y,
                                  cudaStream_t st);
 cudaError_t expert_kernels_init();
-cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream_t st);
+// the f16 copy of x (n elements); MOE_ERANGE in *status for |x| beyond f16's range
+cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, int* status, cudaStream_t st);
 
 // tensor-core (tcgen05) prefill path
 bool tc_path_ok(int fmt, int T, int k, int E, int H, int I);

@@ -1,6 +1,7 @@
 // The C ABI of include/moe.h: layer lifetime, weight packing, the forward
 // pass (router -> top-k / dispatch -> gate/up + SwiGLU -> down -> combine,
 // chained with programmatic dependent launch) and the test hooks.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -52,6 +53,34 @@ struct DeviceGuard {
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Test hook of moe_debug_fail_alloc: the countdown to the allocation that
+// fails (0: none).  Every device or pinned-host allocation the library makes
+// goes through alloc_dev / alloc_host.
+std::atomic<int> g_fail_alloc{0};
+
+bool injected_failure() {
+  int n = g_fail_alloc.load();
+  while (n > 0 && !g_fail_alloc.compare_exchange_weak(n, n - 1)) {
+  }
+  return n == 1;
+}
+
+cudaError_t alloc_dev(void** p, size_t bytes) {
+  *p = nullptr;
+  if (injected_failure()) return cudaErrorMemoryAllocation;
+  return cudaMalloc(p, bytes);
+}
+
+cudaError_t alloc_host(void** p, size_t bytes, unsigned flags) {
+  *p = nullptr;
+  if (injected_failure()) return cudaErrorMemoryAllocation;
+  return cudaHostAlloc(p, bytes, flags);
+}
+
+// Guard regions around the workspace buffers: 256 bytes of this value each.
+constexpr unsigned char kCanary = 0xA5;
+constexpr size_t kGuard = 256;
 
 // Upper bound on routed entries (ceil(count/8) summed over experts) for T tokens.
 int max_routed_entries(int T, int E, int k) {
@@ -106,6 +135,7 @@ struct moe_layer {
   bool router_set = false;
   int router_mode = ROUTER_SOFTMAX;
   int* status = nullptr;
+  long long wait_budget = 0;     // bounded-wait budget of the tensor-core kernels (0: default)
   // workspace
   int T_max = 0;
   void* ws = nullptr;
@@ -128,6 +158,8 @@ struct moe_layer {
   float* ybuf = nullptr;
   uint16_t* x_stage = nullptr;
   float* out_stage = nullptr;
+  std::vector<size_t> guards;    // byte offsets of the workspace's guard regions
+  size_t ws_bytes = 0;
   int last_T = 0;
   bool last_has_logits = false;
 };
@@ -216,6 +248,7 @@ ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
   p.wr = L->router;
   p.rbias = L->has_bias ? L->bias : nullptr;
   p.status = L->status;
+  p.wait_budget = L->wait_budget > 0 ? L->wait_budget : 2000000000LL;
   return p;
 }
 
@@ -253,7 +286,7 @@ bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E,
 int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
   ep.logits_out = L->partial;
-  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, st));
+  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
   CK("tensor-core router kernel launch", launch_tc_router(ep, st));
   return MOE_OK;
 }
@@ -364,15 +397,15 @@ int moe_layer_create(int format, int H, int I, int E, int k, int shared, moe_lay
   }
   const int n_total = E + shared;
   L->arena_bytes = (uint64_t)n_total * L->geom.expert_bytes;
-  if (cudaMalloc(&L->arena, L->arena_bytes) != cudaSuccess ||
-      cudaMalloc(&L->tscale, sizeof(float) * 3 * n_total) != cudaSuccess ||
-      cudaMalloc(&L->router, sizeof(uint16_t) * (size_t)E * H) != cudaSuccess ||
-      cudaMalloc(&L->bias, sizeof(float) * E) != cudaSuccess ||
-      cudaMalloc(&L->status, sizeof(int)) != cudaSuccess) {
+  if (alloc_dev((void**)&L->arena, L->arena_bytes) != cudaSuccess ||
+      alloc_dev((void**)&L->tscale, sizeof(float) * 3 * n_total) != cudaSuccess ||
+      alloc_dev((void**)&L->router, sizeof(uint16_t) * (size_t)E * H) != cudaSuccess ||
+      alloc_dev((void**)&L->bias, sizeof(float) * E) != cudaSuccess ||
+      alloc_dev((void**)&L->status, sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
+    const double mb = (double)L->arena_bytes / 1e6;
     moe_layer_destroy(L);
-    return fail(MOE_ENOMEM, "moe_layer_create: cudaMalloc of %.1f MB failed",
-                L ? (double)L->arena_bytes / 1e6 : 0.0);
+    return fail(MOE_ENOMEM, "moe_layer_create: device allocation failed (arena %.1f MB)", mb);
   }
   if (cudaMemset(L->arena, 0, L->arena_bytes) != cudaSuccess ||
       cudaMemset(L->tscale, 0, sizeof(float) * 3 * n_total) != cudaSuccess ||
@@ -414,24 +447,31 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       ((S + kDispChunk - 1) / kDispChunk) * E * 4,  // blk
   };
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
-  size_t total = 0;
-  for (int i = 0; i < n; ++i) total += align_up(sizes[i], 256);
+  // [guard][buffer 0][guard][buffer 1] ... [guard]: moe_debug_check_workspace
+  // finds a kernel that wrote past the end of its buffer
+  size_t total = kGuard;
+  for (int i = 0; i < n; ++i) total += align_up(sizes[i], 256) + kGuard;
   void* ws = nullptr;
-  if (cudaMalloc(&ws, total) != cudaSuccess) {
+  if (alloc_dev(&ws, total) != cudaSuccess) {
     cudaGetLastError();
-    return fail(MOE_ENOMEM, "moe_layer_reserve: cudaMalloc of %.1f MB failed", total / 1e6);
+    return fail(MOE_ENOMEM, "moe_layer_reserve: device allocation of %.1f MB failed", total / 1e6);
   }
   if (L->ws) {
     cudaDeviceSynchronize();
     cudaFree(L->ws);
   }
   L->ws = ws;
+  L->ws_bytes = total;
+  L->guards.clear();
   char* p = static_cast<char*>(ws);
   void* ptrs[24];
   for (int i = 0; i < n; ++i) {
+    L->guards.push_back((size_t)(p - static_cast<char*>(ws)));
+    p += kGuard;
     ptrs[i] = p;
     p += align_up(sizes[i], 256);
   }
+  L->guards.push_back((size_t)(p - static_cast<char*>(ws)));
   L->partial = (float*)ptrs[0];
   L->logits = (float*)ptrs[1];
   L->idx = (int*)ptrs[2];
@@ -453,6 +493,8 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->blk = (int*)ptrs[18];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
+  for (size_t off : L->guards)
+    CK("moe_layer_reserve: guard regions", cudaMemset(static_cast<char*>(ws) + off, kCanary, kGuard));
   return MOE_OK;
 }
 
@@ -499,11 +541,11 @@ int moe_place_experts(moe_layer* L, const uint8_t* in_hbm) {
   uint8_t* mirror_dev = nullptr;
   const uint8_t** eptr = nullptr;
   cudaError_t err = cudaSuccess;
-  if (n_hbm) err = cudaMalloc(&arena, (size_t)n_hbm * eb);
+  if (n_hbm) err = alloc_dev((void**)&arena, (size_t)n_hbm * eb);
   if (err == cudaSuccess && n_host)
-    err = cudaHostAlloc(&mirror, (size_t)n_host * eb, cudaHostAllocMapped | cudaHostAllocPortable);
+    err = alloc_host((void**)&mirror, (size_t)n_host * eb, cudaHostAllocMapped | cudaHostAllocPortable);
   if (err == cudaSuccess && n_host) err = cudaHostGetDevicePointer(&mirror_dev, mirror, 0);
-  if (err == cudaSuccess && n_host) err = cudaMalloc(&eptr, sizeof(uint8_t*) * n_total);
+  if (err == cudaSuccess && n_host) err = alloc_dev((void**)&eptr, sizeof(uint8_t*) * n_total);
   if (err != cudaSuccess) {
     cudaGetLastError();
     cudaFree(arena);
@@ -601,7 +643,10 @@ int moe_pack_matrix(moe_layer* L, int expert, int matrix, const uint8_t* codes,
   const uint8_t* c = codes;
   const uint8_t* s = scales;
   uint8_t* tmp = nullptr;
-  if (tmp_bytes) CK("moe_pack_matrix: staging cudaMalloc", cudaMalloc(&tmp, tmp_bytes));
+  if (tmp_bytes && alloc_dev((void**)&tmp, tmp_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MOE_ENOMEM, "moe_pack_matrix: staging allocation of %zu bytes failed", tmp_bytes);
+  }
   size_t used = 0;
   if (where != MOE_DEVICE) {
     cudaError_t e = cudaMemcpy(tmp, codes, code_bytes, cudaMemcpyHostToDevice);
@@ -700,6 +745,7 @@ int moe_forward(moe_layer* L, const uint16_t* x, int T, float* out, void* stream
 
 int moe_forward_host(moe_layer* L, const uint16_t* x_host, int T, float* out_host, void* stream) {
   if (!L || !x_host || !out_host) return fail(MOE_EINVAL, "moe_forward_host: null argument");
+  if (!L->ws) return fail(MOE_ESTATE, "moe_forward_host: no workspace (moe_layer_reserve first)");
   int rc = check_forward_args(L, L->x_stage, T, L->out_stage);
   if (rc) return rc;
   DeviceGuard dg(L->device);
@@ -740,12 +786,40 @@ int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* id
   CK("moe_forward_routed: copy idx", cudaMemcpyAsync(L->idx, idx, S * 4, cudaMemcpyDeviceToDevice, st));
   CK("moe_forward_routed: copy gates",
      cudaMemcpyAsync(L->gates, gates, S * 4, cudaMemcpyDeviceToDevice, st));
-  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, st));
+  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
   RouteParams rp = route_params(L, x, T);
   CK("dispatch kernel launch", launch_dispatch(rp, false, st));
   L->last_T = T;
   L->last_has_logits = false;
   return run_experts(L, x, T, out, st);
+}
+
+int moe_set_wait_budget(moe_layer* L, int64_t cycles) {
+  if (!L) return fail(MOE_EINVAL, "moe_set_wait_budget: null layer");
+  L->wait_budget = cycles > 0 ? (long long)cycles : 0;
+  return MOE_OK;
+}
+
+int moe_debug_fail_alloc(int n) {
+  if (n < 0) return fail(MOE_EINVAL, "moe_debug_fail_alloc: n = %d < 0", n);
+  g_fail_alloc.store(n);
+  return MOE_OK;
+}
+
+int moe_debug_check_workspace(moe_layer* L, int* bad_bytes) {
+  if (!L || !bad_bytes) return fail(MOE_EINVAL, "moe_debug_check_workspace: null argument");
+  if (!L->ws) return fail(MOE_ESTATE, "moe_debug_check_workspace: no workspace");
+  DeviceGuard dg(L->device);
+  CK("moe_debug_check_workspace: synchronize", cudaDeviceSynchronize());
+  std::vector<unsigned char> buf(kGuard);
+  int bad = 0;
+  for (size_t off : L->guards) {
+    CK("moe_debug_check_workspace: read guard",
+       cudaMemcpy(buf.data(), static_cast<char*>(L->ws) + off, kGuard, cudaMemcpyDeviceToHost));
+    for (unsigned char b : buf) bad += b != kCanary;
+  }
+  *bad_bytes = bad;
+  return MOE_OK;
 }
 
 int moe_debug_dequant(moe_layer* L, int expert, int matrix, float* out, void* stream) {

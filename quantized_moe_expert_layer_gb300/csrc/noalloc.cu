@@ -64,9 +64,13 @@ extern "C" int moe_route_noalloc(const uint16_t* x, int T, int H, const uint16_t
                                  float* gates, void* stream) {
   if (!x || !wr || !logits || !idx || !gates)
     return moe::record_error(MOE_EINVAL, "moe_route_noalloc: null argument");
-  if (T < 1 || H < 64 || H % 64 || E < 1 || E > moe::kMaxE || k < 1 || k > E || k > moe::kMaxK)
+  if (T < 1 || H < 64 || H % 64 || H > 65536 || E < 1 || E > moe::kMaxE || k < 1 || k > E ||
+      k > moe::kMaxK)
     return moe::record_error(MOE_EINVAL, "moe_route_noalloc: bad sizes T=%d H=%d E=%d k=%d", T, H,
                              E, k);
+  // the router grid has ceil(T / 8) token groups in its y dimension
+  if ((T + moe::kTokTile - 1) / moe::kTokTile > 65535)
+    return moe::record_error(MOE_EINVAL, "moe_route_noalloc: T=%d above %d", T, 65535 * moe::kTokTile);
   if (((uintptr_t)x | (uintptr_t)wr) & 15u)
     return moe::record_error(MOE_EINVAL, "moe_route_noalloc: x and wr must be 16-byte aligned");
   const int ksplit = moe::router_ksplit(T, H, E);
@@ -75,7 +79,7 @@ extern "C" int moe_route_noalloc(const uint16_t* x, int T, int H, const uint16_t
     return moe::record_error(MOE_EINVAL,
                              "moe_route_noalloc: T=%d, E=%d needs %zu floats of scratch; the static "
                              "array holds %zu (T * E <= %zu always fits)",
-                             T, E, need, kScratchFloats, kScratchFloats / 8);
+                             T, E, need, kScratchFloats, kScratchFloats / moe::kMaxKsplitHost);
   float* scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
@@ -95,7 +99,10 @@ extern "C" int moe_route_noalloc(const uint16_t* x, int T, int H, const uint16_t
   p.idx = idx;
   p.gates = gates;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = moe::launch_router(p, st);
+  // Launched without programmatic dependent launch: x, wr and bias are the
+  // caller's and may be written by the kernel just before this call, so the
+  // router reads nothing before that kernel has finished.
+  cudaError_t e = moe::launch_router(p, st, false);
   if (e == cudaSuccess) e = moe::launch_topk(p, false, st);
   if (e != cudaSuccess)
     return moe::record_error(MOE_ECUDA, "moe_route_noalloc: kernel launch: %s", cudaGetErrorName(e));

@@ -151,7 +151,12 @@ __global__ void __launch_bounds__(kDispChunk) dispatch_place_kernel(RouteParams 
   }
 }
 
-__global__ void convert_x_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xh, long n8) {
+// The f16 copy of x the expert kernels read: exact for |x| in [2^-14, 65504]
+// (bf16 has 8 significant bits, f16 11); an element beyond 65504 (or not
+// finite) records MOE_ERANGE in the status word.
+__global__ void convert_x_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xh, long n8,
+                                 int* status) {
+  bool bad = false;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long)gridDim.x * blockDim.x) {
     const uint4 raw = reinterpret_cast<const uint4*>(x)[i];
     const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -161,19 +166,21 @@ __global__ void convert_x_kernel(const uint16_t* __restrict__ x, uint16_t* __res
       const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16),
                                           __uint_as_float(in[q] & 0xFFFF0000u));
       o[q] = *reinterpret_cast<const uint32_t*>(&h);
+      bad |= f16x2_nonfinite(o[q]);
     }
     reinterpret_cast<uint4*>(xh)[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  if (bad) *status = kStatusRange;
 }
 
 }  // namespace
 
-cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, cudaStream_t st) {
+cudaError_t launch_convert_x(const uint16_t* x, uint16_t* xh, long n, int* status, cudaStream_t st) {
   const long n8 = n / 8;
   long blocks = (n8 + 255) / 256;
   if (blocks > 152 * 8) blocks = 152 * 8;
   if (blocks < 1) blocks = 1;
-  convert_x_kernel<<<(int)blocks, 256, 0, st>>>(x, xh, n8);
+  convert_x_kernel<<<(int)blocks, 256, 0, st>>>(x, xh, n8, status);
   return cudaGetLastError();
 }
 
@@ -185,7 +192,7 @@ int router_ksplit(int T, int H, int E) {
   const int tiles = (E + 15) / 16, groups = (T + kTokTile - 1) / kTokTile;
   const int C = H / 64, target = T <= 2 * kTokTile ? 128 : 1024;
   int ks = (target + tiles * groups - 1) / (tiles * groups);
-  if (ks > 8) ks = 8;
+  if (ks > kMaxKsplitHost) ks = kMaxKsplitHost;
   if (ks > C) ks = C;
   // a slice's 8 staged token rows must fit the kernel's shared memory
   // (launch_router: 8 x (slice + 8) bf16 + 4 KB <= 200 KB): at most 12288 columns
@@ -197,13 +204,13 @@ int router_ksplit(int T, int H, int E) {
 
 size_t route_finish_smem(int E) { return (size_t)(64 + (kFinishThreads / 32) * E) * sizeof(int); }
 
-cudaError_t launch_router(const RouteParams& p, cudaStream_t st) {
+cudaError_t launch_router(const RouteParams& p, cudaStream_t st, bool pdl) {
   const int C = p.H / 64;
   const int max_klen = ((C + p.ksplit - 1) / p.ksplit) * 64;
   const size_t smem = (size_t)kTokTile * (max_klen + 8) * 2 + kRouterThreads * 4 * sizeof(float);
   dim3 grid((p.E + 15) / 16, (p.T + kTokTile - 1) / kTokTile, p.ksplit);
-  // launched early: only the weight reads run before the previous kernels finish
-  return launch_k(router_kernel, grid, dim3(kRouterThreads), smem, st, true, p);
+  // with pdl, launched early: only the weight reads run before the previous kernels finish
+  return launch_k(router_kernel, grid, dim3(kRouterThreads), smem, st, pdl, p);
 }
 
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st) {

@@ -13,7 +13,7 @@ namespace {
 
 constexpr int kRouterThreads = 256;
 constexpr int kFinishThreads = 1024;
-constexpr int kMaxKsplit = 8;  // router K slices at most
+constexpr int kMaxKsplit = kMaxKsplitHost;  // router K slices at most
 
 // ---------------------------------------------------------------- router logits
 // ---------------------------------------------------------------- router logits
@@ -66,16 +66,19 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
     const size_t off = (size_t)(t0 + r) * p.H + kbase + 8 * v;
     const uint4 raw = *reinterpret_cast<const uint4*>(p.x + off);
     *reinterpret_cast<uint4*>(xs + r * stride + 8 * v) = raw;
-    if (write_xh) {  // the f16 copy the expert kernels read (exact for |x| in f16's normal range)
+    if (write_xh) {  // the f16 copy the expert kernels read (exact for |x| in [2^-14, 65504])
       const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
       uint32_t o[4];
+      bool bad = false;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16),
                                             __uint_as_float(in[q] & 0xFFFF0000u));
         o[q] = *reinterpret_cast<const uint32_t*>(&h);
+        bad |= f16x2_nonfinite(o[q]);
       }
       *reinterpret_cast<uint4*>(p.xh + off) = make_uint4(o[0], o[1], o[2], o[3]);
+      if (bad && p.status) *p.status = kStatusRange;  // |x| beyond f16's range
     }
   }
   __syncthreads();
@@ -118,9 +121,12 @@ __device__ __forceinline__ void router_partials(const RouteParams& p, int tile, 
 // The sigmoid router's score of a logit (fp32).
 __device__ __forceinline__ float sigmoid_score(float l) { return 1.0f / (1.0f + expf(-l)); }
 
-// Order-preserving map of an fp32 value to a uint32 key (larger value, larger key).
+// Order-preserving map of an fp32 value to a uint32 key (larger value, larger
+// key).  -0 and +0 compare equal, so both get the key of +0: a tie between
+// them goes to the lower expert id like any other tie.
 __device__ __forceinline__ uint32_t f32_key(float v) {
-  const uint32_t u = __float_as_uint(v);
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ float key_f32(uint32_t k) {
@@ -361,7 +367,7 @@ __device__ int block_excl_scan(int v, int* sc, int* total) {
 
 __device__ __forceinline__ int checked_expert(const RouteParams& p, int e) {
   if (e < 0 || e >= p.E) {
-    *p.status = -1;  // MOE_EINVAL
+    *p.status = kStatusInvalid;
     return 0;
   }
   return e;

@@ -136,7 +136,7 @@ __device__ __forceinline__ bool tc_entry(const ExpertParams& p, int y, int& expe
   row = e.y;
   n = e.z;
   if (expert < 0 || expert >= p.E || n < 1 || n > kTcMaxN || row < 0 || row + n > S) {
-    *p.status = -1;  // MOE_EINVAL
+    *p.status = kStatusInvalid;
     return false;
   }
   return true;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_router_kernel(ExpertParams p
       mbar_arrive(&sh->full[c % kTcStages]);
       const int cn = c + kTcLookahead;
       if (cn < KC) {
-        if (!mbar_wait(&sh->empty[cn % kTcStages], ((cn / kTcStages) & 1) ^ 1, abort)) break;
+        if (!mbar_wait(&sh->empty[cn % kTcStages], ((cn / kTcStages) & 1) ^ 1, abort, p.wait_budget)) break;
         issue(cn);
       }
       cp_async_commit();
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_router_kernel(ExpertParams p
       const uint32_t a_s = smem_u32(A), b_s = smem_u32(B);
       for (int c = 0; c < KC; ++c) {
         const int stage = c % kTcStages;
-        if (!mbar_wait(&sh->full[stage], (c / kTcStages) & 1, abort)) break;
+        if (!mbar_wait(&sh->full[stage], (c / kTcStages) & 1, abort, p.wait_budget)) break;
         tc_fence_after();
         const uint64_t ad = sw128_desc(a_s + stage * kTcAStageBytes);
         const uint64_t bd = sw128_desc(b_s + stage * b_stage);
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_router_kernel(ExpertParams p
 
   // ---------------------------------------------------------------- epilogue
   bool ok = true;
-  if (warp < 8) ok = mbar_wait(&sh->acc_full, 0, abort);
+  if (warp < 8) ok = mbar_wait(&sh->acc_full, 0, abort, p.wait_budget);
   if (warp < 8 && !ok) mbar_drain(&sh->acc_full, 0);  // MMAs in flight finish before TMEM is freed
   tc_fence_after();
   if (warp < 8 && ok && !*abort) {
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_router_kernel(ExpertParams p
       }
     }
   }
-  if (*abort && tid == 0) *p.status = -5;  // MOE_ETIMEOUT
+  if (*abort && tid == 0) *p.status = kStatusTimeout;
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         }
       }
       // (waits are made warp-uniform: the warps arrive with one lane after a __syncwarp)
-      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->r_full[c % kTxNR], (c / kTxNR) & 1, abort))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->r_full[c % kTxNR], (c / kTxNR) & 1, abort, p.wait_budget))) break;
       uint4 cv[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         const int m = half + 2 * i;
         if (m >= G) break;
         const int q = c * G + m, slot = q % kTxNA;
-        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->a_empty[slot], ((q / kTxNA) & 1) ^ 1, abort))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->a_empty[slot], ((q / kTxNA) & 1) ^ 1, abort, p.wait_budget))) {
           ok = false;
           break;
         }
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       // refill: chunk c + kTxLB goes to the B stage the MMAs of chunk c + kTxLB - kTxNB freed
       const int cn = c + kTxLB;
       if (cn < KC && half == 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->b_empty[cn % kTxNB], ((cn / kTxNB) & 1) ^ 1, abort)))
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->b_empty[cn % kTxNB], ((cn / kTxNB) & 1) ^ 1, abort, p.wait_budget)))
           break;
         issue_b(cn);
       }
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         const uint64_t bd = sw128_desc(b_s + (c % kTxNB) * b_stage);
         for (int m = 0; m < G; ++m) {
           const int q = c * G + m, slot = q % kTxNA;
-          if (!mbar_wait_sleep(&sh->a_full[slot], (q / kTxNA) & 1, abort)) {
+          if (!mbar_wait_sleep(&sh->a_full[slot], (q / kTxNA) & 1, abort, p.wait_budget)) {
             ok = false;
             break;
           }
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       int issued = 0;  // code chunks issued
       for (int c = 0; c < KC; ++c) {
         const int s = c >> 3, j = c & 7;
-        if (!mbar_wait_sleep(&sh->r_empty[c % kTxNR], ((c / kTxNR) & 1) ^ 1, abort)) break;
+        if (!mbar_wait_sleep(&sh->r_empty[c % kTxNR], ((c / kTxNR) & 1) ^ 1, abort, p.wait_budget)) break;
         mbar_arrive_expect(&sh->r_full[c % kTxNR], (uint32_t)RB);
         tma_load_tiles(r_s + (c % kTxNR) * RB, map, 9 * s + 1 + j, tile0, expert,
                        &sh->r_full[c % kTxNR]);
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 
   // ---------------------------------------------------------------- epilogue
   bool ok = true;
-  if (warp < kTxPW) ok = mbar_wait_sleep(&sh->acc_full, 0, abort);
+  if (warp < kTxPW) ok = mbar_wait_sleep(&sh->acc_full, 0, abort, p.wait_budget);
   if (warp < kTxPW && !ok) mbar_drain(&sh->acc_full, 0);  // MMAs in flight finish before TMEM is freed
   tc_fence_after();
   if (warp < kTxPW && ok && !*abort) {
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             if (lane < 16 && col < n) {
               const float Gv = ts_g * mine, U = ts_u * other;
               const float a = Gv / (1.0f + expf(-Gv)) * U;
-              p.abuf[(size_t)(row0 + col) * p.I + i] = __half_as_ushort(__float2half_rn(a));
+              p.abuf[(size_t)(row0 + col) * p.I + i] = a_to_f16(a, p.status);
             }
           }
         }
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       }
     }
   }
-  if (*abort && tid == 0) *p.status = -5;  // MOE_ETIMEOUT
+  if (*abort && tid == 0) *p.status = kStatusTimeout;
   tc_fence_before();
   __syncthreads();
   if (warp == kTxPW) {

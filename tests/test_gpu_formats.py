@@ -206,3 +206,38 @@ def test_device_built_layer_dequant_bit_exact(widx, experts):
     arena, per_expert = L.info()
     assert arena == per_expert * w.n_experts_total
     L.close()
+
+
+@pytest.mark.parametrize("fmt,shared", [(1, 0), (1, 1), (2, 1), (3, 1)])
+def test_pack_weights_whole_layer_from_host(fmt, shared):
+    """moe_pack_weights: router, bias and every expert's three matrices (the
+    shared expert last) packed from host arrays in the canonical format, here
+    the oracle's own quantisation.  Every matrix decodes bit-exactly to the
+    oracle's dequantisation, and the forward gives the bits of the same layer
+    built on the device (device quantiser + per-matrix packer)."""
+    H, I = (256, 128)
+    w = gen.Workload(f"pack-{fmt}-{shared}", H, I, 8, 2, shared, 5, fmt, "normal", 0.0, 0.1, 21)
+    ol = oracle.layer_for_workload(w)
+    L = moe.MoeLayer(w.fmt, w.H, w.I, w.E, w.k, w.shared)
+    ref = build_layer(w, T_max=w.T)
+    try:
+        L.reserve(w.T)
+        L.pack_weights(gen.router_weights(w), gen.router_bias(w), ol.mats)
+        for e in range(w.n_experts_total):
+            for m in range(3):
+                rows, K = gen.matrix_shape(w, m)
+                got = torch.empty((rows, K), dtype=torch.float32, device="cuda")
+                L.debug_dequant(e, m, got)
+                torch.cuda.synchronize()
+                assert np.array_equal(got.cpu().numpy(), ol.dequant(e, m)), (e, m)
+        x = torch.from_numpy(gen.x_tokens(w).view(np.int16)).cuda()
+        a = torch.full((w.T, w.H), float("nan"), device="cuda")
+        b = torch.full((w.T, w.H), float("nan"), device="cuda")
+        L.forward(x, a)
+        ref.forward(x, b)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+        assert L.status() == 0
+    finally:
+        L.close()
+        ref.close()

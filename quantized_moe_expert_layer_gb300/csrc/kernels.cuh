@@ -77,7 +77,7 @@ struct RouteParams {
   int* status;
 };
 
-// Slots per CTA of the several-CTA dispatch (count, scan, place), used when
+// Slots per CTA of the several-CTA dispatch (count, then scan + place), used when
 // T*k is above kDispOneCtaMax; below it one CTA does the whole dispatch.
 constexpr int kDispChunk = 1024;
 constexpr int kDispOneCtaMax = 8192;
@@ -102,7 +102,7 @@ int router_ksplit(int T, int H, int E);
 // the router weights before its wait: they must not be written by that kernel)
 cudaError_t launch_router(const RouteParams& p, cudaStream_t st, bool pdl = true);
 cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cudaStream_t st);
-// Dispatch of p.idx (top-k done): one CTA, or count / scan / place kernels
+// Dispatch of p.idx (top-k done): one CTA, or count and scan + place kernels
 // for T*k > kDispOneCtaMax.  dispatch_launches: how many kernels that is.
 cudaError_t launch_dispatch(const RouteParams& p, bool pdl, cudaStream_t st);
 int dispatch_launches(int S);

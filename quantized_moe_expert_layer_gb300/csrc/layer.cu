@@ -318,7 +318,7 @@ bool small_path(moe_layer* L, int T) { return small_route_ok(T, L->k) && fused_d
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
   if (small_path(L, T)) return 3;
-  // (convert x, tc router | router), top-k, dispatch (1 or 3 kernels); T <= 16: router, top-k + dispatch
+  // (convert x, tc router | router), top-k, dispatch (1 or 2 kernels); T <= 16: router, top-k + dispatch
   const int dispatch = dispatch_launches(T * L->k);
   const int routing = tc_router(L, T) ? 3 + dispatch : (T <= kFusedTopkMaxT ? 2 : 2 + dispatch);
   if (tc_path(L, T)) return routing + 3;

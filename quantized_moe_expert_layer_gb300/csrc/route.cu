@@ -53,6 +53,17 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
   }
 }
 
+// Top-k of many tokens (T >= kTopkWarpMinT): one warp per token, 8 tokens per
+// CTA; each lane holds E/32 logits, all requested at once, and takes k
+// arg-max rounds (topk_token).  Same picks, order and gates as topk_kernel.
+constexpr int kTopkWarpMinT = 1024;
+__global__ void __launch_bounds__(256) topk_warp_kernel(RouteParams p) {
+  griddep_launch();
+  griddep_wait();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < p.T) topk_token(p, t, threadIdx.x & 31, nullptr);
+}
+
 __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParams p, int do_topk) {
   griddep_launch();
   griddep_wait();
@@ -86,45 +97,43 @@ __global__ void __launch_bounds__(kDispChunk) dispatch_count_kernel(RouteParams 
   for (int i = tid; i < E; i += blockDim.x) p.blk[(size_t)b * E + i] = hist_c[i];
 }
 
-// Per expert (thread e < E, blockDim.x >= E): the chunks' counts become the
-// expert's rows before each chunk (in place); counts, offsets, entries.
-__global__ void __launch_bounds__(1024) dispatch_scan_kernel(RouteParams p, int nb) {
+// Stable placement of chunk b (one slot per thread): row = offsets[e] + rows
+// of e in earlier chunks + rows of e in earlier warps of this chunk + rank
+// among the warp's lanes.  Every CTA sums the per-chunk counts itself
+// (thread e < E reads expert e's column: its rows in all chunks and in the
+// chunks before b; 16 loads in flight) and scans them over the experts, so no
+// single CTA walks the chunks; CTA 0 also writes counts, offsets, the work
+// entries and the shared expert's rows.  Needs blockDim.x >= E.
+__global__ void __launch_bounds__(kDispChunk) dispatch_place_kernel(RouteParams p, int nb) {
   griddep_launch();
   griddep_wait();
-  __shared__ int sc[64];
-  const int tid = threadIdx.x, E = p.E;
-  int c = 0;
+  extern __shared__ int hist_p[];  // [warps][E], then 64 ints of scan scratch
+  const int b = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int E = p.E, S = p.T * p.k, NW = blockDim.x >> 5;
+  int* sc = hist_p + NW * E;
+  int before = 0, total = 0;
   if (tid < E) {
-    for (int b0 = 0; b0 < nb; b0 += 16) {  // 16 loads in flight, then the running sum
+    for (int b0 = 0; b0 < nb; b0 += 16) {
       int v[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) v[u] = (b0 + u < nb) ? p.blk[(size_t)(b0 + u) * E + tid] : 0;
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (b0 + u < nb) {
-          p.blk[(size_t)(b0 + u) * E + tid] = c;
-          c += v[u];
-        }
+      for (int u = 0; u < 16; ++u) {
+        before += (b0 + u < b) ? v[u] : 0;
+        total += v[u];
+      }
     }
   }
-  int total;
-  const int excl = block_excl_scan(tid < E ? c : 0, sc, &total);
-  if (tid < E) {
-    p.counts[tid] = c;
-    p.offsets[tid] = excl;
+  int all;
+  const int excl = block_excl_scan(tid < E ? total : 0, sc, &all);
+  if (b == 0) {  // (uniform in the CTA: write_entries synchronises every thread)
+    if (tid < E) {
+      p.counts[tid] = total;
+      p.offsets[tid] = excl;
+    }
+    if (tid == 0) p.offsets[E] = all;
+    write_entries(p, total, excl, sc);
   }
-  if (tid == 0) p.offsets[E] = total;
-  write_entries(p, c, excl, sc);
-}
-
-// Stable placement of chunk b: row = offsets[e] + rows of e in earlier chunks
-// + rows of e in earlier warps of this chunk + rank among the warp's lanes.
-__global__ void __launch_bounds__(kDispChunk) dispatch_place_kernel(RouteParams p) {
-  griddep_launch();
-  griddep_wait();
-  extern __shared__ int hist_p[];  // [warps][E]
-  const int b = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int E = p.E, S = p.T * p.k, NW = blockDim.x >> 5;
   for (int i = tid; i < NW * E; i += blockDim.x) hist_p[i] = 0;
   __syncthreads();
   const int s = b * kDispChunk + tid;
@@ -134,8 +143,9 @@ __global__ void __launch_bounds__(kDispChunk) dispatch_place_kernel(RouteParams 
   const int rank = __popc(peers & lanemask_lt());
   if (valid && lane == __ffs(peers) - 1) hist_p[w * E + e] = __popc(peers);
   __syncthreads();
-  for (int x = tid; x < E; x += blockDim.x) {
-    int run = p.offsets[x] + p.blk[(size_t)b * E + x];
+  if (tid < E) {
+    const int x = tid;
+    int run = excl + before;
     for (int ww = 0; ww < NW; ++ww) {
       const int v = hist_p[ww * E + x];
       hist_p[ww * E + x] = run;
@@ -214,6 +224,8 @@ cudaError_t launch_router(const RouteParams& p, cudaStream_t st, bool pdl) {
 }
 
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st) {
+  if (p.T >= kTopkWarpMinT)
+    return launch_k(topk_warp_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, pdl, p);
   return launch_k(topk_kernel, dim3(p.T), dim3(256), 0, st, pdl, p);
 }
 
@@ -222,7 +234,7 @@ cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cu
                   pdl, p, do_topk ? 1 : 0);
 }
 
-int dispatch_launches(int S) { return S > kDispOneCtaMax ? 3 : 1; }
+int dispatch_launches(int S) { return S > kDispOneCtaMax ? 2 : 1; }
 
 cudaError_t launch_dispatch(const RouteParams& p, bool pdl, cudaStream_t st) {
   const int S = p.T * p.k;
@@ -230,10 +242,9 @@ cudaError_t launch_dispatch(const RouteParams& p, bool pdl, cudaStream_t st) {
   const int nb = (S + kDispChunk - 1) / kDispChunk;
   cudaError_t e = launch_k(dispatch_count_kernel, dim3(nb), dim3(kDispChunk), p.E * sizeof(int),
                            st, pdl, p);
-  if (e == cudaSuccess) e = launch_k(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, pdl, p, nb);
   if (e == cudaSuccess)
     e = launch_k(dispatch_place_kernel, dim3(nb), dim3(kDispChunk),
-                 (size_t)(kDispChunk / 32) * p.E * sizeof(int), st, pdl, p);
+                 ((size_t)(kDispChunk / 32) * p.E + 64) * sizeof(int), st, pdl, p, nb);
   return e;
 }
 
@@ -242,7 +253,7 @@ cudaError_t route_kernels_init() {
                                        200 * 1024);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(dispatch_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (kDispChunk / 32) * kMaxE * (int)sizeof(int));
+                           ((kDispChunk / 32) * kMaxE + 64) * (int)sizeof(int));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)route_finish_smem(kMaxE));

@@ -43,6 +43,7 @@ METRIC = "routed tokens/s per MoE layer on 1 GB300; HBM GB/s as % of ~8 TB/s roo
 UNIT = "tokens/s"
 WORKLOAD = 4  # prefill-h2048-i512-e512-k10-s1-t4096-nvfp4: the largest config
 PER_CONFIG = [1, 2, 3]  # decode NVFP4, decode FP6, batched T=64: timed in the same run
+                        # (and the prefill with W4A4 activations)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -408,7 +409,7 @@ def graph_time_us(s, fn, reps, warm=3):
     return e0.elapsed_time(e1) * 1e3 / reps
 
 
-def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False):
+def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, act=0):
     """Builds Ln layer instances of workload w, captures one step (the T
     tokens through the Ln layers) as a CUDA graph and times `steps` replays
     after `warmup` (CUDA events, max over ranks).  Also times the dominant
@@ -422,6 +423,8 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False):
     T = w.T
     masks = [placement_mask(w, host_mirror, 1000 * rank + i) for i in range(Ln)]
     layers = [build_layer(w, T_max=T, seed=1000 * rank + i, in_hbm=masks[i]) for i in range(Ln)]
+    for L in layers:
+        L.set_act_format(act)
     x_np = gen.x_tokens(w, T, first=rank * T)
     x = torch.from_numpy(x_np.view(np.int16)).cuda()
     outs = [torch.empty((T, w.H), dtype=torch.float32, device="cuda") for _ in range(Ln)]
@@ -627,16 +630,18 @@ def run_ours(args, w):
     r = measure(w, Ln, args.steps, args.warmup, rank, world, args.host_mirror, headline=True)
     per_config = {}
     if args.per_config:
-        for idx in PER_CONFIG:
+        # the other configurations, then the headline's shape with W4A4 activations
+        for idx, act in [(i, 0) for i in PER_CONFIG] + [(WORKLOAD, 1)]:
             wc = gen.get_workload(idx)
-            if wc.name == w.name:
+            if wc.name == w.name and act == 0:
                 continue
             Lc = default_layers(wc)
             # each config's timed region: about a second of replays
-            one = measure(wc, Lc, max(20, args.warmup), 3, rank, world)
+            one = measure(wc, Lc, max(20, args.warmup), 3, rank, world, act=act)
             steps_c = max(20, min(5000, int(1.0 / max(one["ms"] * 1e-3 / max(20, args.warmup), 1e-6))))
-            rc = measure(wc, Lc, steps_c, 3, rank, world)
-            per_config[wc.name] = {
+            rc = measure(wc, Lc, steps_c, 3, rank, world, act=act)
+            per_config[wc.name + ("-w4a4" if act else "")] = {
+                "activations": "nvfp4 per row (W4A4)" if act else "bf16 x, fp32 a (W4A16)",
                 "tokens_per_step": wc.T, "layer_instances_per_step": Lc, "steps": steps_c,
                 "value": rc["value"], "unit": UNIT, "us_per_layer": rc["us_per_layer"],
                 "format": SHORT_NAMES[wc.fmt], "gpu_launches_per_layer": rc["launches_per_layer"],

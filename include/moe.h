@@ -160,6 +160,24 @@ int moe_set_router(moe_layer* L, const uint16_t* wr_bf16, const float* bias, int
 enum moe_router_mode { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 };
 int moe_set_router_mode(moe_layer* L, int mode);
 
+/* Activation format of the following forwards (default MOE_ACT_BF16):
+ *   MOE_ACT_BF16: W4A16, the activations x and a = silu(g) * u stay exact
+ *     (bf16 x, fp32 a; multiplied as f16 copies, see "Value range");
+ *   MOE_ACT_NVFP4: W4A4, the knivesysl README's nvfp4 tier with four-bit
+ *     activations ("nvfp4 w4a4 for every projection", the table of supported
+ *     service formats): x of each token before gate/up, and a of each
+ *     (token, expert) row (fp32) before down, are quantised to NVFP4 per row
+ *     with the weights' recipe (one fp32 tensor scale per row,
+ *     moe_quantize_act_nvfp4), and the products take the dequantised values.
+ *     The router keeps bf16 x.  The values stay within f16 (|code x block
+ *     scale| <= 2688) and the tensor scales multiply the fp32 accumulators,
+ *     so x and a have no f16 range limit in this mode.  The products run on
+ *     the same tensor-core instructions as W4A16 (f16 operands, exact), not
+ *     on the block-scaled FP4 MMA.
+ * MOE_EINVAL for an unknown format. */
+enum moe_act_format { MOE_ACT_BF16 = 0, MOE_ACT_NVFP4 = 1 };
+int moe_set_act_format(moe_layer* L, int fmt);
+
 /* Pack one expert matrix from the canonical quantised format into the layer's
  * device layout.  The formats are those of the knivesysl README, the
  * paragraph under the table of supported service formats (e2m3 with a
@@ -209,6 +227,15 @@ int moe_pack_weights(moe_layer* L, const uint16_t* wr_bf16, const float* bias,
  * tscale [1].  K % 16 == 0.  Uses no workspace beyond its outputs. */
 int moe_quantize_nvfp4(const float* W, int rows, int K, uint8_t* codes, uint8_t* scales,
                        float* tscale, void* stream);
+
+/* Quantise activation rows to canonical NVFP4 on the device, one tensor scale
+ * per row (the W4A4 activations of moe_set_act_format): in [rows x K] bf16
+ * bits (in_bf16 != 0) or fp32, device; per row tscale = amax(row) / (6 * 448)
+ * and the recipe of moe_quantize_nvfp4 per 16 values.  Device outputs codes
+ * [rows x K/2], scales [rows x K/16], tscale [rows].  K % 16 == 0; in and
+ * codes 16-byte aligned. */
+int moe_quantize_act_nvfp4(const void* in, int in_bf16, int rows, int K, uint8_t* codes,
+                           uint8_t* scales, float* tscale, void* stream);
 
 /* Quantise fp32 weights W [rows x K] (device) to canonical FP6 e2m3 on the
  * device (the knivesysl README's fp6, a power-of-two scale per 128 weights): per 128 weights the exponent E = the smallest integer with

@@ -28,6 +28,7 @@ FMT_FP6 = 2
 FMT_MXFP4 = 3
 GATE, UP, DOWN = 0, 1, 2
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
+ACT_BF16, ACT_NVFP4 = 0, 1
 HOST, DEVICE = 0, 1
 
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT, ERANGE = 0, -1, -2, -3, -4, -5, -6
@@ -40,7 +41,7 @@ EXPORTS = [
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
     "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches", "moe_place_experts",
     "moe_layer_placement", "moe_set_wait_budget", "moe_debug_fail_alloc",
-    "moe_debug_check_workspace"
+    "moe_debug_check_workspace", "moe_set_act_format", "moe_quantize_act_nvfp4"
 ]
 
 _lock = threading.Lock()
@@ -124,6 +125,8 @@ def lib():
                 "moe_set_wait_budget": (I, [P, ctypes.c_int64]),
                 "moe_debug_fail_alloc": (I, [I]),
                 "moe_debug_check_workspace": (I, [P, ctypes.POINTER(I)]),
+                "moe_set_act_format": (I, [P, I]),
+                "moe_quantize_act_nvfp4": (I, [P, I, I, I, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -216,6 +219,10 @@ class MoeLayer:
         """Budget (clock64 cycles) of each bounded wait in the tensor-core
         kernels; 0 restores the default (about one second)."""
         check(lib().moe_set_wait_budget(self.h, int(cycles)))
+
+    def set_act_format(self, fmt):
+        """ACT_BF16 (W4A16, default) or ACT_NVFP4 (W4A4: activations quantised per row)."""
+        check(lib().moe_set_act_format(self.h, fmt))
 
     def check_workspace(self):
         """Guard bytes of the workspace that a kernel overwrote (0 = none)."""
@@ -318,6 +325,16 @@ def quantize_fp6(W, codes, exps, stream=None):
 def quantize_mxfp4(W, codes, exps, stream=None):
     rows, K = W.shape
     check(lib().moe_quantize_mxfp4(_ptr(W), rows, K, _ptr(codes), _ptr(exps), _stream(stream)))
+
+
+def quantize_act_nvfp4(A, codes, scales, tscale, stream=None):
+    """Activation rows A [rows x K] (bf16 bits as int16/uint16, or fp32) to
+    canonical NVFP4 with one tensor scale per row."""
+    import torch
+    rows, K = A.shape
+    in_bf16 = 1 if A.dtype in (torch.int16, torch.bfloat16) else 0
+    check(lib().moe_quantize_act_nvfp4(_ptr(A), in_bf16, rows, K, _ptr(codes), _ptr(scales),
+                                       _ptr(tscale), _stream(stream)))
 
 
 def route_noalloc(x, wr, bias, E, k, logits, idx, gates, stream=None):

@@ -36,8 +36,9 @@ __global__ void __launch_bounds__(kThreads, SMEM ? 3 : 2) gateup_kernel(ExpertPa
   // Shared-expert entries need no routing.  Routed ones wait for it, and only
   // then let the next kernel start: once every CTA here has triggered, the
   // routing outputs (work entries) are complete and the next kernel may read
-  // them before its own wait.
-  if (y >= p.nsh) griddep_wait();
+  // them before its own wait.  With quantised activations (W4A4) every entry
+  // reads the quantised x, written before the router: all of them wait.
+  if (y >= p.nsh || p.ts_x) griddep_wait();
   griddep_launch();
   int expert, row, n;
   if (!get_entry(p, y, expert, row, n)) return;
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, PATH == 1 || PATH == 3 ? 3 : 2) gate
   __shared__ float red[kThreads * 8];
   extern __shared__ __align__(16) uint8_t gu_smem[];
   if (y < p.nsh) {
+    if (p.ts_x) griddep_wait();  // W4A4: the quantised x (written before the router)
     griddep_launch();
     int expert, row, n;
     if (get_entry(p, y, expert, row, n)) gateup_any_task<FMT, PATH>(p, expert, row, n, tpc, gu_smem, red);
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, PATH == 1 || PATH == 3 ? 3 : 2) gate
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stream_kernel(ExpertParams p) {
   const int y = blockIdx.y;
-  if (MODE == 1 || y >= p.nsh) griddep_wait();
+  if (MODE == 1 || y >= p.nsh || p.ts_x) griddep_wait();
   griddep_launch();
   int expert, row, n;
   if (!get_entry(p, y, expert, row, n)) return;
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(ExpertParams p, int t
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = 16 * tile + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
-    if (col < n) p.ybuf[(size_t)(row + col) * p.H + r] = ts * v[i];
+    if (col < n) p.ybuf[(size_t)(row + col) * p.H + r] = (ts * a_scale(p, row + col)) * v[i];
   }
 }
 

@@ -260,6 +260,33 @@ __device__ __forceinline__ bool get_entry(const ExpertParams& p, int y, int& exp
   return true;
 }
 
+// W4A4: the activation tensor scale of token `tok`, and of row `row` of a
+// (1 otherwise; ts * 1.0f is ts exactly, so the W4A16 path keeps its bits).
+__device__ __forceinline__ float x_scale(const ExpertParams& p, int tok) {
+  return p.ts_x ? p.ts_x[tok] : 1.0f;
+}
+__device__ __forceinline__ float a_scale(const ExpertParams& p, int row) {
+  return p.ts_a ? p.ts_a[row] : 1.0f;
+}
+// Token of row `row` of abuf: the shared expert's rows S..S+T-1 are tokens 0..T-1.
+__device__ __forceinline__ int row_tok(const ExpertParams& p, int row) {
+  const int S = p.T * p.k;
+  return row >= S ? row - S : p.row_token[row];
+}
+// The SwiGLU output a of (row, column r): f16 for the down kernels, or fp32
+// for the W4A4 quantiser.
+__device__ __forceinline__ void store_a(const ExpertParams& p, size_t row, int r, float a) {
+  if (p.af)
+    p.af[row * p.I + r] = a;
+  else
+    p.abuf[row * p.I + r] = a_to_f16(a, p.status);
+}
+// Shared-expert entries run ahead of the router and convert x themselves,
+// unless x was quantised (W4A4): then every entry reads the quantised copy.
+__device__ __forceinline__ bool convert_x(const ExpertParams& p, bool shared_entry) {
+  return shared_entry && !p.ts_x;
+}
+
 // Sum the per-warp partials of warps sharing a tile (fixed order) into warp ks == 0.
 template <int NV>
 __device__ __forceinline__ void reduce_ksplit(float* red, float (&v)[NV], int tpc, int nks) {
@@ -297,18 +324,18 @@ __device__ __forceinline__ void gateup_task(const ExpertParams& p, int expert, i
                                    eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
   // routed entries read the router's f16 copy of x; the shared expert's
   // entries run ahead of the router and read (and convert) x itself
-  const bool shared_entry = expert == p.E;
+  const bool shared_entry = expert == p.E, cvt = convert_x(p, shared_entry);
   const uint16_t* brow = nullptr;
   if (gi < n) {
     const int tok = shared_entry ? row - S + gi : p.row_token[row + gi];
-    brow = (shared_entry ? p.x : p.xh) + (size_t)tok * p.H;
+    brow = (cvt ? p.x : p.xh) + (size_t)tok * p.H;
   }
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   if (valid) {
     // the warp's later K-units are requested from L2 now, so their loads do not wait on HBM
     prefetch_tile(FMT, tiles[0], g, ks + nks, nks);
     prefetch_tile(FMT, tiles[1], g, ks + nks, nks);
-    tiles_mma<FMT, 2>(tiles, g, ks, nks, brow, shared_entry, acc);
+    tiles_mma<FMT, 2>(tiles, g, ks, nks, brow, cvt, acc);
   }
   float v[8];
 #pragma unroll
@@ -323,9 +350,10 @@ __device__ __forceinline__ void gateup_task(const ExpertParams& p, int expert, i
   for (int i = 0; i < 4; ++i) {
     const int r = 16 * pair + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
     if (col < n) {
-      const float G = ts_g * v[i], U = ts_u * v[4 + i];
+      const float sx = x_scale(p, row_tok(p, row + col));
+      const float G = (ts_g * sx) * v[i], U = (ts_u * sx) * v[4 + i];
       const float a = G / (1.0f + expf(-G)) * U;
-      p.abuf[(size_t)(row + col) * p.I + r] = a_to_f16(a, p.status);
+      store_a(p, row + col, r, a);
     }
   }
 }
@@ -472,8 +500,8 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
   const uint8_t* const tiles[2] = {eb + (size_t)(2 * pair) * p.gu_tile_bytes,
                                    eb + (size_t)(2 * pair + 1) * p.gu_tile_bytes};
   const uint32_t wst = smem_u32(smem) + warp * nst * sbytes;
-  const bool shared_entry = expert == p.E;
-  const uint16_t* xsrc = shared_entry ? p.x : p.xh;
+  const bool shared_entry = expert == p.E, cvt = convert_x(p, shared_entry);
+  const uint16_t* xsrc = cvt ? p.x : p.xh;
   auto tok_of = [&](int r) { return shared_entry ? row - S + r : p.row_token[row + r]; };
   if (warp < nh) nv_unit_copy(tiles, g, warp, wst, xsrc, p.H, n, p.T, tok_of);
   cp_async_commit();
@@ -492,7 +520,7 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
     cp_async_wait<1>();
     __syncwarp();  // the other lanes' token-row pieces of this stage
     nv_units_mma<2>(g, hh, st, st + kNvUnitBytes + 2 * (xslot > 0 ? xslot : 0) * kNvXStride,
-                    xslot >= 0, shared_entry, acc);
+                    xslot >= 0, cvt, acc);
     __syncwarp();  // every lane is done with the stage before it is refilled
     if (hh + 2 * kWarps < nh)
       nv_unit_copy(tiles, g, hh + 2 * kWarps, st, xsrc, p.H, n, p.T, tok_of);
@@ -520,9 +548,10 @@ __device__ __forceinline__ void gateup_task_nv(const ExpertParams& p, int expert
   for (int i = 0; i < 4; ++i) {
     const int r = 16 * pair + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
     if (col < n) {
-      const float G = ts_g * v[i], U = ts_u * v[4 + i];
+      const float sx = x_scale(p, row_tok(p, row + col));
+      const float G = (ts_g * sx) * v[i], U = (ts_u * sx) * v[4 + i];
       const float a = G / (1.0f + expf(-G)) * U;
-      p.abuf[(size_t)(row + col) * p.I + r] = a_to_f16(a, p.status);
+      store_a(p, row + col, r, a);
     }
   }
 }
@@ -683,7 +712,7 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
     const uint32_t dst = xs_base + 2 * ((by_token ? tok : r) * xs + 8 * c);
     if (MODE == 1) {
       cp_async16(dst, p.abuf + (size_t)(row + r) * p.I + 8 * c);
-    } else if (!shared_entry) {
+    } else if (!convert_x(p, shared_entry)) {
       cp_async16(dst, p.xh + (size_t)tok * p.H + 8 * c);
     } else {  // the shared expert's entries run ahead of the router: convert x here
       const uint4 q = *reinterpret_cast<const uint4*>(p.x + (size_t)tok * p.H + 8 * c);
@@ -748,10 +777,11 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
     for (int i = 0; i < 4; ++i) {
       const int r = 16 * idx + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
       if (col < n) {
-        const float G = ts_g * (acc[0][0][i] + acc[0][1][i]);
-        const float U = ts_u * (acc[NT - 1][0][i] + acc[NT - 1][1][i]);
+        const float sx = x_scale(p, row_tok(p, row + col));
+        const float G = (ts_g * sx) * (acc[0][0][i] + acc[0][1][i]);
+        const float U = (ts_u * sx) * (acc[NT - 1][0][i] + acc[NT - 1][1][i]);
         const float a = G / (1.0f + expf(-G)) * U;
-        p.abuf[(size_t)(row + col) * p.I + r] = a_to_f16(a, p.status);
+        store_a(p, row + col, r, a);
       }
     }
   } else {
@@ -761,7 +791,8 @@ __device__ __forceinline__ void stream_task(const ExpertParams& p, int expert, i
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = 16 * (2 * idx + q) + gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
-        if (col < n) p.ybuf[(size_t)(row + col) * p.H + r] = ts * (acc[q][0][i] + acc[q][1][i]);
+        if (col < n)
+          p.ybuf[(size_t)(row + col) * p.H + r] = (ts * a_scale(p, row + col)) * (acc[q][0][i] + acc[q][1][i]);
       }
   }
 }
@@ -865,7 +896,7 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
-        if (col < pre.n) ys[(pre.row + col) * 16 + r] = pre.ts * acc[i];
+        if (col < pre.n) ys[(pre.row + col) * 16 + r] = (pre.ts * a_scale(p, pre.row + col)) * acc[i];
       }
       continue;
     }
@@ -952,7 +983,7 @@ __device__ __forceinline__ void down_combine_task(const ExpertParams& p, int til
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = gi + ((i & 2) ? 8 : 0), col = 2 * t + (i & 1);
-      if (col < n) ys[(row + col) * 16 + r] = ts * acc[0][i];
+      if (col < n) ys[(row + col) * 16 + r] = (ts * a_scale(p, row + col)) * acc[0][i];
     }
   }
   __syncthreads();

@@ -39,6 +39,13 @@ struct ExpertParams {
   float* logits_out;     // router logits [T x E] (tensor-core router only)
   int* status;
   long long wait_budget; // clock64 cycles one bounded wait of the tensor-core kernels may take
+  // W4A4 (activations quantised to NVFP4 per row), else all null: the f16
+  // copies of x (xh) and of a (abuf) then hold the activations' e2m1 code x
+  // e4m3 block scale (exact in f16) and these fp32 tensor scales multiply the
+  // accumulators; the gate/up kernels write a in fp32 to af for the quantiser
+  const float* ts_x;     // [T] per token
+  const float* ts_a;     // [T*k + T] per row of abuf
+  float* af;             // [(T*k + T) x I] fp32 a before quantisation
 };
 
 #ifdef __CUDACC__
@@ -95,6 +102,15 @@ cudaError_t launch_pack(int fmt, const uint8_t* codes, const uint8_t* scales, in
                         float* ts_dst, cudaStream_t st);
 cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stride, int rows,
                                  int K, const float* ts_ptr, float* out, cudaStream_t st);
+// Activations to NVFP4 per row (the weights' recipe with one tensor scale per
+// row): in [rows x K] bf16 (in_bf16) or fp32; optional outputs: canonical
+// codes [rows x K/2] and e4m3 scales [rows x K/16], the f16 values e2m1 code x
+// e4m3 scale [rows x K] (exact), and the tensor scales ts [rows].  A row whose
+// amax is not finite records MOE_ERANGE in *status (if status).  pdl: may
+// start while the previous kernel drains.
+cudaError_t launch_quantize_act(const void* in, bool in_bf16, int rows, int K, uint8_t* codes,
+                                uint8_t* scales, uint16_t* out_f16, float* ts, int* status,
+                                bool pdl, cudaStream_t st);
 
 // routing
 int router_ksplit(int T, int H, int E);

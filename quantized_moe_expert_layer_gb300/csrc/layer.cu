@@ -136,6 +136,7 @@ struct moe_layer {
   int router_mode = ROUTER_SOFTMAX;
   int* status = nullptr;
   long long wait_budget = 0;     // bounded-wait budget of the tensor-core kernels (0: default)
+  int act_fmt = MOE_ACT_BF16;    // MOE_ACT_NVFP4: W4A4, activations quantised per row
   // workspace
   int T_max = 0;
   void* ws = nullptr;
@@ -158,6 +159,8 @@ struct moe_layer {
   float* ybuf = nullptr;
   uint16_t* x_stage = nullptr;
   float* out_stage = nullptr;
+  float* ts_x = nullptr;         // W4A4: per-token activation tensor scales
+  float* ts_a = nullptr;         // W4A4: per-row tensor scales of a
   std::vector<size_t> guards;    // byte offsets of the workspace's guard regions
   size_t ws_bytes = 0;
   int last_T = 0;
@@ -210,7 +213,7 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.row_token = L->row_token;
   p.entries = L->entries;
   p.n_entries = L->n_entries;
-  p.xh = L->xh;
+  p.xh = L->act_fmt == MOE_ACT_NVFP4 ? nullptr : L->xh;  // W4A4: the quantiser writes it
   p.tc_entries = tc ? L->tc_entries : nullptr;
   p.n_tc_entries = tc ? L->n_tc_entries : nullptr;
   p.blk = L->blk;
@@ -249,6 +252,11 @@ ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
   p.rbias = L->has_bias ? L->bias : nullptr;
   p.status = L->status;
   p.wait_budget = L->wait_budget > 0 ? L->wait_budget : 2000000000LL;
+  if (L->act_fmt == MOE_ACT_NVFP4) {
+    p.ts_x = L->ts_x;
+    p.ts_a = L->ts_a;
+    p.af = L->ybuf;  // a in fp32 until quantised; the down kernels write y after that
+  }
   return p;
 }
 
@@ -283,10 +291,30 @@ bool tc_path(moe_layer* L, int T) {
 // dispatch as usual (the GEMM's output is the one K slice the top-k reads)
 bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E, L->H); }
 
+bool w4a4(const moe_layer* L) { return L->act_fmt == MOE_ACT_NVFP4; }
+
+// W4A4: x quantised per token into the f16 copy the expert kernels read
+// (e2m1 code x e4m3 block scale) and the per-token tensor scales
+int launch_quant_x(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
+  CK("activation quantiser launch (x)", launch_quantize_act(x, true, T, L->H, nullptr, nullptr, L->xh,
+                                                             L->ts_x, L->status, true, st));
+  return MOE_OK;
+}
+
+// W4A4: the rows of a (fp32, written by gate/up) quantised into abuf and ts_a
+int launch_quant_a(moe_layer* L, int T, cudaStream_t st) {
+  const int rows = T * L->k + (L->shared ? T : 0);
+  CK("activation quantiser launch (a)", launch_quantize_act(L->ybuf, false, rows, L->I, nullptr,
+                                                             nullptr, L->abuf, L->ts_a, L->status,
+                                                             true, st));
+  return MOE_OK;
+}
+
 int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
   ep.logits_out = L->partial;
-  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
+  if (!w4a4(L))  // (W4A4: the quantiser wrote the f16 copy before the router)
+    CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
   CK("tensor-core router kernel launch", launch_tc_router(ep, st));
   return MOE_OK;
 }
@@ -296,12 +324,14 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   if (tc_path(L, T)) {
     const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
     CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, L->map_gu, st));
+    if (w4a4(L) && launch_quant_a(L, T, st)) return MOE_ECUDA;
     CK("tensor-core down kernel launch", launch_tc_down(ep, gy, L->map_dn, st));
     CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
     return MOE_OK;
   }
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
   CK("gate/up kernel launch", launch_gateup(ep, grid_y, true, st));
+  if (w4a4(L) && launch_quant_a(L, T, st)) return MOE_ECUDA;
   if (fused_down(L, T)) {
     CK("down+combine kernel launch", launch_down_combine(ep, L->gates, L->inv, out, true, false, st));
     return MOE_OK;
@@ -317,23 +347,30 @@ bool small_path(moe_layer* L, int T) { return small_route_ok(T, L->k) && fused_d
 
 // kernels one forward of T tokens launches
 int forward_launches(moe_layer* L, int T) {
-  if (small_path(L, T)) return 3;
+  // W4A4: the quantiser of a, and of x (in place of the x conversion before the tensor-core router)
+  const int q = w4a4(L) ? 1 + (tc_router(L, T) ? 0 : 1) : 0;
+  if (small_path(L, T)) return 3 + q;
   // (convert x, tc router | router), top-k, dispatch (1 or 2 kernels); T <= 16: router, top-k + dispatch
   const int dispatch = dispatch_launches(T * L->k);
   const int routing = tc_router(L, T) ? 3 + dispatch : (T <= kFusedTopkMaxT ? 2 : 2 + dispatch);
-  if (tc_path(L, T)) return routing + 3;
-  return routing + (fused_down(L, T) ? 2 : 3);
+  if (tc_path(L, T)) return routing + 3 + q;
+  return routing + (fused_down(L, T) ? 2 : 3) + q;
 }
 
 int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   RouteParams rp = route_params(L, x, T);
   L->last_T = T;
   L->last_has_logits = true;
+  if (w4a4(L)) {
+    const int rc = launch_quant_x(L, x, T, st);
+    if (rc) return rc;
+  }
   if (small_path(L, T)) {
     ExpertParams ep = expert_params(L, x, T);
     CK("router kernel launch", launch_router(rp, st));
     CK("gate/up kernel launch",
        launch_gateup_routed(ep, rp, ep.nsh + max_routed_entries(T, L->E, L->k), st));
+    if (w4a4(L) && launch_quant_a(L, T, st)) return MOE_ECUDA;
     CK("down+combine kernel launch", launch_down_combine(ep, L->gates, L->inv, out, true, true, st));
     return MOE_OK;
   }
@@ -441,10 +478,12 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       (size_t)max_tc_entries(T_max, L->E, L->k) * 16, 16,  // tc_entries, n_tc_entries
       (size_t)T_max * L->H * 2,          // xh
       (S + T_max) * L->I * 2,            // abuf
-      (S + T_max) * L->H * 4,            // ybuf
+      (S + T_max) * (size_t)(L->H > L->I ? L->H : L->I) * 4,  // ybuf (W4A4: fp32 a first)
       (size_t)T_max * L->H * 2,          // x_stage
       (size_t)T_max * L->H * 4,          // out_stage
       ((S + kDispChunk - 1) / kDispChunk) * E * 4,  // blk
+      (size_t)T_max * 4,                 // ts_x
+      (S + T_max) * 4,                   // ts_a
   };
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   // [guard][buffer 0][guard][buffer 1] ... [guard]: moe_debug_check_workspace
@@ -491,6 +530,8 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->x_stage = (uint16_t*)ptrs[16];
   L->out_stage = (float*)ptrs[17];
   L->blk = (int*)ptrs[18];
+  L->ts_x = (float*)ptrs[19];
+  L->ts_a = (float*)ptrs[20];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   for (size_t off : L->guards)
@@ -786,12 +827,37 @@ int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* id
   CK("moe_forward_routed: copy idx", cudaMemcpyAsync(L->idx, idx, S * 4, cudaMemcpyDeviceToDevice, st));
   CK("moe_forward_routed: copy gates",
      cudaMemcpyAsync(L->gates, gates, S * 4, cudaMemcpyDeviceToDevice, st));
-  CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
+  if (w4a4(L)) {
+    rc = launch_quant_x(L, x, T, st);
+    if (rc) return rc;
+  } else {
+    CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
+  }
   RouteParams rp = route_params(L, x, T);
   CK("dispatch kernel launch", launch_dispatch(rp, false, st));
   L->last_T = T;
   L->last_has_logits = false;
   return run_experts(L, x, T, out, st);
+}
+
+int moe_set_act_format(moe_layer* L, int fmt) {
+  if (!L) return fail(MOE_EINVAL, "moe_set_act_format: null layer");
+  if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_NVFP4)
+    return fail(MOE_EINVAL, "moe_set_act_format: unknown activation format %d", fmt);
+  L->act_fmt = fmt;
+  return MOE_OK;
+}
+
+int moe_quantize_act_nvfp4(const void* in, int in_bf16, int rows, int K, uint8_t* codes,
+                           uint8_t* scales, float* tscale, void* stream) {
+  if (!in || !codes || !scales || !tscale)
+    return fail(MOE_EINVAL, "moe_quantize_act_nvfp4: null argument");
+  if (rows < 1 || K < 16 || K % 16) return fail(MOE_EINVAL, "moe_quantize_act_nvfp4: bad shape %dx%d", rows, K);
+  if (((uintptr_t)in | (uintptr_t)codes) & 15u)
+    return fail(MOE_EINVAL, "moe_quantize_act_nvfp4: in and codes must be 16-byte aligned");
+  CK("moe_quantize_act_nvfp4", launch_quantize_act(in, in_bf16 != 0, rows, K, codes, scales, nullptr,
+                                                   tscale, nullptr, false, (cudaStream_t)stream));
+  return MOE_OK;
 }
 
 int moe_set_wait_budget(moe_layer* L, int64_t cycles) {
@@ -869,6 +935,9 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
   RouteParams rp = route_params(L, x, T);
   ExpertParams ep = expert_params(L, x, T);
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
+  // W4A4: the x quantiser runs with the routing phase, the a quantiser with the down phase
+  if (w4a4(L) && phase == 0 && (rc = launch_quant_x(L, x, T, st))) return rc;
+  if (w4a4(L) && phase == 3 && (rc = launch_quant_a(L, T, st))) return rc;
   if (small_path(L, T)) {  // router; gate/up (routing inside); down + combine (routing inside)
     if (phase < 0 || phase > 4) return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
     if (phase == 0) CK("router", launch_router(rp, st));

@@ -88,6 +88,102 @@ __global__ void quant_nvfp4_kernel(const float* __restrict__ W, int rows, int K,
   }
 }
 
+// Activation rows to NVFP4 with one tensor scale per row: one CTA per row.
+// The same arithmetic as quant_nvfp4_kernel (IEEE fp32 divisions, e4m3 and
+// e2m1 round to nearest even), so a row gives the bytes the weight quantiser
+// gives for a one-row matrix.
+template <bool IN_BF16>
+__global__ void __launch_bounds__(256) quant_act_kernel(const void* __restrict__ in, int K,
+                                                        uint8_t* __restrict__ codes,
+                                                        uint8_t* __restrict__ scales,
+                                                        uint16_t* __restrict__ out_f16,
+                                                        float* __restrict__ ts_out, int* status) {
+  griddep_wait();
+  griddep_launch();
+  const int row = blockIdx.x, tid = threadIdx.x;
+  __shared__ float red[8];
+  auto load16 = [&](int b, float (&w)[16]) {
+    if constexpr (IN_BF16) {
+      const uint4* q = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(in) +
+                                                      (size_t)row * K + 16 * b);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 v = q[h];
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w[8 * h + 2 * i] = __uint_as_float(u[i] << 16);
+          w[8 * h + 2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+        }
+      }
+    } else {
+      const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(in) +
+                                                        (size_t)row * K + 16 * b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = q[i];
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+    }
+  };
+  const int nb = K / 16;
+  float m = 0.0f;
+  for (int b = tid; b < nb; b += blockDim.x) {
+    float w[16];
+    load16(b, w);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
+  }
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  float A = 0.0f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) A = fmaxf(A, red[i]);
+  if (!(A <= 3.0e38f)) {  // inf or NaN in the row
+    if (tid == 0 && status) *status = kStatusRange;
+    A = 0.0f;
+  }
+  const float ts = (A > 0.0f) ? __fdiv_rn(A, 2688.0f) : 0.0f;
+  if (tid == 0) ts_out[row] = ts;
+  for (int b = tid; b < nb; b += blockDim.x) {
+    float w[16];
+    load16(b, w);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(w[i]));
+    uint32_t s = 0;
+    if (ts > 0.0f) s = f32_to_e4m3_satfinite(__fdiv_rn(__fdiv_rn(amax, 6.0f), ts));
+    uint32_t packed[2] = {0u, 0u};
+    if (s != 0) {
+      const float denom = __fmul_rn(e4m3_to_f32(s), ts);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float v = __fdiv_rn(w[i], denom);
+        uint32_t q = e2m1_code_rne(fabsf(v));
+        if (v < 0.0f && q != 0u) q |= 8u;
+        packed[i / 8] |= q << (4 * (i % 8));
+      }
+    }
+    const size_t blk = (size_t)row * nb + b;
+    if (codes) reinterpret_cast<uint2*>(codes)[blk] = make_uint2(packed[0], packed[1]);
+    if (scales) scales[blk] = (uint8_t)s;
+    if (out_f16) {  // e2m1 code x e4m3 scale: both exact in f16, so is the product
+      const uint32_t sp = dup_lo(e4m3x2_to_f16x2(s));
+      uint32_t h[8];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t f[4];
+        e2m1x8_to_f16x8(packed[q], f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[4 * q + i] = hmul2(f[i], sp);
+      }
+      uint4* o = reinterpret_cast<uint4*>(out_f16 + (size_t)row * K + 16 * b);
+      o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+      o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
 __global__ void amax_to_tscale_kernel(float* tscale) {
   const float A = tscale[0];  // holds amax bits (a non-negative float)
   tscale[0] = (A > 0.0f) ? __fdiv_rn(A, 2688.0f) : 0.0f;
@@ -418,6 +514,17 @@ cudaError_t launch_quantize_nvfp4(const float* W, int rows, int K, uint8_t* code
       W, rows, K, codes, scales, amax_bits);
   amax_to_tscale_kernel<<<1, 1, 0, st>>>(tscale);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_act(const void* in, bool in_bf16, int rows, int K, uint8_t* codes,
+                                uint8_t* scales, uint16_t* out_f16, float* ts, int* status,
+                                bool pdl, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (in_bf16)
+    return launch_k(quant_act_kernel<true>, dim3(rows), dim3(256), 0, st, pdl, in, K, codes, scales,
+                    out_f16, ts, status);
+  return launch_k(quant_act_kernel<false>, dim3(rows), dim3(256), 0, st, pdl, in, K, codes, scales,
+                  out_f16, ts, status);
 }
 
 cudaError_t launch_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,

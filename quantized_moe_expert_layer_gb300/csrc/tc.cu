@@ -567,9 +567,13 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
             const int col = c0 + qq;
             if (lane < 16 && col < n) {
-              const float Gv = ts_g * mine, U = ts_u * other;
+              const float sx = p.ts_x ? p.ts_x[sh->tok[col]] : 1.0f;  // W4A4: the token's scale
+              const float Gv = (ts_g * sx) * mine, U = (ts_u * sx) * other;
               const float a = Gv / (1.0f + expf(-Gv)) * U;
-              p.abuf[(size_t)(row0 + col) * p.I + i] = a_to_f16(a, p.status);
+              if (p.af)
+                p.af[(size_t)(row0 + col) * p.I + i] = a;
+              else
+                p.abuf[(size_t)(row0 + col) * p.I + i] = a_to_f16(a, p.status);
             }
           }
         }
@@ -582,7 +586,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 #pragma unroll
           for (int qq = 0; qq < 32; ++qq) {
             const int col = c0 + qq;
-            if (col < n) p.ybuf[(size_t)(row0 + col) * p.H + h] = ts * __uint_as_float(v[qq]);
+            if (col < n) {
+              const float sa = p.ts_a ? p.ts_a[row0 + col] : 1.0f;  // W4A4: the row's scale
+              p.ybuf[(size_t)(row0 + col) * p.H + h] = (ts * sa) * __uint_as_float(v[qq]);
+            }
           }
         }
       }

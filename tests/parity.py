@@ -119,9 +119,9 @@ def run_gpu(L, x_np, w, want_routing=True):
     return res
 
 
-def compare_layer(w, L, x_np, sample=None, orc_layer=None, route_all=False):
+def compare_layer(w, L, x_np, sample=None, orc_layer=None, route_all=False, act_fp4=False):
     """Full forward on the GPU; the oracle's layer output on the sampled tokens
-    (default: all).  The routing (logits, top-k, gates) is compared on the
+    (default: all; act_fp4: the W4A4 oracle).  The routing (logits, top-k, gates) is compared on the
     sampled tokens, or on every token with route_all (the router and top-k
     are cheap next to the expert FFNs).  Returns (max rel-L2, near-tie token
     count over the routed rows)."""
@@ -161,6 +161,7 @@ def compare_layer(w, L, x_np, sample=None, orc_layer=None, route_all=False):
         gates_use[i] = gates_for(lg_o[i], idx_use[i])
     need = set(idx_use.ravel().tolist()) | ({w.E} if w.shared else set())
     ol = orc_layer if orc_layer is not None else oracle.layer_for_workload(w, sorted(need))
+    ol.act_fp4 = act_fp4  # W4A4: the oracle quantises the activations of every product too
     ref = ol.combine(xs, idx_use, gates_use)
     got = g["out"][rows]
     rel = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)

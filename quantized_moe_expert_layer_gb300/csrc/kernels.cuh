@@ -81,6 +81,7 @@ struct RouteParams {
   int4* tc_entries;       // optional: entries of up to kTcMaxN tokens (tensor-core path)
   int* n_tc_entries;
   int* blk;               // [ceil(T*k / kDispChunk) x E] per-chunk expert counts, then bases
+  int* ticket;            // CTAs of the fused top-k + dispatch done so far (0 between forwards)
   int* status;
 };
 
@@ -123,6 +124,9 @@ cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cu
 cudaError_t launch_dispatch(const RouteParams& p, bool pdl, cudaStream_t st);
 int dispatch_launches(int S);
 cudaError_t launch_topk(const RouteParams& p, bool pdl, cudaStream_t st);
+// Top-k and dispatch in one launch (topk_dispatch_kernel) when topk_dispatch_ok.
+bool topk_dispatch_ok(int T, int k, int E);
+cudaError_t launch_topk_dispatch(const RouteParams& p, bool pdl, cudaStream_t st);
 size_t route_finish_smem(int E);
 cudaError_t route_kernels_init();
 

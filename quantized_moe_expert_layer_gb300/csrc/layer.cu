@@ -161,6 +161,7 @@ struct moe_layer {
   float* out_stage = nullptr;
   float* ts_x = nullptr;         // W4A4: per-token activation tensor scales
   float* ts_a = nullptr;         // W4A4: per-row tensor scales of a
+  int* ticket = nullptr;         // the fused top-k + dispatch's CTA count (0 between forwards)
   std::vector<size_t> guards;    // byte offsets of the workspace's guard regions
   size_t ws_bytes = 0;
   int last_T = 0;
@@ -217,6 +218,7 @@ RouteParams route_params(moe_layer* L, const uint16_t* x, int T) {
   p.tc_entries = tc ? L->tc_entries : nullptr;
   p.n_tc_entries = tc ? L->n_tc_entries : nullptr;
   p.blk = L->blk;
+  p.ticket = L->ticket;
   p.status = L->status;
   return p;
 }
@@ -293,6 +295,17 @@ bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E,
 
 bool w4a4(const moe_layer* L) { return L->act_fmt == MOE_ACT_NVFP4; }
 
+// top-k then dispatch: one fused launch where it applies, else two (or three)
+int launch_topk_and_dispatch(moe_layer* L, const RouteParams& rp, int T, bool pdl, cudaStream_t st) {
+  if (topk_dispatch_ok(T, L->k, L->E)) {
+    CK("top-k + dispatch kernel launch", launch_topk_dispatch(rp, pdl, st));
+    return MOE_OK;
+  }
+  CK("top-k kernel launch", launch_topk(rp, pdl, st));
+  CK("dispatch kernel launch", launch_dispatch(rp, pdl, st));
+  return MOE_OK;
+}
+
 // W4A4: x quantised per token into the f16 copy the expert kernels read
 // (e2m1 code x e4m3 block scale) and the per-token tensor scales
 int launch_quant_x(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
@@ -352,7 +365,9 @@ int forward_launches(moe_layer* L, int T) {
   if (small_path(L, T)) return 3 + q;
   // (convert x, tc router | router), top-k, dispatch (1 or 2 kernels); T <= 16: router, top-k + dispatch
   const int dispatch = dispatch_launches(T * L->k);
-  const int routing = tc_router(L, T) ? 3 + dispatch : (T <= kFusedTopkMaxT ? 2 : 2 + dispatch);
+  // top-k + dispatch: one kernel (T <= 16, or the fused one), else top-k then dispatch
+  const int topk_disp = topk_dispatch_ok(T, L->k, L->E) ? 1 : 1 + dispatch;
+  const int routing = tc_router(L, T) ? 2 + topk_disp : (T <= kFusedTopkMaxT ? 2 : 1 + topk_disp);
   if (tc_path(L, T)) return routing + 3 + q;
   return routing + (fused_down(L, T) ? 2 : 3) + q;
 }
@@ -377,15 +392,15 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
   if (tc_router(L, T)) {
     const int rc = launch_tc_routing_gemm(L, x, T, st);
     if (rc) return rc;
-    CK("top-k kernel launch", launch_topk(rp, true, st));
-    CK("dispatch kernel launch", launch_dispatch(rp, true, st));
+    const int rc2 = launch_topk_and_dispatch(L, rp, T, true, st);
+    if (rc2) return rc2;
   } else if (T <= kFusedTopkMaxT) {
     CK("router kernel launch", launch_router(rp, st));
     CK("top-k/dispatch kernel launch", launch_route_finish(rp, true, true, st));
   } else {
     CK("router kernel launch", launch_router(rp, st));
-    CK("top-k kernel launch", launch_topk(rp, true, st));
-    CK("dispatch kernel launch", launch_dispatch(rp, true, st));
+    const int rc2 = launch_topk_and_dispatch(L, rp, T, true, st);
+    if (rc2) return rc2;
   }
   L->last_T = T;
   L->last_has_logits = true;
@@ -484,6 +499,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       ((S + kDispChunk - 1) / kDispChunk) * E * 4,  // blk
       (size_t)T_max * 4,                 // ts_x
       (S + T_max) * 4,                   // ts_a
+      4,                                 // ticket
   };
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   // [guard][buffer 0][guard][buffer 1] ... [guard]: moe_debug_check_workspace
@@ -532,6 +548,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->blk = (int*)ptrs[18];
   L->ts_x = (float*)ptrs[19];
   L->ts_a = (float*)ptrs[20];
+  L->ticket = (int*)ptrs[21];
   L->T_max = T_max;
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   for (size_t off : L->guards)
@@ -959,9 +976,8 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
     case 1:
       if (T <= kFusedTopkMaxT && !tc_router(L, T)) {
         CK("top-k/dispatch", launch_route_finish(rp, true, false, st));
-      } else {
-        CK("top-k", launch_topk(rp, false, st));
-        CK("dispatch", launch_dispatch(rp, false, st));
+      } else if ((rc = launch_topk_and_dispatch(L, rp, T, false, st))) {
+        return rc;
       }
       break;
     case 2:

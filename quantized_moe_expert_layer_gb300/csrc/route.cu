@@ -64,6 +64,34 @@ __global__ void __launch_bounds__(256) topk_warp_kernel(RouteParams p) {
   if (t < p.T) topk_token(p, t, threadIdx.x & 31, nullptr);
 }
 
+// Top-k of one token per CTA (the two levels of topk_kernel over blockDim / 32
+// warps), then the dispatch by the CTA that finishes last: every CTA makes its
+// picks visible and takes a ticket; the one that draws the last ticket runs
+// dispatch_block over all the picks and clears the ticket for the next
+// forward.  No CTA waits for another.  One launch instead of two for
+// 16 < T with T*k <= kDispOneCtaMax and E <= 512 (dispatch_block needs a
+// thread per expert).
+template <int V2>
+__global__ void __launch_bounds__(512) topk_dispatch_kernel(RouteParams p) {
+  griddep_launch();
+  griddep_wait();
+  extern __shared__ int smem_td[];  // keys, ids [warps x kMaxK each], scan scratch [64], histograms
+  const int NW = blockDim.x >> 5;
+  uint32_t* ck = reinterpret_cast<uint32_t*>(smem_td);
+  int* ci = smem_td + NW * kMaxK;
+  int* sc = ci + NW * kMaxK;
+  __shared__ int last;
+  topk_token_cta<1, V2>(p, blockIdx.x, nullptr, ck, ci);  // (ends synchronised)
+  __threadfence();  // this CTA's picks, before its ticket
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(p.ticket, 1) == p.T - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();  // every other CTA's picks, after the last ticket
+  dispatch_block(p, sc + 64, sc);
+  if (threadIdx.x == 0) *p.ticket = 0;
+}
+
 __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(RouteParams p, int do_topk) {
   griddep_launch();
   griddep_wait();
@@ -236,6 +264,24 @@ cudaError_t launch_route_finish(const RouteParams& p, bool do_topk, bool pdl, cu
 
 int dispatch_launches(int S) { return S > kDispOneCtaMax ? 2 : 1; }
 
+// a thread per expert (at least 8 warps), at most 512
+static int topk_dispatch_threads(int E) { return E <= 256 ? 256 : 512; }
+
+bool topk_dispatch_ok(int T, int k, int E) {
+  return T > 16 && T < kTopkWarpMinT && (long)T * k <= kDispOneCtaMax && E <= 512;
+}
+
+cudaError_t launch_topk_dispatch(const RouteParams& p, bool pdl, cudaStream_t st) {
+  const int threads = topk_dispatch_threads(p.E), NW = threads / 32;
+  const size_t smem = ((size_t)2 * NW * kMaxK + 64 + (size_t)NW * p.E) * sizeof(int);
+  // warp 0 merges NW * k candidates, V2 per lane
+  if (NW * p.k <= 96)
+    return launch_k(topk_dispatch_kernel<3>, dim3(p.T), dim3(threads), smem, st, pdl, p);
+  if (NW * p.k <= 256)
+    return launch_k(topk_dispatch_kernel<8>, dim3(p.T), dim3(threads), smem, st, pdl, p);
+  return launch_k(topk_dispatch_kernel<16>, dim3(p.T), dim3(threads), smem, st, pdl, p);
+}
+
 cudaError_t launch_dispatch(const RouteParams& p, bool pdl, cudaStream_t st) {
   const int S = p.T * p.k;
   if (S <= kDispOneCtaMax) return launch_route_finish(p, false, pdl, st);
@@ -255,6 +301,12 @@ cudaError_t route_kernels_init() {
   e = cudaFuncSetAttribute(dispatch_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            ((kDispChunk / 32) * kMaxE + 64) * (int)sizeof(int));
   if (e != cudaSuccess) return e;
+  for (auto f : {(const void*)topk_dispatch_kernel<3>, (const void*)topk_dispatch_kernel<8>,
+                 (const void*)topk_dispatch_kernel<16>}) {
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((2 * 16 * kMaxK + 64 + 16 * 512) * sizeof(int)));
+    if (e != cudaSuccess) return e;
+  }
   return cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)route_finish_smem(kMaxE));
 }

@@ -52,8 +52,8 @@ def test_tiny_workload():
 @pytest.mark.parametrize("T", [1, 5, 13, 64, 70, 200])
 def test_small_layers_ragged_token_counts(fmt, T):
     """Several tiles, ragged last entries, the routing paths (T = 1 in-CTA,
-    T <= 16 top-k inside the dispatch kernel, larger T a separate top-k
-    kernel), all formats, with a shared expert."""
+    T <= 16 top-k inside the dispatch kernel, larger T the top-k kernel whose
+    last CTA dispatches), all formats, with a shared expert."""
     w = small(fmt=fmt, H=384 if fmt == 2 else 320, I=256 if fmt == 2 else 192, E=24, k=3, T=T)
     compare_layer(w, layer(w), gen.x_tokens(w, T))
 
@@ -65,7 +65,7 @@ def test_tensor_core_path_small_layer(T):
     work items of up to 256 tokens."""
     w = small(fmt=1, H=256, I=128, E=8, k=2, T=T, seed=5)
     L = layer(w)
-    assert L.launches(T) == 6  # router, top-k, dispatch, tc gate/up, tc down, combine
+    assert L.launches(T) == 5  # router, top-k + dispatch (one kernel), tc gate/up, tc down, combine
     compare_layer(w, L, gen.x_tokens(w, T))
 
 

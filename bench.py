@@ -46,6 +46,7 @@ PER_CONFIG = [1, 2, 3]  # decode NVFP4, decode FP6, batched T=64: timed in the s
                         # (and the prefill with W4A4 activations)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor rate (13.5 / 2.25 PFLOP/s)
 
 
 def parse():
@@ -495,7 +496,7 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
     tc = tc_path(w, T)
     gu = packed_gateup_bytes(w)
     dn = packed_down_bytes(w)
-    per_launch, padded, host_per_launch = [], [], []
+    per_launch, padded, host_per_launch, fq_bytes = [], [], [], []
     # for T <= 8 (NVFP4) gate/up also asks L2 for the touched experts' down
     # matrices, which the down kernel then reads from L2
     prefetch_down = T <= 8 and w.fmt in (1, 3)
@@ -516,6 +517,9 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
                 cols = sum(((min(128, v - 128 * j) + 15) // 16) * 16
                            for v in n for j in range((v + 127) // 128))
                 padded.append(2.0 * cols * 2 * w.I * w.H)
+                # bytes of the block-scaled (W4A4) launch: the touched experts' packed gate/up
+                # tiles, x's NVFP4 codes and scales, a written in fp32
+                fq_bytes.append(D * gu + T * w.H * 9 // 16 + sum(n) * w.I * 4)
             else:  # unique weight bytes, x, and a (+ the down matrices it pulls into L2)
                 per_launch.append(D * (gu + 8 + (dn if prefetch_down else 0)) + T * w.H * 2
                                   + (T * w.k + T * w.shared) * w.I * 2)
@@ -525,7 +529,26 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
             L.run_phase(2, x, o, stream=s)
     k_us = graph_time_us(s, run_gateup, max(20, min(200, steps))) / Ln
     work = sum(per_launch) / len(per_launch)
-    if tc:
+    if tc and act:
+        # the block-scaled FP4 GEMM: HBM-bound at these token counts (its FLOPs
+        # at the FP4 rate take a fraction of the time its weight bytes take)
+        kname = "tc_fp4_kernel"
+        peak, peak_kind = peaks("hbm")
+        tpeak, tpeak_kind = peaks("tensor")
+        fp4_peak = tpeak * FP4_OVER_BF16
+        fb = sum(fq_bytes) / len(fq_bytes)
+        achieved = fb / (k_us * 1e-6) / 1e9
+        t_flops = work / (k_us * 1e-6) / 1e12
+        roofline = {"bound": "hbm", "kernel": kname + "<0> (gate/up + SwiGLU, kind::mxf4nvf4)",
+                    "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "algorithmic_bytes_per_launch": fb,
+                    "tensor": {"achieved": t_flops, "peak": fp4_peak, "unit": "TFLOP/s",
+                               "frac": t_flops / fp4_peak, "algorithmic_flops_per_launch": work,
+                               "peak_source": tpeak_kind + " x 6 (nominal dense FP4 / bf16: "
+                                                           "13.5 / 2.25 PFLOP/s)"},
+                    "note": "bytes: the touched experts' packed gate/up tiles, x's NVFP4 codes "
+                            "and scales, a written in fp32 for its quantiser"}
+    elif tc:
         kname = "tc_expert_kernel"
         peak, peak_kind = peaks("tensor")
         achieved = work / (k_us * 1e-6) / 1e12

@@ -100,6 +100,16 @@ int moe_layer_status(moe_layer* L, int reset, int* status);
 /* Number of kernels one moe_forward of T tokens launches (>= 0), or an error. */
 int moe_forward_launches(moe_layer* L, int T);
 
+/* The expert path one moe_forward of T tokens takes with the layer's current
+ * format, placement and activation format (>= 0), or an error. */
+enum moe_path {
+  MOE_PATH_DECODE = 0,    /* T <= 8: gate/up routes itself; fused down + combine */
+  MOE_PATH_STREAM = 1,    /* streamed GEMVs over expert-sorted token groups */
+  MOE_PATH_TC_F16 = 2,    /* tcgen05 kind::f16 GEMMs on exactly dequantised weights */
+  MOE_PATH_TC_FP4 = 3     /* W4A4: tcgen05 kind::mxf4nvf4 block-scaled GEMMs */
+};
+int moe_forward_path(moe_layer* L, int T);
+
 /* Budget of each bounded wait in the tensor-core kernels, in SM clock cycles
  * (clock64); cycles <= 0 restores the default of 2e9 (about one second).  A
  * wait that runs out stops its CTA's work: the CTA lets its copies and MMAs in

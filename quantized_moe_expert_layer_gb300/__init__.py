@@ -29,6 +29,7 @@ FMT_MXFP4 = 3
 GATE, UP, DOWN = 0, 1, 2
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 ACT_BF16, ACT_NVFP4 = 0, 1
+PATH_DECODE, PATH_STREAM, PATH_TC_F16, PATH_TC_FP4 = 0, 1, 2, 3
 HOST, DEVICE = 0, 1
 
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT, ERANGE = 0, -1, -2, -3, -4, -5, -6
@@ -39,7 +40,8 @@ EXPORTS = [
     "moe_layer_status", "moe_layer_info", "moe_set_router", "moe_pack_matrix",
     "moe_pack_weights", "moe_set_router_mode", "moe_quantize_nvfp4", "moe_quantize_fp6", "moe_quantize_mxfp4", "moe_forward",
     "moe_forward_host", "moe_forward_routed", "moe_debug_dequant", "moe_debug_routing",
-    "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches", "moe_place_experts",
+    "moe_debug_run_phase", "moe_route_noalloc", "moe_forward_launches", "moe_forward_path",
+    "moe_place_experts",
     "moe_layer_placement", "moe_set_wait_budget", "moe_debug_fail_alloc",
     "moe_debug_check_workspace", "moe_set_act_format", "moe_quantize_act_nvfp4"
 ]
@@ -120,6 +122,7 @@ def lib():
                 "moe_debug_run_phase": (I, [P, I, P, I, P, P]),
                 "moe_route_noalloc": (I, [P, I, I, P, P, I, I, P, P, P, P]),
                 "moe_forward_launches": (I, [P, I]),
+                "moe_forward_path": (I, [P, I]),
                 "moe_place_experts": (I, [P, P]),
                 "moe_layer_placement": (I, [P, P, ctypes.POINTER(U64), ctypes.POINTER(U64)]),
                 "moe_set_wait_budget": (I, [P, ctypes.c_int64]),
@@ -186,6 +189,11 @@ class MoeLayer:
     def launches(self, T):
         """Kernels one forward of T tokens launches."""
         return check(lib().moe_forward_launches(self.h, T))
+
+    def path(self, T):
+        """The expert path a forward of T tokens takes: PATH_DECODE, PATH_STREAM,
+        PATH_TC_F16 or PATH_TC_FP4."""
+        return check(lib().moe_forward_path(self.h, T))
 
     def info(self):
         a, e = ctypes.c_uint64(), ctypes.c_uint64()

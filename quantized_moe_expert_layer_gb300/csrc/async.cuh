@@ -1,6 +1,6 @@
 // Asynchronous-copy and mbarrier helpers (sm_103a): shared-memory mbarriers
 // with bounded waits (the tensor-core kernels' TMA and MMA hand-offs) and
-// cp.async (16 bytes, per thread).
+// cp.async (16 or 4 bytes, per thread).
 #pragma once
 
 #include <stdint.h>
@@ -100,6 +100,10 @@ __device__ __forceinline__ void fence_async_smem() {
 // ---------------------------------------------------------------- cp.async (per thread)
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+// 4 bytes (both addresses 4-byte aligned)
+__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr), "l"(g) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>

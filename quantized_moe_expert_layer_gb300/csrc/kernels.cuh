@@ -46,6 +46,16 @@ struct ExpertParams {
   const float* ts_x;     // [T] per token
   const float* ts_a;     // [T*k + T] per row of abuf
   float* af;             // [(T*k + T) x I] fp32 a before quantisation
+  // W4A4 on the block-scaled tensor-core path: the activations' NVFP4 codes
+  // [rows x K/2] (low nibble = lower column) and e4m3 block scales [rows x K/16]
+  const uint8_t* xq;     // x: [T x H/2]
+  const uint8_t* xqs;    // [T x H/16]
+  const uint8_t* aq;     // a: [(T*k + T) x I/2]
+  const uint8_t* aqs;    // [(T*k + T) x I/16]
+  // the weights in the MMA layout (layout.cuh): per expert mma_expert_bytes,
+  // the gate/up and down block scales at mma_gu_sc and mma_dn_sc
+  const uint8_t* mma;
+  uint64_t mma_expert_bytes, mma_gu_sc, mma_dn_sc;
 };
 
 #ifdef __CUDACC__
@@ -103,6 +113,14 @@ cudaError_t launch_pack(int fmt, const uint8_t* codes, const uint8_t* scales, in
                         float* ts_dst, cudaStream_t st);
 cudaError_t launch_debug_dequant(int fmt, const uint8_t* src, uint64_t tile_stride, int rows,
                                  int K, const float* ts_ptr, float* out, cudaStream_t st);
+// The packed NVFP4 tiles of one matrix region (src_off into each expert,
+// rows M, K columns) of n_experts experts into the MMA layout (layout.cuh) at
+// dst (dst_expert_bytes per expert; the region's codes and scales at
+// codes_off and scales_off).
+cudaError_t launch_to_mma_layout(const uint8_t* arena, uint64_t expert_bytes, uint64_t src_off,
+                                 int tile_bytes, int M, int K, int n_experts, uint8_t* dst,
+                                 uint64_t dst_expert_bytes, uint64_t codes_off, uint64_t scales_off,
+                                 cudaStream_t st);
 // Activations to NVFP4 per row (the weights' recipe with one tensor scale per
 // row): in [rows x K] bf16 (in_bf16) or fp32; optional outputs: canonical
 // codes [rows x K/2] and e4m3 scales [rows x K/16], the f16 values e2m1 code x
@@ -159,6 +177,17 @@ cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, const void* tile
                              cudaStream_t st);
 cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, const void* tile_map,
                            cudaStream_t st);
+// W4A4: the same GEMMs on the block-scaled FP4 MMA (kind::mxf4nvf4), both
+// operands NVFP4, the weights read from their MMA layout; tile_map: the
+// CUtensorMap of the region's codes made by tc_make_mma_map with
+// box_rows = 128 * tc_fp4_group(M-blocks of the matrix).  grid: a CTA per SM.
+int tc_fp4_group(int mblocks);
+cudaError_t tc_make_mma_map(void* map, const uint8_t* codes, int n_experts, int rows, int stages,
+                            uint64_t expert_stride, int box_rows);
+cudaError_t launch_tc_fp4_gateup(const ExpertParams& p, int grid_y, const void* tile_map,
+                                 cudaStream_t st);
+cudaError_t launch_tc_fp4_down(const ExpertParams& p, int grid_y, const void* tile_map,
+                               cudaStream_t st);
 bool tc_router_ok(int E, int H);
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);
 cudaError_t tc_kernels_init();

@@ -117,6 +117,15 @@ struct moe_layer {
   alignas(64) unsigned char map_gu[128] = {};
   alignas(64) unsigned char map_dn[128] = {};
   bool maps_ok = false;
+  // W4A4 on the tensor-core path: the packed tiles again in the MMA layout
+  // (layout.cuh), rebuilt from the arena before the first forward after any
+  // change to it, and the TMA maps of its code regions
+  uint8_t* mma = nullptr;
+  uint64_t mma_expert_bytes = 0;
+  bool mma_dirty = true;
+  alignas(64) unsigned char map_gu_mma[128] = {};
+  alignas(64) unsigned char map_dn_mma[128] = {};
+  bool mma_maps_ok = false;
   uint8_t* arena = nullptr;      // HBM: every expert in order, or the HBM slots of a split placement
   uint64_t arena_bytes = 0;
   // Split placement (moe_place_experts): experts without an HBM slot live in a
@@ -172,8 +181,11 @@ namespace {
 
 // The TMA tile maps of the tensor-core path view the arena as
 // [expert][tile][piece]: only while every expert sits there in expert order.
+void make_mma_maps(moe_layer* L);
+
 void make_tile_maps(moe_layer* L) {
   L->maps_ok = false;
+  L->mma_dirty = true;
   if (L->eptr || L->dev_fmt != FMT_NVFP4 || L->H % 128 || (2 * L->I) % 128) return;
   const ExpertGeom& g = L->geom;
   const int n_total = L->E + L->shared, gu_tiles = 2 * L->I / 16, dn_tiles = L->H / 16;
@@ -182,6 +194,44 @@ void make_tile_maps(moe_layer* L) {
                        8 * tc_group(gu_tiles / 8)) == cudaSuccess &&
       tc_make_tile_map(L->map_dn, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
                        g.expert_bytes, 8 * tc_group(dn_tiles / 8)) == cudaSuccess;
+  make_mma_maps(L);
+}
+
+// the MMA layout's regions within an expert: gate/up codes, scales, down codes, scales
+void mma_geoms(const moe_layer* L, MmaGeom& gu, MmaGeom& dn) {
+  gu = mma_geom(2 * L->I, L->H);
+  dn = mma_geom(L->H, L->I);
+}
+
+void make_mma_maps(moe_layer* L) {
+  L->mma_maps_ok = false;
+  if (!L->mma || !L->maps_ok) return;
+  MmaGeom gu, dn;
+  mma_geoms(L, gu, dn);
+  const int n_total = L->E + L->shared;
+  L->mma_maps_ok =
+      tc_make_mma_map(L->map_gu_mma, L->mma, n_total, gu.M, gu.KS, L->mma_expert_bytes,
+                      128 * tc_fp4_group(gu.M / 128)) == cudaSuccess &&
+      tc_make_mma_map(L->map_dn_mma, L->mma + gu.codes + gu.scales, n_total, dn.M, dn.KS,
+                      L->mma_expert_bytes, 128 * tc_fp4_group(dn.M / 128)) == cudaSuccess;
+}
+
+// the MMA layout from the arena (every expert in it, in order), when the arena changed
+int refresh_mma(moe_layer* L, cudaStream_t st) {
+  if (!L->mma_dirty) return MOE_OK;
+  MmaGeom gu, dn;
+  mma_geoms(L, gu, dn);
+  const ExpertGeom& g = L->geom;
+  const int n_total = L->E + L->shared;
+  CK("MMA-layout conversion (gate/up)",
+     launch_to_mma_layout(L->arena, g.expert_bytes, 0, g.gu.tile_bytes, gu.M, gu.K, n_total, L->mma,
+                          L->mma_expert_bytes, 0, gu.codes, st));
+  CK("MMA-layout conversion (down)",
+     launch_to_mma_layout(L->arena, g.expert_bytes, g.gu_bytes, g.dn.tile_bytes, dn.M, dn.K, n_total,
+                          L->mma, L->mma_expert_bytes, gu.codes + gu.scales,
+                          gu.codes + gu.scales + dn.codes, st));
+  L->mma_dirty = false;
+  return MOE_OK;
 }
 
 // Device address of expert e's packed matrices, wherever they are placed.
@@ -258,6 +308,20 @@ ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
     p.ts_x = L->ts_x;
     p.ts_a = L->ts_a;
     p.af = L->ybuf;  // a in fp32 until quantised; the down kernels write y after that
+    // the block-scaled path's NVFP4 activations, in the f16 copies' space
+    const size_t rows = (size_t)T * L->k + (L->shared ? T : 0);
+    p.xq = reinterpret_cast<const uint8_t*>(L->xh);
+    p.xqs = p.xq + (size_t)T * L->H / 2;
+    p.aq = reinterpret_cast<const uint8_t*>(L->abuf);
+    p.aqs = p.aq + rows * L->I / 2;
+    if (L->mma) {
+      MmaGeom gu, dn;
+      mma_geoms(L, gu, dn);
+      p.mma = L->mma;
+      p.mma_expert_bytes = L->mma_expert_bytes;
+      p.mma_gu_sc = gu.codes;
+      p.mma_dn_sc = gu.codes + gu.scales + dn.codes;
+    }
   }
   return p;
 }
@@ -295,6 +359,9 @@ bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E,
 
 bool w4a4(const moe_layer* L) { return L->act_fmt == MOE_ACT_NVFP4; }
 
+// W4A4 on the tensor-core path: the expert GEMMs on the block-scaled FP4 MMA
+bool fq_path(moe_layer* L, int T) { return w4a4(L) && tc_path(L, T) && L->mma_maps_ok; }
+
 // top-k then dispatch: one fused launch where it applies, else two (or three)
 int launch_topk_and_dispatch(moe_layer* L, const RouteParams& rp, int T, bool pdl, cudaStream_t st) {
   if (topk_dispatch_ok(T, L->k, L->E)) {
@@ -306,20 +373,39 @@ int launch_topk_and_dispatch(moe_layer* L, const RouteParams& rp, int T, bool pd
   return MOE_OK;
 }
 
-// W4A4: x quantised per token into the f16 copy the expert kernels read
-// (e2m1 code x e4m3 block scale) and the per-token tensor scales
+// W4A4: x quantised per token, with the per-token tensor scales, into the
+// f16 copy the expert kernels read (e2m1 code x e4m3 block scale), or, for the
+// block-scaled FP4 GEMMs, into codes and block scales in the same space
 int launch_quant_x(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
-  CK("activation quantiser launch (x)", launch_quantize_act(x, true, T, L->H, nullptr, nullptr, L->xh,
+  uint8_t* codes = nullptr;
+  uint8_t* scales = nullptr;
+  uint16_t* f16 = L->xh;
+  if (fq_path(L, T)) {
+    const ExpertParams ep = expert_params(L, x, T);
+    codes = const_cast<uint8_t*>(ep.xq);
+    scales = const_cast<uint8_t*>(ep.xqs);
+    f16 = nullptr;
+  }
+  CK("activation quantiser launch (x)", launch_quantize_act(x, true, T, L->H, codes, scales, f16,
                                                              L->ts_x, L->status, true, st));
   return MOE_OK;
 }
 
-// W4A4: the rows of a (fp32, written by gate/up) quantised into abuf and ts_a
+// W4A4: the rows of a (fp32, written by gate/up) quantised into abuf (f16
+// values, or codes and block scales for the FP4 GEMMs) and ts_a
 int launch_quant_a(moe_layer* L, int T, cudaStream_t st) {
   const int rows = T * L->k + (L->shared ? T : 0);
-  CK("activation quantiser launch (a)", launch_quantize_act(L->ybuf, false, rows, L->I, nullptr,
-                                                             nullptr, L->abuf, L->ts_a, L->status,
-                                                             true, st));
+  uint8_t* codes = nullptr;
+  uint8_t* scales = nullptr;
+  uint16_t* f16 = L->abuf;
+  if (fq_path(L, T)) {
+    const ExpertParams ep = expert_params(L, nullptr, T);
+    codes = const_cast<uint8_t*>(ep.aq);
+    scales = const_cast<uint8_t*>(ep.aqs);
+    f16 = nullptr;
+  }
+  CK("activation quantiser launch (a)", launch_quantize_act(L->ybuf, false, rows, L->I, codes, scales,
+                                                             f16, L->ts_a, L->status, true, st));
   return MOE_OK;
 }
 
@@ -334,6 +420,15 @@ int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t 
 
 int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
+  if (fq_path(L, T)) {
+    const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
+    if (refresh_mma(L, st)) return MOE_ECUDA;
+    CK("FP4 tensor-core gate/up kernel launch", launch_tc_fp4_gateup(ep, gy, L->map_gu_mma, st));
+    if (launch_quant_a(L, T, st)) return MOE_ECUDA;
+    CK("FP4 tensor-core down kernel launch", launch_tc_fp4_down(ep, gy, L->map_dn_mma, st));
+    CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
+    return MOE_OK;
+  }
   if (tc_path(L, T)) {
     const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
     CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, L->map_gu, st));
@@ -563,6 +658,7 @@ void moe_layer_destroy(moe_layer* L) {
   cudaFree(L->arena);
   cudaFreeHost(L->mirror);
   cudaFree(L->eptr);
+  cudaFree(L->mma);
   cudaFree(L->tscale);
   cudaFree(L->router);
   cudaFree(L->bias);
@@ -583,6 +679,14 @@ int moe_layer_status(moe_layer* L, int reset, int* status) {
 int moe_forward_launches(moe_layer* L, int T) {
   if (!L || T < 1) return fail(MOE_EINVAL, "moe_forward_launches: bad argument");
   return forward_launches(L, T);
+}
+
+int moe_forward_path(moe_layer* L, int T) {
+  if (!L || T < 1) return fail(MOE_EINVAL, "moe_forward_path: bad argument");
+  if (small_path(L, T)) return MOE_PATH_DECODE;
+  if (fq_path(L, T)) return MOE_PATH_TC_FP4;
+  if (tc_path(L, T)) return MOE_PATH_TC_F16;
+  return MOE_PATH_STREAM;
 }
 
 int moe_place_experts(moe_layer* L, const uint8_t* in_hbm) {
@@ -689,6 +793,7 @@ int moe_pack_matrix(moe_layer* L, int expert, int matrix, const uint8_t* codes,
   if (matrix < 0 || matrix > 2) return fail(MOE_EINVAL, "moe_pack_matrix: matrix %d", matrix);
   DeviceGuard dg(L->device);
   cudaStream_t st = (cudaStream_t)stream;
+  L->mma_dirty = true;  // (the MMA layout follows the arena)
   const int rows = matrix == MOE_DOWN ? L->H : L->I, K = matrix == MOE_DOWN ? L->I : L->H;
   const bool fp4 = L->dev_fmt == FMT_NVFP4, mx = L->fmt == MOE_FMT_MXFP4;
   const size_t code_bytes = fp4 ? (size_t)rows * K / 2 : (size_t)rows * K;
@@ -861,6 +966,30 @@ int moe_set_act_format(moe_layer* L, int fmt) {
   if (!L) return fail(MOE_EINVAL, "moe_set_act_format: null layer");
   if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_NVFP4)
     return fail(MOE_EINVAL, "moe_set_act_format: unknown activation format %d", fmt);
+  if (fmt == MOE_ACT_NVFP4 && L->dev_fmt == FMT_NVFP4 && !L->mma && L->H % 128 == 0 &&
+      (2 * L->I) % 128 == 0) {
+    // the block-scaled GEMMs' copy of the weights in the MMA layout (built before the next forward)
+    DeviceGuard dg(L->device);
+    MmaGeom gu, dn;
+    mma_geoms(L, gu, dn);
+    const uint64_t eb = gu.codes + gu.scales + dn.codes + dn.scales;
+    const size_t bytes = (size_t)eb * (L->E + L->shared);
+    uint8_t* mma = nullptr;
+    if (alloc_dev((void**)&mma, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(MOE_ENOMEM, "moe_set_act_format: allocation of the MMA-layout weights (%zu bytes) failed",
+                  bytes);
+    }
+    const cudaError_t e = cudaMemset(mma, 0, bytes);
+    if (e != cudaSuccess) {
+      cudaFree(mma);
+      CK("moe_set_act_format: clear the MMA-layout weights", e);
+    }
+    L->mma = mma;
+    L->mma_expert_bytes = eb;
+    L->mma_dirty = true;
+    make_mma_maps(L);
+  }
   L->act_fmt = fmt;
   return MOE_OK;
 }
@@ -981,13 +1110,19 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       }
       break;
     case 2:
-      if (tc_path(L, T))
+      if (fq_path(L, T) && (rc = refresh_mma(L, st))) return rc;
+      if (fq_path(L, T))
+        CK("gate/up", launch_tc_fp4_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu_mma, st));
+      else if (tc_path(L, T))
         CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu, st));
       else
         CK("gate/up", launch_gateup(ep, grid_y, false, st));
       break;
     case 3:
-      if (tc_path(L, T))
+      if (fq_path(L, T) && (rc = refresh_mma(L, st))) return rc;
+      if (fq_path(L, T))
+        CK("down", launch_tc_fp4_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn_mma, st));
+      else if (tc_path(L, T))
         CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn, st));
       else if (fused)
         CK("down+combine", launch_down_combine(ep, L->gates, L->inv, out, false, false, st));

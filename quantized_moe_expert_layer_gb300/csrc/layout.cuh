@@ -101,4 +101,30 @@ MOE_HD uint64_t tile_offset(const ExpertGeom& e, int m, int r) {
   return ((uint64_t)r * 2u + (uint64_t)m) * (uint64_t)e.gu.tile_bytes;
 }
 
+// MMA layout of an NVFP4 matrix region (a second copy of the packed tiles,
+// kept for the block-scaled tensor-core GEMMs): M rows in tile order (gate/up:
+// M = 2I, 16-row gate and up tiles alternating; down: M = H), K columns, in
+// stages of 256 columns (KS = ceil(K/256));
+//   codes  [KS][M][128 B]: row r's columns 256s .. 256s + 255 in natural order
+//          (low nibble = lower column, zero past K), so that the 128 rows x
+//          128 bytes of a stage of an M-block are one contiguous 16 KB read;
+//   scales [KS][M/128 blocks][4 K-steps of 64][512 B], a K-step's 512 bytes
+//          holding row r's 4 block scales at (r % 32) * 16 + (r / 32) * 4 + b
+//          (the groups tcgen05.cp moves).
+// Per expert: gate/up codes, gate/up scales, down codes, down scales.
+struct MmaGeom {
+  int M, K, KS;
+  uint64_t codes, scales;  // bytes
+};
+
+MOE_HD MmaGeom mma_geom(int M, int K) {
+  MmaGeom g;
+  g.M = M;
+  g.K = K;
+  g.KS = (K + 255) / 256;
+  g.codes = (uint64_t)g.KS * (uint64_t)M * 128u;
+  g.scales = (uint64_t)g.KS * (uint64_t)(M / 128) * 2048u;
+  return g;
+}
+
 }  // namespace moe

@@ -88,20 +88,21 @@ __global__ void quant_nvfp4_kernel(const float* __restrict__ W, int rows, int K,
   }
 }
 
-// Activation rows to NVFP4 with one tensor scale per row: one CTA per row.
+// Activation rows to NVFP4 with one tensor scale per row: one warp per row,
+// 8 rows per CTA; lane l takes the 16-column blocks l, l + 32, ...
 // The same arithmetic as quant_nvfp4_kernel (IEEE fp32 divisions, e4m3 and
 // e2m1 round to nearest even), so a row gives the bytes the weight quantiser
 // gives for a one-row matrix.
 template <bool IN_BF16>
-__global__ void __launch_bounds__(256) quant_act_kernel(const void* __restrict__ in, int K,
+__global__ void __launch_bounds__(256) quant_act_kernel(const void* __restrict__ in, int rows, int K,
                                                         uint8_t* __restrict__ codes,
                                                         uint8_t* __restrict__ scales,
                                                         uint16_t* __restrict__ out_f16,
                                                         float* __restrict__ ts_out, int* status) {
   griddep_wait();
   griddep_launch();
-  const int row = blockIdx.x, tid = threadIdx.x;
-  __shared__ float red[8];
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= rows) return;
   auto load16 = [&](int b, float (&w)[16]) {
     if constexpr (IN_BF16) {
       const uint4* q = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(in) +
@@ -128,24 +129,21 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void* __restrict__
   };
   const int nb = K / 16;
   float m = 0.0f;
-  for (int b = tid; b < nb; b += blockDim.x) {
+  for (int b = lane; b < nb; b += 32) {
     float w[16];
     load16(b, w);
 #pragma unroll
     for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
   }
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((tid & 31) == 0) red[tid >> 5] = m;
-  __syncthreads();
-  float A = 0.0f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) A = fmaxf(A, red[i]);
+  float A = m;
   if (!(A <= 3.0e38f)) {  // inf or NaN in the row
-    if (tid == 0 && status) *status = kStatusRange;
+    if (lane == 0 && status) *status = kStatusRange;
     A = 0.0f;
   }
   const float ts = (A > 0.0f) ? __fdiv_rn(A, 2688.0f) : 0.0f;
-  if (tid == 0) ts_out[row] = ts;
-  for (int b = tid; b < nb; b += blockDim.x) {
+  if (lane == 0) ts_out[row] = ts;
+  for (int b = lane; b < nb; b += 32) {  // (the row again, from L1)
     float w[16];
     load16(b, w);
     float amax = 0.0f;
@@ -442,6 +440,52 @@ __global__ void dequant_nvfp4_kernel(const uint8_t* __restrict__ src, uint64_t t
   }
 }
 
+// Packed NVFP4 tiles of one matrix region (rows M, K columns) of every
+// expert -> the MMA layout (layout.cuh): one thread per (expert, tile,
+// super-chunk, lane), as the packer.  A code vector's word w holds bytes
+// (row g: columns 4w, 4w+1), (row g+8: 4w, 4w+1), (g: 4w+2, 4w+3),
+// (g+8: 4w+2, 4w+3) of the lane's 16 columns: two byte permutes give each
+// row's 8 bytes in column order.
+__global__ void to_mma_layout_kernel(const uint8_t* __restrict__ arena, uint64_t expert_bytes,
+                                     uint64_t src_off, int tile_bytes, int M, int K, int n_experts,
+                                     uint8_t* __restrict__ dst, uint64_t dst_expert_bytes,
+                                     uint64_t codes_off, uint64_t scales_off) {
+  const MatGeom g = mat_geom(FMT_NVFP4, K);
+  const int tiles = M / 16;
+  const int64_t total = (int64_t)n_experts * tiles * g.nsc * 32;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int lane = (int)(i % 32), s = (int)((i / 32) % g.nsc), r = (int)((i / (32 * g.nsc)) % tiles);
+  const int64_t e = i / ((int64_t)32 * g.nsc * tiles);
+  const int gi = lane >> 2, t = lane & 3;
+  const int ra = 16 * r + gi, rb = ra + 8;
+  const uint8_t* base = arena + (uint64_t)e * expert_bytes + src_off + (uint64_t)r * tile_bytes +
+                        (uint64_t)s * g.sc_bytes;
+  uint8_t* codes = dst + (uint64_t)e * dst_expert_bytes + codes_off;
+  uint8_t* scl = dst + (uint64_t)e * dst_expert_bytes + scales_off;
+  const uint4 sv = *reinterpret_cast<const uint4*>(base + 16 * lane);
+  const int mblocks = M / 128;
+  for (int j = 0; j < sc_units(g, s); ++j) {
+    const int c = 8 * s + j;
+    const uint4 cv = *reinterpret_cast<const uint4*>(base + 512 * (1 + j) + 16 * lane);
+    // stage c / 4, bytes 32 (c % 4) + 8t of the row's 128
+    const uint64_t at = ((uint64_t)(c / 4) * M) * 128 + 32 * (c % 4) + 8 * t;
+    *reinterpret_cast<uint2*>(codes + at + (uint64_t)ra * 128) =
+        make_uint2(__byte_perm(cv.x, cv.y, 0x6420), __byte_perm(cv.z, cv.w, 0x6420));
+    *reinterpret_cast<uint2*>(codes + at + (uint64_t)rb * 128) =
+        make_uint2(__byte_perm(cv.x, cv.y, 0x7531), __byte_perm(cv.z, cv.w, 0x7531));
+    const uint32_t sp = u4get(sv, j >> 1) >> (16 * (j & 1));  // block 4c + t of rows ra, rb
+    const int st = c / 4, kk = c % 4;
+    const int rows[2] = {ra, rb};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int x = rows[h], mb = x / 128, rr = x % 128;
+      scl[((uint64_t)(st * mblocks + mb) * 4 + kk) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + t] =
+          (uint8_t)((sp >> (8 * h)) & 0xFFu);
+    }
+  }
+}
+
 __device__ __forceinline__ float pow2_from_ue8m0(uint32_t b) {
   return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
 }
@@ -520,10 +564,11 @@ cudaError_t launch_quantize_act(const void* in, bool in_bf16, int rows, int K, u
                                 uint8_t* scales, uint16_t* out_f16, float* ts, int* status,
                                 bool pdl, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
+  const dim3 grid((rows + 7) / 8);
   if (in_bf16)
-    return launch_k(quant_act_kernel<true>, dim3(rows), dim3(256), 0, st, pdl, in, K, codes, scales,
+    return launch_k(quant_act_kernel<true>, grid, dim3(256), 0, st, pdl, in, rows, K, codes, scales,
                     out_f16, ts, status);
-  return launch_k(quant_act_kernel<false>, dim3(rows), dim3(256), 0, st, pdl, in, K, codes, scales,
+  return launch_k(quant_act_kernel<false>, grid, dim3(256), 0, st, pdl, in, rows, K, codes, scales,
                   out_f16, ts, status);
 }
 
@@ -558,6 +603,18 @@ cudaError_t launch_pack(int fmt, const uint8_t* codes, const uint8_t* scales, in
                                               ts_val, ts_dst);
   else
     pack_fp6_kernel<<<blocks, 128, 0, st>>>(codes, scales, rows, K, dst, tile_stride, ts_dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_mma_layout(const uint8_t* arena, uint64_t expert_bytes, uint64_t src_off,
+                                 int tile_bytes, int M, int K, int n_experts, uint8_t* dst,
+                                 uint64_t dst_expert_bytes, uint64_t codes_off, uint64_t scales_off,
+                                 cudaStream_t st) {
+  const MatGeom g = mat_geom(FMT_NVFP4, K);
+  const int64_t n = (int64_t)n_experts * (M / 16) * g.nsc * 32;
+  to_mma_layout_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+      arena, expert_bytes, src_off, tile_bytes, M, K, n_experts, dst, dst_expert_bytes, codes_off,
+      scales_off);
   return cudaGetLastError();
 }
 

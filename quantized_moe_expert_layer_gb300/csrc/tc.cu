@@ -111,6 +111,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 struct TcShared {
   uint64_t full[kTcStages];
@@ -340,6 +343,64 @@ __device__ __forceinline__ void tma_load_tiles(uint32_t dst, const CUtensorMap* 
       : "memory");
 }
 
+// Epilogue of the expert GEMMs, by the 16 producer warps (warp w reads TMEM
+// lanes 32(w%4)..+31 and every fourth group of 32 columns): G accumulators of
+// npc columns side by side, row r of M-block m in lane r.  MODE 0: rows 32q..
+// 32q+15 of quadrant q are a gate tile and 32q+16.. the matching up tile;
+// a = silu(ts_g * g) * (ts_u * u) (times the token's scale in W4A4) goes to
+// af (fp32) or abuf (f16).  MODE 1: y rows (times the row's scale in W4A4).
+template <int MODE>
+__device__ __forceinline__ void tx_epilogue(const ExpertParams& p, int expert, int row0, int n,
+                                            int n_pad, int npc, int G, uint32_t tmem_d,
+                                            const int* tok) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qd = warp & 3;             // TMEM lane quadrant of this warp
+  const int r = 32 * qd + lane;        // row of the 128-row block
+  const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+  for (int m = 0; m < G; ++m) {
+    const int mb = G * blockIdx.x + m;  // M-block of the matrix
+    const uint32_t acc = tmem_d + lane_addr + (uint32_t)(m * npc);
+    if (MODE == 0) {
+      const int pair = 4 * mb + qd, i = 16 * pair + (lane & 15);
+      const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
+      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 32 * (kTxPW / 4)) {
+        uint32_t v[32];
+        tmem_ld32(acc + c0, v);
+#pragma unroll
+        for (int qq = 0; qq < 32; ++qq) {
+          const float mine = __uint_as_float(v[qq]);
+          const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+          const int col = c0 + qq;
+          if (lane < 16 && col < n) {
+            const float sx = p.ts_x ? p.ts_x[tok[col]] : 1.0f;  // W4A4: the token's scale
+            const float Gv = (ts_g * sx) * mine, U = (ts_u * sx) * other;
+            const float a = Gv / (1.0f + expf(-Gv)) * U;
+            if (p.af)
+              p.af[(size_t)(row0 + col) * p.I + i] = a;
+            else
+              p.abuf[(size_t)(row0 + col) * p.I + i] = a_to_f16(a, p.status);
+          }
+        }
+      }
+    } else {
+      const float ts = p.tscale[expert * 3 + 2];
+      const int h = kTcM * mb + r;
+      for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 32 * (kTxPW / 4)) {
+        uint32_t v[32];
+        tmem_ld32(acc + c0, v);
+#pragma unroll
+        for (int qq = 0; qq < 32; ++qq) {
+          const int col = c0 + qq;
+          if (col < n) {
+            const float sa = p.ts_a ? p.ts_a[row0 + col] : 1.0f;  // W4A4: the row's scale
+            p.ybuf[(size_t)(row0 + col) * p.H + h] = (ts * sa) * __uint_as_float(v[qq]);
+          }
+        }
+      }
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kTxThreads, 1)
     tc_expert_kernel(ExpertParams p, const __grid_constant__ CUtensorMap tmap, int G) {
@@ -548,59 +609,456 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   if (warp < kTxPW) ok = mbar_wait_sleep(&sh->acc_full, 0, abort, p.wait_budget);
   if (warp < kTxPW && !ok) mbar_drain(&sh->acc_full, 0);  // MMAs in flight finish before TMEM is freed
   tc_fence_after();
-  if (warp < kTxPW && ok && !*abort) {
-    const int qd = warp & 3;             // TMEM lane quadrant of this warp
-    const int r = 32 * qd + lane;        // row of the 128-row block
-    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
-    for (int m = 0; m < G; ++m) {
-      const int mb = G * blockIdx.x + m;  // M-block of the matrix
-      const uint32_t acc = tmem_d + lane_addr + (uint32_t)(m * npc);
-      if (MODE == 0) {
-        const int pair = 4 * mb + qd, i = 16 * pair + (lane & 15);
-        const float ts_g = p.tscale[expert * 3 + 0], ts_u = p.tscale[expert * 3 + 1];
-        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 32 * (kTxPW / 4)) {
-          uint32_t v[32];
-          tmem_ld32(acc + c0, v);
-#pragma unroll
-          for (int qq = 0; qq < 32; ++qq) {
-            const float mine = __uint_as_float(v[qq]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-            const int col = c0 + qq;
-            if (lane < 16 && col < n) {
-              const float sx = p.ts_x ? p.ts_x[sh->tok[col]] : 1.0f;  // W4A4: the token's scale
-              const float Gv = (ts_g * sx) * mine, U = (ts_u * sx) * other;
-              const float a = Gv / (1.0f + expf(-Gv)) * U;
-              if (p.af)
-                p.af[(size_t)(row0 + col) * p.I + i] = a;
-              else
-                p.abuf[(size_t)(row0 + col) * p.I + i] = a_to_f16(a, p.status);
-            }
-          }
-        }
-      } else {
-        const float ts = p.tscale[expert * 3 + 2];
-        const int h = kTcM * mb + r;
-        for (int c0 = 32 * (warp >> 2); c0 < n_pad; c0 += 32 * (kTxPW / 4)) {
-          uint32_t v[32];
-          tmem_ld32(acc + c0, v);
-#pragma unroll
-          for (int qq = 0; qq < 32; ++qq) {
-            const int col = c0 + qq;
-            if (col < n) {
-              const float sa = p.ts_a ? p.ts_a[row0 + col] : 1.0f;  // W4A4: the row's scale
-              p.ybuf[(size_t)(row0 + col) * p.H + h] = (ts * sa) * __uint_as_float(v[qq]);
-            }
-          }
-        }
-      }
-    }
-  }
+  if (warp < kTxPW && ok && !*abort) tx_epilogue<MODE>(p, expert, row0, n, n_pad, npc, G, tmem_d, sh->tok);
   if (*abort && tid == 0) *p.status = kStatusTimeout;
   tc_fence_before();
   __syncthreads();
   if (warp == kTxPW) {
     tc_fence_after();
     tmem_dealloc(tmem_d, ncols);
+  }
+}
+
+// ---------------------------------------------------------------- W4A4: the block-scaled FP4 MMA
+// With the activations quantised to NVFP4 per row (x per token, a per
+// (token, expert) row), both operands of the expert GEMMs are e2m1 codes with
+// an e4m3 scale per 16 columns, and the products run on tcgen05.mma
+// kind::mxf4nvf4 (scale_vec::4X: four block scales per row and K = 64 step;
+// fp32 accumulators in TMEM).  The weights come from their MMA layout
+// (layout.cuh), so no thread touches them on the way in.
+//
+// Persistent: one CTA per SM walks the work units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ...; unit u = (work item u / M-blocks: an expert
+// and up to 128 of its tokens, 128-row M-block u % M-blocks).  The stage ring
+// (kFqNS stages of 256 columns of K) runs on across units, and the
+// accumulators are double-buffered, so a unit's epilogue overlaps the next
+// unit's loads and MMAs.  Per stage:
+//   * the TMA warp loads the M-block's codes (one 128-byte x 128-row box, 16
+//     contiguous KB of the layout, 128B-swizzled: the K-major layout the MMA
+//     reads) and its block scales (2 KB, one bulk copy);
+//   * warps 0-7 copy the token rows with cp.async, two stages ahead: codes
+//     (128 bytes a row) into the B stage, block scales (4 bytes a row per
+//     K-step) into 512-byte groups;
+//   * one thread each (warps 18 and 19) moves the stage's block scales of A
+//     and of B into tensor memory with tcgen05.cp 32x128b.warpx4 (a 512-byte
+//     group of 32 rows x 16 bytes, row l holding the 4 scales of rows l, l+32,
+//     l+64 and l+96, lands in lanes l of all four lane quadrants, one 32-bit
+//     column per 32-row group) and commits them to the slot's mbarrier: a
+//     copy takes about as long to issue as an MMA, so three threads share the
+//     issuing;
+//   * the MMA thread waits for both and issues the stage's 4 MMAs;
+//   * warps 8-15 read a finished unit's accumulators (the activation scales
+//     of their columns loaded before the wait) and hand the buffer back.
+constexpr int kFqThreads = 32 * 20;       // copy 0-7, epilogue 8-15, MMA 16, TMA 17, scale copies 18-19
+constexpr int kFqK = 256;                 // K per stage (4 steps of 64)
+constexpr int kFqNS = 6;                  // stages in flight
+constexpr int kFqLB = 3;                  // token-row stages copied ahead
+constexpr int kFqAStage = kTcM * 128;     // 16 KB of codes
+constexpr int kFqBStage = kTcMaxN * 128;  // 16 KB of codes
+constexpr int kFqSf = 4 * 512;            // block scales of a stage: 4 K-steps x 128 rows x 4
+constexpr int kFqStage = kFqAStage + kFqBStage + 2 * kFqSf;
+// TMEM columns: two accumulators of 128, then 16 columns of A scales and 16
+// of B scales per stage slot
+constexpr uint32_t kFqSfaCol = 256;
+constexpr uint32_t kFqSfbCol = kFqSfaCol + 16 * kFqNS;
+static_assert(kFqSfbCol + 16 * kFqNS <= 512, "tensor memory columns");
+
+struct FqShared {
+  uint64_t full_a[kFqNS];  // the TMA's codes and scales of the slot (transaction bytes)
+  uint64_t full_b[kFqNS];  // the 8 copy warps' token rows of the slot
+  uint64_t sfa[kFqNS];     // the slot's A scales are in tensor memory
+  uint64_t sfb[kFqNS];     // the slot's B scales are in tensor memory
+  uint64_t empty[kFqNS];   // the MMAs reading the slot are done
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t fin, fin2[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__host__ __device__ constexpr size_t fq_smem_bytes() {
+  return 1024 + (size_t)kFqNS * kFqStage + sizeof(FqShared);
+}
+
+// Instruction descriptor of kind::mxf4nvf4: A and B e2m1 (format 1), both
+// K-major, e4m3 block scales (scale format 0), D fp32 (implied), M x N; the
+// scale-factor ids stay 0 (at scale_vec::4X all four bytes of a column count).
+__device__ __forceinline__ uint32_t idesc_mxf4nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem));
+}
+
+// Shared-memory descriptor of a 512-byte group of 32 rows x 16 bytes without
+// swizzle: 8-row core matrices of 128 contiguous bytes, 128 bytes apart (both
+// offsets 128, so the group is read as one contiguous block either way).
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128 >> 4) << 16;
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  return d;
+}
+
+// lanes l of all four TMEM lane quadrants, 4 columns from taddr <- row l of the group
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// byte of the block scale (row r, K-step kk of the stage, block b of the step) in a staging area
+__device__ __forceinline__ uint32_t sf_off(int r, int kk, int b) {
+  return (uint32_t)(kk * 512 + (r & 31) * 16 + (r >> 5) * 4 + b);
+}
+
+// L2 policies: the weights stream through once (evict first), the token rows
+// are read once per M-block (evict last)
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tiled TMA load of the MMA layout's box at (row y, stage s, expert e), counted on `bar`
+__device__ __forceinline__ void tma_load_codes(uint32_t dst, const CUtensorMap* map, int y, int s, int e,
+                                               uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(s), "r"(e), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned), counted on `bar`
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// cp.async of 16 (or 4) bytes with an L2 policy
+__device__ __forceinline__ void cp_async16_pol(uint32_t saddr, const void* g, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4_pol(uint32_t saddr, const void* g, uint64_t pol) {
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2;" ::"r"(saddr), "l"(g), "l"(pol)
+               : "memory");
+}
+
+struct FqUnit {
+  int expert, row0, n, mb;
+};
+
+// The first valid unit at or after u among u, u + gridDim.x, ... (< n_units);
+// n_units when there is none.  Every role of the CTA walks the same sequence.
+__device__ __forceinline__ int fq_next(const ExpertParams& p, int u, int n_units, int mblocks,
+                                       FqUnit& w) {
+  for (; u < n_units; u += gridDim.x) {
+    if (tc_entry(p, u / mblocks, w.expert, w.row0, w.n)) {
+      w.mb = u % mblocks;
+      return u;
+    }
+  }
+  return n_units;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kFqThreads, 1)
+    tc_fp4_kernel(ExpertParams p, const __grid_constant__ CUtensorMap tmap, int max_items) {
+  griddep_wait();
+  extern __shared__ __align__(1024) uint8_t fq_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(fq_smem_raw) + 1023) & ~(uintptr_t)1023);
+  // per stage slot: A codes (16 KB), B codes (16 KB), A scales (2 KB), B scales (2 KB)
+  FqShared* sh = reinterpret_cast<FqShared*>(base + kFqNS * kFqStage);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.T * p.k;
+  const int K = MODE == 1 ? p.I : p.H;
+  const int KC = K / 64, KS = (K + kFqK - 1) / kFqK;
+  const int mblocks = (MODE == 1 ? p.H : 2 * p.I) / kTcM;
+  const int items = min(p.nsh_tc + *p.n_tc_entries, max_items);
+  const int n_units = mblocks * max(items, 0);
+  const uint32_t s0 = smem_u32(base);
+  auto a_addr = [&](int slot) { return s0 + slot * kFqStage; };
+  auto b_addr = [&](int slot) { return s0 + slot * kFqStage + kFqAStage; };
+  auto sa_addr = [&](int slot) { return s0 + slot * kFqStage + kFqAStage + kFqBStage; };
+  auto sb_addr = [&](int slot) { return sa_addr(slot) + kFqSf; };
+
+  if (tid == 0) {
+    for (int i = 0; i < kFqNS; ++i) {
+      mbar_init(&sh->full_a[i], 1);
+      mbar_init(&sh->full_b[i], 8);
+      mbar_init(&sh->sfa[i], 1);
+      mbar_init(&sh->sfb[i], 1);
+      mbar_init(&sh->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->acc_full[i], 1);
+      mbar_init(&sh->acc_empty[i], 8);  // the 8 epilogue warps
+    }
+    mbar_init(&sh->fin, 1);
+    mbar_init(&sh->fin2[0], 1);
+    mbar_init(&sh->fin2[1], 1);
+    sh->abort = 0;
+    mbar_init_fence();
+  }
+  // B codes and scales start zero: rows past a unit's tokens are only ever written with zeros
+  for (int i = tid; i < kFqNS * (kFqBStage + 2 * kFqSf) / 16; i += kFqThreads) {
+    const int slot = i / ((kFqBStage + 2 * kFqSf) / 16), o = i % ((kFqBStage + 2 * kFqSf) / 16);
+    st_shared_v4(b_addr(slot) + 16 * o, 0, 0, 0, 0);  // (B codes, then the A and B scale groups)
+  }
+  fence_async_smem();  // (the zeros, for the MMAs and scale copies)
+  if (warp == kTxPW) tmem_alloc(&sh->tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = sh->tmem_base;
+  volatile int* abort = &sh->abort;
+  // row of x (MODE 0: the token) or of a (MODE 1) behind column r of a unit
+  auto b_row = [&](const FqUnit& w, int r) -> size_t {
+    if (MODE == 1) return (size_t)(w.row0 + r);
+    return (size_t)(w.expert == p.E ? w.row0 - S + r : p.row_token[w.row0 + r]);
+  };
+
+  if (warp < 8) {
+    // ---------------------------------------------------------------- token rows, kFqLB stages ahead
+    const uint8_t* bcodes = MODE == 0 ? p.xq : p.aq;
+    const uint8_t* bscales = MODE == 0 ? p.xqs : p.aqs;
+    // thread tid takes row tid / 2 of a unit (`row`: its row of x or a,
+    // loaded once per unit), half tid % 2 of its code pieces and scale words;
+    // rows past the unit's tokens that held an earlier, longer unit's get zeros
+    const int br = tid >> 1, bh = tid & 1;
+    const uint64_t pol = l2_evict_last();
+    int bn[kFqNS] = {};  // tokens each slot's B rows last held (the same in every copier thread)
+    FqUnit w;
+    int u = fq_next(p, blockIdx.x, n_units, mblocks, w), s = 0;
+    size_t row = (u < n_units && br < w.n) ? b_row(w, br) : 0;
+    int issued = 0, done = 0;
+    bool ok = true;
+    auto issue_next = [&]() {  // the next stage of the unit sequence into its slot
+      if (ok && u < n_units) {
+        const int slot = issued % kFqNS;
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->empty[slot], ((issued / kFqNS) & 1) ^ 1,
+                                                     abort, p.wait_budget))) {
+          ok = false;
+        } else {
+          const int nsub = min(4, KC - 4 * s);
+          const uint32_t bs = b_addr(slot), fs = sb_addr(slot);
+          if (br < w.n) {
+            for (int pc = bh * nsub; pc < (bh + 1) * nsub; ++pc)  // 16-byte code pieces
+              cp_async16_pol(bs + swz(br, pc), bcodes + row * (K / 2) + 128 * s + 16 * pc, pol);
+            for (int kk = 2 * bh; kk < min(2 * bh + 2, nsub); ++kk)  // 4 scales per K-step
+              cp_async4_pol(fs + sf_off(br, kk, 0), bscales + row * (K / 16) + 16 * s + 4 * kk, pol);
+          } else if (br < bn[slot]) {
+            for (int pc = 4 * bh; pc < 4 * bh + 4; ++pc) st_shared_v4(bs + swz(br, pc), 0, 0, 0, 0);
+            for (int kk = 2 * bh; kk < 2 * bh + 2; ++kk) st_shared_u32(fs + sf_off(br, kk, 0), 0u);
+          }
+          bn[slot] = w.n;
+          ++issued;
+          if (++s == KS) {
+            s = 0;
+            u = fq_next(p, u + gridDim.x, n_units, mblocks, w);
+            if (u < n_units && br < w.n) row = b_row(w, br);
+          }
+        }
+      }
+      cp_async_commit();
+    };
+    for (int i = 0; i < kFqLB; ++i) issue_next();
+    while (ok && done < issued) {
+      issue_next();
+      cp_async_wait<kFqLB>();  // this thread's copies of stage `done` have landed
+      fence_async_smem();      // (for the async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->full_b[done % kFqNS]);
+      ++done;
+    }
+    cp_async_wait<0>();
+  } else if (warp < kTxPW) {
+    // ---------------------------------------------------------------- epilogue
+    // warp 8 + 4h + q: TMEM lane quadrant q (rows 32q..32q+31), columns 64h..64h+63
+    const int qd = warp & 3, ch = (warp - 8) >> 2;
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    FqUnit cur;
+    int uk = 0;
+    for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units;
+         u = fq_next(p, u + gridDim.x, n_units, mblocks, cur), ++uk) {
+      const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+      float sc_lane[2] = {1.0f, 1.0f};  // W4A4 scales of columns 64h + 32c + lane
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col = 64 * ch + 32 * c + lane;
+        if (col < cur.n) {
+          if (MODE == 0 && p.ts_x) sc_lane[c] = p.ts_x[b_row(cur, col)];
+          if (MODE == 1 && p.ts_a) sc_lane[c] = p.ts_a[cur.row0 + col];
+        }
+      }
+      if (!mbar_wait_sleep(&sh->acc_full[buf], (uk >> 1) & 1, abort, p.wait_budget)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem_d + lane_addr + (uint32_t)(128 * buf);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int c0 = 64 * ch + 32 * c;
+        if (c0 >= n_pad) break;
+        uint32_t v[32];
+        tmem_ld32(acc + c0, v);
+        if (MODE == 0) {
+          // lanes 0-15 hold gate rows, 16-31 the matching up rows: lane l < 16
+          // computes columns 0-15 of its row, lane l + 16 columns 16-31
+          const int i = 16 * (4 * cur.mb + qd) + (lane & 15);
+          const bool hi = lane >= 16;
+          const float ts_g = p.tscale[cur.expert * 3 + 0], ts_u = p.tscale[cur.expert * 3 + 1];
+#pragma unroll
+          for (int qq = 0; qq < 16; ++qq) {
+            const float lo_v = __uint_as_float(v[qq]), hi_v = __uint_as_float(v[16 + qq]);
+            const float recv = __shfl_xor_sync(0xffffffffu, hi ? lo_v : hi_v, 16);
+            const int cq = hi ? 16 + qq : qq;
+            const float gv = hi ? recv : lo_v, uv = hi ? hi_v : recv;
+            const float sx = __shfl_sync(0xffffffffu, sc_lane[c], cq);
+            const int col = c0 + cq;
+            if (col < cur.n) {
+              const float Gv = (ts_g * sx) * gv, U = (ts_u * sx) * uv;
+              const float a = Gv / (1.0f + expf(-Gv)) * U;
+              if (p.af)
+                p.af[(size_t)(cur.row0 + col) * p.I + i] = a;
+              else
+                p.abuf[(size_t)(cur.row0 + col) * p.I + i] = a_to_f16(a, p.status);
+            }
+          }
+        } else {
+          const float ts = p.tscale[cur.expert * 3 + 2];
+          const int h = kTcM * cur.mb + 32 * qd + lane;
+#pragma unroll
+          for (int qq = 0; qq < 32; ++qq) {
+            const float sa = __shfl_sync(0xffffffffu, sc_lane[c], qq);
+            const int col = c0 + qq;
+            if (col < cur.n) p.ybuf[(size_t)(cur.row0 + col) * p.H + h] = (ts * sa) * __uint_as_float(v[qq]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
+    }
+  } else if (warp == kTxPW) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- scale copies and MMA issue
+      FqUnit cur;
+      int gs = 0, uk = 0;
+      bool ok = true;
+      for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units && ok;
+           u = fq_next(p, u + gridDim.x, n_units, mblocks, cur), ++uk) {
+        const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+        const uint32_t idesc = idesc_mxf4nvf4(kTcM, n_pad);
+        // the epilogue of the unit before the previous one has read this accumulator
+        if (!mbar_wait(&sh->acc_empty[buf], ((uk >> 1) & 1) ^ 1, abort, p.wait_budget)) break;
+        tc_fence_after();
+        for (int s = 0; s < KS; ++s, ++gs) {
+          const int nsub = min(4, KC - 4 * s), slot = gs % kFqNS, ph = (gs / kFqNS) & 1;
+          // the codes and token rows (already in when the scales are), and the scales
+          if (!mbar_wait(&sh->sfa[slot], ph, abort, p.wait_budget) ||
+              !mbar_wait(&sh->sfb[slot], ph, abort, p.wait_budget) ||
+              !mbar_wait(&sh->full_a[slot], ph, abort, p.wait_budget) ||
+              !mbar_wait(&sh->full_b[slot], ph, abort, p.wait_budget)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = tmem_d + kFqSfaCol + 16 * slot, sfb = tmem_d + kFqSfbCol + 16 * slot;
+          const uint64_t ad = sw128_desc(a_addr(slot)), bd = sw128_desc(b_addr(slot));
+          for (int kk = 0; kk < nsub; ++kk)  // +32 bytes (64 codes) per K-step
+            umma_mxf4nvf4(tmem_d + 128 * buf, ad + 2 * kk, bd + 2 * kk, idesc, sfa + 4 * kk,
+                          sfb + 4 * kk, (s | kk) != 0);
+          umma_commit(&sh->empty[slot]);
+        }
+        if (ok) umma_commit(&sh->acc_full[buf]);
+      }
+      umma_commit(&sh->fin);  // every copy and MMA issued before TMEM is freed
+      mbar_drain(&sh->fin, 0);
+    }
+    __syncwarp();
+  } else if (warp >= kTxPW + 2) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- scale copies (A: warp 18, B: 19)
+      const bool is_a = warp == kTxPW + 2;
+      FqUnit cur;
+      int gs = 0;
+      bool ok = true;
+      for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units && ok;
+           u = fq_next(p, u + gridDim.x, n_units, mblocks, cur)) {
+        for (int s = 0; s < KS; ++s, ++gs) {
+          const int nsub = min(4, KC - 4 * s), slot = gs % kFqNS, ph = (gs / kFqNS) & 1;
+          if (!mbar_wait(is_a ? &sh->full_a[slot] : &sh->full_b[slot], ph, abort, p.wait_budget)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dst = tmem_d + (is_a ? kFqSfaCol : kFqSfbCol) + 16 * slot;
+          const uint32_t src = is_a ? sa_addr(slot) : sb_addr(slot);
+          for (int kk = 0; kk < nsub; ++kk) tmem_cp_sf(dst + 4 * kk, sf_desc(src + 512 * kk));
+          umma_commit(is_a ? &sh->sfa[slot] : &sh->sfb[slot]);
+        }
+      }
+      umma_commit(&sh->fin2[is_a ? 0 : 1]);  // (its copies done before TMEM is freed)
+      mbar_drain(&sh->fin2[is_a ? 0 : 1], 0);
+    }
+    __syncwarp();
+  } else {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA issue
+      const CUtensorMap* map = &tmap;
+      const uint64_t sc_off = MODE == 1 ? p.mma_dn_sc : p.mma_gu_sc;
+      const uint64_t pol = l2_evict_first();
+      int issued = 0;  // stages issued
+      FqUnit cur;
+      bool ok = true;
+      for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units && ok;
+           u = fq_next(p, u + gridDim.x, n_units, mblocks, cur)) {
+        const uint8_t* scales = p.mma + (size_t)cur.expert * p.mma_expert_bytes + sc_off;
+        for (int s = 0; s < KS; ++s) {
+          const int slot = issued % kFqNS;
+          if (!mbar_wait(&sh->empty[slot], ((issued / kFqNS) & 1) ^ 1, abort, p.wait_budget)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect(&sh->full_a[slot], (uint32_t)(kFqAStage + kFqSf));
+          tma_load_codes(a_addr(slot), map, kTcM * cur.mb, s, cur.expert, &sh->full_a[slot], pol);
+          bulk_load(sa_addr(slot), scales + ((size_t)s * mblocks + cur.mb) * kFqSf, (uint32_t)kFqSf,
+                    &sh->full_a[slot], pol);
+          ++issued;
+        }
+      }
+      if (*abort) {  // let the copies in flight land before the CTA exits (bounded waits)
+        for (int c = (issued > kFqNS ? issued - kFqNS : 0); c < issued; ++c)
+          mbar_drain(&sh->full_a[c % kFqNS], (c / kFqNS) & 1);
+      }
+    }
+    __syncwarp();
+  }
+
+  if (*abort && tid == 0) *p.status = kStatusTimeout;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTxPW) {
+    tc_fence_after();
+    tmem_dealloc(tmem_d, 512);
   }
 }
 
@@ -634,6 +1092,33 @@ cudaError_t tc_make_tile_map(void* map, const uint8_t* region, int n_experts, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// [expert][stage][row][128 B] codes of the MMA layout; a box: the 128 bytes
+// (256 codes) of box_rows consecutive rows of a stage, 128B-swizzled as the
+// MMA reads them
+cudaError_t tc_make_mma_map(void* map, const uint8_t* codes, int n_experts, int rows, int stages,
+                            uint64_t expert_stride, int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // (the bytes viewed as 8-byte elements: 16 to a 128-byte row)
+  const cuuint64_t dims[4] = {16, (cuuint64_t)rows, (cuuint64_t)stages, (cuuint64_t)n_experts};
+  const cuuint64_t strides[3] = {128, (cuuint64_t)rows * 128, expert_stride};
+  const cuuint32_t box[4] = {16, (cuuint32_t)box_rows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT64, 4,
+                            const_cast<uint8_t*>(codes), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool tc_path_ok(int fmt, int T, int k, int E, int H, int I) {
   // NVFP4 only; enough tokens per expert for a dense contraction; tile shapes
   return fmt == FMT_NVFP4 && (long)T * k >= 16L * E && H % kTcM == 0 && (2 * I) % kTcM == 0 &&
@@ -662,6 +1147,37 @@ cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, const void* tile_m
                   tx_smem_bytes(G), st, true, p, map, G);
 }
 
+// M-blocks per work unit of the block-scaled FP4 GEMMs (one: the accumulators are double-buffered)
+int tc_fp4_group(int) { return 1; }
+
+// persistent grid: one CTA per SM, or one per unit when there are fewer
+static int fq_grid(int units) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      sms = 1;
+  }
+  return units < sms ? (units > 0 ? units : 1) : sms;
+}
+
+cudaError_t launch_tc_fp4_gateup(const ExpertParams& p, int items, const void* tile_map,
+                                 cudaStream_t st) {
+  const int mblocks = (2 * p.I) / kTcM;
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  return launch_k(tc_fp4_kernel<0>, dim3(fq_grid(mblocks * items)), dim3(kFqThreads),
+                  fq_smem_bytes(), st, true, p, map, items);
+}
+
+cudaError_t launch_tc_fp4_down(const ExpertParams& p, int items, const void* tile_map,
+                               cudaStream_t st) {
+  const int mblocks = p.H / kTcM;
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  return launch_k(tc_fp4_kernel<1>, dim3(fq_grid(mblocks * items)), dim3(kFqThreads),
+                  fq_smem_bytes(), st, true, p, map, items);
+}
+
 bool tc_router_ok(int E, int H) { return E % kTcM == 0 && H % kTcK == 0; }
 
 // logits_out gets the fp32 dot products (one K slice: the top-k step adds the bias)
@@ -676,6 +1192,12 @@ cudaError_t tc_kernels_init() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc_expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tx_smem_bytes(kTxMaxG));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_fp4_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)fq_smem_bytes());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_fp4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)fq_smem_bytes());
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(tc_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tc_smem());

@@ -92,14 +92,18 @@ def test_activation_quantiser_bit_exact_fp32_rows():
 
 
 # ---------------------------------------------------------------- the layer
-@pytest.mark.parametrize("T", [1, 4, 13, 64, 300])
+@pytest.mark.parametrize("T", [1, 4, 13, 40, 64, 300])
 def test_w4a4_layer_every_path(T):
     """T = 1 and 4: decode (self-routed gate/up, fused down + combine); 13:
-    top-k in the dispatch CTA; 64: streamed GEMVs; 300: tensor-core GEMMs."""
+    top-k in the dispatch CTA; 40: streamed GEMVs; 64 and 300 (T k >= 16 E):
+    the block-scaled FP4 tensor-core GEMMs (kind::mxf4nvf4)."""
     w = small(fmt=1, H=256, I=128, E=8, k=2, T=T, seed=5)
     L = layer(w, T_max=300)
     L.set_act_format(moe.ACT_NVFP4)
     try:
+        want = {1: moe.PATH_DECODE, 4: moe.PATH_DECODE, 13: moe.PATH_STREAM, 40: moe.PATH_STREAM,
+                64: moe.PATH_TC_FP4, 300: moe.PATH_TC_FP4}[T]
+        assert L.path(T) == want
         n16 = L.launches(T)
         rel, ties = compare_layer(w, L, gen.x_tokens(w, T), act_fp4=True)
         assert L.status() == 0 and L.check_workspace() == 0
@@ -176,10 +180,54 @@ def test_w4a4_prefill_full_size_sampled():
     w = gen.get_workload(4)
     L = build_layer(w, T_max=w.T)
     try:
+        assert L.path(w.T) == moe.PATH_TC_F16
         L.set_act_format(moe.ACT_NVFP4)
+        assert L.path(w.T) == moe.PATH_TC_FP4
         sample = [0, 1, 7, 8, 511, 1024, 2047, 2048, 3000, 4093, 4094, 4095]
         rel, ties = compare_layer(w, L, gen.x_tokens(w), sample=sample, act_fp4=True)
         assert L.status() == 0
         print(f"W4A4 prefill (sampled): rel-L2 {rel:.2e}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("H,I,E,T", [(256, 128, 8, 300), (512, 256, 16, 600), (384, 192, 24, 700)])
+def test_block_scaled_gemms_ragged_shapes(H, I, E, T):
+    """The FP4 GEMMs on shapes whose K is not a multiple of a 256-column stage
+    (I = 192: a down stage of 3 K-steps; H = 384) and with items of every
+    token count: against the act_fp4 oracle, bit-identical over repeats,
+    every output element written."""
+    w = small(fmt=1, H=H, I=I, E=E, k=3, T=T, seed=11)
+    L = build_layer(w, T_max=T)
+    try:
+        L.set_act_format(moe.ACT_NVFP4)
+        assert L.path(T) == moe.PATH_TC_FP4
+        x = gen.x_tokens(w, T)
+        compare_layer(w, L, x, sample=list(range(0, T, 5)), act_fp4=True)
+        a = run_gpu(L, x, w, want_routing=False)["out"]
+        b = run_gpu(L, x, w, want_routing=False)["out"]
+        assert np.array_equal(a, b)
+        assert L.status() == 0 and L.check_workspace() == 0
+    finally:
+        L.close()
+
+
+def test_block_scaled_gemms_follow_a_repack():
+    """Packing new weights into the layer after W4A4 is on rebuilds the MMA
+    layout before the next forward."""
+    w = small(fmt=1, H=256, I=128, E=8, k=2, T=300, seed=5)
+    L = build_layer(w, T_max=300)
+    try:
+        L.set_act_format(moe.ACT_NVFP4)
+        x = gen.x_tokens(w, 300)
+        compare_layer(w, L, x, sample=list(range(0, 300, 7)), act_fp4=True)
+        w2 = small(fmt=1, H=256, I=128, E=8, k=2, T=300, seed=6)  # other expert weights
+        ol = oracle.layer_for_workload(w2, list(range(w2.n_experts_total)))
+        for e in range(w2.n_experts_total):
+            for m in range(3):
+                c, sc, ts = ol.mats[(e, m)]
+                L.pack_matrix(e, m, c, sc, ts)
+        # (the router stays w's: the oracle routes with it and combines w2's experts)
+        compare_layer(w, L, x, sample=list(range(0, 300, 7)), orc_layer=ol, act_fp4=True)
     finally:
         L.close()

@@ -253,3 +253,19 @@ def test_w4a4_layer_differs_from_w4a16_by_activation_rounding_only():
         Z.set_matrix(e, 2, np.zeros_like(Z.mats[(e, 2)][0]), np.zeros_like(Z.mats[(e, 2)][1]), 1.0)
     Z.act_fp4 = True
     assert np.all(Z.forward(xz)[3] == 0.0)
+
+
+def test_w4a4_tie_evaluation_matches_the_oracle():
+    """The tie-tolerant W4A4 comparison of the GPU tests (tests/parity.py,
+    w4a4_tie_rel) re-evaluates a token in numpy with a scaled by 1 +- eta
+    before its quantisation.  Against the oracle's own output it gives ~0
+    (the smallest eta leaves the codes of a non-tie token alone), and against
+    an output off by 1% it reports about 1%."""
+    import parity
+    L, x = _tiny_layer(E=8, k=3, shared=1, seed=4)
+    L.act_fp4 = True
+    lg, idx, gates, out = L.forward(x)
+    for t in range(x.shape[0]):
+        assert parity.w4a4_tie_rel(L, x[t], idx[t], gates[t], out[t]) < 1e-6
+        r = parity.w4a4_tie_rel(L, x[t], idx[t], gates[t], out[t] * 1.01)
+        assert 0.009 < r < 0.011

@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--no-per-config", dest="per_config", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--act", choices=["bf16", "nvfp4"], default="bf16",
+                    help="activations of the timed workload: bf16 (W4A16), or NVFP4 per row (W4A4)")
     ap.add_argument("--host-mirror", type=float, default=0.0,
                     help="fraction of each layer's experts placed in the pinned host mirror "
                          "(the coldest by router bias; the kernels read them over the CPU-GPU link)")
@@ -650,21 +652,22 @@ def run_ours(args, w):
     gen.build(device=True)
     moe.build()
     Ln = args.layers or default_layers(w, args.host_mirror)
-    r = measure(w, Ln, args.steps, args.warmup, rank, world, args.host_mirror, headline=True)
+    act = 1 if args.act == "nvfp4" else 0
+    r = measure(w, Ln, args.steps, args.warmup, rank, world, args.host_mirror, headline=True, act=act)
     per_config = {}
     if args.per_config:
         # the other configurations, then the headline's shape with W4A4 activations
-        for idx, act in [(i, 0) for i in PER_CONFIG] + [(WORKLOAD, 1)]:
+        for idx, act_c in [(i, 0) for i in PER_CONFIG] + [(WORKLOAD, 1)]:
             wc = gen.get_workload(idx)
-            if wc.name == w.name and act == 0:
+            if wc.name == w.name and act_c == act:
                 continue
             Lc = default_layers(wc)
             # each config's timed region: about a second of replays
-            one = measure(wc, Lc, max(20, args.warmup), 3, rank, world, act=act)
+            one = measure(wc, Lc, max(20, args.warmup), 3, rank, world, act=act_c)
             steps_c = max(20, min(5000, int(1.0 / max(one["ms"] * 1e-3 / max(20, args.warmup), 1e-6))))
-            rc = measure(wc, Lc, steps_c, 3, rank, world, act=act)
-            per_config[wc.name + ("-w4a4" if act else "")] = {
-                "activations": "nvfp4 per row (W4A4)" if act else "bf16 x, fp32 a (W4A16)",
+            rc = measure(wc, Lc, steps_c, 3, rank, world, act=act_c)
+            per_config[wc.name + ("-w4a4" if act_c else "")] = {
+                "activations": "nvfp4 per row (W4A4)" if act_c else "bf16 x, fp32 a (W4A16)",
                 "tokens_per_step": wc.T, "layer_instances_per_step": Lc, "steps": steps_c,
                 "value": rc["value"], "unit": UNIT, "us_per_layer": rc["us_per_layer"],
                 "format": SHORT_NAMES[wc.fmt], "gpu_launches_per_layer": rc["launches_per_layer"],
@@ -674,11 +677,15 @@ def run_ours(args, w):
     line = {"metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16 x f16 -> f32 (" + SHORT_NAMES[w.fmt] + " weights dequantised exactly to "
-                     "f16; bf16 x copied exactly to f16)",
+            "dtype": ("e2m1 x e2m1 -> f32 with e4m3 block scales (W4A4: x and a quantised to "
+                      "NVFP4 per row; kind::mxf4nvf4 where the tensor-core path runs)") if act else
+                     ("f16 x f16 -> f32 (" + SHORT_NAMES[w.fmt] + " weights dequantised exactly to "
+                      "f16; bf16 x copied exactly to f16)"),
             "data": "synthetic (seeded generator; random-init weights quantised on the device)",
             "config": config_block(w, Ln, {"us_per_layer": r["us_per_layer"],
                                            "host_mirror_fraction": args.host_mirror,
+                                           "activations": "nvfp4 per row (W4A4)" if act else
+                                                          "bf16 x, fp32 a (W4A16)",
                                            "phase_us_alone": r["phase_us_alone"],
                                            "parallelism": f"replicas x{world}"}),
             "roofline": r["roofline"], "e2e": r["e2e"],

@@ -46,12 +46,6 @@ struct ExpertParams {
   const float* ts_x;     // [T] per token
   const float* ts_a;     // [T*k + T] per row of abuf
   float* af;             // [(T*k + T) x I] fp32 a before quantisation
-  // W4A4 on the block-scaled tensor-core path: the activations' NVFP4 codes
-  // [rows x K/2] (low nibble = lower column) and e4m3 block scales [rows x K/16]
-  const uint8_t* xq;     // x: [T x H/2]
-  const uint8_t* xqs;    // [T x H/16]
-  const uint8_t* aq;     // a: [(T*k + T) x I/2]
-  const uint8_t* aqs;    // [(T*k + T) x I/16]
   // the weights in the MMA layout (layout.cuh): per expert mma_expert_bytes,
   // the gate/up and down block scales at mma_gu_sc and mma_dn_sc
   const uint8_t* mma;
@@ -123,13 +117,16 @@ cudaError_t launch_to_mma_layout(const uint8_t* arena, uint64_t expert_bytes, ui
                                  cudaStream_t st);
 // Activations to NVFP4 per row (the weights' recipe with one tensor scale per
 // row): in [rows x K] bf16 (in_bf16) or fp32; optional outputs: canonical
-// codes [rows x K/2] and e4m3 scales [rows x K/16], the f16 values e2m1 code x
-// e4m3 scale [rows x K] (exact), and the tensor scales ts [rows].  A row whose
-// amax is not finite records MOE_ERANGE in *status (if status).  pdl: may
-// start while the previous kernel drains.
+// codes (rows cpitch bytes apart, default K/2) and e4m3 scales (spitch apart,
+// default K/16), the f16 values e2m1 code x e4m3 scale [rows x K] (exact), and
+// the tensor scales ts [rows].  With inv, input row t's codes and scales go to
+// the kd output rows inv[t*kd + j] and, if shared_base >= 0, to row
+// shared_base + t.  A row whose amax is not finite records MOE_ERANGE in
+// *status (if status).  pdl: may start while the previous kernel drains.
 cudaError_t launch_quantize_act(const void* in, bool in_bf16, int rows, int K, uint8_t* codes,
                                 uint8_t* scales, uint16_t* out_f16, float* ts, int* status,
-                                bool pdl, cudaStream_t st);
+                                bool pdl, cudaStream_t st, int cpitch = 0, int spitch = 0,
+                                const int* inv = nullptr, int kd = 0, int shared_base = -1);
 
 // routing
 int router_ksplit(int T, int H, int E);
@@ -184,10 +181,13 @@ cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, const void* tile_m
 int tc_fp4_group(int mblocks);
 cudaError_t tc_make_mma_map(void* map, const uint8_t* codes, int n_experts, int rows, int stages,
                             uint64_t expert_stride, int box_rows);
-cudaError_t launch_tc_fp4_gateup(const ExpertParams& p, int grid_y, const void* tile_map,
-                                 cudaStream_t st);
-cudaError_t launch_tc_fp4_down(const ExpertParams& p, int grid_y, const void* tile_map,
-                               cudaStream_t st);
+cudaError_t launch_tc_fp4_gateup(const ExpertParams& p, int items, const void* tile_map,
+                                 const void* bmap_c, const void* bmap_s, cudaStream_t st);
+cudaError_t launch_tc_fp4_down(const ExpertParams& p, int items, const void* tile_map,
+                               const void* bmap_c, const void* bmap_s, cudaStream_t st);
+// the maps of the activation rows the block-scaled GEMMs read (B operands):
+// [rows][row_bytes], codes (128-byte boxes, 128B-swizzled) or scales (16-byte boxes)
+cudaError_t tc_make_rows_map(void* map, const uint8_t* base, size_t rows, int row_bytes, bool codes);
 bool tc_router_ok(int E, int H);
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);
 cudaError_t tc_kernels_init();

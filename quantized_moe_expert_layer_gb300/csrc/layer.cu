@@ -126,6 +126,16 @@ struct moe_layer {
   alignas(64) unsigned char map_gu_mma[128] = {};
   alignas(64) unsigned char map_dn_mma[128] = {};
   bool mma_maps_ok = false;
+  // ... and their B operands: x quantised into its expert-sorted rows (xg) and
+  // the rows of a (aqb), codes then scales, each row padded (act_pitches),
+  // with the TMA maps of their codes and scales
+  uint8_t* xg = nullptr;
+  uint8_t* aqb = nullptr;
+  alignas(64) unsigned char map_bx_c[128] = {};
+  alignas(64) unsigned char map_bx_s[128] = {};
+  alignas(64) unsigned char map_ba_c[128] = {};
+  alignas(64) unsigned char map_ba_s[128] = {};
+  bool bmaps_ok = false;
   uint8_t* arena = nullptr;      // HBM: every expert in order, or the HBM slots of a split placement
   uint64_t arena_bytes = 0;
   // Split placement (moe_place_experts): experts without an HBM slot live in a
@@ -214,6 +224,24 @@ void make_mma_maps(moe_layer* L) {
                       128 * tc_fp4_group(gu.M / 128)) == cudaSuccess &&
       tc_make_mma_map(L->map_dn_mma, L->mma + gu.codes + gu.scales, n_total, dn.M, dn.KS,
                       L->mma_expert_bytes, 128 * tc_fp4_group(dn.M / 128)) == cudaSuccess;
+}
+
+// rows of the block-scaled GEMMs' B operands: codes padded to 128-byte
+// multiples (one TMA box of a stage), scales to 16-byte multiples
+int act_cpitch(int K) { return (K / 2 + 127) / 128 * 128; }
+int act_spitch(int K) { return (K / 16 + 15) / 16 * 16; }
+size_t act_rows_cap(const moe_layer* L) { return (size_t)L->T_max * L->k + (L->shared ? L->T_max : 0); }
+
+void make_b_maps(moe_layer* L) {
+  L->bmaps_ok = false;
+  if (!L->xg || !L->aqb) return;
+  const size_t rows = act_rows_cap(L);
+  const int cH = act_cpitch(L->H), sH = act_spitch(L->H), cI = act_cpitch(L->I), sI = act_spitch(L->I);
+  L->bmaps_ok =
+      tc_make_rows_map(L->map_bx_c, L->xg, rows, cH, true) == cudaSuccess &&
+      tc_make_rows_map(L->map_bx_s, L->xg + rows * cH, rows, sH, false) == cudaSuccess &&
+      tc_make_rows_map(L->map_ba_c, L->aqb, rows, cI, true) == cudaSuccess &&
+      tc_make_rows_map(L->map_ba_s, L->aqb + rows * cI, rows, sI, false) == cudaSuccess;
 }
 
 // the MMA layout from the arena (every expert in it, in order), when the arena changed
@@ -308,12 +336,6 @@ ExpertParams expert_params(moe_layer* L, const uint16_t* x, int T) {
     p.ts_x = L->ts_x;
     p.ts_a = L->ts_a;
     p.af = L->ybuf;  // a in fp32 until quantised; the down kernels write y after that
-    // the block-scaled path's NVFP4 activations, in the f16 copies' space
-    const size_t rows = (size_t)T * L->k + (L->shared ? T : 0);
-    p.xq = reinterpret_cast<const uint8_t*>(L->xh);
-    p.xqs = p.xq + (size_t)T * L->H / 2;
-    p.aq = reinterpret_cast<const uint8_t*>(L->abuf);
-    p.aqs = p.aq + rows * L->I / 2;
     if (L->mma) {
       MmaGeom gu, dn;
       mma_geoms(L, gu, dn);
@@ -360,7 +382,9 @@ bool tc_router(moe_layer* L, int T) { return tc_path(L, T) && tc_router_ok(L->E,
 bool w4a4(const moe_layer* L) { return L->act_fmt == MOE_ACT_NVFP4; }
 
 // W4A4 on the tensor-core path: the expert GEMMs on the block-scaled FP4 MMA
-bool fq_path(moe_layer* L, int T) { return w4a4(L) && tc_path(L, T) && L->mma_maps_ok; }
+bool fq_path(moe_layer* L, int T) {
+  return w4a4(L) && tc_path(L, T) && L->mma_maps_ok && L->bmaps_ok;
+}
 
 // top-k then dispatch: one fused launch where it applies, else two (or three)
 int launch_topk_and_dispatch(moe_layer* L, const RouteParams& rp, int T, bool pdl, cudaStream_t st) {
@@ -377,17 +401,19 @@ int launch_topk_and_dispatch(moe_layer* L, const RouteParams& rp, int T, bool pd
 // f16 copy the expert kernels read (e2m1 code x e4m3 block scale), or, for the
 // block-scaled FP4 GEMMs, into codes and block scales in the same space
 int launch_quant_x(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
-  uint8_t* codes = nullptr;
-  uint8_t* scales = nullptr;
-  uint16_t* f16 = L->xh;
-  if (fq_path(L, T)) {
-    const ExpertParams ep = expert_params(L, x, T);
-    codes = const_cast<uint8_t*>(ep.xq);
-    scales = const_cast<uint8_t*>(ep.xqs);
-    f16 = nullptr;
-  }
-  CK("activation quantiser launch (x)", launch_quantize_act(x, true, T, L->H, codes, scales, f16,
+  CK("activation quantiser launch (x)", launch_quantize_act(x, true, T, L->H, nullptr, nullptr, L->xh,
                                                              L->ts_x, L->status, true, st));
+  return MOE_OK;
+}
+
+// W4A4 on the block-scaled GEMMs: x quantised per token into each of its
+// expert-sorted rows of xg (after the dispatch: the rows come from inv)
+int launch_quant_x_rows(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
+  const size_t rows = act_rows_cap(L);
+  const int c = act_cpitch(L->H), sc = act_spitch(L->H);
+  CK("activation quantiser launch (x rows)",
+     launch_quantize_act(x, true, T, L->H, L->xg, L->xg + rows * c, nullptr, L->ts_x, L->status,
+                         true, st, c, sc, L->inv, L->k, L->shared ? T * L->k : -1));
   return MOE_OK;
 }
 
@@ -395,17 +421,17 @@ int launch_quant_x(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
 // values, or codes and block scales for the FP4 GEMMs) and ts_a
 int launch_quant_a(moe_layer* L, int T, cudaStream_t st) {
   const int rows = T * L->k + (L->shared ? T : 0);
-  uint8_t* codes = nullptr;
-  uint8_t* scales = nullptr;
-  uint16_t* f16 = L->abuf;
   if (fq_path(L, T)) {
-    const ExpertParams ep = expert_params(L, nullptr, T);
-    codes = const_cast<uint8_t*>(ep.aq);
-    scales = const_cast<uint8_t*>(ep.aqs);
-    f16 = nullptr;
+    const size_t cap = act_rows_cap(L);
+    const int c = act_cpitch(L->I), sc = act_spitch(L->I);
+    CK("activation quantiser launch (a rows)",
+       launch_quantize_act(L->ybuf, false, rows, L->I, L->aqb, L->aqb + cap * c, nullptr, L->ts_a,
+                           L->status, true, st, c, sc));
+    return MOE_OK;
   }
-  CK("activation quantiser launch (a)", launch_quantize_act(L->ybuf, false, rows, L->I, codes, scales,
-                                                             f16, L->ts_a, L->status, true, st));
+  CK("activation quantiser launch (a)", launch_quantize_act(L->ybuf, false, rows, L->I, nullptr,
+                                                             nullptr, L->abuf, L->ts_a, L->status,
+                                                             true, st));
   return MOE_OK;
 }
 
@@ -423,9 +449,12 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   if (fq_path(L, T)) {
     const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
     if (refresh_mma(L, st)) return MOE_ECUDA;
-    CK("FP4 tensor-core gate/up kernel launch", launch_tc_fp4_gateup(ep, gy, L->map_gu_mma, st));
+    if (launch_quant_x_rows(L, x, T, st)) return MOE_ECUDA;
+    CK("FP4 tensor-core gate/up kernel launch",
+       launch_tc_fp4_gateup(ep, gy, L->map_gu_mma, L->map_bx_c, L->map_bx_s, st));
     if (launch_quant_a(L, T, st)) return MOE_ECUDA;
-    CK("FP4 tensor-core down kernel launch", launch_tc_fp4_down(ep, gy, L->map_dn_mma, st));
+    CK("FP4 tensor-core down kernel launch",
+       launch_tc_fp4_down(ep, gy, L->map_dn_mma, L->map_ba_c, L->map_ba_s, st));
     CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
     return MOE_OK;
   }
@@ -471,7 +500,7 @@ int forward_impl(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_
   RouteParams rp = route_params(L, x, T);
   L->last_T = T;
   L->last_has_logits = true;
-  if (w4a4(L)) {
+  if (w4a4(L) && !fq_path(L, T)) {  // (the block-scaled path quantises x after the dispatch)
     const int rc = launch_quant_x(L, x, T, st);
     if (rc) return rc;
   }
@@ -595,6 +624,9 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
       (size_t)T_max * 4,                 // ts_x
       (S + T_max) * 4,                   // ts_a
       4,                                 // ticket
+      // W4A4 block-scaled GEMMs: x's and a's NVFP4 rows (codes, then scales)
+      (S + (L->shared ? T_max : 0)) * (size_t)(act_cpitch(L->H) + act_spitch(L->H)),  // xg
+      (S + (L->shared ? T_max : 0)) * (size_t)(act_cpitch(L->I) + act_spitch(L->I)),  // aqb
   };
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   // [guard][buffer 0][guard][buffer 1] ... [guard]: moe_debug_check_workspace
@@ -644,7 +676,10 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->ts_x = (float*)ptrs[19];
   L->ts_a = (float*)ptrs[20];
   L->ticket = (int*)ptrs[21];
+  L->xg = (uint8_t*)ptrs[22];
+  L->aqb = (uint8_t*)ptrs[23];
   L->T_max = T_max;
+  make_b_maps(L);
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   for (size_t off : L->guards)
     CK("moe_layer_reserve: guard regions", cudaMemset(static_cast<char*>(ws) + off, kCanary, kGuard));
@@ -950,8 +985,7 @@ int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* id
   CK("moe_forward_routed: copy gates",
      cudaMemcpyAsync(L->gates, gates, S * 4, cudaMemcpyDeviceToDevice, st));
   if (w4a4(L)) {
-    rc = launch_quant_x(L, x, T, st);
-    if (rc) return rc;
+    if (!fq_path(L, T) && (rc = launch_quant_x(L, x, T, st))) return rc;
   } else {
     CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
   }
@@ -1082,7 +1116,7 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
   ExpertParams ep = expert_params(L, x, T);
   const int grid_y = ep.nsh + max_routed_entries(T, L->E, L->k);
   // W4A4: the x quantiser runs with the routing phase, the a quantiser with the down phase
-  if (w4a4(L) && phase == 0 && (rc = launch_quant_x(L, x, T, st))) return rc;
+  if (w4a4(L) && phase == 0 && !fq_path(L, T) && (rc = launch_quant_x(L, x, T, st))) return rc;
   if (w4a4(L) && phase == 3 && (rc = launch_quant_a(L, T, st))) return rc;
   if (small_path(L, T)) {  // router; gate/up (routing inside); down + combine (routing inside)
     if (phase < 0 || phase > 4) return fail(MOE_EINVAL, "moe_debug_run_phase: phase %d", phase);
@@ -1110,9 +1144,11 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       }
       break;
     case 2:
-      if (fq_path(L, T) && (rc = refresh_mma(L, st))) return rc;
+      if (fq_path(L, T) && ((rc = refresh_mma(L, st)) || (rc = launch_quant_x_rows(L, x, T, st))))
+        return rc;
       if (fq_path(L, T))
-        CK("gate/up", launch_tc_fp4_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu_mma, st));
+        CK("gate/up", launch_tc_fp4_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu_mma,
+                                           L->map_bx_c, L->map_bx_s, st));
       else if (tc_path(L, T))
         CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu, st));
       else
@@ -1121,7 +1157,8 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
     case 3:
       if (fq_path(L, T) && (rc = refresh_mma(L, st))) return rc;
       if (fq_path(L, T))
-        CK("down", launch_tc_fp4_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn_mma, st));
+        CK("down", launch_tc_fp4_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn_mma,
+                                      L->map_ba_c, L->map_ba_s, st));
       else if (tc_path(L, T))
         CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn, st));
       else if (fused)

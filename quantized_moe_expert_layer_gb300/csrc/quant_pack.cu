@@ -92,13 +92,19 @@ __global__ void quant_nvfp4_kernel(const float* __restrict__ W, int rows, int K,
 // 8 rows per CTA; lane l takes the 16-column blocks l, l + 32, ...
 // The same arithmetic as quant_nvfp4_kernel (IEEE fp32 divisions, e4m3 and
 // e2m1 round to nearest even), so a row gives the bytes the weight quantiser
-// gives for a one-row matrix.
+// gives for a one-row matrix.  Codes and scales of output row r start at
+// r * cpitch and r * spitch; with `inv`, input row t (a token) goes to the
+// kd output rows inv[t * kd + j] (its expert-sorted slots) and, when
+// shared_base >= 0, to row shared_base + t (its shared-expert row).
 template <bool IN_BF16>
 __global__ void __launch_bounds__(256) quant_act_kernel(const void* __restrict__ in, int rows, int K,
                                                         uint8_t* __restrict__ codes,
                                                         uint8_t* __restrict__ scales,
                                                         uint16_t* __restrict__ out_f16,
-                                                        float* __restrict__ ts_out, int* status) {
+                                                        float* __restrict__ ts_out, int* status,
+                                                        int cpitch, int spitch,
+                                                        const int* __restrict__ inv, int kd,
+                                                        int shared_base) {
   griddep_wait();
   griddep_launch();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -162,9 +168,16 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void* __restrict__
         packed[i / 8] |= q << (4 * (i % 8));
       }
     }
-    const size_t blk = (size_t)row * nb + b;
-    if (codes) reinterpret_cast<uint2*>(codes)[blk] = make_uint2(packed[0], packed[1]);
-    if (scales) scales[blk] = (uint8_t)s;
+    auto put = [&](size_t r) {
+      if (codes) *reinterpret_cast<uint2*>(codes + r * cpitch + 8 * b) = make_uint2(packed[0], packed[1]);
+      if (scales) scales[r * spitch + b] = (uint8_t)s;
+    };
+    if (inv) {
+      for (int j = 0; j < kd; ++j) put((size_t)inv[(size_t)row * kd + j]);
+      if (shared_base >= 0) put((size_t)shared_base + row);
+    } else {
+      put((size_t)row);
+    }
     if (out_f16) {  // e2m1 code x e4m3 scale: both exact in f16, so is the product
       const uint32_t sp = dup_lo(e4m3x2_to_f16x2(s));
       uint32_t h[8];
@@ -562,14 +575,17 @@ cudaError_t launch_quantize_nvfp4(const float* W, int rows, int K, uint8_t* code
 
 cudaError_t launch_quantize_act(const void* in, bool in_bf16, int rows, int K, uint8_t* codes,
                                 uint8_t* scales, uint16_t* out_f16, float* ts, int* status,
-                                bool pdl, cudaStream_t st) {
+                                bool pdl, cudaStream_t st, int cpitch, int spitch, const int* inv,
+                                int kd, int shared_base) {
   if (rows <= 0) return cudaSuccess;
   const dim3 grid((rows + 7) / 8);
+  if (cpitch <= 0) cpitch = K / 2;
+  if (spitch <= 0) spitch = K / 16;
   if (in_bf16)
     return launch_k(quant_act_kernel<true>, grid, dim3(256), 0, st, pdl, in, rows, K, codes, scales,
-                    out_f16, ts, status);
+                    out_f16, ts, status, cpitch, spitch, inv, kd, shared_base);
   return launch_k(quant_act_kernel<false>, grid, dim3(256), 0, st, pdl, in, rows, K, codes, scales,
-                  out_f16, ts, status);
+                  out_f16, ts, status, cpitch, spitch, inv, kd, shared_base);
 }
 
 cudaError_t launch_quantize_fp6(const float* W, int rows, int K, uint8_t* codes, uint8_t* exps,

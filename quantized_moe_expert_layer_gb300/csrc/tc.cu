@@ -625,7 +625,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 // an e4m3 scale per 16 columns, and the products run on tcgen05.mma
 // kind::mxf4nvf4 (scale_vec::4X: four block scales per row and K = 64 step;
 // fp32 accumulators in TMEM).  The weights come from their MMA layout
-// (layout.cuh), so no thread touches them on the way in.
+// (layout.cuh) and the activations from rows in expert-sorted order (x
+// quantised into the rows of its slots after the dispatch; a in slot order),
+// so every operand byte arrives by the Tensor Memory Accelerator.
 //
 // Persistent: one CTA per SM walks the work units u = blockIdx.x,
 // blockIdx.x + gridDim.x, ...; unit u = (work item u / M-blocks: an expert
@@ -635,28 +637,32 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 // unit's loads and MMAs.  Per stage:
 //   * the TMA warp loads the M-block's codes (one 128-byte x 128-row box, 16
 //     contiguous KB of the layout, 128B-swizzled: the K-major layout the MMA
-//     reads) and its block scales (2 KB, one bulk copy);
-//   * warps 0-7 copy the token rows with cp.async, two stages ahead: codes
-//     (128 bytes a row) into the B stage, block scales (4 bytes a row per
-//     K-step) into 512-byte groups;
-//   * one thread each (warps 18 and 19) moves the stage's block scales of A
-//     and of B into tensor memory with tcgen05.cp 32x128b.warpx4 (a 512-byte
-//     group of 32 rows x 16 bytes, row l holding the 4 scales of rows l, l+32,
-//     l+64 and l+96, lands in lanes l of all four lane quadrants, one 32-bit
-//     column per 32-row group) and commits them to the slot's mbarrier: a
-//     copy takes about as long to issue as an MMA, so three threads share the
-//     issuing;
-//   * the MMA thread waits for both and issues the stage's 4 MMAs;
-//   * warps 8-15 read a finished unit's accumulators (the activation scales
+//     reads) and block scales (2 KB, one bulk copy), and the item's 128 token
+//     rows: codes (one 128-byte x 128-row box, 128B-swizzled) and block
+//     scales (16 bytes a row); rows past the item's tokens hold other rows'
+//     values and only reach accumulator columns the epilogue never reads;
+//   * warps 0-3 (a row per thread) move the token rows' scales into the
+//     512-byte groups tcgen05.cp reads (row l of a group: the 4 scales of
+//     rows l, l+32, l+64 and l+96 for one K-step);
+//   * one thread each (warps 14 and 15) moves the stage's block scales of A
+//     and of B into tensor memory with tcgen05.cp 32x128b.warpx4 (a group
+//     lands in lanes l of all four lane quadrants, one 32-bit column per
+//     32-row group) and commits them to the slot's mbarrier: a copy takes
+//     about as long to issue as an MMA, so three threads share the issuing;
+//   * the MMA thread (warp 12) waits for both and issues the stage's 4 MMAs;
+//   * warps 4-11 read a finished unit's accumulators (the activation scales
 //     of their columns loaded before the wait) and hand the buffer back.
-constexpr int kFqThreads = 32 * 20;       // copy 0-7, epilogue 8-15, MMA 16, TMA 17, scale copies 18-19
+constexpr int kFqThreads = 32 * 16;
+constexpr int kFqEpi0 = 4;                // epilogue warps 4-11
+constexpr int kFqMmaWarp = 12, kFqTmaWarp = 13, kFqSfaWarp = 14, kFqSfbWarp = 15;
+static_assert(32 * (kFqSfbWarp + 1) == kFqThreads, "warp roles");
 constexpr int kFqK = 256;                 // K per stage (4 steps of 64)
-constexpr int kFqNS = 6;                  // stages in flight
-constexpr int kFqLB = 3;                  // token-row stages copied ahead
-constexpr int kFqAStage = kTcM * 128;     // 16 KB of codes
-constexpr int kFqBStage = kTcMaxN * 128;  // 16 KB of codes
+constexpr int kFqNS = 5;                  // stages in flight
+constexpr int kFqList = 128;              // units a CTA keeps in its list
+constexpr int kFqAStage = kTcM * 128;     // 16 KB of weight codes
+constexpr int kFqBStage = kTcMaxN * 128;  // 16 KB of token-row codes
 constexpr int kFqSf = 4 * 512;            // block scales of a stage: 4 K-steps x 128 rows x 4
-constexpr int kFqStage = kFqAStage + kFqBStage + 2 * kFqSf;
+constexpr int kFqStage = kFqAStage + kFqBStage + 3 * kFqSf;  // + A scales, B scales, B scales as loaded
 // TMEM columns: two accumulators of 128, then 16 columns of A scales and 16
 // of B scales per stage slot
 constexpr uint32_t kFqSfaCol = 256;
@@ -664,11 +670,12 @@ constexpr uint32_t kFqSfbCol = kFqSfaCol + 16 * kFqNS;
 static_assert(kFqSfbCol + 16 * kFqNS <= 512, "tensor memory columns");
 
 struct FqShared {
-  uint64_t full_a[kFqNS];  // the TMA's codes and scales of the slot (transaction bytes)
-  uint64_t full_b[kFqNS];  // the 8 copy warps' token rows of the slot
-  uint64_t sfa[kFqNS];     // the slot's A scales are in tensor memory
-  uint64_t sfb[kFqNS];     // the slot's B scales are in tensor memory
-  uint64_t empty[kFqNS];   // the MMAs reading the slot are done
+  uint64_t full_a[kFqNS];   // weight codes and scales of the slot (transaction bytes)
+  uint64_t full_bt[kFqNS];  // token-row codes and scales of the slot (transaction bytes)
+  uint64_t full_b[kFqNS];   // the token rows' scales regrouped (4 warp arrivals)
+  uint64_t sfa[kFqNS];      // the slot's A scales are in tensor memory
+  uint64_t sfb[kFqNS];      // the slot's B scales are in tensor memory
+  uint64_t empty[kFqNS];    // the MMAs reading the slot are done
   uint64_t acc_full[2], acc_empty[2];
   uint64_t fin, fin2[2];
   uint32_t tmem_base;
@@ -676,7 +683,7 @@ struct FqShared {
 };
 
 __host__ __device__ constexpr size_t fq_smem_bytes() {
-  return 1024 + (size_t)kFqNS * kFqStage + sizeof(FqShared);
+  return 1024 + (size_t)kFqNS * kFqStage + sizeof(FqShared) + 16 + 16 * kFqList;  // + the unit list
 }
 
 // Instruction descriptor of kind::mxf4nvf4: A and B e2m1 (format 1), both
@@ -714,13 +721,6 @@ __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
                : "memory");
 }
 
-// byte of the block scale (row r, K-step kk of the stage, block b of the step) in a staging area
-__device__ __forceinline__ uint32_t sf_off(int r, int kk, int b) {
-  return (uint32_t)(kk * 512 + (r & 31) * 16 + (r >> 5) * 4 + b);
-}
-
-// L2 policies: the weights stream through once (evict first), the token rows
-// are read once per M-block (evict last)
 __device__ __forceinline__ uint64_t l2_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -752,42 +752,53 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// cp.async of 16 (or 4) bytes with an L2 policy
-__device__ __forceinline__ void cp_async16_pol(uint32_t saddr, const void* g, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "l"(pol)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4_pol(uint32_t saddr, const void* g, uint64_t pol) {
-  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2;" ::"r"(saddr), "l"(g), "l"(pol)
-               : "memory");
+// 2-D tiled TMA load of the box at (x, row y) of an activation-row map, counted on `bar`
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                              uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
 }
 
 struct FqUnit {
   int expert, row0, n, mb;
 };
 
-// The first valid unit at or after u among u, u + gridDim.x, ... (< n_units);
-// n_units when there is none.  Every role of the CTA walks the same sequence.
-__device__ __forceinline__ int fq_next(const ExpertParams& p, int u, int n_units, int mblocks,
-                                       FqUnit& w) {
-  for (; u < n_units; u += gridDim.x) {
-    if (tc_entry(p, u / mblocks, w.expert, w.row0, w.n)) {
-      w.mb = u % mblocks;
-      return u;
-    }
+// Unit i of this CTA (u = blockIdx.x + i * gridDim.x): false past the last.
+// The first kFqList come from the CTA's list in shared memory (filled at the
+// start), later ones are read from the work entries.  A unit whose entry
+// fails its bounds check gets n = 0 (every role skips it).
+__device__ __forceinline__ bool fq_unit(const ExpertParams& p, const int4* list, int i, int n_units,
+                                        int mblocks, FqUnit& w) {
+  const int u = blockIdx.x + i * gridDim.x;
+  if (u >= n_units) return false;
+  if (i < kFqList) {
+    const int4 v = list[i];
+    w.expert = v.x;
+    w.row0 = v.y;
+    w.n = v.z;
+    w.mb = v.w;
+    return true;
   }
-  return n_units;
+  if (!tc_entry(p, u / mblocks, w.expert, w.row0, w.n)) w.n = 0;
+  w.mb = u % mblocks;
+  return true;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kFqThreads, 1)
-    tc_fp4_kernel(ExpertParams p, const __grid_constant__ CUtensorMap tmap, int max_items) {
+    tc_fp4_kernel(ExpertParams p, const __grid_constant__ CUtensorMap tmap,
+                  const __grid_constant__ CUtensorMap bmap_c, const __grid_constant__ CUtensorMap bmap_s,
+                  int max_items) {
   griddep_wait();
   extern __shared__ __align__(1024) uint8_t fq_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(fq_smem_raw) + 1023) & ~(uintptr_t)1023);
-  // per stage slot: A codes (16 KB), B codes (16 KB), A scales (2 KB), B scales (2 KB)
+  // per stage slot: A codes (16 KB), B codes (16 KB), A scales, B scales, B scales as loaded (2 KB each)
   FqShared* sh = reinterpret_cast<FqShared*>(base + kFqNS * kFqStage);
+  int4* list = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(sh + 1) + 15) & ~(uintptr_t)15);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.T * p.k;
   const int K = MODE == 1 ? p.I : p.H;
@@ -800,11 +811,13 @@ __global__ void __launch_bounds__(kFqThreads, 1)
   auto b_addr = [&](int slot) { return s0 + slot * kFqStage + kFqAStage; };
   auto sa_addr = [&](int slot) { return s0 + slot * kFqStage + kFqAStage + kFqBStage; };
   auto sb_addr = [&](int slot) { return sa_addr(slot) + kFqSf; };
+  auto sn_addr = [&](int slot) { return sa_addr(slot) + 2 * kFqSf; };
 
   if (tid == 0) {
     for (int i = 0; i < kFqNS; ++i) {
       mbar_init(&sh->full_a[i], 1);
-      mbar_init(&sh->full_b[i], 8);
+      mbar_init(&sh->full_bt[i], 1);
+      mbar_init(&sh->full_b[i], 4);
       mbar_init(&sh->sfa[i], 1);
       mbar_init(&sh->sfb[i], 1);
       mbar_init(&sh->empty[i], 1);
@@ -819,94 +832,72 @@ __global__ void __launch_bounds__(kFqThreads, 1)
     sh->abort = 0;
     mbar_init_fence();
   }
-  // B codes and scales start zero: rows past a unit's tokens are only ever written with zeros
-  for (int i = tid; i < kFqNS * (kFqBStage + 2 * kFqSf) / 16; i += kFqThreads) {
-    const int slot = i / ((kFqBStage + 2 * kFqSf) / 16), o = i % ((kFqBStage + 2 * kFqSf) / 16);
-    st_shared_v4(b_addr(slot) + 16 * o, 0, 0, 0, 0);  // (B codes, then the A and B scale groups)
+  if (warp == 0) {  // the unit list: {expert, first row, tokens, M-block}
+    for (int i = lane; i < kFqList; i += 32) {
+      const int u = blockIdx.x + i * gridDim.x;
+      int4 v = make_int4(0, 0, 0, 0);
+      if (u < n_units) {
+        int e, r0, n;
+        v = tc_entry(p, u / mblocks, e, r0, n) ? make_int4(e, r0, n, u % mblocks)
+                                               : make_int4(0, 0, 0, u % mblocks);
+      }
+      list[i] = v;
+    }
   }
-  fence_async_smem();  // (the zeros, for the MMAs and scale copies)
-  if (warp == kTxPW) tmem_alloc(&sh->tmem_base, 512);
+  if (warp == kFqMmaWarp) tmem_alloc(&sh->tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_d = sh->tmem_base;
   volatile int* abort = &sh->abort;
-  // row of x (MODE 0: the token) or of a (MODE 1) behind column r of a unit
-  auto b_row = [&](const FqUnit& w, int r) -> size_t {
-    if (MODE == 1) return (size_t)(w.row0 + r);
-    return (size_t)(w.expert == p.E ? w.row0 - S + r : p.row_token[w.row0 + r]);
-  };
 
-  if (warp < 8) {
-    // ---------------------------------------------------------------- token rows, kFqLB stages ahead
-    const uint8_t* bcodes = MODE == 0 ? p.xq : p.aq;
-    const uint8_t* bscales = MODE == 0 ? p.xqs : p.aqs;
-    // thread tid takes row tid / 2 of a unit (`row`: its row of x or a,
-    // loaded once per unit), half tid % 2 of its code pieces and scale words;
-    // rows past the unit's tokens that held an earlier, longer unit's get zeros
-    const int br = tid >> 1, bh = tid & 1;
-    const uint64_t pol = l2_evict_last();
-    int bn[kFqNS] = {};  // tokens each slot's B rows last held (the same in every copier thread)
-    FqUnit w;
-    int u = fq_next(p, blockIdx.x, n_units, mblocks, w), s = 0;
-    size_t row = (u < n_units && br < w.n) ? b_row(w, br) : 0;
-    int issued = 0, done = 0;
+  if (warp < kFqEpi0) {
+    // ---------------------------------------------------------------- token-row scales into groups
+    const int r = tid;  // row of the stage (0..127)
+    int gs = 0;
+    FqUnit cur;
     bool ok = true;
-    auto issue_next = [&]() {  // the next stage of the unit sequence into its slot
-      if (ok && u < n_units) {
-        const int slot = issued % kFqNS;
-        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->empty[slot], ((issued / kFqNS) & 1) ^ 1,
-                                                     abort, p.wait_budget))) {
+    for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+      if (cur.n == 0) continue;
+      for (int s = 0; s < KS; ++s, ++gs) {
+        const int slot = gs % kFqNS;
+        // (sleeping waits: the spinning MMA and TMA threads share these warps' schedulers)
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->full_bt[slot], (gs / kFqNS) & 1, abort,
+                                                     p.wait_budget))) {
           ok = false;
-        } else {
-          const int nsub = min(4, KC - 4 * s);
-          const uint32_t bs = b_addr(slot), fs = sb_addr(slot);
-          if (br < w.n) {
-            for (int pc = bh * nsub; pc < (bh + 1) * nsub; ++pc)  // 16-byte code pieces
-              cp_async16_pol(bs + swz(br, pc), bcodes + row * (K / 2) + 128 * s + 16 * pc, pol);
-            for (int kk = 2 * bh; kk < min(2 * bh + 2, nsub); ++kk)  // 4 scales per K-step
-              cp_async4_pol(fs + sf_off(br, kk, 0), bscales + row * (K / 16) + 16 * s + 4 * kk, pol);
-          } else if (br < bn[slot]) {
-            for (int pc = 4 * bh; pc < 4 * bh + 4; ++pc) st_shared_v4(bs + swz(br, pc), 0, 0, 0, 0);
-            for (int kk = 2 * bh; kk < 2 * bh + 2; ++kk) st_shared_u32(fs + sf_off(br, kk, 0), 0u);
-          }
-          bn[slot] = w.n;
-          ++issued;
-          if (++s == KS) {
-            s = 0;
-            u = fq_next(p, u + gridDim.x, n_units, mblocks, w);
-            if (u < n_units && br < w.n) row = b_row(w, br);
-          }
+          break;
         }
+        const uint4 w4 = lds128(sn_addr(slot) + 16 * r);  // the row's scales of K-steps 0..3
+        const uint32_t g = sb_addr(slot) + (r & 31) * 16 + (r >> 5) * 4;
+        st_shared_u32(g, w4.x);
+        st_shared_u32(g + 512, w4.y);
+        st_shared_u32(g + 1024, w4.z);
+        st_shared_u32(g + 1536, w4.w);
+        fence_async_smem();  // (for tcgen05.cp)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->full_b[slot]);
       }
-      cp_async_commit();
-    };
-    for (int i = 0; i < kFqLB; ++i) issue_next();
-    while (ok && done < issued) {
-      issue_next();
-      cp_async_wait<kFqLB>();  // this thread's copies of stage `done` have landed
-      fence_async_smem();      // (for the async proxy)
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->full_b[done % kFqNS]);
-      ++done;
     }
-    cp_async_wait<0>();
-  } else if (warp < kTxPW) {
+  } else if (warp < kFqMmaWarp) {
     // ---------------------------------------------------------------- epilogue
-    // warp 8 + 4h + q: TMEM lane quadrant q (rows 32q..32q+31), columns 64h..64h+63
-    const int qd = warp & 3, ch = (warp - 8) >> 2;
+    // warp 4 + 4h + q: TMEM lane quadrant q (rows 32q..32q+31), columns 64h..64h+63
+    const int qd = warp & 3, ch = (warp - kFqEpi0) >> 2;
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    // row of x (MODE 0: the token) behind column r of a unit
+    auto tok = [&](const FqUnit& w, int r) -> size_t {
+      return (size_t)(w.expert == p.E ? w.row0 - S + r : p.row_token[w.row0 + r]);
+    };
     FqUnit cur;
     int uk = 0;
-    for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units;
-         u = fq_next(p, u + gridDim.x, n_units, mblocks, cur), ++uk) {
+    for (int i = 0; fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+      if (cur.n == 0) continue;
       const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
       float sc_lane[2] = {1.0f, 1.0f};  // W4A4 scales of columns 64h + 32c + lane
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int col = 64 * ch + 32 * c + lane;
         if (col < cur.n) {
-          if (MODE == 0 && p.ts_x) sc_lane[c] = p.ts_x[b_row(cur, col)];
+          if (MODE == 0 && p.ts_x) sc_lane[c] = p.ts_x[tok(cur, col)];
           if (MODE == 1 && p.ts_a) sc_lane[c] = p.ts_a[cur.row0 + col];
         }
       }
@@ -956,27 +947,28 @@ __global__ void __launch_bounds__(kFqThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
+      ++uk;
     }
-  } else if (warp == kTxPW) {
+  } else if (warp == kFqMmaWarp) {
     if (lane == 0) {
-      // ---------------------------------------------------------------- scale copies and MMA issue
+      // ---------------------------------------------------------------- MMA issue
       FqUnit cur;
       int gs = 0, uk = 0;
       bool ok = true;
-      for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units && ok;
-           u = fq_next(p, u + gridDim.x, n_units, mblocks, cur), ++uk) {
+      for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+        if (cur.n == 0) continue;
         const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
         const uint32_t idesc = idesc_mxf4nvf4(kTcM, n_pad);
         // the epilogue of the unit before the previous one has read this accumulator
-        if (!mbar_wait(&sh->acc_empty[buf], ((uk >> 1) & 1) ^ 1, abort, p.wait_budget)) break;
+        if (!mbar_wait_fast(&sh->acc_empty[buf], ((uk >> 1) & 1) ^ 1, abort, p.wait_budget)) break;
         tc_fence_after();
         for (int s = 0; s < KS; ++s, ++gs) {
           const int nsub = min(4, KC - 4 * s), slot = gs % kFqNS, ph = (gs / kFqNS) & 1;
-          // the codes and token rows (already in when the scales are), and the scales
-          if (!mbar_wait(&sh->sfa[slot], ph, abort, p.wait_budget) ||
-              !mbar_wait(&sh->sfb[slot], ph, abort, p.wait_budget) ||
-              !mbar_wait(&sh->full_a[slot], ph, abort, p.wait_budget) ||
-              !mbar_wait(&sh->full_b[slot], ph, abort, p.wait_budget)) {
+          // the scales in tensor memory: their threads committed them after
+          // observing the operands' barriers (weight codes, token rows), so
+          // the operands are in too (release / acquire through the commits)
+          if (!mbar_wait_fast(&sh->sfa[slot], ph, abort, p.wait_budget) ||
+              !mbar_wait_fast(&sh->sfb[slot], ph, abort, p.wait_budget)) {
             ok = false;
             break;
           }
@@ -989,23 +981,60 @@ __global__ void __launch_bounds__(kFqThreads, 1)
           umma_commit(&sh->empty[slot]);
         }
         if (ok) umma_commit(&sh->acc_full[buf]);
+        ++uk;
       }
-      umma_commit(&sh->fin);  // every copy and MMA issued before TMEM is freed
+      umma_commit(&sh->fin);  // every MMA issued before TMEM is freed
       mbar_drain(&sh->fin, 0);
     }
     __syncwarp();
-  } else if (warp >= kTxPW + 2) {
+  } else if (warp == kFqTmaWarp) {
     if (lane == 0) {
-      // ---------------------------------------------------------------- scale copies (A: warp 18, B: 19)
-      const bool is_a = warp == kTxPW + 2;
+      // ---------------------------------------------------------------- TMA issue
+      const CUtensorMap* map = &tmap;
+      const uint64_t sc_off = MODE == 1 ? p.mma_dn_sc : p.mma_gu_sc;
+      const uint64_t wpol = l2_evict_first(), apol = l2_evict_last();
+      int issued = 0;  // stages issued
+      FqUnit cur;
+      bool ok = true;
+      for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+        if (cur.n == 0) continue;
+        const uint8_t* scales = p.mma + (size_t)cur.expert * p.mma_expert_bytes + sc_off;
+        for (int s = 0; s < KS; ++s) {
+          const int slot = issued % kFqNS;
+          if (!mbar_wait(&sh->empty[slot], ((issued / kFqNS) & 1) ^ 1, abort, p.wait_budget)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect(&sh->full_a[slot], (uint32_t)(kFqAStage + kFqSf));
+          tma_load_codes(a_addr(slot), map, kTcM * cur.mb, s, cur.expert, &sh->full_a[slot], wpol);
+          bulk_load(sa_addr(slot), scales + ((size_t)s * mblocks + cur.mb) * kFqSf, (uint32_t)kFqSf,
+                    &sh->full_a[slot], wpol);
+          mbar_arrive_expect(&sh->full_bt[slot], (uint32_t)(kFqBStage + kFqSf));
+          tma_load_rows(b_addr(slot), &bmap_c, 16 * s, cur.row0, &sh->full_bt[slot], apol);
+          tma_load_rows(sn_addr(slot), &bmap_s, 2 * s, cur.row0, &sh->full_bt[slot], apol);
+          ++issued;
+        }
+      }
+      if (*abort) {  // let the copies in flight land before the CTA exits (bounded waits)
+        for (int c = (issued > kFqNS ? issued - kFqNS : 0); c < issued; ++c) {
+          mbar_drain(&sh->full_a[c % kFqNS], (c / kFqNS) & 1);
+          mbar_drain(&sh->full_bt[c % kFqNS], (c / kFqNS) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- scale copies (A: warp 14, B: 15)
+      const bool is_a = warp == kFqSfaWarp;
       FqUnit cur;
       int gs = 0;
       bool ok = true;
-      for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units && ok;
-           u = fq_next(p, u + gridDim.x, n_units, mblocks, cur)) {
+      for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+        if (cur.n == 0) continue;
         for (int s = 0; s < KS; ++s, ++gs) {
           const int nsub = min(4, KC - 4 * s), slot = gs % kFqNS, ph = (gs / kFqNS) & 1;
-          if (!mbar_wait(is_a ? &sh->full_a[slot] : &sh->full_b[slot], ph, abort, p.wait_budget)) {
+          if (!mbar_wait_sleep(is_a ? &sh->full_a[slot] : &sh->full_b[slot], ph, abort, p.wait_budget)) {
             ok = false;
             break;
           }
@@ -1020,43 +1049,12 @@ __global__ void __launch_bounds__(kFqThreads, 1)
       mbar_drain(&sh->fin2[is_a ? 0 : 1], 0);
     }
     __syncwarp();
-  } else {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- TMA issue
-      const CUtensorMap* map = &tmap;
-      const uint64_t sc_off = MODE == 1 ? p.mma_dn_sc : p.mma_gu_sc;
-      const uint64_t pol = l2_evict_first();
-      int issued = 0;  // stages issued
-      FqUnit cur;
-      bool ok = true;
-      for (int u = fq_next(p, blockIdx.x, n_units, mblocks, cur); u < n_units && ok;
-           u = fq_next(p, u + gridDim.x, n_units, mblocks, cur)) {
-        const uint8_t* scales = p.mma + (size_t)cur.expert * p.mma_expert_bytes + sc_off;
-        for (int s = 0; s < KS; ++s) {
-          const int slot = issued % kFqNS;
-          if (!mbar_wait(&sh->empty[slot], ((issued / kFqNS) & 1) ^ 1, abort, p.wait_budget)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect(&sh->full_a[slot], (uint32_t)(kFqAStage + kFqSf));
-          tma_load_codes(a_addr(slot), map, kTcM * cur.mb, s, cur.expert, &sh->full_a[slot], pol);
-          bulk_load(sa_addr(slot), scales + ((size_t)s * mblocks + cur.mb) * kFqSf, (uint32_t)kFqSf,
-                    &sh->full_a[slot], pol);
-          ++issued;
-        }
-      }
-      if (*abort) {  // let the copies in flight land before the CTA exits (bounded waits)
-        for (int c = (issued > kFqNS ? issued - kFqNS : 0); c < issued; ++c)
-          mbar_drain(&sh->full_a[c % kFqNS], (c / kFqNS) & 1);
-      }
-    }
-    __syncwarp();
   }
 
   if (*abort && tid == 0) *p.status = kStatusTimeout;
   tc_fence_before();
   __syncthreads();
-  if (warp == kTxPW) {
+  if (warp == kFqMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_d, 512);
   }
@@ -1119,6 +1117,32 @@ cudaError_t tc_make_mma_map(void* map, const uint8_t* codes, int n_experts, int 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// [rows][row_bytes] activation rows; a box: 128 rows of 128 bytes (codes,
+// 128B-swizzled) or of 16 bytes (scales, as they are)
+cudaError_t tc_make_rows_map(void* map, const uint8_t* base, size_t rows, int row_bytes, bool codes) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // (8-byte elements: 16 to a 128-byte box row, 2 to a 16-byte one)
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes / 8, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {codes ? 16u : 2u, (cuuint32_t)kTcMaxN};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
+                            const_cast<uint8_t*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            codes ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool tc_path_ok(int fmt, int T, int k, int E, int H, int I) {
   // NVFP4 only; enough tokens per expert for a dense contraction; tile shapes
   return fmt == FMT_NVFP4 && (long)T * k >= 16L * E && H % kTcM == 0 && (2 * I) % kTcM == 0 &&
@@ -1163,19 +1187,23 @@ static int fq_grid(int units) {
 }
 
 cudaError_t launch_tc_fp4_gateup(const ExpertParams& p, int items, const void* tile_map,
-                                 cudaStream_t st) {
+                                 const void* bmap_c, const void* bmap_s, cudaStream_t st) {
   const int mblocks = (2 * p.I) / kTcM;
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  const CUtensorMap& bc = *reinterpret_cast<const CUtensorMap*>(bmap_c);
+  const CUtensorMap& bs = *reinterpret_cast<const CUtensorMap*>(bmap_s);
   return launch_k(tc_fp4_kernel<0>, dim3(fq_grid(mblocks * items)), dim3(kFqThreads),
-                  fq_smem_bytes(), st, true, p, map, items);
+                  fq_smem_bytes(), st, true, p, map, bc, bs, items);
 }
 
 cudaError_t launch_tc_fp4_down(const ExpertParams& p, int items, const void* tile_map,
-                               cudaStream_t st) {
+                               const void* bmap_c, const void* bmap_s, cudaStream_t st) {
   const int mblocks = p.H / kTcM;
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  const CUtensorMap& bc = *reinterpret_cast<const CUtensorMap*>(bmap_c);
+  const CUtensorMap& bs = *reinterpret_cast<const CUtensorMap*>(bmap_s);
   return launch_k(tc_fp4_kernel<1>, dim3(fq_grid(mblocks * items)), dim3(kFqThreads),
-                  fq_smem_bytes(), st, true, p, map, items);
+                  fq_smem_bytes(), st, true, p, map, bc, bs, items);
 }
 
 bool tc_router_ok(int E, int H) { return E % kTcM == 0 && H % kTcK == 0; }

@@ -88,7 +88,10 @@ __global__ void __launch_bounds__(512) topk_dispatch_kernel(RouteParams p) {
   __syncthreads();
   if (!last) return;
   __threadfence();  // every other CTA's picks, after the last ticket
-  dispatch_block(p, sc + 64, sc);
+  if (p.T <= 64)  // (the top-k's picks of a token are distinct)
+    dispatch_block_t64(p, reinterpret_cast<unsigned long long*>(sc + 64), sc);
+  else
+    dispatch_block(p, sc + 64, sc);
   if (threadIdx.x == 0) *p.ticket = 0;
 }
 

@@ -443,7 +443,40 @@ __device__ void dispatch_block(const RouteParams& p, int* hist, int* sc) {
   write_entries(p, c, excl, sc);
 }
 
-// slots of the few-token path (T * k at most)
+// Dispatch of T <= 64 tokens whose k picks are distinct (the top-k's), by
+// one CTA with a thread per expert: expert e's rows are its tokens in
+// ascending order (its slots in slot order), so slot (t, j) of expert e lands
+// at offsets[e] + (tokens below t in e's 64-bit token mask).  The rows come
+// out the same as dispatch_block's.  Ends synchronised.
+__device__ void dispatch_block_t64(const RouteParams& p, unsigned long long* mask, int* sc) {
+  const int E = p.E, k = p.k, S = p.T * k, tid = threadIdx.x;
+  int* off = reinterpret_cast<int*>(mask + E);
+  for (int e = tid; e < E; e += blockDim.x) mask[e] = 0ull;
+  __syncthreads();
+  for (int s = tid; s < S; s += blockDim.x)
+    atomicOr(&mask[checked_expert(p, p.idx[s])], 1ull << (s / k));
+  __syncthreads();
+  const int c = tid < E ? __popcll(mask[tid]) : 0;
+  int total;
+  const int excl = block_excl_scan(c, sc, &total);
+  if (tid < E) {
+    p.counts[tid] = c;
+    p.offsets[tid] = excl;
+    off[tid] = excl;
+  }
+  if (tid == 0) p.offsets[E] = total;
+  __syncthreads();
+  for (int s = tid; s < S; s += blockDim.x) {
+    const int e = checked_expert(p, p.idx[s]), t = s / k;
+    const int pos = off[e] + __popcll(mask[e] & ((1ull << t) - 1ull));
+    p.perm[pos] = s;
+    p.inv[s] = pos;
+    p.row_token[pos] = t;
+  }
+  write_entries(p, c, excl, sc);
+}
+
+// slots of the few-token path (T * k at most)// slots of the few-token path (T * k at most)
 constexpr int kSmallSlots = 256;
 
 // ---------------------------------------------------------------- routing of a few tokens by one CTA

@@ -581,7 +581,8 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
                     "note": "bytes read from the pinned host mirror over the CPU-GPU link"}
         peak_kind = "measured here: 256 MiB pinned host -> device copy, best of 10"
     roofline.update({"traffic": None if host_per_launch else traffic_from_profile(
-                         kname.split("<")[0], w.name, os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
+                         kname.split("<")[0], w.name + ("-w4a4" if act else ""),
+                         os.path.join(ROOT, "quantized_moe_expert_layer_gb300", "csrc")),
                      "avg_launch_us": k_us, "peak_source": peak_kind,
                      "timing": "CUDA events over a graph of back-to-back launches, gaps included"})
     res["roofline"] = roofline

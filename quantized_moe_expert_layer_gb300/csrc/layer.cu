@@ -117,6 +117,16 @@ struct moe_layer {
   alignas(64) unsigned char map_gu[128] = {};
   alignas(64) unsigned char map_dn[128] = {};
   bool maps_ok = false;
+  // the same with a box of one M-block (8 tiles), and the maps of the f16
+  // token rows in slot order (x gathered into the y buffer, which the down
+  // GEMM writes only after gate/up; the rows of a) for the W4A16 GEMMs with
+  // the weights in tensor memory
+  alignas(64) unsigned char map_gu8[128] = {};
+  alignas(64) unsigned char map_dn8[128] = {};
+  alignas(64) unsigned char map_xs[128] = {};
+  alignas(64) unsigned char map_ab[128] = {};
+  bool tm_maps_ok = false;
+  bool rows_maps_ok = false;
   // W4A4 on the tensor-core path: the packed tiles again in the MMA layout
   // (layout.cuh), rebuilt from the arena before the first forward after any
   // change to it, and the TMA maps of its code regions
@@ -204,6 +214,12 @@ void make_tile_maps(moe_layer* L) {
                        8 * tc_group(gu_tiles / 8)) == cudaSuccess &&
       tc_make_tile_map(L->map_dn, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
                        g.expert_bytes, 8 * tc_group(dn_tiles / 8)) == cudaSuccess;
+  L->tm_maps_ok =
+      L->maps_ok &&
+      tc_make_tile_map(L->map_gu8, L->arena, n_total, gu_tiles, g.gu.tile_bytes, g.expert_bytes, 8) ==
+          cudaSuccess &&
+      tc_make_tile_map(L->map_dn8, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
+                       g.expert_bytes, 8) == cudaSuccess;
   make_mma_maps(L);
 }
 
@@ -231,6 +247,14 @@ void make_mma_maps(moe_layer* L) {
 int act_cpitch(int K) { return (K / 2 + 127) / 128 * 128; }
 int act_spitch(int K) { return (K / 16 + 15) / 16 * 16; }
 size_t act_rows_cap(const moe_layer* L) { return (size_t)L->T_max * L->k + (L->shared ? L->T_max : 0); }
+
+uint16_t* xs_rows(const moe_layer* L) { return reinterpret_cast<uint16_t*>(L->ybuf); }
+
+void make_rows_maps(moe_layer* L) {
+  L->rows_maps_ok = L->ybuf && L->abuf &&
+                    tc_make_rows16_map(L->map_xs, xs_rows(L), act_rows_cap(L), L->H) == cudaSuccess &&
+                    tc_make_rows16_map(L->map_ab, L->abuf, act_rows_cap(L), L->I) == cudaSuccess;
+}
 
 void make_b_maps(moe_layer* L) {
   L->bmaps_ok = false;
@@ -386,6 +410,19 @@ bool fq_path(moe_layer* L, int T) {
   return w4a4(L) && tc_path(L, T) && L->mma_maps_ok && L->bmaps_ok;
 }
 
+// the tensor-core path's f16 GEMMs with the weights in tensor memory (W4A16:
+// W4A4 keeps a in fp32 in the y buffer, where these read x's rows)
+bool tm_path(moe_layer* L, int T) {
+  return !w4a4(L) && tc_path(L, T) && L->tm_maps_ok && L->rows_maps_ok;
+}
+
+int launch_tm_gateup(moe_layer* L, const ExpertParams& ep, int T, cudaStream_t st) {
+  const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
+  CK("row gather kernel launch", launch_gather_rows(ep, T * L->k + (L->shared ? T : 0), xs_rows(L), st));
+  CK("tensor-core gate/up kernel launch", launch_tc_tm_gateup(ep, gy, L->map_gu8, L->map_xs, st));
+  return MOE_OK;
+}
+
 // top-k then dispatch: one fused launch where it applies, else two (or three)
 int launch_topk_and_dispatch(moe_layer* L, const RouteParams& rp, int T, bool pdl, cudaStream_t st) {
   if (topk_dispatch_ok(T, L->k, L->E)) {
@@ -460,9 +497,17 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   }
   if (tc_path(L, T)) {
     const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
-    CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, L->map_gu, st));
+    if (tm_path(L, T)) {
+      const int rc = launch_tm_gateup(L, ep, T, st);
+      if (rc) return rc;
+    } else {
+      CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, L->map_gu, st));
+    }
     if (w4a4(L) && launch_quant_a(L, T, st)) return MOE_ECUDA;
-    CK("tensor-core down kernel launch", launch_tc_down(ep, gy, L->map_dn, st));
+    if (tm_path(L, T))
+      CK("tensor-core down kernel launch", launch_tc_tm_down(ep, gy, L->map_dn8, L->map_ab, st));
+    else
+      CK("tensor-core down kernel launch", launch_tc_down(ep, gy, L->map_dn, st));
     CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
     return MOE_OK;
   }
@@ -492,7 +537,7 @@ int forward_launches(moe_layer* L, int T) {
   // top-k + dispatch: one kernel (T <= 16, or the fused one), else top-k then dispatch
   const int topk_disp = topk_dispatch_ok(T, L->k, L->E) ? 1 : 1 + dispatch;
   const int routing = tc_router(L, T) ? 2 + topk_disp : (T <= kFusedTopkMaxT ? 2 : 1 + topk_disp);
-  if (tc_path(L, T)) return routing + 3 + q;
+  if (tc_path(L, T)) return routing + 3 + q + (tm_path(L, T) ? 1 : 0);  // (+ the row gather)
   return routing + (fused_down(L, T) ? 2 : 3) + q;
 }
 
@@ -680,6 +725,7 @@ int moe_layer_reserve(moe_layer* L, int T_max) {
   L->aqb = (uint8_t*)ptrs[23];
   L->T_max = T_max;
   make_b_maps(L);
+  make_rows_maps(L);
   CK("moe_layer_reserve: clear workspace", cudaMemset(ws, 0, total));
   for (size_t off : L->guards)
     CK("moe_layer_reserve: guard regions", cudaMemset(static_cast<char*>(ws) + off, kCanary, kGuard));
@@ -1149,6 +1195,9 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       if (fq_path(L, T))
         CK("gate/up", launch_tc_fp4_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu_mma,
                                            L->map_bx_c, L->map_bx_s, st));
+      else if (tm_path(L, T)) {
+        if ((rc = launch_tm_gateup(L, ep, T, st))) return rc;
+      }
       else if (tc_path(L, T))
         CK("gate/up", launch_tc_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu, st));
       else
@@ -1159,6 +1208,9 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       if (fq_path(L, T))
         CK("down", launch_tc_fp4_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn_mma,
                                       L->map_ba_c, L->map_ba_s, st));
+      else if (tm_path(L, T))
+        CK("down", launch_tc_tm_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn8,
+                                     L->map_ab, st));
       else if (tc_path(L, T))
         CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn, st));
       else if (fused)

@@ -1060,6 +1060,383 @@ __global__ void __launch_bounds__(kFqThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- W4A16: the weights in tensor memory
+// The expert GEMMs of the W4A16 prefill (f16 activations) with the
+// dequantised weights kept in tensor memory: producer warps write each weight
+// row's f16 values (e2m1 code x e4m3 block scale, exact in f16) with
+// tcgen05.st, and the MMA takes A from there (tcgen05.mma kind::f16 [d], [a],
+// b_desc), so only the token rows pass through shared memory.
+//
+// Persistent like tc_fp4_kernel: a CTA per SM walks units (work item, 128-row
+// M-block), its unit list in shared memory; a ring of kTmNS stages of 64
+// columns of K (each with its own 32-column A slot in TMEM) runs across units,
+// and the accumulators are double-buffered.  Per stage:
+//   * one of two TMA warps (even and odd stages: a single issuing thread
+//     keeps too few copies in flight) loads the M-block's code vectors of the
+//     chunk (one box of the arena's tile map: the same 512-byte piece of 8
+//     consecutive 16-row tiles, 4 KB), at the first chunk of a super-chunk
+//     also the tiles' scale vectors, and the chunk's 64 columns of the item's
+//     128 token rows (one 16 KB box, 128B-swizzled: the K-major layout the MMA
+//     reads) from rows in slot order: x gathered into them by
+//     gather_rows_kernel (gate/up), or a (down); rows past the item's tokens
+//     belong to other items and only reach accumulator columns the epilogue
+//     never reads;
+//   * producer warps 0-7 (warp w: TMEM lane quadrant w % 4, columns 32(w / 4)
+//     .. +31 of the chunk) rebuild their row's codes from the tile's fragment
+//     order (one byte permute per 8 codes), convert and scale them to f16 and
+//     store 16 TMEM columns, then arrive once per warp;
+//   * the MMA thread (warp 16) issues the stage's 4 MMAs (K = 16 each) and
+//     commits the stage (its shared memory and its A slot) back;
+//   * epilogue warps 8-15 read a finished unit's accumulators (SwiGLU into a,
+//     or y rows) and hand the buffer back.
+constexpr int kTmThreads = 32 * 19;
+constexpr int kTmEpi0 = 8;                     // epilogue warps 8-15
+constexpr int kTmMmaWarp = 16, kTmTmaWarp = 17;  // TMA warps 17 (even stages) and 18 (odd)
+static_assert(32 * (kTmTmaWarp + 2) == kTmThreads, "warp roles");
+constexpr int kTmNS = 8;                       // stages in flight (and A slots)
+constexpr int kTmB = kTcMaxN * 128;            // token rows of a stage: 128 x 64 f16
+constexpr int kTmCodes = 8 * 512;              // one 512-byte piece of 8 tiles
+constexpr int kTmStage = kTmB + 2 * kTmCodes;  // token rows, code vectors, scale vectors
+constexpr uint32_t kTmACol = 256;              // A slots (32 columns each) after two accumulators
+static_assert(kTmACol + 32 * kTmNS <= 512, "tensor memory columns");
+static_assert(kTmStage % 1024 == 0, "stages stay 1024-byte aligned");
+
+struct TmShared {
+  uint64_t full[kTmNS];   // the stage's codes (+ scales) and token rows landed (transaction bytes)
+  uint64_t afull[kTmNS];  // the stage's A slot is written (8 producer warps)
+  uint64_t empty[kTmNS];  // the MMAs reading the stage and its A slot are done
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t fin;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__host__ __device__ constexpr size_t tm_smem_bytes() {
+  return 1024 + (size_t)kTmNS * kTmStage + sizeof(TmShared) + 16 + 16 * kFqList;
+}
+
+// 4-D tiled TMA load of the tile map box at (0, piece, tile, expert) with an L2 policy
+__device__ __forceinline__ void tma_load_tiles_pol(uint32_t dst, const CUtensorMap* map, int piece,
+                                                   int tile, int expert, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(piece), "r"(tile), "r"(expert),
+      "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+
+// 32 TMEM lanes (one per thread of the warp) x 16 consecutive 32-bit columns
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D (TMEM) += A (TMEM, 128 lanes x 8 columns of f16 pairs) . B (shared memory)^T
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// One row's 16-column block from a lane's 16-byte code vector of the packed
+// tile (word w: bytes [(g, 4w..4w+1), (g+8, 4w..4w+1), (g, 4w+2..), (g+8, 4w+2..)],
+// two codes a byte): `sel` picks row g's bytes (0x6420) or row g+8's (0x7531)
+// in column order; each f16 pair is multiplied by the block scale `sc` (both
+// halves the scale).
+__device__ __forceinline__ void tm_block(const uint4& cv, uint32_t sel, uint32_t sc, uint32_t* out) {
+  uint32_t hh[4];
+  e2m1x8_to_f16x8(prmt(cv.x, cv.y, sel), hh);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) out[k] = hmul2(hh[k], sc);
+  e2m1x8_to_f16x8(prmt(cv.z, cv.w, sel), hh);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) out[4 + k] = hmul2(hh[k], sc);
+}
+
+// The token rows of the gate/up GEMM in slot order: row r of xs = the f16 copy
+// of x's row of token row_token[r] (r < T*k), or of token r - T*k (the shared
+// expert's rows); a warp per row.
+__global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int rows, uint16_t* xs) {
+  griddep_wait();
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int S = p.T * p.k;
+  const int t = r >= S ? r - S : p.row_token[r];
+  if (t < 0 || t >= p.T) {
+    if (lane == 0) *p.status = kStatusInvalid;
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(p.xh + (size_t)t * p.H);
+  uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * p.H);
+  for (int v = lane; v < p.H / 8; v += 32) dst[v] = src[v];
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTmThreads, 1)
+    tc_tmem_kernel(ExpertParams p, const __grid_constant__ CUtensorMap tmap,
+                   const __grid_constant__ CUtensorMap bmap, int max_items) {
+  griddep_wait();
+  extern __shared__ __align__(1024) uint8_t tm_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tm_smem_raw) + 1023) & ~(uintptr_t)1023);
+  TmShared* sh = reinterpret_cast<TmShared*>(base + kTmNS * kTmStage);
+  int4* list = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(sh + 1) + 15) & ~(uintptr_t)15);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.T * p.k;
+  const int K = MODE == 1 ? p.I : p.H;
+  const int KC = K / kTcK;
+  const int mblocks = (MODE == 1 ? p.H : 2 * p.I) / kTcM;
+  const int items = min(p.nsh_tc + *p.n_tc_entries, max_items);
+  const int n_units = mblocks * max(items, 0);
+  const uint32_t s0 = smem_u32(base);
+  auto b_addr = [&](int s) { return s0 + s * kTmStage; };  // 1024-byte aligned
+  auto c_addr = [&](int s) { return s0 + s * kTmStage + kTmB; };
+  auto v_addr = [&](int s) { return s0 + s * kTmStage + kTmB + kTmCodes; };
+
+  if (tid == 0) {
+    for (int i = 0; i < kTmNS; ++i) {
+      mbar_init(&sh->full[i], 1);
+      mbar_init(&sh->afull[i], 8);  // the 8 producer warps
+      mbar_init(&sh->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->acc_full[i], 1);
+      mbar_init(&sh->acc_empty[i], 8);  // the 8 epilogue warps
+    }
+    mbar_init(&sh->fin, 1);
+    sh->abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) {  // the unit list: {expert, first row, tokens, M-block}
+    for (int i = lane; i < kFqList; i += 32) {
+      const int u = blockIdx.x + i * gridDim.x;
+      int4 v = make_int4(0, 0, 0, 0);
+      if (u < n_units) {
+        int e, r0, n;
+        v = tc_entry(p, u / mblocks, e, r0, n) ? make_int4(e, r0, n, u % mblocks)
+                                               : make_int4(0, 0, 0, u % mblocks);
+      }
+      list[i] = v;
+    }
+  }
+  if (warp == kTmMmaWarp) tmem_alloc(&sh->tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = sh->tmem_base;
+  volatile int* abort = &sh->abort;
+
+  if (warp < kTmEpi0) {
+    // ---------------------------------------------------------------- producers: A into TMEM
+    // row r of the M-block = TMEM lane r: tile r / 16, row g or g + 8 of it
+    const int q = warp & 3, h = warp >> 2;
+    const int r = 32 * q + lane, tile = r >> 4, g8 = lane & 7, hi = (lane >> 3) & 1;
+    const uint32_t sel = hi ? 0x7531u : 0x6420u;
+    // the lanes (g8, 2h) and (g8, 2h + 1) of the tile's vectors: this row's
+    // 16-column blocks 2h and 2h + 1 of every chunk (scales: byte 2j + hi)
+    const uint32_t voff = (uint32_t)(tile * 512 + 16 * (4 * g8 + 2 * h));
+    const uint32_t tdst = tmem_d + ((uint32_t)(32 * q) << 16) + kTmACol + 16 * h;
+    uint4 sv0 = make_uint4(0, 0, 0, 0), sv1 = sv0;
+    int gs = 0;
+    FqUnit cur;
+    bool ok = true;
+    for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+      if (cur.n == 0) continue;
+      for (int c = 0; c < KC; ++c, ++gs) {
+        const int s = gs % kTmNS, j = c & 7;
+        const uint32_t ph = (gs / kTmNS) & 1;
+        // the stage's copies landed; the MMAs that last read the A slot are done
+        // (the TMA warp waited for them before these copies)
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->full[s], ph, abort, p.wait_budget) &&
+                                          mbar_wait_fast(&sh->empty[s], ph ^ 1, abort, p.wait_budget))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (j == 0) {  // the super-chunk's scale vectors, kept for its 8 chunks
+          sv0 = lds128(v_addr(s) + voff);
+          sv1 = lds128(v_addr(s) + voff + 16);
+        }
+        const uint4 cv0 = lds128(c_addr(s) + voff), cv1 = lds128(c_addr(s) + voff + 16);
+        const int sb = 2 * j + hi;
+        const uint32_t e0 = (u4get(sv0, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
+        const uint32_t e1 = (u4get(sv1, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
+        const uint32_t sp = e4m3x2_to_f16x2(e0 | (e1 << 8));
+        uint32_t v[16];
+        tm_block(cv0, sel, dup_lo(sp), v);
+        tm_block(cv1, sel, dup_hi(sp), v + 8);
+        tmem_st16(tdst + 32 * s, v);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->afull[s]);
+      }
+    }
+  } else if (warp < kTmMmaWarp) {
+    // ---------------------------------------------------------------- epilogue
+    // warp 8 + 4h + q: TMEM lane quadrant q (rows 32q..32q+31), columns 64h..64h+63
+    const int qd = warp & 3, ch = (warp - kTmEpi0) >> 2;
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    auto tok = [&](const FqUnit& w, int r) -> size_t {
+      return (size_t)(w.expert == p.E ? w.row0 - S + r : p.row_token[w.row0 + r]);
+    };
+    FqUnit cur;
+    int uk = 0;
+    for (int i = 0; fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+      if (cur.n == 0) continue;
+      const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+      float sc_lane[2] = {1.0f, 1.0f};  // W4A4 (activations quantised): the columns' scales
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col = 64 * ch + 32 * c + lane;
+        if (col < cur.n) {
+          if (MODE == 0 && p.ts_x) sc_lane[c] = p.ts_x[tok(cur, col)];
+          if (MODE == 1 && p.ts_a) sc_lane[c] = p.ts_a[cur.row0 + col];
+        }
+      }
+      if (!mbar_wait_sleep(&sh->acc_full[buf], (uk >> 1) & 1, abort, p.wait_budget)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem_d + lane_addr + (uint32_t)(128 * buf);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int c0 = 64 * ch + 32 * c;
+        if (c0 >= n_pad) break;
+        uint32_t v[32];
+        tmem_ld32(acc + c0, v);
+        if (MODE == 0) {
+          // lanes 0-15 hold gate rows, 16-31 the matching up rows: lane l < 16
+          // computes columns 0-15 of its row, lane l + 16 columns 16-31
+          const int i = 16 * (4 * cur.mb + qd) + (lane & 15);
+          const bool hi = lane >= 16;
+          const float ts_g = p.tscale[cur.expert * 3 + 0], ts_u = p.tscale[cur.expert * 3 + 1];
+#pragma unroll
+          for (int qq = 0; qq < 16; ++qq) {
+            const float lo_v = __uint_as_float(v[qq]), hi_v = __uint_as_float(v[16 + qq]);
+            const float recv = __shfl_xor_sync(0xffffffffu, hi ? lo_v : hi_v, 16);
+            const int cq = hi ? 16 + qq : qq;
+            const float gv = hi ? recv : lo_v, uv = hi ? hi_v : recv;
+            const float sx = __shfl_sync(0xffffffffu, sc_lane[c], cq);
+            const int col = c0 + cq;
+            if (col < cur.n) {
+              const float Gv = (ts_g * sx) * gv, U = (ts_u * sx) * uv;
+              const float a = Gv / (1.0f + expf(-Gv)) * U;
+              if (p.af)
+                p.af[(size_t)(cur.row0 + col) * p.I + i] = a;
+              else
+                p.abuf[(size_t)(cur.row0 + col) * p.I + i] = a_to_f16(a, p.status);
+            }
+          }
+        } else {
+          const float ts = p.tscale[cur.expert * 3 + 2];
+          const int hrow = kTcM * cur.mb + 32 * qd + lane;
+#pragma unroll
+          for (int qq = 0; qq < 32; ++qq) {
+            const float sa = __shfl_sync(0xffffffffu, sc_lane[c], qq);
+            const int col = c0 + qq;
+            if (col < cur.n)
+              p.ybuf[(size_t)(cur.row0 + col) * p.H + hrow] = (ts * sa) * __uint_as_float(v[qq]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
+      ++uk;
+    }
+  } else if (warp == kTmMmaWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issue
+      FqUnit cur;
+      int gs = 0, uk = 0;
+      bool ok = true;
+      for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+        if (cur.n == 0) continue;
+        const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+        const uint32_t idesc = idesc_f16(kTcM, n_pad);
+        // the epilogue of the unit before the previous one has read this accumulator
+        if (!mbar_wait_fast(&sh->acc_empty[buf], ((uk >> 1) & 1) ^ 1, abort, p.wait_budget)) break;
+        tc_fence_after();
+        for (int c = 0; c < KC; ++c, ++gs) {
+          const int s = gs % kTmNS;
+          const uint32_t ph = (gs / kTmNS) & 1;
+          if (!mbar_wait_fast(&sh->afull[s], ph, abort, p.wait_budget) ||
+              !mbar_wait_fast(&sh->full[s], ph, abort, p.wait_budget)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bd = sw128_desc(b_addr(s));
+          const uint32_t a0 = tmem_d + kTmACol + 32 * s;
+#pragma unroll
+          for (int kk = 0; kk < kTcK / 16; ++kk)  // A: +8 columns, B: +32 bytes per K-step of 16
+            umma_f16_tmem_a(tmem_d + 128 * buf, a0 + 8 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
+          umma_commit(&sh->empty[s]);
+        }
+        if (ok) umma_commit(&sh->acc_full[buf]);
+        ++uk;
+      }
+      umma_commit(&sh->fin);  // every MMA issued before TMEM is freed
+      mbar_drain(&sh->fin, 0);
+    }
+    __syncwarp();
+  } else {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA issue
+      const CUtensorMap* map = &tmap;
+      const uint64_t wpol = l2_evict_first(), apol = l2_evict_last();
+      const int tw = warp - kTmTmaWarp;  // this warp's stages: gs % 2 == tw
+      int gs = 0;
+      FqUnit cur;
+      bool ok = true;
+      for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
+        if (cur.n == 0) continue;
+        for (int c = 0; c < KC; ++c, ++gs) {
+          if ((gs & 1) != tw) continue;
+          const int s = gs % kTmNS, j = c & 7;
+          if (!mbar_wait(&sh->empty[s], ((gs / kTmNS) & 1) ^ 1, abort, p.wait_budget)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect(&sh->full[s], (uint32_t)(kTmCodes + kTmB) + (j == 0 ? (uint32_t)kTmCodes : 0u));
+          tma_load_tiles_pol(c_addr(s), map, 9 * (c >> 3) + 1 + j, 8 * cur.mb, cur.expert, &sh->full[s], wpol);
+          if (j == 0)
+            tma_load_tiles_pol(v_addr(s), map, 9 * (c >> 3), 8 * cur.mb, cur.expert, &sh->full[s], wpol);
+          tma_load_rows(b_addr(s), &bmap, kTcK * c, cur.row0, &sh->full[s], apol);
+        }
+      }
+      if (*abort) {  // let this warp's copies in flight land before the CTA exits (bounded waits)
+        for (int c = (gs > kTmNS ? gs - kTmNS : 0); c < gs; ++c)
+          if ((c & 1) == tw) mbar_drain(&sh->full[c % kTmNS], (c / kTmNS) & 1);
+      }
+    }
+    __syncwarp();
+  }
+
+  if (*abort && tid == 0) *p.status = kStatusTimeout;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTmMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_d, 512);
+  }
+}
+
 }  // namespace
 
 // M-blocks per CTA of the TMA-fed expert GEMMs: 4 where they divide the matrix
@@ -1206,6 +1583,53 @@ cudaError_t launch_tc_fp4_down(const ExpertParams& p, int items, const void* til
                   fq_smem_bytes(), st, true, p, map, bc, bs, items);
 }
 
+// [rows][cols] f16 rows in slot order (x gathered, or a); a box: 64 columns
+// of 128 rows, 128B-swizzled
+cudaError_t tc_make_rows16_map(void* map, const uint16_t* base, size_t rows, int cols) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcMaxN};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                            const_cast<uint16_t*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gather_rows(const ExpertParams& p, int rows, uint16_t* xs, cudaStream_t st) {
+  const int blocks = (rows + 7) / 8;
+  return launch_k(gather_rows_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, st, true, p, rows, xs);
+}
+
+cudaError_t launch_tc_tm_gateup(const ExpertParams& p, int items, const void* tile_map,
+                                const void* xmap, cudaStream_t st) {
+  const int mblocks = (2 * p.I) / kTcM;
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(xmap);
+  return launch_k(tc_tmem_kernel<0>, dim3(fq_grid(mblocks * items)), dim3(kTmThreads),
+                  tm_smem_bytes(), st, true, p, map, bm, items);
+}
+
+cudaError_t launch_tc_tm_down(const ExpertParams& p, int items, const void* tile_map,
+                              const void* amap, cudaStream_t st) {
+  const int mblocks = p.H / kTcM;
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(amap);
+  return launch_k(tc_tmem_kernel<1>, dim3(fq_grid(mblocks * items)), dim3(kTmThreads),
+                  tm_smem_bytes(), st, true, p, map, bm, items);
+}
+
 bool tc_router_ok(int E, int H) { return E % kTcM == 0 && H % kTcK == 0; }
 
 // logits_out gets the fp32 dot products (one K slice: the top-k step adds the bias)
@@ -1226,6 +1650,12 @@ cudaError_t tc_kernels_init() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc_fp4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)fq_smem_bytes());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_tmem_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tm_smem_bytes());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_tmem_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tm_smem_bytes());
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(tc_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tc_smem());

@@ -169,7 +169,8 @@ int max_tc_entries(int T, int E, int k);
 // made by tc_make_tile_map with box_tiles = 8 * tc_group(M-blocks of the matrix)
 int tc_group(int mblocks);
 cudaError_t tc_make_tile_map(void* map, const uint8_t* region, int n_experts, int tiles,
-                             uint64_t tile_bytes, uint64_t expert_bytes, int box_tiles);
+                             uint64_t tile_bytes, uint64_t expert_bytes, int box_tiles,
+                             int box_pieces = 1);
 cudaError_t launch_tc_gateup(const ExpertParams& p, int grid_y, const void* tile_map,
                              cudaStream_t st);
 cudaError_t launch_tc_down(const ExpertParams& p, int grid_y, const void* tile_map,
@@ -187,16 +188,18 @@ cudaError_t launch_tc_fp4_down(const ExpertParams& p, int items, const void* til
                                const void* bmap_c, const void* bmap_s, cudaStream_t st);
 // the maps of the activation rows the block-scaled GEMMs read (B operands):
 // [rows][row_bytes], codes (128-byte boxes, 128B-swizzled) or scales (16-byte boxes)
-// W4A16 expert GEMMs with the dequantised weights in tensor memory: tile_map
-// made by tc_make_tile_map with box_tiles = 8; xmap / amap by
+// W4A16 expert GEMMs with the dequantised weights in tensor memory (H and I
+// multiples of 128: tc_tm_ok): code_map made by tc_make_tile_map with
+// box_tiles = 8 and box_pieces = 2, scale_map with box_tiles = 8; xmap / amap by
 // tc_make_rows16_map over x gathered into slot order (xs, written by
 // launch_gather_rows: rows = T*k + T) / the rows of a.  grid: a CTA per SM.
 cudaError_t tc_make_rows16_map(void* map, const uint16_t* base, size_t rows, int cols);
 cudaError_t launch_gather_rows(const ExpertParams& p, int rows, uint16_t* xs, cudaStream_t st);
-cudaError_t launch_tc_tm_gateup(const ExpertParams& p, int items, const void* tile_map,
-                                const void* xmap, cudaStream_t st);
-cudaError_t launch_tc_tm_down(const ExpertParams& p, int items, const void* tile_map,
-                              const void* amap, cudaStream_t st);
+bool tc_tm_ok(int H, int I);
+cudaError_t launch_tc_tm_gateup(const ExpertParams& p, int items, const void* code_map,
+                                const void* scale_map, const void* xmap, cudaStream_t st);
+cudaError_t launch_tc_tm_down(const ExpertParams& p, int items, const void* code_map,
+                              const void* scale_map, const void* amap, cudaStream_t st);
 cudaError_t tc_make_rows_map(void* map, const uint8_t* base, size_t rows, int row_bytes, bool codes);
 bool tc_router_ok(int E, int H);
 cudaError_t launch_tc_router(const ExpertParams& p, cudaStream_t st);

@@ -121,8 +121,10 @@ struct moe_layer {
   // token rows in slot order (x gathered into the y buffer, which the down
   // GEMM writes only after gate/up; the rows of a) for the W4A16 GEMMs with
   // the weights in tensor memory
-  alignas(64) unsigned char map_gu8[128] = {};
+  alignas(64) unsigned char map_gu8[128] = {};   // code boxes: 2 pieces of 8 tiles
   alignas(64) unsigned char map_dn8[128] = {};
+  alignas(64) unsigned char map_gu8s[128] = {};  // scale boxes: 1 piece of 8 tiles
+  alignas(64) unsigned char map_dn8s[128] = {};
   alignas(64) unsigned char map_xs[128] = {};
   alignas(64) unsigned char map_ab[128] = {};
   bool tm_maps_ok = false;
@@ -215,11 +217,15 @@ void make_tile_maps(moe_layer* L) {
       tc_make_tile_map(L->map_dn, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
                        g.expert_bytes, 8 * tc_group(dn_tiles / 8)) == cudaSuccess;
   L->tm_maps_ok =
-      L->maps_ok &&
-      tc_make_tile_map(L->map_gu8, L->arena, n_total, gu_tiles, g.gu.tile_bytes, g.expert_bytes, 8) ==
+      L->maps_ok && tc_tm_ok(L->H, L->I) &&
+      tc_make_tile_map(L->map_gu8, L->arena, n_total, gu_tiles, g.gu.tile_bytes, g.expert_bytes, 8, 2) ==
           cudaSuccess &&
       tc_make_tile_map(L->map_dn8, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
-                       g.expert_bytes, 8) == cudaSuccess;
+                       g.expert_bytes, 8, 2) == cudaSuccess &&
+      tc_make_tile_map(L->map_gu8s, L->arena, n_total, gu_tiles, g.gu.tile_bytes, g.expert_bytes, 8, 1) ==
+          cudaSuccess &&
+      tc_make_tile_map(L->map_dn8s, L->arena + g.gu_bytes, n_total, dn_tiles, g.dn.tile_bytes,
+                       g.expert_bytes, 8, 1) == cudaSuccess;
   make_mma_maps(L);
 }
 
@@ -419,7 +425,8 @@ bool tm_path(moe_layer* L, int T) {
 int launch_tm_gateup(moe_layer* L, const ExpertParams& ep, int T, cudaStream_t st) {
   const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
   CK("row gather kernel launch", launch_gather_rows(ep, T * L->k + (L->shared ? T : 0), xs_rows(L), st));
-  CK("tensor-core gate/up kernel launch", launch_tc_tm_gateup(ep, gy, L->map_gu8, L->map_xs, st));
+  CK("tensor-core gate/up kernel launch",
+     launch_tc_tm_gateup(ep, gy, L->map_gu8, L->map_gu8s, L->map_xs, st));
   return MOE_OK;
 }
 
@@ -505,7 +512,8 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
     }
     if (w4a4(L) && launch_quant_a(L, T, st)) return MOE_ECUDA;
     if (tm_path(L, T))
-      CK("tensor-core down kernel launch", launch_tc_tm_down(ep, gy, L->map_dn8, L->map_ab, st));
+      CK("tensor-core down kernel launch",
+         launch_tc_tm_down(ep, gy, L->map_dn8, L->map_dn8s, L->map_ab, st));
     else
       CK("tensor-core down kernel launch", launch_tc_down(ep, gy, L->map_dn, st));
     CK("combine kernel launch", launch_combine(ep, L->gates, L->inv, out, true, st));
@@ -1210,7 +1218,7 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
                                       L->map_ba_c, L->map_ba_s, st));
       else if (tm_path(L, T))
         CK("down", launch_tc_tm_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn8,
-                                     L->map_ab, st));
+                                     L->map_dn8s, L->map_ab, st));
       else if (tc_path(L, T))
         CK("down", launch_tc_down(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_dn, st));
       else if (fused)

@@ -762,6 +762,47 @@ __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* m
       : "memory");
 }
 
+// y rows from a 32-column accumulator chunk (lane l = row h0 + l of the
+// M-block, v[c] = column c0 + c): 4 x 4 transposes within lane quads (two
+// shuffle rounds) give lane 4a + b the rows h0 + 4a .. + 3 of column c0 + 4m + b,
+// so each store instruction writes 4 rows of y x 128 bytes (16 bytes a lane)
+// instead of one.  y = (ts * column scale) * D.
+__device__ __forceinline__ void store_y_chunk(const ExpertParams& p, const uint32_t (&v)[32], int row0,
+                                              int c0, int n, int h0, float ts, float sc_lane) {
+  const int lane = threadIdx.x & 31;
+  const bool b1 = lane & 1, b2 = lane & 2;
+  float* yb = p.ybuf + h0 + 4 * (lane >> 2);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    float w0 = __uint_as_float(v[4 * m]), w1 = __uint_as_float(v[4 * m + 1]);
+    float w2 = __uint_as_float(v[4 * m + 2]), w3 = __uint_as_float(v[4 * m + 3]);
+    float s0 = b2 ? w0 : w2, s1 = b2 ? w1 : w3;
+    float r0 = __shfl_xor_sync(0xffffffffu, s0, 2), r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+    if (b2) {
+      w0 = r0;
+      w1 = r1;
+    } else {
+      w2 = r0;
+      w3 = r1;
+    }
+    s0 = b1 ? w0 : w1;
+    s1 = b1 ? w2 : w3;
+    r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+    r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+    if (b1) {
+      w0 = r0;
+      w2 = r1;
+    } else {
+      w1 = r0;
+      w3 = r1;
+    }
+    const int cq = 4 * m + (lane & 3), col = c0 + cq;
+    const float sc = ts * __shfl_sync(0xffffffffu, sc_lane, cq);
+    if (col < n)
+      *reinterpret_cast<float4*>(yb + (size_t)(row0 + col) * p.H) = make_float4(sc * w0, sc * w1, sc * w2, sc * w3);
+  }
+}
+
 struct FqUnit {
   int expert, row0, n, mb;
 };
@@ -892,6 +933,10 @@ __global__ void __launch_bounds__(kFqThreads, 1)
     for (int i = 0; fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
       if (cur.n == 0) continue;
       const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+      // the unit's tensor scales, read before the accumulator wait (an L2 round
+      // trip under this load takes about a microsecond)
+      const float ts_g = p.tscale[cur.expert * 3 + (MODE == 1 ? 2 : 0)];
+      const float ts_u = MODE == 0 ? p.tscale[cur.expert * 3 + 1] : 0.0f;
       float sc_lane[2] = {1.0f, 1.0f};  // W4A4 scales of columns 64h + 32c + lane
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -915,7 +960,6 @@ __global__ void __launch_bounds__(kFqThreads, 1)
           // computes columns 0-15 of its row, lane l + 16 columns 16-31
           const int i = 16 * (4 * cur.mb + qd) + (lane & 15);
           const bool hi = lane >= 16;
-          const float ts_g = p.tscale[cur.expert * 3 + 0], ts_u = p.tscale[cur.expert * 3 + 1];
 #pragma unroll
           for (int qq = 0; qq < 16; ++qq) {
             const float lo_v = __uint_as_float(v[qq]), hi_v = __uint_as_float(v[16 + qq]);
@@ -934,14 +978,7 @@ __global__ void __launch_bounds__(kFqThreads, 1)
             }
           }
         } else {
-          const float ts = p.tscale[cur.expert * 3 + 2];
-          const int h = kTcM * cur.mb + 32 * qd + lane;
-#pragma unroll
-          for (int qq = 0; qq < 32; ++qq) {
-            const float sa = __shfl_sync(0xffffffffu, sc_lane[c], qq);
-            const int col = c0 + qq;
-            if (col < cur.n) p.ybuf[(size_t)(cur.row0 + col) * p.H + h] = (ts * sa) * __uint_as_float(v[qq]);
-          }
+          store_y_chunk(p, v, cur.row0, c0, cur.n, kTcM * cur.mb + 32 * qd, ts_g, sc_lane[c]);
         }
       }
       tc_fence_before();
@@ -1068,37 +1105,42 @@ __global__ void __launch_bounds__(kFqThreads, 1)
 // b_desc), so only the token rows pass through shared memory.
 //
 // Persistent like tc_fp4_kernel: a CTA per SM walks units (work item, 128-row
-// M-block), its unit list in shared memory; a ring of kTmNS stages of 64
-// columns of K (each with its own 32-column A slot in TMEM) runs across units,
+// M-block), its unit list in shared memory; a ring of kTmNS stages of 128
+// columns of K (each with its own 64-column A slot in TMEM) runs across units,
 // and the accumulators are double-buffered.  Per stage:
 //   * one of two TMA warps (even and odd stages: a single issuing thread
 //     keeps too few copies in flight) loads the M-block's code vectors of the
-//     chunk (one box of the arena's tile map: the same 512-byte piece of 8
-//     consecutive 16-row tiles, 4 KB), at the first chunk of a super-chunk
-//     also the tiles' scale vectors, and the chunk's 64 columns of the item's
-//     128 token rows (one 16 KB box, 128B-swizzled: the K-major layout the MMA
-//     reads) from rows in slot order: x gathered into them by
+//     stage's two 64-column chunks (one box of the arena's tile map: the same
+//     two 512-byte pieces of 8 consecutive 16-row tiles, 8 KB), at the first
+//     chunk of a super-chunk also the tiles' scale vectors (4 KB), and the
+//     stage's 128 columns of the item's 128 token rows (two 16 KB boxes,
+//     128B-swizzled: the K-major layout the MMA reads) from rows in slot
+//     order: x gathered into them by
 //     gather_rows_kernel (gate/up), or a (down); rows past the item's tokens
 //     belong to other items and only reach accumulator columns the epilogue
 //     never reads;
 //   * producer warps 0-7 (warp w: TMEM lane quadrant w % 4, columns 32(w / 4)
-//     .. +31 of the chunk) rebuild their row's codes from the tile's fragment
+//     .. +31 of each chunk) rebuild their row's codes from the tile's fragment
 //     order (one byte permute per 8 codes), convert and scale them to f16 and
-//     store 16 TMEM columns, then arrive once per warp;
-//   * the MMA thread (warp 16) issues the stage's 4 MMAs (K = 16 each) and
-//     commits the stage (its shared memory and its A slot) back;
+//     store 2 x 16 TMEM columns, then arrive once per warp;
+//   * the MMA thread (warp 16) issues the stage's 8 MMAs (K = 16 each) and
+//     commits the stage (its shared memory and its A slot) back: the thread's
+//     waits and commit per stage cost about as much as 4 MMAs, so a stage
+//     carries 8;
 //   * epilogue warps 8-15 read a finished unit's accumulators (SwiGLU into a,
 //     or y rows) and hand the buffer back.
 constexpr int kTmThreads = 32 * 19;
 constexpr int kTmEpi0 = 8;                     // epilogue warps 8-15
 constexpr int kTmMmaWarp = 16, kTmTmaWarp = 17;  // TMA warps 17 (even stages) and 18 (odd)
 static_assert(32 * (kTmTmaWarp + 2) == kTmThreads, "warp roles");
-constexpr int kTmNS = 8;                       // stages in flight (and A slots)
-constexpr int kTmB = kTcMaxN * 128;            // token rows of a stage: 128 x 64 f16
-constexpr int kTmCodes = 8 * 512;              // one 512-byte piece of 8 tiles
-constexpr int kTmStage = kTmB + 2 * kTmCodes;  // token rows, code vectors, scale vectors
-constexpr uint32_t kTmACol = 256;              // A slots (32 columns each) after two accumulators
-static_assert(kTmACol + 32 * kTmNS <= 512, "tensor memory columns");
+constexpr int kTmK = 128;                      // K per stage: two 64-column chunks
+constexpr int kTmNS = 4;                       // stages in flight (and A slots)
+constexpr int kTmB = 2 * kTcMaxN * 128;        // token rows of a stage: 2 x (128 rows x 64 f16)
+constexpr int kTmCodes = 2 * 8 * 512;          // two 512-byte pieces of 8 tiles
+constexpr int kTmScales = 8 * 512;             // the scale vectors of 8 tiles
+constexpr int kTmStage = kTmB + kTmCodes + kTmScales;  // token rows, code vectors, scale vectors
+constexpr uint32_t kTmACol = 256;              // A slots (64 columns each) after two accumulators
+static_assert(kTmACol + 64 * kTmNS <= 512, "tensor memory columns");
 static_assert(kTmStage % 1024 == 0, "stages stay 1024-byte aligned");
 
 struct TmShared {
@@ -1190,7 +1232,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int ro
 template <int MODE>
 __global__ void __launch_bounds__(kTmThreads, 1)
     tc_tmem_kernel(ExpertParams p, const __grid_constant__ CUtensorMap tmap,
-                   const __grid_constant__ CUtensorMap bmap, int max_items) {
+                   const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap bmap,
+                   int max_items) {
   griddep_wait();
   extern __shared__ __align__(1024) uint8_t tm_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -1200,13 +1243,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.T * p.k;
   const int K = MODE == 1 ? p.I : p.H;
-  const int KC = K / kTcK;
+  const int KC = K / kTmK;  // stages per unit
   const int mblocks = (MODE == 1 ? p.H : 2 * p.I) / kTcM;
   const int items = min(p.nsh_tc + *p.n_tc_entries, max_items);
   const int n_units = mblocks * max(items, 0);
   const uint32_t s0 = smem_u32(base);
   auto b_addr = [&](int s) { return s0 + s * kTmStage; };  // 1024-byte aligned
-  auto c_addr = [&](int s) { return s0 + s * kTmStage + kTmB; };
+  auto c_addr = [&](int s) { return s0 + s * kTmStage + kTmB; };  // [tile][piece 0..1][512 B]
   auto v_addr = [&](int s) { return s0 + s * kTmStage + kTmB + kTmCodes; };
 
   if (tid == 0) {
@@ -1250,7 +1293,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     const uint32_t sel = hi ? 0x7531u : 0x6420u;
     // the lanes (g8, 2h) and (g8, 2h + 1) of the tile's vectors: this row's
     // 16-column blocks 2h and 2h + 1 of every chunk (scales: byte 2j + hi)
-    const uint32_t voff = (uint32_t)(tile * 512 + 16 * (4 * g8 + 2 * h));
+    const uint32_t loff = (uint32_t)(16 * (4 * g8 + 2 * h));
     const uint32_t tdst = tmem_d + ((uint32_t)(32 * q) << 16) + kTmACol + 16 * h;
     uint4 sv0 = make_uint4(0, 0, 0, 0), sv1 = sv0;
     int gs = 0;
@@ -1259,7 +1302,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
       if (cur.n == 0) continue;
       for (int c = 0; c < KC; ++c, ++gs) {
-        const int s = gs % kTmNS, j = c & 7;
+        const int s = gs % kTmNS, j0 = 2 * (c & 3);  // chunks j0, j0 + 1 of the super-chunk
         const uint32_t ph = (gs / kTmNS) & 1;
         // the stage's copies landed; the MMAs that last read the A slot are done
         // (the TMA warp waited for them before these copies)
@@ -1269,19 +1312,23 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           break;
         }
         tc_fence_after();
-        if (j == 0) {  // the super-chunk's scale vectors, kept for its 8 chunks
-          sv0 = lds128(v_addr(s) + voff);
-          sv1 = lds128(v_addr(s) + voff + 16);
+        if (j0 == 0) {  // the super-chunk's scale vectors, kept for its 8 chunks
+          sv0 = lds128(v_addr(s) + tile * 512 + loff);
+          sv1 = lds128(v_addr(s) + tile * 512 + loff + 16);
         }
-        const uint4 cv0 = lds128(c_addr(s) + voff), cv1 = lds128(c_addr(s) + voff + 16);
-        const int sb = 2 * j + hi;
-        const uint32_t e0 = (u4get(sv0, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
-        const uint32_t e1 = (u4get(sv1, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
-        const uint32_t sp = e4m3x2_to_f16x2(e0 | (e1 << 8));
-        uint32_t v[16];
-        tm_block(cv0, sel, dup_lo(sp), v);
-        tm_block(cv1, sel, dup_hi(sp), v + 8);
-        tmem_st16(tdst + 32 * s, v);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {  // the stage's two chunks
+          const uint32_t ca = c_addr(s) + tile * 1024 + hh * 512 + loff;
+          const uint4 cv0 = lds128(ca), cv1 = lds128(ca + 16);
+          const int sb = 2 * (j0 + hh) + hi;
+          const uint32_t e0 = (u4get(sv0, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
+          const uint32_t e1 = (u4get(sv1, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
+          const uint32_t sp = e4m3x2_to_f16x2(e0 | (e1 << 8));
+          uint32_t v[16];
+          tm_block(cv0, sel, dup_lo(sp), v);
+          tm_block(cv1, sel, dup_hi(sp), v + 8);
+          tmem_st16(tdst + 64 * s + 32 * hh, v);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -1301,6 +1348,10 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     for (int i = 0; fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
       if (cur.n == 0) continue;
       const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+      // the unit's tensor scales, read before the accumulator wait (an L2 round
+      // trip under this load takes about a microsecond)
+      const float ts_g = p.tscale[cur.expert * 3 + (MODE == 1 ? 2 : 0)];
+      const float ts_u = MODE == 0 ? p.tscale[cur.expert * 3 + 1] : 0.0f;
       float sc_lane[2] = {1.0f, 1.0f};  // W4A4 (activations quantised): the columns' scales
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -1324,7 +1375,6 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           // computes columns 0-15 of its row, lane l + 16 columns 16-31
           const int i = 16 * (4 * cur.mb + qd) + (lane & 15);
           const bool hi = lane >= 16;
-          const float ts_g = p.tscale[cur.expert * 3 + 0], ts_u = p.tscale[cur.expert * 3 + 1];
 #pragma unroll
           for (int qq = 0; qq < 16; ++qq) {
             const float lo_v = __uint_as_float(v[qq]), hi_v = __uint_as_float(v[16 + qq]);
@@ -1343,15 +1393,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             }
           }
         } else {
-          const float ts = p.tscale[cur.expert * 3 + 2];
-          const int hrow = kTcM * cur.mb + 32 * qd + lane;
-#pragma unroll
-          for (int qq = 0; qq < 32; ++qq) {
-            const float sa = __shfl_sync(0xffffffffu, sc_lane[c], qq);
-            const int col = c0 + qq;
-            if (col < cur.n)
-              p.ybuf[(size_t)(cur.row0 + col) * p.H + hrow] = (ts * sa) * __uint_as_float(v[qq]);
-          }
+          store_y_chunk(p, v, cur.row0, c0, cur.n, kTcM * cur.mb + 32 * qd, ts_g, sc_lane[c]);
         }
       }
       tc_fence_before();
@@ -1382,10 +1424,12 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           }
           tc_fence_after();
           const uint64_t bd = sw128_desc(b_addr(s));
-          const uint32_t a0 = tmem_d + kTmACol + 32 * s;
+          const uint32_t a0 = tmem_d + kTmACol + 64 * s;
 #pragma unroll
-          for (int kk = 0; kk < kTcK / 16; ++kk)  // A: +8 columns, B: +32 bytes per K-step of 16
-            umma_f16_tmem_a(tmem_d + 128 * buf, a0 + 8 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
+          for (int kk = 0; kk < kTmK / 16; ++kk)  // A: +8 columns per K-step of 16; B: +32 bytes
+            // within a 64-column box, the second box 16 KB on
+            umma_f16_tmem_a(tmem_d + 128 * buf, a0 + 8 * kk, bd + 2 * (kk & 3) + (kk >> 2) * (kTcMaxN * 128 >> 4),
+                            idesc, (c | kk) != 0);
           umma_commit(&sh->empty[s]);
         }
         if (ok) umma_commit(&sh->acc_full[buf]);
@@ -1408,16 +1452,16 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         if (cur.n == 0) continue;
         for (int c = 0; c < KC; ++c, ++gs) {
           if ((gs & 1) != tw) continue;
-          const int s = gs % kTmNS, j = c & 7;
+          const int s = gs % kTmNS, j0 = 2 * (c & 3), sc = c >> 2;
           if (!mbar_wait(&sh->empty[s], ((gs / kTmNS) & 1) ^ 1, abort, p.wait_budget)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect(&sh->full[s], (uint32_t)(kTmCodes + kTmB) + (j == 0 ? (uint32_t)kTmCodes : 0u));
-          tma_load_tiles_pol(c_addr(s), map, 9 * (c >> 3) + 1 + j, 8 * cur.mb, cur.expert, &sh->full[s], wpol);
-          if (j == 0)
-            tma_load_tiles_pol(v_addr(s), map, 9 * (c >> 3), 8 * cur.mb, cur.expert, &sh->full[s], wpol);
-          tma_load_rows(b_addr(s), &bmap, kTcK * c, cur.row0, &sh->full[s], apol);
+          mbar_arrive_expect(&sh->full[s], (uint32_t)(kTmCodes + kTmB) + (j0 == 0 ? (uint32_t)kTmScales : 0u));
+          tma_load_tiles_pol(c_addr(s), map, 9 * sc + 1 + j0, 8 * cur.mb, cur.expert, &sh->full[s], wpol);
+          if (j0 == 0) tma_load_tiles_pol(v_addr(s), &smap, 9 * sc, 8 * cur.mb, cur.expert, &sh->full[s], wpol);
+          tma_load_rows(b_addr(s), &bmap, kTmK * c, cur.row0, &sh->full[s], apol);
+          tma_load_rows(b_addr(s) + kTcMaxN * 128, &bmap, kTmK * c + kTcK, cur.row0, &sh->full[s], apol);
         }
       }
       if (*abort) {  // let this warp's copies in flight land before the CTA exits (bounded waits)
@@ -1443,7 +1487,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 int tc_group(int mblocks) { return mblocks % 4 == 0 ? 4 : (mblocks % 2 == 0 ? 2 : 1); }
 
 cudaError_t tc_make_tile_map(void* map, const uint8_t* region, int n_experts, int tiles,
-                             uint64_t tile_bytes, uint64_t expert_bytes, int box_tiles) {
+                             uint64_t tile_bytes, uint64_t expert_bytes, int box_tiles, int box_pieces) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -1454,11 +1498,12 @@ cudaError_t tc_make_tile_map(void* map, const uint8_t* region, int n_experts, in
     if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  // [expert][tile][512-byte piece][64 x 8 bytes]; a box: one piece of box_tiles consecutive tiles
+  // [expert][tile][512-byte piece][64 x 8 bytes]; a box: box_pieces consecutive
+  // pieces of box_tiles consecutive tiles
   const cuuint64_t dims[4] = {64, (cuuint64_t)(tile_bytes / 512), (cuuint64_t)tiles,
                               (cuuint64_t)n_experts};
   const cuuint64_t strides[3] = {512, tile_bytes, expert_bytes};
-  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tiles, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_pieces, (cuuint32_t)box_tiles, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT64, 4,
                             const_cast<uint8_t*>(region), dims, strides, box, estr,
@@ -1612,22 +1657,26 @@ cudaError_t launch_gather_rows(const ExpertParams& p, int rows, uint16_t* xs, cu
   return launch_k(gather_rows_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, st, true, p, rows, xs);
 }
 
-cudaError_t launch_tc_tm_gateup(const ExpertParams& p, int items, const void* tile_map,
-                                const void* xmap, cudaStream_t st) {
+bool tc_tm_ok(int H, int I) { return H % kTmK == 0 && I % kTmK == 0; }
+
+cudaError_t launch_tc_tm_gateup(const ExpertParams& p, int items, const void* code_map,
+                                const void* scale_map, const void* xmap, cudaStream_t st) {
   const int mblocks = (2 * p.I) / kTcM;
-  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  const CUtensorMap& cm = *reinterpret_cast<const CUtensorMap*>(code_map);
+  const CUtensorMap& sm = *reinterpret_cast<const CUtensorMap*>(scale_map);
   const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(xmap);
   return launch_k(tc_tmem_kernel<0>, dim3(fq_grid(mblocks * items)), dim3(kTmThreads),
-                  tm_smem_bytes(), st, true, p, map, bm, items);
+                  tm_smem_bytes(), st, true, p, cm, sm, bm, items);
 }
 
-cudaError_t launch_tc_tm_down(const ExpertParams& p, int items, const void* tile_map,
-                              const void* amap, cudaStream_t st) {
+cudaError_t launch_tc_tm_down(const ExpertParams& p, int items, const void* code_map,
+                              const void* scale_map, const void* amap, cudaStream_t st) {
   const int mblocks = p.H / kTcM;
-  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(tile_map);
+  const CUtensorMap& cm = *reinterpret_cast<const CUtensorMap*>(code_map);
+  const CUtensorMap& sm = *reinterpret_cast<const CUtensorMap*>(scale_map);
   const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(amap);
   return launch_k(tc_tmem_kernel<1>, dim3(fq_grid(mblocks * items)), dim3(kTmThreads),
-                  tm_smem_bytes(), st, true, p, map, bm, items);
+                  tm_smem_bytes(), st, true, p, cm, sm, bm, items);
 }
 
 bool tc_router_ok(int E, int H) { return E % kTcM == 0 && H % kTcK == 0; }

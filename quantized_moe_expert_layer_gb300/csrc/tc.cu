@@ -114,6 +114,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 
 struct TcShared {
   uint64_t full[kTcStages];
@@ -1105,56 +1108,68 @@ __global__ void __launch_bounds__(kFqThreads, 1)
 // b_desc), so only the token rows pass through shared memory.
 //
 // Persistent like tc_fp4_kernel: a CTA per SM walks units (work item, 128-row
-// M-block), its unit list in shared memory; a ring of kTmNS stages of 128
-// columns of K (each with its own 64-column A slot in TMEM) runs across units,
-// and the accumulators are double-buffered.  Per stage:
-//   * one of two TMA warps (even and odd stages: a single issuing thread
-//     keeps too few copies in flight) loads the M-block's code vectors of the
-//     stage's two 64-column chunks (one box of the arena's tile map: the same
-//     two 512-byte pieces of 8 consecutive 16-row tiles, 8 KB), at the first
-//     chunk of a super-chunk also the tiles' scale vectors (4 KB), and the
-//     stage's 128 columns of the item's 128 token rows (two 16 KB boxes,
-//     128B-swizzled: the K-major layout the MMA reads) from rows in slot
-//     order: x gathered into them by
-//     gather_rows_kernel (gate/up), or a (down); rows past the item's tokens
-//     belong to other items and only reach accumulator columns the epilogue
-//     never reads;
-//   * producer warps 0-7 (warp w: TMEM lane quadrant w % 4, columns 32(w / 4)
-//     .. +31 of each chunk) rebuild their row's codes from the tile's fragment
-//     order (one byte permute per 8 codes), convert and scale them to f16 and
-//     store 2 x 16 TMEM columns, then arrive once per warp;
-//   * the MMA thread (warp 16) issues the stage's 8 MMAs (K = 16 each) and
-//     commits the stage (its shared memory and its A slot) back: the thread's
-//     waits and commit per stage cost about as much as 4 MMAs, so a stage
-//     carries 8;
-//   * epilogue warps 8-15 read a finished unit's accumulators (SwiGLU into a,
-//     or y rows) and hand the buffer back.
-constexpr int kTmThreads = 32 * 19;
-constexpr int kTmEpi0 = 8;                     // epilogue warps 8-15
-constexpr int kTmMmaWarp = 16, kTmTmaWarp = 17;  // TMA warps 17 (even stages) and 18 (odd)
-static_assert(32 * (kTmTmaWarp + 2) == kTmThreads, "warp roles");
+// M-block), its unit list in shared memory.  One thread issuing MMAs into one
+// accumulator reaches a fraction of the tensor core's rate (each further
+// issuing thread with its own accumulator adds about as much again), so the
+// CTA runs two pipelines: pipeline q takes the CTA's units q, q + 2, ..., with
+// its own MMA thread, accumulator (128 TMEM columns), two TMA warps, four
+// producer warps, a ring of kTmNB token-row stages of 128 columns of K (each
+// with a 64-column A slot in TMEM) and a deeper ring of kTmNC code stages, so
+// that the codes (from HBM) and their conversion run ahead of the token rows
+// and off the path that sets the stage rate.  The epilogue warps serve both
+// pipelines, unit after unit, so one pipeline's epilogue overlaps the other's
+// MMAs.  Per stage of a pipeline:
+//   * its code TMA warp loads the M-block's code vectors of the stage's two
+//     64-column chunks (one box of the arena's tile map: the same two 512-byte
+//     pieces of 8 consecutive 16-row tiles, 8 KB), at the first chunk of a
+//     super-chunk also the tiles' scale vectors (4 KB);
+//   * its row TMA warp loads the stage's 128 columns of the item's 128 token
+//     rows (two 16 KB boxes, 128B-swizzled: the K-major layout the MMA reads)
+//     from rows in slot order: x gathered into them by gather_rows_kernel
+//     (gate/up), or a (down); rows past the item's tokens belong to other
+//     items and only reach accumulator columns the epilogue never reads;
+//   * its producer warps (warp w: TMEM lane quadrant w % 4) rebuild their
+//     row's codes from the tile's fragment order (one byte permute per 8
+//     codes), convert and scale them to f16 and store 64 TMEM columns, then
+//     arrive once per warp;
+//   * its MMA thread issues the stage's 8 MMAs (K = 16 each) and commits the
+//     stage (its shared memory and its A slot) back;
+//   * epilogue warps 8-15 read a finished unit's accumulator (SwiGLU into a,
+//     or y rows) and hand it back to its pipeline.
+constexpr int kTmPipes = 2;                        // pipelines (MMA issuers)
+constexpr int kTmProd = 4;                         // producer warps per pipeline
+constexpr int kTmEpi0 = kTmPipes * kTmProd;        // epilogue warps 8-15
+constexpr int kTmMmaWarp = kTmEpi0 + 8;            // MMA warps 16 + q
+constexpr int kTmTmaWarp = kTmMmaWarp + kTmPipes;  // TMA warps: token rows 18 + q, codes 20 + q
+constexpr int kTmThreads = 32 * (kTmTmaWarp + 2 * kTmPipes);
 constexpr int kTmK = 128;                      // K per stage: two 64-column chunks
-constexpr int kTmNS = 4;                       // stages in flight (and A slots)
+constexpr int kTmNB = 2;                       // token-row stages (and A slots) per pipeline
+constexpr int kTmNC = 3;                       // code stages per pipeline
 constexpr int kTmB = 2 * kTcMaxN * 128;        // token rows of a stage: 2 x (128 rows x 64 f16)
 constexpr int kTmCodes = 2 * 8 * 512;          // two 512-byte pieces of 8 tiles
 constexpr int kTmScales = 8 * 512;             // the scale vectors of 8 tiles
-constexpr int kTmStage = kTmB + kTmCodes + kTmScales;  // token rows, code vectors, scale vectors
-constexpr uint32_t kTmACol = 256;              // A slots (64 columns each) after two accumulators
-static_assert(kTmACol + 64 * kTmNS <= 512, "tensor memory columns");
-static_assert(kTmStage % 1024 == 0, "stages stay 1024-byte aligned");
+constexpr int kTmCStage = kTmCodes + kTmScales;
+constexpr uint32_t kTmACol = 256;              // A slots (64 columns each) after the two accumulators
+static_assert(kTmACol + 64 * kTmPipes * kTmNB <= 512, "tensor memory columns");
+static_assert(kTmB % 1024 == 0 && kTmCStage % 1024 == 0, "stages stay 1024-byte aligned");
 
 struct TmShared {
-  uint64_t full[kTmNS];   // the stage's codes (+ scales) and token rows landed (transaction bytes)
-  uint64_t afull[kTmNS];  // the stage's A slot is written (8 producer warps)
-  uint64_t empty[kTmNS];  // the MMAs reading the stage and its A slot are done
-  uint64_t acc_full[2], acc_empty[2];
-  uint64_t fin;
+  uint64_t bfull[kTmPipes * kTmNB];   // the stage's token rows landed (transaction bytes)
+  uint64_t afull[kTmPipes * kTmNB];   // the stage's A slot is written (the pipeline's producer warps)
+  uint64_t empty[kTmPipes * kTmNB];   // the MMAs reading the token rows and the A slot are done
+  uint64_t cfull[kTmPipes * kTmNC];   // the stage's codes (+ scales) landed (transaction bytes)
+  uint64_t cempty[kTmPipes * kTmNC];  // the producers have read them
+  uint64_t acc_full[kTmPipes], acc_empty[kTmPipes];
+  uint64_t fin[kTmPipes];
   uint32_t tmem_base;
   int abort;
 };
 
+constexpr int kTmStaging = 8 * 1024;  // the epilogue warps' a tiles (gate/up): 32 columns x 16 rows of f16 each
+constexpr size_t kTmRings = (size_t)kTmPipes * (kTmNB * kTmB + kTmNC * kTmCStage);
+
 __host__ __device__ constexpr size_t tm_smem_bytes() {
-  return 1024 + (size_t)kTmNS * kTmStage + sizeof(TmShared) + 16 + 16 * kFqList;
+  return 1024 + kTmRings + kTmStaging + sizeof(TmShared) + 16 + 16 * kFqList;
 }
 
 // 4-D tiled TMA load of the tile map box at (0, piece, tile, expert) with an L2 policy
@@ -1169,13 +1184,16 @@ __device__ __forceinline__ void tma_load_tiles_pol(uint32_t dst, const CUtensorM
 }
 
 
-// 32 TMEM lanes (one per thread of the warp) x 16 consecutive 32-bit columns
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+// 32 TMEM lanes (one per thread of the warp) x 32 consecutive 32-bit columns
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -1238,31 +1256,35 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   extern __shared__ __align__(1024) uint8_t tm_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tm_smem_raw) + 1023) & ~(uintptr_t)1023);
-  TmShared* sh = reinterpret_cast<TmShared*>(base + kTmNS * kTmStage);
+  TmShared* sh = reinterpret_cast<TmShared*>(base + kTmRings + kTmStaging);
   int4* list = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(sh + 1) + 15) & ~(uintptr_t)15);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = p.T * p.k;
   const int K = MODE == 1 ? p.I : p.H;
   const int KC = K / kTmK;  // stages per unit
   const int mblocks = (MODE == 1 ? p.H : 2 * p.I) / kTcM;
   const int items = min(p.nsh_tc + *p.n_tc_entries, max_items);
   const int n_units = mblocks * max(items, 0);
   const uint32_t s0 = smem_u32(base);
-  auto b_addr = [&](int s) { return s0 + s * kTmStage; };  // 1024-byte aligned
-  auto c_addr = [&](int s) { return s0 + s * kTmStage + kTmB; };  // [tile][piece 0..1][512 B]
-  auto v_addr = [&](int s) { return s0 + s * kTmStage + kTmB + kTmCodes; };
+  // token-row slot r = q * kTmNB + b; code slot r = q * kTmNC + c (all 1024-byte aligned)
+  auto b_addr = [&](int r) { return s0 + r * kTmB; };
+  auto c_addr = [&](int r) { return s0 + kTmPipes * kTmNB * kTmB + r * kTmCStage; };  // [tile][piece 0..1][512 B]
+  auto v_addr = [&](int r) { return c_addr(r) + kTmCodes; };  // [tile][512 B]
 
   if (tid == 0) {
-    for (int i = 0; i < kTmNS; ++i) {
-      mbar_init(&sh->full[i], 1);
-      mbar_init(&sh->afull[i], 8);  // the 8 producer warps
+    for (int i = 0; i < kTmPipes * kTmNB; ++i) {
+      mbar_init(&sh->bfull[i], 1);
+      mbar_init(&sh->afull[i], kTmProd);  // the pipeline's producer warps
       mbar_init(&sh->empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTmPipes * kTmNC; ++i) {
+      mbar_init(&sh->cfull[i], 1);
+      mbar_init(&sh->cempty[i], kTmProd);
+    }
+    for (int i = 0; i < kTmPipes; ++i) {
       mbar_init(&sh->acc_full[i], 1);
       mbar_init(&sh->acc_empty[i], 8);  // the 8 epilogue warps
+      mbar_init(&sh->fin[i], 1);
     }
-    mbar_init(&sh->fin, 1);
     sh->abort = 0;
     mbar_init_fence();
   }
@@ -1284,55 +1306,62 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_d = sh->tmem_base;
   volatile int* abort = &sh->abort;
+  // (every role walks the CTA's units in the same order; uk counts the units
+  // with tokens, and unit uk belongs to pipeline uk % 2)
 
   if (warp < kTmEpi0) {
     // ---------------------------------------------------------------- producers: A into TMEM
     // row r of the M-block = TMEM lane r: tile r / 16, row g or g + 8 of it
-    const int q = warp & 3, h = warp >> 2;
-    const int r = 32 * q + lane, tile = r >> 4, g8 = lane & 7, hi = (lane >> 3) & 1;
+    const int q = warp / kTmProd, qd = warp & 3;
+    const int r = 32 * qd + lane, tile = r >> 4, g8 = lane & 7, hi = (lane >> 3) & 1;
     const uint32_t sel = hi ? 0x7531u : 0x6420u;
-    // the lanes (g8, 2h) and (g8, 2h + 1) of the tile's vectors: this row's
-    // 16-column blocks 2h and 2h + 1 of every chunk (scales: byte 2j + hi)
-    const uint32_t loff = (uint32_t)(16 * (4 * g8 + 2 * h));
-    const uint32_t tdst = tmem_d + ((uint32_t)(32 * q) << 16) + kTmACol + 16 * h;
-    uint4 sv0 = make_uint4(0, 0, 0, 0), sv1 = sv0;
-    int gs = 0;
+    // the lanes (g8, t) of the tile's vectors hold this row's 16-column block t
+    // of every chunk (scales: byte 2j + hi of the scale vector, chunk j)
+    const uint32_t loff = (uint32_t)(tile * 512 + 64 * g8);
+    const uint32_t tdst = tmem_d + ((uint32_t)(32 * qd) << 16) + kTmACol;
+    uint4 sv[4];  // the super-chunk's scale vectors of lanes (g8, 0..3)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) sv[t] = make_uint4(0, 0, 0, 0);
+    int gs = 0, uk = 0;
     FqUnit cur;
     bool ok = true;
     for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
       if (cur.n == 0) continue;
+      if ((uk++ & 1) != q) continue;
       for (int c = 0; c < KC; ++c, ++gs) {
-        const int s = gs % kTmNS, j0 = 2 * (c & 3);  // chunks j0, j0 + 1 of the super-chunk
-        const uint32_t ph = (gs / kTmNS) & 1;
-        // the stage's copies landed; the MMAs that last read the A slot are done
-        // (the TMA warp waited for them before these copies)
-        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh->full[s], ph, abort, p.wait_budget) &&
-                                          mbar_wait_fast(&sh->empty[s], ph ^ 1, abort, p.wait_budget))) {
+        const int rb = q * kTmNB + gs % kTmNB, rc = q * kTmNC + gs % kTmNC;
+        const int j0 = 2 * (c & 3);  // chunks j0, j0 + 1 of the super-chunk
+        // the stage's codes landed; the MMAs that last read the A slot are done
+        if (!__all_sync(0xffffffffu, mbar_wait_fast(&sh->cfull[rc], (gs / kTmNC) & 1, abort, p.wait_budget) &&
+                                          mbar_wait_fast(&sh->empty[rb], ((gs / kTmNB) & 1) ^ 1, abort,
+                                                         p.wait_budget))) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (j0 == 0) {  // the super-chunk's scale vectors, kept for its 8 chunks
-          sv0 = lds128(v_addr(s) + tile * 512 + loff);
-          sv1 = lds128(v_addr(s) + tile * 512 + loff + 16);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) sv[t] = lds128(v_addr(rc) + loff + 16 * t);
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {  // the stage's two chunks
-          const uint32_t ca = c_addr(s) + tile * 1024 + hh * 512 + loff;
-          const uint4 cv0 = lds128(ca), cv1 = lds128(ca + 16);
           const int sb = 2 * (j0 + hh) + hi;
-          const uint32_t e0 = (u4get(sv0, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
-          const uint32_t e1 = (u4get(sv1, sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
-          const uint32_t sp = e4m3x2_to_f16x2(e0 | (e1 << 8));
-          uint32_t v[16];
-          tm_block(cv0, sel, dup_lo(sp), v);
-          tm_block(cv1, sel, dup_hi(sp), v + 8);
-          tmem_st16(tdst + 64 * s + 32 * hh, v);
+          uint32_t v[32];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {  // 16-column block t: TMEM columns 8t .. 8t + 7 of the chunk
+            const uint4 cv = lds128(c_addr(rc) + tile * 1024 + hh * 512 + 64 * g8 + 16 * t);
+            const uint32_t e = (u4get(sv[t], sb >> 2) >> (8 * (sb & 3))) & 0xFFu;
+            const uint32_t sp = e4m3x2_to_f16x2(e | (e << 8));
+            tm_block(cv, sel, sp, v + 8 * t);
+          }
+          tmem_st32(tdst + 64 * rb + 32 * hh, v);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->cempty[rc]);  // (every lane's code reads are done)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->afull[s]);
+        if (lane == 0) mbar_arrive(&sh->afull[rb]);
       }
     }
   } else if (warp < kTmMmaWarp) {
@@ -1340,27 +1369,16 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     // warp 8 + 4h + q: TMEM lane quadrant q (rows 32q..32q+31), columns 64h..64h+63
     const int qd = warp & 3, ch = (warp - kTmEpi0) >> 2;
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
-    auto tok = [&](const FqUnit& w, int r) -> size_t {
-      return (size_t)(w.expert == p.E ? w.row0 - S + r : p.row_token[w.row0 + r]);
-    };
+    const uint32_t tile = s0 + (uint32_t)kTmRings + (warp - kTmEpi0) * 1024;
     FqUnit cur;
     int uk = 0;
     for (int i = 0; fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
       if (cur.n == 0) continue;
-      const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+      const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;  // (the unit's pipeline)
       // the unit's tensor scales, read before the accumulator wait (an L2 round
       // trip under this load takes about a microsecond)
       const float ts_g = p.tscale[cur.expert * 3 + (MODE == 1 ? 2 : 0)];
       const float ts_u = MODE == 0 ? p.tscale[cur.expert * 3 + 1] : 0.0f;
-      float sc_lane[2] = {1.0f, 1.0f};  // W4A4 (activations quantised): the columns' scales
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col = 64 * ch + 32 * c + lane;
-        if (col < cur.n) {
-          if (MODE == 0 && p.ts_x) sc_lane[c] = p.ts_x[tok(cur, col)];
-          if (MODE == 1 && p.ts_a) sc_lane[c] = p.ts_a[cur.row0 + col];
-        }
-      }
       if (!mbar_wait_sleep(&sh->acc_full[buf], (uk >> 1) & 1, abort, p.wait_budget)) break;
       tc_fence_after();
       const uint32_t acc = tmem_d + lane_addr + (uint32_t)(128 * buf);
@@ -1372,28 +1390,37 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         tmem_ld32(acc + c0, v);
         if (MODE == 0) {
           // lanes 0-15 hold gate rows, 16-31 the matching up rows: lane l < 16
-          // computes columns 0-15 of its row, lane l + 16 columns 16-31
-          const int i = 16 * (4 * cur.mb + qd) + (lane & 15);
+          // computes columns 0-15 of its row, lane l + 16 columns 16-31.  The
+          // f16 values go through the warp's tile [32 columns][16 rows of a],
+          // so that a store instruction writes 16 columns x 32 bytes of a.
           const bool hi = lane >= 16;
+          bool bad = false;
 #pragma unroll
           for (int qq = 0; qq < 16; ++qq) {
             const float lo_v = __uint_as_float(v[qq]), hi_v = __uint_as_float(v[16 + qq]);
             const float recv = __shfl_xor_sync(0xffffffffu, hi ? lo_v : hi_v, 16);
             const int cq = hi ? 16 + qq : qq;
             const float gv = hi ? recv : lo_v, uv = hi ? hi_v : recv;
-            const float sx = __shfl_sync(0xffffffffu, sc_lane[c], cq);
-            const int col = c0 + cq;
-            if (col < cur.n) {
-              const float Gv = (ts_g * sx) * gv, U = (ts_u * sx) * uv;
-              const float a = Gv / (1.0f + expf(-Gv)) * U;
-              if (p.af)
-                p.af[(size_t)(cur.row0 + col) * p.I + i] = a;
-              else
-                p.abuf[(size_t)(cur.row0 + col) * p.I + i] = a_to_f16(a, p.status);
-            }
+            const float Gv = ts_g * gv, U = ts_u * uv;
+            const float a = Gv / (1.0f + expf(-Gv)) * U;
+            const uint16_t h = __half_as_ushort(__float2half_rn(a));
+            bad |= f16_nonfinite(h);
+            st_shared_u16(tile + cq * 32 + (lane & 15) * 2, h);
           }
+          if (bad) *p.status = kStatusRange;
+          __syncwarp();
+          // lane j: column 16g + j / 2 of the chunk, rows 8 (j % 2) .. + 7 of the 16
+          const int i0 = 16 * (4 * cur.mb + qd);
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int cq = 16 * g + (lane >> 1), col = c0 + cq;
+            const uint4 w = lds128(tile + cq * 32 + (lane & 1) * 16);
+            if (col < cur.n)
+              *reinterpret_cast<uint4*>(p.abuf + (size_t)(cur.row0 + col) * p.I + i0 + 8 * (lane & 1)) = w;
+          }
+          __syncwarp();  // (the next chunk rewrites the tile)
         } else {
-          store_y_chunk(p, v, cur.row0, c0, cur.n, kTcM * cur.mb + 32 * qd, ts_g, sc_lane[c]);
+          store_y_chunk(p, v, cur.row0, c0, cur.n, kTcM * cur.mb + 32 * qd, ts_g, 1.0f);
         }
       }
       tc_fence_before();
@@ -1401,72 +1428,83 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
       ++uk;
     }
-  } else if (warp == kTmMmaWarp) {
+  } else if (warp < kTmTmaWarp) {
+    const int q = warp - kTmMmaWarp;
     if (lane == 0) {
-      // ---------------------------------------------------------------- MMA issue
+      // ---------------------------------------------------------------- MMA issue (pipeline q)
       FqUnit cur;
       int gs = 0, uk = 0;
       bool ok = true;
       for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
         if (cur.n == 0) continue;
-        const int n_pad = (cur.n + 15) & ~15, buf = uk & 1;
+        const int me = uk++;
+        if ((me & 1) != q) continue;
+        const int n_pad = (cur.n + 15) & ~15;
         const uint32_t idesc = idesc_f16(kTcM, n_pad);
-        // the epilogue of the unit before the previous one has read this accumulator
-        if (!mbar_wait_fast(&sh->acc_empty[buf], ((uk >> 1) & 1) ^ 1, abort, p.wait_budget)) break;
+        // the epilogue has read this pipeline's accumulator (its previous unit)
+        if (!mbar_wait_fast(&sh->acc_empty[q], ((me >> 1) & 1) ^ 1, abort, p.wait_budget)) break;
         tc_fence_after();
         for (int c = 0; c < KC; ++c, ++gs) {
-          const int s = gs % kTmNS;
-          const uint32_t ph = (gs / kTmNS) & 1;
-          if (!mbar_wait_fast(&sh->afull[s], ph, abort, p.wait_budget) ||
-              !mbar_wait_fast(&sh->full[s], ph, abort, p.wait_budget)) {
+          const int rs = q * kTmNB + gs % kTmNB;
+          const uint32_t ph = (gs / kTmNB) & 1;
+          if (!mbar_wait_fast(&sh->afull[rs], ph, abort, p.wait_budget) ||
+              !mbar_wait_fast(&sh->bfull[rs], ph, abort, p.wait_budget)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t bd = sw128_desc(b_addr(s));
-          const uint32_t a0 = tmem_d + kTmACol + 64 * s;
+          const uint64_t bd = sw128_desc(b_addr(rs));
+          const uint32_t a0 = tmem_d + kTmACol + 64 * rs;
 #pragma unroll
           for (int kk = 0; kk < kTmK / 16; ++kk)  // A: +8 columns per K-step of 16; B: +32 bytes
             // within a 64-column box, the second box 16 KB on
-            umma_f16_tmem_a(tmem_d + 128 * buf, a0 + 8 * kk, bd + 2 * (kk & 3) + (kk >> 2) * (kTcMaxN * 128 >> 4),
+            umma_f16_tmem_a(tmem_d + 128 * q, a0 + 8 * kk, bd + 2 * (kk & 3) + (kk >> 2) * (kTcMaxN * 128 >> 4),
                             idesc, (c | kk) != 0);
-          umma_commit(&sh->empty[s]);
+          umma_commit(&sh->empty[rs]);
         }
-        if (ok) umma_commit(&sh->acc_full[buf]);
-        ++uk;
+        if (ok) umma_commit(&sh->acc_full[q]);
       }
-      umma_commit(&sh->fin);  // every MMA issued before TMEM is freed
-      mbar_drain(&sh->fin, 0);
+      umma_commit(&sh->fin[q]);  // every MMA issued before TMEM is freed
+      mbar_drain(&sh->fin[q], 0);
     }
     __syncwarp();
   } else {
+    const int q = (warp - kTmTmaWarp) % kTmPipes;
+    const bool rows = warp < kTmTmaWarp + kTmPipes;  // token rows, else codes
     if (lane == 0) {
-      // ---------------------------------------------------------------- TMA issue
+      // ---------------------------------------------------------------- TMA issue (pipeline q)
       const CUtensorMap* map = &tmap;
       const uint64_t wpol = l2_evict_first(), apol = l2_evict_last();
-      const int tw = warp - kTmTmaWarp;  // this warp's stages: gs % 2 == tw
-      int gs = 0;
+      const int depth = rows ? kTmNB : kTmNC;
+      uint64_t* full = rows ? sh->bfull + q * kTmNB : sh->cfull + q * kTmNC;
+      uint64_t* empty = rows ? sh->empty + q * kTmNB : sh->cempty + q * kTmNC;
+      int gs = 0, uk = 0;
       FqUnit cur;
       bool ok = true;
       for (int i = 0; ok && fq_unit(p, list, i, n_units, mblocks, cur); ++i) {
         if (cur.n == 0) continue;
+        if ((uk++ & 1) != q) continue;
         for (int c = 0; c < KC; ++c, ++gs) {
-          if ((gs & 1) != tw) continue;
-          const int s = gs % kTmNS, j0 = 2 * (c & 3), sc = c >> 2;
-          if (!mbar_wait(&sh->empty[s], ((gs / kTmNS) & 1) ^ 1, abort, p.wait_budget)) {
+          const int slot = gs % depth, j0 = 2 * (c & 3), sc = c >> 2;
+          if (!mbar_wait(&empty[slot], ((gs / depth) & 1) ^ 1, abort, p.wait_budget)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect(&sh->full[s], (uint32_t)(kTmCodes + kTmB) + (j0 == 0 ? (uint32_t)kTmScales : 0u));
-          tma_load_tiles_pol(c_addr(s), map, 9 * sc + 1 + j0, 8 * cur.mb, cur.expert, &sh->full[s], wpol);
-          if (j0 == 0) tma_load_tiles_pol(v_addr(s), &smap, 9 * sc, 8 * cur.mb, cur.expert, &sh->full[s], wpol);
-          tma_load_rows(b_addr(s), &bmap, kTmK * c, cur.row0, &sh->full[s], apol);
-          tma_load_rows(b_addr(s) + kTcMaxN * 128, &bmap, kTmK * c + kTcK, cur.row0, &sh->full[s], apol);
+          if (rows) {
+            const uint32_t dst = b_addr(q * kTmNB + slot);
+            mbar_arrive_expect(&full[slot], (uint32_t)kTmB);
+            tma_load_rows(dst, &bmap, kTmK * c, cur.row0, &full[slot], apol);
+            tma_load_rows(dst + kTcMaxN * 128, &bmap, kTmK * c + kTcK, cur.row0, &full[slot], apol);
+          } else {
+            const int r = q * kTmNC + slot;
+            mbar_arrive_expect(&full[slot], (uint32_t)kTmCodes + (j0 == 0 ? (uint32_t)kTmScales : 0u));
+            tma_load_tiles_pol(c_addr(r), map, 9 * sc + 1 + j0, 8 * cur.mb, cur.expert, &full[slot], wpol);
+            if (j0 == 0) tma_load_tiles_pol(v_addr(r), &smap, 9 * sc, 8 * cur.mb, cur.expert, &full[slot], wpol);
+          }
         }
       }
       if (*abort) {  // let this warp's copies in flight land before the CTA exits (bounded waits)
-        for (int c = (gs > kTmNS ? gs - kTmNS : 0); c < gs; ++c)
-          if ((c & 1) == tw) mbar_drain(&sh->full[c % kTmNS], (c / kTmNS) & 1);
+        for (int c = (gs > depth ? gs - depth : 0); c < gs; ++c) mbar_drain(&full[c % depth], (c / depth) & 1);
       }
     }
     __syncwarp();

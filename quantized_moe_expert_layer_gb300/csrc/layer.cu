@@ -482,7 +482,9 @@ int launch_quant_a(moe_layer* L, int T, cudaStream_t st) {
 int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t st) {
   ExpertParams ep = expert_params(L, x, T);
   ep.logits_out = L->partial;
-  if (!w4a4(L))  // (W4A4: the quantiser wrote the f16 copy before the router)
+  // (W4A4: the quantiser wrote the f16 copy before the router; the GEMMs with
+  // the weights in tensor memory convert x while gathering its rows)
+  if (!w4a4(L) && !tm_path(L, T))
     CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
   CK("tensor-core router kernel launch", launch_tc_router(ep, st));
   return MOE_OK;
@@ -545,7 +547,9 @@ int forward_launches(moe_layer* L, int T) {
   // top-k + dispatch: one kernel (T <= 16, or the fused one), else top-k then dispatch
   const int topk_disp = topk_dispatch_ok(T, L->k, L->E) ? 1 : 1 + dispatch;
   const int routing = tc_router(L, T) ? 2 + topk_disp : (T <= kFusedTopkMaxT ? 2 : 1 + topk_disp);
-  if (tc_path(L, T)) return routing + 3 + q + (tm_path(L, T) ? 1 : 0);  // (+ the row gather)
+  // (the GEMMs with the weights in tensor memory: + the row gather, which
+  // replaces the x conversion before the tensor-core router)
+  if (tc_path(L, T)) return routing + 3 + q + (tm_path(L, T) && !tc_router(L, T) ? 1 : 0);
   return routing + (fused_down(L, T) ? 2 : 3) + q;
 }
 
@@ -1040,7 +1044,7 @@ int moe_forward_routed(moe_layer* L, const uint16_t* x, int T, const int32_t* id
      cudaMemcpyAsync(L->gates, gates, S * 4, cudaMemcpyDeviceToDevice, st));
   if (w4a4(L)) {
     if (!fq_path(L, T) && (rc = launch_quant_x(L, x, T, st))) return rc;
-  } else {
+  } else if (!tm_path(L, T)) {
     CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
   }
   RouteParams rp = route_params(L, x, T);

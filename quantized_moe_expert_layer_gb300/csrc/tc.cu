@@ -1229,9 +1229,10 @@ __device__ __forceinline__ void tm_block(const uint4& cv, uint32_t sel, uint32_t
   for (int k = 0; k < 4; ++k) out[4 + k] = hmul2(hh[k], sc);
 }
 
-// The token rows of the gate/up GEMM in slot order: row r of xs = the f16 copy
-// of x's row of token row_token[r] (r < T*k), or of token r - T*k (the shared
-// expert's rows); a warp per row.
+// The token rows of the gate/up GEMM in slot order: row r of xs = x's row of
+// token row_token[r] (r < T*k), or of token r - T*k (the shared expert's
+// rows), converted from bf16 to f16 (exact for |x| in [2^-14, 65504]; an
+// element beyond 65504, or not finite, records MOE_ERANGE); a warp per row.
 __global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int rows, uint16_t* xs) {
   griddep_wait();
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -1242,9 +1243,22 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int ro
     if (lane == 0) *p.status = kStatusInvalid;
     return;
   }
-  const uint4* src = reinterpret_cast<const uint4*>(p.xh + (size_t)t * p.H);
+  const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * p.H);
-  for (int v = lane; v < p.H / 8; v += 32) dst[v] = src[v];
+  bool bad = false;
+  for (int v = lane; v < p.H / 8; v += 32) {
+    const uint4 raw = src[v];
+    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16), __uint_as_float(in[q] & 0xFFFF0000u));
+      o[q] = *reinterpret_cast<const uint32_t*>(&h);
+      bad |= f16x2_nonfinite(o[q]);
+    }
+    dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (bad) *p.status = kStatusRange;
 }
 
 template <int MODE>

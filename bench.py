@@ -551,7 +551,7 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
                     "note": "bytes: the touched experts' packed gate/up tiles, x's NVFP4 codes "
                             "and scales, a written in fp32 for its quantiser"}
     elif tc:
-        kname = "tc_expert_kernel"
+        kname = "tc_tmem_kernel" if w.H % 128 == 0 and w.I % 128 == 0 else "tc_expert_kernel"
         peak, peak_kind = peaks("tensor")
         achieved = work / (k_us * 1e-6) / 1e12
         pw = sum(padded) / len(padded)

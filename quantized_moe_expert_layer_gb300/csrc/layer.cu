@@ -422,9 +422,14 @@ bool tm_path(moe_layer* L, int T) {
   return !w4a4(L) && tc_path(L, T) && L->tm_maps_ok && L->rows_maps_ok;
 }
 
+// x's rows in slot order (the gate/up GEMM's token rows), after the dispatch
+int launch_row_gather(moe_layer* L, const ExpertParams& ep, int T, cudaStream_t st) {
+  CK("row gather kernel launch", launch_gather_rows(ep, T * L->k + (L->shared ? T : 0), xs_rows(L), st));
+  return MOE_OK;
+}
+
 int launch_tm_gateup(moe_layer* L, const ExpertParams& ep, int T, cudaStream_t st) {
   const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
-  CK("row gather kernel launch", launch_gather_rows(ep, T * L->k + (L->shared ? T : 0), xs_rows(L), st));
   CK("tensor-core gate/up kernel launch",
      launch_tc_tm_gateup(ep, gy, L->map_gu8, L->map_gu8s, L->map_xs, st));
   return MOE_OK;
@@ -507,7 +512,8 @@ int run_experts(moe_layer* L, const uint16_t* x, int T, float* out, cudaStream_t
   if (tc_path(L, T)) {
     const int gy = ep.nsh_tc + max_tc_entries(T, L->E, L->k);
     if (tm_path(L, T)) {
-      const int rc = launch_tm_gateup(L, ep, T, st);
+      int rc = launch_row_gather(L, ep, T, st);
+      if (!rc) rc = launch_tm_gateup(L, ep, T, st);
       if (rc) return rc;
     } else {
       CK("tensor-core gate/up kernel launch", launch_tc_gateup(ep, gy, L->map_gu, st));
@@ -1200,10 +1206,13 @@ int moe_debug_run_phase(moe_layer* L, int phase, const uint16_t* x, int T, float
       } else if ((rc = launch_topk_and_dispatch(L, rp, T, false, st))) {
         return rc;
       }
-      break;
-    case 2:
+      // the token rows in slot order for the tensor-core GEMMs (a4 gather): x
+      // gathered (W4A16), or quantised into its rows (W4A4)
+      if (tm_path(L, T) && (rc = launch_row_gather(L, ep, T, st))) return rc;
       if (fq_path(L, T) && ((rc = refresh_mma(L, st)) || (rc = launch_quant_x_rows(L, x, T, st))))
         return rc;
+      break;
+    case 2:
       if (fq_path(L, T))
         CK("gate/up", launch_tc_fp4_gateup(ep, ep.nsh_tc + max_tc_entries(T, L->E, L->k), L->map_gu_mma,
                                            L->map_bx_c, L->map_bx_s, st));

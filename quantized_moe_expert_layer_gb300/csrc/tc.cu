@@ -1500,7 +1500,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         if ((uk++ & 1) != q) continue;
         for (int c = 0; c < KC; ++c, ++gs) {
           const int slot = gs % depth, j0 = 2 * (c & 3), sc = c >> 2;
-          if (!mbar_wait(&empty[slot], ((gs / depth) & 1) ^ 1, abort, p.wait_budget)) {
+          if (!mbar_wait_sleep(&empty[slot], ((gs / depth) & 1) ^ 1, abort, p.wait_budget)) {
             ok = false;
             break;
           }

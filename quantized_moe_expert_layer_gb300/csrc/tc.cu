@@ -1418,7 +1418,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             const float Gv = ts_g * gv, U = ts_u * uv;
             const float a = Gv / (1.0f + expf(-Gv)) * U;
             const uint16_t h = __half_as_ushort(__float2half_rn(a));
-            bad |= f16_nonfinite(h);
+            // (columns past the item's tokens hold stale accumulators: never stored, never flagged)
+            bad |= c0 + cq < cur.n && f16_nonfinite(h);
             st_shared_u16(tile + cq * 32 + (lane & 15) * 2, h);
           }
           if (bad) *p.status = kStatusRange;

@@ -65,7 +65,8 @@ def test_tensor_core_path_small_layer(T):
     work items of up to 256 tokens."""
     w = small(fmt=1, H=256, I=128, E=8, k=2, T=T, seed=5)
     L = layer(w)
-    assert L.launches(T) == 5  # router, top-k + dispatch (one kernel), tc gate/up, tc down, combine
+    # router, top-k + dispatch (one kernel), row gather, tc gate/up, tc down, combine
+    assert L.launches(T) == 6
     compare_layer(w, L, gen.x_tokens(w, T))
 
 
@@ -79,7 +80,8 @@ def test_several_cta_dispatch_ragged_chunks(T):
     picks (compare_layer), the output on sampled tokens."""
     w = small(fmt=1, H=256, I=128, E=24, k=3, T=T, seed=9)
     L = layer(w)
-    assert L.launches(T) == 7  # router, top-k, count, scan + place, tc gate/up, tc down, combine
+    # router, top-k, count, scan + place, row gather, tc gate/up, tc down, combine
+    assert L.launches(T) == 8
     compare_layer(w, L, gen.x_tokens(w, T), sample=[0, 1, T // 2, T - 2, T - 1])
 
 
@@ -89,7 +91,8 @@ def test_tensor_core_router_small_layer(T):
     token tiles of 128 with a ragged last one), ahead of the grouped expert GEMMs."""
     w = small(fmt=1, H=256, I=128, E=128, k=2, T=T, seed=7)
     L = layer(w)
-    assert L.launches(T) == 7  # convert x, tc router, top-k, dispatch, tc gate/up, tc down, combine
+    # tc router, top-k, dispatch, row gather (with the x conversion), tc gate/up, tc down, combine
+    assert L.launches(T) == 7
     compare_layer(w, L, gen.x_tokens(w, T))
 
 
@@ -182,8 +185,8 @@ def test_deepseek_shape_mxfp4_prefill_sampled():
     w = gen.get_workload(7)
     L = build_layer(w, T_max=w.T)
     try:
-        # convert x, tc router, top-k, dispatch (count, scan + place: T*k > 8192), tc gate/up,
-        # tc down, combine
+        # tc router, top-k, dispatch (count, scan + place: T*k > 8192), row gather (with the x
+        # conversion), tc gate/up, tc down, combine
         assert L.launches(w.T) == 8
         sample = [0, 1, 100, 2047, 2048, 4095]
         rel, ties = compare_layer(w, L, gen.x_tokens(w), sample=sample, route_all=True)

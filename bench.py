@@ -529,7 +529,9 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
     def run_gateup():
         for L, o in zip(layers, outs):
             L.run_phase(2, x, o, stream=s)
-    k_us = graph_time_us(s, run_gateup, max(20, min(200, steps))) / Ln
+    # (30 replays, as the per-phase times: a seconds-long loop of the dense
+    # GEMM drops the SM clock under the power cap, which the sustained peak covers)
+    k_us = graph_time_us(s, run_gateup, 30) / Ln
     work = sum(per_launch) / len(per_launch)
     if tc and act:
         # the block-scaled FP4 GEMM: HBM-bound at these token counts (its FLOPs

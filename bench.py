@@ -529,6 +529,11 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
     def run_gateup():
         for L, o in zip(layers, outs):
             L.run_phase(2, x, o, stream=s)
+    # (the token rows in slot order again: on the W4A16 tensor-core path they
+    # share their buffer with y, which the last forward's down phase wrote)
+    with torch.cuda.stream(s):
+        for L, o in zip(layers, outs):
+            L.run_phase(1, x, o, stream=s)
     # (30 replays, as the per-phase times: a seconds-long loop of the dense
     # GEMM drops the SM clock under the power cap, which the sustained peak covers)
     k_us = graph_time_us(s, run_gateup, 30) / Ln

@@ -194,7 +194,8 @@ cudaError_t launch_tc_fp4_down(const ExpertParams& p, int items, const void* til
 // tc_make_rows16_map over x gathered into slot order (xs, written by
 // launch_gather_rows: rows = T*k + T) / the rows of a.  grid: a CTA per SM.
 cudaError_t tc_make_rows16_map(void* map, const uint16_t* base, size_t rows, int cols);
-cudaError_t launch_gather_rows(const ExpertParams& p, int rows, uint16_t* xs, cudaStream_t st);
+cudaError_t launch_gather_rows(const ExpertParams& p, int rows, uint16_t* xs, bool from_f16,
+                               cudaStream_t st);
 bool tc_tm_ok(int H, int I);
 cudaError_t launch_tc_tm_gateup(const ExpertParams& p, int items, const void* code_map,
                                 const void* scale_map, const void* xmap, cudaStream_t st);

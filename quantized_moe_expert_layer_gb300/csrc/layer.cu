@@ -197,6 +197,7 @@ struct moe_layer {
   size_t ws_bytes = 0;
   int last_T = 0;
   bool last_has_logits = false;
+  bool x_mapped = false;         // this forward's x is pinned host memory read in place
 };
 
 namespace {
@@ -424,7 +425,8 @@ bool tm_path(moe_layer* L, int T) {
 
 // x's rows in slot order (the gate/up GEMM's token rows), after the dispatch
 int launch_row_gather(moe_layer* L, const ExpertParams& ep, int T, cudaStream_t st) {
-  CK("row gather kernel launch", launch_gather_rows(ep, T * L->k + (L->shared ? T : 0), xs_rows(L), st));
+  CK("row gather kernel launch",
+     launch_gather_rows(ep, T * L->k + (L->shared ? T : 0), xs_rows(L), L->x_mapped, st));
   return MOE_OK;
 }
 
@@ -489,7 +491,9 @@ int launch_tc_routing_gemm(moe_layer* L, const uint16_t* x, int T, cudaStream_t 
   ep.logits_out = L->partial;
   // (W4A4: the quantiser wrote the f16 copy before the router; the GEMMs with
   // the weights in tensor memory convert x while gathering its rows)
-  if (!w4a4(L) && !tm_path(L, T))
+  // (x in mapped host memory: converted once here, and the gather copies the
+  // f16 rows instead of reading x over the link once per row)
+  if (!w4a4(L) && (!tm_path(L, T) || L->x_mapped))
     CK("x conversion kernel launch", launch_convert_x(x, L->xh, (long)T * L->H, L->status, st));
   CK("tensor-core router kernel launch", launch_tc_router(ep, st));
   return MOE_OK;
@@ -1020,8 +1024,10 @@ int moe_forward_host(moe_layer* L, const uint16_t* x_host, int T, float* out_hos
       ax.devicePointer && cudaPointerGetAttributes(&ao, out_host) == cudaSuccess &&
       ao.type == cudaMemoryTypeHost && ao.devicePointer &&
       !(((uintptr_t)ax.devicePointer | (uintptr_t)ao.devicePointer) & 15u)) {
+    L->x_mapped = true;
     rc = forward_impl(L, static_cast<const uint16_t*>(ax.devicePointer), T,
                       static_cast<float*>(ao.devicePointer), st);
+    L->x_mapped = false;
     if (rc) return rc;
     CK("moe_forward_host: synchronize", cudaStreamSynchronize(st));
     return MOE_OK;

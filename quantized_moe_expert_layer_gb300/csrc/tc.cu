@@ -1233,7 +1233,10 @@ __device__ __forceinline__ void tm_block(const uint4& cv, uint32_t sel, uint32_t
 // token row_token[r] (r < T*k), or of token r - T*k (the shared expert's
 // rows), converted from bf16 to f16 (exact for |x| in [2^-14, 65504]; an
 // element beyond 65504, or not finite, records MOE_ERANGE); a warp per row.
-__global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int rows, uint16_t* xs) {
+// from_f16: copied from the f16 copy of x instead (x in host memory mapped
+// for the device: read once by the conversion, not once per row here).
+__global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int rows, uint16_t* xs,
+                                                          int from_f16) {
   griddep_wait();
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -1243,8 +1246,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int ro
     if (lane == 0) *p.status = kStatusInvalid;
     return;
   }
-  const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * p.H);
+  if (from_f16) {
+    const uint4* h = reinterpret_cast<const uint4*>(p.xh + (size_t)t * p.H);
+    for (int v = lane; v < p.H / 8; v += 32) dst[v] = h[v];
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H);
   bool bad = false;
   for (int v = lane; v < p.H / 8; v += 32) {
     const uint4 raw = src[v];
@@ -1705,9 +1713,10 @@ cudaError_t tc_make_rows16_map(void* map, const uint16_t* base, size_t rows, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gather_rows(const ExpertParams& p, int rows, uint16_t* xs, cudaStream_t st) {
+cudaError_t launch_gather_rows(const ExpertParams& p, int rows, uint16_t* xs, bool from_f16, cudaStream_t st) {
   const int blocks = (rows + 7) / 8;
-  return launch_k(gather_rows_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, st, true, p, rows, xs);
+  return launch_k(gather_rows_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, st, true, p, rows, xs,
+                  from_f16 ? 1 : 0);
 }
 
 bool tc_tm_ok(int H, int I) { return H % kTmK == 0 && I % kTmK == 0; }

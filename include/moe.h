@@ -105,7 +105,8 @@ int moe_forward_launches(moe_layer* L, int T);
 enum moe_path {
   MOE_PATH_DECODE = 0,    /* T <= 8: gate/up routes itself; fused down + combine */
   MOE_PATH_STREAM = 1,    /* streamed GEMVs over expert-sorted token groups */
-  MOE_PATH_TC_F16 = 2,    /* tcgen05 kind::f16 GEMMs on exactly dequantised weights */
+  MOE_PATH_TC_F16 = 2,    /* tcgen05 kind::f16 GEMMs on exactly dequantised weights (held in
+                             tensor memory when H and I are multiples of 128) */
   MOE_PATH_TC_FP4 = 3     /* W4A4: tcgen05 kind::mxf4nvf4 block-scaled GEMMs */
 };
 int moe_forward_path(moe_layer* L, int T);
@@ -181,9 +182,10 @@ int moe_set_router_mode(moe_layer* L, int mode);
  *     moe_quantize_act_nvfp4), and the products take the dequantised values.
  *     The router keeps bf16 x.  The values stay within f16 (|code x block
  *     scale| <= 2688) and the tensor scales multiply the fp32 accumulators,
- *     so x and a have no f16 range limit in this mode.  The products run on
- *     the same tensor-core instructions as W4A16 (f16 operands, exact), not
- *     on the block-scaled FP4 MMA.
+ *     so x and a have no f16 range limit in this mode.  On the tensor-core
+ *     path (MOE_PATH_TC_FP4) the products run on the block-scaled FP4 MMA
+ *     (tcgen05 kind::mxf4nvf4, both operands' e4m3 scales applied by the
+ *     tensor core); on the other paths on f16 copies of the exact values.
  * MOE_EINVAL for an unknown format. */
 enum moe_act_format { MOE_ACT_BF16 = 0, MOE_ACT_NVFP4 = 1 };
 int moe_set_act_format(moe_layer* L, int fmt);

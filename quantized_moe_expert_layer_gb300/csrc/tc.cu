@@ -1,6 +1,12 @@
 // Prefill path: grouped expert GEMMs on the 5th-generation tensor cores
-// (tcgen05 kind::f16, fp32 accumulators in tensor memory), and the router as
-// a bf16 GEMM.
+// (tcgen05, fp32 accumulators in tensor memory), and the router as a bf16
+// GEMM.  Three forms of the expert GEMMs:
+//   * tc_tmem_kernel (W4A16, H and I multiples of 128): the weights
+//     dequantised into tensor memory, two MMA-issuing pipelines per SM (see
+//     its section below);
+//   * tc_fp4_kernel (W4A4): both operands NVFP4 on kind::mxf4nvf4;
+//   * tc_expert_kernel (the other shapes): the weights dequantised into
+//     shared memory, described here.
 //
 // Expert GEMMs (tc_expert_kernel): per work item (expert e, up to 128 tokens
 // routed to e) and group of G 128-row blocks of W,
@@ -1247,24 +1253,40 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(ExpertParams p, int ro
     return;
   }
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * p.H);
+  const int n16 = p.H / 8;  // 16-byte vectors of a row; 4 of a lane's in flight at once
   if (from_f16) {
     const uint4* h = reinterpret_cast<const uint4*>(p.xh + (size_t)t * p.H);
-    for (int v = lane; v < p.H / 8; v += 32) dst[v] = h[v];
+    for (int v0 = lane; v0 < n16; v0 += 128) {
+      uint4 w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < n16) w[u] = h[v0 + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < n16) dst[v0 + 32 * u] = w[u];
+    }
     return;
   }
   const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H);
   bool bad = false;
-  for (int v = lane; v < p.H / 8; v += 32) {
-    const uint4 raw = src[v];
-    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t o[4];
+  for (int v0 = lane; v0 < n16; v0 += 128) {
+    uint4 raw[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16), __uint_as_float(in[q] & 0xFFFF0000u));
-      o[q] = *reinterpret_cast<const uint32_t*>(&h);
-      bad |= f16x2_nonfinite(o[q]);
+    for (int u = 0; u < 4; ++u)
+      if (v0 + 32 * u < n16) raw[u] = src[v0 + 32 * u];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (v0 + 32 * u >= n16) break;
+      const uint32_t in[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(in[q] << 16), __uint_as_float(in[q] & 0xFFFF0000u));
+        o[q] = *reinterpret_cast<const uint32_t*>(&h);
+        bad |= f16x2_nonfinite(o[q]);
+      }
+      dst[v0 + 32 * u] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (bad) *p.status = kStatusRange;
 }

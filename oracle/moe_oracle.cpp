@@ -22,7 +22,8 @@
 //     brings its own 8 experts" (nextsycl README, "Lessons learned").
 //   * The expert is a SwiGLU FFN: y = W_down (silu(W_gate x) * (W_up x)).
 //
-// Readings where the pages are silent (each one is listed in the design doc):
+// Readings where the pages are silent (R1, R2, ...; the same labels name them in
+// the design notes):
 //   R1 NVFP4 tensor scale ts = amax(W) / (6 * 448), one per (expert, matrix);
 //      block scale s_b = e4m3_rne((amax_b / 6) / ts); q = e2m1_rne(w / (s_b*ts)).
 //   R2 blocks run along K (the reduction dimension), contiguous.

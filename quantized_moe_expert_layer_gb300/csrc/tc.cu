@@ -1446,7 +1446,9 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             const int cq = hi ? 16 + qq : qq;
             const float gv = hi ? recv : lo_v, uv = hi ? hi_v : recv;
             const float Gv = ts_g * gv, U = ts_u * uv;
-            const float a = Gv / (1.0f + expf(-Gv)) * U;
+            // (the fast exponential and division: a becomes f16, 11 bits, so their few
+            // ulps of fp32 error do not show; the epilogue stays short of the MMAs)
+            const float a = __fdividef(Gv, 1.0f + __expf(-Gv)) * U;
             const uint16_t h = __half_as_ushort(__float2half_rn(a));
             // (columns past the item's tokens hold stale accumulators: never stored, never flagged)
             bad |= c0 + cq < cur.n && f16_nonfinite(h);

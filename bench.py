@@ -362,6 +362,17 @@ def traffic_from_profile(kernel, workload, csrc):
     return b if sources_sha256(csrc, unit) == sha else None
 
 
+def prefill_flops(w, counts):
+    """FLOPs of the tensor-core gate/up GEMM for per-expert token counts: the
+    routed (token, expert) pairs and the shared experts' T tokens, 2 n 2I H
+    each; and the FLOPs as the MMA runs them (each work item of at most 128
+    tokens padded to a multiple of 16)."""
+    n = [int(v) for v in counts if v > 0] + [w.T] * w.shared
+    algo = 2.0 * sum(n) * 2 * w.I * w.H
+    cols = sum(((min(128, v - 128 * j) + 15) // 16) * 16 for v in n for j in range((v + 127) // 128))
+    return algo, 2.0 * cols * 2 * w.I * w.H
+
+
 def sources_sha256(csrc, unit):
     """Hash of the translation unit `unit` and the local headers it includes,
     followed recursively, in sorted file-name order."""
@@ -515,10 +526,9 @@ def measure(w, Ln, steps, warmup, rank, world, host_mirror=0.0, headline=False, 
             if tc:  # FLOPs of the contraction: the routed (token, expert) pairs as computed,
                 # and as the MMA runs them (N padded to 16 per work item of <= 128 tokens)
                 n = [int(v) for v in c if v > 0] + [T] * w.shared
-                per_launch.append(2.0 * sum(n) * 2 * w.I * w.H)
-                cols = sum(((min(128, v - 128 * j) + 15) // 16) * 16
-                           for v in n for j in range((v + 127) // 128))
-                padded.append(2.0 * cols * 2 * w.I * w.H)
+                algo, as_run = prefill_flops(w, c)
+                per_launch.append(algo)
+                padded.append(as_run)
                 # bytes of the block-scaled (W4A4) launch: the touched experts' packed gate/up
                 # tiles, x's NVFP4 codes and scales, a written in fp32
                 fq_bytes.append(D * gu + T * w.H * 9 // 16 + sum(n) * w.I * 4)

@@ -85,3 +85,43 @@ def test_reference_arm_two_ranks_rank0_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_profile_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    """The roofline's `traffic` comes from a committed ncu summary only while the
+    kernel's translation unit and the local headers it includes (followed
+    through other headers) hash as they did when the summary was written; a
+    header it does not include does not matter."""
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    (csrc / "k.cu").write_text('#include "a.cuh"\n__global__ void kern() {}\n')
+    (csrc / "a.cuh").write_text('#include "b.cuh"\n// a\n')
+    (csrc / "b.cuh").write_text("// b\n")
+    (csrc / "other.cuh").write_text("// not included\n")
+    sha = bench.sources_sha256(str(csrc), "k.cu")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "kern_wl.md").write_text(
+        f"# kern\n\ndram_bytes_per_launch: 12345\nsource_unit: k.cu\nsource_sha256: {sha}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_from_profile("kern", "wl", str(csrc)) == 12345.0
+    (csrc / "other.cuh").write_text("// changed, still not included\n")
+    assert bench.traffic_from_profile("kern", "wl", str(csrc)) == 12345.0
+    (csrc / "b.cuh").write_text("// b changed\n")  # included through a.cuh
+    assert bench.traffic_from_profile("kern", "wl", str(csrc)) is None
+    assert bench.traffic_from_profile("kern", "missing", str(csrc)) is None
+
+
+def test_prefill_flops_count_the_routed_pairs():
+    """bench.prefill_flops: 2 (T k + T) 2I H FLOPs for the gate/up GEMM (the
+    routed pairs and the shared expert's tokens), and the MMA's padding of each
+    work item of at most 128 tokens to a multiple of 16, on hand-counted items."""
+    w = gen.get_workload(4)
+    counts = np.zeros(w.E, dtype=np.int64)
+    counts[:3] = [1, 130, 16]  # experts with 1, 130 (items of 128 and 2) and 16 tokens
+    algo, as_run = bench.prefill_flops(w, counts)
+    unit = 2.0 * 2 * w.I * w.H  # FLOPs of one token through one expert's gate/up
+    assert algo == unit * (1 + 130 + 16 + w.T)
+    # items padded: 1 -> 16; 130 -> 128 + 16; 16 -> 16; the shared 4096 -> 32 x 128
+    assert as_run == unit * (16 + 128 + 16 + 16 + 4096)
+    assert bench.prefill_flops(w, np.zeros(w.E))[0] == unit * w.T * w.shared
